@@ -1,0 +1,143 @@
+"""Seeded synthetic inputs for the fused MoE forward pass.
+
+This module holds the workload recipes and the random generators only: it computes nothing
+of the method.  Both the CUDA path and the CPU oracle are fed copies of the same tensors.
+
+Recipe (the pages' workloads; TileOPs benchmark page "MoE" section, FusedMoEFwd and
+FusedMoESharedExpertFwd shape lists; flashinfer PR #4048 DeepSeek-V3 benchmark workload):
+  hidden_states  ~ N(0, 1)                      rounded to bf16/f16 (round to nearest even)
+  gating_output  ~ N(0, 1) in f32
+  correction_bias ~ N(0, 0.1^2) in f32          (sigmoid workloads)
+  w_gate_up      ~ N(0, 1/H)  (std 1/sqrt(fan_in), fan_in = H)
+  w_down         ~ N(0, 1/F)  (fan_in = F)
+  shared_w_gate_up ~ N(0, 1/H), shared_w_down ~ N(0, 1/S)
+One torch.Generator seeded with `seed` draws, in this order: hidden, gating, bias, w_gate_up,
+w_down, shared_w_gate_up, shared_w_down.  Large weights are drawn expert by expert (chunks of
+rows) so the f32 staging stays small; the chunking is part of the recipe.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    T: int
+    H: int
+    E: int
+    F: int
+    top_k: int
+    scoring_func: str = "softmax"
+    renormalize: bool = True
+    bias_std: float = 0.0          # 0: no correction_bias
+    num_expert_group: int = 0
+    topk_group: int = 0
+    routed_scaling_factor: float = 1.0
+    S: int = 0
+    dtype: torch.dtype = torch.bfloat16
+
+    def with_(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+    def flops(self) -> float:
+        """2*T*k*3*F*H (+ 2*T*3*S*H): the FLOP count the TileOPs MoE page's TFLOP/s uses."""
+        return 2.0 * self.T * self.top_k * 3 * self.F * self.H + 2.0 * self.T * 3 * self.S * self.H
+
+    def kwargs(self) -> dict:
+        return dict(top_k=self.top_k, scoring_func=self.scoring_func,
+                    renormalize=self.renormalize, num_expert_group=self.num_expert_group,
+                    topk_group=self.topk_group,
+                    routed_scaling_factor=self.routed_scaling_factor)
+
+
+# The five workloads this project is measured on (sizes from the pages' shape lists).
+WORKLOADS = {
+    "tiny-softmax": Workload("tiny-softmax", T=4, H=128, E=8, F=64, top_k=2),
+    "qwen3-30b-a3b-decode-t32": Workload("qwen3-30b-a3b-decode-t32", T=32, H=2048, E=128,
+                                         F=768, top_k=8),
+    "qwen3-235b-a22b-decode-t512": Workload("qwen3-235b-a22b-decode-t512", T=512, H=4096,
+                                            E=128, F=1536, top_k=8),
+    "deepseek-v3-grouped-prefill-t4096": Workload(
+        "deepseek-v3-grouped-prefill-t4096", T=4096, H=7168, E=256, F=2048, top_k=8,
+        scoring_func="sigmoid", bias_std=0.1, num_expert_group=8, topk_group=4,
+        routed_scaling_factor=2.5),
+    "kimi-k2-shared-t512": Workload(
+        "kimi-k2-shared-t512", T=512, H=7168, E=384, F=2048, top_k=8, scoring_func="sigmoid",
+        bias_std=0.1, routed_scaling_factor=2.827, S=18432),
+}
+
+_CHUNK_ELEMS = 1 << 28  # f32 staging per draw: 1 GiB
+
+
+def _randn(shape, gen, device, std, dtype):
+    """N(0, std^2) drawn in f32 chunks along dim 0, rounded to `dtype`."""
+    out = torch.empty(shape, dtype=dtype, device=device)
+    if out.numel() == 0:
+        return out
+    per_row = out[0].numel() if out.dim() > 1 else 1
+    rows = max(1, _CHUNK_ELEMS // max(per_row, 1))
+    flat = out.view(shape[0], -1) if out.dim() > 1 else out.view(-1, 1)
+    for r0 in range(0, shape[0], rows):
+        r1 = min(shape[0], r0 + rows)
+        x = torch.randn((r1 - r0, flat.shape[1]), generator=gen, device=device,
+                        dtype=torch.float32)
+        if std != 1.0:
+            x.mul_(std)
+        flat[r0:r1].copy_(x.to(dtype))
+        del x
+    return out
+
+
+def generate(w: Workload, seed: int = 0, device="cuda") -> dict:
+    """All inputs of workload `w` as tensors on `device` (the recipe in the module doc)."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    dt = w.dtype
+    d = {}
+    d["hidden_states"] = _randn((w.T, w.H), gen, device, 1.0, dt)
+    d["gating_output"] = _randn((w.T, w.E), gen, device, 1.0, torch.float32)
+    d["correction_bias"] = (_randn((w.E,), gen, device, w.bias_std, torch.float32)
+                            if w.bias_std > 0 else None)
+    d["w_gate_up"] = _randn((w.E, 2 * w.F, w.H), gen, device, 1.0 / math.sqrt(w.H), dt)
+    d["w_down"] = _randn((w.E, w.H, w.F), gen, device, 1.0 / math.sqrt(w.F), dt)
+    if w.S > 0:
+        d["shared_w_gate_up"] = _randn((2 * w.S, w.H), gen, device, 1.0 / math.sqrt(w.H), dt)
+        d["shared_w_down"] = _randn((w.H, w.S), gen, device, 1.0 / math.sqrt(w.S), dt)
+    else:
+        d["shared_w_gate_up"] = None
+        d["shared_w_down"] = None
+    return d
+
+
+def random_ids(T: int, top_k: int, E: int, seed: int = 0, device="cpu", pad_frac: float = 0.0,
+               distinct: bool = True) -> torch.Tensor:
+    """Seeded topk_ids [T, top_k] int32 for the staged sort/GEMM tests: distinct experts per
+    token (unless distinct=False), a fraction pad_frac of routes set to -1 (padding)."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    if distinct:
+        ids = torch.stack([torch.randperm(E, generator=gen)[:top_k] for _ in range(T)]) \
+            if T > 0 else torch.empty((0, top_k), dtype=torch.int64)
+    else:
+        ids = torch.randint(0, E, (T, top_k), generator=gen)
+    if pad_frac > 0 and T > 0:
+        mask = torch.rand((T, top_k), generator=gen) < pad_frac
+        ids = ids.masked_fill(mask, -1)
+    return ids.to(torch.int32).to(device)
+
+
+def random_rows(n: int, cols: int, seed: int, dtype=torch.bfloat16, device="cpu",
+                std: float = 1.0) -> torch.Tensor:
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    return (torch.randn((n, cols), generator=gen) * std).to(dtype).to(device)
+
+
+def random_weights(n: int, seed: int, device="cpu") -> torch.Tensor:
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    return torch.rand((n,), generator=gen, dtype=torch.float32).to(device)

@@ -1,0 +1,224 @@
+"""CPU oracle for the fused MoE forward pass -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl reference``
+legs of ``bench.py`` may import this package.  The product library never loads it, and it
+imports nothing from the product package.
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64, a per-token loop); this module compiles it
+with gcc (``build()``), loads it with ctypes and marshals numpy arrays.  Each function cites the
+passage of the source pages it follows in ``oracle.c``.
+
+Sources: TileOPs benchmark page, "MoE" section (ops FusedMoEFwd, FusedMoESharedExpertFwd,
+FusedTopKFwd, MoEPermuteAlignFwd, MoEPostPermuteFwd, MoEGroupedGemmFwd silu_and_mul,
+SharedExpertMLPFwd); ROCm/aiter PR #5973 "[FlyDSL] Optimize MI308 MoE decoding (3/3)",
+"Changes" (expert id -1 is a skipped padding route; the sort returns each route's sorted row).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+OK, ERR_ARG, ERR_ID = 0, 1, 6
+BF16, F16 = 0, 1
+SOFTMAX, SIGMOID = 0, 1
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into oracle/_build/liboracle.so (gcc, OpenMP when available)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
+    try:
+        subprocess.run(base + ["-fopenmp", "-o", tmp, _SRC, "-lm"], check=True,
+                       capture_output=True, text=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base + ["-o", tmp, _SRC, "-lm"], check=True, capture_output=True, text=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+            _lib.oracle_half_bits_to_double.restype = f64
+            _lib.oracle_half_bits_to_double.argtypes = [i32, ctypes.c_uint16]
+            _lib.oracle_decode_array.argtypes = [i32, P, P, i64]
+            _lib.oracle_exp_f32.restype = ctypes.c_float
+            _lib.oracle_exp_f32.argtypes = [ctypes.c_float]
+            _lib.oracle_sigmoid_key_f32.restype = ctypes.c_float
+            _lib.oracle_sigmoid_key_f32.argtypes = [ctypes.c_float]
+            _lib.oracle_route.argtypes = [i32, i32, i32, i32, i32, i32, i32, f64, P, P, P, P, P]
+            _lib.oracle_align_sort.argtypes = [i32, i32, i32, i32, P, P, P, P, i64, P, i64, P]
+            _lib.oracle_moe_tokens.argtypes = [i32, P, i32, i32, i32, i32, i32, i32, P, P, P, P,
+                                               P, P, i32, P, P, P]
+            _lib.oracle_expert_act.argtypes = [i32, i32, i32, i32, P, P, P, P]
+            _lib.oracle_expert_down.argtypes = [i32, i32, i32, i32, P, P, P, P, P]
+            _lib.oracle_combine.argtypes = [i32, i32, i32, i32, P, P, P, P]
+            _lib.oracle_num_threads.restype = i32
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _bits(a):
+    """Accept a uint16/int16 bit array (or a torch bf16/f16 tensor) and return uint16 bits."""
+    if a is None:
+        return None
+    if hasattr(a, "view") and hasattr(a, "dtype") and "torch" in type(a).__module__:
+        import torch
+        t = a.detach().contiguous().cpu()
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return np.ascontiguousarray(a).view(np.uint16)
+
+
+def _check(rc, what):
+    if rc == ERR_ID:
+        raise ValueError(f"{what}: expert id out of range")
+    if rc != OK:
+        raise ValueError(f"{what}: invalid arguments (code {rc})")
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def half_bits_to_double(dtype: int, bits: np.ndarray) -> np.ndarray:
+    b = _c(bits, np.uint16)
+    out = np.empty(b.shape, np.float64)
+    _load().oracle_decode_array(dtype, _ptr(b), _ptr(out), b.size)
+    return out
+
+
+def exp_f32(z: float) -> float:
+    return float(_load().oracle_exp_f32(float(z)))
+
+
+def sigmoid_key_f32(x: float) -> float:
+    return float(_load().oracle_sigmoid_key_f32(float(x)))
+
+
+def route(gating, top_k, scoring=SOFTMAX, renormalize=True, num_expert_group=0, topk_group=0,
+          routed_scaling_factor=1.0, bias=None):
+    """Return (ids int32 [T,k], weights float64 [T,k], near_tie int32 [T])."""
+    g = _c(gating, np.float32)
+    T, E = g.shape
+    b = None if bias is None else _c(bias, np.float32)
+    ids = np.empty((T, top_k), np.int32)
+    w = np.empty((T, top_k), np.float64)
+    nt = np.empty((T,), np.int32)
+    rc = _load().oracle_route(T, E, top_k, scoring, int(bool(renormalize)), num_expert_group,
+                              topk_group, float(routed_scaling_factor), _ptr(g), _ptr(b),
+                              _ptr(ids), _ptr(w), _ptr(nt))
+    _check(rc, "oracle_route")
+    return ids, w, nt
+
+
+def align_sort(ids, E, block_m):
+    """Counting sort of flat routes into expert segments padded to block_m.
+
+    Returns dict(counts, offsets, sorted_ids, tile_expert, inv_route); sorted_ids has
+    P + E*(block_m-1) slots and tile_expert that many / block_m (rounded up)."""
+    i = _c(ids, np.int32)
+    T, k = i.shape
+    P = T * k
+    sorted_len = P + E * (block_m - 1)
+    tile_len = (sorted_len + block_m - 1) // block_m
+    counts = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    sorted_ids = np.empty(sorted_len, np.int32)
+    tile_expert = np.empty(tile_len, np.int32)
+    inv = np.empty(P, np.int32)
+    rc = _load().oracle_align_sort(T, k, E, block_m, _ptr(i), _ptr(counts), _ptr(offsets),
+                                   _ptr(sorted_ids), sorted_len, _ptr(tile_expert), tile_len,
+                                   _ptr(inv))
+    _check(rc, "oracle_align_sort")
+    return dict(counts=counts, offsets=offsets, sorted_ids=sorted_ids, tile_expert=tile_expert,
+                inv_route=inv)
+
+
+def moe_tokens(hidden, ids, weights, w_gate_up, w_down, dtype, tokens=None, expert_slot=None,
+               shared_w_gate_up=None, shared_w_down=None, num_experts=None):
+    """fp64 fused MoE output for the listed tokens (all tokens when ``tokens`` is None).
+
+    hidden/w_* are 16-bit bit arrays (or torch tensors).  When ``expert_slot`` is given,
+    w_gate_up/w_down hold only the slots it maps experts to and ``num_experts`` is E."""
+    hb = _bits(hidden)
+    T, H = hb.shape
+    idv = _c(ids, np.int32)
+    k = idv.shape[1]
+    wv = _c(weights, np.float64)
+    wgu = _bits(w_gate_up)
+    wd = _bits(w_down)
+    F = wgu.shape[-2] // 2
+    E = num_experts if num_experts is not None else wgu.shape[0]
+    slot = None if expert_slot is None else _c(expert_slot, np.int32)
+    sgu = _bits(shared_w_gate_up)
+    sd = _bits(shared_w_down)
+    S = 0 if sgu is None else sgu.shape[0] // 2
+    tl = np.arange(T, dtype=np.int32) if tokens is None else _c(tokens, np.int32)
+    out = np.empty((tl.size, H), np.float64)
+    rc = _load().oracle_moe_tokens(tl.size, _ptr(tl), T, H, E, F, k, dtype, _ptr(hb), _ptr(idv),
+                                   _ptr(wv), _ptr(wgu), _ptr(wd), _ptr(slot), S, _ptr(sgu),
+                                   _ptr(sd), _ptr(out))
+    _check(rc, "oracle_moe_tokens")
+    return out
+
+
+def expert_act(x_rows, expert_of_row, w_gate_up, dtype):
+    xb = _bits(x_rows)
+    n, H = xb.shape
+    wgu = _bits(w_gate_up)
+    F = wgu.shape[1] // 2
+    eo = _c(expert_of_row, np.int32)
+    act = np.empty((n, F), np.float64)
+    _check(_load().oracle_expert_act(n, H, F, dtype, _ptr(xb), _ptr(eo), _ptr(wgu), _ptr(act)),
+           "oracle_expert_act")
+    return act
+
+
+def expert_down(act_rows, expert_of_row, scale, w_down, dtype):
+    ab = _bits(act_rows)
+    n, F = ab.shape
+    wd = _bits(w_down)
+    H = wd.shape[1]
+    eo = _c(expert_of_row, np.int32)
+    sc = _c(scale, np.float64)
+    y = np.empty((n, H), np.float64)
+    _check(_load().oracle_expert_down(n, H, F, dtype, _ptr(ab), _ptr(eo), _ptr(sc), _ptr(wd),
+                                      _ptr(y)), "oracle_expert_down")
+    return y
+
+
+def combine(rows, inv_route, top_k, dtype, shared=None):
+    rb = _bits(rows)
+    H = rb.shape[1]
+    inv = _c(inv_route, np.int32)
+    T = inv.size // top_k
+    sb = _bits(shared)
+    out = np.empty((T, H), np.float64)
+    _check(_load().oracle_combine(T, H, top_k, dtype, _ptr(rb), _ptr(inv), _ptr(sb), _ptr(out)),
+           "oracle_combine")
+    return out

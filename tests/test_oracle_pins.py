@@ -1,0 +1,370 @@
+"""Pins of the CPU oracle against facts it does not itself compute (CPU only).
+
+Each test checks one oracle function against something independent of its code: every bit
+pattern of a 16-bit float, fp64 libm, brute-force full sorts on tiny inputs, library routines
+(numpy matmul / argsort / bincount, scipy softmax / expit) on special cases, closed forms and
+invariants, and the throughput figures printed on the TileOPs MoE page.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+from mixture_experts_forward_moe_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+F32_ULP = 2.0 ** -23
+
+
+# ---------------------------------------------------------------------------------- decoding
+def test_bf16_decode_every_pattern():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.half_bits_to_double(oracle.BF16, bits)
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_f16_decode_every_pattern():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.half_bits_to_double(oracle.F16, bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+# ---------------------------------------------------------------- f32 exp / sigmoid routing key
+def test_exp_f32_within_two_ulp_of_fp64():
+    z = np.concatenate([np.linspace(-80, 80, 4001), np.linspace(-1, 1, 2001)]).astype(np.float32)
+    for v in z:
+        got = oracle.exp_f32(float(v))
+        ref = math.exp(float(v))
+        assert abs(got - ref) <= 2 * F32_ULP * ref, (v, got, ref)
+
+
+def test_exp_f32_exact_points():
+    assert oracle.exp_f32(0.0) == 1.0
+    assert oracle.sigmoid_key_f32(0.0) == 0.5
+
+
+def test_sigmoid_key_close_to_expit():
+    for x in np.linspace(-30, 30, 1201).astype(np.float32):
+        got = oracle.sigmoid_key_f32(float(x))
+        ref = float(scipy.special.expit(np.float64(x)))
+        assert abs(got - ref) <= 3 * F32_ULP * ref, (x, got, ref)
+
+
+def test_sigmoid_key_saturates():
+    assert oracle.sigmoid_key_f32(200.0) == 1.0
+    assert 0.0 < oracle.sigmoid_key_f32(-200.0) < 1e-34
+
+
+# ------------------------------------------------------------------------ routing brute force
+def _full_sort_topk(keys, k, allowed=None):
+    idx = [e for e in range(len(keys)) if allowed is None or allowed[e]]
+    return sorted(idx, key=lambda e: (-float(keys[e]), e))[:k]
+
+
+@pytest.mark.parametrize("E,k", [(4, 1), (8, 2), (16, 4), (16, 16)])
+@pytest.mark.parametrize("renorm", [True, False])
+def test_route_softmax_brute_force(E, k, renorm):
+    rng = np.random.default_rng(E * 100 + k)
+    g = rng.standard_normal((40, E)).astype(np.float32)
+    g[0, :] = 0.25  # all-equal row: ties go to the lower id
+    g[1, : E // 2] = g[1, E // 2 :]  # pairwise ties
+    ids, w, _ = oracle.route(g, k, oracle.SOFTMAX, renorm, routed_scaling_factor=1.0)
+    for t in range(g.shape[0]):
+        sel = _full_sort_topk(g[t], k)
+        assert list(ids[t]) == sel
+        p = scipy.special.softmax(g[t].astype(np.float64))
+        ref = p[sel] / p[sel].sum() if renorm else p[sel]
+        np.testing.assert_allclose(w[t], ref, rtol=1e-12, atol=0)
+    assert list(ids[0]) == list(range(k))
+
+
+def test_route_softmax_k_equals_e_is_full_softmax():
+    rng = np.random.default_rng(7)
+    g = rng.standard_normal((10, 8)).astype(np.float32)
+    ids, w, _ = oracle.route(g, 8, oracle.SOFTMAX, True)
+    for t in range(10):
+        full = scipy.special.softmax(g[t].astype(np.float64))
+        np.testing.assert_allclose(w[t], full[ids[t]], rtol=1e-12)
+        np.testing.assert_allclose(w[t].sum(), 1.0, rtol=1e-13)
+
+
+@pytest.mark.parametrize("renorm,rsf", [(True, 1.0), (True, 2.5), (False, 1.0), (False, 2.827)])
+def test_route_sigmoid_bias_brute_force(renorm, rsf):
+    rng = np.random.default_rng(11)
+    E, k = 16, 4
+    g = rng.standard_normal((60, E)).astype(np.float32)
+    bias = (0.1 * rng.standard_normal(E)).astype(np.float32)
+    ids, w, _ = oracle.route(g, k, oracle.SIGMOID, renorm, routed_scaling_factor=rsf, bias=bias)
+    for t in range(g.shape[0]):
+        s32 = np.array([oracle.sigmoid_key_f32(float(v)) for v in g[t]], np.float32)
+        keys = s32 + bias  # f32 addition
+        sel = _full_sort_topk(keys, k)
+        assert list(ids[t]) == sel
+        s = scipy.special.expit(g[t].astype(np.float64))[sel]
+        ref = (s / s.sum() if renorm else s) * rsf
+        np.testing.assert_allclose(w[t], ref, rtol=1e-12)
+        if renorm:
+            np.testing.assert_allclose(w[t].sum(), rsf, rtol=1e-12)
+
+
+@pytest.mark.parametrize("E,G,keep,k", [(16, 4, 2, 4), (24, 6, 3, 5), (32, 8, 4, 8), (12, 4, 1, 2)])
+def test_route_grouped_brute_force(E, G, keep, k):
+    rng = np.random.default_rng(E + G + keep)
+    g = rng.standard_normal((60, E)).astype(np.float32)
+    bias = (0.1 * rng.standard_normal(E)).astype(np.float32)
+    g[0, :] = 0.0  # every group ties: lower groups and ids win
+    bias_t = bias.copy()
+    ids, w, _ = oracle.route(g, k, oracle.SIGMOID, True, G, keep, 2.5, bias_t)
+    gs = E // G
+    for t in range(g.shape[0]):
+        s32 = np.array([oracle.sigmoid_key_f32(float(v)) for v in g[t]], np.float32)
+        keys = s32 + bias
+        scores = []
+        for grp in range(G):
+            top2 = sorted(keys[grp * gs:(grp + 1) * gs].tolist())[-2:]
+            scores.append(float(np.float32(top2[0]) + np.float32(top2[1])))
+        # Best subset of `keep` groups: enumerate all subsets, compare by sorted scores then ids.
+        def rank(sub):
+            return sorted(((-scores[x], x) for x in sub))
+        best = min(itertools.combinations(range(G), keep), key=rank)
+        allowed = [(e // gs) in best for e in range(E)]
+        sel = _full_sort_topk(keys, k, allowed)
+        assert list(ids[t]) == sel, t
+        s = scipy.special.expit(g[t].astype(np.float64))[sel]
+        np.testing.assert_allclose(w[t], s / s.sum() * 2.5, rtol=1e-12)
+
+
+def test_grouping_with_all_groups_kept_equals_ungrouped():
+    rng = np.random.default_rng(3)
+    g = rng.standard_normal((50, 32)).astype(np.float32)
+    b = (0.1 * rng.standard_normal(32)).astype(np.float32)
+    a = oracle.route(g, 6, oracle.SIGMOID, True, 8, 8, 1.0, b)
+    c = oracle.route(g, 6, oracle.SIGMOID, True, 0, 0, 1.0, b)
+    assert np.array_equal(a[0], c[0])
+    np.testing.assert_array_equal(a[1], c[1])
+
+
+def test_route_rejects_bad_arguments():
+    g = np.zeros((2, 8), np.float32)
+    with pytest.raises(ValueError):
+        oracle.route(g, 9)
+    with pytest.raises(ValueError):
+        oracle.route(g, 2, oracle.SIGMOID, True, 3, 1)  # 8 % 3 != 0
+    with pytest.raises(ValueError):
+        oracle.route(g, 5, oracle.SIGMOID, True, 4, 2)  # 2 groups x 2 experts < 5
+
+
+# -------------------------------------------------------------------------------------- sort
+@pytest.mark.parametrize("block_m", [1, 4, 16, 128])
+@pytest.mark.parametrize("pad_frac", [0.0, 0.2])
+def test_align_sort_matches_stable_argsort(block_m, pad_frac):
+    T, k, E = 37, 4, 10
+    ids = inputs.random_ids(T, k, E, seed=5, pad_frac=pad_frac).numpy()
+    r = oracle.align_sort(ids, E, block_m)
+    flat = ids.reshape(-1)
+    live = flat >= 0
+    counts = np.bincount(flat[live], minlength=E)
+    assert np.array_equal(r["counts"], counts)
+    padded = (counts + block_m - 1) // block_m * block_m
+    assert np.array_equal(r["offsets"], np.concatenate([[0], np.cumsum(padded)]))
+    order = np.argsort(np.where(live, flat, E), kind="stable")[: live.sum()]
+    got = []
+    for e in range(E):
+        seg = r["sorted_ids"][r["offsets"][e]: r["offsets"][e + 1]]
+        assert np.all(seg[counts[e]:] == -1)
+        got.extend(seg[: counts[e]].tolist())
+        for p in range(r["offsets"][e], r["offsets"][e + 1], block_m):
+            assert r["tile_expert"][p // block_m] == e
+    assert got == order.tolist()
+    assert np.all(r["sorted_ids"][r["offsets"][E]:] == -1)
+    assert np.all(r["tile_expert"][r["offsets"][E] // block_m:] == -1)
+    inv = r["inv_route"]
+    for q in range(flat.size):
+        if flat[q] < 0:
+            assert inv[q] == -1
+        else:
+            assert r["sorted_ids"][inv[q]] == q
+
+
+def test_align_sort_rejects_bad_ids():
+    ids = np.array([[0, 9]], np.int32)
+    with pytest.raises(ValueError):
+        oracle.align_sort(ids, 4, 1)
+    with pytest.raises(ValueError):
+        oracle.align_sort(np.array([[0, -2]], np.int32), 4, 1)
+
+
+# -------------------------------------------------------------------------------- expert MLP
+def _bits(t):
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _dense_swiglu(x, wgu, wd):
+    F = wgu.shape[0] // 2
+    g = wgu[:F] @ x
+    u = wgu[F:] @ x
+    return wd @ (g / (1.0 + np.exp(-g)) * u)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_single_expert_top1_is_dense_swiglu(dtype):
+    w = inputs.Workload("t", T=6, H=48, E=1, F=24, top_k=1, dtype=dtype)
+    d = inputs.generate(w, seed=1, device="cpu")
+    ids, wts, _ = oracle.route(d["gating_output"].numpy(), 1)
+    assert np.all(ids == 0) and np.all(wts == 1.0)
+    dt = oracle.BF16 if dtype == torch.bfloat16 else oracle.F16
+    out = oracle.moe_tokens(d["hidden_states"], ids, wts, d["w_gate_up"], d["w_down"], dt)
+    x = d["hidden_states"].double().numpy()
+    wgu = d["w_gate_up"][0].double().numpy()
+    wd = d["w_down"][0].double().numpy()
+    for t in range(w.T):
+        np.testing.assert_allclose(out[t], _dense_swiglu(x[t], wgu, wd), rtol=1e-10, atol=1e-12)
+
+
+def _routed_case(seed=2, T=9, E=6, k=3, H=32, F=16, S=0, rsf=1.0):
+    w = inputs.Workload("t", T=T, H=H, E=E, F=F, top_k=k, S=S, routed_scaling_factor=rsf)
+    d = inputs.generate(w, seed=seed, device="cpu")
+    ids, wts, _ = oracle.route(d["gating_output"].numpy(), k, routed_scaling_factor=rsf)
+    return w, d, ids, wts
+
+
+def test_routed_output_is_weighted_sum_of_dense_experts():
+    w, d, ids, wts = _routed_case()
+    out = oracle.moe_tokens(d["hidden_states"], ids, wts, d["w_gate_up"], d["w_down"], 0)
+    x = d["hidden_states"].double().numpy()
+    for t in range(w.T):
+        ref = sum(wts[t, j] * _dense_swiglu(x[t], d["w_gate_up"][ids[t, j]].double().numpy(),
+                                            d["w_down"][ids[t, j]].double().numpy())
+                  for j in range(w.top_k))
+        np.testing.assert_allclose(out[t], ref, rtol=1e-10, atol=1e-12)
+
+
+def test_token_permutation_permutes_output():
+    w, d, ids, wts = _routed_case(seed=4)
+    out = oracle.moe_tokens(d["hidden_states"], ids, wts, d["w_gate_up"], d["w_down"], 0)
+    perm = np.random.default_rng(0).permutation(w.T)
+    out_p = oracle.moe_tokens(d["hidden_states"][perm], ids[perm], wts[perm], d["w_gate_up"],
+                              d["w_down"], 0)
+    np.testing.assert_array_equal(out_p, out[perm])
+
+
+def test_zeroed_down_projection_equals_dropped_route():
+    w, d, ids, wts = _routed_case(seed=6)
+    e0 = int(ids[0, 0])
+    wd = d["w_down"].clone()
+    wd[e0].zero_()
+    a = oracle.moe_tokens(d["hidden_states"], ids, wts, d["w_gate_up"], wd, 0)
+    ids2 = np.where(ids == e0, -1, ids).astype(np.int32)
+    b = oracle.moe_tokens(d["hidden_states"], ids2, wts, d["w_gate_up"], d["w_down"], 0)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_zero_hidden_gives_zero_output():
+    w, d, ids, wts = _routed_case(seed=8, S=16)
+    z = torch.zeros_like(d["hidden_states"])
+    out = oracle.moe_tokens(z, ids, wts, d["w_gate_up"], d["w_down"], 0,
+                            shared_w_gate_up=d["shared_w_gate_up"],
+                            shared_w_down=d["shared_w_down"])
+    assert np.all(out == 0.0)
+
+
+def test_routed_output_linear_in_scaling_factor():
+    _, d, ids, w1 = _routed_case(seed=9, rsf=1.0)
+    _, _, ids2, w25 = _routed_case(seed=9, rsf=2.5)
+    assert np.array_equal(ids, ids2)
+    a = oracle.moe_tokens(d["hidden_states"], ids, w1, d["w_gate_up"], d["w_down"], 0)
+    b = oracle.moe_tokens(d["hidden_states"], ids, w25, d["w_gate_up"], d["w_down"], 0)
+    np.testing.assert_allclose(b, 2.5 * a, rtol=1e-12, atol=1e-15)
+
+
+def test_shared_expert_adds_a_dense_swiglu():
+    w, d, ids, wts = _routed_case(seed=10, S=24)
+    a = oracle.moe_tokens(d["hidden_states"], ids, wts, d["w_gate_up"], d["w_down"], 0)
+    b = oracle.moe_tokens(d["hidden_states"], ids, wts, d["w_gate_up"], d["w_down"], 0,
+                          shared_w_gate_up=d["shared_w_gate_up"],
+                          shared_w_down=d["shared_w_down"])
+    x = d["hidden_states"].double().numpy()
+    sgu = d["shared_w_gate_up"].double().numpy()
+    sd = d["shared_w_down"].double().numpy()
+    for t in range(w.T):
+        np.testing.assert_allclose(b[t] - a[t], _dense_swiglu(x[t], sgu, sd), rtol=1e-9,
+                                   atol=1e-12)
+
+
+def test_expert_slot_subset_matches_full_weights():
+    w, d, ids, wts = _routed_case(seed=12, E=8)
+    full = oracle.moe_tokens(d["hidden_states"], ids, wts, d["w_gate_up"], d["w_down"], 0,
+                             tokens=[1, 4])
+    used = sorted(set(ids[[1, 4]].reshape(-1).tolist()))
+    slot = np.full(w.E, -1, np.int32)
+    slot[used] = np.arange(len(used))
+    sub = oracle.moe_tokens(d["hidden_states"], ids, wts, d["w_gate_up"][used], d["w_down"][used],
+                            0, tokens=[1, 4], expert_slot=slot, num_experts=w.E)
+    np.testing.assert_array_equal(full, sub)
+
+
+def test_stage_references_match_numpy():
+    rng = np.random.default_rng(1)
+    H, F, E, n = 40, 24, 3, 7
+    x = inputs.random_rows(n, H, seed=1)
+    wgu = (torch.randn((E, 2 * F, H), generator=torch.Generator().manual_seed(2)) / 6).to(
+        torch.bfloat16)
+    wd = (torch.randn((E, H, F), generator=torch.Generator().manual_seed(3)) / 5).to(torch.bfloat16)
+    eo = np.array([0, 2, -1, 1, 1, 0, 2], np.int32)
+    act = oracle.expert_act(x, eo, wgu, 0)
+    for r in range(n):
+        if eo[r] < 0:
+            assert np.all(act[r] == 0)
+            continue
+        W = wgu[eo[r]].double().numpy()
+        g, u = W[:F] @ x[r].double().numpy(), W[F:] @ x[r].double().numpy()
+        np.testing.assert_allclose(act[r], g / (1 + np.exp(-g)) * u, rtol=1e-10, atol=1e-13)
+    a16 = torch.from_numpy(act).to(torch.bfloat16)
+    sc = rng.random(n)
+    y = oracle.expert_down(a16, eo, sc, wd, 0)
+    for r in range(n):
+        if eo[r] < 0:
+            assert np.all(y[r] == 0)
+            continue
+        ref = sc[r] * (wd[eo[r]].double().numpy() @ a16[r].double().numpy())
+        np.testing.assert_allclose(y[r], ref, rtol=1e-10, atol=1e-13)
+
+
+def test_combine_matches_numpy_gather_sum():
+    T, k, H = 5, 3, 16
+    rows = inputs.random_rows(20, H, seed=4)
+    inv = np.array([3, 7, -1, 0, 1, 2, 19, 18, 17, 4, 5, 6, -1, -1, 9], np.int32)
+    sh = inputs.random_rows(T, H, seed=5)
+    out = oracle.combine(rows, inv, k, 0, shared=sh)
+    R = rows.double().numpy()
+    ref = sh.double().numpy().copy()
+    for t in range(T):
+        for j in range(k):
+            p = inv[t * k + j]
+            if p >= 0:
+                ref[t] += R[p]
+    np.testing.assert_allclose(out, ref, rtol=1e-15, atol=0)
+
+
+# ------------------------------------------------------------------------------ metric pin
+def test_flop_formula_reproduces_printed_throughput():
+    with open(os.path.join(GOLDEN, "tileops_moe_throughput.json")) as f:
+        rows = json.load(f)["rows"]
+    for r in rows:
+        w = inputs.Workload(r["workload"], T=r["T"], H=r["H"], E=r["E"], F=r["F"], top_k=8,
+                            S=r["S"])
+        tflops = w.flops() / (r["ms"] * 1e-3) / 1e12
+        # printed to three significant figures
+        assert abs(tflops - r["tflops"]) <= 0.006 * r["tflops"], (r["workload"], tflops)
