@@ -1,0 +1,471 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 fused MoE forward (one JSON line on rank 0).
+
+A step is one fused_moe_fwd call (router, sort, gather, gemm1 + SwiGLU, gemm2 x route weight,
+combine, shared expert when present) over one batch of seeded synthetic inputs that are already
+resident in HBM.  The L2 is flushed (a 256 MiB write) between steps, outside the timed events.
+Each step is timed with a CUDA event pair on the launching stream; the K step times are
+summed.  `value` is whole-job TFLOP/s with the TileOPs MoE page's FLOP count
+2*T*k*3*F*H (+ 2*T*3*S*H).
+
+Also reported: HBM GB/s over the algorithmic bytes, the roofline of the dominant kernel (its
+event-timed average launch against the measured HBM copy peak), an end-to-end figure through
+the public API from pinned host buffers (host->device inputs and device->host output inside the
+timed region), SM clocks sampled during the timed region, and the CPU oracle timed on the
+host's cores on a bounded sample of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Under torchrun every rank runs its own replica of the workload on its own GPU (no collective on
+the data path: weak scaling); the timed region is bracketed by a barrier and a synchronize on
+both sides and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "qwen3-30b-a3b-decode-t32"
+METRIC = "fused_moe_fwd device ms, TFLOP/s & HBM GB/s; % of GB300 roofline per config"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+# Throughput printed on the TileOPs benchmark page ("MoE" section, FusedMoEFwd and
+# FusedMoESharedExpertFwd tables) for the same shapes; hardware not stated there.
+PUBLISHED_TFLOPS = {
+    ("qwen3-30b-a3b-decode-t32", "bf16"): 9.11,
+    ("qwen3-235b-a22b-decode-t512", "bf16"): 128.0,
+    ("qwen3-235b-a22b-decode-t512", "f16"): 129.0,
+    ("deepseek-v3-grouped-prefill-t4096", "bf16"): 406.0,
+    ("kimi-k2-shared-t512", "bf16"): 151.0,
+}
+
+
+# ----------------------------------------------------------------------- rank helpers (CPU ok)
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float) -> float:
+    """The largest x over all ranks (x itself without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def job_throughput(units_per_rank: float, n_ranks: int, steps: int, max_ms: float) -> float:
+    """Whole-job rate: units every rank processed in `steps` steps over the slowest rank's time."""
+    return units_per_rank * n_ranks * steps / (max_ms * 1e-3)
+
+
+# --------------------------------------------------------------------------------- accounting
+def elt_bytes(w) -> int:
+    return 2
+
+
+def algorithmic_bytes(w, n_unique: int) -> dict:
+    """Bytes the path must move at least once (weights of the experts touched, activations)."""
+    eb = elt_bytes(w)
+    P = w.T * w.top_k
+    weights = n_unique * 3 * w.F * w.H * eb + 3 * w.S * w.H * eb
+    acts = w.T * w.H * eb * 2 + w.T * w.E * 4 + (w.E * 4 if w.bias_std > 0 else 0)
+    direct = w.T <= 8 and P <= 128
+    b1 = w.T * w.H * eb if direct else P * w.H * eb  # gemm1 token rows read
+    return dict(
+        total=weights + acts,
+        gemm1=n_unique * 2 * w.F * w.H * eb + b1 + P * w.F * eb,
+        gemm2=n_unique * w.H * w.F * eb + P * w.F * eb + P * w.H * eb,
+        shared_gemm1=2 * w.S * w.H * eb + w.T * w.H * eb + w.T * w.S * eb,
+        shared_gemm2=w.S * w.H * eb + w.T * w.S * eb + w.T * w.H * eb,
+    )
+
+
+def stage_flops(w) -> dict:
+    P = w.T * w.top_k
+    return dict(gemm1=2.0 * P * 2 * w.F * w.H, gemm2=2.0 * P * w.F * w.H,
+                shared_gemm1=2.0 * w.T * 2 * w.S * w.H, shared_gemm2=2.0 * w.T * w.S * w.H)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return (float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]),
+                "measured")
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mixture_experts_forward_moe_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, stage: str):
+    """DRAM bytes per launch of `stage` from the committed ncu summary, if the kernels have not
+    changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return d.get("per_launch_bytes", {}).get(workload, {}).get(stage)
+
+
+# ------------------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+        target = vis[gpu_index].strip() if gpu_index < len(vis) else str(gpu_index)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", target],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------- CPU oracle arm
+def oracle_rate(w, d, budget_s: float, max_tokens=None):
+    """Time the CPU oracle (routing + per-token expert MLP) on a bounded token sample.
+
+    Returns (TFLOP/s, seconds, tokens per pass, passes, cores)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    flops_tok = w.flops() / w.T
+    gating = d["gating_output"].cpu().numpy()
+    bias = None if d["correction_bias"] is None else d["correction_bias"].cpu().numpy()
+    sc = oracle.SOFTMAX if w.scoring_func == "softmax" else oracle.SIGMOID
+    ids, wts, _ = oracle.route(gating, w.top_k, sc, w.renormalize, w.num_expert_group,
+                               w.topk_group, w.routed_scaling_factor, bias)
+    # Sample: the first n tokens, n sized for about 1/4 of the budget per pass.
+    cores = oracle.num_threads()
+    n = max(1, min(w.T, int(0.25 * budget_s * 2e9 * cores / flops_tok)))
+    if max_tokens:
+        n = min(n, max_tokens)
+    toks = np.arange(n, dtype=np.int32)
+    used = sorted(set(int(e) for e in ids[:n].reshape(-1) if e >= 0))
+    slot = np.full(w.E, -1, np.int32)
+    slot[used] = np.arange(len(used), dtype=np.int32)
+    idx = torch.tensor(used, dtype=torch.long, device=d["w_gate_up"].device)
+    wgu = d["w_gate_up"].index_select(0, idx).cpu()
+    wdn = d["w_down"].index_select(0, idx).cpu()
+    sgu = None if d["shared_w_gate_up"] is None else d["shared_w_gate_up"].cpu()
+    sdn = None if d["shared_w_down"] is None else d["shared_w_down"].cpu()
+    hid = d["hidden_states"].cpu()
+    dt = oracle.BF16 if w.dtype == torch.bfloat16 else oracle.F16
+    g_n = np.ascontiguousarray(gating[:n])
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        i2, w2, _ = oracle.route(g_n, w.top_k, sc, w.renormalize, w.num_expert_group,
+                                 w.topk_group, w.routed_scaling_factor, bias)
+        oracle.moe_tokens(hid, ids, wts, wgu, wdn, dt, tokens=toks, expert_slot=slot,
+                          num_experts=w.E, shared_w_gate_up=sgu, shared_w_down=sdn)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (passes >= 1 and el * (passes + 1) / passes > 3 * budget_s):
+            break
+    return flops_tok * n * passes / el / 1e12, el, n, passes, cores
+
+
+# ------------------------------------------------------------------------------------ main arm
+def run_ours(args, w, ws_n, rank, local):
+    import numpy as np
+    import torch
+
+    from mixture_experts_forward_moe_gb300 import binding as B
+    from mixture_experts_forward_moe_gb300 import inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    d = inputs.generate(w, seed=args.seed, device=dev)
+    kw = dict(correction_bias=d["correction_bias"], shared_w_gate_up=d["shared_w_gate_up"],
+              shared_w_down=d["shared_w_down"], **w.kwargs())
+    prob = B.make_problem(w.T, w.H, w.E, w.F, w.top_k, w.dtype, w.scoring_func, w.renormalize,
+                          w.num_expert_group, w.topk_group, w.routed_scaling_factor, w.S)
+    wsp = B.new_workspace(B.workspace_size(prob), dev)
+    out = torch.empty((w.T, w.H), dtype=w.dtype, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        B.fused_moe_fwd(d["hidden_states"], d["gating_output"], d["w_gate_up"], d["w_down"],
+                        out=out, workspace=wsp, **kw)
+
+    ids, _ = B.moe_route(d["gating_output"], w.top_k, w.scoring_func, w.renormalize,
+                         d["correction_bias"], w.num_expert_group, w.topk_group,
+                         w.routed_scaling_factor)
+    n_unique = int(torch.unique(ids[ids >= 0]).numel())
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st = B.get_device_status(wsp)
+    if st != B.MOE_OK:
+        raise RuntimeError(f"device status after warm-up: {B.status_string(st)}")
+
+    dominant_candidates = ["gemm1", "gemm2"] + (["shared_gemm1", "shared_gemm2"] if w.S else [])
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local) if rank == 0 else None
+    barrier()
+    torch.cuda.synchronize()
+    B.profile_enable(dominant_candidates)
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    prof = B.profile_collect()
+    B.profile_enable([])
+    clk = clocks.stop() if clocks else None
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = float(sum(step_ms))
+    max_ms = max_over_ranks(total_ms)
+    st = B.get_device_status(wsp)
+    if st != B.MOE_OK:
+        raise RuntimeError(f"device status after timed steps: {B.status_string(st)}")
+
+    flops = w.flops()
+    value = job_throughput(flops, ws_n, args.steps, max_ms) / 1e12
+    ms_per_step = max_ms / args.steps
+    ab = algorithmic_bytes(w, n_unique)
+    hbm_gbs, bf16_peak, bf16_sust, peak_src = measured_peaks()
+    launches = sum(v[2] for v in prof.values())
+
+    # Dominant kernel: the instrumented stage with the largest summed device time.
+    dom = max(dominant_candidates, key=lambda s: prof[s][0])
+    dom_ms, dom_calls, _ = prof[dom]
+    dom_avg = dom_ms / max(dom_calls, 1)
+    achieved = ab[dom] / (dom_avg * 1e-3) / 1e9
+    traffic = recorded_traffic(w.name, dom)
+    roofline = {"bound": "hbm", "kernel": f"moe_gemm_kernel ({dom})", "achieved": achieved,
+                "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
+                "traffic": traffic, "algorithmic_bytes": ab[dom], "avg_launch_ms": dom_avg,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_src == "measured" else "fallback 6.8 TB/s"}
+    tensor = {"achieved_tflops": stage_flops(w)[dom] / (dom_avg * 1e-3) / 1e12,
+              "peak_tflops": bf16_sust, "peak_source": f"{peak_src} bf16_tflops_sustained"}
+    tensor["frac"] = tensor["achieved_tflops"] / bf16_sust
+    roofline["tensor"] = tensor
+    stages = {k: {"avg_ms": v[0] / v[1], "calls": v[1]} for k, v in prof.items() if v[1]}
+
+    res = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws_n,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f16",
+        "data": "synthetic: seeded N(0,1) hidden states and router logits, N(0,1/fan_in) "
+                "weights" + (", N(0, 0.1^2) correction bias" if w.bias_std else ""),
+        "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "F": w.F,
+                   "top_k": w.top_k, "S": w.S, "scoring": w.scoring_func,
+                   "num_expert_group": w.num_expert_group, "topk_group": w.topk_group,
+                   "routed_scaling_factor": w.routed_scaling_factor,
+                   "global_batch": w.T * ws_n, "parallelism": f"replicas x{ws_n}",
+                   "l2": "flushed between steps (256 MiB write outside the timed events)",
+                   "timing": "CUDA event pair per step on the launching stream; sum of K"},
+        "ms_median": statistics.median(step_ms), "hbm_gbs": ab["total"] / (ms_per_step * 1e-3) / 1e9,
+        "hbm_frac": ab["total"] / (ms_per_step * 1e-3) / 1e9 / hbm_gbs,
+        "unique_experts": n_unique, "roofline": roofline, "gpu_launches": launches,
+        "launches_per_step": launches / args.steps, "stages": stages, "clocks": clk,
+    }
+    pub = PUBLISHED_TFLOPS.get((w.name, res["dtype"]))
+    if pub:
+        res["vs_baseline"] = value / pub
+
+    # End to end through the public API from pinned host buffers.
+    if not args.no_e2e:
+        h_hidden = d["hidden_states"].cpu().pin_memory()
+        h_gating = d["gating_output"].cpu().pin_memory()
+        h_out = torch.empty((w.T, w.H), dtype=w.dtype, pin_memory=True)
+        bufs = {"hidden": torch.empty_like(d["hidden_states"]),
+                "gating": torch.empty_like(d["gating_output"]), "out": out}
+        n_e2e = max(1, min(args.steps, 200))
+        for _ in range(3):
+            B.fused_moe_fwd_host(h_hidden, h_gating, d["w_gate_up"], d["w_down"], out_host=h_out,
+                                 dev_bufs=bufs, workspace=wsp, **kw)
+        torch.cuda.synchronize()
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_e2e)]
+        barrier()
+        torch.cuda.synchronize()
+        for i in range(n_e2e):
+            flush.zero_()
+            es[2 * i].record(stream)
+            B.fused_moe_fwd_host(h_hidden, h_gating, d["w_gate_up"], d["w_down"], out_host=h_out,
+                                 dev_bufs=bufs, workspace=wsp, **kw)
+            es[2 * i + 1].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = max_over_ranks(sum(es[2 * i].elapsed_time(es[2 * i + 1]) for i in range(n_e2e)))
+        res["e2e"] = {"value": job_throughput(flops, ws_n, n_e2e, e2e_ms) / 1e12,
+                      "unit": "TFLOP/s", "steps": n_e2e,
+                      "h2d_bytes_per_step": h_hidden.numel() * h_hidden.element_size()
+                      + h_gating.numel() * 4,
+                      "d2h_bytes_per_step": h_out.numel() * h_out.element_size(),
+                      "ms_per_step": e2e_ms / n_e2e}
+
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        rate, el, n, passes, cores = oracle_rate(w, d, budget_s=args.cpu_budget)
+        res["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": cores,
+                               "kind": "oracle",
+                               "sample": f"{n} of {w.T} tokens (routing + expert MLP, fp64), "
+                                         f"{passes} passes in {el:.1f} s"}
+    return res
+
+
+def run_reference(args, w):
+    """The CPU oracle as a bench arm: each step is one oracle pass over a bounded token sample."""
+    import torch
+
+    from mixture_experts_forward_moe_gb300 import inputs
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    d = inputs.generate(w, seed=args.seed, device=dev)
+    per_step = max(0.5, min(10.0, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_rate(w, d, budget_s=0.0, max_tokens=None)
+    times, flops, n_last, cores = [], 0.0, 0, 1
+    for _ in range(args.steps):
+        rate, el, n, passes, cores = oracle_rate(w, d, budget_s=per_step)
+        times.append(el)
+        flops += rate * el * 1e12
+        n_last = n
+    total = sum(times)
+    value = flops / total / 1e12
+    res = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "f64", "data": "synthetic (same seeded inputs as the GPU arm)",
+           "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "F": w.F,
+                      "top_k": w.top_k, "S": w.S},
+           "impl": "reference",
+           "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                            "sample": f"{n_last} of {w.T} tokens per pass, ~{per_step:.1f} s "
+                                      f"per step"},
+           "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    return res
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    import torch
+
+    from mixture_experts_forward_moe_gb300 import inputs
+    w = inputs.WORKLOADS[args.workload]
+    if args.dtype == "f16":
+        w = w.with_(dtype=torch.float16)
+    ws_n, rank, local = dist_env()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        res = run_reference(args, w)
+        print(json.dumps(res), flush=True)
+        return 0
+
+    if ws_n > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    try:
+        res = run_ours(args, w, ws_n, rank, local)
+    finally:
+        if ws_n > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,259 @@
+/*
+ * moe.h -- C ABI of the GB300 fused Mixture-of-Experts forward library (libgb300moe.so).
+ *
+ * The problem statement follows the TileOPs benchmark page, "MoE" section:
+ *   op FusedMoEFwd:  hidden_states[T,H], gating_output[T,E] f32, w_gate_up[E,2F,H],
+ *                    w_down[E,H,F], top_k, renormalize; the sigmoid form adds
+ *                    correction_bias[E] f32, num_expert_group, topk_group and
+ *                    routed_scaling_factor;
+ *   op FusedMoESharedExpertFwd: adds shared_w_gate_up[2S,H] and shared_w_down[H,S].
+ * The path has five steps: router top-k, expert sort, grouped gate/up GEMM with SiLU(gate)*up,
+ * grouped down GEMM with the route weight, and the top-k combine (plus the shared expert).
+ *
+ * Conventions (all entry points):
+ *  - Pointers are DEVICE pointers unless stated; tensors are row-major and contiguous, with the
+ *    shapes given.  16-bit tensors (hidden_states, weights, out, intermediate rows) all have the
+ *    problem's dtype (bf16 or f16).  gating_output, correction_bias and route weights are f32.
+ *  - `stream` is a cudaStream_t passed as void*; all device work is enqueued on it and the call
+ *    returns without synchronising (except moe_get_device_status).
+ *  - Ownership: the caller owns every buffer.  The library never allocates device memory and
+ *    keeps no cached arenas; scratch space comes from the caller's `workspace`, sized by
+ *    moe_workspace_size.  Buffer addresses are fixed for the life of a call, so a call can be
+ *    captured into a CUDA graph and replayed with the same buffers.
+ *  - Errors: argument errors return synchronously, before any launch, and enqueue nothing.
+ *    A failed launch returns MOE_ERR_CUDA.  Errors found on the device (an expert id outside
+ *    [-1, E), a bounded wait that gave up) are written to a status word inside the workspace
+ *    and read with moe_get_device_status.
+ *  - Expert id -1 in a caller-supplied topk_ids marks a padding route: it is skipped and
+ *    contributes nothing (ROCm/aiter PR #5973 "[FlyDSL] Optimize MI308 MoE decoding (3/3)",
+ *    "Changes": routes with expert ID -1 are skipped).
+ *  - Supported sizes: H, F, S multiples of 8 (16-byte row pitch); 1 <= top_k <= 32;
+ *    top_k <= E <= 1024; T >= 0.  Unsupported combinations return MOE_ERR_UNSUPPORTED.
+ *  - Functions are reentrant given distinct workspaces.
+ */
+#ifndef GB300_MOE_H
+#define GB300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,         /* null pointer, negative or inconsistent size */
+  MOE_ERR_UNSUPPORTED = 2,         /* a valid problem outside the supported sizes */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < the size the call needs */
+  MOE_ERR_CUDA = 4,                /* a CUDA launch or API call failed */
+  MOE_ERR_TIMEOUT = 5,             /* device: a bounded wait inside a kernel gave up */
+  MOE_ERR_BAD_EXPERT_ID = 6        /* device: an expert id outside [-1, E) was seen */
+} moe_status_t;
+
+typedef enum { MOE_BF16 = 0, MOE_F16 = 1 } moe_dtype_t;
+typedef enum { MOE_SOFTMAX = 0, MOE_SIGMOID = 1 } moe_scoring_t;
+
+/* Problem description.  Enumerations are stored as int32 so the layout is fixed. */
+typedef struct {
+  int32_t T;           /* tokens */
+  int32_t H;           /* hidden size */
+  int32_t E;           /* routed experts */
+  int32_t F;           /* expert intermediate size (w_gate_up has 2F rows per expert) */
+  int32_t top_k;       /* experts per token */
+  int32_t dtype;       /* moe_dtype_t of hidden_states, weights and outputs */
+  int32_t scoring;     /* moe_scoring_t */
+  int32_t renormalize; /* nonzero: route weights are normalised over the selected experts */
+  int32_t num_expert_group; /* 0 or 1: no grouping; else E % G == 0 and E/G >= 2 (sigmoid) */
+  int32_t topk_group;       /* groups kept when grouping, 1 <= topk_group <= G */
+  float routed_scaling_factor; /* multiplies every route weight; 1.0f when unused */
+  int32_t S;           /* shared-expert intermediate size; 0 = no shared expert */
+} moe_problem_t;
+
+/* ---------------------------------------------------------------------------------------- */
+/* Sizes (host only, no device work).                                                         */
+/* ---------------------------------------------------------------------------------------- */
+
+/* Bytes of workspace fused_moe_fwd needs for problem p (0 if p is invalid).  The first 256
+ * bytes hold the device status word; they must be zero before the workspace is first used
+ * (moe_workspace_init does this).  It also serves the staged entry points when the sort ran
+ * with block_m = 1 (see moe_stage_workspace_size for other alignments). */
+size_t moe_workspace_size(const moe_problem_t* p);
+
+/* Slots of sorted_ids (and rows of the sorted intermediate buffers) moe_align_sort may use for
+ * alignment block_m: T*top_k + E*(block_m-1).  -1 if the arguments are invalid. */
+int64_t moe_sorted_capacity(const moe_problem_t* p, int32_t block_m);
+
+/* Bytes of workspace the staged entry points need when moe_align_sort ran with block_m
+ * (block_m = 1 gives moe_workspace_size(p)).  0 if the arguments are invalid. */
+size_t moe_stage_workspace_size(const moe_problem_t* p, int32_t block_m);
+
+/* Zero the workspace's status header on `stream` (one 256-byte memset). */
+moe_status_t moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------- */
+/* Whole path.                                                                                */
+/* ---------------------------------------------------------------------------------------- */
+
+/*
+ * fused_moe_fwd -- TileOPs "MoE" page, ops FusedMoEFwd and FusedMoESharedExpertFwd.
+ *   out[t,:] = sum_j w[t,j] * W_down[e_tj] . (SiLU(W_gate[e_tj] x_t) * (W_up[e_tj] x_t))
+ *              + shared(x_t)
+ * where W_gate[e] = w_gate_up[e, 0:F, :], W_up[e] = w_gate_up[e, F:2F, :], (e_tj, w[t,j]) come
+ * from the router (moe_route), and shared(x) = shared_w_down . (SiLU(Wsg x) * (Wsu x)) with
+ * Wsg = shared_w_gate_up[0:S, :], Wsu = shared_w_gate_up[S:2S, :] (added unweighted).
+ *   hidden_states   [T,H] dtype
+ *   gating_output   [T,E] f32 router logits
+ *   w_gate_up       [E,2F,H] dtype;  w_down [E,H,F] dtype
+ *   correction_bias [E] f32 or NULL (sigmoid scoring only)
+ *   shared_w_gate_up [2S,H], shared_w_down [H,S] dtype; both NULL iff p->S == 0
+ *   out             [T,H] dtype (written in full)
+ * For T <= 8 the experts run straight from the router's ids (no sort); otherwise the routes are
+ * sorted into expert-contiguous rows first.
+ */
+moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
+                           const float* gating_output, const void* w_gate_up, const void* w_down,
+                           const float* correction_bias, const void* shared_w_gate_up,
+                           const void* shared_w_down, void* out, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------- */
+/* Staged entry points (the same kernels, callable one at a time).                          */
+/* ---------------------------------------------------------------------------------------- */
+
+/*
+ * moe_route -- TileOPs "MoE" page, op FusedTopKFwd (and the routing of FusedMoEFwd).
+ * Per token, ids in selection order (descending key, equal keys -> lower expert id):
+ *   softmax: key = the raw logit (softmax is monotone); weight_j = exp(x_j - max) / D with D
+ *            summed over the selected experts if renormalize, else over all E.
+ *   sigmoid: s_e = sigmoid(x_e); key = s_e + correction_bias_e.  With num_expert_group G > 1
+ *            the experts form G contiguous groups; a group's score is the sum of its two
+ *            largest keys; the topk_group best groups are kept (ties -> lower group) and only
+ *            their experts are candidates.  weight_j = s_j / sum_selected(s) if renormalize,
+ *            else s_j.
+ *   Every weight is then multiplied by routed_scaling_factor.
+ * The f32 sigmoid used for the selection key is a fixed sequence of correctly rounded f32
+ * operations (Cody-Waite reduction of exp with a degree-7 Taylor polynomial), so the same
+ * logits give the same ids on every run.
+ *   gating_output [T,E] f32; correction_bias [E] f32 or NULL
+ *   topk_ids [T,top_k] int32 (out); topk_weights [T,top_k] f32 (out)
+ */
+moe_status_t moe_route(const moe_problem_t* p, const float* gating_output,
+                       const float* correction_bias, int32_t* topk_ids, float* topk_weights,
+                       void* stream);
+
+/*
+ * moe_align_sort -- TileOPs "MoE" page, op MoEPermuteAlignFwd; the inverse map follows aiter
+ * PR #5973 "Changes" (the sort returns each route's sorted row).  A stable counting sort of the
+ * flat route index r = t*top_k + j by expert.
+ *   topk_ids     [T,top_k] int32 in; -1 = padding route (skipped)
+ *   counts       [E] out: live routes per expert
+ *   offsets      [E+1] out: start of each expert's segment; each segment is padded to a
+ *                multiple of block_m; offsets[E] = padded total
+ *   sorted_ids   [cap] out, cap = moe_sorted_capacity(p, block_m): the routes of each segment
+ *                in ascending r, then -1 in padding slots; -1 from offsets[E] to cap
+ *   tile_expert  [ceil(cap/block_m)] out or NULL: expert owning rows [i*block_m,(i+1)*block_m),
+ *                -1 past the end
+ *   inv_route    [T*top_k] out: sorted position of each route, -1 for padding routes
+ *   workspace    scratch (moe_workspace_size bytes) also holding the status word; an id outside
+ *                [-1,E) is treated as padding and sets MOE_ERR_BAD_EXPERT_ID there.
+ */
+moe_status_t moe_align_sort(const moe_problem_t* p, int32_t block_m, const int32_t* topk_ids,
+                            int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
+                            int32_t* tile_expert, int32_t* inv_route, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/*
+ * moe_gemm1_swiglu -- TileOPs "MoE" page, op MoEGroupedGemmFwd with activation=silu_and_mul
+ * (contiguous layout): gathers hidden_states rows in sorted order and, per expert segment e,
+ *   act[p, f] = SiLU(sum_h Wg[e,f,h] x[h]) * (sum_h Wu[e,f,h] x[h]),  x = hidden[sorted_ids[p]/k]
+ * on the tensor cores (bf16/f16 operands, f32 accumulation, f32 epilogue, one rounding to dtype).
+ *   hidden_states [T,H]; block_m, sorted_ids, offsets: as given to / produced by
+ *   moe_align_sort; w_gate_up [E,2F,H]; act [cap,F] out, cap = moe_sorted_capacity(p,block_m)
+ *   (rows of padding slots are written as zero).  workspace: moe_stage_workspace_size bytes.
+ */
+moe_status_t moe_gemm1_swiglu(const moe_problem_t* p, int32_t block_m, const void* hidden_states,
+                              const int32_t* sorted_ids, const int32_t* offsets,
+                              const void* w_gate_up, void* act, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
+ * moe_gemm2 -- TileOPs "MoE" page, op MoEGroupedGemmFwd (down projection, contiguous layout),
+ * with the route weight applied in the epilogue:
+ *   y_route[p, h] = topk_weights[sorted_ids[p]] * sum_f Wd[e,h,f] act[p,f]   (0 for padding)
+ *   block_m, sorted_ids, offsets: as for moe_gemm1_swiglu; act [cap,F];
+ *   topk_weights [T*top_k] f32; w_down [E,H,F]; y_route [cap,H] out.
+ */
+moe_status_t moe_gemm2(const moe_problem_t* p, int32_t block_m, const void* act,
+                       const int32_t* sorted_ids,
+                       const int32_t* offsets, const float* topk_weights, const void* w_down,
+                       void* y_route, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * moe_combine -- TileOPs "MoE" page, op MoEPostPermuteFwd; aiter PR #5973 "Changes"
+ * (sorted_sum writes the output in full, so no pre-clear is needed):
+ *   out[t,:] = round( sum_{j=0..k-1} y_route[inv_route[t*k+j], :] (+ shared_out[t,:]) )
+ * summed in f32 in fixed j order (deterministic: no atomics).  Routes with inv_route -1, or
+ * with topk_ids -1 when topk_ids is given, are skipped.  inv_route NULL means the identity
+ * (route r at row r).
+ *   y_route [rows,H]; inv_route [T*k] or NULL; topk_ids [T*k] or NULL;
+ *   shared_out [T,H] or NULL; out [T,H]
+ */
+moe_status_t moe_combine(const moe_problem_t* p, const void* y_route, const int32_t* inv_route,
+                         const int32_t* topk_ids, const void* shared_out, void* out,
+                         void* stream);
+
+/*
+ * moe_shared_expert_fwd -- TileOPs "MoE" page, op SharedExpertMLPFwd: the dense SwiGLU MLP
+ *   shared_out = shared_w_down . (SiLU(Wsg x) * (Wsu x)) for every token, no routing weight.
+ *   hidden_states [T,H]; shared_w_gate_up [2S,H]; shared_w_down [H,S]; shared_out [T,H] out.
+ */
+moe_status_t moe_shared_expert_fwd(const moe_problem_t* p, const void* hidden_states,
+                                   const void* shared_w_gate_up, const void* shared_w_down,
+                                   void* shared_out, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/* ---------------------------------------------------------------------------------------- */
+/* Status.                                                                                    */
+/* ---------------------------------------------------------------------------------------- */
+
+/* Synchronises `stream`, returns the first device-side error recorded in the workspace's
+ * status word since it was last read (MOE_OK if none) and clears it. */
+moe_status_t moe_get_device_status(void* workspace, void* stream);
+
+/* Static English description of a status code. */
+const char* moe_status_string(moe_status_t s);
+
+/* Test-only knob: the limit, in nanoseconds, of every bounded wait inside the kernels
+ * (default 2e9).  A limit of 0 makes the first wait that is not already satisfied give up, so
+ * the timeout path can be exercised without a hang.  Returns the previous value. */
+uint64_t moe_set_wait_limit_ns(uint64_t limit_ns);
+
+/* ---------------------------------------------------------------------------------------- */
+/* Stage profiling (benchmarks).                                                              */
+/* ---------------------------------------------------------------------------------------- */
+
+/* Stages of fused_moe_fwd, in launch order: 0 route, 1 sort, 2 tiles, 3 permute, 4 gemm1,
+ * 5 gemm2, 6 shared_gemm1, 7 shared_gemm2, 8 combine. */
+#define MOE_NUM_STAGES 9
+
+/* Name of stage i (NULL when out of range). */
+const char* moe_stage_name(int32_t stage);
+
+/* stage_mask != 0: from now on fused_moe_fwd records a CUDA event pair around every stage i
+ * whose bit (1 << i) is set, on the call's stream (host-side event objects, no device memory);
+ * kernel launches are counted for every stage.  Totals are reset.  stage_mask == 0 stops the
+ * event recording.  Must not be enabled while a call is being captured into a CUDA graph. */
+moe_status_t moe_profile_enable(int32_t stage_mask);
+
+/* Synchronises on the recorded events and writes, per stage, the summed device milliseconds,
+ * the number of recorded calls and the number of kernel launches since moe_profile_enable;
+ * returns the number of stages written (<= max_stages) and resets the totals. */
+int32_t moe_profile_collect(double* total_ms, int64_t* calls, int64_t* launches,
+                            int32_t max_stages);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_MOE_H */

@@ -1,0 +1,406 @@
+"""Thin ctypes binding over libgb300moe.so, with the C ABI's names.
+
+Argument marshalling only: every step of the path runs in the library's CUDA kernels.  torch is
+used for device memory (outputs, workspaces) and for the current CUDA stream.  There is no
+fallback: if the library cannot be loaded the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED = 0, 1, 2
+MOE_ERR_WORKSPACE_TOO_SMALL, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_BAD_EXPERT_ID = 3, 4, 5, 6
+MOE_BF16, MOE_F16 = 0, 1
+MOE_SOFTMAX, MOE_SIGMOID = 0, 1
+
+_DTYPES = {torch.bfloat16: MOE_BF16, torch.float16: MOE_F16}
+_SCORING = {"softmax": MOE_SOFTMAX, "sigmoid": MOE_SIGMOID}
+
+# Every symbol include/moe.h declares.
+EXPORTED = (
+    "moe_workspace_size", "moe_sorted_capacity", "moe_stage_workspace_size",
+    "moe_workspace_init", "fused_moe_fwd", "moe_route", "moe_align_sort", "moe_gemm1_swiglu",
+    "moe_gemm2", "moe_combine", "moe_shared_expert_fwd", "moe_get_device_status",
+    "moe_status_string", "moe_set_wait_limit_ns", "moe_stage_name", "moe_profile_enable",
+    "moe_profile_collect",
+)
+
+
+class MoeProblem(ctypes.Structure):
+    _fields_ = [
+        ("T", ctypes.c_int32), ("H", ctypes.c_int32), ("E", ctypes.c_int32),
+        ("F", ctypes.c_int32), ("top_k", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("scoring", ctypes.c_int32), ("renormalize", ctypes.c_int32),
+        ("num_expert_group", ctypes.c_int32), ("topk_group", ctypes.c_int32),
+        ("routed_scaling_factor", ctypes.c_float), ("S", ctypes.c_int32),
+    ]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} (code {code})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load libgb300moe.so (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            L = ctypes.CDLL(path)
+            P, sz, i32, i64, u64 = (ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32,
+                                    ctypes.c_int64, ctypes.c_uint64)
+            PP = ctypes.POINTER(MoeProblem)
+            L.moe_workspace_size.restype = sz
+            L.moe_workspace_size.argtypes = [PP]
+            L.moe_sorted_capacity.restype = i64
+            L.moe_sorted_capacity.argtypes = [PP, i32]
+            L.moe_stage_workspace_size.restype = sz
+            L.moe_stage_workspace_size.argtypes = [PP, i32]
+            L.moe_workspace_init.argtypes = [P, sz, P]
+            L.fused_moe_fwd.argtypes = [PP, P, P, P, P, P, P, P, P, P, sz, P]
+            L.moe_route.argtypes = [PP, P, P, P, P, P]
+            L.moe_align_sort.argtypes = [PP, i32, P, P, P, P, P, P, P, sz, P]
+            L.moe_gemm1_swiglu.argtypes = [PP, i32, P, P, P, P, P, P, sz, P]
+            L.moe_gemm2.argtypes = [PP, i32, P, P, P, P, P, P, P, sz, P]
+            L.moe_combine.argtypes = [PP, P, P, P, P, P, P]
+            L.moe_shared_expert_fwd.argtypes = [PP, P, P, P, P, P, sz, P]
+            L.moe_get_device_status.argtypes = [P, P]
+            L.moe_status_string.restype = ctypes.c_char_p
+            L.moe_status_string.argtypes = [ctypes.c_int]
+            L.moe_set_wait_limit_ns.restype = u64
+            L.moe_set_wait_limit_ns.argtypes = [u64]
+            L.moe_stage_name.restype = ctypes.c_char_p
+            L.moe_stage_name.argtypes = [i32]
+            L.moe_profile_enable.restype = ctypes.c_int
+            L.moe_profile_enable.argtypes = [i32]
+            L.moe_profile_collect.restype = i32
+            L.moe_profile_collect.argtypes = [P, P, P, i32]
+            for fn in ("fused_moe_fwd", "moe_route", "moe_align_sort", "moe_gemm1_swiglu",
+                       "moe_gemm2", "moe_combine", "moe_shared_expert_fwd",
+                       "moe_get_device_status", "moe_workspace_init"):
+                getattr(L, fn).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().moe_status_string(int(code)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != MOE_OK:
+        raise MoeError(rc, what)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def make_problem(T, H, E, F, top_k, dtype=torch.bfloat16, scoring_func="softmax",
+                 renormalize=True, num_expert_group=0, topk_group=0, routed_scaling_factor=1.0,
+                 S=0) -> MoeProblem:
+    if dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dtype}")
+    if scoring_func not in _SCORING:
+        raise ValueError(f"unsupported scoring_func {scoring_func}")
+    return MoeProblem(int(T), int(H), int(E), int(F), int(top_k), _DTYPES[dtype],
+                      _SCORING[scoring_func], int(bool(renormalize)), int(num_expert_group),
+                      int(topk_group), float(routed_scaling_factor), int(S))
+
+
+def workspace_size(prob: MoeProblem) -> int:
+    n = lib().moe_workspace_size(ctypes.byref(prob))
+    if n == 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, "moe_workspace_size")
+    return int(n)
+
+
+def stage_workspace_size(prob: MoeProblem, block_m: int) -> int:
+    n = lib().moe_stage_workspace_size(ctypes.byref(prob), int(block_m))
+    if n == 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, "moe_stage_workspace_size")
+    return int(n)
+
+
+def sorted_capacity(prob: MoeProblem, block_m: int) -> int:
+    n = lib().moe_sorted_capacity(ctypes.byref(prob), int(block_m))
+    if n < 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, "moe_sorted_capacity")
+    return int(n)
+
+
+def new_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A zeroed uint8 device buffer (the status header must start at zero)."""
+    return torch.zeros(int(nbytes), dtype=torch.uint8, device=device or "cuda")
+
+
+_ws_cache: dict = {}
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    key = (str(device), threading.get_ident())
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = new_workspace(nbytes, device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def get_device_status(workspace: torch.Tensor, stream=None) -> int:
+    return int(lib().moe_get_device_status(_p(workspace), _stream(stream)))
+
+
+def set_wait_limit_ns(limit_ns: int) -> int:
+    return int(lib().moe_set_wait_limit_ns(int(limit_ns)))
+
+
+NUM_STAGES = 9
+
+
+def stage_names():
+    return [lib().moe_stage_name(i).decode() for i in range(NUM_STAGES)]
+
+
+def profile_enable(stages=None):
+    """Record event pairs around the named stages (all when None; none when [])."""
+    names = stage_names()
+    if stages is None:
+        mask = (1 << NUM_STAGES) - 1
+    else:
+        mask = 0
+        for s in stages:
+            mask |= 1 << names.index(s)
+    _check(lib().moe_profile_enable(mask), "moe_profile_enable")
+
+
+def profile_collect() -> dict:
+    """{stage: (total_ms, calls, launches)} since profile_enable; resets the totals."""
+    ms = (ctypes.c_double * NUM_STAGES)()
+    calls = (ctypes.c_int64 * NUM_STAGES)()
+    launches = (ctypes.c_int64 * NUM_STAGES)()
+    n = lib().moe_profile_collect(ms, calls, launches, NUM_STAGES)
+    names = stage_names()
+    return {names[i]: (float(ms[i]), int(calls[i]), int(launches[i])) for i in range(n)}
+
+
+def fused_moe_fwd(hidden_states, gating_output, w_gate_up, w_down, top_k, renormalize=True,
+                  scoring_func="softmax", correction_bias=None, num_expert_group=0, topk_group=0,
+                  routed_scaling_factor=1.0, shared_w_gate_up=None, shared_w_down=None, out=None,
+                  workspace=None, stream=None):
+    """The whole fused MoE forward (include/moe.h: fused_moe_fwd); returns out [T, H]."""
+    T, H = hidden_states.shape
+    E, F2, _ = w_gate_up.shape
+    F = F2 // 2
+    S = 0 if shared_w_gate_up is None else shared_w_gate_up.shape[0] // 2
+    dt = hidden_states.dtype
+    _need(hidden_states, "hidden_states", dt)
+    _need(gating_output, "gating_output", torch.float32, (T, E))
+    _need(w_gate_up, "w_gate_up", dt, (E, 2 * F, H))
+    _need(w_down, "w_down", dt, (E, H, F))
+    if correction_bias is not None:
+        _need(correction_bias, "correction_bias", torch.float32, (E,))
+    if S:
+        _need(shared_w_gate_up, "shared_w_gate_up", dt, (2 * S, H))
+        _need(shared_w_down, "shared_w_down", dt, (H, S))
+    prob = make_problem(T, H, E, F, top_k, dt, scoring_func, renormalize, num_expert_group,
+                        topk_group, routed_scaling_factor, S)
+    nbytes = workspace_size(prob)
+    if workspace is None:
+        workspace = _workspace(nbytes, hidden_states.device)
+    if out is None:
+        out = torch.empty((T, H), dtype=dt, device=hidden_states.device)
+    _need(out, "out", dt, (T, H))
+    rc = lib().fused_moe_fwd(ctypes.byref(prob), _p(hidden_states), _p(gating_output),
+                             _p(w_gate_up), _p(w_down), _p(correction_bias),
+                             _p(shared_w_gate_up), _p(shared_w_down), _p(out), _p(workspace),
+                             workspace.numel(), _stream(stream))
+    _check(rc, "fused_moe_fwd")
+    return out
+
+
+def moe_route(gating_output, top_k, scoring_func="softmax", renormalize=True,
+              correction_bias=None, num_expert_group=0, topk_group=0,
+              routed_scaling_factor=1.0, stream=None):
+    """Router top-k (include/moe.h: moe_route); returns (topk_ids int32, topk_weights f32)."""
+    _need(gating_output, "gating_output", torch.float32)
+    T, E = gating_output.shape
+    if correction_bias is not None:
+        _need(correction_bias, "correction_bias", torch.float32, (E,))
+    prob = make_problem(T, 8, E, 8, top_k, torch.bfloat16, scoring_func, renormalize,
+                        num_expert_group, topk_group, routed_scaling_factor)
+    ids = torch.empty((T, top_k), dtype=torch.int32, device=gating_output.device)
+    w = torch.empty((T, top_k), dtype=torch.float32, device=gating_output.device)
+    _check(lib().moe_route(ctypes.byref(prob), _p(gating_output), _p(correction_bias), _p(ids),
+                           _p(w), _stream(stream)), "moe_route")
+    return ids, w
+
+
+def moe_align_sort(topk_ids, num_experts, block_m=1, workspace=None, stream=None,
+                   want_tile_expert=True):
+    """Expert sort (include/moe.h: moe_align_sort); returns a dict of device tensors."""
+    _need(topk_ids, "topk_ids", torch.int32)
+    T, k = topk_ids.shape
+    E = int(num_experts)
+    prob = make_problem(T, 8, E, 8, k)
+    cap = sorted_capacity(prob, block_m)
+    dev = topk_ids.device
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    sorted_ids = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+    tile_len = (cap + block_m - 1) // block_m
+    tile_expert = (torch.empty(max(tile_len, 1), dtype=torch.int32, device=dev)
+                   if want_tile_expert else None)
+    inv = torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)
+    nbytes = workspace_size(prob)
+    if workspace is None:
+        workspace = _workspace(nbytes, dev)
+    _check(lib().moe_align_sort(ctypes.byref(prob), int(block_m), _p(topk_ids), _p(counts),
+                                _p(offsets), _p(sorted_ids), _p(tile_expert), _p(inv),
+                                _p(workspace), workspace.numel(), _stream(stream)),
+           "moe_align_sort")
+    return dict(counts=counts, offsets=offsets, sorted_ids=sorted_ids[:cap],
+                tile_expert=None if tile_expert is None else tile_expert[:tile_len],
+                inv_route=inv[:T * k], workspace=workspace)
+
+
+def moe_gemm1_swiglu(hidden_states, sorted_ids, offsets, w_gate_up, top_k, block_m=1,
+                     workspace=None, stream=None):
+    """Grouped gate/up GEMM + SiLU*up (include/moe.h: moe_gemm1_swiglu); returns act [cap, F]."""
+    T, H = hidden_states.shape
+    E, F2, _ = w_gate_up.shape
+    F = F2 // 2
+    dt = hidden_states.dtype
+    _need(hidden_states, "hidden_states", dt)
+    _need(w_gate_up, "w_gate_up", dt, (E, F2, H))
+    _need(sorted_ids, "sorted_ids", torch.int32)
+    _need(offsets, "offsets", torch.int32, (E + 1,))
+    prob = make_problem(T, H, E, F, top_k, dt)
+    cap = sorted_capacity(prob, block_m)
+    act = torch.empty((max(cap, 1), F), dtype=dt, device=hidden_states.device)
+    nbytes = stage_workspace_size(prob, block_m)
+    if workspace is None:
+        workspace = _workspace(nbytes, hidden_states.device)
+    _check(lib().moe_gemm1_swiglu(ctypes.byref(prob), int(block_m), _p(hidden_states),
+                                  _p(sorted_ids), _p(offsets), _p(w_gate_up), _p(act),
+                                  _p(workspace), workspace.numel(), _stream(stream)),
+           "moe_gemm1_swiglu")
+    return act[:cap]
+
+
+def moe_gemm2(act, sorted_ids, offsets, topk_weights, w_down, T, top_k, block_m=1,
+              workspace=None, stream=None):
+    """Grouped down GEMM x route weight (include/moe.h: moe_gemm2); returns y_route [cap, H]."""
+    E, H, F = w_down.shape
+    dt = w_down.dtype
+    _need(w_down, "w_down", dt)
+    _need(act, "act", dt)
+    _need(sorted_ids, "sorted_ids", torch.int32)
+    _need(offsets, "offsets", torch.int32, (E + 1,))
+    _need(topk_weights, "topk_weights", torch.float32)
+    prob = make_problem(T, H, E, F, top_k, dt)
+    cap = sorted_capacity(prob, block_m)
+    if act.shape[0] < cap or act.shape[1] != F:
+        raise ValueError(f"act must have at least {cap} rows of {F} columns")
+    y = torch.empty((max(cap, 1), H), dtype=dt, device=w_down.device)
+    nbytes = stage_workspace_size(prob, block_m)
+    if workspace is None:
+        workspace = _workspace(nbytes, w_down.device)
+    _check(lib().moe_gemm2(ctypes.byref(prob), int(block_m), _p(act), _p(sorted_ids),
+                           _p(offsets), _p(topk_weights), _p(w_down), _p(y), _p(workspace),
+                           workspace.numel(), _stream(stream)), "moe_gemm2")
+    return y[:cap]
+
+
+def moe_combine(y_route, inv_route, T, top_k, topk_ids=None, shared_out=None, out=None,
+                stream=None):
+    """Deterministic top-k combine (include/moe.h: moe_combine); returns out [T, H]."""
+    _need(y_route, "y_route")
+    H = y_route.shape[1]
+    dt = y_route.dtype
+    if inv_route is not None:
+        _need(inv_route, "inv_route", torch.int32)
+    if topk_ids is not None:
+        _need(topk_ids, "topk_ids", torch.int32)
+    if shared_out is not None:
+        _need(shared_out, "shared_out", dt, (T, H))
+    prob = make_problem(T, H, max(top_k, 1), 8, top_k, dt)
+    if out is None:
+        out = torch.empty((T, H), dtype=dt, device=y_route.device)
+    _check(lib().moe_combine(ctypes.byref(prob), _p(y_route), _p(inv_route), _p(topk_ids),
+                             _p(shared_out), _p(out), _stream(stream)), "moe_combine")
+    return out
+
+
+def moe_shared_expert_fwd(hidden_states, shared_w_gate_up, shared_w_down, workspace=None,
+                          stream=None):
+    """Dense SwiGLU shared expert (include/moe.h: moe_shared_expert_fwd); returns [T, H]."""
+    T, H = hidden_states.shape
+    S = shared_w_gate_up.shape[0] // 2
+    dt = hidden_states.dtype
+    _need(hidden_states, "hidden_states", dt)
+    _need(shared_w_gate_up, "shared_w_gate_up", dt, (2 * S, H))
+    _need(shared_w_down, "shared_w_down", dt, (H, S))
+    prob = make_problem(T, H, 1, 8, 1, dt, S=S)
+    out = torch.empty((T, H), dtype=dt, device=hidden_states.device)
+    nbytes = workspace_size(prob)
+    if workspace is None:
+        workspace = _workspace(nbytes, hidden_states.device)
+    _check(lib().moe_shared_expert_fwd(ctypes.byref(prob), _p(hidden_states),
+                                       _p(shared_w_gate_up), _p(shared_w_down), _p(out),
+                                       _p(workspace), workspace.numel(), _stream(stream)),
+           "moe_shared_expert_fwd")
+    return out
+
+
+def fused_moe_fwd_host(hidden_host, gating_host, w_gate_up, w_down, top_k, out_host=None,
+                       dev_bufs=None, **kw):
+    """End-to-end call from pinned HOST buffers: host->device copies of the step's inputs, the
+    fused forward, and the device->host copy of the output, all on the current stream."""
+    dev = w_gate_up.device
+    if dev_bufs is None:
+        dev_bufs = dict(hidden=torch.empty(hidden_host.shape, dtype=hidden_host.dtype, device=dev),
+                        gating=torch.empty(gating_host.shape, dtype=gating_host.dtype, device=dev))
+    dev_bufs["hidden"].copy_(hidden_host, non_blocking=True)
+    dev_bufs["gating"].copy_(gating_host, non_blocking=True)
+    out = fused_moe_fwd(dev_bufs["hidden"], dev_bufs["gating"], w_gate_up, w_down, top_k,
+                        out=dev_bufs.get("out"), **kw)
+    dev_bufs["out"] = out
+    if out_host is None:
+        out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    out_host.copy_(out, non_blocking=True)
+    return out_host

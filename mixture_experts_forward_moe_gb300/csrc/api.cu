@@ -1,0 +1,569 @@
+// api.cu -- the C ABI declared in include/moe.h: argument validation, workspace carving and
+// the launch sequence of the fused MoE forward (router -> sort -> gather -> gemm1+SwiGLU ->
+// gemm2 x route weight -> combine, plus the shared expert).
+#include <stdio.h>
+
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+
+namespace gb300moe {
+
+namespace {
+
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+
+// ---- stage profiler: event pairs around each stage of fused_moe_fwd (opt-in) ----------------
+enum Stage { kRoute, kSort, kTiles, kPermute, kGemm1, kGemm2, kSharedGemm1, kSharedGemm2,
+             kCombine, kNumStages };
+static_assert(kNumStages == MOE_NUM_STAGES, "stage count");
+const char* const kStageNames[kNumStages] = {"route", "sort", "tiles", "permute", "gemm1",
+                                             "gemm2", "shared_gemm1", "shared_gemm2",
+                                             "combine"};
+
+struct Profiler {
+  std::mutex mu;
+  uint32_t mask = 0;
+  std::vector<cudaEvent_t> ev[kNumStages];  // pairs: start at 2i, end at 2i+1
+  size_t used[kNumStages] = {};
+  int64_t launches[kNumStages] = {};
+};
+Profiler g_prof;
+
+// Records the start of `stage` on `s`; returns the pair index or -1 when profiling is off.
+int prof_begin(int stage, cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (!((g_prof.mask >> stage) & 1u)) return -1;
+  auto& v = g_prof.ev[stage];
+  const size_t i = g_prof.used[stage];
+  if (2 * i + 2 > v.size()) {
+    cudaEvent_t a, b;
+    if (cudaEventCreate(&a) != cudaSuccess) return -1;
+    if (cudaEventCreate(&b) != cudaSuccess) {
+      cudaEventDestroy(a);
+      return -1;
+    }
+    v.push_back(a);
+    v.push_back(b);
+  }
+  if (cudaEventRecord(v[2 * i], s) != cudaSuccess) return -1;
+  g_prof.used[stage] = i + 1;
+  return (int)i;
+}
+
+void prof_end(int stage, int idx, cudaStream_t s, int n_launches) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  g_prof.launches[stage] += n_launches;
+  if (idx >= 0 && ((g_prof.mask >> stage) & 1u)) cudaEventRecord(g_prof.ev[stage][2 * idx + 1], s);
+}
+
+struct StageTimer {
+  int stage, idx;
+  cudaStream_t s;
+  StageTimer(int st, cudaStream_t st_s) : stage(st), idx(prof_begin(st, st_s)), s(st_s) {}
+  void done(int n_launches) { prof_end(stage, idx, s, n_launches); }
+};
+
+constexpr int kMaxE = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kDirectMaxT = 8;
+constexpr int kDirectMaxRoutes = kTileRows;
+constexpr int kSortChunk = 256;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int elt_bytes(const moe_problem_t&) { return 2; }
+
+// Checks the problem; returns MOE_OK, MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED.
+moe_status_t check_problem(const moe_problem_t* p) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  if (p->T < 0 || p->H <= 0 || p->E <= 0 || p->F <= 0 || p->top_k <= 0 || p->S < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (p->top_k > p->E) return MOE_ERR_INVALID_ARG;
+  if (p->dtype != MOE_BF16 && p->dtype != MOE_F16) return MOE_ERR_INVALID_ARG;
+  if (p->scoring != MOE_SOFTMAX && p->scoring != MOE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (!(p->routed_scaling_factor == p->routed_scaling_factor)) return MOE_ERR_INVALID_ARG;
+  if (p->num_expert_group < 0 || p->topk_group < 0) return MOE_ERR_INVALID_ARG;
+  if (p->num_expert_group > 1) {
+    const int G = p->num_expert_group;
+    if (p->E % G != 0 || p->E / G < 2) return MOE_ERR_INVALID_ARG;
+    if (p->topk_group < 1 || p->topk_group > G) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)p->topk_group * (p->E / G) < p->top_k) return MOE_ERR_INVALID_ARG;
+    if (G > 32) return MOE_ERR_UNSUPPORTED;
+    if (p->scoring != MOE_SIGMOID && p->topk_group < G) return MOE_ERR_UNSUPPORTED;
+  }
+  if (p->E > kMaxE || p->top_k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  if (p->H % 8 != 0 || p->F % 8 != 0 || p->S % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)p->T * p->top_k > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+bool use_direct(const moe_problem_t& p) {
+  return p.T <= kDirectMaxT && (int64_t)p.T * p.top_k <= kDirectMaxRoutes;
+}
+
+// Workspace layout of a call (all offsets 256-byte aligned).
+struct Layout {
+  int64_t P, cap, n_chunks, max_tiles;
+  size_t ids, w, counts, offsets, sorted, inv, chunk, tiles, a_sorted, act, y, sh_act, sh_out;
+  size_t total;
+};
+
+Layout make_layout(const moe_problem_t& p, int block_m) {
+  Layout L;
+  const int eb = elt_bytes(p);
+  L.P = (int64_t)p.T * p.top_k;
+  L.cap = L.P + (int64_t)p.E * (block_m - 1);
+  L.n_chunks = (L.P + kSortChunk - 1) / kSortChunk;
+  L.max_tiles = L.cap / kTileRows + p.E + 1;
+  const bool direct = block_m == 1 && use_direct(p);
+  size_t off = kHeaderBytes;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  L.ids = take(sizeof(int32_t) * L.P);
+  L.w = take(sizeof(float) * L.P);
+  L.counts = take(sizeof(int32_t) * p.E);
+  L.offsets = take(sizeof(int32_t) * (p.E + 1));
+  L.sorted = take(sizeof(int32_t) * L.cap);
+  L.inv = take(sizeof(int32_t) * L.P);
+  L.chunk = take(sizeof(int32_t) * L.n_chunks * p.E);
+  L.tiles = take(sizeof(Tile) * L.max_tiles);
+  L.a_sorted = take(direct ? 0 : (size_t)L.cap * p.H * eb);
+  L.act = take((size_t)L.cap * p.F * eb);
+  L.y = take((size_t)L.cap * p.H * eb);
+  L.sh_act = take((size_t)p.T * p.S * eb);
+  L.sh_out = take(p.S > 0 ? (size_t)p.T * p.H * eb : 0);
+  L.total = off;
+  return L;
+}
+
+template <typename P>
+P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
+}
+
+int* status_word(void* ws) { return static_cast<int*>(ws); }
+int* tile_counter(void* ws) { return reinterpret_cast<int*>(static_cast<char*>(ws) + 64); }
+
+moe_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                                 \
+  do {                                                \
+    cudaError_t _e = (expr);                          \
+    if (_e != cudaSuccess) return MOE_ERR_CUDA;       \
+  } while (0)
+
+GemmCall base_call(const moe_problem_t& p, int* status) {
+  GemmCall c{};
+  c.dtype = p.dtype;
+  c.status = status;
+  c.top_k = p.top_k;
+  c.T = p.T;
+  c.P = p.T * p.top_k;
+  c.E = p.E;
+  return c;
+}
+
+// Shared expert: dense gemm1 (hidden -> sh_act) and dense gemm2 (sh_act -> sh_out).
+cudaError_t run_shared(const moe_problem_t& p, const void* hidden, const void* sgu,
+                       const void* sd, void* sh_act, void* sh_out, int* status, cudaStream_t s) {
+  GemmCall g1 = base_call(p, status);
+  g1.gemm1 = 1;
+  g1.mode = kDense;
+  g1.K = p.H;
+  g1.n_out = p.S;
+  g1.E = 1;
+  g1.w = sgu;
+  g1.b = hidden;
+  g1.b_rows = p.T;
+  g1.out = sh_act;
+  g1.dense_rows = p.T;
+  cudaError_t e;
+  {
+    StageTimer t(kSharedGemm1, s);
+    e = launch_gemm(g1, s);
+    t.done(1);
+  }
+  if (e != cudaSuccess) return e;
+  GemmCall g2 = base_call(p, status);
+  g2.gemm1 = 0;
+  g2.mode = kDense;
+  g2.K = p.S;
+  g2.n_out = p.H;
+  g2.E = 1;
+  g2.w = sd;
+  g2.b = sh_act;
+  g2.b_rows = p.T;
+  g2.out = sh_out;
+  g2.dense_rows = p.T;
+  StageTimer t(kSharedGemm2, s);
+  e = launch_gemm(g2, s);
+  t.done(1);
+  return e;
+}
+
+}  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
+
+int num_sms() {
+  static int cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+}  // namespace gb300moe
+
+using namespace gb300moe;
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_problem_t* p) {
+  if (check_problem(p) != MOE_OK) return 0;
+  return make_layout(*p, 1).total;
+}
+
+size_t moe_stage_workspace_size(const moe_problem_t* p, int32_t block_m) {
+  if (check_problem(p) != MOE_OK || block_m <= 0 || block_m > 1024) return 0;
+  return make_layout(*p, block_m).total;
+}
+
+int64_t moe_sorted_capacity(const moe_problem_t* p, int32_t block_m) {
+  if (check_problem(p) != MOE_OK || block_m <= 0) return -1;
+  return (int64_t)p->T * p->top_k + (int64_t)p->E * (block_m - 1);
+}
+
+moe_status_t moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes < kHeaderBytes) return MOE_ERR_INVALID_ARG;
+  return from_cuda(cudaMemsetAsync(workspace, 0, kHeaderBytes, (cudaStream_t)stream));
+}
+
+moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
+                           const float* gating_output, const void* w_gate_up, const void* w_down,
+                           const float* correction_bias, const void* shared_w_gate_up,
+                           const void* shared_w_down, void* out, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  moe_status_t st = check_problem(p);
+  if (st != MOE_OK) return st;
+  if (!workspace) return MOE_ERR_INVALID_ARG;
+  if (p->T > 0 && (!hidden_states || !gating_output || !w_gate_up || !w_down || !out))
+    return MOE_ERR_INVALID_ARG;
+  if ((p->S > 0) != (shared_w_gate_up != nullptr) || (p->S > 0) != (shared_w_down != nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (correction_bias && p->scoring != MOE_SIGMOID) return MOE_ERR_UNSUPPORTED;
+  const Layout L = make_layout(*p, 1);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (p->T == 0) return MOE_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  void* ws = workspace;
+  int* status = status_word(ws);
+  int32_t* ids = at<int32_t>(ws, L.ids);
+  float* w = at<float>(ws, L.w);
+  const moe_problem_t& P = *p;
+
+  {
+    StageTimer t(kRoute, s);
+    MOE_TRY(launch_route(P, gating_output, correction_bias, ids, w, s));
+    t.done(1);
+  }
+
+  const void* y_rows = at<void>(ws, L.y);
+  const int32_t* inv = nullptr;
+  if (use_direct(P)) {
+    GemmCall g1 = base_call(P, status);
+    g1.gemm1 = 1;
+    g1.mode = kDirect;
+    g1.K = P.H;
+    g1.n_out = P.F;
+    g1.w = w_gate_up;
+    g1.b = hidden_states;
+    g1.b_rows = P.T;
+    g1.out = at<void>(ws, L.act);
+    g1.topk_ids = ids;
+    {
+      StageTimer t(kGemm1, s);
+      MOE_TRY(launch_gemm(g1, s));
+      t.done(1);
+    }
+    GemmCall g2 = base_call(P, status);
+    g2.gemm1 = 0;
+    g2.mode = kDirect;
+    g2.K = P.F;
+    g2.n_out = P.H;
+    g2.w = w_down;
+    g2.b = at<void>(ws, L.act);
+    g2.b_rows = L.P;
+    g2.out = at<void>(ws, L.y);
+    g2.topk_ids = ids;
+    g2.topk_w = w;
+    {
+      StageTimer t(kGemm2, s);
+      MOE_TRY(launch_gemm(g2, s));
+      t.done(1);
+    }
+  } else {
+    int32_t* counts = at<int32_t>(ws, L.counts);
+    int32_t* offsets = at<int32_t>(ws, L.offsets);
+    int32_t* sorted = at<int32_t>(ws, L.sorted);
+    int32_t* inv_route = at<int32_t>(ws, L.inv);
+    {
+      StageTimer t(kSort, s);
+      MOE_TRY(launch_align_sort(P, 1, ids, counts, offsets, sorted, L.cap, nullptr, inv_route,
+                                at<int32_t>(ws, L.chunk), status, s));
+      t.done(3);
+    }
+    Tile* tiles = at<Tile>(ws, L.tiles);
+    {
+      StageTimer t(kTiles, s);
+      MOE_TRY(launch_build_tiles(P.E, offsets, tiles, tile_counter(ws), s));
+      t.done(1);
+    }
+    {
+      StageTimer t(kPermute, s);
+      MOE_TRY(launch_permute(P.dtype, P.top_k, P.H, hidden_states, sorted, offsets, P.E, L.cap,
+                             at<void>(ws, L.a_sorted), s));
+      t.done(1);
+    }
+    GemmCall g1 = base_call(P, status);
+    g1.gemm1 = 1;
+    g1.mode = kSorted;
+    g1.K = P.H;
+    g1.n_out = P.F;
+    g1.w = w_gate_up;
+    g1.b = at<void>(ws, L.a_sorted);
+    g1.b_rows = L.cap;
+    g1.out = at<void>(ws, L.act);
+    g1.tiles = tiles;
+    g1.n_tiles = tile_counter(ws);
+    g1.max_tiles = (int)L.max_tiles;
+    {
+      StageTimer t(kGemm1, s);
+      MOE_TRY(launch_gemm(g1, s));
+      t.done(1);
+    }
+    GemmCall g2 = g1;
+    g2.gemm1 = 0;
+    g2.K = P.F;
+    g2.n_out = P.H;
+    g2.w = w_down;
+    g2.b = at<void>(ws, L.act);
+    g2.out = at<void>(ws, L.y);
+    g2.sorted_ids = sorted;
+    g2.topk_w = w;
+    {
+      StageTimer t(kGemm2, s);
+      MOE_TRY(launch_gemm(g2, s));
+      t.done(1);
+    }
+    inv = inv_route;
+  }
+  const void* sh_out = nullptr;
+  if (P.S > 0) {
+    MOE_TRY(run_shared(P, hidden_states, shared_w_gate_up, shared_w_down, at<void>(ws, L.sh_act),
+                       at<void>(ws, L.sh_out), status, s));
+    sh_out = at<void>(ws, L.sh_out);
+  }
+  {
+    StageTimer t(kCombine, s);
+    MOE_TRY(launch_combine(P, y_rows, inv, ids, sh_out, out, s));
+    t.done(1);
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_route(const moe_problem_t* p, const float* gating_output,
+                       const float* correction_bias, int32_t* topk_ids, float* topk_weights,
+                       void* stream) {
+  moe_status_t st = check_problem(p);
+  if (st != MOE_OK) return st;
+  if (p->T > 0 && (!gating_output || !topk_ids || !topk_weights)) return MOE_ERR_INVALID_ARG;
+  if (correction_bias && p->scoring != MOE_SIGMOID) return MOE_ERR_UNSUPPORTED;
+  return from_cuda(
+      launch_route(*p, gating_output, correction_bias, topk_ids, topk_weights, (cudaStream_t)stream));
+}
+
+moe_status_t moe_align_sort(const moe_problem_t* p, int32_t block_m, const int32_t* topk_ids,
+                            int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
+                            int32_t* tile_expert, int32_t* inv_route, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  moe_status_t st = check_problem(p);
+  if (st != MOE_OK) return st;
+  if (block_m <= 0 || block_m > 1024) return MOE_ERR_INVALID_ARG;
+  if (!counts || !offsets || !sorted_ids || !inv_route || !workspace) return MOE_ERR_INVALID_ARG;
+  if (p->T > 0 && !topk_ids) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(*p, 1);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const int64_t cap = moe_sorted_capacity(p, block_m);
+  return from_cuda(launch_align_sort(*p, block_m, topk_ids, counts, offsets, sorted_ids, cap,
+                                     tile_expert, inv_route, at<int32_t>(workspace, L.chunk),
+                                     status_word(workspace), (cudaStream_t)stream));
+}
+
+moe_status_t moe_gemm1_swiglu(const moe_problem_t* p, int32_t block_m, const void* hidden_states,
+                              const int32_t* sorted_ids, const int32_t* offsets,
+                              const void* w_gate_up, void* act, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  moe_status_t st = check_problem(p);
+  if (st != MOE_OK) return st;
+  if (block_m <= 0 || block_m > 1024) return MOE_ERR_INVALID_ARG;
+  if (!workspace || !sorted_ids || !offsets || !act) return MOE_ERR_INVALID_ARG;
+  if (p->T > 0 && (!hidden_states || !w_gate_up)) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(*p, block_m);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = (cudaStream_t)stream;
+  void* ws = workspace;
+  Tile* tiles = at<Tile>(ws, L.tiles);
+  MOE_TRY(launch_build_tiles(p->E, offsets, tiles, tile_counter(ws), s));
+  MOE_TRY(launch_permute(p->dtype, p->top_k, p->H, hidden_states, sorted_ids, offsets, p->E,
+                         L.cap, at<void>(ws, L.a_sorted), s));
+  GemmCall g1 = base_call(*p, status_word(ws));
+  g1.gemm1 = 1;
+  g1.mode = kSorted;
+  g1.K = p->H;
+  g1.n_out = p->F;
+  g1.w = w_gate_up;
+  g1.b = at<void>(ws, L.a_sorted);
+  g1.b_rows = L.cap;
+  g1.out = act;
+  g1.tiles = tiles;
+  g1.n_tiles = tile_counter(ws);
+  g1.max_tiles = (int)L.max_tiles;
+  return from_cuda(launch_gemm(g1, s));
+}
+
+moe_status_t moe_gemm2(const moe_problem_t* p, int32_t block_m, const void* act,
+                       const int32_t* sorted_ids, const int32_t* offsets,
+                       const float* topk_weights, const void* w_down, void* y_route,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  moe_status_t st = check_problem(p);
+  if (st != MOE_OK) return st;
+  if (block_m <= 0 || block_m > 1024) return MOE_ERR_INVALID_ARG;
+  if (!workspace || !sorted_ids || !offsets || !y_route) return MOE_ERR_INVALID_ARG;
+  if (p->T > 0 && (!act || !topk_weights || !w_down)) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(*p, block_m);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = (cudaStream_t)stream;
+  void* ws = workspace;
+  Tile* tiles = at<Tile>(ws, L.tiles);
+  MOE_TRY(launch_build_tiles(p->E, offsets, tiles, tile_counter(ws), s));
+  GemmCall g2 = base_call(*p, status_word(ws));
+  g2.gemm1 = 0;
+  g2.mode = kSorted;
+  g2.K = p->F;
+  g2.n_out = p->H;
+  g2.w = w_down;
+  g2.b = act;
+  g2.b_rows = L.cap;
+  g2.out = y_route;
+  g2.tiles = tiles;
+  g2.n_tiles = tile_counter(ws);
+  g2.max_tiles = (int)L.max_tiles;
+  g2.sorted_ids = sorted_ids;
+  g2.topk_w = topk_weights;
+  return from_cuda(launch_gemm(g2, s));
+}
+
+moe_status_t moe_combine(const moe_problem_t* p, const void* y_route, const int32_t* inv_route,
+                         const int32_t* topk_ids, const void* shared_out, void* out,
+                         void* stream) {
+  moe_status_t st = check_problem(p);
+  if (st != MOE_OK) return st;
+  if (p->T > 0 && (!y_route || !out)) return MOE_ERR_INVALID_ARG;
+  return from_cuda(
+      launch_combine(*p, y_route, inv_route, topk_ids, shared_out, out, (cudaStream_t)stream));
+}
+
+moe_status_t moe_shared_expert_fwd(const moe_problem_t* p, const void* hidden_states,
+                                   const void* shared_w_gate_up, const void* shared_w_down,
+                                   void* shared_out, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+  moe_status_t st = check_problem(p);
+  if (st != MOE_OK) return st;
+  if (p->S <= 0) return MOE_ERR_INVALID_ARG;
+  if (!workspace || (p->T > 0 && (!hidden_states || !shared_w_gate_up || !shared_w_down ||
+                                  !shared_out)))
+    return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(*p, 1);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (p->T == 0) return MOE_OK;
+  return from_cuda(run_shared(*p, hidden_states, shared_w_gate_up, shared_w_down,
+                              at<void>(workspace, L.sh_act), shared_out,
+                              status_word(workspace), (cudaStream_t)stream));
+}
+
+moe_status_t moe_get_device_status(void* workspace, void* stream) {
+  if (!workspace) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  return (moe_status_t)v;
+}
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported problem size or option";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA launch or API error";
+    case MOE_ERR_TIMEOUT: return "a bounded wait inside a kernel timed out";
+    case MOE_ERR_BAD_EXPERT_ID: return "expert id outside [-1, E)";
+  }
+  return "unknown status";
+}
+
+uint64_t moe_set_wait_limit_ns(uint64_t limit_ns) { return g_wait_limit_ns.exchange(limit_ns); }
+
+const char* moe_stage_name(int32_t stage) {
+  return stage >= 0 && stage < kNumStages ? kStageNames[stage] : nullptr;
+}
+
+moe_status_t moe_profile_enable(int32_t stage_mask) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  g_prof.mask = (uint32_t)stage_mask;
+  for (int i = 0; i < kNumStages; ++i) {
+    g_prof.used[i] = 0;
+    g_prof.launches[i] = 0;
+  }
+  return MOE_OK;
+}
+
+int32_t moe_profile_collect(double* total_ms, int64_t* calls, int64_t* launches,
+                            int32_t max_stages) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  const int n = max_stages < kNumStages ? max_stages : kNumStages;
+  for (int i = 0; i < n; ++i) {
+    double tot = 0.0;
+    for (size_t j = 0; j < g_prof.used[i]; ++j) {
+      float ms = 0.0f;
+      cudaEventSynchronize(g_prof.ev[i][2 * j + 1]);
+      if (cudaEventElapsedTime(&ms, g_prof.ev[i][2 * j], g_prof.ev[i][2 * j + 1]) == cudaSuccess)
+        tot += ms;
+    }
+    if (total_ms) total_ms[i] = tot;
+    if (calls) calls[i] = (int64_t)g_prof.used[i];
+    if (launches) launches[i] = g_prof.launches[i];
+  }
+  for (int i = 0; i < kNumStages; ++i) {
+    g_prof.used[i] = 0;
+    g_prof.launches[i] = 0;
+  }
+  return n;
+}
+
+}  // extern "C"

@@ -1,0 +1,104 @@
+// common.cuh -- shared definitions of the GB300 MoE kernels (status word, dtype traits, launch
+// prototypes).  Everything here is device-side product code; nothing is shared with the oracle.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace gb300moe {
+
+// Number of SMs on a GB300 (2 dies x 76); the launchers read the real count at run time and
+// use this only as an upper bound for static tables.
+constexpr int kMaxSMs = 256;
+
+// Token rows per GEMM tile (the N side of the tcgen05 MMA) and weight rows per slab (the M
+// side); K is staged 64 elements (128 bytes) at a time with the 128-byte swizzle.
+constexpr int kTileRows = 128;
+constexpr int kSlab = 128;
+constexpr int kBlockK = 64;
+
+// Workspace header: status word at offset 0, tile counter at offset 64.
+constexpr size_t kHeaderBytes = 256;
+
+// First error wins; later errors are dropped until the host reads and clears the word.
+__device__ __forceinline__ void set_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+template <typename T> struct DT;
+template <> struct DT<__nv_bfloat16> {
+  static constexpr int kIsBF16 = 1;
+  __device__ __forceinline__ static float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+  __device__ __forceinline__ static __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+};
+template <> struct DT<__half> {
+  static constexpr int kIsBF16 = 0;
+  __device__ __forceinline__ static float to_f(__half v) { return __half2float(v); }
+  __device__ __forceinline__ static __half from_f(float v) { return __float2half_rn(v); }
+};
+
+// A tile of the grouped GEMM schedule: expert, first row, number of rows (<= kTileRows).
+struct Tile {
+  int e, row0, nrows, pad;
+};
+
+// ---- launchers (defined in the .cu files, called by api.cu) ------------------------------
+cudaError_t launch_route(const moe_problem_t& p, const float* gating, const float* bias,
+                         int32_t* ids, float* w, cudaStream_t s);
+
+cudaError_t launch_align_sort(const moe_problem_t& p, int block_m, const int32_t* ids,
+                              int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
+                              int64_t cap, int32_t* tile_expert, int32_t* inv_route,
+                              int32_t* chunk_scratch, int* status, cudaStream_t s);
+
+cudaError_t launch_build_tiles(int E, const int32_t* offsets, Tile* tiles, int* n_tiles,
+                               cudaStream_t s);
+
+cudaError_t launch_permute(int dtype, int top_k, int H, const void* hidden,
+                           const int32_t* sorted_ids, const int32_t* offsets, int E, int64_t cap,
+                           void* a_sorted, cudaStream_t s);
+
+cudaError_t launch_combine(const moe_problem_t& p, const void* y_route,
+                           const int32_t* inv_route, const int32_t* ids, const void* shared_out,
+                           void* out, cudaStream_t s);
+
+// Grouped GEMM on tcgen05.  mode: 0 = sorted segments (tile list), 1 = direct from topk_ids
+// (T <= 8), 2 = dense rows (one expert, all rows: the shared expert).
+enum GemmMode { kSorted = 0, kDirect = 1, kDense = 2 };
+
+struct GemmCall {
+  int gemm1;      // 1: gate/up + SiLU*up; 0: down projection with route weight
+  int mode;       // GemmMode
+  int dtype;      // moe_dtype_t
+  int K;          // reduction length (H for gemm1, F for gemm2)
+  int n_out;      // output columns (F for gemm1, H for gemm2)
+  int E;          // experts (1 for dense)
+  const void* w;  // weights: gemm1 [E, 2*n_out, K]; gemm2 [E, n_out, K]
+  const void* b;  // token rows [b_rows, K]
+  int64_t b_rows; // rows of b (tensor extent)
+  void* out;      // [*, n_out]
+  // sorted mode
+  const Tile* tiles;
+  const int* n_tiles;
+  int max_tiles;  // upper bound of *n_tiles (grid sizing)
+  const int32_t* sorted_ids;  // gemm2 scale lookup
+  // direct mode
+  const int32_t* topk_ids;
+  int P, top_k, T;
+  // dense mode
+  int dense_rows;
+  // gemm2 route weights
+  const float* topk_w;
+  int* status;
+};
+
+cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s);
+
+uint64_t wait_limit_ns();
+int num_sms();
+
+}  // namespace gb300moe

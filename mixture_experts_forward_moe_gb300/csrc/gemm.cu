@@ -1,0 +1,458 @@
+// gemm.cu -- grouped expert GEMMs on the sm_103a tensor cores (tcgen05 + TMA + TMEM).
+//
+// TileOPs "MoE" page, op MoEGroupedGemmFwd (contiguous layout; activation=silu_and_mul for the
+// gate/up projection) and op SharedExpertMLPFwd.  The design is GB300-first:
+//
+//  * Weight-stationary orientation ("swap AB").  Every config on the pages streams far more
+//    weight bytes than activation bytes, so the 128-row MMA side (M) is a slab of 128 weight
+//    rows and the N side is the expert's token rows (16..128, a multiple of 16).  Each unit of
+//    work reads its weight slab from HBM exactly once along K, whatever the number of tokens.
+//  * gemm1: the slab is 128 gate rows [f0, f0+128) and the matching 128 up rows [F+f0, ...),
+//    two MMAs per K step into two TMEM accumulators, so epilogue thread i holds gate row i and
+//    up row i and computes SiLU(g)*u in f32 with no data exchange.
+//  * gemm2: the slab is 128 rows of w_down; the epilogue multiplies by the route weight.
+//  * Warp roles (192 threads, one CTA per SM, persistent over units):
+//      warp 0  TMA producer: weight boxes {64 x 128} and token boxes {64 x 16}, 128-byte
+//              swizzle, into a multi-stage shared-memory ring (mbarrier complete_tx);
+//      warp 1  MMA issuer: tcgen05.mma kind::f16, f32 accumulators in TMEM, double-buffered
+//              so the epilogue of one unit overlaps the K loop of the next;
+//      warps 2-5  epilogue: tcgen05.ld -> f32 math -> one rounding to bf16/f16 -> transposed
+//              into shared memory -> 16-byte stores of whole output rows.
+//  * Cluster size 1 and no multicast: each CTA fetches its own tiles.
+//  * Every wait is bounded (global timer); on expiry the kernel records MOE_ERR_TIMEOUT, the
+//    roles stop, in-flight copies and MMAs are drained, TMEM is freed and the kernel returns.
+//
+// Modes (how a unit index maps to an expert, token rows and output rows):
+//   sorted  units = tiles x slabs; tile = (expert, first row, rows) over the expert-contiguous
+//           rows produced by the sort; output row = input row.
+//   direct  units = routes x slabs for T <= 8 (aiter PR #5973 "Changes": direct decoding runs
+//           straight from topk_ids without sorting); a unit is owned by the first route of its
+//           expert; the token side is every token (gemm1) or every route row (gemm2), and the
+//           epilogue writes the rows of the routes that chose the expert.
+//   dense   one expert over all rows in order (the shared expert).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace gb300moe {
+
+namespace {
+
+template <bool kGemm1>
+struct Cfg {
+  static constexpr int kStages = kGemm1 ? 4 : 6;
+  static constexpr int kABytes = (kGemm1 ? 2 : 1) * kSlab * kBlockK * 2;
+  static constexpr int kBBytes = kTileRows * kBlockK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStagingBytes = kTileRows * kSlab * 2;
+  static constexpr int kAccCols = kGemm1 ? 2 * kSlab : kSlab;  // per accumulator buffer
+  static constexpr int kTmemCols = 2 * kAccCols;                // double-buffered
+  static constexpr int kSmemBytes = kStages * kStageBytes + kStagingBytes + 1024;
+};
+
+struct KParams {
+  int mode;
+  int K, n_out, E, n_slabs, num_kb, w_rows_per_expert;
+  const Tile* tiles;
+  const int* n_tiles;
+  const int32_t* sorted_ids;
+  const int32_t* topk_ids;
+  const float* topk_w;
+  int P, top_k, T, dense_rows;
+  void* out;
+  int* status;
+  uint64_t limit_ns;
+};
+
+struct Unit {
+  int e, row0, nrows, n_mma, slab;
+};
+
+__device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
+
+template <bool kGemm1>
+__device__ __forceinline__ bool decode_unit(const KParams& p, int u, Unit& U) {
+  U.slab = u % p.n_slabs;
+  const int q = u / p.n_slabs;
+  if (p.mode == kSorted) {
+    const Tile t = p.tiles[q];
+    U.e = t.e;
+    U.row0 = t.row0;
+    U.nrows = t.nrows;
+  } else if (p.mode == kDense) {
+    U.e = 0;
+    U.row0 = q * kTileRows;
+    U.nrows = min(kTileRows, p.dense_rows - U.row0);
+  } else {
+    const int e = p.topk_ids[q];
+    if (e < 0 || e >= p.E) {
+      if (e != -1) set_status(p.status, MOE_ERR_BAD_EXPERT_ID);
+      return false;
+    }
+    for (int r = 0; r < q; ++r)
+      if (p.topk_ids[r] == e) return false;  // owned by an earlier route
+    U.e = e;
+    U.row0 = 0;
+    U.nrows = kGemm1 ? p.T : p.P;
+  }
+  U.n_mma = round16(U.nrows);
+  return U.nrows > 0;
+}
+
+// Plain bounded wait (ignores the abort flag and the wait-limit knob) used while draining the
+// copies and MMAs a CTA has in flight before it frees TMEM and exits; they finish in
+// microseconds, so one second is only a backstop.
+constexpr uint64_t kDrainLimitNs = 1000000000ull;
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kDrainLimitNs) return;
+  }
+}
+
+template <bool kGemm1, typename T>
+__global__ void __launch_bounds__(192, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
+                    const __grid_constant__ CUtensorMap tmB, const KParams p) {
+  using C = Cfg<kGemm1>;
+  extern __shared__ uint8_t dsmem[];
+  __shared__ __align__(8) uint64_t full_bar[C::kStages];
+  __shared__ __align__(8) uint64_t empty_bar[C::kStages];
+  __shared__ __align__(8) uint64_t tfull_bar[2];
+  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t s_tmem_base;
+  __shared__ int s_abort;
+  __shared__ int s_n_units;
+  __shared__ int ent_col[kTileRows];
+  __shared__ int ent_dst[kTileRows];
+  __shared__ float col_scale[kTileRows];
+
+  // 1024-byte alignment for the 128-byte swizzle atoms.
+  const uint32_t raw = smem_u32(dsmem);
+  uint8_t* smem = dsmem + ((1024u - (raw & 1023u)) & 1023u);
+  uint8_t* staging = smem + C::kStages * C::kStageBytes;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int* abort_flag = &s_abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], 128);
+    }
+    mbar_init(&drain_bar, 1);
+    s_abort = 0;
+    int n = 0;
+    if (p.mode == kSorted)
+      n = (*p.n_tiles) * p.n_slabs;
+    else if (p.mode == kDirect)
+      n = p.P * p.n_slabs;
+    else
+      n = ((p.dense_rows + kTileRows - 1) / kTileRows) * p.n_slabs;
+    s_n_units = n;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmW);
+    prefetch_tensormap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem_base;
+  const int n_units = s_n_units;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        Unit U;
+        if (!decode_unit<kGemm1>(p, u, U)) continue;
+        const uint32_t bytes = C::kABytes + U.n_mma * kBlockK * 2;
+        const int wrow = U.e * p.w_rows_per_expert + U.slab * kSlab;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.limit_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * C::kStageBytes;
+          uint8_t* sb = sa + C::kABytes;
+          mbar_arrive_expect_tx(&full_bar[stage], bytes);
+          const int kx = kb * kBlockK;
+          tma_load_2d(sa, &tmW, &full_bar[stage], kx, wrow);
+          if (kGemm1)
+            tma_load_2d(sa + kSlab * kBlockK * 2, &tmW, &full_bar[stage], kx, wrow + p.n_out);
+          for (int j = 0; j < U.n_mma / 16; ++j)
+            tma_load_2d(sb + j * 16 * kBlockK * 2, &tmB, &full_bar[stage], kx, U.row0 + 16 * j);
+          ++issued;
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (*abort_flag) {
+        // Let every copy still in flight land before the CTA goes away.
+        const int n = issued < C::kStages ? issued : C::kStages;
+        for (int i = issued - n; i < issued; ++i)
+          mbar_wait_drain(&full_bar[i % C::kStages], (uint32_t)((i / C::kStages) & 1));
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      bool issued_any = false;
+      const uint32_t smem_base = smem_u32(smem);
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        Unit U;
+        if (!decode_unit<kGemm1>(p, u, U)) continue;
+        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.limit_ns, p.status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * C::kAccCols);
+        const uint32_t idesc = idesc_f16_m128(U.n_mma, DT<T>::kIsBF16);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.limit_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_base + (uint32_t)(stage * C::kStageBytes);
+          const uint32_t sb = sa + C::kABytes;
+#pragma unroll
+          for (int k = 0; k < kBlockK / 16; ++k) {
+            const uint64_t bdesc = sw128_kmajor_desc(sb + k * 32);
+            const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+            umma_f16(d, sw128_kmajor_desc(sa + k * 32), bdesc, idesc, accum);
+            if (kGemm1)
+              umma_f16(d + kSlab, sw128_kmajor_desc(sa + kSlab * kBlockK * 2 + k * 32), bdesc,
+                       idesc, accum);
+          }
+          umma_commit(&empty_bar[stage]);
+          issued_any = true;
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull_bar[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // Every MMA issued by this thread has completed once drain_bar flips.
+      if (issued_any) {
+        umma_commit(&drain_bar);
+        mbar_wait_drain(&drain_bar, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue (128 thr)
+    const int q = warp & 3;  // the TMEM lane quarter this warp may read
+    const int row = q * 32 + lane;
+    const int et = threadIdx.x - 64;
+    T* out = static_cast<T*>(p.out);
+    T* stg = reinterpret_cast<T*>(staging);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      Unit U;
+      if (!decode_unit<kGemm1>(p, u, U)) continue;
+      // Output rows of this unit: (accumulator column, destination row).
+      int n_ent;
+      if (p.mode == kDirect) {
+        n_ent = p.P;
+        if (et < p.P) {
+          const bool mine = p.topk_ids[et] == U.e;
+          ent_col[et] = mine ? (kGemm1 ? et / p.top_k : et) : -1;
+          ent_dst[et] = et;
+        }
+      } else {
+        n_ent = U.nrows;
+        if (et < U.nrows) {
+          ent_col[et] = et;
+          ent_dst[et] = U.row0 + et;
+        }
+      }
+      if (!kGemm1 && et < U.n_mma) {
+        float sc = 0.0f;
+        if (p.mode == kSorted) {
+          if (et < U.nrows) {
+            const int sid = p.sorted_ids[U.row0 + et];
+            sc = sid >= 0 ? p.topk_w[sid] : 0.0f;
+          }
+        } else if (p.mode == kDirect) {
+          sc = et < p.P ? p.topk_w[et] : 0.0f;
+        } else {
+          sc = 1.0f;
+        }
+        col_scale[et] = sc;
+      }
+      const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.limit_ns, p.status);
+      if (!named_bar_and(1, 128, got)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
+      for (int c0 = 0; c0 < U.n_mma; c0 += 16) {
+        float g[16];
+        if (kGemm1) {
+          float v[16];
+          tmem_ld2_x16(tb + c0, tb + kSlab + c0, g, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float h = __fdividef(g[j], 1.0f + __expf(-g[j])) * v[j];
+            stg[(c0 + j) * kSlab + row] = DT<T>::from_f(h);
+          }
+        } else {
+          tmem_ld_x16(tb + c0, g);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) stg[(c0 + j) * kSlab + row] = DT<T>::from_f(g[j] * col_scale[c0 + j]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty_bar[acc]);
+      named_bar_sync(1, 128);
+      // 16-byte stores of whole output rows: entry en, chunk ch of 8 columns.
+      const int width = min(kSlab, p.n_out - U.slab * kSlab);
+      const int nch = width / 8;
+      for (int idx = et; idx < n_ent * 16; idx += 128) {
+        const int en = idx >> 4, ch = idx & 15;
+        if (ch >= nch) continue;
+        const int col = ent_col[en];
+        if (col < 0) continue;
+        const uint4 v = *reinterpret_cast<const uint4*>(stg + col * kSlab + ch * 8);
+        *reinterpret_cast<uint4*>(out + (int64_t)ent_dst[en] * p.n_out + U.slab * kSlab + ch * 8) = v;
+      }
+      named_bar_sync(1, 128);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ---- host side -----------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// 2-D map over a row-major [rows, inner] 16-bit tensor, box {64, box_rows}, 128-byte swizzle,
+// zero fill outside the tensor.
+bool make_map(CUtensorMap* m, int dtype, const void* base, uint64_t inner, uint64_t rows,
+              uint32_t box_rows) {
+  if (!get_encode()) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBlockK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m,
+                        dtype == MOE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool kGemm1, typename T>
+cudaError_t launch_typed(const GemmCall& c, const KParams& kp, int grid, cudaStream_t s) {
+  CUtensorMap tmW, tmB;
+  const uint64_t w_rows = (uint64_t)c.E * (uint64_t)kp.w_rows_per_expert;
+  if (!make_map(&tmW, c.dtype, c.w, (uint64_t)c.K, w_rows, kSlab)) return cudaErrorInvalidValue;
+  if (!make_map(&tmB, c.dtype, c.b, (uint64_t)c.K, (uint64_t)c.b_rows, 16))
+    return cudaErrorInvalidValue;
+  auto kern = moe_gemm_kernel<kGemm1, T>;
+  static bool attr_set = false;  // one instantiation per (kGemm1, T): set once per process
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<kGemm1>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kern<<<grid, 192, Cfg<kGemm1>::kSmemBytes, s>>>(tmW, tmB, kp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s) {
+  KParams kp;
+  kp.mode = c.mode;
+  kp.K = c.K;
+  kp.n_out = c.n_out;
+  kp.E = c.E;
+  kp.n_slabs = (c.n_out + kSlab - 1) / kSlab;
+  kp.num_kb = (c.K + kBlockK - 1) / kBlockK;
+  kp.w_rows_per_expert = c.gemm1 ? 2 * c.n_out : c.n_out;
+  kp.tiles = c.tiles;
+  kp.n_tiles = c.n_tiles;
+  kp.sorted_ids = c.sorted_ids;
+  kp.topk_ids = c.topk_ids;
+  kp.topk_w = c.topk_w;
+  kp.P = c.P;
+  kp.top_k = c.top_k;
+  kp.T = c.T;
+  kp.dense_rows = c.dense_rows;
+  kp.out = c.out;
+  kp.status = c.status;
+  kp.limit_ns = wait_limit_ns();
+
+  long long upper = 0;
+  if (c.mode == kSorted)
+    upper = (long long)c.max_tiles * kp.n_slabs;
+  else if (c.mode == kDirect)
+    upper = (long long)c.P * kp.n_slabs;
+  else
+    upper = (long long)((c.dense_rows + kTileRows - 1) / kTileRows) * kp.n_slabs;
+  if (upper <= 0 || c.b_rows <= 0) return cudaSuccess;
+  const int sms = num_sms();
+  const int grid = (int)(upper < sms ? upper : sms);
+
+  if (c.gemm1) {
+    return c.dtype == MOE_BF16 ? launch_typed<true, __nv_bfloat16>(c, kp, grid, s)
+                               : launch_typed<true, __half>(c, kp, grid, s);
+  }
+  return c.dtype == MOE_BF16 ? launch_typed<false, __nv_bfloat16>(c, kp, grid, s)
+                             : launch_typed<false, __half>(c, kp, grid, s);
+}
+
+}  // namespace gb300moe

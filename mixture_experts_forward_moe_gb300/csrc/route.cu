@@ -1,0 +1,222 @@
+// route.cu -- router top-k (TileOPs "MoE" page, op FusedTopKFwd and the routing of FusedMoEFwd):
+// one warp per token, expert e held by lane e % 32, selection by warp-wide argmax with shuffles.
+#include <limits.h>
+#include <math.h>
+
+#include "common.cuh"
+
+namespace gb300moe {
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kWarpsPerBlock = 8;
+
+// f32 sigmoid used as the selection key for scoring_func=sigmoid.  It is a fixed sequence of
+// correctly rounded f32 operations, so the same logit always gives the same key:
+//   exp(z): n = rint(z*log2 e); r = z - n*ln2 (ln2 as a 16-bit head, exact when multiplied by
+//   n, plus an f32 tail) by two fused multiply-adds; e^r by the degree-7 Taylor polynomial
+//   (coefficients 1/k!) in Horner form with fused multiply-adds; times 2^n built from bits.
+//   sigmoid(x) = 1 / (1 + exp(-x)), with -x clamped to [-80, 80] so 2^n stays normal.
+// The polynomial remainder is below 1e-8 relative on |r| <= ln2/2.
+__device__ __forceinline__ float key_exp_f32(float z) {
+  const float n = rintf(__fmul_rn(z, 0x1.715476p+0f));
+  float r = __fmaf_rn(-n, 0x1.62e4p-1f, z);
+  r = __fmaf_rn(-n, 0x1.7f7d1cp-20f, r);
+  float q = 0x1.a01a02p-13f;        // 1/7!
+  q = __fmaf_rn(q, r, 0x1.6c16c2p-10f);  // 1/6!
+  q = __fmaf_rn(q, r, 0x1.111112p-7f);   // 1/5!
+  q = __fmaf_rn(q, r, 0x1.555556p-5f);   // 1/4!
+  q = __fmaf_rn(q, r, 0x1.555556p-3f);   // 1/3!
+  q = __fmaf_rn(q, r, 0x1p-1f);          // 1/2!
+  q = __fmaf_rn(q, r, 1.0f);
+  q = __fmaf_rn(q, r, 1.0f);
+  const int ni = static_cast<int>(n);
+  return __fmul_rn(q, __int_as_float((ni + 127) << 23));
+}
+
+__device__ __forceinline__ float key_sigmoid_f32(float x) {
+  const float z = fminf(fmaxf(-x, -80.0f), 80.0f);
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, key_exp_f32(z)));
+}
+
+// (ka, ea) ranks before (kb, eb): larger key, then lower expert id.
+__device__ __forceinline__ bool before(float ka, int ea, float kb, int eb) {
+  return ka > kb || (ka == kb && ea < eb);
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    route_kernel(int T, int E, int K, int scoring, int renorm, int G, int keepG, float rsf,
+                 const float* __restrict__ gating, const float* __restrict__ bias,
+                 int32_t* __restrict__ ids, float* __restrict__ wout) {
+  __shared__ float s_gscore[kWarpsPerBlock][32];
+  const int lane = threadIdx.x & 31;
+  const int wib = threadIdx.x >> 5;
+  const int t = blockIdx.x * kWarpsPerBlock + wib;
+  if (t >= T) return;
+  const float* x = gating + (size_t)t * E;
+
+  float key[VPL], sc[VPL];
+  bool live[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    live[i] = e < E;
+    const float v = live[i] ? x[e] : 0.0f;
+    if (scoring == MOE_SOFTMAX) {
+      sc[i] = v;
+      key[i] = v;
+    } else {
+      const float s = key_sigmoid_f32(v);
+      sc[i] = s;
+      key[i] = (bias != nullptr && live[i]) ? __fadd_rn(s, bias[e]) : s;
+    }
+    if (key[i] != key[i]) key[i] = -INFINITY;  // NaN ranks lowest
+  }
+
+  // Grouped selection: group g = experts [g*E/G, (g+1)*E/G); score = sum of its two largest
+  // keys; keep the keepG best groups (ties -> lower group id); exclude the rest.
+  if (G > 1 && keepG < G) {
+    const int gsz = E / G;
+    for (int g = 0; g < G; ++g) {
+      float m1 = -INFINITY, m2 = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && e / gsz == g) {
+          const float v = key[i];
+          if (v > m1) {
+            m2 = m1;
+            m1 = v;
+          } else if (v > m2) {
+            m2 = v;
+          }
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float o1 = __shfl_xor_sync(kFull, m1, off);
+        const float o2 = __shfl_xor_sync(kFull, m2, off);
+        const float hi = fmaxf(m1, o1);
+        const float lo = fmaxf(fminf(m1, o1), fmaxf(m2, o2));
+        m1 = hi;
+        m2 = lo;
+      }
+      if (lane == 0) s_gscore[wib][g] = __fadd_rn(m1, m2);
+    }
+    __syncwarp();
+    uint32_t kept = 0;
+    for (int j = 0; j < keepG; ++j) {
+      int bg = -1;
+      float bs = 0.0f;
+      for (int g = 0; g < G; ++g) {
+        if ((kept >> g) & 1u) continue;
+        const float v = s_gscore[wib][g];
+        if (bg < 0 || before(v, g, bs, bg)) {
+          bs = v;
+          bg = g;
+        }
+      }
+      kept |= 1u << bg;
+    }
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((kept >> (e / gsz)) & 1u)) live[i] = false;
+    }
+  }
+
+  // top_k rounds of warp argmax; lane j keeps the j-th selection.
+  int my_e = -1;
+  float my_v = 0.0f;
+  for (int j = 0; j < K; ++j) {
+    float bk = -INFINITY;
+    int be = INT_MAX;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      if (live[i] && (be == INT_MAX || before(key[i], e, bk, be))) {
+        bk = key[i];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ok = __shfl_xor_sync(kFull, bk, off);
+      const int oe = __shfl_xor_sync(kFull, be, off);
+      if (before(ok, oe, bk, be)) {
+        bk = ok;
+        be = oe;
+      }
+    }
+    float cand = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      if (lane + 32 * i == be) {
+        live[i] = false;
+        cand = sc[i];
+      }
+    }
+    const float v = __shfl_sync(kFull, cand, be & 31);
+    if (lane == j) {
+      my_e = be;
+      my_v = v;
+    }
+  }
+
+  // Weights.
+  float w = 0.0f;
+  if (scoring == MOE_SOFTMAX) {
+    const float m = __shfl_sync(kFull, my_v, 0);  // the first selection is the largest logit
+    float part = 0.0f;
+    if (renorm) {
+      if (lane < K) part = expf(my_v - m);
+    } else {
+#pragma unroll
+      for (int i = 0; i < VPL; ++i)
+        if (lane + 32 * i < E) part += expf(sc[i] - m);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFull, part, off);
+    w = expf(my_v - m) / part;
+  } else {
+    float part = lane < K ? my_v : 0.0f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFull, part, off);
+    w = renorm ? my_v / part : my_v;
+  }
+  if (lane < K) {
+    ids[(size_t)t * K + lane] = my_e;
+    wout[(size_t)t * K + lane] = w * rsf;
+  }
+}
+
+template <int VPL>
+cudaError_t launch_vpl(const moe_problem_t& p, const float* gating, const float* bias,
+                       int32_t* ids, float* w, cudaStream_t s) {
+  const int G = p.num_expert_group > 1 ? p.num_expert_group : 1;
+  const int keepG = G > 1 ? p.topk_group : 1;
+  const int blocks = (p.T + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  route_kernel<VPL><<<blocks, kWarpsPerBlock * 32, 0, s>>>(
+      p.T, p.E, p.top_k, p.scoring, p.renormalize, G, keepG, p.routed_scaling_factor, gating,
+      bias, ids, w);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_route(const moe_problem_t& p, const float* gating, const float* bias,
+                         int32_t* ids, float* w, cudaStream_t s) {
+  if (p.T == 0) return cudaSuccess;
+  const int need = (p.E + 31) / 32;
+  if (need <= 1) return launch_vpl<1>(p, gating, bias, ids, w, s);
+  if (need <= 2) return launch_vpl<2>(p, gating, bias, ids, w, s);
+  if (need <= 4) return launch_vpl<4>(p, gating, bias, ids, w, s);
+  if (need <= 8) return launch_vpl<8>(p, gating, bias, ids, w, s);
+  if (need <= 12) return launch_vpl<12>(p, gating, bias, ids, w, s);
+  if (need <= 16) return launch_vpl<16>(p, gating, bias, ids, w, s);
+  return launch_vpl<32>(p, gating, bias, ids, w, s);
+}
+
+}  // namespace gb300moe

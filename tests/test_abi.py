@@ -1,0 +1,110 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side argument checks
+(CPU only: none of these calls reaches the device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixture_experts_forward_moe_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for fn in sorted(os.listdir(inc)):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(inc, fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(\w+)\s*\(", text, flags=re.M):
+            if m.group(1) not in ("if", "while"):
+                names.append(m.group(1))
+    return names
+
+
+def test_header_declares_the_binding_names():
+    assert sorted(_declared_functions()) == sorted(B.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(B.library_path() if os.path.exists(B.library_path()) else B.lib()._name)
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def _prob(**kw):
+    base = dict(T=32, H=256, E=16, F=128, top_k=4)
+    base.update(kw)
+    return B.make_problem(**base)
+
+
+def test_workspace_size_and_capacity():
+    L = B.lib()
+    p = _prob()
+    n = L.moe_workspace_size(ctypes.byref(p))
+    assert n > 0 and n % 256 == 0
+    assert L.moe_sorted_capacity(ctypes.byref(p), 1) == 32 * 4
+    assert L.moe_sorted_capacity(ctypes.byref(p), 16) == 32 * 4 + 16 * 15
+    assert L.moe_stage_workspace_size(ctypes.byref(p), 16) > n
+    assert L.moe_stage_workspace_size(ctypes.byref(p), 1) == n
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=-1), B.MOE_ERR_INVALID_ARG),
+    (dict(top_k=17), B.MOE_ERR_INVALID_ARG),          # top_k > E
+    (dict(H=100), B.MOE_ERR_UNSUPPORTED),             # not a multiple of 8
+    (dict(F=36), B.MOE_ERR_UNSUPPORTED),
+    (dict(E=2048, top_k=4), B.MOE_ERR_UNSUPPORTED),   # E > 1024
+    (dict(num_expert_group=3, topk_group=1, scoring_func="sigmoid"), B.MOE_ERR_INVALID_ARG),
+    (dict(num_expert_group=4, topk_group=0, scoring_func="sigmoid"), B.MOE_ERR_INVALID_ARG),
+    (dict(num_expert_group=8, topk_group=1, scoring_func="sigmoid", top_k=4),
+     B.MOE_ERR_INVALID_ARG),                           # 1 group of 2 experts < top_k
+    (dict(num_expert_group=4, topk_group=2, scoring_func="softmax"), B.MOE_ERR_UNSUPPORTED),
+])
+def test_invalid_problems_rejected_before_launch(kw, code):
+    L = B.lib()
+    p = _prob(**kw)
+    assert L.moe_workspace_size(ctypes.byref(p)) == 0
+    dummy = ctypes.c_void_p(16)
+    rc = L.fused_moe_fwd(ctypes.byref(p), dummy, dummy, dummy, dummy, None, None, None, dummy,
+                         dummy, 1 << 40, None)
+    assert rc == code
+
+
+def test_null_pointers_and_short_workspace_rejected():
+    L = B.lib()
+    p = _prob()
+    d = ctypes.c_void_p(16)
+    need = L.moe_workspace_size(ctypes.byref(p))
+    assert L.fused_moe_fwd(ctypes.byref(p), None, d, d, d, None, None, None, d, d, need,
+                           None) == B.MOE_ERR_INVALID_ARG
+    assert L.fused_moe_fwd(ctypes.byref(p), d, d, d, d, None, None, None, d, None, need,
+                           None) == B.MOE_ERR_INVALID_ARG
+    assert L.fused_moe_fwd(ctypes.byref(p), d, d, d, d, None, None, None, d, d, need - 1,
+                           None) == B.MOE_ERR_WORKSPACE_TOO_SMALL
+    # shared weights must come as a pair and agree with S
+    assert L.fused_moe_fwd(ctypes.byref(p), d, d, d, d, None, d, None, d, d, need,
+                           None) == B.MOE_ERR_INVALID_ARG
+    # correction bias only with sigmoid scoring
+    assert L.fused_moe_fwd(ctypes.byref(p), d, d, d, d, d, None, None, d, d, need,
+                           None) == B.MOE_ERR_UNSUPPORTED
+    assert L.moe_align_sort(ctypes.byref(p), 0, d, d, d, d, None, d, d, need,
+                            None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_gemm1_swiglu(ctypes.byref(p), 1, d, d, d, d, d, d, 8, None) == \
+        B.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert L.moe_shared_expert_fwd(ctypes.byref(p), d, d, d, d, d, need, None) == \
+        B.MOE_ERR_INVALID_ARG  # S == 0
+
+
+def test_status_strings():
+    for code in range(7):
+        assert B.status_string(code)
+    assert B.status_string(99) == "unknown status"
+
+
+def test_wait_limit_knob_round_trips():
+    old = B.set_wait_limit_ns(12345)
+    assert B.set_wait_limit_ns(old) == 12345

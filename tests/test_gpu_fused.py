@@ -1,0 +1,138 @@
+"""fused_moe_fwd on the GPU vs the fp64 oracle, end to end.
+
+Small cases cover every routing mode, both dtypes, the direct (T <= 8) and sorted paths, the
+shared expert, ragged sizes and several tiles per expert; every output element is compared.
+The five workloads the project is measured on run at full size: routing is compared bit-exact
+on every token and the output on a sample of tokens (the oracle computes them one by one)."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import assert_rms_close, oracle_fused, oracle_route, run_fused, run_route
+from mixture_experts_forward_moe_gb300 import binding as B
+from mixture_experts_forward_moe_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+W = inputs.Workload
+SMALL = [
+    W("direct-t1", T=1, H=256, E=16, F=128, top_k=4),
+    W("direct-t3-f16", T=3, H=192, E=8, F=72, top_k=2, dtype=torch.float16),
+    W("direct-t8-k8", T=8, H=320, E=64, F=192, top_k=8),
+    W("direct-t8-sigmoid-shared", T=8, H=256, E=32, F=128, top_k=4, scoring_func="sigmoid",
+      bias_std=0.1, routed_scaling_factor=2.5, S=256),
+    W("sorted-t9", T=9, H=256, E=16, F=128, top_k=4),
+    W("sorted-t37-ragged", T=37, H=328, E=12, F=200, top_k=3),
+    W("sorted-t300-multitile", T=300, H=256, E=4, F=128, top_k=2),
+    W("sorted-t200-f16", T=200, H=192, E=16, F=256, top_k=4, dtype=torch.float16),
+    W("sorted-grouped", T=160, H=256, E=64, F=128, top_k=6, scoring_func="sigmoid",
+      bias_std=0.1, num_expert_group=8, topk_group=3, routed_scaling_factor=2.5),
+    W("sorted-sigmoid-shared", T=96, H=256, E=24, F=96, top_k=4, scoring_func="sigmoid",
+      bias_std=0.1, routed_scaling_factor=2.827, S=384),
+    W("sorted-norenorm", T=50, H=128, E=10, F=64, top_k=3, renormalize=False),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_fused_small_matches_oracle(w, cuda_device):
+    d = inputs.generate(w, seed=1, device=cuda_device)
+    out = run_fused(w, d)
+    ids, _ = run_route(w, d)
+    torch.cuda.synchronize()
+    ref, r_ids, _, _ = oracle_fused(w, d)
+    assert np.array_equal(ids.cpu().numpy(), r_ids)
+    assert_rms_close(out, ref, what=w.name)
+    assert B.get_device_status(B._workspace(0, cuda_device)) == B.MOE_OK
+
+
+@pytest.mark.parametrize("w", [SMALL[2], SMALL[6], SMALL[9]], ids=lambda w: w.name)
+def test_fused_is_deterministic_and_graph_replayable(w, cuda_device):
+    d = inputs.generate(w, seed=2, device=cuda_device)
+    prob = B.make_problem(w.T, w.H, w.E, w.F, w.top_k, w.dtype, w.scoring_func, w.renormalize,
+                          w.num_expert_group, w.topk_group, w.routed_scaling_factor, w.S)
+    ws = B.new_workspace(B.workspace_size(prob), cuda_device)
+    a = run_fused(w, d, workspace=ws).clone()
+    b = run_fused(w, d, workspace=ws).clone()
+    assert torch.equal(a, b)
+    out = torch.empty_like(a)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run_fused(w, d, workspace=ws, out=out)  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run_fused(w, d, workspace=ws, out=out)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, a)
+
+
+@pytest.mark.parametrize("w", [SMALL[2], SMALL[5], SMALL[9]], ids=lambda w: w.name)
+def test_fused_ignores_poisoned_workspace(w, cuda_device):
+    """Every workspace byte past the status header starts as 0xFF (NaN for bf16/f16 and -1 for
+    ints): nothing may read scratch it did not write."""
+    d = inputs.generate(w, seed=3, device=cuda_device)
+    prob = B.make_problem(w.T, w.H, w.E, w.F, w.top_k, w.dtype, w.scoring_func, w.renormalize,
+                          w.num_expert_group, w.topk_group, w.routed_scaling_factor, w.S)
+    clean = B.new_workspace(B.workspace_size(prob), cuda_device)
+    ref = run_fused(w, d, workspace=clean).clone()
+    poison = B.new_workspace(B.workspace_size(prob), cuda_device)
+    poison[256:] = 0xFF
+    out = torch.full_like(ref, float("nan"))
+    run_fused(w, d, workspace=poison, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    assert B.get_device_status(poison) == B.MOE_OK
+
+
+def test_fused_empty_batch(cuda_device):
+    w = W("empty", T=0, H=128, E=8, F=64, top_k=2)
+    d = inputs.generate(w, seed=0, device=cuda_device)
+    out = run_fused(w, d)
+    assert out.shape == (0, 128)
+
+
+# ---------------------------------------------------------------- full-size measured workloads
+FULL = [
+    ("tiny-softmax", None),
+    ("qwen3-30b-a3b-decode-t32", None),
+    ("qwen3-235b-a22b-decode-t512", 24),
+    ("deepseek-v3-grouped-prefill-t4096", 8),
+    ("kimi-k2-shared-t512", 8),
+]
+
+
+@pytest.mark.parametrize("name,n_sample", FULL, ids=[f[0] for f in FULL])
+def test_fused_full_size_workloads(name, n_sample, cuda_device):
+    w = inputs.WORKLOADS[name]
+    _full_size_check(w, n_sample, cuda_device)
+
+
+def test_fused_full_size_qwen3_235b_f16(cuda_device):
+    w = inputs.WORKLOADS["qwen3-235b-a22b-decode-t512"].with_(dtype=torch.float16)
+    _full_size_check(w, 16, cuda_device)
+
+
+def _full_size_check(w, n_sample, dev):
+    d = inputs.generate(w, seed=0, device=dev)
+    out = run_fused(w, d)
+    ids, wts = run_route(w, d)
+    torch.cuda.synchronize()
+    routed = oracle_route(w, d)
+    assert np.array_equal(ids.cpu().numpy(), routed[0]), "routing ids differ"
+    np.testing.assert_allclose(wts.cpu().numpy(), routed[1], rtol=2e-6, atol=1e-7)
+    if n_sample is None:
+        tokens = np.arange(w.T)
+    else:  # first, last and evenly spread tokens
+        tokens = np.unique(np.linspace(0, w.T - 1, n_sample).astype(np.int32))
+    ref, _, _, _ = oracle_fused(w, d, tokens=tokens, routed=routed)
+    assert_rms_close(out[torch.from_numpy(tokens).to(dev).long()], ref, what=w.name)
+    out2 = run_fused(w, d)
+    assert torch.equal(out, out2), "repeat call not bit-identical"
+    assert B.get_device_status(B._workspace(0, dev)) == B.MOE_OK
+    del d
+    torch.cuda.empty_cache()

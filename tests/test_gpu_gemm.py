@@ -1,0 +1,103 @@
+"""Grouped GEMMs, combine and shared expert on the GPU (staged C-ABI calls) vs the oracle.
+
+Shapes are small enough for the oracle to finish in seconds but span several K blocks, a
+ragged K tail, a ragged weight slab (F, H not multiples of 128), experts with more than one
+128-row tile, empty experts and padding rows."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import assert_rms_close, dt_code
+from mixture_experts_forward_moe_gb300 import binding as B
+from mixture_experts_forward_moe_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+# (T, k, E, H, F, block_m, pad_frac, dtype)
+GEMM_CASES = [
+    (150, 4, 6, 320, 192, 1, 0.0, torch.bfloat16),     # ~100 rows/expert, ragged K and slab
+    (300, 2, 3, 256, 128, 1, 0.0, torch.bfloat16),     # 200 rows/expert: two tiles each
+    (64, 8, 32, 192, 256, 16, 0.1, torch.bfloat16),    # padded segments, padding routes
+    (40, 4, 12, 136, 72, 1, 0.0, torch.float16),       # K tail of 8, F < 128
+    (9, 8, 64, 512, 96, 1, 0.0, torch.bfloat16),       # decode-like: 1-2 rows per expert
+]
+
+
+def _expert_of_rows(sorted_ids, offsets, E):
+    eo = np.full(sorted_ids.size, -1, np.int32)
+    for e in range(E):
+        seg = slice(offsets[e], offsets[e + 1])
+        eo[seg] = np.where(sorted_ids[seg] >= 0, e, -1)
+    return eo
+
+
+@pytest.mark.parametrize("T,k,E,H,F,block_m,pad,dtype", GEMM_CASES)
+def test_gemm1_and_gemm2_match_oracle(T, k, E, H, F, block_m, pad, dtype, cuda_device):
+    w = inputs.Workload("g", T=T, H=H, E=E, F=F, top_k=k, dtype=dtype)
+    d = inputs.generate(w, seed=T + E, device=cuda_device)
+    ids = inputs.random_ids(T, k, E, seed=T * 7 + E, pad_frac=pad)
+    srt = oracle.align_sort(ids.numpy(), E, block_m)
+    sorted_ids = torch.from_numpy(srt["sorted_ids"]).to(cuda_device)
+    offsets = torch.from_numpy(srt["offsets"]).to(cuda_device)
+    act = B.moe_gemm1_swiglu(d["hidden_states"], sorted_ids, offsets, d["w_gate_up"], k, block_m)
+    torch.cuda.synchronize()
+    # oracle act, row by row in sorted order
+    eo = _expert_of_rows(srt["sorted_ids"], srt["offsets"], E)
+    rows = srt["offsets"][E]
+    x_rows = torch.zeros((rows, H), dtype=dtype)
+    hid = d["hidden_states"].cpu()
+    sid = srt["sorted_ids"][:rows]
+    live = sid >= 0
+    x_rows[torch.from_numpy(np.nonzero(live)[0])] = hid[torch.from_numpy(sid[live] // k)]
+    ref_act = oracle.expert_act(x_rows, eo[:rows], d["w_gate_up"].cpu(), dt_code(dtype))
+    assert_rms_close(act[:rows], ref_act, what="act")
+    assert torch.all(act[:rows][torch.from_numpy(~live).to(cuda_device)] == 0)
+
+    # gemm2 on a seeded act (not the GPU's), with route weights
+    a_in = inputs.random_rows(act.shape[0], F, seed=3, dtype=dtype, std=0.5).to(cuda_device)
+    tw = inputs.random_weights(T * k, seed=4).to(cuda_device)
+    y = B.moe_gemm2(a_in, sorted_ids, offsets, tw, d["w_down"], T, k, block_m)
+    torch.cuda.synchronize()
+    scale = np.where(live, tw.cpu().numpy()[np.maximum(sid, 0)], 0.0)
+    ref_y = oracle.expert_down(a_in[:rows].cpu(), eo[:rows], scale, d["w_down"].cpu(),
+                               dt_code(dtype))
+    assert_rms_close(y[:rows], ref_y, what="y_route")
+    assert torch.all(y[:rows][torch.from_numpy(~live).to(cuda_device)] == 0)
+    ws = B._workspace(0, cuda_device)
+    assert B.get_device_status(ws) == B.MOE_OK
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_combine_matches_oracle(dtype, cuda_device):
+    T, k, E, H = 70, 4, 9, 264
+    ids = inputs.random_ids(T, k, E, seed=2, pad_frac=0.1)
+    srt = oracle.align_sort(ids.numpy(), E, 4)
+    cap = srt["sorted_ids"].size
+    y = inputs.random_rows(cap, H, seed=5, dtype=dtype).to(cuda_device)
+    sh = inputs.random_rows(T, H, seed=6, dtype=dtype).to(cuda_device)
+    inv = torch.from_numpy(srt["inv_route"]).to(cuda_device)
+    out = B.moe_combine(y, inv, T, k, topk_ids=ids.to(cuda_device), shared_out=sh)
+    ref = oracle.combine(y.cpu(), srt["inv_route"], k, dt_code(dtype), shared=sh.cpu())
+    # one rounding of an f32 sum: half an ulp of the 16-bit type, plus f32 summation error
+    eps = 2.0 ** -8 if dtype == torch.bfloat16 else 2.0 ** -11
+    got = out.double().cpu().numpy()
+    assert np.all(np.abs(got - ref) <= eps * np.abs(ref) + 1e-6 * np.abs(ref).max())
+    out2 = B.moe_combine(y, None, T, k, topk_ids=ids.to(cuda_device))  # identity map
+    ref2 = oracle.combine(y.cpu(), np.where(ids.numpy().reshape(-1) >= 0,
+                                            np.arange(T * k), -1).astype(np.int32), k,
+                          dt_code(dtype))
+    assert np.all(np.abs(out2.double().cpu().numpy() - ref2) <= eps * np.abs(ref2) + 1e-6)
+
+
+@pytest.mark.parametrize("T,H,S", [(1, 256, 128), (37, 192, 320), (300, 128, 136)])
+def test_shared_expert_matches_oracle(T, H, S, cuda_device):
+    w = inputs.Workload("s", T=T, H=H, E=2, F=16, top_k=1, S=S)
+    d = inputs.generate(w, seed=S, device=cuda_device)
+    out = B.moe_shared_expert_fwd(d["hidden_states"], d["shared_w_gate_up"], d["shared_w_down"])
+    torch.cuda.synchronize()
+    none = np.full((T, 1), -1, np.int32)
+    ref = oracle.moe_tokens(d["hidden_states"].cpu(), none, np.zeros((T, 1)), d["w_gate_up"].cpu(),
+                            d["w_down"].cpu(), 0, shared_w_gate_up=d["shared_w_gate_up"].cpu(),
+                            shared_w_down=d["shared_w_down"].cpu())
+    assert_rms_close(out, ref, what="shared")
