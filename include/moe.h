@@ -181,8 +181,9 @@ moe_status_t moe_gemm1_swiglu(const moe_problem_t* p, int32_t block_m, const voi
  * moe_gemm2 -- TileOPs "MoE" page, op MoEGroupedGemmFwd (down projection, contiguous layout),
  * with the route weight applied in the epilogue:
  *   y_route[p, h] = topk_weights[sorted_ids[p]] * sum_f Wd[e,h,f] act[p,f]   (0 for padding)
- *   block_m, sorted_ids, offsets: as for moe_gemm1_swiglu; act [cap,F];
- *   topk_weights [T*top_k] f32; w_down [E,H,F]; y_route [cap,H] out.
+ *   block_m, sorted_ids, offsets: as for moe_gemm1_swiglu; act [cap,F] dtype;
+ *   topk_weights [T*top_k] f32; w_down [E,H,F] dtype; y_route [cap,H] f32 out (kept in f32
+ *   so that the only rounding after the down projection is the combine's final one).
  */
 moe_status_t moe_gemm2(const moe_problem_t* p, int32_t block_m, const void* act,
                        const int32_t* sorted_ids,
@@ -193,11 +194,11 @@ moe_status_t moe_gemm2(const moe_problem_t* p, int32_t block_m, const void* act,
  * moe_combine -- TileOPs "MoE" page, op MoEPostPermuteFwd; aiter PR #5973 "Changes"
  * (sorted_sum writes the output in full, so no pre-clear is needed):
  *   out[t,:] = round( sum_{j=0..k-1} y_route[inv_route[t*k+j], :] (+ shared_out[t,:]) )
- * summed in f32 in fixed j order (deterministic: no atomics).  Routes with inv_route -1, or
- * with topk_ids -1 when topk_ids is given, are skipped.  inv_route NULL means the identity
- * (route r at row r).
- *   y_route [rows,H]; inv_route [T*k] or NULL; topk_ids [T*k] or NULL;
- *   shared_out [T,H] or NULL; out [T,H]
+ * summed in f32 in fixed j order, shared term last (deterministic: no atomics), rounded once
+ * to dtype.  Routes with inv_route -1, or with topk_ids -1 when topk_ids is given, are
+ * skipped.  inv_route NULL means the identity (route r at row r).
+ *   y_route [rows,H] f32; inv_route [T*k] or NULL; topk_ids [T*k] or NULL;
+ *   shared_out [T,H] f32 or NULL; out [T,H] dtype
  */
 moe_status_t moe_combine(const moe_problem_t* p, const void* y_route, const int32_t* inv_route,
                          const int32_t* topk_ids, const void* shared_out, void* out,
@@ -206,7 +207,8 @@ moe_status_t moe_combine(const moe_problem_t* p, const void* y_route, const int3
 /*
  * moe_shared_expert_fwd -- TileOPs "MoE" page, op SharedExpertMLPFwd: the dense SwiGLU MLP
  *   shared_out = shared_w_down . (SiLU(Wsg x) * (Wsu x)) for every token, no routing weight.
- *   hidden_states [T,H]; shared_w_gate_up [2S,H]; shared_w_down [H,S]; shared_out [T,H] out.
+ *   hidden_states [T,H]; shared_w_gate_up [2S,H]; shared_w_down [H,S];
+ *   shared_out [T,H] f32 out (the form moe_combine adds).
  */
 moe_status_t moe_shared_expert_fwd(const moe_problem_t* p, const void* hidden_states,
                                    const void* shared_w_gate_up, const void* shared_w_down,

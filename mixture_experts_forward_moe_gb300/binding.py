@@ -324,7 +324,8 @@ def moe_gemm1_swiglu(hidden_states, sorted_ids, offsets, w_gate_up, top_k, block
 
 def moe_gemm2(act, sorted_ids, offsets, topk_weights, w_down, T, top_k, block_m=1,
               workspace=None, stream=None):
-    """Grouped down GEMM x route weight (include/moe.h: moe_gemm2); returns y_route [cap, H]."""
+    """Grouped down GEMM x route weight (include/moe.h: moe_gemm2); returns f32 y_route
+    [cap, H]."""
     E, H, F = w_down.shape
     dt = w_down.dtype
     _need(w_down, "w_down", dt)
@@ -336,7 +337,7 @@ def moe_gemm2(act, sorted_ids, offsets, topk_weights, w_down, T, top_k, block_m=
     cap = sorted_capacity(prob, block_m)
     if act.shape[0] < cap or act.shape[1] != F:
         raise ValueError(f"act must have at least {cap} rows of {F} columns")
-    y = torch.empty((max(cap, 1), H), dtype=dt, device=w_down.device)
+    y = torch.empty((max(cap, 1), H), dtype=torch.float32, device=w_down.device)
     nbytes = stage_workspace_size(prob, block_m)
     if workspace is None:
         workspace = _workspace(nbytes, w_down.device)
@@ -347,20 +348,20 @@ def moe_gemm2(act, sorted_ids, offsets, topk_weights, w_down, T, top_k, block_m=
 
 
 def moe_combine(y_route, inv_route, T, top_k, topk_ids=None, shared_out=None, out=None,
-                stream=None):
-    """Deterministic top-k combine (include/moe.h: moe_combine); returns out [T, H]."""
-    _need(y_route, "y_route")
+                dtype=torch.bfloat16, stream=None):
+    """Deterministic top-k combine (include/moe.h: moe_combine) of f32 rows; returns out
+    [T, H] in `dtype`."""
+    _need(y_route, "y_route", torch.float32)
     H = y_route.shape[1]
-    dt = y_route.dtype
     if inv_route is not None:
         _need(inv_route, "inv_route", torch.int32)
     if topk_ids is not None:
         _need(topk_ids, "topk_ids", torch.int32)
     if shared_out is not None:
-        _need(shared_out, "shared_out", dt, (T, H))
-    prob = make_problem(T, H, max(top_k, 1), 8, top_k, dt)
+        _need(shared_out, "shared_out", torch.float32, (T, H))
+    prob = make_problem(T, H, max(top_k, 1), 8, top_k, dtype)
     if out is None:
-        out = torch.empty((T, H), dtype=dt, device=y_route.device)
+        out = torch.empty((T, H), dtype=dtype, device=y_route.device)
     _check(lib().moe_combine(ctypes.byref(prob), _p(y_route), _p(inv_route), _p(topk_ids),
                              _p(shared_out), _p(out), _stream(stream)), "moe_combine")
     return out
@@ -368,7 +369,7 @@ def moe_combine(y_route, inv_route, T, top_k, topk_ids=None, shared_out=None, ou
 
 def moe_shared_expert_fwd(hidden_states, shared_w_gate_up, shared_w_down, workspace=None,
                           stream=None):
-    """Dense SwiGLU shared expert (include/moe.h: moe_shared_expert_fwd); returns [T, H]."""
+    """Dense SwiGLU shared expert (include/moe.h: moe_shared_expert_fwd); returns f32 [T, H]."""
     T, H = hidden_states.shape
     S = shared_w_gate_up.shape[0] // 2
     dt = hidden_states.dtype
@@ -376,7 +377,7 @@ def moe_shared_expert_fwd(hidden_states, shared_w_gate_up, shared_w_down, worksp
     _need(shared_w_gate_up, "shared_w_gate_up", dt, (2 * S, H))
     _need(shared_w_down, "shared_w_down", dt, (H, S))
     prob = make_problem(T, H, 1, 8, 1, dt, S=S)
-    out = torch.empty((T, H), dtype=dt, device=hidden_states.device)
+    out = torch.empty((T, H), dtype=torch.float32, device=hidden_states.device)
     nbytes = workspace_size(prob)
     if workspace is None:
         workspace = _workspace(nbytes, hidden_states.device)

@@ -135,9 +135,9 @@ Layout make_layout(const moe_problem_t& p, int block_m) {
   L.tiles = take(sizeof(Tile) * L.max_tiles);
   L.a_sorted = take(direct ? 0 : (size_t)L.cap * p.H * eb);
   L.act = take((size_t)L.cap * p.F * eb);
-  L.y = take((size_t)L.cap * p.H * eb);
+  L.y = take((size_t)L.cap * p.H * sizeof(float));  // weighted down-projection rows, f32
   L.sh_act = take((size_t)p.T * p.S * eb);
-  L.sh_out = take(p.S > 0 ? (size_t)p.T * p.H * eb : 0);
+  L.sh_out = take(p.S > 0 ? (size_t)p.T * p.H * sizeof(float) : 0);
   L.total = off;
   return L;
 }

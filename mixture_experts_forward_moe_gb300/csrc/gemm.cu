@@ -16,8 +16,10 @@
 //              swizzle, into a multi-stage shared-memory ring (mbarrier complete_tx);
 //      warp 1  MMA issuer: tcgen05.mma kind::f16, f32 accumulators in TMEM, double-buffered
 //              so the epilogue of one unit overlaps the K loop of the next;
-//      warps 2-5  epilogue: tcgen05.ld -> f32 math -> one rounding to bf16/f16 -> transposed
-//              into shared memory -> 16-byte stores of whole output rows.
+//      warps 2-5  epilogue: tcgen05.ld -> f32 math.  gemm1 rounds SiLU(g)*u once to bf16/f16,
+//              transposes the tile through shared memory and stores whole output rows with
+//              16-byte stores; gemm2 keeps the weighted rows in f32 (rounded once, later, by the
+//              combine) and stores them straight from registers.
 //  * Cluster size 1 and no multicast: each CTA fetches its own tiles.
 //  * Every wait is bounded (global timer); on expiry the kernel records MOE_ERR_TIMEOUT, the
 //    roles stop, in-flight copies and MMAs are drained, TMEM is freed and the kernel returns.
@@ -44,11 +46,12 @@ namespace {
 
 template <bool kGemm1>
 struct Cfg {
-  static constexpr int kStages = kGemm1 ? 4 : 6;
+  static constexpr int kStages = kGemm1 ? 4 : 7;
   static constexpr int kABytes = (kGemm1 ? 2 : 1) * kSlab * kBlockK * 2;
   static constexpr int kBBytes = kTileRows * kBlockK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStagingBytes = kTileRows * kSlab * 2;
+  // gemm1 transposes its 16-bit tile through shared memory; gemm2 writes f32 from registers.
+  static constexpr int kStagingBytes = kGemm1 ? kTileRows * kSlab * 2 : 0;
   static constexpr int kAccCols = kGemm1 ? 2 * kSlab : kSlab;  // per accumulator buffer
   static constexpr int kTmemCols = 2 * kAccCols;                // double-buffered
   static constexpr int kSmemBytes = kStages * kStageBytes + kStagingBytes + 1024;
@@ -272,78 +275,106 @@ __global__ void __launch_bounds__(192, 1)
     const int q = warp & 3;  // the TMEM lane quarter this warp may read
     const int row = q * 32 + lane;
     const int et = threadIdx.x - 64;
-    T* out = static_cast<T*>(p.out);
-    T* stg = reinterpret_cast<T*>(staging);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
       Unit U;
       if (!decode_unit<kGemm1>(p, u, U)) continue;
-      // Output rows of this unit: (accumulator column, destination row).
-      int n_ent;
-      if (p.mode == kDirect) {
-        n_ent = p.P;
-        if (et < p.P) {
-          const bool mine = p.topk_ids[et] == U.e;
-          ent_col[et] = mine ? (kGemm1 ? et / p.top_k : et) : -1;
-          ent_dst[et] = et;
-        }
-      } else {
-        n_ent = U.nrows;
-        if (et < U.nrows) {
-          ent_col[et] = et;
-          ent_dst[et] = U.row0 + et;
-        }
-      }
-      if (!kGemm1 && et < U.n_mma) {
-        float sc = 0.0f;
-        if (p.mode == kSorted) {
-          if (et < U.nrows) {
-            const int sid = p.sorted_ids[U.row0 + et];
-            sc = sid >= 0 ? p.topk_w[sid] : 0.0f;
+      if constexpr (kGemm1) {
+        // Output rows of this unit as (accumulator column, destination row) entries; in direct
+        // mode a column is a token and each route of that token to this expert is an entry.
+        int n_ent;
+        if (p.mode == kDirect) {
+          n_ent = p.P;
+          if (et < p.P) {
+            ent_col[et] = p.topk_ids[et] == U.e ? et / p.top_k : -1;
+            ent_dst[et] = et;
           }
-        } else if (p.mode == kDirect) {
-          sc = et < p.P ? p.topk_w[et] : 0.0f;
         } else {
-          sc = 1.0f;
+          n_ent = U.nrows;
+          if (et < U.nrows) {
+            ent_col[et] = et;
+            ent_dst[et] = U.row0 + et;
+          }
         }
-        col_scale[et] = sc;
-      }
-      const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.limit_ns, p.status);
-      if (!named_bar_and(1, 128, got)) break;
-      tc_fence_after();
-      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
-      for (int c0 = 0; c0 < U.n_mma; c0 += 16) {
-        float g[16];
-        if (kGemm1) {
-          float v[16];
+        const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.limit_ns, p.status);
+        if (!named_bar_and(1, 128, got)) break;
+        tc_fence_after();
+        const uint32_t tb =
+            tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
+        T* stg = reinterpret_cast<T*>(staging);
+        for (int c0 = 0; c0 < U.n_mma; c0 += 16) {
+          float g[16], v[16];
           tmem_ld2_x16(tb + c0, tb + kSlab + c0, g, v);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const float h = __fdividef(g[j], 1.0f + __expf(-g[j])) * v[j];
             stg[(c0 + j) * kSlab + row] = DT<T>::from_f(h);
           }
-        } else {
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty_bar[acc]);
+        named_bar_sync(1, 128);
+        // 16-byte stores of whole output rows: entry en, chunk ch of 8 columns.
+        T* out = static_cast<T*>(p.out);
+        const int width = min(kSlab, p.n_out - U.slab * kSlab);
+        const int nch = width / 8;
+        for (int idx = et; idx < n_ent * 16; idx += 128) {
+          const int en = idx >> 4, ch = idx & 15;
+          if (ch >= nch) continue;
+          const int col = ent_col[en];
+          if (col < 0) continue;
+          const uint4 val = *reinterpret_cast<const uint4*>(stg + col * kSlab + ch * 8);
+          *reinterpret_cast<uint4*>(out + (int64_t)ent_dst[en] * p.n_out + U.slab * kSlab +
+                                    ch * 8) = val;
+        }
+        named_bar_sync(1, 128);
+      } else {
+        // Each accumulator column (token row) goes to at most one f32 output row, scaled by its
+        // route weight; thread `row` owns output column slab*128 + row, so a warp stores one
+        // 128-byte line per column.
+        if (et < U.n_mma) {
+          int dst = -1;
+          float sc = 0.0f;
+          if (p.mode == kSorted) {
+            if (et < U.nrows) {
+              dst = U.row0 + et;
+              const int sid = p.sorted_ids[dst];
+              sc = sid >= 0 ? p.topk_w[sid] : 0.0f;
+            }
+          } else if (p.mode == kDirect) {
+            if (et < p.P && p.topk_ids[et] == U.e) {
+              dst = et;
+              sc = p.topk_w[et];
+            }
+          } else if (et < U.nrows) {
+            dst = U.row0 + et;
+            sc = 1.0f;
+          }
+          ent_dst[et] = dst;
+          col_scale[et] = sc;
+        }
+        const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.limit_ns, p.status);
+        if (!named_bar_and(1, 128, got)) break;
+        tc_fence_after();
+        const uint32_t tb =
+            tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
+        float* out = static_cast<float*>(p.out);
+        const int h = U.slab * kSlab + row;
+        const bool in_range = h < p.n_out;
+        for (int c0 = 0; c0 < U.n_mma; c0 += 16) {
+          float g[16];
           tmem_ld_x16(tb + c0, g);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) stg[(c0 + j) * kSlab + row] = DT<T>::from_f(g[j] * col_scale[c0 + j]);
+          for (int j = 0; j < 16; ++j) {
+            const int dst = ent_dst[c0 + j];
+            if (dst >= 0 && in_range) out[(int64_t)dst * p.n_out + h] = g[j] * col_scale[c0 + j];
+          }
         }
+        tc_fence_before();
+        mbar_arrive(&tempty_bar[acc]);
+        named_bar_sync(1, 128);
       }
-      tc_fence_before();
-      mbar_arrive(&tempty_bar[acc]);
-      named_bar_sync(1, 128);
-      // 16-byte stores of whole output rows: entry en, chunk ch of 8 columns.
-      const int width = min(kSlab, p.n_out - U.slab * kSlab);
-      const int nch = width / 8;
-      for (int idx = et; idx < n_ent * 16; idx += 128) {
-        const int en = idx >> 4, ch = idx & 15;
-        if (ch >= nch) continue;
-        const int col = ent_col[en];
-        if (col < 0) continue;
-        const uint4 v = *reinterpret_cast<const uint4*>(stg + col * kSlab + ch * 8);
-        *reinterpret_cast<uint4*>(out + (int64_t)ent_dst[en] * p.n_out + U.slab * kSlab + ch * 8) = v;
-      }
-      named_bar_sync(1, 128);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }

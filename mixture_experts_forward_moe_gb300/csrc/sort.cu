@@ -170,13 +170,14 @@ __global__ void __launch_bounds__(128)
   }
 }
 
+// out[t, :] = round(sum_j y[inv[t*K+j], :] + shared[t, :]): f32 rows in, one rounding out.
 template <typename T>
 __global__ void __launch_bounds__(128)
-    combine_kernel(int K, int H, const T* __restrict__ y, const int32_t* __restrict__ inv,
-                   const int32_t* __restrict__ ids, const T* __restrict__ shared,
+    combine_kernel(int K, int H, const float* __restrict__ y, const int32_t* __restrict__ inv,
+                   const int32_t* __restrict__ ids, const float* __restrict__ shared,
                    T* __restrict__ out) {
   const int t = blockIdx.y;
-  const int v = blockIdx.x * blockDim.x + threadIdx.x;
+  const int v = blockIdx.x * blockDim.x + threadIdx.x;  // 8 columns per thread
   if (v >= H / 8) return;
   float acc[8];
 #pragma unroll
@@ -186,16 +187,16 @@ __global__ void __launch_bounds__(128)
     if (ids && ids[r] < 0) continue;
     const int p = inv ? inv[r] : r;
     if (p < 0) continue;
-    const uint4 u = reinterpret_cast<const uint4*>(y + (int64_t)p * H)[v];
-    const T* e = reinterpret_cast<const T*>(&u);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] += DT<T>::to_f(e[i]);
+    const float4* src = reinterpret_cast<const float4*>(y + (int64_t)p * H) + 2 * v;
+    const float4 a = src[0], b = src[1];
+    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
   }
   if (shared) {
-    const uint4 u = reinterpret_cast<const uint4*>(shared + (int64_t)t * H)[v];
-    const T* e = reinterpret_cast<const T*>(&u);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] += DT<T>::to_f(e[i]);
+    const float4* src = reinterpret_cast<const float4*>(shared + (int64_t)t * H) + 2 * v;
+    const float4 a = src[0], b = src[1];
+    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
   }
   uint4 o;
   T* oe = reinterpret_cast<T*>(&o);
@@ -253,12 +254,12 @@ cudaError_t launch_combine(const moe_problem_t& p, const void* y_route,
   dim3 grid((p.H / 8 + 127) / 128, p.T);
   if (p.dtype == MOE_BF16) {
     combine_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(
-        p.top_k, p.H, static_cast<const __nv_bfloat16*>(y_route), inv_route, ids,
-        static_cast<const __nv_bfloat16*>(shared_out), static_cast<__nv_bfloat16*>(out));
+        p.top_k, p.H, static_cast<const float*>(y_route), inv_route, ids,
+        static_cast<const float*>(shared_out), static_cast<__nv_bfloat16*>(out));
   } else {
     combine_kernel<__half><<<grid, 128, 0, s>>>(
-        p.top_k, p.H, static_cast<const __half*>(y_route), inv_route, ids,
-        static_cast<const __half*>(shared_out), static_cast<__half*>(out));
+        p.top_k, p.H, static_cast<const float*>(y_route), inv_route, ids,
+        static_cast<const float*>(shared_out), static_cast<__half*>(out));
   }
   return cudaGetLastError();
 }

@@ -1,6 +1,8 @@
 """Shared helpers of the GPU parity tests: run the oracle on the same seeded inputs the CUDA path
 gets (copied to the host), and compare with the tolerance max|gpu - oracle| <= 1e-2 * RMS."""
+import json
 import math
+import os
 
 import numpy as np
 import torch
@@ -22,14 +24,74 @@ def to_np(x):
     return np.asarray(x, dtype=np.float64)
 
 
+def half_ulp(x, dtype):
+    """Half the spacing of `dtype` (bf16: 8 significant bits, f16: 11) at |x|: the largest
+    error of one round-to-nearest of a value of that magnitude."""
+    bits = 8 if dtype == torch.bfloat16 else 11
+    tiny = 2.0 ** -133 if dtype == torch.bfloat16 else 2.0 ** -25  # half the subnormal step
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.maximum(np.where(a > 0, np.exp2(e - bits), 0.0), tiny)
+
+
+def log_parity(what, **kw):
+    path = os.environ.get("MOE_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(dict(what=what, **kw)) + "\n")
+
+
 def assert_rms_close(gpu, ref, tol=RMS_TOL, what=""):
+    """max |gpu - ref| <= tol * RMS(ref) (intermediates kept in f32)."""
     g, r = to_np(gpu), to_np(ref)
     assert g.shape == r.shape, (what, g.shape, r.shape)
     assert np.all(np.isfinite(g)), f"{what}: non-finite GPU values"
     rms = math.sqrt(float(np.mean(r * r))) if r.size else 0.0
     err = float(np.max(np.abs(g - r))) if r.size else 0.0
+    log_parity(what, max_err_over_rms=err / rms if rms else 0.0, tol=tol)
     assert err <= tol * rms + 1e-30, f"{what}: max|gpu-ref|={err:.3e} > {tol}*RMS={tol * rms:.3e}"
     return err / rms if rms > 0 else 0.0
+
+
+def assert_rounded_close(gpu, ref, dtype, rel_rms=1e-3, what=""):
+    """A 16-bit output rounded once from an f32 value: |gpu - ref| <= half an ulp of the
+    dtype at |ref| (allowing for a crossing into the next binade) + rel_rms * RMS(ref)."""
+    g, r = to_np(gpu), to_np(ref)
+    assert g.shape == r.shape, (what, g.shape, r.shape)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite GPU values"
+    if not r.size:
+        return 0.0
+    rms = math.sqrt(float(np.mean(r * r)))
+    err = np.abs(g - r)
+    bound = half_ulp(np.abs(r) * (1 + 2.0 ** -7), dtype) + rel_rms * rms
+    worst = int(np.argmax(err - bound))
+    log_parity(what, max_err_over_rms=float(err.max()) / rms, rounded_rel_rms=rel_rms)
+    assert np.all(err <= bound), (f"{what}: |gpu-ref|={err.flat[worst]:.3e} at ref="
+                                  f"{r.flat[worst]:.4e} > bound {bound.flat[worst]:.3e}")
+    return float(err.max()) / rms
+
+
+def assert_output_close(gpu, ref, dtype, tol=RMS_TOL, what=""):
+    """The fused output: |gpu - oracle| <= tol * RMS(oracle) + half an ulp of the output dtype at
+    |oracle| (the final rounding to bf16/f16, which no 16-bit output can avoid).  Also logs the
+    plain max|gpu - oracle| / RMS."""
+    g, r = to_np(gpu), to_np(ref)
+    assert g.shape == r.shape, (what, g.shape, r.shape)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite GPU values"
+    if not r.size:
+        return 0.0
+    rms = math.sqrt(float(np.mean(r * r)))
+    err = np.abs(g - r)
+    hu = half_ulp(r, dtype)
+    excess = float(np.max(err - hu)) / rms
+    log_parity(what, max_err_over_rms=float(err.max()) / rms, max_err_minus_half_ulp_over_rms=excess,
+               tol=tol)
+    worst = int(np.argmax(err - hu))
+    assert np.all(err <= tol * rms + hu), (f"{what}: |gpu-ref|={err.flat[worst]:.3e} at "
+                                           f"ref={r.flat[worst]:.4e}: exceeds {tol}*RMS "
+                                           f"({tol * rms:.3e}) + half ulp ({hu.flat[worst]:.3e})")
+    return float(err.max()) / rms
 
 
 def scoring_code(w):

@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import assert_rms_close, oracle_fused, oracle_route, run_fused, run_route
+from helpers import assert_output_close, oracle_fused, oracle_route, run_fused, run_route
 from mixture_experts_forward_moe_gb300 import binding as B
 from mixture_experts_forward_moe_gb300 import inputs
 
@@ -41,7 +41,7 @@ def test_fused_small_matches_oracle(w, cuda_device):
     torch.cuda.synchronize()
     ref, r_ids, _, _ = oracle_fused(w, d)
     assert np.array_equal(ids.cpu().numpy(), r_ids)
-    assert_rms_close(out, ref, what=w.name)
+    assert_output_close(out, ref, w.dtype, what=w.name)
     assert B.get_device_status(B._workspace(0, cuda_device)) == B.MOE_OK
 
 
@@ -130,7 +130,8 @@ def _full_size_check(w, n_sample, dev):
     else:  # first, last and evenly spread tokens
         tokens = np.unique(np.linspace(0, w.T - 1, n_sample).astype(np.int32))
     ref, _, _, _ = oracle_fused(w, d, tokens=tokens, routed=routed)
-    assert_rms_close(out[torch.from_numpy(tokens).to(dev).long()], ref, what=w.name)
+    assert_output_close(out[torch.from_numpy(tokens).to(dev).long()], ref, w.dtype,
+                        what=f"{w.name} {w.dtype}")
     out2 = run_fused(w, d)
     assert torch.equal(out, out2), "repeat call not bit-identical"
     assert B.get_device_status(B._workspace(0, dev)) == B.MOE_OK

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import assert_rms_close, dt_code
+from helpers import assert_rms_close, assert_rounded_close, dt_code, log_parity
 from mixture_experts_forward_moe_gb300 import binding as B
 from mixture_experts_forward_moe_gb300 import inputs
 
@@ -51,7 +51,7 @@ def test_gemm1_and_gemm2_match_oracle(T, k, E, H, F, block_m, pad, dtype, cuda_d
     live = sid >= 0
     x_rows[torch.from_numpy(np.nonzero(live)[0])] = hid[torch.from_numpy(sid[live] // k)]
     ref_act = oracle.expert_act(x_rows, eo[:rows], d["w_gate_up"].cpu(), dt_code(dtype))
-    assert_rms_close(act[:rows], ref_act, what="act")
+    assert_rounded_close(act[:rows], ref_act, dtype, what=f"act T={T} E={E} H={H} F={F}")
     assert torch.all(act[:rows][torch.from_numpy(~live).to(cuda_device)] == 0)
 
     # gemm2 on a seeded act (not the GPU's), with route weights
@@ -62,7 +62,7 @@ def test_gemm1_and_gemm2_match_oracle(T, k, E, H, F, block_m, pad, dtype, cuda_d
     scale = np.where(live, tw.cpu().numpy()[np.maximum(sid, 0)], 0.0)
     ref_y = oracle.expert_down(a_in[:rows].cpu(), eo[:rows], scale, d["w_down"].cpu(),
                                dt_code(dtype))
-    assert_rms_close(y[:rows], ref_y, what="y_route")
+    assert_rms_close(y[:rows], ref_y, tol=1e-4, what=f"y_route T={T} E={E} H={H} F={F}")
     assert torch.all(y[:rows][torch.from_numpy(~live).to(cuda_device)] == 0)
     ws = B._workspace(0, cuda_device)
     assert B.get_device_status(ws) == B.MOE_OK
@@ -74,20 +74,19 @@ def test_combine_matches_oracle(dtype, cuda_device):
     ids = inputs.random_ids(T, k, E, seed=2, pad_frac=0.1)
     srt = oracle.align_sort(ids.numpy(), E, 4)
     cap = srt["sorted_ids"].size
-    y = inputs.random_rows(cap, H, seed=5, dtype=dtype).to(cuda_device)
-    sh = inputs.random_rows(T, H, seed=6, dtype=dtype).to(cuda_device)
+    # f32 rows that are exactly representable in bf16 so the oracle can read them as bits
+    y16 = inputs.random_rows(cap, H, seed=5, dtype=torch.bfloat16)
+    sh16 = inputs.random_rows(T, H, seed=6, dtype=torch.bfloat16)
+    y = y16.float().to(cuda_device)
+    sh = sh16.float().to(cuda_device)
     inv = torch.from_numpy(srt["inv_route"]).to(cuda_device)
-    out = B.moe_combine(y, inv, T, k, topk_ids=ids.to(cuda_device), shared_out=sh)
-    ref = oracle.combine(y.cpu(), srt["inv_route"], k, dt_code(dtype), shared=sh.cpu())
-    # one rounding of an f32 sum: half an ulp of the 16-bit type, plus f32 summation error
-    eps = 2.0 ** -8 if dtype == torch.bfloat16 else 2.0 ** -11
-    got = out.double().cpu().numpy()
-    assert np.all(np.abs(got - ref) <= eps * np.abs(ref) + 1e-6 * np.abs(ref).max())
-    out2 = B.moe_combine(y, None, T, k, topk_ids=ids.to(cuda_device))  # identity map
-    ref2 = oracle.combine(y.cpu(), np.where(ids.numpy().reshape(-1) >= 0,
-                                            np.arange(T * k), -1).astype(np.int32), k,
-                          dt_code(dtype))
-    assert np.all(np.abs(out2.double().cpu().numpy() - ref2) <= eps * np.abs(ref2) + 1e-6)
+    out = B.moe_combine(y, inv, T, k, topk_ids=ids.to(cuda_device), shared_out=sh, dtype=dtype)
+    ref = oracle.combine(y16, srt["inv_route"], k, oracle.BF16, shared=sh16)
+    assert_rounded_close(out, ref, dtype, rel_rms=1e-6, what="combine")
+    out2 = B.moe_combine(y, None, T, k, topk_ids=ids.to(cuda_device), dtype=dtype)  # identity
+    ref2 = oracle.combine(y16, np.where(ids.numpy().reshape(-1) >= 0,
+                                        np.arange(T * k), -1).astype(np.int32), k, oracle.BF16)
+    assert_rounded_close(out2, ref2, dtype, rel_rms=1e-6, what="combine identity")
 
 
 @pytest.mark.parametrize("T,H,S", [(1, 256, 128), (37, 192, 320), (300, 128, 136)])
@@ -100,4 +99,13 @@ def test_shared_expert_matches_oracle(T, H, S, cuda_device):
     ref = oracle.moe_tokens(d["hidden_states"].cpu(), none, np.zeros((T, 1)), d["w_gate_up"].cpu(),
                             d["w_down"].cpu(), 0, shared_w_gate_up=d["shared_w_gate_up"].cpu(),
                             shared_w_down=d["shared_w_down"].cpu())
-    assert_rms_close(out, ref, what="shared")
+    # The only rounding on the path is SiLU(g)*u to bf16 (at most 2^-8 relative) before the f32
+    # down projection, so |gpu - oracle|_h <= 2^-8 * sum_f |Wd[h,f]| |act_f| (+ f32 slack).
+    act = oracle.expert_act(d["hidden_states"].cpu(), np.zeros(T, np.int32),
+                            d["shared_w_gate_up"].cpu()[None], oracle.BF16)
+    wd_abs = np.abs(d["shared_w_down"].double().cpu().numpy())
+    bound = 2.0 ** -8 * (np.abs(act) @ wd_abs.T) + 1e-5 * np.sqrt(np.mean(ref * ref))
+    err = np.abs(out.double().cpu().numpy() - ref)
+    log_parity(f"shared T={T} H={H} S={S}", max_err_over_rms=float(err.max()) /
+               float(np.sqrt(np.mean(ref * ref))), max_err_over_bound=float((err / bound).max()))
+    assert np.all(err <= bound)
