@@ -215,6 +215,27 @@ moe_status_t moe_shared_expert_fwd(const moe_problem_t* p, const void* hidden_st
                                    void* shared_out, void* workspace, size_t workspace_bytes,
                                    void* stream);
 
+/*
+ * moe_align_sort_noalloc -- the sort of moe_align_sort for callers that cannot allocate device
+ * memory when they need it: a serving engine that has handed all device memory to its own pool
+ * and forbids later cudaMalloc (which would synchronise the device and fragment the pool), or a
+ * plugin entry point whose framework passes only input and output buffers and no workspace.
+ * The source pages have no counterpart of this entry point.
+ * Same arguments and results as moe_align_sort, minus the workspace: the scratch (per-chunk
+ * expert histograms and a status word) lives in a static device array of 256 KiB + 256 bytes
+ * inside the library, which every GPU that loads the library holds until the process exits.
+ *   status_out  device int32 or NULL: receives MOE_OK or MOE_ERR_BAD_EXPERT_ID for this call
+ * Limits: ceil(T*top_k/256) * E <= 65536, else MOE_ERR_WORKSPACE_TOO_SMALL (nothing enqueued);
+ * E <= 1024.  The first call on a device looks up the array's address (cudaGetSymbolAddress,
+ * with that device current); make it before any stream capture.  No call allocates.  Every call
+ * shares the array and the array keeps the last call's contents: each call clears the status
+ * word itself, and calls that overlap on the GPU (concurrent streams or threads) race.
+ */
+moe_status_t moe_align_sort_noalloc(const moe_problem_t* p, int32_t block_m,
+                                    const int32_t* topk_ids, int32_t* counts, int32_t* offsets,
+                                    int32_t* sorted_ids, int32_t* tile_expert,
+                                    int32_t* inv_route, int32_t* status_out, void* stream);
+
 /* ---------------------------------------------------------------------------------------- */
 /* Status.                                                                                    */
 /* ---------------------------------------------------------------------------------------- */

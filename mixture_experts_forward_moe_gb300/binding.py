@@ -28,7 +28,7 @@ EXPORTED = (
     "moe_workspace_init", "fused_moe_fwd", "moe_route", "moe_align_sort", "moe_gemm1_swiglu",
     "moe_gemm2", "moe_combine", "moe_shared_expert_fwd", "moe_get_device_status",
     "moe_status_string", "moe_set_wait_limit_ns", "moe_stage_name", "moe_profile_enable",
-    "moe_profile_collect",
+    "moe_profile_collect", "moe_align_sort_noalloc",
 )
 
 
@@ -91,6 +91,8 @@ def lib():
             L.moe_profile_enable.argtypes = [i32]
             L.moe_profile_collect.restype = i32
             L.moe_profile_collect.argtypes = [P, P, P, i32]
+            L.moe_align_sort_noalloc.restype = ctypes.c_int
+            L.moe_align_sort_noalloc.argtypes = [PP, i32, P, P, P, P, P, P, P, P]
             for fn in ("fused_moe_fwd", "moe_route", "moe_align_sort", "moe_gemm1_swiglu",
                        "moe_gemm2", "moe_combine", "moe_shared_expert_fwd",
                        "moe_get_device_status", "moe_workspace_init"):
@@ -296,6 +298,32 @@ def moe_align_sort(topk_ids, num_experts, block_m=1, workspace=None, stream=None
     return dict(counts=counts, offsets=offsets, sorted_ids=sorted_ids[:cap],
                 tile_expert=None if tile_expert is None else tile_expert[:tile_len],
                 inv_route=inv[:T * k], workspace=workspace)
+
+
+def moe_align_sort_noalloc(topk_ids, num_experts, block_m=1, stream=None):
+    """The expert sort with the library's static scratch instead of a workspace (include/moe.h:
+    moe_align_sort_noalloc), for callers that cannot allocate device memory when they sort;
+    the output tensors here are torch's, the sort itself allocates nothing.  Returns the same
+    dict as moe_align_sort plus a device int32 `status`."""
+    _need(topk_ids, "topk_ids", torch.int32)
+    T, k = topk_ids.shape
+    E = int(num_experts)
+    prob = make_problem(T, 8, E, 8, k)
+    cap = sorted_capacity(prob, block_m)
+    dev = topk_ids.device
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    sorted_ids = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+    tile_len = (cap + block_m - 1) // block_m
+    tile_expert = torch.empty(max(tile_len, 1), dtype=torch.int32, device=dev)
+    inv = torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)
+    status = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    _check(lib().moe_align_sort_noalloc(ctypes.byref(prob), int(block_m), _p(topk_ids),
+                                        _p(counts), _p(offsets), _p(sorted_ids),
+                                        _p(tile_expert), _p(inv), _p(status), _stream(stream)),
+           "moe_align_sort_noalloc")
+    return dict(counts=counts, offsets=offsets, sorted_ids=sorted_ids[:cap],
+                tile_expert=tile_expert[:tile_len], inv_route=inv[:T * k], status=status)
 
 
 def moe_gemm1_swiglu(hidden_states, sorted_ids, offsets, w_gate_up, top_k, block_m=1,
