@@ -104,10 +104,25 @@ bool use_direct(const moe_problem_t& p) {
   return p.T <= kDirectMaxT && (int64_t)p.T * p.top_k <= kDirectMaxRoutes;
 }
 
+// Token rows per tile of the sorted down-projection GEMM: 256 when the experts average at
+// least 96 routed rows (prefill), so an expert's weights reach the SMs at most once per 256
+// rows; 128 otherwise (decode), which keeps deeper pipelines.  The gate/up GEMM always uses
+// 128-row tiles: at 256 rows its two accumulators fill TMEM and the epilogue could no longer
+// overlap the next unit's K loop, which measured slower on the prefill shapes.
+int sorted_tile_rows(const moe_problem_t& p) {
+  const int64_t P = (int64_t)p.T * p.top_k;
+  const int64_t active = P < p.E ? P : p.E;
+  return active > 0 && P / active >= 96 ? kTileRowsWide : kTileRows;
+}
+
+// Token rows per tile of the dense shared-expert GEMMs.
+int dense_tile_rows(const moe_problem_t& p) { return p.T > kTileRows ? kTileRowsWide : kTileRows; }
+
 // Workspace layout of a call (all offsets 256-byte aligned).
 struct Layout {
   int64_t P, cap, n_chunks, max_tiles;
-  size_t ids, w, counts, offsets, sorted, inv, chunk, tiles, a_sorted, act, y, sh_act, sh_out;
+  size_t ids, w, counts, offsets, sorted, inv, chunk, tiles, tiles2, a_sorted, act, y, sh_act,
+      sh_out;
   size_t total;
 };
 
@@ -133,6 +148,7 @@ Layout make_layout(const moe_problem_t& p, int block_m) {
   L.inv = take(sizeof(int32_t) * L.P);
   L.chunk = take(sizeof(int32_t) * L.n_chunks * p.E);
   L.tiles = take(sizeof(Tile) * L.max_tiles);
+  L.tiles2 = take(sizeof(Tile) * L.max_tiles);
   L.a_sorted = take(direct ? 0 : (size_t)L.cap * p.H * eb);
   L.act = take((size_t)L.cap * p.F * eb);
   L.y = take((size_t)L.cap * p.H * sizeof(float));  // weighted down-projection rows, f32
@@ -149,6 +165,7 @@ P* at(void* ws, size_t off) {
 
 int* status_word(void* ws) { return static_cast<int*>(ws); }
 int* tile_counter(void* ws) { return reinterpret_cast<int*>(static_cast<char*>(ws) + 64); }
+int* tile_counter2(void* ws) { return reinterpret_cast<int*>(static_cast<char*>(ws) + 128); }
 
 moe_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
@@ -166,12 +183,14 @@ GemmCall base_call(const moe_problem_t& p, int* status) {
   c.T = p.T;
   c.P = p.T * p.top_k;
   c.E = p.E;
+  c.tile_rows = kTileRows;
   return c;
 }
 
 // Shared expert: dense gemm1 (hidden -> sh_act) and dense gemm2 (sh_act -> sh_out).
 cudaError_t run_shared(const moe_problem_t& p, const void* hidden, const void* sgu,
-                       const void* sd, void* sh_act, void* sh_out, int* status, cudaStream_t s) {
+                       const void* sd, void* sh_act, void* sh_out, int* status, cudaStream_t s,
+                       bool pdl) {
   GemmCall g1 = base_call(p, status);
   g1.gemm1 = 1;
   g1.mode = kDense;
@@ -183,10 +202,11 @@ cudaError_t run_shared(const moe_problem_t& p, const void* hidden, const void* s
   g1.b_rows = p.T;
   g1.out = sh_act;
   g1.dense_rows = p.T;
+  g1.tile_rows = dense_tile_rows(p);
   cudaError_t e;
   {
     StageTimer t(kSharedGemm1, s);
-    e = launch_gemm(g1, s);
+    e = launch_gemm(g1, s, pdl);
     t.done(1);
   }
   if (e != cudaSuccess) return e;
@@ -201,8 +221,9 @@ cudaError_t run_shared(const moe_problem_t& p, const void* hidden, const void* s
   g2.b_rows = p.T;
   g2.out = sh_out;
   g2.dense_rows = p.T;
+  g2.tile_rows = dense_tile_rows(p);
   StageTimer t(kSharedGemm2, s);
-  e = launch_gemm(g2, s);
+  e = launch_gemm(g2, s, true);
   t.done(1);
   return e;
 }
@@ -275,7 +296,7 @@ moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
 
   {
     StageTimer t(kRoute, s);
-    MOE_TRY(launch_route(P, gating_output, correction_bias, ids, w, s));
+    MOE_TRY(launch_route(P, gating_output, correction_bias, ids, w, s, false));
     t.done(1);
   }
 
@@ -294,7 +315,7 @@ moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
     g1.topk_ids = ids;
     {
       StageTimer t(kGemm1, s);
-      MOE_TRY(launch_gemm(g1, s));
+      MOE_TRY(launch_gemm(g1, s, true));
       t.done(1);
     }
     GemmCall g2 = base_call(P, status);
@@ -310,7 +331,7 @@ moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
     g2.topk_w = w;
     {
       StageTimer t(kGemm2, s);
-      MOE_TRY(launch_gemm(g2, s));
+      MOE_TRY(launch_gemm(g2, s, true));
       t.done(1);
     }
   } else {
@@ -318,22 +339,31 @@ moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
     int32_t* offsets = at<int32_t>(ws, L.offsets);
     int32_t* sorted = at<int32_t>(ws, L.sorted);
     int32_t* inv_route = at<int32_t>(ws, L.inv);
-    {
+    Tile* tiles = at<Tile>(ws, L.tiles);    // gemm1: 128-row tiles
+    Tile* tiles2 = at<Tile>(ws, L.tiles2);  // gemm2: tile_rows2-row tiles
+    const int tile_rows2 = sorted_tile_rows(P);
+    if (fused_sort_fits(P)) {  // sort and both tile lists in one launch
       StageTimer t(kSort, s);
-      MOE_TRY(launch_align_sort(P, 1, ids, counts, offsets, sorted, L.cap, nullptr, inv_route,
-                                at<int32_t>(ws, L.chunk), status, s));
-      t.done(3);
-    }
-    Tile* tiles = at<Tile>(ws, L.tiles);
-    {
-      StageTimer t(kTiles, s);
-      MOE_TRY(launch_build_tiles(P.E, offsets, tiles, tile_counter(ws), s));
+      MOE_TRY(launch_sort_fused(P, 1, ids, counts, offsets, sorted, L.cap, nullptr, inv_route,
+                                tiles, tile_counter(ws), kTileRows, tiles2, tile_counter2(ws),
+                                tile_rows2, status, s, true));
       t.done(1);
+    } else {
+      {
+        StageTimer t(kSort, s);
+        MOE_TRY(launch_align_sort_chunked(P, 1, ids, counts, offsets, sorted, L.cap, nullptr,
+                                          inv_route, at<int32_t>(ws, L.chunk), status, s, true));
+        t.done(3);
+      }
+      StageTimer t(kTiles, s);
+      MOE_TRY(launch_build_tiles(P.E, offsets, tiles, tile_counter(ws), kTileRows, s, true));
+      MOE_TRY(launch_build_tiles(P.E, offsets, tiles2, tile_counter2(ws), tile_rows2, s, true));
+      t.done(2);
     }
     {
       StageTimer t(kPermute, s);
       MOE_TRY(launch_permute(P.dtype, P.top_k, P.H, hidden_states, sorted, offsets, P.E, L.cap,
-                             at<void>(ws, L.a_sorted), s));
+                             at<void>(ws, L.a_sorted), s, true));
       t.done(1);
     }
     GemmCall g1 = base_call(P, status);
@@ -348,9 +378,10 @@ moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
     g1.tiles = tiles;
     g1.n_tiles = tile_counter(ws);
     g1.max_tiles = (int)L.max_tiles;
+    g1.tile_rows = kTileRows;
     {
       StageTimer t(kGemm1, s);
-      MOE_TRY(launch_gemm(g1, s));
+      MOE_TRY(launch_gemm(g1, s, true));
       t.done(1);
     }
     GemmCall g2 = g1;
@@ -362,9 +393,12 @@ moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
     g2.out = at<void>(ws, L.y);
     g2.sorted_ids = sorted;
     g2.topk_w = w;
+    g2.tiles = tiles2;
+    g2.n_tiles = tile_counter2(ws);
+    g2.tile_rows = tile_rows2;
     {
       StageTimer t(kGemm2, s);
-      MOE_TRY(launch_gemm(g2, s));
+      MOE_TRY(launch_gemm(g2, s, true));
       t.done(1);
     }
     inv = inv_route;
@@ -372,12 +406,12 @@ moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
   const void* sh_out = nullptr;
   if (P.S > 0) {
     MOE_TRY(run_shared(P, hidden_states, shared_w_gate_up, shared_w_down, at<void>(ws, L.sh_act),
-                       at<void>(ws, L.sh_out), status, s));
+                       at<void>(ws, L.sh_out), status, s, true));
     sh_out = at<void>(ws, L.sh_out);
   }
   {
     StageTimer t(kCombine, s);
-    MOE_TRY(launch_combine(P, y_rows, inv, ids, sh_out, out, s));
+    MOE_TRY(launch_combine(P, y_rows, inv, ids, sh_out, out, s, true));
     t.done(1);
   }
   return MOE_OK;
@@ -390,8 +424,8 @@ moe_status_t moe_route(const moe_problem_t* p, const float* gating_output,
   if (st != MOE_OK) return st;
   if (p->T > 0 && (!gating_output || !topk_ids || !topk_weights)) return MOE_ERR_INVALID_ARG;
   if (correction_bias && p->scoring != MOE_SIGMOID) return MOE_ERR_UNSUPPORTED;
-  return from_cuda(
-      launch_route(*p, gating_output, correction_bias, topk_ids, topk_weights, (cudaStream_t)stream));
+  return from_cuda(launch_route(*p, gating_output, correction_bias, topk_ids, topk_weights,
+                                (cudaStream_t)stream, false));
 }
 
 moe_status_t moe_align_sort(const moe_problem_t* p, int32_t block_m, const int32_t* topk_ids,
@@ -408,7 +442,7 @@ moe_status_t moe_align_sort(const moe_problem_t* p, int32_t block_m, const int32
   const int64_t cap = moe_sorted_capacity(p, block_m);
   return from_cuda(launch_align_sort(*p, block_m, topk_ids, counts, offsets, sorted_ids, cap,
                                      tile_expert, inv_route, at<int32_t>(workspace, L.chunk),
-                                     status_word(workspace), (cudaStream_t)stream));
+                                     status_word(workspace), (cudaStream_t)stream, false));
 }
 
 moe_status_t moe_gemm1_swiglu(const moe_problem_t* p, int32_t block_m, const void* hidden_states,
@@ -425,9 +459,10 @@ moe_status_t moe_gemm1_swiglu(const moe_problem_t* p, int32_t block_m, const voi
   cudaStream_t s = (cudaStream_t)stream;
   void* ws = workspace;
   Tile* tiles = at<Tile>(ws, L.tiles);
-  MOE_TRY(launch_build_tiles(p->E, offsets, tiles, tile_counter(ws), s));
+  const int tile_rows = kTileRows;
+  MOE_TRY(launch_build_tiles(p->E, offsets, tiles, tile_counter(ws), tile_rows, s, false));
   MOE_TRY(launch_permute(p->dtype, p->top_k, p->H, hidden_states, sorted_ids, offsets, p->E,
-                         L.cap, at<void>(ws, L.a_sorted), s));
+                         L.cap, at<void>(ws, L.a_sorted), s, true));
   GemmCall g1 = base_call(*p, status_word(ws));
   g1.gemm1 = 1;
   g1.mode = kSorted;
@@ -440,7 +475,8 @@ moe_status_t moe_gemm1_swiglu(const moe_problem_t* p, int32_t block_m, const voi
   g1.tiles = tiles;
   g1.n_tiles = tile_counter(ws);
   g1.max_tiles = (int)L.max_tiles;
-  return from_cuda(launch_gemm(g1, s));
+  g1.tile_rows = tile_rows;
+  return from_cuda(launch_gemm(g1, s, true));
 }
 
 moe_status_t moe_gemm2(const moe_problem_t* p, int32_t block_m, const void* act,
@@ -457,7 +493,8 @@ moe_status_t moe_gemm2(const moe_problem_t* p, int32_t block_m, const void* act,
   cudaStream_t s = (cudaStream_t)stream;
   void* ws = workspace;
   Tile* tiles = at<Tile>(ws, L.tiles);
-  MOE_TRY(launch_build_tiles(p->E, offsets, tiles, tile_counter(ws), s));
+  const int tile_rows = sorted_tile_rows(*p);
+  MOE_TRY(launch_build_tiles(p->E, offsets, tiles, tile_counter(ws), tile_rows, s, false));
   GemmCall g2 = base_call(*p, status_word(ws));
   g2.gemm1 = 0;
   g2.mode = kSorted;
@@ -470,9 +507,10 @@ moe_status_t moe_gemm2(const moe_problem_t* p, int32_t block_m, const void* act,
   g2.tiles = tiles;
   g2.n_tiles = tile_counter(ws);
   g2.max_tiles = (int)L.max_tiles;
+  g2.tile_rows = tile_rows;
   g2.sorted_ids = sorted_ids;
   g2.topk_w = topk_weights;
-  return from_cuda(launch_gemm(g2, s));
+  return from_cuda(launch_gemm(g2, s, true));
 }
 
 moe_status_t moe_combine(const moe_problem_t* p, const void* y_route, const int32_t* inv_route,
@@ -481,8 +519,8 @@ moe_status_t moe_combine(const moe_problem_t* p, const void* y_route, const int3
   moe_status_t st = check_problem(p);
   if (st != MOE_OK) return st;
   if (p->T > 0 && (!y_route || !out)) return MOE_ERR_INVALID_ARG;
-  return from_cuda(
-      launch_combine(*p, y_route, inv_route, topk_ids, shared_out, out, (cudaStream_t)stream));
+  return from_cuda(launch_combine(*p, y_route, inv_route, topk_ids, shared_out, out,
+                                  (cudaStream_t)stream, false));
 }
 
 moe_status_t moe_shared_expert_fwd(const moe_problem_t* p, const void* hidden_states,
@@ -500,7 +538,7 @@ moe_status_t moe_shared_expert_fwd(const moe_problem_t* p, const void* hidden_st
   if (p->T == 0) return MOE_OK;
   return from_cuda(run_shared(*p, hidden_states, shared_w_gate_up, shared_w_down,
                               at<void>(workspace, L.sh_act), shared_out,
-                              status_word(workspace), (cudaStream_t)stream));
+                              status_word(workspace), (cudaStream_t)stream, false));
 }
 
 moe_status_t moe_get_device_status(void* workspace, void* stream) {

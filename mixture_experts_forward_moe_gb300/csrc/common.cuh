@@ -15,9 +15,11 @@ namespace gb300moe {
 // use this only as an upper bound for static tables.
 constexpr int kMaxSMs = 256;
 
-// Token rows per GEMM tile (the N side of the tcgen05 MMA) and weight rows per slab (the M
-// side); K is staged 64 elements (128 bytes) at a time with the 128-byte swizzle.
+// Token rows per GEMM tile (the N side of the tcgen05 MMA: 128, or 256 when experts have many
+// rows) and weight rows per slab (the M side); K is staged 64 elements (128 bytes) at a time
+// with the 128-byte swizzle.
 constexpr int kTileRows = 128;
+constexpr int kTileRowsWide = 256;
 constexpr int kSlab = 128;
 constexpr int kBlockK = 64;
 
@@ -41,30 +43,69 @@ template <> struct DT<__half> {
   __device__ __forceinline__ static __half from_f(float v) { return __float2half_rn(v); }
 };
 
-// A tile of the grouped GEMM schedule: expert, first row, number of rows (<= kTileRows).
-struct Tile {
-  int e, row0, nrows, pad;
+// A tile of the grouped GEMM schedule: expert, first row, number of rows (<= kTileRows), and
+// the index of the expert's first tile and its tile count (the tiles of an expert are
+// contiguous), so that a unit index maps to (expert, weight slab, tile) in O(1).
+struct __align__(16) Tile {
+  int e, row0, nrows, first;
+  int count, pad0, pad1, pad2;
 };
 
-// ---- launchers (defined in the .cu files, called by api.cu) ------------------------------
-cudaError_t launch_route(const moe_problem_t& p, const float* gating, const float* bias,
-                         int32_t* ids, float* w, cudaStream_t s);
+// Launch `kern` on `s`; with pdl the launch may overlap the tail of the previous kernel on the
+// stream (programmatic stream serialization): the kernel itself waits for it with pdl_wait().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 
+// ---- launchers (defined in the .cu files, called by api.cu) ------------------------------
+// `pdl`: true when the launch follows another kernel of the same entry point.
+cudaError_t launch_route(const moe_problem_t& p, const float* gating, const float* bias,
+                         int32_t* ids, float* w, cudaStream_t s, bool pdl);
+
+// The sort: one launch when it fits, else the chunked form.
 cudaError_t launch_align_sort(const moe_problem_t& p, int block_m, const int32_t* ids,
                               int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
                               int64_t cap, int32_t* tile_expert, int32_t* inv_route,
-                              int32_t* chunk_scratch, int* status, cudaStream_t s);
+                              int32_t* chunk_scratch, int* status, cudaStream_t s, bool pdl);
+
+// The sort in one launch (one CTA) when it fits (T*top_k <= 65536); with `tiles` (`tiles2`)
+// it also writes the GEMM tile list of tile_rows (tile_rows2) rows per tile.
+bool fused_sort_fits(const moe_problem_t& p);
+cudaError_t launch_sort_fused(const moe_problem_t& p, int block_m, const int32_t* ids,
+                              int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
+                              int64_t cap, int32_t* tile_expert, int32_t* inv_route, Tile* tiles,
+                              int* n_tiles, int tile_rows, Tile* tiles2, int* n_tiles2,
+                              int tile_rows2, int* status, cudaStream_t s, bool pdl);
+// The sort as three launches over 256-route chunks (any size), using chunk_scratch
+// (ceil(T*top_k/256) * E int32).
+cudaError_t launch_align_sort_chunked(const moe_problem_t& p, int block_m, const int32_t* ids,
+                                      int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
+                                      int64_t cap, int32_t* tile_expert, int32_t* inv_route,
+                                      int32_t* chunk_scratch, int* status, cudaStream_t s,
+                                      bool pdl);
 
 cudaError_t launch_build_tiles(int E, const int32_t* offsets, Tile* tiles, int* n_tiles,
-                               cudaStream_t s);
+                               int tile_rows, cudaStream_t s, bool pdl);
 
 cudaError_t launch_permute(int dtype, int top_k, int H, const void* hidden,
                            const int32_t* sorted_ids, const int32_t* offsets, int E, int64_t cap,
-                           void* a_sorted, cudaStream_t s);
+                           void* a_sorted, cudaStream_t s, bool pdl);
 
 cudaError_t launch_combine(const moe_problem_t& p, const void* y_route,
                            const int32_t* inv_route, const int32_t* ids, const void* shared_out,
-                           void* out, cudaStream_t s);
+                           void* out, cudaStream_t s, bool pdl);
 
 // Grouped GEMM on tcgen05.  mode: 0 = sorted segments (tile list), 1 = direct from topk_ids
 // (T <= 8), 2 = dense rows (one expert, all rows: the shared expert).
@@ -85,6 +126,7 @@ struct GemmCall {
   const Tile* tiles;
   const int* n_tiles;
   int max_tiles;  // upper bound of *n_tiles (grid sizing)
+  int tile_rows;  // token rows per tile: 128 or 256 (sorted tiles must be built with it)
   const int32_t* sorted_ids;  // gemm2 scale lookup
   // direct mode
   const int32_t* topk_ids;
@@ -96,7 +138,7 @@ struct GemmCall {
   int* status;
 };
 
-cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s);
+cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl);
 
 uint64_t wait_limit_ns();
 int num_sms();

@@ -44,16 +44,24 @@ namespace gb300moe {
 
 namespace {
 
-template <bool kGemm1>
+// Tile configurations: kN token rows per tile (the MMA's N).  kN = 128 keeps two accumulator
+// buffers in TMEM for every GEMM (the epilogue of one unit overlaps the K loop of the next);
+// kN = 256 halves how often an expert with many rows streams its weights, at the cost of a
+// single gemm1 accumulator buffer (2 x 256 columns fill TMEM) and fewer pipeline stages.
+template <bool kGemm1, int kN>
 struct Cfg {
-  static constexpr int kStages = kGemm1 ? 4 : 7;
+  static_assert(kN == 128 || kN == 256, "tile rows");
+  static constexpr int kStages = kGemm1 ? (kN == 128 ? 4 : 3) : (kN == 128 ? 7 : 4);
   static constexpr int kABytes = (kGemm1 ? 2 : 1) * kSlab * kBlockK * 2;
-  static constexpr int kBBytes = kTileRows * kBlockK * 2;
+  static constexpr int kBBytes = kN * kBlockK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  // gemm1 transposes its 16-bit tile through shared memory; gemm2 writes f32 from registers.
-  static constexpr int kStagingBytes = kGemm1 ? kTileRows * kSlab * 2 : 0;
-  static constexpr int kAccCols = kGemm1 ? 2 * kSlab : kSlab;  // per accumulator buffer
-  static constexpr int kTmemCols = 2 * kAccCols;                // double-buffered
+  // gemm1 transposes 64 token columns at a time through shared memory; gemm2 writes f32 rows
+  // straight from registers.
+  static constexpr int kPassCols = 64;
+  static constexpr int kStagingBytes = kGemm1 ? kPassCols * kSlab * 2 : 0;
+  static constexpr int kAccCols = kGemm1 ? 2 * kN : kN;  // per accumulator buffer
+  static constexpr int kAccBufs = (kGemm1 && kN == 256) ? 1 : 2;
+  static constexpr int kTmemCols = kAccBufs * kAccCols;
   static constexpr int kSmemBytes = kStages * kStageBytes + kStagingBytes + 1024;
 };
 
@@ -77,20 +85,30 @@ struct Unit {
 
 __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
 
-template <bool kGemm1>
+template <bool kGemm1, int kN>
 __device__ __forceinline__ bool decode_unit(const KParams& p, int u, Unit& U) {
-  U.slab = u % p.n_slabs;
-  const int q = u / p.n_slabs;
   if (p.mode == kSorted) {
-    const Tile t = p.tiles[q];
+    // Units of expert e occupy [n_slabs*first, n_slabs*(first+count)), ordered slab-major:
+    // the `count` tiles of one (expert, weight slab) are adjacent, so they run at the same time
+    // on neighbouring CTAs and can share the slab's weights through L2.  Tile u / n_slabs
+    // always lies in the range of the unit's expert.
+    const Tile owner = p.tiles[u / p.n_slabs];
+    const int local = u - p.n_slabs * owner.first;
+    U.slab = local / owner.count;
+    const Tile t = p.tiles[owner.first + local % owner.count];
     U.e = t.e;
     U.row0 = t.row0;
     U.nrows = t.nrows;
   } else if (p.mode == kDense) {
+    // One expert over all rows, slab-major: the row tiles of a weight slab are adjacent.
+    const int n_tiles = (p.dense_rows + kN - 1) / kN;
+    U.slab = u / n_tiles;
     U.e = 0;
-    U.row0 = q * kTileRows;
-    U.nrows = min(kTileRows, p.dense_rows - U.row0);
+    U.row0 = (u % n_tiles) * kN;
+    U.nrows = min(kN, p.dense_rows - U.row0);
   } else {
+    U.slab = u % p.n_slabs;
+    const int q = u / p.n_slabs;
     const int e = p.topk_ids[q];
     if (e < 0 || e >= p.E) {
       if (e != -1) set_status(p.status, MOE_ERR_BAD_EXPERT_ID);
@@ -117,23 +135,23 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) 
   }
 }
 
-template <bool kGemm1, typename T>
+template <bool kGemm1, int kN, typename T>
 __global__ void __launch_bounds__(192, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmB, const KParams p) {
-  using C = Cfg<kGemm1>;
+  using C = Cfg<kGemm1, kN>;
   extern __shared__ uint8_t dsmem[];
   __shared__ __align__(8) uint64_t full_bar[C::kStages];
   __shared__ __align__(8) uint64_t empty_bar[C::kStages];
-  __shared__ __align__(8) uint64_t tfull_bar[2];
-  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ __align__(8) uint64_t tfull_bar[C::kAccBufs];
+  __shared__ __align__(8) uint64_t tempty_bar[C::kAccBufs];
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
   __shared__ int s_n_units;
-  __shared__ int ent_col[kTileRows];
-  __shared__ int ent_dst[kTileRows];
-  __shared__ float col_scale[kTileRows];
+  __shared__ int ent_col[kGemm1 ? kN : 1];
+  __shared__ int ent_dst[kN];
+  __shared__ float col_scale[kGemm1 ? 1 : kN];
 
   // 1024-byte alignment for the 128-byte swizzle atoms.
   const uint32_t raw = smem_u32(dsmem);
@@ -143,25 +161,18 @@ __global__ void __launch_bounds__(192, 1)
   const int lane = threadIdx.x & 31;
   volatile int* abort_flag = &s_abort;
 
+  // Prologue that touches no global memory: it overlaps the previous kernel's tail.
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < C::kAccBufs; ++a) {
       mbar_init(&tfull_bar[a], 1);
       mbar_init(&tempty_bar[a], 128);
     }
     mbar_init(&drain_bar, 1);
     s_abort = 0;
-    int n = 0;
-    if (p.mode == kSorted)
-      n = (*p.n_tiles) * p.n_slabs;
-    else if (p.mode == kDirect)
-      n = p.P * p.n_slabs;
-    else
-      n = ((p.dense_rows + kTileRows - 1) / kTileRows) * p.n_slabs;
-    s_n_units = n;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -171,6 +182,18 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 1) {
     tmem_alloc(&s_tmem_base, C::kTmemCols);
     tmem_relinquish();
+  }
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    int n = 0;
+    if (p.mode == kSorted)
+      n = (*p.n_tiles) * p.n_slabs;
+    else if (p.mode == kDirect)
+      n = p.P * p.n_slabs;
+    else
+      n = ((p.dense_rows + kN - 1) / kN) * p.n_slabs;
+    s_n_units = n;
   }
   tc_fence_before();
   __syncthreads();
@@ -187,7 +210,7 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         Unit U;
-        if (!decode_unit<kGemm1>(p, u, U)) continue;
+        if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
         const uint32_t bytes = C::kABytes + U.n_mma * kBlockK * 2;
         const int wrow = U.e * p.w_rows_per_expert + U.slab * kSlab;
         for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -230,7 +253,7 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t smem_base = smem_u32(smem);
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         Unit U;
-        if (!decode_unit<kGemm1>(p, u, U)) continue;
+        if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.limit_ns, p.status)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * C::kAccCols);
@@ -249,7 +272,7 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
             umma_f16(d, sw128_kmajor_desc(sa + k * 32), bdesc, idesc, accum);
             if (kGemm1)
-              umma_f16(d + kSlab, sw128_kmajor_desc(sa + kSlab * kBlockK * 2 + k * 32), bdesc,
+              umma_f16(d + kN, sw128_kmajor_desc(sa + kSlab * kBlockK * 2 + k * 32), bdesc,
                        idesc, accum);
           }
           umma_commit(&empty_bar[stage]);
@@ -261,8 +284,10 @@ __global__ void __launch_bounds__(192, 1)
         }
         if (!ok) break;
         umma_commit(&tfull_bar[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        if (++acc == C::kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
       // Every MMA issued by this thread has completed once drain_bar flips.
       if (issued_any) {
@@ -279,22 +304,19 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t acc_phase = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
       Unit U;
-      if (!decode_unit<kGemm1>(p, u, U)) continue;
+      if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
       if constexpr (kGemm1) {
         // Output rows of this unit as (accumulator column, destination row) entries; in direct
         // mode a column is a token and each route of that token to this expert is an entry.
-        int n_ent;
-        if (p.mode == kDirect) {
-          n_ent = p.P;
-          if (et < p.P) {
-            ent_col[et] = p.topk_ids[et] == U.e ? et / p.top_k : -1;
-            ent_dst[et] = et;
-          }
-        } else {
-          n_ent = U.nrows;
-          if (et < U.nrows) {
-            ent_col[et] = et;
-            ent_dst[et] = U.row0 + et;
+        const bool direct = p.mode == kDirect;
+        const int n_ent = direct ? p.P : U.nrows;
+        for (int i = et; i < n_ent; i += 128) {
+          if (direct) {
+            ent_col[i] = p.topk_ids[i] == U.e ? i / p.top_k : -1;
+            ent_dst[i] = i;
+          } else {
+            ent_col[i] = i;
+            ent_dst[i] = U.row0 + i;
           }
         }
         const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.limit_ns, p.status);
@@ -303,56 +325,62 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t tb =
             tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
         T* stg = reinterpret_cast<T*>(staging);
-        for (int c0 = 0; c0 < U.n_mma; c0 += 16) {
-          float g[16], v[16];
-          tmem_ld2_x16(tb + c0, tb + kSlab + c0, g, v);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float h = __fdividef(g[j], 1.0f + __expf(-g[j])) * v[j];
-            stg[(c0 + j) * kSlab + row] = DT<T>::from_f(h);
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(&tempty_bar[acc]);
-        named_bar_sync(1, 128);
-        // 16-byte stores of whole output rows: entry en, chunk ch of 8 columns.
         T* out = static_cast<T*>(p.out);
         const int width = min(kSlab, p.n_out - U.slab * kSlab);
         const int nch = width / 8;
-        for (int idx = et; idx < n_ent * 16; idx += 128) {
-          const int en = idx >> 4, ch = idx & 15;
-          if (ch >= nch) continue;
-          const int col = ent_col[en];
-          if (col < 0) continue;
-          const uint4 val = *reinterpret_cast<const uint4*>(stg + col * kSlab + ch * 8);
-          *reinterpret_cast<uint4*>(out + (int64_t)ent_dst[en] * p.n_out + U.slab * kSlab +
-                                    ch * 8) = val;
+        for (int c0 = 0; c0 < U.n_mma; c0 += C::kPassCols) {
+          const int c1 = min(U.n_mma, c0 + C::kPassCols);
+          for (int c = c0; c < c1; c += 16) {
+            float g[16], v[16];
+            tmem_ld2_x16(tb + c, tb + kN + c, g, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float h = __fdividef(g[j], 1.0f + __expf(-g[j])) * v[j];
+              stg[(c - c0 + j) * kSlab + row] = DT<T>::from_f(h);
+            }
+          }
+          if (c1 == U.n_mma) {  // every TMEM column of this unit has been read
+            tc_fence_before();
+            mbar_arrive(&tempty_bar[acc]);
+          }
+          named_bar_sync(1, 128);
+          // 16-byte stores of whole output rows: entry en, chunk ch of 8 columns.
+          const int en_lo = direct ? 0 : c0, en_hi = direct ? n_ent : min(n_ent, c1);
+          for (int idx = et; idx < (en_hi - en_lo) * 16; idx += 128) {
+            const int en = en_lo + (idx >> 4), ch = idx & 15;
+            if (ch >= nch) continue;
+            const int col = ent_col[en];
+            if (col < c0 || col >= c1) continue;
+            const uint4 val = *reinterpret_cast<const uint4*>(stg + (col - c0) * kSlab + ch * 8);
+            *reinterpret_cast<uint4*>(out + (int64_t)ent_dst[en] * p.n_out + U.slab * kSlab +
+                                      ch * 8) = val;
+          }
+          named_bar_sync(1, 128);
         }
-        named_bar_sync(1, 128);
       } else {
         // Each accumulator column (token row) goes to at most one f32 output row, scaled by its
         // route weight; thread `row` owns output column slab*128 + row, so a warp stores one
         // 128-byte line per column.
-        if (et < U.n_mma) {
+        for (int i = et; i < U.n_mma; i += 128) {
           int dst = -1;
           float sc = 0.0f;
           if (p.mode == kSorted) {
-            if (et < U.nrows) {
-              dst = U.row0 + et;
+            if (i < U.nrows) {
+              dst = U.row0 + i;
               const int sid = p.sorted_ids[dst];
               sc = sid >= 0 ? p.topk_w[sid] : 0.0f;
             }
           } else if (p.mode == kDirect) {
-            if (et < p.P && p.topk_ids[et] == U.e) {
-              dst = et;
-              sc = p.topk_w[et];
+            if (i < p.P && p.topk_ids[i] == U.e) {
+              dst = i;
+              sc = p.topk_w[i];
             }
-          } else if (et < U.nrows) {
-            dst = U.row0 + et;
+          } else if (i < U.nrows) {
+            dst = U.row0 + i;
             sc = 1.0f;
           }
-          ent_dst[et] = dst;
-          col_scale[et] = sc;
+          ent_dst[i] = dst;
+          col_scale[i] = sc;
         }
         const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.limit_ns, p.status);
         if (!named_bar_and(1, 128, got)) break;
@@ -375,8 +403,10 @@ __global__ void __launch_bounds__(192, 1)
         mbar_arrive(&tempty_bar[acc]);
         named_bar_sync(1, 128);
       }
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      if (++acc == C::kAccBufs) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
     }
   }
 
@@ -424,28 +454,36 @@ bool make_map(CUtensorMap* m, int dtype, const void* base, uint64_t inner, uint6
   return r == CUDA_SUCCESS;
 }
 
-template <bool kGemm1, typename T>
-cudaError_t launch_typed(const GemmCall& c, const KParams& kp, int grid, cudaStream_t s) {
+template <bool kGemm1, int kN, typename T>
+cudaError_t launch_typed(const GemmCall& c, const KParams& kp, int grid, cudaStream_t s,
+                         bool pdl) {
+  using C = Cfg<kGemm1, kN>;
   CUtensorMap tmW, tmB;
   const uint64_t w_rows = (uint64_t)c.E * (uint64_t)kp.w_rows_per_expert;
   if (!make_map(&tmW, c.dtype, c.w, (uint64_t)c.K, w_rows, kSlab)) return cudaErrorInvalidValue;
   if (!make_map(&tmB, c.dtype, c.b, (uint64_t)c.K, (uint64_t)c.b_rows, 16))
     return cudaErrorInvalidValue;
-  auto kern = moe_gemm_kernel<kGemm1, T>;
-  static bool attr_set = false;  // one instantiation per (kGemm1, T): set once per process
+  auto kern = moe_gemm_kernel<kGemm1, kN, T>;
+  static bool attr_set = false;  // one per instantiation: set once per process
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<kGemm1>::kSmemBytes);
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<grid, 192, Cfg<kGemm1>::kSmemBytes, s>>>(tmW, tmB, kp);
-  return cudaGetLastError();
+  return launch_k(kern, dim3(grid), dim3(192), C::kSmemBytes, s, pdl, tmW, tmB, kp);
+}
+
+template <bool kGemm1, typename T>
+cudaError_t launch_rows(const GemmCall& c, const KParams& kp, int grid, cudaStream_t s,
+                        bool pdl) {
+  return c.tile_rows == 256 ? launch_typed<kGemm1, 256, T>(c, kp, grid, s, pdl)
+                            : launch_typed<kGemm1, 128, T>(c, kp, grid, s, pdl);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s) {
+cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   KParams kp;
   kp.mode = c.mode;
   kp.K = c.K;
@@ -467,23 +505,24 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s) {
   kp.status = c.status;
   kp.limit_ns = wait_limit_ns();
 
+  if (c.tile_rows != 128 && c.tile_rows != 256) return cudaErrorInvalidValue;
   long long upper = 0;
   if (c.mode == kSorted)
     upper = (long long)c.max_tiles * kp.n_slabs;
   else if (c.mode == kDirect)
     upper = (long long)c.P * kp.n_slabs;
   else
-    upper = (long long)((c.dense_rows + kTileRows - 1) / kTileRows) * kp.n_slabs;
+    upper = (long long)((c.dense_rows + c.tile_rows - 1) / c.tile_rows) * kp.n_slabs;
   if (upper <= 0 || c.b_rows <= 0) return cudaSuccess;
   const int sms = num_sms();
   const int grid = (int)(upper < sms ? upper : sms);
 
   if (c.gemm1) {
-    return c.dtype == MOE_BF16 ? launch_typed<true, __nv_bfloat16>(c, kp, grid, s)
-                               : launch_typed<true, __half>(c, kp, grid, s);
+    return c.dtype == MOE_BF16 ? launch_rows<true, __nv_bfloat16>(c, kp, grid, s, pdl)
+                               : launch_rows<true, __half>(c, kp, grid, s, pdl);
   }
-  return c.dtype == MOE_BF16 ? launch_typed<false, __nv_bfloat16>(c, kp, grid, s)
-                             : launch_typed<false, __half>(c, kp, grid, s);
+  return c.dtype == MOE_BF16 ? launch_rows<false, __nv_bfloat16>(c, kp, grid, s, pdl)
+                             : launch_rows<false, __half>(c, kp, grid, s, pdl);
 }
 
 }  // namespace gb300moe

@@ -18,6 +18,16 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// ---- programmatic dependent launch ------------------------------------------------------------
+// Every kernel of the path calls pdl_wait() before it touches global memory that an earlier
+// kernel of the stream writes or reads, and pdl_trigger() only after that wait, so when kernel
+// X+1 starts early, every kernel before X has completed.  Both are no-ops for a kernel launched
+// without the programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- mbarrier --------------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)

@@ -4,6 +4,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace gb300moe {
 
@@ -51,6 +52,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
                  const float* __restrict__ gating, const float* __restrict__ bias,
                  int32_t* __restrict__ ids, float* __restrict__ wout) {
   __shared__ float s_gscore[kWarpsPerBlock][32];
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
   const int t = blockIdx.x * kWarpsPerBlock + wib;
@@ -194,29 +197,28 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 
 template <int VPL>
 cudaError_t launch_vpl(const moe_problem_t& p, const float* gating, const float* bias,
-                       int32_t* ids, float* w, cudaStream_t s) {
+                       int32_t* ids, float* w, cudaStream_t s, bool pdl) {
   const int G = p.num_expert_group > 1 ? p.num_expert_group : 1;
   const int keepG = G > 1 ? p.topk_group : 1;
   const int blocks = (p.T + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  route_kernel<VPL><<<blocks, kWarpsPerBlock * 32, 0, s>>>(
-      p.T, p.E, p.top_k, p.scoring, p.renormalize, G, keepG, p.routed_scaling_factor, gating,
-      bias, ids, w);
-  return cudaGetLastError();
+  return launch_k(route_kernel<VPL>, dim3(blocks), dim3(kWarpsPerBlock * 32), 0, s, pdl, p.T,
+                  p.E, p.top_k, p.scoring, p.renormalize, G, keepG, p.routed_scaling_factor,
+                  gating, bias, ids, w);
 }
 
 }  // namespace
 
 cudaError_t launch_route(const moe_problem_t& p, const float* gating, const float* bias,
-                         int32_t* ids, float* w, cudaStream_t s) {
+                         int32_t* ids, float* w, cudaStream_t s, bool pdl) {
   if (p.T == 0) return cudaSuccess;
   const int need = (p.E + 31) / 32;
-  if (need <= 1) return launch_vpl<1>(p, gating, bias, ids, w, s);
-  if (need <= 2) return launch_vpl<2>(p, gating, bias, ids, w, s);
-  if (need <= 4) return launch_vpl<4>(p, gating, bias, ids, w, s);
-  if (need <= 8) return launch_vpl<8>(p, gating, bias, ids, w, s);
-  if (need <= 12) return launch_vpl<12>(p, gating, bias, ids, w, s);
-  if (need <= 16) return launch_vpl<16>(p, gating, bias, ids, w, s);
-  return launch_vpl<32>(p, gating, bias, ids, w, s);
+  if (need <= 1) return launch_vpl<1>(p, gating, bias, ids, w, s, pdl);
+  if (need <= 2) return launch_vpl<2>(p, gating, bias, ids, w, s, pdl);
+  if (need <= 4) return launch_vpl<4>(p, gating, bias, ids, w, s, pdl);
+  if (need <= 8) return launch_vpl<8>(p, gating, bias, ids, w, s, pdl);
+  if (need <= 12) return launch_vpl<12>(p, gating, bias, ids, w, s, pdl);
+  if (need <= 16) return launch_vpl<16>(p, gating, bias, ids, w, s, pdl);
+  return launch_vpl<32>(p, gating, bias, ids, w, s, pdl);
 }
 
 }  // namespace gb300moe

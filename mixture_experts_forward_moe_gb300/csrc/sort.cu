@@ -12,6 +12,7 @@
 // so every route lands at a position that depends only on topk_ids (bit-exact and
 // deterministic).
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace gb300moe {
 
@@ -23,6 +24,8 @@ __global__ void __launch_bounds__(kChunk)
     sort_count_kernel(const int32_t* __restrict__ ids, int P, int E,
                       int32_t* __restrict__ chunk_counts, int* status) {
   extern __shared__ int hist[];
+  pdl_wait();
+  pdl_trigger();
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   const int r = blockIdx.x * kChunk + threadIdx.x;
@@ -70,6 +73,8 @@ __global__ void __launch_bounds__(1024)
                      int32_t* __restrict__ tile_expert, int64_t tile_len) {
   __shared__ int warp_tot[32];
   __shared__ int s_total;
+  pdl_wait();
+  pdl_trigger();
   const int e = threadIdx.x;
   int total = 0;
   if (e < E) {
@@ -110,6 +115,8 @@ __global__ void __launch_bounds__(kChunk)
                         const int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
                         int32_t* __restrict__ inv_route) {
   __shared__ int s_ids[kChunk];
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x * kChunk + threadIdx.x;
   int e = r < P ? ids[r] : -1;
   if (e < -1 || e >= E) e = -1;  // reported by the count kernel; treated as padding
@@ -127,14 +134,16 @@ __global__ void __launch_bounds__(kChunk)
   inv_route[r] = pos;
 }
 
-// Tiles of at most kTileRows rows over each expert segment [offsets[e], offsets[e+1]).
+// Tiles of at most tile_rows rows over each expert segment [offsets[e], offsets[e+1]).
 __global__ void __launch_bounds__(1024)
     build_tiles_kernel(int E, const int32_t* __restrict__ offsets, Tile* __restrict__ tiles,
-                       int* __restrict__ n_tiles) {
+                       int* __restrict__ n_tiles, int tile_rows) {
   __shared__ int warp_tot[32];
+  pdl_wait();
+  pdl_trigger();
   const int e = threadIdx.x;
   const int seg = e < E ? offsets[e + 1] - offsets[e] : 0;
-  const int nt = (seg + kTileRows - 1) / kTileRows;
+  const int nt = (seg + tile_rows - 1) / tile_rows;
   const int incl = block_inclusive_scan(nt, warp_tot);
   const int base = incl - nt;
   if (e < E) {
@@ -142,13 +151,133 @@ __global__ void __launch_bounds__(1024)
     for (int i = 0; i < nt; ++i) {
       Tile t;
       t.e = e;
-      t.row0 = r0 + i * kTileRows;
-      t.nrows = min(kTileRows, seg - i * kTileRows);
-      t.pad = 0;
+      t.row0 = r0 + i * tile_rows;
+      t.nrows = min(tile_rows, seg - i * tile_rows);
+      t.first = base;
+      t.count = nt;
+      t.pad0 = t.pad1 = t.pad2 = 0;
       tiles[base + i] = t;
     }
   }
   if (e == E - 1) *n_tiles = incl;
+}
+
+// The whole sort in one CTA of 1024 threads (32 warps), for up to kFusedSortMaxRoutes routes:
+// warp w owns the contiguous routes [w*per, (w+1)*per).  Pass A counts each warp's routes per
+// expert (lanes with the same id found with __match_any_sync); a per-expert prefix over the
+// warps, after the block scan of the padded totals, turns the counts into each warp's first
+// position in every expert segment; pass B walks the same routes in the same order and places
+// each one at that base plus its rank among the equal ids before it.  The result is the same
+// stable order as the chunked kernels, from a single launch.  With `tiles` it also writes the
+// GEMM tile list over the segments.
+constexpr int kFusedSortMaxRoutes = 65536;
+
+__global__ void __launch_bounds__(1024)
+    sort_fused_kernel(const int32_t* __restrict__ ids, int P, int E, int block_m, int64_t cap,
+                      int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                      int32_t* __restrict__ sorted_ids, int32_t* __restrict__ tile_expert,
+                      int64_t tile_len, int32_t* __restrict__ inv_route, Tile* __restrict__ tiles,
+                      int* __restrict__ n_tiles, int tile_rows, Tile* __restrict__ tiles2,
+                      int* __restrict__ n_tiles2, int tile_rows2, int* status) {
+  extern __shared__ int warp_cnt[];  // [32][E]
+  __shared__ int warp_tot[32];
+  __shared__ int s_total;
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  for (int i = tid; i < 32 * E; i += blockDim.x) warp_cnt[i] = 0;
+  __syncthreads();
+  int* wc = warp_cnt + w * E;
+  const int per = (P + 31) / 32;
+  const int r0 = w * per, r1 = min(P, r0 + per);
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int b = r0; b < r1; b += 32) {  // pass A: per-warp histogram
+    const int r = b + lane;
+    int e = -1;
+    if (r < r1) {
+      e = ids[r];
+      if (e < -1 || e >= E) {
+        set_status(status, MOE_ERR_BAD_EXPERT_ID);
+        e = -1;
+      }
+    }
+    const unsigned m = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(m) - 1) wc[e] += __popc(m);
+    __syncwarp();
+  }
+  __syncthreads();
+  int total = 0;
+  if (tid < E)
+    for (int ww = 0; ww < 32; ++ww) total += warp_cnt[ww * E + tid];
+  const int padded = tid < E ? (total + block_m - 1) / block_m * block_m : 0;
+  const int incl = block_inclusive_scan(padded, warp_tot);
+  const int excl = incl - padded;
+  if (tid < E) {
+    counts[tid] = total;
+    offsets[tid] = excl;
+    int base = excl;
+    for (int ww = 0; ww < 32; ++ww) {
+      const int c = warp_cnt[ww * E + tid];
+      warp_cnt[ww * E + tid] = base;
+      base += c;
+    }
+  }
+  if (tid == E - 1) {
+    offsets[E] = incl;
+    s_total = incl;
+  }
+  __syncthreads();
+  for (int b = r0; b < r1; b += 32) {  // pass B: stable scatter
+    const int r = b + lane;
+    int e = -1;
+    if (r < r1) {
+      e = ids[r];
+      if (e < -1 || e >= E) e = -1;
+    }
+    const unsigned m = __match_any_sync(0xffffffffu, e);
+    const int base = e >= 0 ? wc[e] : 0;
+    __syncwarp();
+    if (r < r1) {
+      if (e >= 0) {
+        const int pos = base + __popc(m & lt_mask);
+        sorted_ids[pos] = r;
+        inv_route[r] = pos;
+      } else {
+        inv_route[r] = -1;
+      }
+    }
+    if (e >= 0 && lane == __ffs(m) - 1) wc[e] = base + __popc(m);
+    __syncwarp();
+  }
+  const int tot = s_total;
+  if (tid < E)
+    for (int q = excl + total; q < excl + padded; ++q) sorted_ids[q] = -1;
+  for (int64_t q = tot + tid; q < cap; q += blockDim.x) sorted_ids[q] = -1;
+  if (tile_expert) {
+    if (tid < E)
+      for (int i = excl / block_m; i < (excl + padded) / block_m; ++i) tile_expert[i] = tid;
+    for (int64_t i = tot / block_m + tid; i < tile_len; i += blockDim.x) tile_expert[i] = -1;
+  }
+  for (int list = 0; list < 2; ++list) {  // up to two tile lists of different heights
+    Tile* tl = list == 0 ? tiles : tiles2;
+    if (!tl) continue;
+    const int rows = list == 0 ? tile_rows : tile_rows2;
+    __syncthreads();  // warp_tot is reused by every scan
+    const int nt = (padded + rows - 1) / rows;
+    const int tincl = block_inclusive_scan(nt, warp_tot);
+    const int tbase = tincl - nt;
+    for (int i = 0; i < nt; ++i) {
+      Tile t;
+      t.e = tid;
+      t.row0 = excl + i * rows;
+      t.nrows = min(rows, padded - i * rows);
+      t.first = tbase;
+      t.count = nt;
+      t.pad0 = t.pad1 = t.pad2 = 0;
+      tl[tbase + i] = t;
+    }
+    if (tid == E - 1) *(list == 0 ? n_tiles : n_tiles2) = tincl;
+  }
 }
 
 // a_sorted[p, :] = hidden[sorted_ids[p] / top_k, :] for p < offsets[E]; padding rows are zero.
@@ -156,6 +285,8 @@ __global__ void __launch_bounds__(128)
     permute_kernel(int top_k, int H, const uint16_t* __restrict__ hidden,
                    const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ offsets,
                    int E, uint16_t* __restrict__ a_sorted) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t rows = offsets[E];
   const int nvec = H / 8;
   for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
@@ -171,97 +302,143 @@ __global__ void __launch_bounds__(128)
 }
 
 // out[t, :] = round(sum_j y[inv[t*K+j], :] + shared[t, :]): f32 rows in, one rounding out.
+// A thread owns 4 columns; the route rows are loaded 8 at a time before they are summed, in j
+// order, so the sum is the same on every run.
 template <typename T>
 __global__ void __launch_bounds__(128)
     combine_kernel(int K, int H, const float* __restrict__ y, const int32_t* __restrict__ inv,
                    const int32_t* __restrict__ ids, const float* __restrict__ shared,
                    T* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.y;
-  const int v = blockIdx.x * blockDim.x + threadIdx.x;  // 8 columns per thread
-  if (v >= H / 8) return;
-  float acc[8];
+  const int v = blockIdx.x * blockDim.x + threadIdx.x;  // 4 columns per thread
+  if (v >= H / 4) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j0 = 0; j0 < K; j0 += 8) {
+    float4 row[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-  for (int j = 0; j < K; ++j) {
-    const int r = t * K + j;
-    if (ids && ids[r] < 0) continue;
-    const int p = inv ? inv[r] : r;
-    if (p < 0) continue;
-    const float4* src = reinterpret_cast<const float4*>(y + (int64_t)p * H) + 2 * v;
-    const float4 a = src[0], b = src[1];
-    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    for (int jj = 0; jj < 8; ++jj) {
+      const int j = j0 + jj;
+      int p = -1;
+      if (j < K) {
+        const int r = t * K + j;
+        p = (ids && ids[r] < 0) ? -1 : (inv ? inv[r] : r);
+      }
+      row[jj] = p >= 0 ? reinterpret_cast<const float4*>(y + (int64_t)p * H)[v]
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      acc.x += row[jj].x;
+      acc.y += row[jj].y;
+      acc.z += row[jj].z;
+      acc.w += row[jj].w;
+    }
   }
   if (shared) {
-    const float4* src = reinterpret_cast<const float4*>(shared + (int64_t)t * H) + 2 * v;
-    const float4 a = src[0], b = src[1];
-    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    const float4 sh = reinterpret_cast<const float4*>(shared + (int64_t)t * H)[v];
+    acc.x += sh.x;
+    acc.y += sh.y;
+    acc.z += sh.z;
+    acc.w += sh.w;
   }
-  uint4 o;
-  T* oe = reinterpret_cast<T*>(&o);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) oe[i] = DT<T>::from_f(acc[i]);
-  reinterpret_cast<uint4*>(out + (int64_t)t * H)[v] = o;
+  T o[4] = {DT<T>::from_f(acc.x), DT<T>::from_f(acc.y), DT<T>::from_f(acc.z),
+            DT<T>::from_f(acc.w)};
+  *reinterpret_cast<uint2*>(out + (int64_t)t * H + 4 * v) = *reinterpret_cast<const uint2*>(o);
 }
 
 }  // namespace
 
-cudaError_t launch_align_sort(const moe_problem_t& p, int block_m, const int32_t* ids,
+bool fused_sort_fits(const moe_problem_t& p) {
+  return (int64_t)p.T * p.top_k <= kFusedSortMaxRoutes && p.E <= 1024;
+}
+
+cudaError_t launch_sort_fused(const moe_problem_t& p, int block_m, const int32_t* ids,
                               int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
-                              int64_t cap, int32_t* tile_expert, int32_t* inv_route,
-                              int32_t* chunk_scratch, int* status, cudaStream_t s) {
+                              int64_t cap, int32_t* tile_expert, int32_t* inv_route, Tile* tiles,
+                              int* n_tiles, int tile_rows, Tile* tiles2, int* n_tiles2,
+                              int tile_rows2, int* status, cudaStream_t s, bool pdl) {
+  const int P = p.T * p.top_k;
+  const size_t smem = sizeof(int) * 32 * (size_t)p.E;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(sort_fused_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(sizeof(int) * 32 * 1024));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int64_t tile_len = (cap + block_m - 1) / block_m;
+  return launch_k(sort_fused_kernel, dim3(1), dim3(1024), smem, s, pdl, ids, P, p.E, block_m,
+                  cap, counts, offsets, sorted_ids, tile_expert, tile_len, inv_route, tiles,
+                  n_tiles, tile_rows, tiles2, n_tiles2, tile_rows2, status);
+}
+
+cudaError_t launch_align_sort_chunked(const moe_problem_t& p, int block_m, const int32_t* ids,
+                                      int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
+                                      int64_t cap, int32_t* tile_expert, int32_t* inv_route,
+                                      int32_t* chunk_scratch, int* status, cudaStream_t s,
+                                      bool pdl) {
   const int P = p.T * p.top_k;
   const int n_chunks = (P + kChunk - 1) / kChunk;
   const int64_t tile_len = (cap + block_m - 1) / block_m;
   if (n_chunks > 0) {
-    sort_count_kernel<<<n_chunks, kChunk, sizeof(int) * p.E, s>>>(ids, P, p.E, chunk_scratch,
-                                                                   status);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_k(sort_count_kernel, dim3(n_chunks), dim3(kChunk),
+                               sizeof(int) * p.E, s, pdl, ids, P, p.E, chunk_scratch, status);
     if (err != cudaSuccess) return err;
+    pdl = true;
   }
-  sort_scan_kernel<<<1, 1024, 0, s>>>(n_chunks, p.E, block_m, cap, chunk_scratch, counts,
-                                      offsets, sorted_ids, tile_expert, tile_len);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_k(sort_scan_kernel, dim3(1), dim3(1024), 0, s, pdl, n_chunks, p.E,
+                             block_m, cap, chunk_scratch, counts, offsets, sorted_ids,
+                             tile_expert, tile_len);
   if (err != cudaSuccess || n_chunks == 0) return err;
-  sort_scatter_kernel<<<n_chunks, kChunk, 0, s>>>(ids, P, p.E, chunk_scratch, offsets,
-                                                  sorted_ids, inv_route);
-  return cudaGetLastError();
+  return launch_k(sort_scatter_kernel, dim3(n_chunks), dim3(kChunk), 0, s, true, ids, P, p.E,
+                  static_cast<const int32_t*>(chunk_scratch),
+                  static_cast<const int32_t*>(offsets), sorted_ids, inv_route);
+}
+
+cudaError_t launch_align_sort(const moe_problem_t& p, int block_m, const int32_t* ids,
+                              int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
+                              int64_t cap, int32_t* tile_expert, int32_t* inv_route,
+                              int32_t* chunk_scratch, int* status, cudaStream_t s, bool pdl) {
+  if (fused_sort_fits(p))
+    return launch_sort_fused(p, block_m, ids, counts, offsets, sorted_ids, cap, tile_expert,
+                             inv_route, nullptr, nullptr, kTileRows, nullptr, nullptr, kTileRows,
+                             status, s, pdl);
+  return launch_align_sort_chunked(p, block_m, ids, counts, offsets, sorted_ids, cap,
+                                   tile_expert, inv_route, chunk_scratch, status, s, pdl);
 }
 
 cudaError_t launch_build_tiles(int E, const int32_t* offsets, Tile* tiles, int* n_tiles,
-                               cudaStream_t s) {
-  build_tiles_kernel<<<1, 1024, 0, s>>>(E, offsets, tiles, n_tiles);
-  return cudaGetLastError();
+                               int tile_rows, cudaStream_t s, bool pdl) {
+  return launch_k(build_tiles_kernel, dim3(1), dim3(1024), 0, s, pdl, E, offsets, tiles,
+                  n_tiles, tile_rows);
 }
 
 cudaError_t launch_permute(int dtype, int top_k, int H, const void* hidden,
                            const int32_t* sorted_ids, const int32_t* offsets, int E, int64_t cap,
-                           void* a_sorted, cudaStream_t s) {
+                           void* a_sorted, cudaStream_t s, bool pdl) {
   (void)dtype;  // a row copy: the element type does not matter
   if (cap <= 0) return cudaSuccess;
   const int64_t grid = cap < 4096 ? cap : 4096;
-  permute_kernel<<<(int)grid, 128, 0, s>>>(top_k, H, static_cast<const uint16_t*>(hidden),
-                                           sorted_ids, offsets, E,
-                                           static_cast<uint16_t*>(a_sorted));
-  return cudaGetLastError();
+  return launch_k(permute_kernel, dim3((int)grid), dim3(128), 0, s, pdl, top_k, H,
+                  static_cast<const uint16_t*>(hidden), sorted_ids, offsets, E,
+                  static_cast<uint16_t*>(a_sorted));
 }
 
 cudaError_t launch_combine(const moe_problem_t& p, const void* y_route,
                            const int32_t* inv_route, const int32_t* ids, const void* shared_out,
-                           void* out, cudaStream_t s) {
+                           void* out, cudaStream_t s, bool pdl) {
   if (p.T == 0) return cudaSuccess;
-  dim3 grid((p.H / 8 + 127) / 128, p.T);
-  if (p.dtype == MOE_BF16) {
-    combine_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(
-        p.top_k, p.H, static_cast<const float*>(y_route), inv_route, ids,
-        static_cast<const float*>(shared_out), static_cast<__nv_bfloat16*>(out));
-  } else {
-    combine_kernel<__half><<<grid, 128, 0, s>>>(
-        p.top_k, p.H, static_cast<const float*>(y_route), inv_route, ids,
-        static_cast<const float*>(shared_out), static_cast<__half*>(out));
-  }
-  return cudaGetLastError();
+  dim3 grid((p.H / 4 + 127) / 128, p.T);
+  const float* y = static_cast<const float*>(y_route);
+  const float* sh = static_cast<const float*>(shared_out);
+  if (p.dtype == MOE_BF16)
+    return launch_k(combine_kernel<__nv_bfloat16>, grid, dim3(128), 0, s, pdl, p.top_k, p.H, y,
+                    inv_route, ids, sh, static_cast<__nv_bfloat16*>(out));
+  return launch_k(combine_kernel<__half>, grid, dim3(128), 0, s, pdl, p.top_k, p.H, y,
+                  inv_route, ids, sh, static_cast<__half*>(out));
 }
 
 }  // namespace gb300moe

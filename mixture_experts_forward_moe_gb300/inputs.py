@@ -70,6 +70,19 @@ WORKLOADS = {
         bias_std=0.1, routed_scaling_factor=2.827, S=18432),
 }
 
+# Small cases of the same kernels for hardware-counter captures, which must stay at a few GB on
+# the device: the DeepSeek-V3 expert shapes and routing with 32 experts (about 128 routed rows
+# per expert, skewed by the correction bias), 2.8 GB of weights.
+PROBES = {
+    "prefill-probe-e32-t512": Workload(
+        "prefill-probe-e32-t512", T=512, H=7168, E=32, F=2048, top_k=8, scoring_func="sigmoid",
+        bias_std=0.1, num_expert_group=8, topk_group=4, routed_scaling_factor=2.5),
+}
+
+
+def workload(name: str) -> Workload:
+    return WORKLOADS[name] if name in WORKLOADS else PROBES[name]
+
 _CHUNK_ELEMS = 1 << 28  # f32 staging per draw: 1 GiB
 
 

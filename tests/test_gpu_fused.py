@@ -30,6 +30,10 @@ SMALL = [
     W("sorted-sigmoid-shared", T=96, H=256, E=24, F=96, top_k=4, scoring_func="sigmoid",
       bias_std=0.1, routed_scaling_factor=2.827, S=384),
     W("sorted-norenorm", T=50, H=128, E=10, F=64, top_k=3, renormalize=False),
+    W("sorted-wide-tiles", T=600, H=256, E=4, F=192, top_k=2),  # 256-row tiles, 2 per expert
+    W("sorted-wide-grouped-shared", T=400, H=192, E=16, F=128, top_k=4,
+      scoring_func="sigmoid", bias_std=0.1, num_expert_group=4, topk_group=2,
+      routed_scaling_factor=2.5, S=256),
 ]
 
 

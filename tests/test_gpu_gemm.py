@@ -21,6 +21,8 @@ GEMM_CASES = [
     (64, 8, 32, 192, 256, 16, 0.1, torch.bfloat16),    # padded segments, padding routes
     (40, 4, 12, 136, 72, 1, 0.0, torch.float16),       # K tail of 8, F < 128
     (9, 8, 64, 512, 96, 1, 0.0, torch.bfloat16),       # decode-like: 1-2 rows per expert
+    (800, 2, 3, 256, 136, 1, 0.0, torch.bfloat16),     # 256-row tiles, ~530 rows per expert
+    (260, 4, 8, 192, 128, 8, 0.05, torch.float16),     # 256-row tiles with padded segments
 ]
 
 
