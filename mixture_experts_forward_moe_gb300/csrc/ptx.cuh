@@ -57,10 +57,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait: returns false (and raises *abort) when the phase has not completed within
-// limit_ns, or when another role has already raised *abort.
+// limit_ns, or when another role has already raised *abort.  A limit of 0 gives up at the first
+// poll that finds the phase incomplete (the test knob that exercises this path).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns, int* status) {
   if (mbar_try_wait(bar, parity)) return true;
+  if (limit_ns == 0) {
+    *abort = 1;
+    if (status) atomicCAS(status, 0, (int)MOE_ERR_TIMEOUT);
+    return false;
+  }
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
