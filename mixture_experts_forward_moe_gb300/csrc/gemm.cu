@@ -12,8 +12,9 @@
 //    up row i and computes SiLU(g)*u in f32 with no data exchange.
 //  * gemm2: the slab is 128 rows of w_down; the epilogue multiplies by the route weight.
 //  * Warp roles (192 threads, one CTA per SM, persistent over units):
-//      warp 0  TMA producer: weight boxes {64 x 128} and token boxes {64 x 16}, 128-byte
-//              swizzle, into a multi-stage shared-memory ring (mbarrier complete_tx);
+//      warp 0  TMA producer: weight boxes {64 x 128} and token boxes of 128, 64 and 16 rows
+//              (as few copies as the tile's rows allow), 128-byte swizzle, into a multi-stage
+//              shared-memory ring (mbarrier complete_tx);
 //      warp 1  MMA issuer: tcgen05.mma kind::f16, f32 accumulators in TMEM, double-buffered
 //              so the epilogue of one unit overlaps the K loop of the next;
 //      warps 2-5  epilogue: tcgen05.ld -> f32 math.  gemm1 rounds SiLU(g)*u once to bf16/f16,
@@ -138,7 +139,9 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) 
 template <bool kGemm1, int kN, typename T>
 __global__ void __launch_bounds__(192, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
-                    const __grid_constant__ CUtensorMap tmB, const KParams p) {
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmB64,
+                    const __grid_constant__ CUtensorMap tmB128, const KParams p) {
   using C = Cfg<kGemm1, kN>;
   extern __shared__ uint8_t dsmem[];
   __shared__ __align__(8) uint64_t full_bar[C::kStages];
@@ -178,6 +181,8 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tmW);
     prefetch_tensormap(&tmB);
+    prefetch_tensormap(&tmB64);
+    prefetch_tensormap(&tmB128);
   }
   if (warp == 1) {
     tmem_alloc(&s_tmem_base, C::kTmemCols);
@@ -225,8 +230,14 @@ __global__ void __launch_bounds__(192, 1)
           tma_load_2d(sa, &tmW, &full_bar[stage], kx, wrow);
           if (kGemm1)
             tma_load_2d(sa + kSlab * kBlockK * 2, &tmW, &full_bar[stage], kx, wrow + p.n_out);
-          for (int j = 0; j < U.n_mma / 16; ++j)
-            tma_load_2d(sb + j * 16 * kBlockK * 2, &tmB, &full_bar[stage], kx, U.row0 + 16 * j);
+          // Token rows in as few copies as possible: 128-, then 64-, then 16-row boxes.
+          int r = 0;
+          for (; r + 128 <= U.n_mma; r += 128)
+            tma_load_2d(sb + r * kBlockK * 2, &tmB128, &full_bar[stage], kx, U.row0 + r);
+          for (; r + 64 <= U.n_mma; r += 64)
+            tma_load_2d(sb + r * kBlockK * 2, &tmB64, &full_bar[stage], kx, U.row0 + r);
+          for (; r < U.n_mma; r += 16)
+            tma_load_2d(sb + r * kBlockK * 2, &tmB, &full_bar[stage], kx, U.row0 + r);
           ++issued;
           if (++stage == C::kStages) {
             stage = 0;
@@ -458,10 +469,12 @@ template <bool kGemm1, int kN, typename T>
 cudaError_t launch_typed(const GemmCall& c, const KParams& kp, int grid, cudaStream_t s,
                          bool pdl) {
   using C = Cfg<kGemm1, kN>;
-  CUtensorMap tmW, tmB;
+  CUtensorMap tmW, tmB, tmB64, tmB128;
   const uint64_t w_rows = (uint64_t)c.E * (uint64_t)kp.w_rows_per_expert;
   if (!make_map(&tmW, c.dtype, c.w, (uint64_t)c.K, w_rows, kSlab)) return cudaErrorInvalidValue;
-  if (!make_map(&tmB, c.dtype, c.b, (uint64_t)c.K, (uint64_t)c.b_rows, 16))
+  if (!make_map(&tmB, c.dtype, c.b, (uint64_t)c.K, (uint64_t)c.b_rows, 16) ||
+      !make_map(&tmB64, c.dtype, c.b, (uint64_t)c.K, (uint64_t)c.b_rows, 64) ||
+      !make_map(&tmB128, c.dtype, c.b, (uint64_t)c.K, (uint64_t)c.b_rows, 128))
     return cudaErrorInvalidValue;
   auto kern = moe_gemm_kernel<kGemm1, kN, T>;
   static bool attr_set = false;  // one per instantiation: set once per process
@@ -471,7 +484,8 @@ cudaError_t launch_typed(const GemmCall& c, const KParams& kp, int grid, cudaStr
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_k(kern, dim3(grid), dim3(192), C::kSmemBytes, s, pdl, tmW, tmB, kp);
+  return launch_k(kern, dim3(grid), dim3(192), C::kSmemBytes, s, pdl, tmW, tmB, tmB64, tmB128,
+                  kp);
 }
 
 template <bool kGemm1, typename T>

@@ -77,6 +77,11 @@ PROBES = {
     "prefill-probe-e32-t512": Workload(
         "prefill-probe-e32-t512", T=512, H=7168, E=32, F=2048, top_k=8, scoring_func="sigmoid",
         bias_std=0.1, num_expert_group=8, topk_group=4, routed_scaling_factor=2.5),
+    # about 256 rows per expert: several token tiles per expert, as in the T=4096 prefill
+    "prefill-probe-e32-t1024": Workload(
+        "prefill-probe-e32-t1024", T=1024, H=7168, E=32, F=2048, top_k=8,
+        scoring_func="sigmoid", bias_std=0.1, num_expert_group=8, topk_group=4,
+        routed_scaling_factor=2.5),
 }
 
 
