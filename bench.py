@@ -6,8 +6,10 @@ combine, shared expert when present) over one batch of seeded synthetic inputs t
 resident in HBM.  When a step streams more than twice the L2 in expert weights (every measured
 workload but the tiny one) nothing is flushed between steps; otherwise the L2 is flushed by a
 256 MiB write outside the timed events.
-Each step is timed with a CUDA event pair on the launching stream; the K step times are
-summed.  `value` is whole-job TFLOP/s with the TileOPs MoE page's FLOP count
+A step is one replay of a CUDA graph that holds one captured fused_moe_fwd call (its kernels
+and their programmatic dependencies), so the host issues one launch per step; `--eager` times
+the eager calls instead, and the eager time is reported beside it in any case.  Each step is
+timed with a CUDA event pair on the launching stream; the K step times are summed.  `value` is whole-job TFLOP/s with the TileOPs MoE page's FLOP count
 2*T*k*3*F*H (+ 2*T*3*S*H).
 
 Also reported: HBM GB/s over the algorithmic bytes, the roofline of the dominant kernel (its
@@ -301,8 +303,8 @@ def run_ours(args, w, ws_n, rank, local):
 
     dominant_candidates = ["gemm1", "gemm2"] + (["shared_gemm1", "shared_gemm2"] if w.S else [])
 
-    def timed_loop(profile_stages):
-        """K steps, each bracketed by an event pair on the launching stream; with
+    def timed_loop(fn, profile_stages):
+        """K steps of fn, each bracketed by an event pair on the launching stream; with
         profile_stages the library also records event pairs around those stages."""
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -312,7 +314,7 @@ def run_ours(args, w, ws_n, rank, local):
         for i in range(args.steps):
             do_flush()
             starts[i].record(stream)
-            step()
+            fn()
             ends[i].record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -320,15 +322,37 @@ def run_ours(args, w, ws_n, rank, local):
         B.profile_enable([])
         return [a.elapsed_time(b) for a, b in zip(starts, ends)], prof
 
+    # One fused call captured into a CUDA graph (its kernels and their programmatic
+    # dependencies): a replay costs the host one launch instead of one per kernel.
+    graph = None
+    if not args.eager:
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            step()
+        stream.wait_stream(cap)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        torch.cuda.synchronize()
+
+    def replay():
+        graph.replay()
+
+    headline = replay if graph is not None else step
     # The headline loop records no events inside a step: an event between two kernels would
     # stop the next one from starting early (programmatic dependent launch).
     clocks = ClockSampler(local) if rank == 0 else None
-    step_ms, prof_clean = timed_loop([])
+    step_ms, _ = timed_loop(headline, [])
     clk = clocks.stop() if clocks else None
     total_ms = float(sum(step_ms))
     max_ms = max_over_ranks(total_ms)
-    # The roofline loop: the same K steps with event pairs around the GEMM stages.
-    prof_step_ms, prof = timed_loop(dominant_candidates)
+    # The same K steps launched eagerly (one host launch per kernel), for comparison and for the
+    # launch count.
+    eager_ms, prof_clean = timed_loop(step, [])
+    # The roofline loop: the same K steps with event pairs around the GEMM stages (eager).
+    prof_step_ms, prof = timed_loop(step, dominant_candidates)
     st = B.get_device_status(wsp)
     if st != B.MOE_OK:
         raise RuntimeError(f"device status after timed steps: {B.status_string(st)}")
@@ -358,7 +382,6 @@ def run_ours(args, w, ws_n, rank, local):
     tensor["frac"] = tensor["achieved_tflops"] / bf16_sust
     roofline["tensor"] = tensor
     stages = {k: {"avg_ms": v[0] / v[1], "calls": v[1]} for k, v in prof.items() if v[1]}
-    stages["_roofline_loop_ms_per_step"] = statistics.mean(prof_step_ms)
 
     res = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws_n,
@@ -373,7 +396,11 @@ def run_ours(args, w, ws_n, rank, local):
                    "routed_scaling_factor": w.routed_scaling_factor,
                    "global_batch": w.T * ws_n, "parallelism": f"replicas x{ws_n}",
                    "l2": l2_note,
-                   "timing": "CUDA event pair per step on the launching stream; sum of K"},
+                   "timing": ("one CUDA-graph replay of the fused call per step"
+                              if graph is not None else "eager launches")
+                             + "; CUDA event pair per step on the launching stream; sum of K"},
+        "eager_ms_per_step": statistics.mean(eager_ms),
+        "roofline_loop_ms_per_step": statistics.mean(prof_step_ms),
         "ms_median": statistics.median(step_ms), "hbm_gbs": ab["total"] / (ms_per_step * 1e-3) / 1e9,
         "hbm_frac": ab["total"] / (ms_per_step * 1e-3) / 1e9 / hbm_gbs,
         "unique_experts": n_unique, "roofline": roofline, "gpu_launches": launches,
@@ -401,8 +428,14 @@ def run_ours(args, w, ws_n, rank, local):
         for i in range(n_e2e):
             do_flush()
             es[2 * i].record(stream)
-            B.fused_moe_fwd_host(h_hidden, h_gating, d["w_gate_up"], d["w_down"], out_host=h_out,
-                                 dev_bufs=bufs, workspace=wsp, **kw)
+            if graph is not None:  # copies in, the captured fused call, copy out
+                d["hidden_states"].copy_(h_hidden, non_blocking=True)
+                d["gating_output"].copy_(h_gating, non_blocking=True)
+                graph.replay()
+                h_out.copy_(out, non_blocking=True)
+            else:
+                B.fused_moe_fwd_host(h_hidden, h_gating, d["w_gate_up"], d["w_down"],
+                                     out_host=h_out, dev_bufs=bufs, workspace=wsp, **kw)
             es[2 * i + 1].record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -468,6 +501,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="time eager launches instead of a CUDA-graph replay of the fused call")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -257,7 +257,9 @@ uint64_t moe_set_wait_limit_ns(uint64_t limit_ns);
 /* ---------------------------------------------------------------------------------------- */
 
 /* Stages of fused_moe_fwd, in launch order: 0 route, 1 sort, 2 tiles, 3 permute, 4 gemm1,
- * 5 gemm2, 6 shared_gemm1, 7 shared_gemm2, 8 combine. */
+ * 5 gemm2, 6 shared_gemm1, 7 shared_gemm2, 8 combine.  The sort also writes the GEMM tile
+ * lists, so stage 2 launches nothing; stage 3 launches only for T > 128 (below that gemm1 reads
+ * hidden_states directly); stages 1-3 are skipped on the direct path (T <= 8). */
 #define MOE_NUM_STAGES 9
 
 /* Name of stage i (NULL when out of range). */

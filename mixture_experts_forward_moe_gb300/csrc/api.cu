@@ -133,7 +133,6 @@ Layout make_layout(const moe_problem_t& p, int block_m) {
   L.cap = L.P + (int64_t)p.E * (block_m - 1);
   L.n_chunks = (L.P + kSortChunk - 1) / kSortChunk;
   L.max_tiles = L.cap / kTileRows + p.E + 1;
-  const bool direct = block_m == 1 && use_direct(p);
   size_t off = kHeaderBytes;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -149,7 +148,9 @@ Layout make_layout(const moe_problem_t& p, int block_m) {
   L.chunk = take(sizeof(int32_t) * L.n_chunks * p.E);
   L.tiles = take(sizeof(Tile) * L.max_tiles);
   L.tiles2 = take(sizeof(Tile) * L.max_tiles);
-  L.a_sorted = take(direct ? 0 : (size_t)L.cap * p.H * eb);
+  // The gathered rows: the staged gate/up GEMM always gathers; fused_moe_fwd needs them only
+  // for T > 128 (it reads hidden_states directly on the direct path and when T <= 128).
+  L.a_sorted = take((size_t)L.cap * p.H * eb);
   L.act = take((size_t)L.cap * p.F * eb);
   L.y = take((size_t)L.cap * p.H * sizeof(float));  // weighted down-projection rows, f32
   L.sh_act = take((size_t)p.T * p.S * eb);
@@ -349,18 +350,17 @@ moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
                                 tile_rows2, status, s, true));
       t.done(1);
     } else {
-      {
-        StageTimer t(kSort, s);
-        MOE_TRY(launch_align_sort_chunked(P, 1, ids, counts, offsets, sorted, L.cap, nullptr,
-                                          inv_route, at<int32_t>(ws, L.chunk), status, s, true));
-        t.done(3);
-      }
-      StageTimer t(kTiles, s);
-      MOE_TRY(launch_build_tiles(P.E, offsets, tiles, tile_counter(ws), kTileRows, s, true));
-      MOE_TRY(launch_build_tiles(P.E, offsets, tiles2, tile_counter2(ws), tile_rows2, s, true));
-      t.done(2);
+      StageTimer t(kSort, s);
+      MOE_TRY(launch_align_sort_chunked(P, 1, ids, counts, offsets, sorted, L.cap, nullptr,
+                                        inv_route, at<int32_t>(ws, L.chunk), status, s, true,
+                                        tiles, tile_counter(ws), kTileRows, tiles2,
+                                        tile_counter2(ws), tile_rows2));
+      t.done(3);
     }
-    {
+    // With T <= 128 every expert's rows fit one tile of all T tokens: gemm1 reads hidden_states
+    // directly and no gathered copy is made.
+    const bool token_rows = P.T <= kTileRows;
+    if (!token_rows) {
       StageTimer t(kPermute, s);
       MOE_TRY(launch_permute(P.dtype, P.top_k, P.H, hidden_states, sorted, offsets, P.E, L.cap,
                              at<void>(ws, L.a_sorted), s, true));
@@ -372,8 +372,10 @@ moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
     g1.K = P.H;
     g1.n_out = P.F;
     g1.w = w_gate_up;
-    g1.b = at<void>(ws, L.a_sorted);
-    g1.b_rows = L.cap;
+    g1.b = token_rows ? hidden_states : at<void>(ws, L.a_sorted);
+    g1.b_rows = token_rows ? P.T : L.cap;
+    g1.token_rows = token_rows ? 1 : 0;
+    g1.sorted_ids = sorted;
     g1.out = at<void>(ws, L.act);
     g1.tiles = tiles;
     g1.n_tiles = tile_counter(ws);
@@ -386,6 +388,8 @@ moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
     }
     GemmCall g2 = g1;
     g2.gemm1 = 0;
+    g2.token_rows = 0;
+    g2.b_rows = L.cap;
     g2.K = P.F;
     g2.n_out = P.H;
     g2.w = w_down;

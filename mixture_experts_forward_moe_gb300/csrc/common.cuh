@@ -80,7 +80,7 @@ cudaError_t launch_align_sort(const moe_problem_t& p, int block_m, const int32_t
                               int64_t cap, int32_t* tile_expert, int32_t* inv_route,
                               int32_t* chunk_scratch, int* status, cudaStream_t s, bool pdl);
 
-// The sort in one launch (one CTA) when it fits (T*top_k <= 65536); with `tiles` (`tiles2`)
+// The sort in one launch (one CTA) when it fits (T*top_k <= 8192); with `tiles` (`tiles2`)
 // it also writes the GEMM tile list of tile_rows (tile_rows2) rows per tile.
 bool fused_sort_fits(const moe_problem_t& p);
 cudaError_t launch_sort_fused(const moe_problem_t& p, int block_m, const int32_t* ids,
@@ -89,12 +89,14 @@ cudaError_t launch_sort_fused(const moe_problem_t& p, int block_m, const int32_t
                               int* n_tiles, int tile_rows, Tile* tiles2, int* n_tiles2,
                               int tile_rows2, int* status, cudaStream_t s, bool pdl);
 // The sort as three launches over 256-route chunks (any size), using chunk_scratch
-// (ceil(T*top_k/256) * E int32).
+// (ceil(T*top_k/256) * E int32); with `tiles` (`tiles2`) the scan also writes the GEMM tile
+// lists.
 cudaError_t launch_align_sort_chunked(const moe_problem_t& p, int block_m, const int32_t* ids,
                                       int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
                                       int64_t cap, int32_t* tile_expert, int32_t* inv_route,
                                       int32_t* chunk_scratch, int* status, cudaStream_t s,
-                                      bool pdl);
+                                      bool pdl, Tile* tiles, int* n_tiles, int tile_rows,
+                                      Tile* tiles2, int* n_tiles2, int tile_rows2);
 
 cudaError_t launch_build_tiles(int E, const int32_t* offsets, Tile* tiles, int* n_tiles,
                                int tile_rows, cudaStream_t s, bool pdl);
@@ -127,6 +129,8 @@ struct GemmCall {
   const int* n_tiles;
   int max_tiles;  // upper bound of *n_tiles (grid sizing)
   int tile_rows;  // token rows per tile: 128 or 256 (sorted tiles must be built with it)
+  int token_rows; // sorted gemm1 with T <= 128 and no padding slots: b is hidden_states [T, K]
+                  // and each sorted row takes the column of its route's token (no gather)
   const int32_t* sorted_ids;  // gemm2 scale lookup
   // direct mode
   const int32_t* topk_ids;

@@ -68,6 +68,7 @@ struct Cfg {
 
 struct KParams {
   int mode;
+  int token_rows;  // sorted gemm1 with T <= 128: the token side is every row of hidden_states
   int K, n_out, E, n_slabs, num_kb, w_rows_per_expert;
   const Tile* tiles;
   const int* n_tiles;
@@ -82,6 +83,7 @@ struct KParams {
 
 struct Unit {
   int e, row0, nrows, n_mma, slab;
+  int b_row0;  // first token-side row the unit loads
 };
 
 __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
@@ -121,7 +123,12 @@ __device__ __forceinline__ bool decode_unit(const KParams& p, int u, Unit& U) {
     U.row0 = 0;
     U.nrows = kGemm1 ? p.T : p.P;
   }
+  U.b_row0 = U.row0;
   U.n_mma = round16(U.nrows);
+  if (kGemm1 && p.token_rows) {  // load all T token rows; the epilogue picks each row's token
+    U.b_row0 = 0;
+    U.n_mma = round16(p.T);
+  }
   return U.nrows > 0;
 }
 
@@ -233,11 +240,11 @@ __global__ void __launch_bounds__(192, 1)
           // Token rows in as few copies as possible: 128-, then 64-, then 16-row boxes.
           int r = 0;
           for (; r + 128 <= U.n_mma; r += 128)
-            tma_load_2d(sb + r * kBlockK * 2, &tmB128, &full_bar[stage], kx, U.row0 + r);
+            tma_load_2d(sb + r * kBlockK * 2, &tmB128, &full_bar[stage], kx, U.b_row0 + r);
           for (; r + 64 <= U.n_mma; r += 64)
-            tma_load_2d(sb + r * kBlockK * 2, &tmB64, &full_bar[stage], kx, U.row0 + r);
+            tma_load_2d(sb + r * kBlockK * 2, &tmB64, &full_bar[stage], kx, U.b_row0 + r);
           for (; r < U.n_mma; r += 16)
-            tma_load_2d(sb + r * kBlockK * 2, &tmB, &full_bar[stage], kx, U.row0 + r);
+            tma_load_2d(sb + r * kBlockK * 2, &tmB, &full_bar[stage], kx, U.b_row0 + r);
           ++issued;
           if (++stage == C::kStages) {
             stage = 0;
@@ -317,14 +324,20 @@ __global__ void __launch_bounds__(192, 1)
       Unit U;
       if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
       if constexpr (kGemm1) {
-        // Output rows of this unit as (accumulator column, destination row) entries; in direct
-        // mode a column is a token and each route of that token to this expert is an entry.
+        // Output rows of this unit as (accumulator column, destination row) entries.  In direct
+        // mode a column is a token and each route of that token to this expert is an entry; with
+        // token_rows a column is a token and sorted row p reads the column of its route's token.
         const bool direct = p.mode == kDirect;
+        const bool by_token = direct || p.token_rows;
         const int n_ent = direct ? p.P : U.nrows;
         for (int i = et; i < n_ent; i += 128) {
           if (direct) {
             ent_col[i] = p.topk_ids[i] == U.e ? i / p.top_k : -1;
             ent_dst[i] = i;
+          } else if (p.token_rows) {
+            const int sid = p.sorted_ids[U.row0 + i];
+            ent_col[i] = sid >= 0 ? sid / p.top_k : -1;
+            ent_dst[i] = U.row0 + i;
           } else {
             ent_col[i] = i;
             ent_dst[i] = U.row0 + i;
@@ -356,7 +369,7 @@ __global__ void __launch_bounds__(192, 1)
           }
           named_bar_sync(1, 128);
           // 16-byte stores of whole output rows: entry en, chunk ch of 8 columns.
-          const int en_lo = direct ? 0 : c0, en_hi = direct ? n_ent : min(n_ent, c1);
+          const int en_lo = by_token ? 0 : c0, en_hi = by_token ? n_ent : min(n_ent, c1);
           for (int idx = et; idx < (en_hi - en_lo) * 16; idx += 128) {
             const int en = en_lo + (idx >> 4), ch = idx & 15;
             if (ch >= nch) continue;
@@ -500,6 +513,9 @@ cudaError_t launch_rows(const GemmCall& c, const KParams& kp, int grid, cudaStre
 cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   KParams kp;
   kp.mode = c.mode;
+  kp.token_rows = c.gemm1 && c.mode == kSorted && c.token_rows;
+  if (c.token_rows && (!kp.token_rows || c.T > kTileRows || c.tile_rows != kTileRows))
+    return cudaErrorInvalidValue;
   kp.K = c.K;
   kp.n_out = c.n_out;
   kp.E = c.E;

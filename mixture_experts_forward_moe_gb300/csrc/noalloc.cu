@@ -5,7 +5,7 @@
 // cudaMalloc (an allocation there would synchronise the device and fragment the pool), or a
 // plugin entry point whose host framework passes only input and output buffers and offers no
 // workspace.  For them this entry point runs the chunked form of the sort (three kernels over
-// 256-route chunks, the form moe_align_sort uses above 65536 routes), whose per-chunk expert
+// 256-route chunks, the form moe_align_sort uses above 8192 routes), whose per-chunk expert
 // histograms and status word live in `g_sort_scratch` below, a
 // file-scope device array that every GPU loading the library holds until the process exits.
 //
@@ -78,7 +78,8 @@ extern "C" moe_status_t moe_align_sort_noalloc(const moe_problem_t* p, int32_t b
   const int64_t cap = P + (int64_t)p->E * (block_m - 1);
   if (launch_align_sort_chunked(*p, block_m, topk_ids, counts, offsets, sorted_ids, cap,
                                 tile_expert, inv_route, scratch + kNoAllocHeaderInts, status, s,
-                                false) != cudaSuccess)
+                                false, nullptr, nullptr, kTileRows, nullptr, nullptr,
+                                kTileRows) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (status_out &&
       cudaMemcpyAsync(status_out, status, sizeof(int), cudaMemcpyDeviceToDevice, s) != cudaSuccess)

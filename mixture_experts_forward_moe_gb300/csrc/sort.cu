@@ -66,25 +66,63 @@ __device__ int block_inclusive_scan(int v, int* warp_tot) {
   return v + before;
 }
 
+// Tile lists of `rows` rows over the padded expert segments (thread e owns expert e); the
+// caller has synchronised the block, and warp_tot is reused by the block scan.
+__device__ void write_tile_list(int E, int excl, int padded, int rows, Tile* tiles, int* n_tiles,
+                                int* warp_tot) {
+  const int e = threadIdx.x;
+  const int nt = e < E ? (padded + rows - 1) / rows : 0;
+  const int incl = block_inclusive_scan(nt, warp_tot);
+  const int base = incl - nt;
+  for (int i = 0; i < nt; ++i) {
+    Tile t;
+    t.e = e;
+    t.row0 = excl + i * rows;
+    t.nrows = min(rows, padded - i * rows);
+    t.first = base;
+    t.count = nt;
+    t.pad0 = t.pad1 = t.pad2 = 0;
+    tiles[base + i] = t;
+  }
+  if (e == E - 1) *n_tiles = incl;
+}
+
+// Per expert, the exclusive prefix of the chunk histograms over chunks (a warp per expert,
+// lanes over chunks, shuffle scans), then the block scan of the padded totals into the segment
+// offsets, the padding slots, tile_expert and (optionally) the two GEMM tile lists.
 __global__ void __launch_bounds__(1024)
     sort_scan_kernel(int n_chunks, int E, int block_m, int64_t cap,
                      int32_t* __restrict__ chunk_counts, int32_t* __restrict__ counts,
                      int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
-                     int32_t* __restrict__ tile_expert, int64_t tile_len) {
+                     int32_t* __restrict__ tile_expert, int64_t tile_len, Tile* __restrict__ tiles,
+                     int* __restrict__ n_tiles, int tile_rows, Tile* __restrict__ tiles2,
+                     int* __restrict__ n_tiles2, int tile_rows2) {
   __shared__ int warp_tot[32];
   __shared__ int s_total;
+  __shared__ int s_expert_total[1024];
   pdl_wait();
   pdl_trigger();
-  const int e = threadIdx.x;
-  int total = 0;
-  if (e < E) {
-    for (int c = 0; c < n_chunks; ++c) {
-      const size_t i = (size_t)c * E + e;
-      const int v = chunk_counts[i];
-      chunk_counts[i] = total;  // becomes the chunk's base within expert e
-      total += v;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int ex = w; ex < E; ex += 32) {
+    int carry = 0;
+    for (int c0 = 0; c0 < n_chunks; c0 += 32) {
+      const int c = c0 + lane;
+      const size_t i = (size_t)c * E + ex;
+      const int v = c < n_chunks ? chunk_counts[i] : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (c < n_chunks) chunk_counts[i] = carry + incl - v;  // the chunk's base in expert ex
+      carry += __shfl_sync(0xffffffffu, incl, 31);
     }
+    if (lane == 0) s_expert_total[ex] = carry;
   }
+  __syncthreads();
+  const int e = threadIdx.x;
+  const int total = e < E ? s_expert_total[e] : 0;
   const int padded = e < E ? (total + block_m - 1) / block_m * block_m : 0;
   const int incl = block_inclusive_scan(padded, warp_tot);
   const int excl = incl - padded;
@@ -106,6 +144,14 @@ __global__ void __launch_bounds__(1024)
       for (int i = excl / block_m; i < (excl + padded) / block_m; ++i) tile_expert[i] = e;
     for (int64_t i = tot / block_m + threadIdx.x; i < tile_len; i += blockDim.x)
       tile_expert[i] = -1;
+  }
+  if (tiles) {
+    __syncthreads();
+    write_tile_list(E, excl, padded, tile_rows, tiles, n_tiles, warp_tot);
+  }
+  if (tiles2) {
+    __syncthreads();
+    write_tile_list(E, excl, padded, tile_rows2, tiles2, n_tiles2, warp_tot);
   }
 }
 
@@ -162,7 +208,8 @@ __global__ void __launch_bounds__(1024)
   if (e == E - 1) *n_tiles = incl;
 }
 
-// The whole sort in one CTA of 1024 threads (32 warps), for up to kFusedSortMaxRoutes routes:
+// The whole sort in one CTA of 1024 threads (32 warps), for up to kFusedSortMaxRoutes routes
+// (beyond that the chunked kernels, which spread the ranking over many CTAs, are faster):
 // warp w owns the contiguous routes [w*per, (w+1)*per).  Pass A counts each warp's routes per
 // expert (lanes with the same id found with __match_any_sync); a per-expert prefix over the
 // warps, after the block scan of the padded totals, turns the counts into each warp's first
@@ -170,7 +217,7 @@ __global__ void __launch_bounds__(1024)
 // each one at that base plus its rank among the equal ids before it.  The result is the same
 // stable order as the chunked kernels, from a single launch.  With `tiles` it also writes the
 // GEMM tile list over the segments.
-constexpr int kFusedSortMaxRoutes = 65536;
+constexpr int kFusedSortMaxRoutes = 8192;
 
 __global__ void __launch_bounds__(1024)
     sort_fused_kernel(const int32_t* __restrict__ ids, int P, int E, int block_m, int64_t cap,
@@ -191,19 +238,27 @@ __global__ void __launch_bounds__(1024)
   const int per = (P + 31) / 32;
   const int r0 = w * per, r1 = min(P, r0 + per);
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int b = r0; b < r1; b += 32) {  // pass A: per-warp histogram
-    const int r = b + lane;
-    int e = -1;
-    if (r < r1) {
-      e = ids[r];
+  // Routes are read 8 groups of 32 at a time (independent loads, one latency per batch) and
+  // processed in route order.
+  constexpr int kBatch = 8;
+  for (int b0 = r0; b0 < r1; b0 += 32 * kBatch) {  // pass A: per-warp histogram
+    int eb[kBatch];
+#pragma unroll
+    for (int g = 0; g < kBatch; ++g) {
+      const int r = b0 + 32 * g + lane;
+      eb[g] = r < r1 ? ids[r] : -1;
+    }
+#pragma unroll
+    for (int g = 0; g < kBatch; ++g) {
+      int e = eb[g];
       if (e < -1 || e >= E) {
         set_status(status, MOE_ERR_BAD_EXPERT_ID);
         e = -1;
       }
+      const unsigned m = __match_any_sync(0xffffffffu, e);
+      if (e >= 0 && lane == __ffs(m) - 1) wc[e] += __popc(m);
+      __syncwarp();
     }
-    const unsigned m = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && lane == __ffs(m) - 1) wc[e] += __popc(m);
-    __syncwarp();
   }
   __syncthreads();
   int total = 0;
@@ -227,27 +282,33 @@ __global__ void __launch_bounds__(1024)
     s_total = incl;
   }
   __syncthreads();
-  for (int b = r0; b < r1; b += 32) {  // pass B: stable scatter
-    const int r = b + lane;
-    int e = -1;
-    if (r < r1) {
-      e = ids[r];
+  for (int b0 = r0; b0 < r1; b0 += 32 * kBatch) {  // pass B: stable scatter
+    int eb[kBatch];
+#pragma unroll
+    for (int g = 0; g < kBatch; ++g) {
+      const int r = b0 + 32 * g + lane;
+      eb[g] = r < r1 ? ids[r] : -1;
+    }
+#pragma unroll
+    for (int g = 0; g < kBatch; ++g) {
+      const int r = b0 + 32 * g + lane;
+      int e = eb[g];
       if (e < -1 || e >= E) e = -1;
-    }
-    const unsigned m = __match_any_sync(0xffffffffu, e);
-    const int base = e >= 0 ? wc[e] : 0;
-    __syncwarp();
-    if (r < r1) {
-      if (e >= 0) {
-        const int pos = base + __popc(m & lt_mask);
-        sorted_ids[pos] = r;
-        inv_route[r] = pos;
-      } else {
-        inv_route[r] = -1;
+      const unsigned m = __match_any_sync(0xffffffffu, e);
+      const int base = e >= 0 ? wc[e] : 0;
+      __syncwarp();
+      if (r < r1) {
+        if (e >= 0) {
+          const int pos = base + __popc(m & lt_mask);
+          sorted_ids[pos] = r;
+          inv_route[r] = pos;
+        } else {
+          inv_route[r] = -1;
+        }
       }
+      if (e >= 0 && lane == __ffs(m) - 1) wc[e] = base + __popc(m);
+      __syncwarp();
     }
-    if (e >= 0 && lane == __ffs(m) - 1) wc[e] = base + __popc(m);
-    __syncwarp();
   }
   const int tot = s_total;
   if (tid < E)
@@ -258,25 +319,13 @@ __global__ void __launch_bounds__(1024)
       for (int i = excl / block_m; i < (excl + padded) / block_m; ++i) tile_expert[i] = tid;
     for (int64_t i = tot / block_m + tid; i < tile_len; i += blockDim.x) tile_expert[i] = -1;
   }
-  for (int list = 0; list < 2; ++list) {  // up to two tile lists of different heights
-    Tile* tl = list == 0 ? tiles : tiles2;
-    if (!tl) continue;
-    const int rows = list == 0 ? tile_rows : tile_rows2;
+  if (tiles) {
     __syncthreads();  // warp_tot is reused by every scan
-    const int nt = (padded + rows - 1) / rows;
-    const int tincl = block_inclusive_scan(nt, warp_tot);
-    const int tbase = tincl - nt;
-    for (int i = 0; i < nt; ++i) {
-      Tile t;
-      t.e = tid;
-      t.row0 = excl + i * rows;
-      t.nrows = min(rows, padded - i * rows);
-      t.first = tbase;
-      t.count = nt;
-      t.pad0 = t.pad1 = t.pad2 = 0;
-      tl[tbase + i] = t;
-    }
-    if (tid == E - 1) *(list == 0 ? n_tiles : n_tiles2) = tincl;
+    write_tile_list(E, excl, padded, tile_rows, tiles, n_tiles, warp_tot);
+  }
+  if (tiles2) {
+    __syncthreads();
+    write_tile_list(E, excl, padded, tile_rows2, tiles2, n_tiles2, warp_tot);
   }
 }
 
@@ -379,7 +428,8 @@ cudaError_t launch_align_sort_chunked(const moe_problem_t& p, int block_m, const
                                       int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
                                       int64_t cap, int32_t* tile_expert, int32_t* inv_route,
                                       int32_t* chunk_scratch, int* status, cudaStream_t s,
-                                      bool pdl) {
+                                      bool pdl, Tile* tiles, int* n_tiles, int tile_rows,
+                                      Tile* tiles2, int* n_tiles2, int tile_rows2) {
   const int P = p.T * p.top_k;
   const int n_chunks = (P + kChunk - 1) / kChunk;
   const int64_t tile_len = (cap + block_m - 1) / block_m;
@@ -391,7 +441,8 @@ cudaError_t launch_align_sort_chunked(const moe_problem_t& p, int block_m, const
   }
   cudaError_t err = launch_k(sort_scan_kernel, dim3(1), dim3(1024), 0, s, pdl, n_chunks, p.E,
                              block_m, cap, chunk_scratch, counts, offsets, sorted_ids,
-                             tile_expert, tile_len);
+                             tile_expert, tile_len, tiles, n_tiles, tile_rows, tiles2, n_tiles2,
+                             tile_rows2);
   if (err != cudaSuccess || n_chunks == 0) return err;
   return launch_k(sort_scatter_kernel, dim3(n_chunks), dim3(kChunk), 0, s, true, ids, P, p.E,
                   static_cast<const int32_t*>(chunk_scratch),
@@ -407,7 +458,8 @@ cudaError_t launch_align_sort(const moe_problem_t& p, int block_m, const int32_t
                              inv_route, nullptr, nullptr, kTileRows, nullptr, nullptr, kTileRows,
                              status, s, pdl);
   return launch_align_sort_chunked(p, block_m, ids, counts, offsets, sorted_ids, cap,
-                                   tile_expert, inv_route, chunk_scratch, status, s, pdl);
+                                   tile_expert, inv_route, chunk_scratch, status, s, pdl,
+                                   nullptr, nullptr, kTileRows, nullptr, nullptr, kTileRows);
 }
 
 cudaError_t launch_build_tiles(int E, const int32_t* offsets, Tile* tiles, int* n_tiles,

@@ -23,6 +23,7 @@ GEMM_CASES = [
     (9, 8, 64, 512, 96, 1, 0.0, torch.bfloat16),       # decode-like: 1-2 rows per expert
     (800, 2, 3, 256, 136, 1, 0.0, torch.bfloat16),     # 256-row tiles, ~530 rows per expert
     (260, 4, 8, 192, 128, 8, 0.05, torch.float16),     # 256-row tiles with padded segments
+    (6, 4, 16, 256, 128, 1, 0.0, torch.bfloat16),      # T <= 8: staged calls still gather
 ]
 
 
