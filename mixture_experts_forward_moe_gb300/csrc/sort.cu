@@ -103,20 +103,29 @@ __global__ void __launch_bounds__(1024)
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  constexpr int kGroups = 4;  // 4 x 32 chunks loaded at once (independent loads)
   for (int ex = w; ex < E; ex += 32) {
     int carry = 0;
-    for (int c0 = 0; c0 < n_chunks; c0 += 32) {
-      const int c = c0 + lane;
-      const size_t i = (size_t)c * E + ex;
-      const int v = c < n_chunks ? chunk_counts[i] : 0;
-      int incl = v;
+    for (int c0 = 0; c0 < n_chunks; c0 += 32 * kGroups) {
+      int v[kGroups];
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
+      for (int g = 0; g < kGroups; ++g) {
+        const int c = c0 + 32 * g + lane;
+        v[g] = c < n_chunks ? chunk_counts[(size_t)c * E + ex] : 0;
       }
-      if (c < n_chunks) chunk_counts[i] = carry + incl - v;  // the chunk's base in expert ex
-      carry += __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+      for (int g = 0; g < kGroups; ++g) {
+        const int c = c0 + 32 * g + lane;
+        int incl = v[g];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int o = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += o;
+        }
+        if (c < n_chunks)  // the chunk's base within expert ex
+          chunk_counts[(size_t)c * E + ex] = carry + incl - v[g];
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
     }
     if (lane == 0) s_expert_total[ex] = carry;
   }
