@@ -13,7 +13,14 @@ FusedMoESharedExpertFwd shape lists; flashinfer PR #4048 DeepSeek-V3 benchmark w
   shared_w_gate_up ~ N(0, 1/H), shared_w_down ~ N(0, 1/S)
 One torch.Generator seeded with `seed` draws, in this order: hidden, gating, bias, w_gate_up,
 w_down, shared_w_gate_up, shared_w_down.  Large weights are drawn expert by expert (chunks of
-rows) so the f32 staging stays small; the chunking is part of the recipe.
+rows) so the f32 staging stays small; the chunking is part of the recipe.  w_gate_up has 2F
+rows per expert for the gated activations (SiLU, GeGLU-tanh) and F rows for ReLU2.
+
+Skewed routing (flashinfer PR #4048 benchmark, "Skewed routing"): when skew_alpha > 0 the
+gating logits of expert e get the fixed bias -skew_alpha * log(1 + rank[e]), rank a random
+permutation of the experts drawn by a second generator seeded with seed + 7919 (so the other
+inputs are the same as without skew).  skew_alpha is chosen per workload so that the most
+popular expert receives about twice the mean load.
 """
 from __future__ import annotations
 
@@ -39,13 +46,21 @@ class Workload:
     routed_scaling_factor: float = 1.0
     S: int = 0
     dtype: torch.dtype = torch.bfloat16
+    activation: str = "silu"       # "silu", "gelu_tanh" (gated) or "relu2" (single projection)
+    skew_alpha: float = 0.0         # > 0: skewed routing bias on the gating logits
+
+    @property
+    def gated(self) -> bool:
+        return self.activation != "relu2"
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
 
     def flops(self) -> float:
-        """2*T*k*3*F*H (+ 2*T*3*S*H): the FLOP count the TileOPs MoE page's TFLOP/s uses."""
-        return 2.0 * self.T * self.top_k * 3 * self.F * self.H + 2.0 * self.T * 3 * self.S * self.H
+        """2*T*k*3*F*H (+ 2*T*3*S*H): the FLOP count the TileOPs MoE page's TFLOP/s uses (three
+        F x H matrices per expert; two for the single-projection ReLU2 MLP)."""
+        m = 3 if self.gated else 2
+        return 2.0 * self.T * self.top_k * m * self.F * self.H + 2.0 * self.T * m * self.S * self.H
 
     def kwargs(self) -> dict:
         return dict(top_k=self.top_k, scoring_func=self.scoring_func,
@@ -70,6 +85,19 @@ WORKLOADS = {
         bias_std=0.1, routed_scaling_factor=2.827, S=18432),
 }
 
+# Variants of the measured shapes (flashinfer PR #4048: skewed routing; activation variants of
+# the W4A16 follow-up and the W4A8 validation list).  With N(0,1) softmax logits over 128
+# experts and top-8, skew_alpha = 0.10 gives the most popular expert 2.0x the mean load.
+_Q235 = WORKLOADS["qwen3-235b-a22b-decode-t512"]
+VARIANTS = {
+    "qwen3-235b-a22b-decode-t512-skewed": _Q235.with_(
+        name="qwen3-235b-a22b-decode-t512-skewed", skew_alpha=0.10),
+    "qwen3-235b-a22b-decode-t512-gelu-tanh": _Q235.with_(
+        name="qwen3-235b-a22b-decode-t512-gelu-tanh", activation="gelu_tanh"),
+    "qwen3-235b-a22b-decode-t512-relu2": _Q235.with_(
+        name="qwen3-235b-a22b-decode-t512-relu2", activation="relu2"),
+}
+
 # Small cases of the same kernels for hardware-counter captures, which must stay at a few GB on
 # the device: the DeepSeek-V3 expert shapes and routing with 32 experts (about 128 routed rows
 # per expert, skewed by the correction bias), 2.8 GB of weights.
@@ -86,7 +114,10 @@ PROBES = {
 
 
 def workload(name: str) -> Workload:
-    return WORKLOADS[name] if name in WORKLOADS else PROBES[name]
+    for table in (WORKLOADS, VARIANTS, PROBES):
+        if name in table:
+            return table[name]
+    raise KeyError(name)
 
 _CHUNK_ELEMS = 1 << 28  # f32 staging per draw: 1 GiB
 
@@ -118,17 +149,29 @@ def generate(w: Workload, seed: int = 0, device="cuda") -> dict:
     d = {}
     d["hidden_states"] = _randn((w.T, w.H), gen, device, 1.0, dt)
     d["gating_output"] = _randn((w.T, w.E), gen, device, 1.0, torch.float32)
+    if w.skew_alpha > 0:
+        d["gating_output"] += skew_bias(w.E, w.skew_alpha, seed).to(device)
     d["correction_bias"] = (_randn((w.E,), gen, device, w.bias_std, torch.float32)
                             if w.bias_std > 0 else None)
-    d["w_gate_up"] = _randn((w.E, 2 * w.F, w.H), gen, device, 1.0 / math.sqrt(w.H), dt)
+    rows = 2 if w.gated else 1
+    d["w_gate_up"] = _randn((w.E, rows * w.F, w.H), gen, device, 1.0 / math.sqrt(w.H), dt)
     d["w_down"] = _randn((w.E, w.H, w.F), gen, device, 1.0 / math.sqrt(w.F), dt)
     if w.S > 0:
-        d["shared_w_gate_up"] = _randn((2 * w.S, w.H), gen, device, 1.0 / math.sqrt(w.H), dt)
+        d["shared_w_gate_up"] = _randn((rows * w.S, w.H), gen, device, 1.0 / math.sqrt(w.H),
+                                       dt)
         d["shared_w_down"] = _randn((w.H, w.S), gen, device, 1.0 / math.sqrt(w.S), dt)
     else:
         d["shared_w_gate_up"] = None
         d["shared_w_down"] = None
     return d
+
+
+def skew_bias(E: int, alpha: float, seed: int) -> torch.Tensor:
+    """[E] f32: -alpha * log(1 + rank[e]) for a seeded random ranking of the experts."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed + 7919)
+    rank = torch.randperm(E, generator=g).to(torch.float64)
+    return (-alpha * torch.log1p(rank)).to(torch.float32)
 
 
 def random_ids(T: int, top_k: int, E: int, seed: int = 0, device="cpu", pad_frac: float = 0.0,

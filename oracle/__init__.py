@@ -32,6 +32,12 @@ _lib = None
 OK, ERR_ARG, ERR_ID = 0, 1, 6
 BF16, F16 = 0, 1
 SOFTMAX, SIGMOID = 0, 1
+ACT_SILU, ACT_GELU_TANH, ACT_RELU2 = 0, 1, 2
+
+
+def gate_up_rows(activation: int, F: int) -> int:
+    """Rows per expert of w_gate_up: 2F for the gated activations, F for ReLU2."""
+    return F if activation == ACT_RELU2 else 2 * F
 
 
 def build(force: bool = False) -> str:
@@ -66,9 +72,9 @@ def _load():
             _lib.oracle_sigmoid_key_f32.argtypes = [ctypes.c_float]
             _lib.oracle_route.argtypes = [i32, i32, i32, i32, i32, i32, i32, f64, P, P, P, P, P]
             _lib.oracle_align_sort.argtypes = [i32, i32, i32, i32, P, P, P, P, i64, P, i64, P]
-            _lib.oracle_moe_tokens.argtypes = [i32, P, i32, i32, i32, i32, i32, i32, P, P, P, P,
-                                               P, P, i32, P, P, P]
-            _lib.oracle_expert_act.argtypes = [i32, i32, i32, i32, P, P, P, P]
+            _lib.oracle_moe_tokens.argtypes = [i32, P, i32, i32, i32, i32, i32, i32, i32, P, P, P,
+                                               P, P, P, i32, P, P, P]
+            _lib.oracle_expert_act.argtypes = [i32, i32, i32, i32, i32, P, P, P, P]
             _lib.oracle_expert_down.argtypes = [i32, i32, i32, i32, P, P, P, P, P]
             _lib.oracle_combine.argtypes = [i32, i32, i32, i32, P, P, P, P]
             _lib.oracle_num_threads.restype = i32
@@ -160,11 +166,14 @@ def align_sort(ids, E, block_m):
 
 
 def moe_tokens(hidden, ids, weights, w_gate_up, w_down, dtype, tokens=None, expert_slot=None,
-               shared_w_gate_up=None, shared_w_down=None, num_experts=None):
+               shared_w_gate_up=None, shared_w_down=None, num_experts=None,
+               activation=ACT_SILU):
     """fp64 fused MoE output for the listed tokens (all tokens when ``tokens`` is None).
 
     hidden/w_* are 16-bit bit arrays (or torch tensors).  When ``expert_slot`` is given,
-    w_gate_up/w_down hold only the slots it maps experts to and ``num_experts`` is E."""
+    w_gate_up/w_down hold only the slots it maps experts to and ``num_experts`` is E.
+    ``activation`` is ACT_SILU, ACT_GELU_TANH (both gated: w_gate_up has 2F rows per expert) or
+    ACT_RELU2 (F rows per expert)."""
     hb = _bits(hidden)
     T, H = hb.shape
     idv = _c(ids, np.int32)
@@ -172,30 +181,34 @@ def moe_tokens(hidden, ids, weights, w_gate_up, w_down, dtype, tokens=None, expe
     wv = _c(weights, np.float64)
     wgu = _bits(w_gate_up)
     wd = _bits(w_down)
-    F = wgu.shape[-2] // 2
+    F = wd.shape[-1]
     E = num_experts if num_experts is not None else wgu.shape[0]
     slot = None if expert_slot is None else _c(expert_slot, np.int32)
     sgu = _bits(shared_w_gate_up)
     sd = _bits(shared_w_down)
-    S = 0 if sgu is None else sgu.shape[0] // 2
+    S = 0 if sd is None else sd.shape[-1]
     tl = np.arange(T, dtype=np.int32) if tokens is None else _c(tokens, np.int32)
     out = np.empty((tl.size, H), np.float64)
-    rc = _load().oracle_moe_tokens(tl.size, _ptr(tl), T, H, E, F, k, dtype, _ptr(hb), _ptr(idv),
+    if wgu.shape[-2] != gate_up_rows(activation, F) or (
+            sgu is not None and sgu.shape[0] != gate_up_rows(activation, S)):
+        raise ValueError("w_gate_up rows do not match the activation")
+    rc = _load().oracle_moe_tokens(tl.size, _ptr(tl), T, H, E, F, k, dtype, activation,
+                                   _ptr(hb), _ptr(idv),
                                    _ptr(wv), _ptr(wgu), _ptr(wd), _ptr(slot), S, _ptr(sgu),
                                    _ptr(sd), _ptr(out))
     _check(rc, "oracle_moe_tokens")
     return out
 
 
-def expert_act(x_rows, expert_of_row, w_gate_up, dtype):
+def expert_act(x_rows, expert_of_row, w_gate_up, dtype, activation=ACT_SILU):
     xb = _bits(x_rows)
     n, H = xb.shape
     wgu = _bits(w_gate_up)
-    F = wgu.shape[1] // 2
+    F = wgu.shape[1] if activation == ACT_RELU2 else wgu.shape[1] // 2
     eo = _c(expert_of_row, np.int32)
     act = np.empty((n, F), np.float64)
-    _check(_load().oracle_expert_act(n, H, F, dtype, _ptr(xb), _ptr(eo), _ptr(wgu), _ptr(act)),
-           "oracle_expert_act")
+    _check(_load().oracle_expert_act(n, H, F, dtype, activation, _ptr(xb), _ptr(eo), _ptr(wgu),
+                                     _ptr(act)), "oracle_expert_act")
     return act
 
 

@@ -25,7 +25,9 @@
  * oracle_sigmoid_key_f32.
  *
  * Parity pins (tests/test_oracle_pins.py): brute-force routing on tiny inputs, weight sum
- * invariants, E=1/top_k=1 reduction to a dense SwiGLU MLP computed by a textbook matvec,
+ * invariants, E=1/top_k=1 reduction to a dense SwiGLU MLP computed by a textbook matvec, the
+ * GeGLU-tanh activation against the exact GELU x*Phi(x) within the tanh form's error, ReLU2
+ * against max(g,0)^2 on every sign,
  * token-permutation equivariance, zeroed-expert and linearity checks, sort invariants, the
  * bf16/f16 decoders against every bit pattern, and the f32 exp/sigmoid against fp64 within
  * stated ulp bounds.
@@ -320,20 +322,46 @@ int oracle_align_sort(int T, int top_k, int E, int block_m, const int32_t* ids, 
 /* Expert MLP (TileOPs "MoE" page, ops MoEGroupedGemmFwd with activation=silu_and_mul,          */
 /* MoEExpertMLPFwd and SharedExpertMLPFwd): rows [0,F) of w_gate_up are the gate, rows [F,2F)   */
 /* the up projection; act = SiLU(gate) * up with SiLU(g) = g / (1 + e^-g); y = w_down . act.     */
+/* Activation variants (flashinfer PR #4048 follow-up "Extend CuTe DSL W4A16 fused MoE with      */
+/* tanh-approximate GeGLU and SiTU", and the W4A8 validation list naming SwiGLU and ReLU2):      */
+/*   GeGLU-tanh  act = up * GELU_tanh(gate),                                                     */
+/*               GELU_tanh(g) = g/2 * (1 + tanh(sqrt(2/pi) * (g + 0.044715 g^3)));              */
+/*   ReLU2       act = max(g, 0)^2 of a single projection: w_gate_up has F rows (no up half).    */
 /* ------------------------------------------------------------------------------------------ */
 
-/* act[f] = SiLU(sum_h Wg[f,h] x[h]) * (sum_h Wu[f,h] x[h]) for one expert; wgu is [2F, H]. */
-static void swiglu_rows(const double* tab, const uint16_t* wgu, const double* x, int H, int F,
-                        double* act) {
+#define ORACLE_ACT_SILU 0
+#define ORACLE_ACT_GELU_TANH 1
+#define ORACLE_ACT_RELU2 2
+
+/* Rows per expert of w_gate_up: 2F for the gated activations, F for ReLU2. */
+static int64_t gate_up_rows(int activation, int F) {
+  return activation == ORACLE_ACT_RELU2 ? (int64_t)F : (int64_t)2 * F;
+}
+
+static double gelu_tanh(double g) {
+  const double c = sqrt(2.0 / 3.14159265358979323846);
+  return 0.5 * g * (1.0 + tanh(c * (g + 0.044715 * g * g * g)));
+}
+
+/* act[f] for one expert: wgu is [gate_up_rows(activation, F), H]. */
+static void act_rows(const double* tab, const uint16_t* wgu, const double* x, int H, int F,
+                     int activation, double* act) {
   for (int f = 0; f < F; ++f) {
     const uint16_t* wg = wgu + (int64_t)f * H;
-    const uint16_t* wu = wgu + (int64_t)(F + f) * H;
-    double g = 0.0, u = 0.0;
-    for (int h = 0; h < H; ++h) {
-      g += tab[wg[h]] * x[h];
-      u += tab[wu[h]] * x[h];
+    double g = 0.0;
+    for (int h = 0; h < H; ++h) g += tab[wg[h]] * x[h];
+    if (activation == ORACLE_ACT_RELU2) {
+      const double r = g > 0.0 ? g : 0.0;
+      act[f] = r * r;
+      continue;
     }
-    act[f] = g / (1.0 + exp(-g)) * u;
+    const uint16_t* wu = wgu + (int64_t)(F + f) * H;
+    double u = 0.0;
+    for (int h = 0; h < H; ++h) u += tab[wu[h]] * x[h];
+    if (activation == ORACLE_ACT_GELU_TANH)
+      act[f] = gelu_tanh(g) * u;
+    else
+      act[f] = g / (1.0 + exp(-g)) * u;
   }
 }
 
@@ -358,16 +386,19 @@ static const uint16_t* expert_ptr(const uint16_t* base, const int32_t* slot, int
 
 /*
  * oracle_moe_tokens: the fused MoE forward for a list of tokens, per token in fp64:
- *   out[t] = sum_j weights[t,j] * W_down[e_j] . (SiLU(W_gate[e_j] x_t) * W_up[e_j] x_t)
+ *   out[t] = sum_j weights[t,j] * W_down[e_j] . act(x_t; w_gate_up[e_j])
  *            + shared(x_t)            (shared term only when S > 0; unweighted, not scaled)
+ * with act() the activation selected by `activation` (ORACLE_ACT_*, see act_rows); the shared
+ * expert uses the same activation.
  * Routes with id -1 are skipped.  out is [n_tok, H] in the order of tok_list.
  */
 int oracle_moe_tokens(int n_tok, const int32_t* tok_list, int T, int H, int E, int F, int top_k,
-                      int dtype, const uint16_t* hidden, const int32_t* ids,
+                      int dtype, int activation, const uint16_t* hidden, const int32_t* ids,
                       const double* weights, const uint16_t* w_gate_up, const uint16_t* w_down,
                       const int32_t* expert_slot, int S, const uint16_t* shared_w_gate_up,
                       const uint16_t* shared_w_down, double* out) {
-  if (n_tok < 0 || H <= 0 || E <= 0 || F <= 0 || top_k <= 0 || (dtype != 0 && dtype != 1))
+  if (n_tok < 0 || H <= 0 || E <= 0 || F <= 0 || top_k <= 0 || (dtype != 0 && dtype != 1) ||
+      activation < ORACLE_ACT_SILU || activation > ORACLE_ACT_RELU2)
     return ORACLE_ERR_ARG;
   const double* tab = decode_table(dtype);
   int bad = 0;
@@ -392,19 +423,20 @@ int oracle_moe_tokens(int n_tok, const int32_t* tok_list, int T, int H, int E, i
         bad |= 2;
         continue;
       }
-      const uint16_t* wgu = expert_ptr(w_gate_up, expert_slot, e, (int64_t)2 * F * H);
+      const uint16_t* wgu =
+          expert_ptr(w_gate_up, expert_slot, e, gate_up_rows(activation, F) * H);
       const uint16_t* wd = expert_ptr(w_down, expert_slot, e, (int64_t)H * F);
       if (!wgu || !wd) {
         bad |= 1;
         continue;
       }
       double w = weights[(int64_t)t * top_k + j];
-      swiglu_rows(tab, wgu, x, H, F, act);
+      act_rows(tab, wgu, x, H, F, activation, act);
       down_rows(tab, wd, act, H, F, y);
       for (int h = 0; h < H; ++h) o[h] += w * y[h];
     }
     if (S > 0) {
-      swiglu_rows(tab, shared_w_gate_up, x, H, S, act);
+      act_rows(tab, shared_w_gate_up, x, H, S, activation, act);
       down_rows(tab, shared_w_down, act, H, S, y);
       for (int h = 0; h < H; ++h) o[h] += y[h];
     }
@@ -423,9 +455,11 @@ int oracle_moe_tokens(int n_tok, const int32_t* tok_list, int T, int H, int E, i
  * oracle_expert_act: act[r, :] for n_rows input rows x_bits[r, :] (dtype bits, [n_rows, H]) all
  * routed to the expert given per row in expert_of_row[r] (-1: row left at 0).
  */
-int oracle_expert_act(int n_rows, int H, int F, int dtype, const uint16_t* x_bits,
+int oracle_expert_act(int n_rows, int H, int F, int dtype, int activation, const uint16_t* x_bits,
                       const int32_t* expert_of_row, const uint16_t* w_gate_up, double* act) {
-  if (n_rows < 0 || H <= 0 || F <= 0) return ORACLE_ERR_ARG;
+  if (n_rows < 0 || H <= 0 || F <= 0 || activation < ORACLE_ACT_SILU ||
+      activation > ORACLE_ACT_RELU2)
+    return ORACLE_ERR_ARG;
   const double* tab = decode_table(dtype);
 #pragma omp parallel for schedule(dynamic, 4)
   for (int r = 0; r < n_rows; ++r) {
@@ -437,7 +471,8 @@ int oracle_expert_act(int n_rows, int H, int F, int dtype, const uint16_t* x_bit
     }
     double* x = (double*)malloc(sizeof(double) * H);
     for (int h = 0; h < H; ++h) x[h] = tab[x_bits[(int64_t)r * H + h]];
-    swiglu_rows(tab, w_gate_up + (int64_t)e * 2 * F * H, x, H, F, a);
+    act_rows(tab, w_gate_up + (int64_t)e * gate_up_rows(activation, F) * H, x, H, F, activation,
+             a);
     free(x);
   }
   return ORACLE_OK;

@@ -315,6 +315,114 @@ def test_expert_slot_subset_matches_full_weights():
     np.testing.assert_array_equal(full, sub)
 
 
+# ------------------------------------------------------------------- activation variants
+def _activation_probe(g_values, activation, up=1.0):
+    """act for a one-input expert (H = 1, x = 1): gate row f holds g_values[f], up rows hold
+    `up`, so act[f] is the activation of exactly g_values[f] (bf16 values)."""
+    g = torch.tensor(g_values, dtype=torch.float32).to(torch.bfloat16)
+    F = g.numel()
+    rows = [g.view(F, 1)]
+    if activation != oracle.ACT_RELU2:
+        rows.append(torch.full((F, 1), up, dtype=torch.bfloat16))
+    wgu = torch.cat(rows).view(1, -1, 1)
+    x = torch.ones((1, 1), dtype=torch.bfloat16)
+    act = oracle.expert_act(_bits(x), np.zeros(1, np.int32), _bits(wgu), oracle.BF16,
+                            activation=activation)
+    return g.double().numpy(), act[0]
+
+
+def test_gelu_tanh_within_its_error_of_the_exact_gelu():
+    # The tanh form of GELU differs from x*Phi(x) by less than 4.8e-4 everywhere; a wrong
+    # constant (0.04715 for 0.044715, or sqrt(1/pi)) moves it by 1.5e-3 or more.
+    g, act = _activation_probe(np.linspace(-8.0, 8.0, 641), oracle.ACT_GELU_TANH)
+    exact = np.array([0.5 * v * (1.0 + math.erf(v / math.sqrt(2.0))) for v in g])
+    assert np.max(np.abs(act - exact)) < 4.8e-4
+    assert act[np.argmin(np.abs(g))] == 0.0
+
+
+def test_gelu_tanh_is_gated_by_the_up_row():
+    g, a1 = _activation_probe(np.linspace(-3.0, 3.0, 25), oracle.ACT_GELU_TANH, up=1.0)
+    _, a3 = _activation_probe(np.linspace(-3.0, 3.0, 25), oracle.ACT_GELU_TANH, up=-3.0)
+    np.testing.assert_allclose(a3, -3.0 * a1, rtol=1e-15, atol=0)
+
+
+def test_silu_probe_matches_scipy_expit():
+    g, act = _activation_probe(np.linspace(-12.0, 12.0, 97), oracle.ACT_SILU)
+    np.testing.assert_allclose(act, g * scipy.special.expit(g), rtol=1e-14, atol=1e-300)
+
+
+def test_relu2_is_the_squared_positive_part():
+    vals = np.concatenate([np.linspace(-5.0, 5.0, 81), [0.0, -0.0, 1e-30, -1e-30]])
+    g, act = _activation_probe(vals, oracle.ACT_RELU2)
+    np.testing.assert_array_equal(act, np.where(g > 0, g * g, 0.0))
+
+
+def test_relu2_single_projection_layout_is_a_dense_mlp():
+    # ReLU2 experts hold F rows in w_gate_up (no up half): top-1 over one expert reduces to
+    # W_down . max(W x, 0)^2, computed here by numpy matmuls.
+    w = inputs.Workload("t", T=5, H=40, E=1, F=24, top_k=1, activation="relu2", S=16)
+    d = inputs.generate(w, seed=3, device="cpu")
+    assert d["w_gate_up"].shape == (1, 24, 40) and d["shared_w_gate_up"].shape == (16, 40)
+    ids, wts, _ = oracle.route(d["gating_output"].numpy(), 1)
+    out = oracle.moe_tokens(d["hidden_states"], ids, wts, d["w_gate_up"], d["w_down"],
+                            oracle.BF16, shared_w_gate_up=d["shared_w_gate_up"],
+                            shared_w_down=d["shared_w_down"], activation=oracle.ACT_RELU2)
+    x = d["hidden_states"].double().numpy()
+    relu2 = lambda v: np.maximum(v, 0.0) ** 2
+    ref = (relu2(x @ d["w_gate_up"][0].double().numpy().T) @ d["w_down"][0].double().numpy().T
+           + relu2(x @ d["shared_w_gate_up"].double().numpy().T)
+           @ d["shared_w_down"].double().numpy().T)
+    np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
+
+
+def test_gelu_tanh_uses_the_up_half_of_each_expert():
+    # act = GELU_tanh(W_gate x) * (W_up x) with W_gate = rows [0, F) and W_up = rows [F, 2F) of
+    # the expert's w_gate_up: within 4.8e-4 |W_up x| of the exact GELU times the up row.
+    w = inputs.Workload("t", T=3, H=32, E=2, F=16, top_k=1)
+    d = inputs.generate(w, seed=5, device="cpu")
+    x = d["hidden_states"]
+    eo = np.array([1, 0, 1], np.int32)
+    act = oracle.expert_act(x, eo, d["w_gate_up"], oracle.BF16, activation=oracle.ACT_GELU_TANH)
+    for r in range(3):
+        wgu = d["w_gate_up"][eo[r]].double().numpy()
+        xr = x[r].double().numpy()
+        g, u = wgu[:16] @ xr, wgu[16:] @ xr
+        exact = 0.5 * g * (1.0 + scipy.special.erf(g / math.sqrt(2.0))) * u
+        assert np.all(np.abs(act[r] - exact) <= 4.8e-4 * np.abs(u) + 1e-15)
+
+
+def test_activation_rejects_mismatched_weight_rows():
+    w = inputs.Workload("t", T=2, H=16, E=2, F=8, top_k=1)
+    d = inputs.generate(w, seed=1, device="cpu")
+    ids, wts, _ = oracle.route(d["gating_output"].numpy(), 1)
+    with pytest.raises(ValueError):
+        oracle.moe_tokens(d["hidden_states"], ids, wts, d["w_gate_up"], d["w_down"], oracle.BF16,
+                          activation=oracle.ACT_RELU2)
+
+
+# ------------------------------------------------------------------------- skewed routing
+def test_skew_bias_is_minus_alpha_log1p_of_a_ranking():
+    b = inputs.skew_bias(16, 0.1, seed=0).double().numpy()
+    rank = np.rint(np.expm1(-b / 0.1)).astype(int)
+    assert sorted(rank.tolist()) == list(range(16))
+    np.testing.assert_allclose(b, -0.1 * np.log1p(rank), rtol=1e-6)
+
+
+def test_skewed_workload_doubles_the_top_expert_load():
+    # flashinfer PR #4048 "Skewed routing": alpha is chosen so that over many tokens the most
+    # popular expert receives about 2x the mean load.  Checked on 8192 tokens of the recipe.
+    w = inputs.VARIANTS["qwen3-235b-a22b-decode-t512-skewed"].with_(T=8192, H=8, F=8)
+    d = inputs.generate(w, seed=0, device="cpu")
+    ids, _, _ = oracle.route(d["gating_output"].numpy(), w.top_k)
+    counts = np.bincount(ids.reshape(-1), minlength=w.E)
+    assert 1.7 <= counts.max() / counts.mean() <= 2.4
+    plain = inputs.generate(w.with_(skew_alpha=0.0), seed=0, device="cpu")
+    ids0, _, _ = oracle.route(plain["gating_output"].numpy(), w.top_k)
+    c0 = np.bincount(ids0.reshape(-1), minlength=w.E)
+    assert c0.max() / c0.mean() < 1.3
+    assert torch.equal(d["hidden_states"], plain["hidden_states"])
+
+
 def test_stage_references_match_numpy():
     rng = np.random.default_rng(1)
     H, F, E, n = 40, 24, 3, 7
