@@ -98,23 +98,25 @@ def algorithmic_bytes(w, n_unique: int) -> dict:
     """Bytes the path must move at least once (weights of the experts touched, activations)."""
     eb = elt_bytes(w)
     P = w.T * w.top_k
-    weights = n_unique * 3 * w.F * w.H * eb + 3 * w.S * w.H * eb
+    g = 2 if w.gated else 1  # gate/up matrices per expert (ReLU2 has a single projection)
+    weights = n_unique * (g + 1) * w.F * w.H * eb + (g + 1) * w.S * w.H * eb
     acts = w.T * w.H * eb * 2 + w.T * w.E * 4 + (w.E * 4 if w.bias_std > 0 else 0)
     direct = w.T <= 8 and P <= 128
     b1 = w.T * w.H * eb if direct else P * w.H * eb  # gemm1 token rows read
     return dict(
         total=weights + acts,
-        gemm1=n_unique * 2 * w.F * w.H * eb + b1 + P * w.F * eb,
+        gemm1=n_unique * g * w.F * w.H * eb + b1 + P * w.F * eb,
         gemm2=n_unique * w.H * w.F * eb + P * w.F * eb + P * w.H * eb,
-        shared_gemm1=2 * w.S * w.H * eb + w.T * w.H * eb + w.T * w.S * eb,
+        shared_gemm1=g * w.S * w.H * eb + w.T * w.H * eb + w.T * w.S * eb,
         shared_gemm2=w.S * w.H * eb + w.T * w.S * eb + w.T * w.H * eb,
     )
 
 
 def stage_flops(w) -> dict:
     P = w.T * w.top_k
-    return dict(gemm1=2.0 * P * 2 * w.F * w.H, gemm2=2.0 * P * w.F * w.H,
-                shared_gemm1=2.0 * w.T * 2 * w.S * w.H, shared_gemm2=2.0 * w.T * w.S * w.H)
+    g = 2 if w.gated else 1
+    return dict(gemm1=2.0 * P * g * w.F * w.H, gemm2=2.0 * P * w.F * w.H,
+                shared_gemm1=2.0 * w.T * g * w.S * w.H, shared_gemm2=2.0 * w.T * w.S * w.H)
 
 
 def measured_peaks():
@@ -242,7 +244,9 @@ def oracle_rate(w, d, budget_s: float, max_tokens=None):
         i2, w2, _ = oracle.route(g_n, w.top_k, sc, w.renormalize, w.num_expert_group,
                                  w.topk_group, w.routed_scaling_factor, bias)
         oracle.moe_tokens(hid, ids, wts, wgu, wdn, dt, tokens=toks, expert_slot=slot,
-                          num_experts=w.E, shared_w_gate_up=sgu, shared_w_down=sdn)
+                          num_experts=w.E, shared_w_gate_up=sgu, shared_w_down=sdn,
+                          activation={"silu": oracle.ACT_SILU, "gelu_tanh": oracle.ACT_GELU_TANH,
+                                      "relu2": oracle.ACT_RELU2}[w.activation])
         passes += 1
         el = time.perf_counter() - t0
         if el >= budget_s or (passes >= 1 and el * (passes + 1) / passes > 3 * budget_s):
@@ -394,6 +398,7 @@ def run_ours(args, w, ws_n, rank, local):
                    "top_k": w.top_k, "S": w.S, "scoring": w.scoring_func,
                    "num_expert_group": w.num_expert_group, "topk_group": w.topk_group,
                    "routed_scaling_factor": w.routed_scaling_factor,
+                   "activation": w.activation, "skew_alpha": w.skew_alpha,
                    "global_batch": w.T * ws_n, "parallelism": f"replicas x{ws_n}",
                    "l2": l2_note,
                    "timing": ("one CUDA-graph replay of the fused call per step"

@@ -54,12 +54,24 @@ typedef enum {
 typedef enum { MOE_BF16 = 0, MOE_F16 = 1 } moe_dtype_t;
 typedef enum { MOE_SOFTMAX = 0, MOE_SIGMOID = 1 } moe_scoring_t;
 
+/* Expert activation (the routed experts and the shared expert use the same one).
+ *   MOE_ACT_SILU       act = SiLU(gate) * up, SiLU(g) = g / (1 + e^-g)  (TileOPs "MoE" page,
+ *                      op MoEGroupedGemmFwd, activation=silu_and_mul)
+ *   MOE_ACT_GELU_TANH  act = GELU_tanh(gate) * up, GELU_tanh(g) = g/2 (1 + tanh(sqrt(2/pi)
+ *                      (g + 0.044715 g^3)))  (flashinfer W4A16 follow-up PR, "GeGLU-tanh")
+ *   MOE_ACT_RELU2      act = max(h, 0)^2 of a single projection h  (the W4A8 validation list's
+ *                      "ReLU2"; read as squared ReLU with no up half)
+ * The gated forms keep 2F rows per expert in w_gate_up (gate rows [0,F), up rows [F,2F)); ReLU2
+ * keeps F rows.  The same holds for shared_w_gate_up with S. */
+typedef enum { MOE_ACT_SILU = 0, MOE_ACT_GELU_TANH = 1, MOE_ACT_RELU2 = 2 } moe_activation_t;
+
 /* Problem description.  Enumerations are stored as int32 so the layout is fixed. */
 typedef struct {
   int32_t T;           /* tokens */
   int32_t H;           /* hidden size */
   int32_t E;           /* routed experts */
-  int32_t F;           /* expert intermediate size (w_gate_up has 2F rows per expert) */
+  int32_t F;           /* expert intermediate size (w_gate_up rows per expert: 2F, or F for
+                          MOE_ACT_RELU2) */
   int32_t top_k;       /* experts per token */
   int32_t dtype;       /* moe_dtype_t of hidden_states, weights and outputs */
   int32_t scoring;     /* moe_scoring_t */
@@ -68,6 +80,7 @@ typedef struct {
   int32_t topk_group;       /* groups kept when grouping, 1 <= topk_group <= G */
   float routed_scaling_factor; /* multiplies every route weight; 1.0f when unused */
   int32_t S;           /* shared-expert intermediate size; 0 = no shared expert */
+  int32_t activation;  /* moe_activation_t; 0 (MOE_ACT_SILU) when zero-initialised */
 } moe_problem_t;
 
 /* ---------------------------------------------------------------------------------------- */
@@ -102,11 +115,14 @@ moe_status_t moe_workspace_init(void* workspace, size_t workspace_bytes, void* s
  * where W_gate[e] = w_gate_up[e, 0:F, :], W_up[e] = w_gate_up[e, F:2F, :], (e_tj, w[t,j]) come
  * from the router (moe_route), and shared(x) = shared_w_down . (SiLU(Wsg x) * (Wsu x)) with
  * Wsg = shared_w_gate_up[0:S, :], Wsu = shared_w_gate_up[S:2S, :] (added unweighted).
+ * (shown for p->activation = MOE_ACT_SILU; the other activations replace SiLU(.)*(.) as
+ * moe_activation_t states, for the routed and the shared experts alike).
  *   hidden_states   [T,H] dtype
  *   gating_output   [T,E] f32 router logits
- *   w_gate_up       [E,2F,H] dtype;  w_down [E,H,F] dtype
+ *   w_gate_up       [E,2F,H] dtype ([E,F,H] for MOE_ACT_RELU2);  w_down [E,H,F] dtype
  *   correction_bias [E] f32 or NULL (sigmoid scoring only)
- *   shared_w_gate_up [2S,H], shared_w_down [H,S] dtype; both NULL iff p->S == 0
+ *   shared_w_gate_up [2S,H] ([S,H] for MOE_ACT_RELU2), shared_w_down [H,S] dtype; both NULL
+ *                   iff p->S == 0
  *   out             [T,H] dtype (written in full)
  * For T <= 8 the experts run straight from the router's ids (no sort); otherwise the routes are
  * sorted into expert-contiguous rows first.
@@ -168,8 +184,11 @@ moe_status_t moe_align_sort(const moe_problem_t* p, int32_t block_m, const int32
  * (contiguous layout): gathers hidden_states rows in sorted order and, per expert segment e,
  *   act[p, f] = SiLU(sum_h Wg[e,f,h] x[h]) * (sum_h Wu[e,f,h] x[h]),  x = hidden[sorted_ids[p]/k]
  * on the tensor cores (bf16/f16 operands, f32 accumulation, f32 epilogue, one rounding to dtype).
+ * p->activation selects GELU_tanh(.)*(.) or the single-projection max(.,0)^2 instead
+ * (moe_activation_t); the name keeps the default form.
  *   hidden_states [T,H]; block_m, sorted_ids, offsets: as given to / produced by
- *   moe_align_sort; w_gate_up [E,2F,H]; act [cap,F] out, cap = moe_sorted_capacity(p,block_m)
+ *   moe_align_sort; w_gate_up [E,2F,H] ([E,F,H] for MOE_ACT_RELU2); act [cap,F] out,
+ *   cap = moe_sorted_capacity(p,block_m)
  *   (rows of padding slots are written as zero).  workspace: moe_stage_workspace_size bytes.
  */
 moe_status_t moe_gemm1_swiglu(const moe_problem_t* p, int32_t block_m, const void* hidden_states,
@@ -206,8 +225,10 @@ moe_status_t moe_combine(const moe_problem_t* p, const void* y_route, const int3
 
 /*
  * moe_shared_expert_fwd -- TileOPs "MoE" page, op SharedExpertMLPFwd: the dense SwiGLU MLP
- *   shared_out = shared_w_down . (SiLU(Wsg x) * (Wsu x)) for every token, no routing weight.
- *   hidden_states [T,H]; shared_w_gate_up [2S,H]; shared_w_down [H,S];
+ *   shared_out = shared_w_down . (SiLU(Wsg x) * (Wsu x)) for every token, no routing weight
+ *   (or the activation p->activation selects).
+ *   hidden_states [T,H]; shared_w_gate_up [2S,H] ([S,H] for MOE_ACT_RELU2); shared_w_down
+ *   [H,S];
  *   shared_out [T,H] f32 out (the form moe_combine adds).
  */
 moe_status_t moe_shared_expert_fwd(const moe_problem_t* p, const void* hidden_states,

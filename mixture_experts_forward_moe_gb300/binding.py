@@ -21,6 +21,15 @@ MOE_SOFTMAX, MOE_SIGMOID = 0, 1
 
 _DTYPES = {torch.bfloat16: MOE_BF16, torch.float16: MOE_F16}
 _SCORING = {"softmax": MOE_SOFTMAX, "sigmoid": MOE_SIGMOID}
+# moe_activation_t: the two gated forms keep 2F rows per expert in w_gate_up, ReLU2 keeps F.
+_ACTIVATIONS = {"silu": 0, "gelu_tanh": 1, "relu2": 2}
+
+
+def gate_up_rows(activation: str, F: int) -> int:
+    """Rows per expert of w_gate_up for `activation`."""
+    if activation not in _ACTIVATIONS:
+        raise ValueError(f"unsupported activation {activation}")
+    return F if activation == "relu2" else 2 * F
 
 # Every symbol include/moe.h declares.
 EXPORTED = (
@@ -39,6 +48,7 @@ class MoeProblem(ctypes.Structure):
         ("scoring", ctypes.c_int32), ("renormalize", ctypes.c_int32),
         ("num_expert_group", ctypes.c_int32), ("topk_group", ctypes.c_int32),
         ("routed_scaling_factor", ctypes.c_float), ("S", ctypes.c_int32),
+        ("activation", ctypes.c_int32),
     ]
 
 
@@ -135,14 +145,17 @@ def _need(t, name, dtype=None, shape=None):
 
 def make_problem(T, H, E, F, top_k, dtype=torch.bfloat16, scoring_func="softmax",
                  renormalize=True, num_expert_group=0, topk_group=0, routed_scaling_factor=1.0,
-                 S=0) -> MoeProblem:
+                 S=0, activation="silu") -> MoeProblem:
     if dtype not in _DTYPES:
         raise ValueError(f"unsupported dtype {dtype}")
     if scoring_func not in _SCORING:
         raise ValueError(f"unsupported scoring_func {scoring_func}")
+    if activation not in _ACTIVATIONS:
+        raise ValueError(f"unsupported activation {activation}")
     return MoeProblem(int(T), int(H), int(E), int(F), int(top_k), _DTYPES[dtype],
                       _SCORING[scoring_func], int(bool(renormalize)), int(num_expert_group),
-                      int(topk_group), float(routed_scaling_factor), int(S))
+                      int(topk_group), float(routed_scaling_factor), int(S),
+                      _ACTIVATIONS[activation])
 
 
 def workspace_size(prob: MoeProblem) -> int:
@@ -223,24 +236,25 @@ def profile_collect() -> dict:
 def fused_moe_fwd(hidden_states, gating_output, w_gate_up, w_down, top_k, renormalize=True,
                   scoring_func="softmax", correction_bias=None, num_expert_group=0, topk_group=0,
                   routed_scaling_factor=1.0, shared_w_gate_up=None, shared_w_down=None, out=None,
-                  workspace=None, stream=None):
-    """The whole fused MoE forward (include/moe.h: fused_moe_fwd); returns out [T, H]."""
+                  workspace=None, stream=None, activation="silu"):
+    """The whole fused MoE forward (include/moe.h: fused_moe_fwd); returns out [T, H].
+    ``activation``: "silu" (default), "gelu_tanh" or "relu2" (w_gate_up then has F rows)."""
     T, H = hidden_states.shape
-    E, F2, _ = w_gate_up.shape
-    F = F2 // 2
-    S = 0 if shared_w_gate_up is None else shared_w_gate_up.shape[0] // 2
+    E = w_gate_up.shape[0]
+    F = w_down.shape[2]
+    S = 0 if shared_w_down is None else shared_w_down.shape[1]
     dt = hidden_states.dtype
     _need(hidden_states, "hidden_states", dt)
     _need(gating_output, "gating_output", torch.float32, (T, E))
-    _need(w_gate_up, "w_gate_up", dt, (E, 2 * F, H))
+    _need(w_gate_up, "w_gate_up", dt, (E, gate_up_rows(activation, F), H))
     _need(w_down, "w_down", dt, (E, H, F))
     if correction_bias is not None:
         _need(correction_bias, "correction_bias", torch.float32, (E,))
     if S:
-        _need(shared_w_gate_up, "shared_w_gate_up", dt, (2 * S, H))
+        _need(shared_w_gate_up, "shared_w_gate_up", dt, (gate_up_rows(activation, S), H))
         _need(shared_w_down, "shared_w_down", dt, (H, S))
     prob = make_problem(T, H, E, F, top_k, dt, scoring_func, renormalize, num_expert_group,
-                        topk_group, routed_scaling_factor, S)
+                        topk_group, routed_scaling_factor, S, activation)
     nbytes = workspace_size(prob)
     if workspace is None:
         workspace = _workspace(nbytes, hidden_states.device)
@@ -327,17 +341,18 @@ def moe_align_sort_noalloc(topk_ids, num_experts, block_m=1, stream=None):
 
 
 def moe_gemm1_swiglu(hidden_states, sorted_ids, offsets, w_gate_up, top_k, block_m=1,
-                     workspace=None, stream=None):
-    """Grouped gate/up GEMM + SiLU*up (include/moe.h: moe_gemm1_swiglu); returns act [cap, F]."""
+                     workspace=None, stream=None, activation="silu"):
+    """Grouped gate/up GEMM + activation (include/moe.h: moe_gemm1_swiglu); returns act
+    [cap, F].  ``activation``: "silu" (SiLU(gate)*up), "gelu_tanh" or "relu2"."""
     T, H = hidden_states.shape
-    E, F2, _ = w_gate_up.shape
-    F = F2 // 2
+    E, rows, _ = w_gate_up.shape
+    F = rows if activation == "relu2" else rows // 2
     dt = hidden_states.dtype
     _need(hidden_states, "hidden_states", dt)
-    _need(w_gate_up, "w_gate_up", dt, (E, F2, H))
+    _need(w_gate_up, "w_gate_up", dt, (E, gate_up_rows(activation, F), H))
     _need(sorted_ids, "sorted_ids", torch.int32)
     _need(offsets, "offsets", torch.int32, (E + 1,))
-    prob = make_problem(T, H, E, F, top_k, dt)
+    prob = make_problem(T, H, E, F, top_k, dt, activation=activation)
     cap = sorted_capacity(prob, block_m)
     act = torch.empty((max(cap, 1), F), dtype=dt, device=hidden_states.device)
     nbytes = stage_workspace_size(prob, block_m)
@@ -396,15 +411,15 @@ def moe_combine(y_route, inv_route, T, top_k, topk_ids=None, shared_out=None, ou
 
 
 def moe_shared_expert_fwd(hidden_states, shared_w_gate_up, shared_w_down, workspace=None,
-                          stream=None):
-    """Dense SwiGLU shared expert (include/moe.h: moe_shared_expert_fwd); returns f32 [T, H]."""
+                          stream=None, activation="silu"):
+    """Dense shared expert (include/moe.h: moe_shared_expert_fwd); returns f32 [T, H]."""
     T, H = hidden_states.shape
-    S = shared_w_gate_up.shape[0] // 2
+    S = shared_w_down.shape[1]
     dt = hidden_states.dtype
     _need(hidden_states, "hidden_states", dt)
-    _need(shared_w_gate_up, "shared_w_gate_up", dt, (2 * S, H))
+    _need(shared_w_gate_up, "shared_w_gate_up", dt, (gate_up_rows(activation, S), H))
     _need(shared_w_down, "shared_w_down", dt, (H, S))
-    prob = make_problem(T, H, 1, 8, 1, dt, S=S)
+    prob = make_problem(T, H, 1, 8, 1, dt, S=S, activation=activation)
     out = torch.empty((T, H), dtype=torch.float32, device=hidden_states.device)
     nbytes = workspace_size(prob)
     if workspace is None:

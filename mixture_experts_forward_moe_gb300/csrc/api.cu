@@ -84,6 +84,7 @@ moe_status_t check_problem(const moe_problem_t* p) {
   if (p->top_k > p->E) return MOE_ERR_INVALID_ARG;
   if (p->dtype != MOE_BF16 && p->dtype != MOE_F16) return MOE_ERR_INVALID_ARG;
   if (p->scoring != MOE_SOFTMAX && p->scoring != MOE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (p->activation < MOE_ACT_SILU || p->activation > MOE_ACT_RELU2) return MOE_ERR_INVALID_ARG;
   if (!(p->routed_scaling_factor == p->routed_scaling_factor)) return MOE_ERR_INVALID_ARG;
   if (p->num_expert_group < 0 || p->topk_group < 0) return MOE_ERR_INVALID_ARG;
   if (p->num_expert_group > 1) {
@@ -184,6 +185,7 @@ GemmCall base_call(const moe_problem_t& p, int* status) {
   c.T = p.T;
   c.P = p.T * p.top_k;
   c.E = p.E;
+  c.act = p.activation;
   c.tile_rows = kTileRows;
   return c;
 }

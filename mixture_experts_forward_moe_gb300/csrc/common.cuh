@@ -114,13 +114,14 @@ cudaError_t launch_combine(const moe_problem_t& p, const void* y_route,
 enum GemmMode { kSorted = 0, kDirect = 1, kDense = 2 };
 
 struct GemmCall {
-  int gemm1;      // 1: gate/up + SiLU*up; 0: down projection with route weight
+  int gemm1;      // 1: gate/up + activation; 0: down projection with route weight
+  int act;        // gemm1: moe_activation_t (ReLU2: w has n_out rows per expert, not 2*n_out)
   int mode;       // GemmMode
   int dtype;      // moe_dtype_t
   int K;          // reduction length (H for gemm1, F for gemm2)
   int n_out;      // output columns (F for gemm1, H for gemm2)
   int E;          // experts (1 for dense)
-  const void* w;  // weights: gemm1 [E, 2*n_out, K]; gemm2 [E, n_out, K]
+  const void* w;  // weights: gemm1 [E, 2*n_out, K] ([E, n_out, K] for ReLU2); gemm2 [E, n_out, K]
   const void* b;  // token rows [b_rows, K]
   int64_t b_rows; // rows of b (tensor extent)
   void* out;      // [*, n_out]

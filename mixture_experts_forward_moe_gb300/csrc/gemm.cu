@@ -9,7 +9,10 @@
 //    work reads its weight slab from HBM exactly once along K, whatever the number of tokens.
 //  * gemm1: the slab is 128 gate rows [f0, f0+128) and the matching 128 up rows [F+f0, ...),
 //    two MMAs per K step into two TMEM accumulators, so epilogue thread i holds gate row i and
-//    up row i and computes SiLU(g)*u in f32 with no data exchange.
+//    up row i and computes SiLU(g)*u (or GELU_tanh(g)*u) in f32 with no data exchange.  The
+//    single-projection ReLU2 MLP has no up rows: its unit takes 256 consecutive rows as two
+//    128-row halves in the same two accumulators (the second skipped past the last row) and
+//    the epilogue writes max(h,0)^2 of each half to its own 128 output columns.
 //  * gemm2: the slab is 128 rows of w_down; the epilogue multiplies by the route weight.
 //  * Warp roles (192 threads, one CTA per SM, persistent over units):
 //      warp 0  TMA producer: weight boxes {64 x 128} and token boxes of 128, 64 and 16 rows
@@ -69,6 +72,10 @@ struct Cfg {
 struct KParams {
   int mode;
   int token_rows;  // sorted gemm1 with T <= 128: the token side is every row of hidden_states
+  int act;         // gemm1: moe_activation_t
+  int gated;       // gemm1: second weight tile is the up projection (else the next 128 rows)
+  int slab_rows;   // weight rows (output columns) a unit covers: 128, or 256 for ReLU2 gemm1
+  int second_off;  // gemm1: row offset of the second weight tile (F gated, 128 ReLU2)
   int K, n_out, E, n_slabs, num_kb, w_rows_per_expert;
   const Tile* tiles;
   const int* n_tiles;
@@ -84,6 +91,7 @@ struct KParams {
 struct Unit {
   int e, row0, nrows, n_mma, slab;
   int b_row0;  // first token-side row the unit loads
+  bool two;    // gemm1: the second weight tile is used (always when gated)
 };
 
 __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
@@ -125,11 +133,18 @@ __device__ __forceinline__ bool decode_unit(const KParams& p, int u, Unit& U) {
   }
   U.b_row0 = U.row0;
   U.n_mma = round16(U.nrows);
+  U.two = kGemm1 && (p.gated || U.slab * p.slab_rows + kSlab < p.n_out);
   if (kGemm1 && p.token_rows) {  // load all T token rows; the epilogue picks each row's token
     U.b_row0 = 0;
     U.n_mma = round16(p.T);
   }
   return U.nrows > 0;
+}
+
+// GELU, tanh form: g/2 * (1 + tanh(sqrt(2/pi) * (g + 0.044715 g^3))), in f32.
+__device__ __forceinline__ float gelu_tanh_f32(float g) {
+  const float u = 0.7978845608028654f * (g + 0.044715f * g * g * g);
+  return 0.5f * g * (1.0f + tanhf(u));
 }
 
 // Plain bounded wait (ignores the abort flag and the wait-limit knob) used while draining the
@@ -223,8 +238,9 @@ __global__ void __launch_bounds__(192, 1)
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         Unit U;
         if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
-        const uint32_t bytes = C::kABytes + U.n_mma * kBlockK * 2;
-        const int wrow = U.e * p.w_rows_per_expert + U.slab * kSlab;
+        const uint32_t wbytes = U.two ? 2 * kSlab * kBlockK * 2 : kSlab * kBlockK * 2;
+        const uint32_t bytes = wbytes + U.n_mma * kBlockK * 2;
+        const int wrow = U.e * p.w_rows_per_expert + U.slab * p.slab_rows;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.limit_ns, p.status)) {
             ok = false;
@@ -235,8 +251,9 @@ __global__ void __launch_bounds__(192, 1)
           mbar_arrive_expect_tx(&full_bar[stage], bytes);
           const int kx = kb * kBlockK;
           tma_load_2d(sa, &tmW, &full_bar[stage], kx, wrow);
-          if (kGemm1)
-            tma_load_2d(sa + kSlab * kBlockK * 2, &tmW, &full_bar[stage], kx, wrow + p.n_out);
+          if (kGemm1 && U.two)
+            tma_load_2d(sa + kSlab * kBlockK * 2, &tmW, &full_bar[stage], kx,
+                        wrow + p.second_off);
           // Token rows in as few copies as possible: 128-, then 64-, then 16-row boxes.
           int r = 0;
           for (; r + 128 <= U.n_mma; r += 128)
@@ -289,7 +306,7 @@ __global__ void __launch_bounds__(192, 1)
             const uint64_t bdesc = sw128_kmajor_desc(sb + k * 32);
             const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
             umma_f16(d, sw128_kmajor_desc(sa + k * 32), bdesc, idesc, accum);
-            if (kGemm1)
+            if (kGemm1 && U.two)
               umma_f16(d + kN, sw128_kmajor_desc(sa + kSlab * kBlockK * 2 + k * 32), bdesc,
                        idesc, accum);
           }
@@ -350,36 +367,56 @@ __global__ void __launch_bounds__(192, 1)
             tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
         T* stg = reinterpret_cast<T*>(staging);
         T* out = static_cast<T*>(p.out);
-        const int width = min(kSlab, p.n_out - U.slab * kSlab);
-        const int nch = width / 8;
-        for (int c0 = 0; c0 < U.n_mma; c0 += C::kPassCols) {
-          const int c1 = min(U.n_mma, c0 + C::kPassCols);
-          for (int c = c0; c < c1; c += 16) {
-            float g[16], v[16];
-            tmem_ld2_x16(tb + c, tb + kN + c, g, v);
+        const int n_halves = p.gated ? 1 : (U.two ? 2 : 1);
+        for (int half = 0; half < n_halves; ++half) {
+          const int col0 = U.slab * p.slab_rows + half * kSlab;  // first output column
+          const int width = min(kSlab, p.n_out - col0);
+          const int nch = width / 8;
+          for (int c0 = 0; c0 < U.n_mma; c0 += C::kPassCols) {
+            const int c1 = min(U.n_mma, c0 + C::kPassCols);
+            for (int c = c0; c < c1; c += 16) {
+              float h[16];
+              if (p.gated) {
+                float g[16], v[16];
+                tmem_ld2_x16(tb + c, tb + kN + c, g, v);
+                if (p.act == MOE_ACT_GELU_TANH) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float h = __fdividef(g[j], 1.0f + __expf(-g[j])) * v[j];
-              stg[(c - c0 + j) * kSlab + row] = DT<T>::from_f(h);
+                  for (int j = 0; j < 16; ++j) h[j] = gelu_tanh_f32(g[j]) * v[j];
+                } else {
+#pragma unroll
+                  for (int j = 0; j < 16; ++j)
+                    h[j] = __fdividef(g[j], 1.0f + __expf(-g[j])) * v[j];
+                }
+              } else {
+                tmem_ld_x16(tb + (uint32_t)(half * kN) + c, h);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  const float r = fmaxf(h[j], 0.0f);
+                  h[j] = r * r;
+                }
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) stg[(c - c0 + j) * kSlab + row] = DT<T>::from_f(h[j]);
             }
+            if (half == n_halves - 1 && c1 == U.n_mma) {  // every TMEM column has been read
+              tc_fence_before();
+              mbar_arrive(&tempty_bar[acc]);
+            }
+            named_bar_sync(1, 128);
+            // 16-byte stores of whole output rows: entry en, chunk ch of 8 columns.
+            const int en_lo = by_token ? 0 : c0, en_hi = by_token ? n_ent : min(n_ent, c1);
+            for (int idx = et; idx < (en_hi - en_lo) * 16; idx += 128) {
+              const int en = en_lo + (idx >> 4), ch = idx & 15;
+              if (ch >= nch) continue;
+              const int col = ent_col[en];
+              if (col < c0 || col >= c1) continue;
+              const uint4 val =
+                  *reinterpret_cast<const uint4*>(stg + (col - c0) * kSlab + ch * 8);
+              *reinterpret_cast<uint4*>(out + (int64_t)ent_dst[en] * p.n_out + col0 + ch * 8) =
+                  val;
+            }
+            named_bar_sync(1, 128);
           }
-          if (c1 == U.n_mma) {  // every TMEM column of this unit has been read
-            tc_fence_before();
-            mbar_arrive(&tempty_bar[acc]);
-          }
-          named_bar_sync(1, 128);
-          // 16-byte stores of whole output rows: entry en, chunk ch of 8 columns.
-          const int en_lo = by_token ? 0 : c0, en_hi = by_token ? n_ent : min(n_ent, c1);
-          for (int idx = et; idx < (en_hi - en_lo) * 16; idx += 128) {
-            const int en = en_lo + (idx >> 4), ch = idx & 15;
-            if (ch >= nch) continue;
-            const int col = ent_col[en];
-            if (col < c0 || col >= c1) continue;
-            const uint4 val = *reinterpret_cast<const uint4*>(stg + (col - c0) * kSlab + ch * 8);
-            *reinterpret_cast<uint4*>(out + (int64_t)ent_dst[en] * p.n_out + U.slab * kSlab +
-                                      ch * 8) = val;
-          }
-          named_bar_sync(1, 128);
         }
       } else {
         // Each accumulator column (token row) goes to at most one f32 output row, scaled by its
@@ -516,12 +553,17 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   kp.token_rows = c.gemm1 && c.mode == kSorted && c.token_rows;
   if (c.token_rows && (!kp.token_rows || c.T > kTileRows || c.tile_rows != kTileRows))
     return cudaErrorInvalidValue;
+  if (c.gemm1 && (c.act < MOE_ACT_SILU || c.act > MOE_ACT_RELU2)) return cudaErrorInvalidValue;
+  kp.act = c.act;
+  kp.gated = c.gemm1 && c.act != MOE_ACT_RELU2;
+  kp.slab_rows = (c.gemm1 && !kp.gated) ? 2 * kSlab : kSlab;
+  kp.second_off = kp.gated ? c.n_out : kSlab;
   kp.K = c.K;
   kp.n_out = c.n_out;
   kp.E = c.E;
-  kp.n_slabs = (c.n_out + kSlab - 1) / kSlab;
+  kp.n_slabs = (c.n_out + kp.slab_rows - 1) / kp.slab_rows;
   kp.num_kb = (c.K + kBlockK - 1) / kBlockK;
-  kp.w_rows_per_expert = c.gemm1 ? 2 * c.n_out : c.n_out;
+  kp.w_rows_per_expert = kp.gated ? 2 * c.n_out : c.n_out;
   kp.tiles = c.tiles;
   kp.n_tiles = c.n_tiles;
   kp.sorted_ids = c.sorted_ids;

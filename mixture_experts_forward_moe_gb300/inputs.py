@@ -66,7 +66,8 @@ class Workload:
         return dict(top_k=self.top_k, scoring_func=self.scoring_func,
                     renormalize=self.renormalize, num_expert_group=self.num_expert_group,
                     topk_group=self.topk_group,
-                    routed_scaling_factor=self.routed_scaling_factor)
+                    routed_scaling_factor=self.routed_scaling_factor,
+                    activation=self.activation)
 
 
 # The five workloads this project is measured on (sizes from the pages' shape lists).

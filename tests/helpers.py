@@ -98,6 +98,10 @@ def scoring_code(w):
     return oracle.SOFTMAX if w.scoring_func == "softmax" else oracle.SIGMOID
 
 
+ACT_CODES = {"silu": oracle.ACT_SILU, "gelu_tanh": oracle.ACT_GELU_TANH,
+             "relu2": oracle.ACT_RELU2}
+
+
 def oracle_route(w, d):
     bias = None if d["correction_bias"] is None else d["correction_bias"].cpu().numpy()
     return oracle.route(d["gating_output"].cpu().numpy(), w.top_k, scoring_code(w),
@@ -120,7 +124,8 @@ def oracle_fused(w, d, tokens=None, routed=None):
     sd = None if d["shared_w_down"] is None else d["shared_w_down"].cpu()
     out = oracle.moe_tokens(d["hidden_states"].cpu(), ids, wts, wgu, wd, dt_code(w.dtype),
                             tokens=tl, expert_slot=slot, num_experts=w.E,
-                            shared_w_gate_up=sgu, shared_w_down=sd)
+                            shared_w_gate_up=sgu, shared_w_down=sd,
+                            activation=ACT_CODES[w.activation])
     return out, ids, wts, near
 
 

@@ -34,6 +34,18 @@ SMALL = [
     W("sorted-wide-grouped-shared", T=400, H=192, E=16, F=128, top_k=4,
       scoring_func="sigmoid", bias_std=0.1, num_expert_group=4, topk_group=2,
       routed_scaling_factor=2.5, S=256),
+    # activation variants: GeGLU-tanh (gated) and ReLU2 (single projection, 256-row units
+    # whose second half is partial or absent for these F and S)
+    W("direct-t5-gelu-tanh", T=5, H=256, E=16, F=128, top_k=4, activation="gelu_tanh"),
+    W("sorted-t70-gelu-tanh-shared", T=70, H=192, E=12, F=200, top_k=3, scoring_func="sigmoid",
+      bias_std=0.1, routed_scaling_factor=2.5, S=256, activation="gelu_tanh"),
+    W("direct-t4-relu2", T=4, H=256, E=8, F=192, top_k=2, activation="relu2"),
+    W("sorted-t150-relu2-ragged-shared", T=150, H=328, E=12, F=328, top_k=3, S=136,
+      activation="relu2"),
+    W("sorted-t600-relu2-wide", T=600, H=256, E=4, F=384, top_k=2, activation="relu2"),
+    W("sorted-t40-relu2-f16", T=40, H=192, E=8, F=256, top_k=2, activation="relu2",
+      dtype=torch.float16),
+    W("sorted-t300-skewed", T=300, H=256, E=32, F=128, top_k=4, skew_alpha=0.3),
 ]
 
 
@@ -114,6 +126,12 @@ FULL = [
 def test_fused_full_size_workloads(name, n_sample, cuda_device):
     w = inputs.WORKLOADS[name]
     _full_size_check(w, n_sample, cuda_device)
+
+
+@pytest.mark.parametrize("name", sorted(inputs.VARIANTS))
+def test_fused_full_size_variants(name, cuda_device):
+    """Skewed routing and the activation variants on the Qwen3-235B-A22B decode shape."""
+    _full_size_check(inputs.VARIANTS[name], 16, cuda_device)
 
 
 def test_fused_full_size_qwen3_235b_f16(cuda_device):

@@ -27,6 +27,16 @@ GEMM_CASES = [
 ]
 
 
+# (T, k, E, H, F, activation, dtype): the gate/up GEMM with the other activations
+ACT_CASES = [
+    (150, 4, 6, 320, 200, "gelu_tanh", torch.bfloat16),
+    (9, 8, 64, 256, 96, "gelu_tanh", torch.float16),
+    (150, 4, 6, 320, 200, "relu2", torch.bfloat16),   # units of 256 rows: halves 128 + 72
+    (300, 2, 3, 256, 384, "relu2", torch.bfloat16),   # second unit is a single 128-row half
+    (40, 4, 12, 136, 72, "relu2", torch.float16),     # F < 128: no second half at all
+]
+
+
 def _expert_of_rows(sorted_ids, offsets, E):
     eo = np.full(sorted_ids.size, -1, np.int32)
     for e in range(E):
@@ -69,6 +79,28 @@ def test_gemm1_and_gemm2_match_oracle(T, k, E, H, F, block_m, pad, dtype, cuda_d
     assert torch.all(y[:rows][torch.from_numpy(~live).to(cuda_device)] == 0)
     ws = B._workspace(0, cuda_device)
     assert B.get_device_status(ws) == B.MOE_OK
+
+
+@pytest.mark.parametrize("T,k,E,H,F,activation,dtype", ACT_CASES)
+def test_gemm1_activation_variants_match_oracle(T, k, E, H, F, activation, dtype, cuda_device):
+    w = inputs.Workload("g", T=T, H=H, E=E, F=F, top_k=k, dtype=dtype, activation=activation)
+    d = inputs.generate(w, seed=T + E + 1, device=cuda_device)
+    ids = inputs.random_ids(T, k, E, seed=T * 5 + E)
+    srt = oracle.align_sort(ids.numpy(), E, 1)
+    sorted_ids = torch.from_numpy(srt["sorted_ids"]).to(cuda_device)
+    offsets = torch.from_numpy(srt["offsets"]).to(cuda_device)
+    act = B.moe_gemm1_swiglu(d["hidden_states"], sorted_ids, offsets, d["w_gate_up"], k, 1,
+                             activation=activation)
+    torch.cuda.synchronize()
+    eo = _expert_of_rows(srt["sorted_ids"], srt["offsets"], E)
+    rows = srt["offsets"][E]
+    sid = srt["sorted_ids"][:rows]
+    x_rows = d["hidden_states"].cpu()[torch.from_numpy(sid // k).long()]
+    code = {"gelu_tanh": oracle.ACT_GELU_TANH, "relu2": oracle.ACT_RELU2}[activation]
+    ref_act = oracle.expert_act(x_rows, eo[:rows], d["w_gate_up"].cpu(), dt_code(dtype),
+                                activation=code)
+    assert_rounded_close(act[:rows], ref_act, dtype, what=f"act {activation} T={T} F={F}")
+    assert B.get_device_status(B._workspace(0, cuda_device)) == B.MOE_OK
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
