@@ -16,6 +16,16 @@ w_down, shared_w_gate_up, shared_w_down.  Large weights are drawn expert by expe
 rows) so the f32 staging stays small; the chunking is part of the recipe.  w_gate_up has 2F
 rows per expert for the gated activations (SiLU, GeGLU-tanh) and F rows for ReLU2.
 
+NVFP4 experts (flashinfer PR #4048, W4A16): the same N(0, 1/fan_in) draws, quantised per expert
+matrix W [rows, K]: alpha = max|W| / (6 * 448); per block of 16 consecutive k, the E4M3 scale is
+min(448, max|block| / 6 / alpha) rounded to nearest even by torch's float8_e4m3fn conversion;
+each code is the E2M1 value nearest to w / (scale * alpha) (ties toward zero, |v| > 6 clamps to
+6), two codes per byte with element 2i in the low nibble.  A block whose scale rounds to zero
+gets zero codes.
+
+Expert-parallel shard (the same PR's DeepSeek-V3 EP8 benchmark, 32 local of 256 experts): the
+router scores all E experts; only the weights of the ep_local local experts are drawn.
+
 Skewed routing (flashinfer PR #4048 benchmark, "Skewed routing"): when skew_alpha > 0 the
 gating logits of expert e get the fixed bias -skew_alpha * log(1 + rank[e]), rank a random
 permutation of the experts drawn by a second generator seeded with seed + 7919 (so the other
@@ -48,6 +58,13 @@ class Workload:
     dtype: torch.dtype = torch.bfloat16
     activation: str = "silu"       # "silu", "gelu_tanh" (gated) or "relu2" (single projection)
     skew_alpha: float = 0.0         # > 0: skewed routing bias on the gating logits
+    weights: str = "bf16"           # "bf16" (the dtype) or "nvfp4" (W4A16 experts)
+    ep_local: int = 0               # > 0: experts held by this GPU (shard [ep_offset, +ep_local))
+    ep_offset: int = 0
+
+    @property
+    def E_local(self) -> int:
+        return self.ep_local if self.ep_local > 0 else self.E
 
     @property
     def gated(self) -> bool:
@@ -90,6 +107,11 @@ WORKLOADS = {
 # the W4A16 follow-up and the W4A8 validation list).  With N(0,1) softmax logits over 128
 # experts and top-8, skew_alpha = 0.10 gives the most popular expert 2.0x the mean load.
 _Q235 = WORKLOADS["qwen3-235b-a22b-decode-t512"]
+# flashinfer PR #4048's W4A16 benchmark: one DeepSeek-V3 EP8 rank (32 of the 256 experts,
+# top-8, 8 groups keep 4, rsf 2.5, correction-bias scale 0.01) at 32, 512 and 4096 tokens.
+_DSV3_EP8 = Workload("deepseek-v3-ep8-shard", T=32, H=7168, E=256, F=2048, top_k=8,
+                     scoring_func="sigmoid", bias_std=0.01, num_expert_group=8, topk_group=4,
+                     routed_scaling_factor=2.5, ep_local=32)
 VARIANTS = {
     "qwen3-235b-a22b-decode-t512-skewed": _Q235.with_(
         name="qwen3-235b-a22b-decode-t512-skewed", skew_alpha=0.10),
@@ -97,7 +119,13 @@ VARIANTS = {
         name="qwen3-235b-a22b-decode-t512-gelu-tanh", activation="gelu_tanh"),
     "qwen3-235b-a22b-decode-t512-relu2": _Q235.with_(
         name="qwen3-235b-a22b-decode-t512-relu2", activation="relu2"),
+    "qwen3-30b-a3b-decode-t32-w4a16": WORKLOADS["qwen3-30b-a3b-decode-t32"].with_(
+        name="qwen3-30b-a3b-decode-t32-w4a16", weights="nvfp4"),
 }
+for _t in (32, 512, 4096):
+    for _wf in ("bf16", "nvfp4"):
+        _n = f"deepseek-v3-ep8-shard-t{_t}" + ("-w4a16" if _wf == "nvfp4" else "")
+        VARIANTS[_n] = _DSV3_EP8.with_(name=_n, T=_t, weights=_wf)
 
 # Small cases of the same kernels for hardware-counter captures, which must stay at a few GB on
 # the device: the DeepSeek-V3 expert shapes and routing with 32 experts (about 128 routed rows
@@ -142,6 +170,43 @@ def _randn(shape, gen, device, std, dtype):
     return out
 
 
+_E2M1_MIDPOINTS = (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)  # between 0,.5,1,1.5,2,3,4,6
+
+
+def quantize_nvfp4(w: torch.Tensor):
+    """One f32 matrix [rows, K] -> (codes u8 [rows, K/2], scales u8 [rows, K/16], alpha f32)."""
+    rows, K = w.shape
+    amax = float(w.abs().max()) if w.numel() else 0.0
+    alpha = amax / (6.0 * 448.0) if amax > 0 else 1.0
+    alpha = float(torch.tensor(alpha, dtype=torch.float32))
+    blocks = w.view(rows, K // 16, 16)
+    bmax = blocks.abs().amax(-1)
+    sf = (bmax / 6.0 / alpha).clamp_(max=448.0).to(torch.float8_e4m3fn)
+    scale = sf.to(torch.float32) * alpha
+    v = torch.where(scale[..., None] > 0, blocks / scale[..., None].clamp(min=1e-38),
+                    torch.zeros((), device=w.device))
+    mids = torch.tensor(_E2M1_MIDPOINTS, dtype=torch.float32, device=w.device)
+    code = torch.bucketize(v.abs(), mids, right=False).to(torch.uint8)
+    code |= (v < 0).to(torch.uint8) << 3
+    code = code.view(rows, K)
+    q = code[:, 0::2] | (code[:, 1::2] << 4)
+    return q.contiguous(), sf.view(torch.uint8).contiguous(), alpha
+
+
+def _randn_nvfp4(shape, gen, device, std):
+    """N(0, std^2) expert matrices [E, rows, K] drawn as in _randn (f32, chunks of rows per
+    expert), each quantised to NVFP4: returns (codes, scales, alpha [E])."""
+    E, rows, K = shape
+    q = torch.empty((E, rows, K // 2), dtype=torch.uint8, device=device)
+    sf = torch.empty((E, rows, K // 16), dtype=torch.uint8, device=device)
+    alpha = torch.empty((E,), dtype=torch.float32, device=device)
+    for e in range(E):
+        x = _randn((rows, K), gen, device, std, torch.float32)
+        q[e], sf[e], alpha[e] = quantize_nvfp4(x)
+        del x
+    return q, sf, alpha
+
+
 def generate(w: Workload, seed: int = 0, device="cuda") -> dict:
     """All inputs of workload `w` as tensors on `device` (the recipe in the module doc)."""
     gen = torch.Generator(device=device)
@@ -155,8 +220,13 @@ def generate(w: Workload, seed: int = 0, device="cuda") -> dict:
     d["correction_bias"] = (_randn((w.E,), gen, device, w.bias_std, torch.float32)
                             if w.bias_std > 0 else None)
     rows = 2 if w.gated else 1
-    d["w_gate_up"] = _randn((w.E, rows * w.F, w.H), gen, device, 1.0 / math.sqrt(w.H), dt)
-    d["w_down"] = _randn((w.E, w.H, w.F), gen, device, 1.0 / math.sqrt(w.F), dt)
+    El = w.E_local
+    if w.weights == "nvfp4":
+        d["w_gate_up"] = _randn_nvfp4((El, rows * w.F, w.H), gen, device, 1.0 / math.sqrt(w.H))
+        d["w_down"] = _randn_nvfp4((El, w.H, w.F), gen, device, 1.0 / math.sqrt(w.F))
+    else:
+        d["w_gate_up"] = _randn((El, rows * w.F, w.H), gen, device, 1.0 / math.sqrt(w.H), dt)
+        d["w_down"] = _randn((El, w.H, w.F), gen, device, 1.0 / math.sqrt(w.F), dt)
     if w.S > 0:
         d["shared_w_gate_up"] = _randn((rows * w.S, w.H), gen, device, 1.0 / math.sqrt(w.H),
                                        dt)

@@ -78,6 +78,15 @@ def _load():
             _lib.oracle_expert_down.argtypes = [i32, i32, i32, i32, P, P, P, P, P]
             _lib.oracle_combine.argtypes = [i32, i32, i32, i32, P, P, P, P]
             _lib.oracle_num_threads.restype = i32
+            _lib.oracle_e2m1_to_double.restype = f64
+            _lib.oracle_e2m1_to_double.argtypes = [i32]
+            _lib.oracle_e4m3_to_double.restype = f64
+            _lib.oracle_e4m3_to_double.argtypes = [i32]
+            _lib.oracle_nvfp4_dequant.argtypes = [i64, i32, P, P, P, i64, P]
+            _lib.oracle_moe_tokens_w4.argtypes = [i32, P, i32, i32, i32, i32, i32, i32, i32, P,
+                                                  P, P, P, P, P, P, P, P, P]
+            _lib.oracle_expert_act_w4.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P]
+            _lib.oracle_expert_down_w4.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P]
     return _lib
 
 
@@ -235,3 +244,88 @@ def combine(rows, inv_route, top_k, dtype, shared=None):
     _check(_load().oracle_combine(T, H, top_k, dtype, _ptr(rb), _ptr(inv), _ptr(sb), _ptr(out)),
            "oracle_combine")
     return out
+
+
+# ---------------------------------------------------------------------------- NVFP4 weights
+def e2m1_to_double(code: int) -> float:
+    return _load().oracle_e2m1_to_double(int(code))
+
+
+def e4m3_to_double(bits: int) -> float:
+    return _load().oracle_e4m3_to_double(int(bits))
+
+
+def _u8(a):
+    if a is None:
+        return None
+    if hasattr(a, "cpu") and "torch" in type(a).__module__:
+        a = a.cpu().contiguous().view(__import__("torch").uint8).numpy()
+    return np.ascontiguousarray(a, dtype=np.uint8)
+
+
+def _f32(a):
+    if hasattr(a, "cpu") and "torch" in type(a).__module__:
+        a = a.cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def nvfp4_dequant(q, sf, alpha, rows_per_alpha=None):
+    """fp64 [rows, K] from NVFP4 q [.., rows, K/2] u8, sf [.., rows, K/16] u8 and alpha (one per
+    leading index, or per `rows_per_alpha` rows)."""
+    qb, sb, al = _u8(q), _u8(sf), _f32(alpha).reshape(-1)
+    K = qb.shape[-1] * 2
+    rows = qb.size // (K // 2)
+    rpa = rows_per_alpha if rows_per_alpha is not None else rows // al.size
+    out = np.empty((rows, K), np.float64)
+    _check(_load().oracle_nvfp4_dequant(rows, K, _ptr(qb), _ptr(sb), _ptr(al), rpa, _ptr(out)),
+           "oracle_nvfp4_dequant")
+    return out
+
+
+def moe_tokens_w4(hidden, ids, weights, w1, w2, dtype, tokens=None, activation=ACT_SILU):
+    """fp64 fused MoE output with NVFP4 experts.  w1 = (q [E,R1,H/2], sf [E,R1,H/16], alpha [E])
+    for the gate/up projection (R1 = 2F, or F for ReLU2), w2 = (q [E,H,F/2], sf [E,H,F/16],
+    alpha [E]) for the down projection."""
+    hb = _bits(hidden)
+    T, H = hb.shape
+    idv = _c(ids, np.int32)
+    k = idv.shape[1]
+    wv = _c(weights, np.float64)
+    q1, s1, a1 = _u8(w1[0]), _u8(w1[1]), _f32(w1[2])
+    q2, s2, a2 = _u8(w2[0]), _u8(w2[1]), _f32(w2[2])
+    E, _, F2 = q2.shape
+    F = F2 * 2
+    if q1.shape != (E, gate_up_rows(activation, F), H // 2):
+        raise ValueError("w1 does not match the activation and shapes")
+    tl = np.arange(T, dtype=np.int32) if tokens is None else _c(tokens, np.int32)
+    out = np.empty((tl.size, H), np.float64)
+    rc = _load().oracle_moe_tokens_w4(tl.size, _ptr(tl), T, H, E, F, k, dtype, activation,
+                                      _ptr(hb), _ptr(idv), _ptr(wv), _ptr(q1), _ptr(s1), _ptr(a1),
+                                      _ptr(q2), _ptr(s2), _ptr(a2), _ptr(out))
+    _check(rc, "oracle_moe_tokens_w4")
+    return out
+
+
+def expert_act_w4(x_rows, expert_of_row, w1, dtype, activation=ACT_SILU):
+    xb = _bits(x_rows)
+    n, H = xb.shape
+    q1, s1, a1 = _u8(w1[0]), _u8(w1[1]), _f32(w1[2])
+    F = q1.shape[1] if activation == ACT_RELU2 else q1.shape[1] // 2
+    eo = _c(expert_of_row, np.int32)
+    act = np.empty((n, F), np.float64)
+    _check(_load().oracle_expert_act_w4(n, H, F, dtype, activation, _ptr(xb), _ptr(eo), _ptr(q1),
+                                        _ptr(s1), _ptr(a1), _ptr(act)), "oracle_expert_act_w4")
+    return act
+
+
+def expert_down_w4(act_rows, expert_of_row, scale, w2, dtype):
+    ab = _bits(act_rows)
+    n, F = ab.shape
+    q2, s2, a2 = _u8(w2[0]), _u8(w2[1]), _f32(w2[2])
+    H = q2.shape[1]
+    eo = _c(expert_of_row, np.int32)
+    sc = _c(scale, np.float64)
+    y = np.empty((n, H), np.float64)
+    _check(_load().oracle_expert_down_w4(n, H, F, dtype, _ptr(ab), _ptr(eo), _ptr(sc), _ptr(q2),
+                                         _ptr(s2), _ptr(a2), _ptr(y)), "oracle_expert_down_w4")
+    return y

@@ -14,6 +14,9 @@
  *     shared_w_down[H,S].  Op MoEGroupedGemmFwd names the activation silu_and_mul.
  *   - The same page's ops FusedTopKFwd (router), MoEPermuteAlignFwd (sort),
  *     MoEPostPermuteFwd (weighted combine of expert rows through inverse indices).
+ *   - flashinfer PR #4048 (CuTe DSL W4A16 MoE) and its weight-scale placement ablation: NVFP4
+ *     experts, E2M1 codes with E4M3 block scales over 16 elements and an FP32 per-expert scale
+ *     (oracle_moe_tokens_w4 and the stage references after it).
  *   - ROCm/aiter PR #5973 "[FlyDSL] Optimize MI308 MoE decoding (3/3)", section "Changes":
  *     routes whose expert id is -1 are padding and are skipped; the prefill sort returns each
  *     route's sorted row (the inverse map produced here).
@@ -519,6 +522,213 @@ int oracle_combine(int T, int H, int top_k, int dtype, const uint16_t* rows_bits
       if (p < 0) continue;
       for (int h = 0; h < H; ++h) o[h] += tab[rows_bits[(int64_t)p * H + h]];
     }
+  }
+  return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* NVFP4 weights (flashinfer PR #4048 W4A16: NVFP4 weights decoded for a BF16 MMA, the FP32     */
+/* per-expert scale applied to the FP32 accumulator; "W4A16 FP32 weight-scale placement          */
+/* ablation").  A weight is  W[r,k] = e2m1(q) * e4m3(sf[r, k/16]) * alpha[expert]  with two     */
+/* E2M1 codes per byte of q[r, k/2] (element 2i in the low nibble, 2i+1 in the high nibble) and  */
+/* one E4M3 block scale per 16 consecutive k.  The two minifloats are decoded from their         */
+/* definitions (OCP 8-bit and 4-bit floating point):                                           */
+/*   E2M1: sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0, no inf/NaN;                 */
+/*   E4M3: sign bit 7, exponent bits 6..3 (bias 7), mantissa bits 2..0, S.1111.111 is NaN,       */
+/*         no inf.                                                                              */
+/* ------------------------------------------------------------------------------------------ */
+
+double oracle_e2m1_to_double(int code) {
+  const int s = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+  const double mag = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return s ? -mag : mag;
+}
+
+double oracle_e4m3_to_double(int bits) {
+  const int s = (bits >> 7) & 1, e = (bits >> 3) & 15, m = bits & 7;
+  double mag;
+  if (e == 15 && m == 7)
+    mag = NAN;
+  else if (e == 0)
+    mag = ldexp(m / 8.0, -6);
+  else
+    mag = ldexp(1.0 + m / 8.0, e - 7);
+  return s ? -mag : mag;
+}
+
+static double g_e2m1[16];
+static double g_e4m3[256];
+static int g_fp_ready = 0;
+
+static void fp_tables(void) {
+  if (g_fp_ready) return;
+#pragma omp critical(oracle_fp_tables)
+  {
+    if (!g_fp_ready) {
+      for (int c = 0; c < 16; ++c) g_e2m1[c] = oracle_e2m1_to_double(c);
+      for (int b = 0; b < 256; ++b) g_e4m3[b] = oracle_e4m3_to_double(b);
+      g_fp_ready = 1;
+    }
+  }
+}
+
+/* One NVFP4 matrix row: q [K/2] bytes, sf [K/16] bytes. */
+static double nvfp4_elem(const uint8_t* q, const uint8_t* sf, int k) {
+  const uint8_t byte = q[k >> 1];
+  const int code = (k & 1) ? (byte >> 4) : (byte & 15);
+  return g_e2m1[code] * g_e4m3[sf[k >> 4]];
+}
+
+/* Dequantise n_rows rows of K: out[r,k] = W[r,k] with alpha[r / rows_per_alpha]. */
+int oracle_nvfp4_dequant(int64_t n_rows, int K, const uint8_t* q, const uint8_t* sf,
+                         const float* alpha, int64_t rows_per_alpha, double* out) {
+  if (n_rows < 0 || K <= 0 || K % 16 != 0 || rows_per_alpha <= 0) return ORACLE_ERR_ARG;
+  fp_tables();
+  for (int64_t r = 0; r < n_rows; ++r) {
+    const double a = (double)alpha[r / rows_per_alpha];
+    for (int k = 0; k < K; ++k)
+      out[r * K + k] = nvfp4_elem(q + r * (K / 2), sf + r * (K / 16), k) * a;
+  }
+  return ORACLE_OK;
+}
+
+/* NVFP4 expert of `rows` rows of length K: bytes of q and sf per expert. */
+typedef struct {
+  const uint8_t* q;
+  const uint8_t* sf;
+  double alpha;
+  int K;
+} w4_mat;
+
+static w4_mat w4_expert(const uint8_t* q, const uint8_t* sf, const float* alpha, int e,
+                        int64_t rows, int K) {
+  w4_mat m;
+  m.q = q + (int64_t)e * rows * (K / 2);
+  m.sf = sf + (int64_t)e * rows * (K / 16);
+  m.alpha = (double)alpha[e];
+  m.K = K;
+  return m;
+}
+
+/* sum_k W[row, k] x[k] for an NVFP4 matrix (alpha applied to the sum, which is exact math). */
+static double w4_dot(const w4_mat* m, int64_t row, const double* x) {
+  const uint8_t* q = m->q + row * (m->K / 2);
+  const uint8_t* sf = m->sf + row * (m->K / 16);
+  double s = 0.0;
+  for (int k = 0; k < m->K; ++k) s += nvfp4_elem(q, sf, k) * x[k];
+  return m->alpha * s;
+}
+
+static void act_rows_w4(const w4_mat* wgu, const double* x, int F, int activation, double* act) {
+  for (int f = 0; f < F; ++f) {
+    const double g = w4_dot(wgu, f, x);
+    if (activation == ORACLE_ACT_RELU2) {
+      const double r = g > 0.0 ? g : 0.0;
+      act[f] = r * r;
+      continue;
+    }
+    const double u = w4_dot(wgu, (int64_t)F + f, x);
+    act[f] = activation == ORACLE_ACT_GELU_TANH ? gelu_tanh(g) * u : g / (1.0 + exp(-g)) * u;
+  }
+}
+
+/*
+ * oracle_moe_tokens_w4: oracle_moe_tokens with NVFP4 routed experts (no shared expert):
+ *   w1q [E, R1, H/2], w1sf [E, R1, H/16], w1a [E]   (R1 = 2F gated, F for ReLU2)
+ *   w2q [E, H, F/2],  w2sf [E, H, F/16],  w2a [E]
+ * The activations (hidden) are 16-bit; the weight of each term is the NVFP4 value above.
+ */
+int oracle_moe_tokens_w4(int n_tok, const int32_t* tok_list, int T, int H, int E, int F,
+                         int top_k, int dtype, int activation, const uint16_t* hidden,
+                         const int32_t* ids, const double* weights, const uint8_t* w1q,
+                         const uint8_t* w1sf, const float* w1a, const uint8_t* w2q,
+                         const uint8_t* w2sf, const float* w2a, double* out) {
+  if (n_tok < 0 || H <= 0 || E <= 0 || F <= 0 || top_k <= 0 || (dtype != 0 && dtype != 1) ||
+      activation < ORACLE_ACT_SILU || activation > ORACLE_ACT_RELU2 || H % 16 || F % 16)
+    return ORACLE_ERR_ARG;
+  const double* tab = decode_table(dtype);
+  fp_tables();
+  const int64_t R1 = gate_up_rows(activation, F);
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (int i = 0; i < n_tok; ++i) {
+    int t = tok_list ? tok_list[i] : i;
+    double* o = out + (int64_t)i * H;
+    if (t < 0 || t >= T) {
+      bad |= 1;
+      continue;
+    }
+    double* x = (double*)malloc(sizeof(double) * H);
+    double* act = (double*)malloc(sizeof(double) * F);
+    for (int h = 0; h < H; ++h) x[h] = tab[hidden[(int64_t)t * H + h]];
+    for (int h = 0; h < H; ++h) o[h] = 0.0;
+    for (int j = 0; j < top_k; ++j) {
+      int e = ids[(int64_t)t * top_k + j];
+      if (e == -1) continue;
+      if (e < -1 || e >= E) {
+        bad |= 2;
+        continue;
+      }
+      const w4_mat m1 = w4_expert(w1q, w1sf, w1a, e, R1, H);
+      const w4_mat m2 = w4_expert(w2q, w2sf, w2a, e, H, F);
+      act_rows_w4(&m1, x, F, activation, act);
+      const double w = weights[(int64_t)t * top_k + j];
+      for (int h = 0; h < H; ++h) o[h] += w * w4_dot(&m2, h, act);
+    }
+    free(x);
+    free(act);
+  }
+  if (bad & 2) return ORACLE_ERR_ID;
+  if (bad) return ORACLE_ERR_ARG;
+  return ORACLE_OK;
+}
+
+/* Stage references with NVFP4 weights: act rows (gate/up) and route-scaled down rows. */
+int oracle_expert_act_w4(int n_rows, int H, int F, int dtype, int activation,
+                         const uint16_t* x_bits, const int32_t* expert_of_row, const uint8_t* w1q,
+                         const uint8_t* w1sf, const float* w1a, double* act) {
+  if (n_rows < 0 || H <= 0 || F <= 0 || H % 16 || activation < ORACLE_ACT_SILU ||
+      activation > ORACLE_ACT_RELU2)
+    return ORACLE_ERR_ARG;
+  const double* tab = decode_table(dtype);
+  fp_tables();
+  const int64_t R1 = gate_up_rows(activation, F);
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int r = 0; r < n_rows; ++r) {
+    int e = expert_of_row[r];
+    double* a = act + (int64_t)r * F;
+    if (e < 0) {
+      for (int f = 0; f < F; ++f) a[f] = 0.0;
+      continue;
+    }
+    double* x = (double*)malloc(sizeof(double) * H);
+    for (int h = 0; h < H; ++h) x[h] = tab[x_bits[(int64_t)r * H + h]];
+    const w4_mat m1 = w4_expert(w1q, w1sf, w1a, e, R1, H);
+    act_rows_w4(&m1, x, F, activation, a);
+    free(x);
+  }
+  return ORACLE_OK;
+}
+
+int oracle_expert_down_w4(int n_rows, int H, int F, int dtype, const uint16_t* act_bits,
+                          const int32_t* expert_of_row, const double* scale, const uint8_t* w2q,
+                          const uint8_t* w2sf, const float* w2a, double* y) {
+  if (n_rows < 0 || H <= 0 || F <= 0 || F % 16) return ORACLE_ERR_ARG;
+  const double* tab = decode_table(dtype);
+  fp_tables();
+#pragma omp parallel for schedule(dynamic, 4)
+  for (int r = 0; r < n_rows; ++r) {
+    int e = expert_of_row[r];
+    double* o = y + (int64_t)r * H;
+    if (e < 0) {
+      for (int h = 0; h < H; ++h) o[h] = 0.0;
+      continue;
+    }
+    double* a = (double*)malloc(sizeof(double) * F);
+    for (int f = 0; f < F; ++f) a[f] = tab[act_bits[(int64_t)r * F + f]];
+    const w4_mat m2 = w4_expert(w2q, w2sf, w2a, e, H, F);
+    for (int h = 0; h < H; ++h) o[h] = scale[r] * w4_dot(&m2, h, a);
+    free(a);
   }
   return ORACLE_OK;
 }

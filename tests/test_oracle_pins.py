@@ -400,6 +400,110 @@ def test_activation_rejects_mismatched_weight_rows():
                           activation=oracle.ACT_RELU2)
 
 
+# ------------------------------------------------------------------------- NVFP4 weights
+def test_e4m3_decode_matches_torch_float8_every_pattern():
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn)
+    ref = ref.to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_double(b) for b in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    np.testing.assert_array_equal(got[~np.isnan(got)], ref[~np.isnan(ref)])
+    assert np.sum(np.isnan(got)) == 2  # S.1111.111 only
+
+
+def test_e2m1_decode_is_the_fp4_value_set():
+    vals = [oracle.e2m1_to_double(c) for c in range(16)]
+    # magnitudes: zero, the subnormal 1/2, and m * 2^e for m in {1, 1.5}, e in {0, 1, 2}
+    expect = sorted({0.0, 0.5} | {m * 2.0 ** e for m in (1.0, 1.5) for e in (0, 1, 2)})
+    assert vals[:8] == expect  # codes 0..7 in increasing order
+    for c in range(8):
+        assert vals[c | 8] == -vals[c] and math.copysign(1.0, vals[c | 8]) == -1.0
+
+
+def test_e2m1_matches_e4m3_with_the_same_exponent_and_mantissa():
+    # E2M1 (bias 1, 1 mantissa bit) and E4M3 (bias 7, 3 mantissa bits) are the same kind of
+    # minifloat: code (s, e, m) with e > 0 equals the E4M3 code (s, e + 6, m << 2); the E2M1
+    # subnormal 0.5 is the E4M3 normal 2^-1.  Decoded here by torch.
+    f8 = lambda b: float(torch.tensor([b], dtype=torch.uint8).view(torch.float8_e4m3fn).float())
+    for c in range(16):
+        s, e, m = c >> 3, (c >> 1) & 3, c & 1
+        if e > 0:
+            b = (s << 7) | ((e + 6) << 3) | (m << 2)
+        else:
+            b = (s << 7) | ((6 << 3) if m else 0)
+        assert oracle.e2m1_to_double(c) == f8(b), c
+
+
+def test_nvfp4_dequant_layout_nibbles_and_blocks():
+    rows, K = 3, 64
+    q = np.zeros((rows, K // 2), np.uint8)
+    sf = np.full((rows, K // 16), 0x38, np.uint8)  # E4M3 1.0
+    q[1, 5] = 0x3 | (0xC << 4)   # k = 10 -> code 3 (1.5), k = 11 -> code 12 (-2)
+    sf[1, 0] = 0x40               # block 0 (k 0..15) scale 2.0
+    sf[2, 3] = 0x30               # block 3 scale 0.5
+    q[2, 31] = 0x70               # k = 63 -> code 7 (6)
+    W = oracle.nvfp4_dequant(q, sf, np.array([4.0], np.float32))
+    expect = np.zeros((rows, K))
+    expect[1, 10], expect[1, 11] = 1.5 * 2.0 * 4.0, -2.0 * 2.0 * 4.0
+    expect[2, 63] = 6.0 * 0.5 * 4.0
+    np.testing.assert_array_equal(W, expect)
+
+
+def _w4_case(seed, T=6, E=3, H=64, F=32, k=2, activation="silu"):
+    w = inputs.Workload("t", T=T, H=H, E=E, F=F, top_k=k, weights="nvfp4", activation=activation)
+    d = inputs.generate(w, seed=seed, device="cpu")
+    ids, wts, _ = oracle.route(d["gating_output"].numpy(), k)
+    return w, d, ids, wts
+
+
+@pytest.mark.parametrize("activation", [oracle.ACT_SILU, oracle.ACT_GELU_TANH, oracle.ACT_RELU2])
+def test_w4_tokens_equal_bf16_tokens_on_the_dequantised_weights(activation):
+    # With a power-of-two alpha every NVFP4 weight is exactly a bf16 value, so the NVFP4 oracle
+    # must give exactly the bf16 oracle's result on the dequantised weights.
+    name = {oracle.ACT_SILU: "silu", oracle.ACT_GELU_TANH: "gelu_tanh", oracle.ACT_RELU2: "relu2"}
+    w, d, ids, wts = _w4_case(11 + activation, activation=name[activation])
+    (q1, s1, _), (q2, s2, _) = d["w_gate_up"], d["w_down"]
+    a1 = torch.tensor([2.0 ** -6, 2.0 ** -5, 2.0 ** -7])
+    a2 = torch.tensor([2.0 ** -4, 2.0 ** -8, 2.0 ** -5])
+    W1 = torch.from_numpy(oracle.nvfp4_dequant(q1, s1, a1)).view(q1.shape[0], q1.shape[1], -1)
+    W2 = torch.from_numpy(oracle.nvfp4_dequant(q2, s2, a2)).view(q2.shape[0], q2.shape[1], -1)
+    assert torch.equal(W1.to(torch.bfloat16).double(), W1)  # exactly representable
+    out4 = oracle.moe_tokens_w4(d["hidden_states"], ids, wts, (q1, s1, a1), (q2, s2, a2),
+                                oracle.BF16, activation=activation)
+    out16 = oracle.moe_tokens(d["hidden_states"], ids, wts, W1.to(torch.bfloat16),
+                              W2.to(torch.bfloat16), oracle.BF16, activation=activation)
+    np.testing.assert_array_equal(out4, out16)
+
+
+def test_w4_stage_references_compose_to_the_fused_oracle():
+    w, d, ids, wts = _w4_case(21, T=5, E=4, k=3)
+    x = d["hidden_states"]
+    out = oracle.moe_tokens_w4(x, ids, wts, d["w_gate_up"], d["w_down"], oracle.BF16)
+    rows = x.repeat_interleave(3, 0)
+    act = oracle.expert_act_w4(rows, ids.reshape(-1), d["w_gate_up"], oracle.BF16)
+    # the stage reference for the down projection reads 16-bit act rows; feed it the exact
+    # act through a second call with act already in bf16 and compare against a tolerance
+    act16 = torch.from_numpy(act).to(torch.bfloat16)
+    y = oracle.expert_down_w4(act16, ids.reshape(-1), wts.reshape(-1), d["w_down"], oracle.BF16)
+    summed = y.reshape(5, 3, -1).sum(1)
+    rms = np.sqrt(np.mean(out ** 2))
+    assert np.max(np.abs(summed - out)) < 2e-2 * rms  # only the bf16 rounding of act differs
+
+
+def test_ep_shards_partition_the_full_output():
+    # Expert-parallel shards: the router's ids restricted to a shard (others -> -1) give that
+    # shard's partial output; the shards' partial outputs sum to the full output.
+    w = inputs.Workload("t", T=7, H=32, E=8, F=16, top_k=3)
+    d = inputs.generate(w, seed=4, device="cpu")
+    ids, wts, _ = oracle.route(d["gating_output"].numpy(), 3)
+    full = oracle.moe_tokens(d["hidden_states"], ids, wts, d["w_gate_up"], d["w_down"], 0)
+    total = np.zeros_like(full)
+    for off in (0, 4):
+        loc = np.where((ids >= off) & (ids < off + 4), ids - off, -1).astype(np.int32)
+        total += oracle.moe_tokens(d["hidden_states"], loc, wts, d["w_gate_up"][off:off + 4],
+                                   d["w_down"][off:off + 4], 0)
+    np.testing.assert_allclose(total, full, rtol=1e-12, atol=1e-14)
+
+
 # ------------------------------------------------------------------------- skewed routing
 def test_skew_bias_is_minus_alpha_log1p_of_a_ranking():
     b = inputs.skew_bias(16, 0.1, seed=0).double().numpy()
