@@ -49,6 +49,14 @@ FALLBACK_BF16_TFLOPS = 1900.0
 
 # Throughput printed on the TileOPs benchmark page ("MoE" section, FusedMoEFwd and
 # FusedMoESharedExpertFwd tables) for the same shapes; hardware not stated there.
+# Context only (other hardware, other routing seed): the W4A16 PR's B300 medians, ms per call of
+# one DeepSeek-V3 EP8 rank (flashinfer PR #4048, CuTe W4A16 inference / TRTLLM BF16 columns).
+PUBLISHED_MS = {
+    "deepseek-v3-ep8-shard-t32-w4a16": 0.118, "deepseek-v3-ep8-shard-t512-w4a16": 0.169,
+    "deepseek-v3-ep8-shard-t4096-w4a16": 0.363, "deepseek-v3-ep8-shard-t32": 0.285,
+    "deepseek-v3-ep8-shard-t512": 0.435, "deepseek-v3-ep8-shard-t4096": 0.529,
+}
+
 PUBLISHED_TFLOPS = {
     ("qwen3-30b-a3b-decode-t32", "bf16"): 9.11,
     ("qwen3-235b-a22b-decode-t512", "bf16"): 128.0,
@@ -94,26 +102,34 @@ def elt_bytes(w) -> int:
     return 2
 
 
-def algorithmic_bytes(w, n_unique: int) -> dict:
-    """Bytes the path must move at least once (weights of the experts touched, activations)."""
+def weight_bytes_per_elem(w) -> float:
+    """Bytes per routed-expert weight: 2 (bf16/f16), or 0.5 + 1/16 for NVFP4 (an E2M1 code and
+    a sixteenth of an E4M3 block scale)."""
+    return 0.5 + 1.0 / 16.0 if w.weights == "nvfp4" else float(elt_bytes(w))
+
+
+def algorithmic_bytes(w, n_unique: int, P=None) -> dict:
+    """Bytes the path must move at least once (weights of the experts touched, activations).
+    P: routes computed here (T * top_k, or the routes to local experts on a shard)."""
     eb = elt_bytes(w)
-    P = w.T * w.top_k
+    wb = weight_bytes_per_elem(w)
+    P = w.T * w.top_k if P is None else P
     g = 2 if w.gated else 1  # gate/up matrices per expert (ReLU2 has a single projection)
-    weights = n_unique * (g + 1) * w.F * w.H * eb + (g + 1) * w.S * w.H * eb
+    weights = n_unique * (g + 1) * w.F * w.H * wb + (g + 1) * w.S * w.H * eb
     acts = w.T * w.H * eb * 2 + w.T * w.E * 4 + (w.E * 4 if w.bias_std > 0 else 0)
     direct = w.T <= 8 and P <= 128
     b1 = w.T * w.H * eb if direct else P * w.H * eb  # gemm1 token rows read
     return dict(
         total=weights + acts,
-        gemm1=n_unique * g * w.F * w.H * eb + b1 + P * w.F * eb,
-        gemm2=n_unique * w.H * w.F * eb + P * w.F * eb + P * w.H * eb,
+        gemm1=n_unique * g * w.F * w.H * wb + b1 + P * w.F * eb,
+        gemm2=n_unique * w.H * w.F * wb + P * w.F * eb + P * w.H * eb,
         shared_gemm1=g * w.S * w.H * eb + w.T * w.H * eb + w.T * w.S * eb,
         shared_gemm2=w.S * w.H * eb + w.T * w.S * eb + w.T * w.H * eb,
     )
 
 
-def stage_flops(w) -> dict:
-    P = w.T * w.top_k
+def stage_flops(w, P=None) -> dict:
+    P = w.T * w.top_k if P is None else P
     g = 2 if w.gated else 1
     return dict(gemm1=2.0 * P * g * w.F * w.H, gemm2=2.0 * P * w.F * w.H,
                 shared_gemm1=2.0 * w.T * g * w.S * w.H, shared_gemm2=2.0 * w.T * w.S * w.H)
@@ -207,6 +223,16 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def local_ids(w, ids):
+    """Global router ids as indices of this shard's experts (-1 elsewhere); identity when every
+    expert is local."""
+    import numpy as np
+    if w.ep_local <= 0:
+        return ids
+    off = w.ep_offset
+    return np.where((ids >= off) & (ids < off + w.ep_local), ids - off, -1).astype(np.int32)
+
+
 # ------------------------------------------------------------------------------- CPU oracle arm
 def oracle_rate(w, d, budget_s: float, max_tokens=None):
     """Time the CPU oracle (routing + per-token expert MLP) on a bounded token sample.
@@ -216,20 +242,39 @@ def oracle_rate(w, d, budget_s: float, max_tokens=None):
     import torch
 
     import oracle
-    flops_tok = w.flops() / w.T
     gating = d["gating_output"].cpu().numpy()
     bias = None if d["correction_bias"] is None else d["correction_bias"].cpu().numpy()
     sc = oracle.SOFTMAX if w.scoring_func == "softmax" else oracle.SIGMOID
     ids, wts, _ = oracle.route(gating, w.top_k, sc, w.renormalize, w.num_expert_group,
                                w.topk_group, w.routed_scaling_factor, bias)
+    ids = local_ids(w, ids)
+    flops_tok = w.flops(int((ids >= 0).sum())) / w.T
     # Sample: the first n tokens, n sized for about 1/4 of the budget per pass.
     cores = oracle.num_threads()
     n = max(1, min(w.T, int(0.25 * budget_s * 2e9 * cores / flops_tok)))
     if max_tokens:
         n = min(n, max_tokens)
     toks = np.arange(n, dtype=np.int32)
+    act_code = {"silu": oracle.ACT_SILU, "gelu_tanh": oracle.ACT_GELU_TANH,
+                "relu2": oracle.ACT_RELU2}[w.activation]
+    if w.weights == "nvfp4":
+        w1 = tuple(t.cpu() for t in d.get("w_gate_up_canonical", d["w_gate_up"]))
+        w2 = tuple(t.cpu() for t in d.get("w_down_canonical", d["w_down"]))
+        g_n = np.ascontiguousarray(gating[:n])
+        hid = d["hidden_states"].cpu()
+        passes, t0 = 0, time.perf_counter()
+        while True:
+            oracle.route(g_n, w.top_k, sc, w.renormalize, w.num_expert_group, w.topk_group,
+                         w.routed_scaling_factor, bias)
+            oracle.moe_tokens_w4(hid, ids, wts, w1, w2, oracle.BF16, tokens=toks,
+                                 activation=act_code)
+            passes += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s or (passes >= 1 and el * (passes + 1) / passes > 3 * budget_s):
+                break
+        return flops_tok * n * passes / el / 1e12, el, n, passes, cores
     used = sorted(set(int(e) for e in ids[:n].reshape(-1) if e >= 0))
-    slot = np.full(w.E, -1, np.int32)
+    slot = np.full(w.E_local, -1, np.int32)
     slot[used] = np.arange(len(used), dtype=np.int32)
     idx = torch.tensor(used, dtype=torch.long, device=d["w_gate_up"].device)
     wgu = d["w_gate_up"].index_select(0, idx).cpu()
@@ -244,9 +289,8 @@ def oracle_rate(w, d, budget_s: float, max_tokens=None):
         i2, w2, _ = oracle.route(g_n, w.top_k, sc, w.renormalize, w.num_expert_group,
                                  w.topk_group, w.routed_scaling_factor, bias)
         oracle.moe_tokens(hid, ids, wts, wgu, wdn, dt, tokens=toks, expert_slot=slot,
-                          num_experts=w.E, shared_w_gate_up=sgu, shared_w_down=sdn,
-                          activation={"silu": oracle.ACT_SILU, "gelu_tanh": oracle.ACT_GELU_TANH,
-                                      "relu2": oracle.ACT_RELU2}[w.activation])
+                          num_experts=w.E_local, shared_w_gate_up=sgu, shared_w_down=sdn,
+                          activation=act_code)
         passes += 1
         el = time.perf_counter() - t0
         if el >= budget_s or (passes >= 1 and el * (passes + 1) / passes > 3 * budget_s):
@@ -265,8 +309,15 @@ def run_ours(args, w, ws_n, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     d = inputs.generate(w, seed=args.seed, device=dev)
-    kw = dict(correction_bias=d["correction_bias"], shared_w_gate_up=d["shared_w_gate_up"],
-              shared_w_down=d["shared_w_down"], **w.kwargs())
+    w4 = w.weights == "nvfp4"
+    kw = dict(correction_bias=d["correction_bias"], **w.kwargs())
+    if w4:  # the library's packed NVFP4 layout, made once when the weights are loaded
+        d["w_gate_up_canonical"], d["w_down_canonical"] = d["w_gate_up"], d["w_down"]
+        d["w_gate_up"] = B.pack_nvfp4_weights(*d["w_gate_up"])
+        d["w_down"] = B.pack_nvfp4_weights(*d["w_down"])
+    else:
+        kw.update(shared_w_gate_up=d["shared_w_gate_up"], shared_w_down=d["shared_w_down"])
+    fwd = B.fused_moe_fwd_w4a16 if w4 else B.fused_moe_fwd
     prob = B.make_problem(w.T, w.H, w.E, w.F, w.top_k, w.dtype, w.scoring_func, w.renormalize,
                           w.num_expert_group, w.topk_group, w.routed_scaling_factor, w.S)
     wsp = B.new_workspace(B.workspace_size(prob), dev)
@@ -274,17 +325,19 @@ def run_ours(args, w, ws_n, rank, local):
     stream = torch.cuda.current_stream()
 
     def step():
-        B.fused_moe_fwd(d["hidden_states"], d["gating_output"], d["w_gate_up"], d["w_down"],
-                        out=out, workspace=wsp, **kw)
+        fwd(d["hidden_states"], d["gating_output"], d["w_gate_up"], d["w_down"], out=out,
+            workspace=wsp, **kw)
 
     ids, _ = B.moe_route(d["gating_output"], w.top_k, w.scoring_func, w.renormalize,
                          d["correction_bias"], w.num_expert_group, w.topk_group,
                          w.routed_scaling_factor)
-    n_unique = int(torch.unique(ids[ids >= 0]).numel())
+    lids = torch.from_numpy(local_ids(w, ids.cpu().numpy()))
+    n_unique = int(torch.unique(lids[lids >= 0]).numel())
+    P_local = int((lids >= 0).sum())  # routes this GPU computes
     # Between steps: when the expert weights one step streams exceed twice the L2, nothing of a
     # step's weights survives into the next and no flush is needed (a flush by writing would
     # leave dirty lines that the next step pays to write back); otherwise flush by a write.
-    weight_bytes = algorithmic_bytes(w, n_unique)["total"]
+    weight_bytes = algorithmic_bytes(w, n_unique, P_local)["total"]
     if weight_bytes > 2 * L2_BYTES:
         flush = None
         l2_note = (f"no flush: each step streams {weight_bytes / 1e9:.2f} GB of expert weights, "
@@ -361,10 +414,10 @@ def run_ours(args, w, ws_n, rank, local):
     if st != B.MOE_OK:
         raise RuntimeError(f"device status after timed steps: {B.status_string(st)}")
 
-    flops = w.flops()
+    flops = w.flops(P_local)
     value = job_throughput(flops, ws_n, args.steps, max_ms) / 1e12
     ms_per_step = max_ms / args.steps
-    ab = algorithmic_bytes(w, n_unique)
+    ab = algorithmic_bytes(w, n_unique, P_local)
     hbm_gbs, bf16_peak, bf16_sust, peak_src = measured_peaks()
     launches = sum(v[2] for v in prof_clean.values())
 
@@ -374,17 +427,27 @@ def run_ours(args, w, ws_n, rank, local):
     dom_avg = dom_ms / max(dom_calls, 1)
     achieved = ab[dom] / (dom_avg * 1e-3) / 1e9
     traffic = recorded_traffic(w.name, dom)
-    roofline = {"bound": "hbm", "kernel": f"moe_gemm_kernel ({dom})", "achieved": achieved,
-                "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
-                "traffic": traffic, "algorithmic_bytes": ab[dom], "avg_launch_ms": dom_avg,
-                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
-                if peak_src == "measured" else "fallback 6.8 TB/s",
-                "timing": "event pair around each launch of the kernel over a second loop of "
-                          "the same K steps"}
-    tensor = {"achieved_tflops": stage_flops(w)[dom] / (dom_avg * 1e-3) / 1e12,
+    hbm = {"bound": "hbm", "kernel": f"moe_gemm_kernel ({dom})", "achieved": achieved,
+           "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
+           "traffic": traffic, "algorithmic_bytes": ab[dom], "avg_launch_ms": dom_avg,
+           "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+           if peak_src == "measured" else "fallback 6.8 TB/s",
+           "timing": "event pair around each launch of the kernel over a second loop of "
+                     "the same K steps"}
+    dom_flops = stage_flops(w, P_local)[dom]
+    tensor = {"achieved_tflops": dom_flops / (dom_avg * 1e-3) / 1e12,
               "peak_tflops": bf16_sust, "peak_source": f"{peak_src} bf16_tflops_sustained"}
     tensor["frac"] = tensor["achieved_tflops"] / bf16_sust
-    roofline["tensor"] = tensor
+    # The bound is whichever resource the kernel's algorithmic work needs longer on.
+    if dom_flops / (bf16_sust * 1e12) > ab[dom] / (hbm_gbs * 1e9):
+        roofline = {"bound": "tensor", "kernel": hbm["kernel"],
+                    "achieved": tensor["achieved_tflops"], "peak": bf16_sust,
+                    "unit": "TFLOP/s", "frac": tensor["frac"], "traffic": traffic,
+                    "algorithmic_flops": dom_flops, "avg_launch_ms": dom_avg,
+                    "peak_source": tensor["peak_source"], "timing": hbm["timing"], "hbm": hbm}
+    else:
+        roofline = hbm
+        roofline["tensor"] = tensor
     stages = {k: {"avg_ms": v[0] / v[1], "calls": v[1]} for k, v in prof.items() if v[1]}
 
     res = {
@@ -399,6 +462,8 @@ def run_ours(args, w, ws_n, rank, local):
                    "num_expert_group": w.num_expert_group, "topk_group": w.topk_group,
                    "routed_scaling_factor": w.routed_scaling_factor,
                    "activation": w.activation, "skew_alpha": w.skew_alpha,
+                   "weights": w.weights, "ep_local_experts": w.ep_local,
+                   "routes_computed": P_local,
                    "global_batch": w.T * ws_n, "parallelism": f"replicas x{ws_n}",
                    "l2": l2_note,
                    "timing": ("one CUDA-graph replay of the fused call per step"
@@ -411,6 +476,9 @@ def run_ours(args, w, ws_n, rank, local):
         "unique_experts": n_unique, "roofline": roofline, "gpu_launches": launches,
         "launches_per_step": launches / args.steps, "stages": stages, "clocks": clk,
     }
+    if w.name in PUBLISHED_MS:
+        res["context_published_ms"] = {"ms": PUBLISHED_MS[w.name],
+                                       "where": "flashinfer PR #4048, B300, another routing seed"}
     pub = PUBLISHED_TFLOPS.get((w.name, res["dtype"]))
     if pub:
         res["vs_baseline"] = value / pub

@@ -81,6 +81,14 @@ typedef struct {
   float routed_scaling_factor; /* multiplies every route weight; 1.0f when unused */
   int32_t S;           /* shared-expert intermediate size; 0 = no shared expert */
   int32_t activation;  /* moe_activation_t; 0 (MOE_ACT_SILU) when zero-initialised */
+  /* Expert-parallel shard (flashinfer PR #4048 benchmark: a DeepSeek-V3 EP8 rank holds 32 of
+   * the 256 experts).  0 = every expert is local.  Otherwise this GPU holds the experts
+   * [ep_local_offset, ep_local_offset + ep_num_local) of the E the router scores: the weight
+   * tensors hold only those (index e - ep_local_offset), the router's ids are local indices
+   * with routes to other experts set to -1 (padding), and out[t] is the sum over the local
+   * experts only (plus the shared expert), which the caller's collective adds across shards. */
+  int32_t ep_num_local;
+  int32_t ep_local_offset;
 } moe_problem_t;
 
 /* ---------------------------------------------------------------------------------------- */
@@ -133,6 +141,49 @@ moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
                            const void* shared_w_down, void* out, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/*
+ * fused_moe_fwd_w4a16 -- fused_moe_fwd with NVFP4 routed experts and bf16 activations
+ * (flashinfer PR #4048, quant_mode "w4a16": NVFP4 weights decoded for a BF16 MMA, the FP32
+ * per-expert scale applied to the FP32 accumulator, as its weight-scale placement ablation
+ * keeps).  Each routed weight is
+ *   W[e,n,k] = e2m1(code[e,n,k]) * e4m3(sf[e,n,k/16]) * alpha[e]
+ * with E2M1 = 1 sign, 2 exponent (bias 1), 1 mantissa bit, and E4M3 = 1 sign, 4 exponent
+ * (bias 7), 3 mantissa bits (OCP 8-bit floating point; S.1111.111 is NaN).  The codes and
+ * scales are passed in the packed tile layout moe_nvfp4_pack produces:
+ *   w_gate_up_tiles moe_nvfp4_pack of codes [E_l, R1, H/2] and scales [E_l, R1, H/16]
+ *                   (R1 = 2F, gate rows then up rows, or F for MOE_ACT_RELU2)
+ *   w_gate_up_alpha [E_l] f32
+ *   w_down_tiles    moe_nvfp4_pack of codes [E_l, H, F/2] and scales [E_l, H, F/16]
+ *   w_down_alpha    [E_l] f32
+ * (E_l = p->ep_num_local, or E).  Other arguments as fused_moe_fwd.  Requires p->dtype
+ * MOE_BF16, H and F multiples of 128 and p->S == 0 (MOE_ERR_UNSUPPORTED otherwise).
+ */
+moe_status_t fused_moe_fwd_w4a16(const moe_problem_t* p, const void* hidden_states,
+                                 const float* gating_output, const uint8_t* w_gate_up_tiles,
+                                 const float* w_gate_up_alpha, const uint8_t* w_down_tiles,
+                                 const float* w_down_alpha, const float* correction_bias,
+                                 void* out, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
+/*
+ * moe_nvfp4_pack -- rearrange NVFP4 weights into the tile layout the W4A16 GEMMs stream (a
+ * one-time step when weights are loaded; no counterpart on the pages beyond their use of a
+ * kernel-specific scale layout).  For n_mats matrices of `rows` x K:
+ *   codes  [n_mats, rows, K/2] u8 (two E2M1 codes per byte, element 2i in the low nibble),
+ *   scales [n_mats, rows, K/16] u8 (E4M3, one per 16 consecutive k)
+ *   tiles  moe_nvfp4_packed_bytes(n_mats, rows, K) bytes (out): for each (matrix, 128-row slab,
+ *          128-k block) in that order a 9216-byte tile holding the slab's 128 rows of 64 code
+ *          bytes (row r at r*64, its 16-byte chunk j at chunk position j ^ ((r>>1)&3)) followed
+ *          by their 8 scale bytes (row r at 8192 + r*8).
+ * rows and K must be multiples of 128 (MOE_ERR_UNSUPPORTED); codes and tiles 16-byte aligned,
+ * scales 8-byte aligned (MOE_ERR_INVALID_ARG).  Runs on `stream`; the caller owns all buffers.
+ */
+moe_status_t moe_nvfp4_pack(int64_t n_mats, int32_t rows, int32_t K, const uint8_t* codes,
+                            const uint8_t* scales, uint8_t* tiles, void* stream);
+
+/* Bytes of moe_nvfp4_pack's output (codes plus scales), or -1 for unsupported sizes. */
+int64_t moe_nvfp4_packed_bytes(int64_t n_mats, int32_t rows, int32_t K);
+
 /* ---------------------------------------------------------------------------------------- */
 /* Staged entry points (the same kernels, callable one at a time).                          */
 /* ---------------------------------------------------------------------------------------- */
@@ -150,7 +201,8 @@ moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
  *   Every weight is then multiplied by routed_scaling_factor.
  * The f32 sigmoid used for the selection key is a fixed sequence of correctly rounded f32
  * operations (Cody-Waite reduction of exp with a degree-7 Taylor polynomial), so the same
- * logits give the same ids on every run.
+ * logits give the same ids on every run.  With an expert-parallel shard (p->ep_num_local > 0)
+ * the ids are local indices, -1 for experts outside the shard.
  *   gating_output [T,E] f32; correction_bias [E] f32 or NULL
  *   topk_ids [T,top_k] int32 (out); topk_weights [T,top_k] f32 (out)
  */
@@ -196,6 +248,13 @@ moe_status_t moe_gemm1_swiglu(const moe_problem_t* p, int32_t block_m, const voi
                               const void* w_gate_up, void* act, void* workspace,
                               size_t workspace_bytes, void* stream);
 
+/* moe_gemm1_w4a16 -- moe_gemm1_swiglu with NVFP4 gate/up weights (packed tiles and scale as
+ * in fused_moe_fwd_w4a16).  Requires MOE_BF16, H and F multiples of 128. */
+moe_status_t moe_gemm1_w4a16(const moe_problem_t* p, int32_t block_m, const void* hidden_states,
+                             const int32_t* sorted_ids, const int32_t* offsets,
+                             const uint8_t* w_gate_up_tiles, const float* w_gate_up_alpha,
+                             void* act, void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * moe_gemm2 -- TileOPs "MoE" page, op MoEGroupedGemmFwd (down projection, contiguous layout),
  * with the route weight applied in the epilogue:
@@ -208,6 +267,14 @@ moe_status_t moe_gemm2(const moe_problem_t* p, int32_t block_m, const void* act,
                        const int32_t* sorted_ids,
                        const int32_t* offsets, const float* topk_weights, const void* w_down,
                        void* y_route, void* workspace, size_t workspace_bytes, void* stream);
+
+/* moe_gemm2_w4a16 -- moe_gemm2 with NVFP4 down weights (packed tiles and scale as in
+ * fused_moe_fwd_w4a16).  Requires MOE_BF16, H and F multiples of 128. */
+moe_status_t moe_gemm2_w4a16(const moe_problem_t* p, int32_t block_m, const void* act,
+                             const int32_t* sorted_ids, const int32_t* offsets,
+                             const float* topk_weights, const uint8_t* w_down_tiles,
+                             const float* w_down_alpha, void* y_route, void* workspace,
+                             size_t workspace_bytes, void* stream);
 
 /*
  * moe_combine -- TileOPs "MoE" page, op MoEPostPermuteFwd; aiter PR #5973 "Changes"

@@ -37,7 +37,8 @@ EXPORTED = (
     "moe_workspace_init", "fused_moe_fwd", "moe_route", "moe_align_sort", "moe_gemm1_swiglu",
     "moe_gemm2", "moe_combine", "moe_shared_expert_fwd", "moe_get_device_status",
     "moe_status_string", "moe_set_wait_limit_ns", "moe_stage_name", "moe_profile_enable",
-    "moe_profile_collect", "moe_align_sort_noalloc",
+    "moe_profile_collect", "moe_align_sort_noalloc", "fused_moe_fwd_w4a16", "moe_gemm1_w4a16",
+    "moe_gemm2_w4a16", "moe_nvfp4_pack", "moe_nvfp4_packed_bytes",
 )
 
 
@@ -48,7 +49,8 @@ class MoeProblem(ctypes.Structure):
         ("scoring", ctypes.c_int32), ("renormalize", ctypes.c_int32),
         ("num_expert_group", ctypes.c_int32), ("topk_group", ctypes.c_int32),
         ("routed_scaling_factor", ctypes.c_float), ("S", ctypes.c_int32),
-        ("activation", ctypes.c_int32),
+        ("activation", ctypes.c_int32), ("ep_num_local", ctypes.c_int32),
+        ("ep_local_offset", ctypes.c_int32),
     ]
 
 
@@ -103,9 +105,17 @@ def lib():
             L.moe_profile_collect.argtypes = [P, P, P, i32]
             L.moe_align_sort_noalloc.restype = ctypes.c_int
             L.moe_align_sort_noalloc.argtypes = [PP, i32, P, P, P, P, P, P, P, P]
+            L.fused_moe_fwd_w4a16.argtypes = [PP, P, P, P, P, P, P, P, P, P, sz, P]
+            L.moe_gemm1_w4a16.argtypes = [PP, i32, P, P, P, P, P, P, P, sz, P]
+            L.moe_gemm2_w4a16.argtypes = [PP, i32, P, P, P, P, P, P, P, P, sz, P]
+            L.moe_nvfp4_pack.restype = ctypes.c_int
+            L.moe_nvfp4_pack.argtypes = [i64, i32, i32, P, P, P, P]
+            L.moe_nvfp4_packed_bytes.restype = i64
+            L.moe_nvfp4_packed_bytes.argtypes = [i64, i32, i32]
             for fn in ("fused_moe_fwd", "moe_route", "moe_align_sort", "moe_gemm1_swiglu",
                        "moe_gemm2", "moe_combine", "moe_shared_expert_fwd",
-                       "moe_get_device_status", "moe_workspace_init"):
+                       "moe_get_device_status", "moe_workspace_init", "fused_moe_fwd_w4a16",
+                       "moe_gemm1_w4a16", "moe_gemm2_w4a16"):
                 getattr(L, fn).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -145,7 +155,7 @@ def _need(t, name, dtype=None, shape=None):
 
 def make_problem(T, H, E, F, top_k, dtype=torch.bfloat16, scoring_func="softmax",
                  renormalize=True, num_expert_group=0, topk_group=0, routed_scaling_factor=1.0,
-                 S=0, activation="silu") -> MoeProblem:
+                 S=0, activation="silu", ep_num_local=0, ep_local_offset=0) -> MoeProblem:
     if dtype not in _DTYPES:
         raise ValueError(f"unsupported dtype {dtype}")
     if scoring_func not in _SCORING:
@@ -155,7 +165,7 @@ def make_problem(T, H, E, F, top_k, dtype=torch.bfloat16, scoring_func="softmax"
     return MoeProblem(int(T), int(H), int(E), int(F), int(top_k), _DTYPES[dtype],
                       _SCORING[scoring_func], int(bool(renormalize)), int(num_expert_group),
                       int(topk_group), float(routed_scaling_factor), int(S),
-                      _ACTIVATIONS[activation])
+                      _ACTIVATIONS[activation], int(ep_num_local), int(ep_local_offset))
 
 
 def workspace_size(prob: MoeProblem) -> int:
@@ -236,25 +246,29 @@ def profile_collect() -> dict:
 def fused_moe_fwd(hidden_states, gating_output, w_gate_up, w_down, top_k, renormalize=True,
                   scoring_func="softmax", correction_bias=None, num_expert_group=0, topk_group=0,
                   routed_scaling_factor=1.0, shared_w_gate_up=None, shared_w_down=None, out=None,
-                  workspace=None, stream=None, activation="silu"):
+                  workspace=None, stream=None, activation="silu", ep_local_offset=0):
     """The whole fused MoE forward (include/moe.h: fused_moe_fwd); returns out [T, H].
-    ``activation``: "silu" (default), "gelu_tanh" or "relu2" (w_gate_up then has F rows)."""
+    ``activation``: "silu" (default), "gelu_tanh" or "relu2" (w_gate_up then has F rows).
+    When the weights hold fewer experts than gating_output scores, they are the shard
+    [ep_local_offset, ep_local_offset + E_local) of an expert-parallel layout."""
     T, H = hidden_states.shape
-    E = w_gate_up.shape[0]
+    E = gating_output.shape[1]
+    E_l = w_gate_up.shape[0]
     F = w_down.shape[2]
     S = 0 if shared_w_down is None else shared_w_down.shape[1]
     dt = hidden_states.dtype
     _need(hidden_states, "hidden_states", dt)
     _need(gating_output, "gating_output", torch.float32, (T, E))
-    _need(w_gate_up, "w_gate_up", dt, (E, gate_up_rows(activation, F), H))
-    _need(w_down, "w_down", dt, (E, H, F))
+    _need(w_gate_up, "w_gate_up", dt, (E_l, gate_up_rows(activation, F), H))
+    _need(w_down, "w_down", dt, (E_l, H, F))
     if correction_bias is not None:
         _need(correction_bias, "correction_bias", torch.float32, (E,))
     if S:
         _need(shared_w_gate_up, "shared_w_gate_up", dt, (gate_up_rows(activation, S), H))
         _need(shared_w_down, "shared_w_down", dt, (H, S))
     prob = make_problem(T, H, E, F, top_k, dt, scoring_func, renormalize, num_expert_group,
-                        topk_group, routed_scaling_factor, S, activation)
+                        topk_group, routed_scaling_factor, S, activation,
+                        E_l if E_l != E else 0, ep_local_offset)
     nbytes = workspace_size(prob)
     if workspace is None:
         workspace = _workspace(nbytes, hidden_states.device)
@@ -441,10 +455,138 @@ def fused_moe_fwd_host(hidden_host, gating_host, w_gate_up, w_down, top_k, out_h
                         gating=torch.empty(gating_host.shape, dtype=gating_host.dtype, device=dev))
     dev_bufs["hidden"].copy_(hidden_host, non_blocking=True)
     dev_bufs["gating"].copy_(gating_host, non_blocking=True)
-    out = fused_moe_fwd(dev_bufs["hidden"], dev_bufs["gating"], w_gate_up, w_down, top_k,
-                        out=dev_bufs.get("out"), **kw)
+    fwd = fused_moe_fwd_w4a16 if isinstance(w_gate_up, Nvfp4Weights) else fused_moe_fwd
+    out = fwd(dev_bufs["hidden"], dev_bufs["gating"], w_gate_up, w_down, top_k,
+              out=dev_bufs.get("out"), **kw)
     dev_bufs["out"] = out
     if out_host is None:
         out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     out_host.copy_(out, non_blocking=True)
     return out_host
+
+
+# ------------------------------------------------------------------------ NVFP4 (W4A16) experts
+class Nvfp4Weights:
+    """One projection of all (local) experts in the packed layout of moe_nvfp4_pack: `tiles`
+    (uint8), the per-expert FP32 scale `alpha` [n_mats], and the matrix shape rows x K."""
+
+    def __init__(self, tiles, alpha, n_mats, rows, K):
+        self.tiles, self.alpha, self.n_mats, self.rows, self.K = tiles, alpha, n_mats, rows, K
+
+    @property
+    def device(self):
+        return self.tiles.device
+
+
+def nvfp4_packed_bytes(n_mats, rows, K) -> int:
+    n = lib().moe_nvfp4_packed_bytes(int(n_mats), int(rows), int(K))
+    if n < 0:
+        raise MoeError(MOE_ERR_UNSUPPORTED, "moe_nvfp4_packed_bytes")
+    return int(n)
+
+
+def pack_nvfp4_weights(codes, scales, alpha, stream=None) -> Nvfp4Weights:
+    """codes [n, rows, K/2] u8, scales [n, rows, K/16] u8, alpha [n] f32 -> Nvfp4Weights
+    (include/moe.h: moe_nvfp4_pack)."""
+    n, rows, half_k = codes.shape
+    K = half_k * 2
+    _need(codes, "codes", torch.uint8)
+    _need(scales, "scales", torch.uint8, (n, rows, K // 16))
+    _need(alpha, "alpha", torch.float32, (n,))
+    tiles = torch.empty(nvfp4_packed_bytes(n, rows, K), dtype=torch.uint8, device=codes.device)
+    _check(lib().moe_nvfp4_pack(n, rows, K, _p(codes), _p(scales), _p(tiles), _stream(stream)),
+           "moe_nvfp4_pack")
+    return Nvfp4Weights(tiles, alpha, n, rows, K)
+
+
+def _need_w4(w, name, E_l, rows, K):
+    if not isinstance(w, Nvfp4Weights):
+        raise TypeError(f"{name} must be Nvfp4Weights (pack_nvfp4_weights)")
+    if (w.n_mats, w.rows, w.K) != (E_l, rows, K):
+        raise ValueError(f"{name} must hold {E_l} matrices of {rows} x {K}, "
+                         f"got {w.n_mats} of {w.rows} x {w.K}")
+    _need(w.tiles, name + " tiles", torch.uint8)
+    _need(w.alpha, name + " alpha", torch.float32, (E_l,))
+
+
+def fused_moe_fwd_w4a16(hidden_states, gating_output, w_gate_up, w_down, top_k, renormalize=True,
+                        scoring_func="softmax", correction_bias=None, num_expert_group=0,
+                        topk_group=0, routed_scaling_factor=1.0, out=None, workspace=None,
+                        stream=None, activation="silu", ep_local_offset=0):
+    """Fused MoE forward with NVFP4 routed experts (include/moe.h: fused_moe_fwd_w4a16).
+    w_gate_up / w_down are Nvfp4Weights; returns out [T, H] bf16."""
+    T, H = hidden_states.shape
+    E = gating_output.shape[1]
+    E_l = w_gate_up.n_mats
+    F = w_down.K
+    dt = hidden_states.dtype
+    _need(hidden_states, "hidden_states", torch.bfloat16)
+    _need(gating_output, "gating_output", torch.float32, (T, E))
+    _need_w4(w_gate_up, "w_gate_up", E_l, gate_up_rows(activation, F), H)
+    _need_w4(w_down, "w_down", E_l, H, F)
+    if correction_bias is not None:
+        _need(correction_bias, "correction_bias", torch.float32, (E,))
+    prob = make_problem(T, H, E, F, top_k, dt, scoring_func, renormalize, num_expert_group,
+                        topk_group, routed_scaling_factor, 0, activation,
+                        E_l if E_l != E else 0, ep_local_offset)
+    nbytes = workspace_size(prob)
+    if workspace is None:
+        workspace = _workspace(nbytes, hidden_states.device)
+    if out is None:
+        out = torch.empty((T, H), dtype=dt, device=hidden_states.device)
+    _need(out, "out", dt, (T, H))
+    rc = lib().fused_moe_fwd_w4a16(ctypes.byref(prob), _p(hidden_states), _p(gating_output),
+                                   _p(w_gate_up.tiles), _p(w_gate_up.alpha), _p(w_down.tiles),
+                                   _p(w_down.alpha), _p(correction_bias), _p(out),
+                                   _p(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "fused_moe_fwd_w4a16")
+    return out
+
+
+def moe_gemm1_w4a16(hidden_states, sorted_ids, offsets, w_gate_up, top_k, block_m=1,
+                    workspace=None, stream=None, activation="silu"):
+    """Grouped gate/up GEMM with NVFP4 weights + activation (include/moe.h: moe_gemm1_w4a16);
+    returns act [cap, F] bf16."""
+    T, H = hidden_states.shape
+    E_l, rows = w_gate_up.n_mats, w_gate_up.rows
+    F = rows if activation == "relu2" else rows // 2
+    _need(hidden_states, "hidden_states", torch.bfloat16)
+    _need_w4(w_gate_up, "w_gate_up", E_l, gate_up_rows(activation, F), H)
+    _need(sorted_ids, "sorted_ids", torch.int32)
+    _need(offsets, "offsets", torch.int32, (E_l + 1,))
+    prob = make_problem(T, H, E_l, F, top_k, torch.bfloat16, activation=activation)
+    cap = sorted_capacity(prob, block_m)
+    act = torch.empty((max(cap, 1), F), dtype=torch.bfloat16, device=hidden_states.device)
+    nbytes = stage_workspace_size(prob, block_m)
+    if workspace is None:
+        workspace = _workspace(nbytes, hidden_states.device)
+    _check(lib().moe_gemm1_w4a16(ctypes.byref(prob), int(block_m), _p(hidden_states),
+                                 _p(sorted_ids), _p(offsets), _p(w_gate_up.tiles),
+                                 _p(w_gate_up.alpha), _p(act), _p(workspace), workspace.numel(),
+                                 _stream(stream)), "moe_gemm1_w4a16")
+    return act[:cap]
+
+
+def moe_gemm2_w4a16(act, sorted_ids, offsets, topk_weights, w_down, T, top_k, block_m=1,
+                    workspace=None, stream=None):
+    """Grouped down GEMM with NVFP4 weights x route weight (include/moe.h: moe_gemm2_w4a16);
+    returns f32 y_route [cap, H]."""
+    E_l, H, F = w_down.n_mats, w_down.rows, w_down.K
+    _need_w4(w_down, "w_down", E_l, H, F)
+    _need(act, "act", torch.bfloat16)
+    _need(sorted_ids, "sorted_ids", torch.int32)
+    _need(offsets, "offsets", torch.int32, (E_l + 1,))
+    _need(topk_weights, "topk_weights", torch.float32)
+    prob = make_problem(T, H, E_l, F, top_k, torch.bfloat16)
+    cap = sorted_capacity(prob, block_m)
+    if act.shape[0] < cap or act.shape[1] != F:
+        raise ValueError(f"act must have at least {cap} rows of {F} columns")
+    y = torch.empty((max(cap, 1), H), dtype=torch.float32, device=act.device)
+    nbytes = stage_workspace_size(prob, block_m)
+    if workspace is None:
+        workspace = _workspace(nbytes, act.device)
+    _check(lib().moe_gemm2_w4a16(ctypes.byref(prob), int(block_m), _p(act), _p(sorted_ids),
+                                 _p(offsets), _p(topk_weights), _p(w_down.tiles),
+                                 _p(w_down.alpha), _p(y), _p(workspace), workspace.numel(),
+                                 _stream(stream)), "moe_gemm2_w4a16")
+    return y[:cap]

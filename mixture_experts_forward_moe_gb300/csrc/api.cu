@@ -85,6 +85,10 @@ moe_status_t check_problem(const moe_problem_t* p) {
   if (p->dtype != MOE_BF16 && p->dtype != MOE_F16) return MOE_ERR_INVALID_ARG;
   if (p->scoring != MOE_SOFTMAX && p->scoring != MOE_SIGMOID) return MOE_ERR_INVALID_ARG;
   if (p->activation < MOE_ACT_SILU || p->activation > MOE_ACT_RELU2) return MOE_ERR_INVALID_ARG;
+  if (p->ep_num_local < 0 || p->ep_local_offset < 0) return MOE_ERR_INVALID_ARG;
+  if (p->ep_num_local > 0 && (int64_t)p->ep_local_offset + p->ep_num_local > p->E)
+    return MOE_ERR_INVALID_ARG;
+  if (p->ep_num_local == 0 && p->ep_local_offset != 0) return MOE_ERR_INVALID_ARG;
   if (!(p->routed_scaling_factor == p->routed_scaling_factor)) return MOE_ERR_INVALID_ARG;
   if (p->num_expert_group < 0 || p->topk_group < 0) return MOE_ERR_INVALID_ARG;
   if (p->num_expert_group > 1) {
@@ -274,16 +278,40 @@ moe_status_t moe_workspace_init(void* workspace, size_t workspace_bytes, void* s
   return from_cuda(cudaMemsetAsync(workspace, 0, kHeaderBytes, (cudaStream_t)stream));
 }
 
-moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
-                           const float* gating_output, const void* w_gate_up, const void* w_down,
-                           const float* correction_bias, const void* shared_w_gate_up,
-                           const void* shared_w_down, void* out, void* workspace,
-                           size_t workspace_bytes, void* stream) {
+// The routed experts' weights: 16-bit (w1, w2), or NVFP4 packed tiles (w1, w2) with their
+// per-expert scales (a1, a2).
+struct Experts {
+  const void* w1;
+  const void* w2;
+  const float* a1;
+  const float* a2;
+  int w4;
+};
+
+void set_weights(GemmCall& g, const Experts& X, bool first) {
+  g.w = first ? X.w1 : X.w2;
+  g.w4 = X.w4;
+  g.alpha = first ? X.a1 : X.a2;
+}
+
+// Limits of the NVFP4 GEMMs (bf16 activations, 128-k stages, 128-row weight slabs).
+moe_status_t check_w4(const moe_problem_t& p) {
+  if (p.dtype != MOE_BF16 || p.H % 128 != 0 || p.F % 128 != 0 || p.S != 0)
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status_t run_fused(const moe_problem_t* p, const Experts& X, const void* hidden_states,
+                       const float* gating_output, const float* correction_bias,
+                       const void* shared_w_gate_up, const void* shared_w_down, void* out,
+                       void* workspace, size_t workspace_bytes, void* stream) {
   moe_status_t st = check_problem(p);
   if (st != MOE_OK) return st;
+  if (X.w4 && (st = check_w4(*p)) != MOE_OK) return st;
   if (!workspace) return MOE_ERR_INVALID_ARG;
-  if (p->T > 0 && (!hidden_states || !gating_output || !w_gate_up || !w_down || !out))
+  if (p->T > 0 && (!hidden_states || !gating_output || !X.w1 || !X.w2 || !out))
     return MOE_ERR_INVALID_ARG;
+  if (X.w4 && p->T > 0 && (!X.a1 || !X.a2)) return MOE_ERR_INVALID_ARG;
   if ((p->S > 0) != (shared_w_gate_up != nullptr) || (p->S > 0) != (shared_w_down != nullptr))
     return MOE_ERR_INVALID_ARG;
   if (correction_bias && p->scoring != MOE_SIGMOID) return MOE_ERR_UNSUPPORTED;
@@ -295,13 +323,13 @@ moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
   int* status = status_word(ws);
   int32_t* ids = at<int32_t>(ws, L.ids);
   float* w = at<float>(ws, L.w);
-  const moe_problem_t& P = *p;
-
   {
     StageTimer t(kRoute, s);
-    MOE_TRY(launch_route(P, gating_output, correction_bias, ids, w, s, false));
+    MOE_TRY(launch_route(*p, gating_output, correction_bias, ids, w, s, false));
     t.done(1);
   }
+  // Past the router every id is a local expert index (or -1): the stages see E_local experts.
+  const moe_problem_t P = local_view(*p);
 
   const void* y_rows = at<void>(ws, L.y);
   const int32_t* inv = nullptr;
@@ -311,7 +339,7 @@ moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
     g1.mode = kDirect;
     g1.K = P.H;
     g1.n_out = P.F;
-    g1.w = w_gate_up;
+    set_weights(g1, X, true);
     g1.b = hidden_states;
     g1.b_rows = P.T;
     g1.out = at<void>(ws, L.act);
@@ -326,7 +354,7 @@ moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
     g2.mode = kDirect;
     g2.K = P.F;
     g2.n_out = P.H;
-    g2.w = w_down;
+    set_weights(g2, X, false);
     g2.b = at<void>(ws, L.act);
     g2.b_rows = L.P;
     g2.out = at<void>(ws, L.y);
@@ -344,7 +372,7 @@ moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
     int32_t* inv_route = at<int32_t>(ws, L.inv);
     Tile* tiles = at<Tile>(ws, L.tiles);    // gemm1: 128-row tiles
     Tile* tiles2 = at<Tile>(ws, L.tiles2);  // gemm2: tile_rows2-row tiles
-    const int tile_rows2 = sorted_tile_rows(P);
+    const int tile_rows2 = X.w4 ? kTileRows : sorted_tile_rows(P);
     if (fused_sort_fits(P)) {  // sort and both tile lists in one launch
       StageTimer t(kSort, s);
       MOE_TRY(launch_sort_fused(P, 1, ids, counts, offsets, sorted, L.cap, nullptr, inv_route,
@@ -373,7 +401,7 @@ moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
     g1.mode = kSorted;
     g1.K = P.H;
     g1.n_out = P.F;
-    g1.w = w_gate_up;
+    set_weights(g1, X, true);
     g1.b = token_rows ? hidden_states : at<void>(ws, L.a_sorted);
     g1.b_rows = token_rows ? P.T : L.cap;
     g1.token_rows = token_rows ? 1 : 0;
@@ -394,7 +422,7 @@ moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
     g2.b_rows = L.cap;
     g2.K = P.F;
     g2.n_out = P.H;
-    g2.w = w_down;
+    set_weights(g2, X, false);
     g2.b = at<void>(ws, L.act);
     g2.out = at<void>(ws, L.y);
     g2.sorted_ids = sorted;
@@ -423,6 +451,27 @@ moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
   return MOE_OK;
 }
 
+moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
+                           const float* gating_output, const void* w_gate_up, const void* w_down,
+                           const float* correction_bias, const void* shared_w_gate_up,
+                           const void* shared_w_down, void* out, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  const Experts X{w_gate_up, w_down, nullptr, nullptr, 0};
+  return run_fused(p, X, hidden_states, gating_output, correction_bias, shared_w_gate_up,
+                   shared_w_down, out, workspace, workspace_bytes, stream);
+}
+
+moe_status_t fused_moe_fwd_w4a16(const moe_problem_t* p, const void* hidden_states,
+                                 const float* gating_output, const uint8_t* w_gate_up_tiles,
+                                 const float* w_gate_up_alpha, const uint8_t* w_down_tiles,
+                                 const float* w_down_alpha, const float* correction_bias,
+                                 void* out, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  const Experts X{w_gate_up_tiles, w_down_tiles, w_gate_up_alpha, w_down_alpha, 1};
+  return run_fused(p, X, hidden_states, gating_output, correction_bias, nullptr, nullptr, out,
+                   workspace, workspace_bytes, stream);
+}
+
 moe_status_t moe_route(const moe_problem_t* p, const float* gating_output,
                        const float* correction_bias, int32_t* topk_ids, float* topk_weights,
                        void* stream) {
@@ -446,35 +495,38 @@ moe_status_t moe_align_sort(const moe_problem_t* p, int32_t block_m, const int32
   const Layout L = make_layout(*p, 1);
   if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   const int64_t cap = moe_sorted_capacity(p, block_m);
-  return from_cuda(launch_align_sort(*p, block_m, topk_ids, counts, offsets, sorted_ids, cap,
+  return from_cuda(launch_align_sort(local_view(*p), block_m, topk_ids, counts, offsets,
+                                     sorted_ids, cap,
                                      tile_expert, inv_route, at<int32_t>(workspace, L.chunk),
                                      status_word(workspace), (cudaStream_t)stream, false));
 }
 
-moe_status_t moe_gemm1_swiglu(const moe_problem_t* p, int32_t block_m, const void* hidden_states,
-                              const int32_t* sorted_ids, const int32_t* offsets,
-                              const void* w_gate_up, void* act, void* workspace,
-                              size_t workspace_bytes, void* stream) {
+moe_status_t gemm1_staged(const moe_problem_t* p, int32_t block_m, const void* hidden_states,
+                          const int32_t* sorted_ids, const int32_t* offsets, const Experts& X,
+                          void* act, void* workspace, size_t workspace_bytes, void* stream) {
   moe_status_t st = check_problem(p);
   if (st != MOE_OK) return st;
+  if (X.w4 && (st = check_w4(*p)) != MOE_OK) return st;
   if (block_m <= 0 || block_m > 1024) return MOE_ERR_INVALID_ARG;
   if (!workspace || !sorted_ids || !offsets || !act) return MOE_ERR_INVALID_ARG;
-  if (p->T > 0 && (!hidden_states || !w_gate_up)) return MOE_ERR_INVALID_ARG;
+  if (p->T > 0 && (!hidden_states || !X.w1)) return MOE_ERR_INVALID_ARG;
+  if (X.w4 && p->T > 0 && !X.a1) return MOE_ERR_INVALID_ARG;
+  const moe_problem_t P = local_view(*p);
   const Layout L = make_layout(*p, block_m);
   if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = (cudaStream_t)stream;
   void* ws = workspace;
   Tile* tiles = at<Tile>(ws, L.tiles);
   const int tile_rows = kTileRows;
-  MOE_TRY(launch_build_tiles(p->E, offsets, tiles, tile_counter(ws), tile_rows, s, false));
-  MOE_TRY(launch_permute(p->dtype, p->top_k, p->H, hidden_states, sorted_ids, offsets, p->E,
-                         L.cap, at<void>(ws, L.a_sorted), s, true));
-  GemmCall g1 = base_call(*p, status_word(ws));
+  MOE_TRY(launch_build_tiles(P.E, offsets, tiles, tile_counter(ws), tile_rows, s, false));
+  MOE_TRY(launch_permute(P.dtype, P.top_k, P.H, hidden_states, sorted_ids, offsets, P.E, L.cap,
+                         at<void>(ws, L.a_sorted), s, true));
+  GemmCall g1 = base_call(P, status_word(ws));
   g1.gemm1 = 1;
   g1.mode = kSorted;
-  g1.K = p->H;
-  g1.n_out = p->F;
-  g1.w = w_gate_up;
+  g1.K = P.H;
+  g1.n_out = P.F;
+  set_weights(g1, X, true);
   g1.b = at<void>(ws, L.a_sorted);
   g1.b_rows = L.cap;
   g1.out = act;
@@ -485,28 +537,31 @@ moe_status_t moe_gemm1_swiglu(const moe_problem_t* p, int32_t block_m, const voi
   return from_cuda(launch_gemm(g1, s, true));
 }
 
-moe_status_t moe_gemm2(const moe_problem_t* p, int32_t block_m, const void* act,
-                       const int32_t* sorted_ids, const int32_t* offsets,
-                       const float* topk_weights, const void* w_down, void* y_route,
-                       void* workspace, size_t workspace_bytes, void* stream) {
+moe_status_t gemm2_staged(const moe_problem_t* p, int32_t block_m, const void* act,
+                          const int32_t* sorted_ids, const int32_t* offsets,
+                          const float* topk_weights, const Experts& X, void* y_route,
+                          void* workspace, size_t workspace_bytes, void* stream) {
   moe_status_t st = check_problem(p);
   if (st != MOE_OK) return st;
+  if (X.w4 && (st = check_w4(*p)) != MOE_OK) return st;
   if (block_m <= 0 || block_m > 1024) return MOE_ERR_INVALID_ARG;
   if (!workspace || !sorted_ids || !offsets || !y_route) return MOE_ERR_INVALID_ARG;
-  if (p->T > 0 && (!act || !topk_weights || !w_down)) return MOE_ERR_INVALID_ARG;
+  if (p->T > 0 && (!act || !topk_weights || !X.w2)) return MOE_ERR_INVALID_ARG;
+  if (X.w4 && p->T > 0 && !X.a2) return MOE_ERR_INVALID_ARG;
+  const moe_problem_t P = local_view(*p);
   const Layout L = make_layout(*p, block_m);
   if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = (cudaStream_t)stream;
   void* ws = workspace;
   Tile* tiles = at<Tile>(ws, L.tiles);
-  const int tile_rows = sorted_tile_rows(*p);
-  MOE_TRY(launch_build_tiles(p->E, offsets, tiles, tile_counter(ws), tile_rows, s, false));
-  GemmCall g2 = base_call(*p, status_word(ws));
+  const int tile_rows = X.w4 ? kTileRows : sorted_tile_rows(P);
+  MOE_TRY(launch_build_tiles(P.E, offsets, tiles, tile_counter(ws), tile_rows, s, false));
+  GemmCall g2 = base_call(P, status_word(ws));
   g2.gemm1 = 0;
   g2.mode = kSorted;
-  g2.K = p->F;
-  g2.n_out = p->H;
-  g2.w = w_down;
+  g2.K = P.F;
+  g2.n_out = P.H;
+  set_weights(g2, X, false);
   g2.b = act;
   g2.b_rows = L.cap;
   g2.out = y_route;
@@ -517,6 +572,43 @@ moe_status_t moe_gemm2(const moe_problem_t* p, int32_t block_m, const void* act,
   g2.sorted_ids = sorted_ids;
   g2.topk_w = topk_weights;
   return from_cuda(launch_gemm(g2, s, true));
+}
+
+moe_status_t moe_gemm1_swiglu(const moe_problem_t* p, int32_t block_m, const void* hidden_states,
+                              const int32_t* sorted_ids, const int32_t* offsets,
+                              const void* w_gate_up, void* act, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  const Experts X{w_gate_up, nullptr, nullptr, nullptr, 0};
+  return gemm1_staged(p, block_m, hidden_states, sorted_ids, offsets, X, act, workspace,
+                      workspace_bytes, stream);
+}
+
+moe_status_t moe_gemm1_w4a16(const moe_problem_t* p, int32_t block_m, const void* hidden_states,
+                             const int32_t* sorted_ids, const int32_t* offsets,
+                             const uint8_t* w_gate_up_tiles, const float* w_gate_up_alpha,
+                             void* act, void* workspace, size_t workspace_bytes, void* stream) {
+  const Experts X{w_gate_up_tiles, nullptr, w_gate_up_alpha, nullptr, 1};
+  return gemm1_staged(p, block_m, hidden_states, sorted_ids, offsets, X, act, workspace,
+                      workspace_bytes, stream);
+}
+
+moe_status_t moe_gemm2(const moe_problem_t* p, int32_t block_m, const void* act,
+                       const int32_t* sorted_ids, const int32_t* offsets,
+                       const float* topk_weights, const void* w_down, void* y_route,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  const Experts X{nullptr, w_down, nullptr, nullptr, 0};
+  return gemm2_staged(p, block_m, act, sorted_ids, offsets, topk_weights, X, y_route, workspace,
+                      workspace_bytes, stream);
+}
+
+moe_status_t moe_gemm2_w4a16(const moe_problem_t* p, int32_t block_m, const void* act,
+                             const int32_t* sorted_ids, const int32_t* offsets,
+                             const float* topk_weights, const uint8_t* w_down_tiles,
+                             const float* w_down_alpha, void* y_route, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  const Experts X{nullptr, w_down_tiles, nullptr, w_down_alpha, 1};
+  return gemm2_staged(p, block_m, act, sorted_ids, offsets, topk_weights, X, y_route, workspace,
+                      workspace_bytes, stream);
 }
 
 moe_status_t moe_combine(const moe_problem_t* p, const void* y_route, const int32_t* inv_route,
@@ -545,6 +637,21 @@ moe_status_t moe_shared_expert_fwd(const moe_problem_t* p, const void* hidden_st
   return from_cuda(run_shared(*p, hidden_states, shared_w_gate_up, shared_w_down,
                               at<void>(workspace, L.sh_act), shared_out,
                               status_word(workspace), (cudaStream_t)stream, false));
+}
+
+int64_t moe_nvfp4_packed_bytes(int64_t n_mats, int32_t rows, int32_t K) {
+  if (n_mats < 0 || rows <= 0 || K <= 0 || rows % 128 != 0 || K % 128 != 0) return -1;
+  return n_mats * (int64_t)rows * K / 2 + n_mats * (int64_t)rows * K / 16;
+}
+
+moe_status_t moe_nvfp4_pack(int64_t n_mats, int32_t rows, int32_t K, const uint8_t* codes,
+                            const uint8_t* scales, uint8_t* tiles, void* stream) {
+  if (moe_nvfp4_packed_bytes(n_mats, rows, K) < 0) return MOE_ERR_UNSUPPORTED;
+  if (n_mats > 0 && (!codes || !scales || !tiles)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(codes) & 15) || (reinterpret_cast<uintptr_t>(scales) & 7) ||
+      (reinterpret_cast<uintptr_t>(tiles) & 15))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(launch_nvfp4_pack(n_mats, rows, K, codes, scales, tiles, (cudaStream_t)stream));
 }
 
 moe_status_t moe_get_device_status(void* workspace, void* stream) {

@@ -26,6 +26,19 @@ constexpr int kBlockK = 64;
 // Workspace header: status word at offset 0, tile counter at offset 64.
 constexpr size_t kHeaderBytes = 256;
 
+// Experts whose weights this GPU holds (an expert-parallel shard, or all E), and the problem
+// as the post-routing stages see it: ids are local indices in [0, local_experts) or -1.
+inline int local_experts(const moe_problem_t& p) {
+  return p.ep_num_local > 0 ? p.ep_num_local : p.E;
+}
+inline moe_problem_t local_view(const moe_problem_t& p) {
+  moe_problem_t q = p;
+  q.E = local_experts(p);
+  q.ep_num_local = 0;
+  q.ep_local_offset = 0;
+  return q;
+}
+
 // First error wins; later errors are dropped until the host reads and clears the word.
 __device__ __forceinline__ void set_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
@@ -105,6 +118,10 @@ cudaError_t launch_permute(int dtype, int top_k, int H, const void* hidden,
                            const int32_t* sorted_ids, const int32_t* offsets, int E, int64_t cap,
                            void* a_sorted, cudaStream_t s, bool pdl);
 
+// NVFP4 weights -> the packed tile layout the W4A16 GEMMs read (nvfp4_pack.cu).
+cudaError_t launch_nvfp4_pack(int64_t n_mats, int rows, int K, const uint8_t* codes,
+                              const uint8_t* scales, uint8_t* tiles, cudaStream_t s);
+
 cudaError_t launch_combine(const moe_problem_t& p, const void* y_route,
                            const int32_t* inv_route, const int32_t* ids, const void* shared_out,
                            void* out, cudaStream_t s, bool pdl);
@@ -122,6 +139,9 @@ struct GemmCall {
   int n_out;      // output columns (F for gemm1, H for gemm2)
   int E;          // experts (1 for dense)
   const void* w;  // weights: gemm1 [E, 2*n_out, K] ([E, n_out, K] for ReLU2); gemm2 [E, n_out, K]
+                  // (NVFP4: the packed tiles of moe_nvfp4_pack)
+  int w4;         // 1: NVFP4 weights (E2M1 codes, E4M3 scales per 16 k, FP32 scale per expert)
+  const float* alpha;   // NVFP4 per-expert scale [E]
   const void* b;  // token rows [b_rows, K]
   int64_t b_rows; // rows of b (tensor extent)
   void* out;      // [*, n_out]

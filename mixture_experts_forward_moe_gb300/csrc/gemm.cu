@@ -42,6 +42,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "nvfp4.cuh"
 #include "ptx.cuh"
 
 namespace gb300moe {
@@ -52,21 +53,55 @@ namespace {
 // buffers in TMEM for every GEMM (the epilogue of one unit overlaps the K loop of the next);
 // kN = 256 halves how often an expert with many rows streams its weights, at the cost of a
 // single gemm1 accumulator buffer (2 x 256 columns fill TMEM) and fewer pipeline stages.
-template <bool kGemm1, int kN>
+//
+// NVFP4 weights (kW4, the W4A16 GEMMs).  A stage covers 128 k, and the weights and the tokens
+// travel in separate rings so that a weight slot is refilled as soon as it has been decoded:
+//  * weight ring (kNW slots): per slab one 9216-byte tile of the packed weight layout
+//    (moe_nvfp4_pack: the 128 rows' E2M1 codes for 128 k, then their E4M3 block scales), one
+//    contiguous bulk copy; freed by the decoders;
+//  * token ring (kNT slots): two 128-byte-swizzled 64-k boxes of token rows; freed by the MMA;
+//  * TMEM ring (kAStages slots of 64 k): eight decoder warps turn the codes into bf16 and store
+//    them there (one column holds two consecutive k of one weight row); the MMA reads its A
+//    operand from it.  The accumulators take the first 256 columns and the ring the rest.
+// Every tcgen05.mma of M = 128 and k = 16 takes about the same time whatever N and wherever A
+// comes from, so at decode sizes the MMA issue rate bounds these GEMMs; the rings are sized so
+// that the decoders and the loads keep it fed.
+template <bool kGemm1, int kN, bool kW4 = false>
 struct Cfg {
   static_assert(kN == 128 || kN == 256, "tile rows");
+  static_assert(!kW4 || kN == 128, "NVFP4 tiles are 128 token rows");
+  static constexpr int kSlabs = kGemm1 ? 2 : 1;
+  static constexpr int kStageK = kW4 ? 128 : kBlockK;  // k per pipeline stage
   static constexpr int kStages = kGemm1 ? (kN == 128 ? 4 : 3) : (kN == 128 ? 7 : 4);
-  static constexpr int kABytes = (kGemm1 ? 2 : 1) * kSlab * kBlockK * 2;
-  static constexpr int kBBytes = kN * kBlockK * 2;
+  static constexpr int kABytes = kSlabs * kSlab * kBlockK * 2;
+  static constexpr int kBBytes = kN * kStageK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
+  // NVFP4 rings
+  static constexpr int kQBytes = kSlab * 64;  // packed codes of one slab (128 k)
+  static constexpr int kSfBytes = kSlab * 8;  // block scales of one slab (128 k)
+  static constexpr int kTileBytes = kQBytes + kSfBytes;  // one tile of the packed layout
+  static constexpr int kWBytes = kSlabs * kTileBytes;
+  static constexpr int kNW = kGemm1 ? 6 : 8;
+  static constexpr int kNT = kGemm1 ? 3 : 4;
+  static constexpr int kRingBytes = kW4 ? kNW * kWBytes + kNT * kBBytes : kStages * kStageBytes;
+  static constexpr int kFullBars = kW4 ? kNT : kStages;  // token (or combined) ring barriers
   // gemm1 transposes 64 token columns at a time through shared memory; gemm2 writes f32 rows
   // straight from registers.
   static constexpr int kPassCols = 64;
   static constexpr int kStagingBytes = kGemm1 ? kPassCols * kSlab * 2 : 0;
   static constexpr int kAccCols = kGemm1 ? 2 * kN : kN;  // per accumulator buffer
-  static constexpr int kAccBufs = (kGemm1 && kN == 256) ? 1 : 2;
-  static constexpr int kTmemCols = kAccBufs * kAccCols;
-  static constexpr int kSmemBytes = kStages * kStageBytes + kStagingBytes + 1024;
+  static constexpr int kAccBufs = kW4 ? (kGemm1 ? 1 : 2) : ((kGemm1 && kN == 256) ? 1 : 2);
+  static constexpr int kABase = kAccBufs * kAccCols;  // first TMEM ring column
+  static constexpr int kASlotCols = kSlabs * 32;      // 64 k of every slab
+  static constexpr int kAStages = kW4 ? (512 - kABase) / kASlotCols : 1;
+  static constexpr int kTmemCols = kW4 ? 512 : kAccBufs * kAccCols;
+  static constexpr int kThreads = kW4 ? 480 : 192;
+  static constexpr int kSmemBytes = kRingBytes + kStagingBytes + 1024;
+  static_assert(!kW4 || kABase + kAStages * kASlotCols <= 512, "TMEM columns");
+  static_assert(kStageBytes % 1024 == 0 && kABytes % 1024 == 0 && kWBytes % 1024 == 0 &&
+                    kBBytes % 1024 == 0,
+                "swizzle-atom alignment");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
 struct KParams {
@@ -77,6 +112,9 @@ struct KParams {
   int slab_rows;   // weight rows (output columns) a unit covers: 128, or 256 for ReLU2 gemm1
   int second_off;  // gemm1: row offset of the second weight tile (F gated, 128 ReLU2)
   int K, n_out, E, n_slabs, num_kb, w_rows_per_expert;
+  // NVFP4 weights: packed tiles (moe_nvfp4_pack) and the per-expert FP32 scale
+  const uint8_t* w4;
+  const float* alpha;
   const Tile* tiles;
   const int* n_tiles;
   const int32_t* sorted_ids;
@@ -158,19 +196,23 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) 
   }
 }
 
-template <bool kGemm1, int kN, typename T>
-__global__ void __launch_bounds__(192, 1)
+template <bool kGemm1, int kN, typename T, bool kW4>
+__global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmB64,
                     const __grid_constant__ CUtensorMap tmB128, const KParams p) {
-  using C = Cfg<kGemm1, kN>;
+  using C = Cfg<kGemm1, kN, kW4>;
   extern __shared__ uint8_t dsmem[];
-  __shared__ __align__(8) uint64_t full_bar[C::kStages];
-  __shared__ __align__(8) uint64_t empty_bar[C::kStages];
+  __shared__ __align__(8) uint64_t full_bar[C::kFullBars];   // NVFP4: the token ring
+  __shared__ __align__(8) uint64_t empty_bar[C::kFullBars];
   __shared__ __align__(8) uint64_t tfull_bar[C::kAccBufs];
   __shared__ __align__(8) uint64_t tempty_bar[C::kAccBufs];
   __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t afull_bar[C::kAStages];   // NVFP4: decoded slot ready
+  __shared__ __align__(8) uint64_t aempty_bar[C::kAStages];  // NVFP4: slot consumed by the MMA
+  __shared__ __align__(8) uint64_t wfull_bar[kW4 ? C::kNW : 1];   // NVFP4: weights landed
+  __shared__ __align__(8) uint64_t wempty_bar[kW4 ? C::kNW : 1];  // NVFP4: weights decoded
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
   __shared__ int s_n_units;
@@ -181,16 +223,27 @@ __global__ void __launch_bounds__(192, 1)
   // 1024-byte alignment for the 128-byte swizzle atoms.
   const uint32_t raw = smem_u32(dsmem);
   uint8_t* smem = dsmem + ((1024u - (raw & 1023u)) & 1023u);
-  uint8_t* staging = smem + C::kStages * C::kStageBytes;
+  uint8_t* staging = smem + C::kRingBytes;
+  uint8_t* tring = smem + (kW4 ? C::kNW * C::kWBytes : 0);  // NVFP4 token ring
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int* abort_flag = &s_abort;
 
   // Prologue that touches no global memory: it overlaps the previous kernel's tail.
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < C::kFullBars; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
+    }
+    if (kW4) {
+      for (int s = 0; s < C::kNW; ++s) {
+        mbar_init(&wfull_bar[s], 1);
+        mbar_init(&wempty_bar[s], 8);      // one arrival per decoder warp
+      }
+      for (int a = 0; a < C::kAStages; ++a) {
+        mbar_init(&afull_bar[a], kGemm1 ? 8 : 4);  // the warps that write the slot
+        mbar_init(&aempty_bar[a], 1);
+      }
     }
     for (int a = 0; a < C::kAccBufs; ++a) {
       mbar_init(&tfull_bar[a], 1);
@@ -228,7 +281,177 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem_base = s_tmem_base;
   const int n_units = s_n_units;
 
-  if (warp == 0) {
+  if (kW4 && warp == 0) {
+    // ---------------------------------------------- NVFP4 weight producer (one lane)
+    // One bulk copy per slab and stage: the tile of (expert, 128 rows, 128 k) is contiguous.
+    if (lane == 0) {
+      int ws = 0;
+      uint32_t wph = 0;
+      int issued = 0;
+      bool ok = true;
+      const int64_t slabs_per_expert = p.w_rows_per_expert / kSlab;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        Unit U;
+        if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
+        const int n_w = U.two ? 2 : 1;
+        const int64_t t0 = ((int64_t)U.e * slabs_per_expert + U.slab * p.slab_rows / kSlab) *
+                           p.num_kb;
+        const int64_t t1 = t0 + (int64_t)(p.second_off / kSlab) * p.num_kb;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(&wempty_bar[ws], wph ^ 1u, abort_flag, p.limit_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sw = smem + ws * C::kWBytes;
+          mbar_arrive_expect_tx(&wfull_bar[ws], n_w * C::kTileBytes);
+          bulk_load(sw, p.w4 + (t0 + kb) * C::kTileBytes, C::kTileBytes, &wfull_bar[ws]);
+          if (kGemm1 && U.two)
+            bulk_load(sw + C::kTileBytes, p.w4 + (t1 + kb) * C::kTileBytes, C::kTileBytes,
+                      &wfull_bar[ws]);
+          ++issued;
+          if (++ws == C::kNW) {
+            ws = 0;
+            wph ^= 1u;
+          }
+        }
+      }
+      if (*abort_flag) {
+        const int n = issued < C::kNW ? issued : C::kNW;
+        for (int i = issued - n; i < issued; ++i)
+          mbar_wait_drain(&wfull_bar[i % C::kNW], (uint32_t)((i / C::kNW) & 1));
+      }
+    }
+  } else if (kW4 && warp == 14) {
+    // ---------------------------------------------- NVFP4 token producer (one lane)
+    if (lane == 0) {
+      int ts = 0;
+      uint32_t tph = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        Unit U;
+        if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(&empty_bar[ts], tph ^ 1u, abort_flag, p.limit_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sb = tring + ts * C::kBBytes;
+          mbar_arrive_expect_tx(&full_bar[ts], U.n_mma * C::kStageK * 2);
+#pragma unroll
+          for (int a = 0; a < C::kStageK / kBlockK; ++a) {
+            uint8_t* sba = sb + a * kN * kBlockK * 2;
+            const int kx = kb * C::kStageK + a * kBlockK;
+            int r = 0;
+            for (; r + 128 <= U.n_mma; r += 128)
+              tma_load_2d(sba + r * kBlockK * 2, &tmB128, &full_bar[ts], kx, U.b_row0 + r);
+            for (; r + 64 <= U.n_mma; r += 64)
+              tma_load_2d(sba + r * kBlockK * 2, &tmB64, &full_bar[ts], kx, U.b_row0 + r);
+            for (; r < U.n_mma; r += 16)
+              tma_load_2d(sba + r * kBlockK * 2, &tmB, &full_bar[ts], kx, U.b_row0 + r);
+          }
+          ++issued;
+          if (++ts == C::kNT) {
+            ts = 0;
+            tph ^= 1u;
+          }
+        }
+      }
+      if (*abort_flag) {
+        const int n = issued < C::kNT ? issued : C::kNT;
+        for (int i = issued - n; i < issued; ++i)
+          mbar_wait_drain(&full_bar[i % C::kNT], (uint32_t)((i / C::kNT) & 1));
+      }
+    }
+  } else if (kW4 && warp >= 6) {
+    // ------------------------------------------------------- NVFP4 decoders (8 warps)
+    // Warp w owns TMEM lanes 32*(w%4)..+31, i.e. weight rows of the slab.  gemm1: group 0
+    // (warps 6-9) decodes the gate slab and group 1 the up slab, both into the same 64-k ring
+    // slot (columns 0-31 and 32-63).  gemm2: group g decodes k 64g..64g+63 of the stage into
+    // its own slot.  A thread decodes one weight row: 16-byte chunks of 32 codes, two scales
+    // each.  Stores are pipelined: a slot's tcgen05.st is waited for and the slot handed to the
+    // MMA only after the next half has been decoded, so the store latency hides behind ALU work.
+    const int dg = (warp - 6) >> 2;
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+    int ws = 0;
+    uint32_t wph = 0;
+    int a_cnt = 0;
+    int pending = -1;  // ring slot whose store is in flight
+    bool ok = true;
+    auto hand_over = [&](int slot) {  // make this warp's part of `slot` visible to the MMA
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&afull_bar[slot]);
+    };
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      Unit U;
+      if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
+      const bool active = !kGemm1 || dg == 0 || U.two;
+      const int slab = kGemm1 ? dg : 0;
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        if (!mbar_wait(&wfull_bar[ws], wph, abort_flag, p.limit_ns, p.status)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* tile = smem + ws * C::kWBytes + slab * C::kTileBytes;
+        const uint8_t* qrow = tile + row * 64;
+        const uint2 sfw = *reinterpret_cast<const uint2*>(tile + C::kQBytes + row * 8);
+        uint32_t s2[8];
+        nvfp4_scales(sfw.x, *reinterpret_cast<uint32_t(*)[4]>(&s2[0]));
+        nvfp4_scales(sfw.y, *reinterpret_cast<uint32_t(*)[4]>(&s2[4]));
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          // gemm1: both groups write half hh of the stage; gemm2: group dg writes half dg.
+          if (!kGemm1 && hh != dg) continue;
+          const int idx = a_cnt + hh;
+          const int slot = idx % C::kAStages;
+          if (!mbar_wait(&aempty_bar[slot], (uint32_t)(((idx / C::kAStages) & 1) ^ 1),
+                         abort_flag, p.limit_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (!active) {
+            hand_over(slot);
+            continue;
+          }
+          uint32_t v[32];
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            const int j = 2 * hh + jj;  // 32-k chunk of the stage
+            // packed layout: chunk j of row r sits at chunk j ^ ((r >> 1) & 3)
+            const uint4 qw = *reinterpret_cast<const uint4*>(qrow + ((j ^ ((row >> 1) & 3)) << 4));
+            nvfp4_decode8(qw.x, s2[2 * j], *reinterpret_cast<uint32_t(*)[4]>(&v[16 * jj]));
+            nvfp4_decode8(qw.y, s2[2 * j], *reinterpret_cast<uint32_t(*)[4]>(&v[16 * jj + 4]));
+            nvfp4_decode8(qw.z, s2[2 * j + 1], *reinterpret_cast<uint32_t(*)[4]>(&v[16 * jj + 8]));
+            nvfp4_decode8(qw.w, s2[2 * j + 1],
+                          *reinterpret_cast<uint32_t(*)[4]>(&v[16 * jj + 12]));
+          }
+          if (pending >= 0) {  // the previous store has had a whole decode to land
+            tmem_wait_st();
+            hand_over(pending);
+          }
+          const uint32_t col =
+              (uint32_t)(C::kABase + slot * C::kASlotCols + (kGemm1 ? slab * 32 : 0));
+          tmem_st_x32(tmem_base + lane_addr + col, v);
+          pending = slot;
+        }
+        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&wempty_bar[ws]);  // this warp has read the weight slot
+        a_cnt += 2;
+        if (++ws == C::kNW) {
+          ws = 0;
+          wph ^= 1u;
+        }
+      }
+    }
+    if (pending >= 0) {  // the last store (also on the way out after a timeout)
+      tmem_wait_st();
+      if (ok) hand_over(pending);
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int stage = 0;
@@ -283,6 +506,7 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
+      int a_cnt = 0;  // NVFP4: TMEM ring slots consumed so far
       bool ok = true;
       bool issued_any = false;
       const uint32_t smem_base = smem_u32(smem);
@@ -301,20 +525,52 @@ __global__ void __launch_bounds__(192, 1)
           tc_fence_after();
           const uint32_t sa = smem_base + (uint32_t)(stage * C::kStageBytes);
           const uint32_t sb = sa + C::kABytes;
+          if constexpr (kW4) {
+            // A (decoded weights) from two TMEM ring slots of 64 k each; B: the token slot.
+            const uint32_t tb = smem_base + (uint32_t)(C::kNW * C::kWBytes + stage * C::kBBytes);
+            for (int hh = 0; hh < 2 && ok; ++hh) {
+              const int idx = a_cnt + hh;
+              const int slot = idx % C::kAStages;
+              if (!mbar_wait(&afull_bar[slot], (uint32_t)((idx / C::kAStages) & 1), abort_flag,
+                             p.limit_ns, p.status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t a = tmem_base + (uint32_t)(C::kABase + slot * C::kASlotCols);
 #pragma unroll
-          for (int k = 0; k < kBlockK / 16; ++k) {
-            const uint64_t bdesc = sw128_kmajor_desc(sb + k * 32);
-            const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
-            umma_f16(d, sw128_kmajor_desc(sa + k * 32), bdesc, idesc, accum);
-            if (kGemm1 && U.two)
-              umma_f16(d + kN, sw128_kmajor_desc(sa + kSlab * kBlockK * 2 + k * 32), bdesc,
-                       idesc, accum);
-          }
-          umma_commit(&empty_bar[stage]);
-          issued_any = true;
-          if (++stage == C::kStages) {
-            stage = 0;
-            phase ^= 1u;
+              for (int k = 0; k < kBlockK / 16; ++k) {
+                const uint64_t bdesc = sw128_kmajor_desc(tb + hh * (kN * kBlockK * 2) + k * 32);
+                const uint32_t accum = (kb | hh | k) != 0 ? 1u : 0u;
+                umma_f16_tmem_a(d, a + k * 8, bdesc, idesc, accum);
+                if (kGemm1 && U.two) umma_f16_tmem_a(d + kN, a + 32 + k * 8, bdesc, idesc, accum);
+              }
+              umma_commit(&aempty_bar[slot]);
+              issued_any = true;
+            }
+            if (!ok) break;
+            a_cnt += 2;
+            umma_commit(&empty_bar[stage]);
+            if (++stage == C::kFullBars) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < kBlockK / 16; ++k) {
+              const uint64_t bdesc = sw128_kmajor_desc(sb + k * 32);
+              const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+              umma_f16(d, sw128_kmajor_desc(sa + k * 32), bdesc, idesc, accum);
+              if (kGemm1 && U.two)
+                umma_f16(d + kN, sw128_kmajor_desc(sa + kSlab * kBlockK * 2 + k * 32), bdesc,
+                         idesc, accum);
+            }
+            umma_commit(&empty_bar[stage]);
+            issued_any = true;
+            if (++stage == C::kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
         if (!ok) break;
@@ -340,6 +596,8 @@ __global__ void __launch_bounds__(192, 1)
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
       Unit U;
       if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
+      // NVFP4: the expert's FP32 scale multiplies the FP32 accumulator (before the activation)
+      const float al = kW4 ? p.alpha[U.e] : 1.0f;
       if constexpr (kGemm1) {
         // Output rows of this unit as (accumulator column, destination row) entries.  In direct
         // mode a column is a token and each route of that token to this expert is an entry; with
@@ -379,6 +637,13 @@ __global__ void __launch_bounds__(192, 1)
               if (p.gated) {
                 float g[16], v[16];
                 tmem_ld2_x16(tb + c, tb + kN + c, g, v);
+                if constexpr (kW4) {
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) {
+                    g[j] *= al;
+                    v[j] *= al;
+                  }
+                }
                 if (p.act == MOE_ACT_GELU_TANH) {
 #pragma unroll
                   for (int j = 0; j < 16; ++j) h[j] = gelu_tanh_f32(g[j]) * v[j];
@@ -391,7 +656,7 @@ __global__ void __launch_bounds__(192, 1)
                 tmem_ld_x16(tb + (uint32_t)(half * kN) + c, h);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                  const float r = fmaxf(h[j], 0.0f);
+                  const float r = fmaxf(h[j] * al, 0.0f);
                   h[j] = r * r;
                 }
               }
@@ -457,7 +722,8 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int dst = ent_dst[c0 + j];
-            if (dst >= 0 && in_range) out[(int64_t)dst * p.n_out + h] = g[j] * col_scale[c0 + j];
+            if (dst >= 0 && in_range)
+              out[(int64_t)dst * p.n_out + h] = (kW4 ? g[j] * al : g[j]) * col_scale[c0 + j];
           }
         }
         tc_fence_before();
@@ -515,18 +781,21 @@ bool make_map(CUtensorMap* m, int dtype, const void* base, uint64_t inner, uint6
   return r == CUDA_SUCCESS;
 }
 
-template <bool kGemm1, int kN, typename T>
+template <bool kGemm1, int kN, typename T, bool kW4>
 cudaError_t launch_typed(const GemmCall& c, const KParams& kp, int grid, cudaStream_t s,
                          bool pdl) {
-  using C = Cfg<kGemm1, kN>;
+  using C = Cfg<kGemm1, kN, kW4>;
   CUtensorMap tmW, tmB, tmB64, tmB128;
   const uint64_t w_rows = (uint64_t)c.E * (uint64_t)kp.w_rows_per_expert;
-  if (!make_map(&tmW, c.dtype, c.w, (uint64_t)c.K, w_rows, kSlab)) return cudaErrorInvalidValue;
+  // NVFP4 weights are read with plain bulk copies: tmW is then a copy of the token map, unused.
+  if (!kW4 && !make_map(&tmW, c.dtype, c.w, (uint64_t)c.K, w_rows, kSlab))
+    return cudaErrorInvalidValue;
   if (!make_map(&tmB, c.dtype, c.b, (uint64_t)c.K, (uint64_t)c.b_rows, 16) ||
       !make_map(&tmB64, c.dtype, c.b, (uint64_t)c.K, (uint64_t)c.b_rows, 64) ||
       !make_map(&tmB128, c.dtype, c.b, (uint64_t)c.K, (uint64_t)c.b_rows, 128))
     return cudaErrorInvalidValue;
-  auto kern = moe_gemm_kernel<kGemm1, kN, T>;
+  if (kW4) tmW = tmB;
+  auto kern = moe_gemm_kernel<kGemm1, kN, T, kW4>;
   static bool attr_set = false;  // one per instantiation: set once per process
   if (!attr_set) {
     cudaError_t e =
@@ -534,15 +803,16 @@ cudaError_t launch_typed(const GemmCall& c, const KParams& kp, int grid, cudaStr
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_k(kern, dim3(grid), dim3(192), C::kSmemBytes, s, pdl, tmW, tmB, tmB64, tmB128,
-                  kp);
+  return launch_k(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, pdl, tmW, tmB, tmB64,
+                  tmB128, kp);
 }
 
 template <bool kGemm1, typename T>
 cudaError_t launch_rows(const GemmCall& c, const KParams& kp, int grid, cudaStream_t s,
                         bool pdl) {
-  return c.tile_rows == 256 ? launch_typed<kGemm1, 256, T>(c, kp, grid, s, pdl)
-                            : launch_typed<kGemm1, 128, T>(c, kp, grid, s, pdl);
+  if (c.w4) return launch_typed<kGemm1, 128, __nv_bfloat16, true>(c, kp, grid, s, pdl);
+  return c.tile_rows == 256 ? launch_typed<kGemm1, 256, T, false>(c, kp, grid, s, pdl)
+                            : launch_typed<kGemm1, 128, T, false>(c, kp, grid, s, pdl);
 }
 
 }  // namespace
@@ -564,6 +834,18 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   kp.n_slabs = (c.n_out + kp.slab_rows - 1) / kp.slab_rows;
   kp.num_kb = (c.K + kBlockK - 1) / kBlockK;
   kp.w_rows_per_expert = kp.gated ? 2 * c.n_out : c.n_out;
+  kp.w4 = nullptr;
+  kp.alpha = nullptr;
+  if (c.w4) {
+    // NVFP4 weights: bf16 activations, 128-row token tiles, K and the output width whole
+    // multiples of 128 (one stage is 128 k; a weight slab never crosses an expert).
+    if (c.dtype != MOE_BF16 || c.tile_rows != kTileRows || c.K % 128 != 0 || c.n_out % 128 != 0 ||
+        !c.alpha || (reinterpret_cast<uintptr_t>(c.w) & 15) != 0)
+      return cudaErrorInvalidValue;
+    kp.num_kb = c.K / 128;
+    kp.w4 = static_cast<const uint8_t*>(c.w);
+    kp.alpha = c.alpha;
+  }
   kp.tiles = c.tiles;
   kp.n_tiles = c.n_tiles;
   kp.sorted_ids = c.sorted_ids;

@@ -67,16 +67,17 @@ extern "C" moe_status_t moe_align_sort_noalloc(const moe_problem_t* p, int32_t b
   if (block_m <= 0 || block_m > 1024) return MOE_ERR_INVALID_ARG;
   if (!counts || !offsets || !sorted_ids || !inv_route) return MOE_ERR_INVALID_ARG;
   if (p->T > 0 && !topk_ids) return MOE_ERR_INVALID_ARG;
+  const moe_problem_t Pl = local_view(*p);  // ids index the local experts of a shard
   const int64_t P = (int64_t)p->T * p->top_k;
   const int64_t n_chunks = (P + 255) / 256;
-  if (n_chunks * p->E > kNoAllocHistInts) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (n_chunks * Pl.E > kNoAllocHistInts) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = (cudaStream_t)stream;
   int32_t* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
   int* status = reinterpret_cast<int*>(scratch);
   if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
   const int64_t cap = P + (int64_t)p->E * (block_m - 1);
-  if (launch_align_sort_chunked(*p, block_m, topk_ids, counts, offsets, sorted_ids, cap,
+  if (launch_align_sort_chunked(Pl, block_m, topk_ids, counts, offsets, sorted_ids, cap,
                                 tile_expert, inv_route, scratch + kNoAllocHeaderInts, status, s,
                                 false, nullptr, nullptr, kTileRows, nullptr, nullptr,
                                 kTileRows) != cudaSuccess)

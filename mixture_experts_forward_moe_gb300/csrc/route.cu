@@ -49,8 +49,9 @@ __device__ __forceinline__ bool before(float ka, int ea, float kb, int eb) {
 template <int VPL>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     route_kernel(int T, int E, int K, int scoring, int renorm, int G, int keepG, float rsf,
-                 const float* __restrict__ gating, const float* __restrict__ bias,
-                 int32_t* __restrict__ ids, float* __restrict__ wout) {
+                 int loc0, int nloc, const float* __restrict__ gating,
+                 const float* __restrict__ bias, int32_t* __restrict__ ids,
+                 float* __restrict__ wout) {
   __shared__ float s_gscore[kWarpsPerBlock][32];
   pdl_wait();
   pdl_trigger();
@@ -190,7 +191,9 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     w = renorm ? my_v / part : my_v;
   }
   if (lane < K) {
-    ids[(size_t)t * K + lane] = my_e;
+    // Expert-parallel shard: local index, or -1 (padding) for an expert held elsewhere.
+    const int le = my_e - loc0;
+    ids[(size_t)t * K + lane] = (le >= 0 && le < nloc) ? le : -1;
     wout[(size_t)t * K + lane] = w * rsf;
   }
 }
@@ -201,9 +204,11 @@ cudaError_t launch_vpl(const moe_problem_t& p, const float* gating, const float*
   const int G = p.num_expert_group > 1 ? p.num_expert_group : 1;
   const int keepG = G > 1 ? p.topk_group : 1;
   const int blocks = (p.T + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  const int loc0 = p.ep_num_local > 0 ? p.ep_local_offset : 0;
+  const int nloc = local_experts(p);
   return launch_k(route_kernel<VPL>, dim3(blocks), dim3(kWarpsPerBlock * 32), 0, s, pdl, p.T,
                   p.E, p.top_k, p.scoring, p.renormalize, G, keepG, p.routed_scaling_factor,
-                  gating, bias, ids, w);
+                  loc0, nloc, gating, bias, ids, w);
 }
 
 }  // namespace

@@ -73,18 +73,20 @@ class Workload:
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
 
-    def flops(self) -> float:
+    def flops(self, routes=None) -> float:
         """2*T*k*3*F*H (+ 2*T*3*S*H): the FLOP count the TileOPs MoE page's TFLOP/s uses (three
-        F x H matrices per expert; two for the single-projection ReLU2 MLP)."""
+        F x H matrices per expert; two for the single-projection ReLU2 MLP).  `routes` replaces
+        T*k when only some routes are computed (the local experts of a shard)."""
         m = 3 if self.gated else 2
-        return 2.0 * self.T * self.top_k * m * self.F * self.H + 2.0 * self.T * m * self.S * self.H
+        P = self.T * self.top_k if routes is None else routes
+        return 2.0 * P * m * self.F * self.H + 2.0 * self.T * m * self.S * self.H
 
     def kwargs(self) -> dict:
         return dict(top_k=self.top_k, scoring_func=self.scoring_func,
                     renormalize=self.renormalize, num_expert_group=self.num_expert_group,
                     topk_group=self.topk_group,
                     routed_scaling_factor=self.routed_scaling_factor,
-                    activation=self.activation)
+                    activation=self.activation, ep_local_offset=self.ep_offset)
 
 
 # The five workloads this project is measured on (sizes from the pages' shape lists).

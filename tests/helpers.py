@@ -109,13 +109,30 @@ def oracle_route(w, d):
                         w.routed_scaling_factor, bias)
 
 
+def local_ids(w, ids):
+    """The router's global ids as indices of the shard's experts (-1 outside the shard)."""
+    if w.ep_local <= 0:
+        return ids
+    off = w.ep_offset
+    return np.where((ids >= off) & (ids < off + w.ep_local), ids - off, -1).astype(np.int32)
+
+
 def oracle_fused(w, d, tokens=None, routed=None):
-    """fp64 oracle output for `tokens` (all when None), its ids and weights.  Only the experts
-    the listed tokens use are copied to the host."""
+    """fp64 oracle output for `tokens` (all when None), its (global) ids and weights.  Only the
+    experts the listed tokens use are copied to the host (16-bit weights)."""
     ids, wts, near = routed if routed is not None else oracle_route(w, d)
     tl = np.arange(w.T, dtype=np.int32) if tokens is None else np.asarray(tokens, np.int32)
+    lids = local_ids(w, ids)
+    if w.weights == "nvfp4":
+        w1 = tuple(t.cpu() for t in d["w_gate_up"])
+        w2 = tuple(t.cpu() for t in d["w_down"])
+        out = oracle.moe_tokens_w4(d["hidden_states"].cpu(), lids, wts, w1, w2,
+                                   dt_code(w.dtype), tokens=tl,
+                                   activation=ACT_CODES[w.activation])
+        return out, ids, wts, near
+    ids_g, ids = ids, lids
     used = sorted(set(int(e) for e in ids[tl].reshape(-1) if e >= 0))
-    slot = np.full(w.E, -1, np.int32)
+    slot = np.full(w.E_local, -1, np.int32)
     slot[used] = np.arange(len(used), dtype=np.int32)
     idx = torch.tensor(used, dtype=torch.long, device=d["w_gate_up"].device)
     wgu = d["w_gate_up"].index_select(0, idx).cpu() if used else d["w_gate_up"][:1].cpu()
@@ -123,13 +140,24 @@ def oracle_fused(w, d, tokens=None, routed=None):
     sgu = None if d["shared_w_gate_up"] is None else d["shared_w_gate_up"].cpu()
     sd = None if d["shared_w_down"] is None else d["shared_w_down"].cpu()
     out = oracle.moe_tokens(d["hidden_states"].cpu(), ids, wts, wgu, wd, dt_code(w.dtype),
-                            tokens=tl, expert_slot=slot, num_experts=w.E,
+                            tokens=tl, expert_slot=slot, num_experts=w.E_local,
                             shared_w_gate_up=sgu, shared_w_down=sd,
                             activation=ACT_CODES[w.activation])
-    return out, ids, wts, near
+    return out, ids_g, wts, near
+
+
+def packed_w4(d):
+    """The NVFP4 weights of input dict d in the library's packed layout (packed once, kept in d)."""
+    if "w4_packed" not in d:
+        d["w4_packed"] = (B.pack_nvfp4_weights(*d["w_gate_up"]), B.pack_nvfp4_weights(*d["w_down"]))
+    return d["w4_packed"]
 
 
 def run_fused(w, d, **kw):
+    if w.weights == "nvfp4":
+        w1, w2 = packed_w4(d)
+        return B.fused_moe_fwd_w4a16(d["hidden_states"], d["gating_output"], w1, w2,
+                                     correction_bias=d["correction_bias"], **w.kwargs(), **kw)
     return B.fused_moe_fwd(d["hidden_states"], d["gating_output"], d["w_gate_up"], d["w_down"],
                            correction_bias=d["correction_bias"],
                            shared_w_gate_up=d["shared_w_gate_up"],
