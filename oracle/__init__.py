@@ -78,6 +78,8 @@ def _load():
             _lib.oracle_expert_down.argtypes = [i32, i32, i32, i32, P, P, P, P, P]
             _lib.oracle_combine.argtypes = [i32, i32, i32, i32, P, P, P, P]
             _lib.oracle_num_threads.restype = i32
+            _lib.oracle_grouped_gemm.argtypes = [i32, i32, i32, i32, i64, i32, i32, P, P, P, P]
+            _lib.oracle_post_permute.argtypes = [i32, i32, i32, i32, P, P, P, P]
             _lib.oracle_e2m1_to_double.restype = f64
             _lib.oracle_e2m1_to_double.argtypes = [i32]
             _lib.oracle_e4m3_to_double.restype = f64
@@ -329,3 +331,35 @@ def expert_down_w4(act_rows, expert_of_row, scale, w2, dtype):
     _check(_load().oracle_expert_down_w4(n, H, F, dtype, _ptr(ab), _ptr(eo), _ptr(sc), _ptr(q2),
                                          _ptr(s2), _ptr(a2), _ptr(y)), "oracle_expert_down_w4")
     return y
+
+
+# --------------------------------------------------------------- grouped GEMM and post-permute
+def grouped_gemm(a, b, meta, dtype, activation=0, max_m=0):
+    """fp64 grouped GEMM (oracle.c: oracle_grouped_gemm).  Masked layout when max_m > 0
+    (a [E, max_m, K], meta = valid rows per group), else contiguous (a [P, K], meta = inclusive
+    prefix sums).  activation 1 = silu_and_mul (b [E, 2N, K]).  Returns out [rows, N]."""
+    ab = _bits(a)
+    K = ab.shape[-1]
+    ab = ab.reshape(-1, K)
+    bb = _bits(b)
+    E = bb.shape[0]
+    N = bb.shape[1] // (2 if activation else 1)
+    mv = _c(meta, np.int32)
+    out = np.empty((ab.shape[0], N), np.float64)
+    _check(_load().oracle_grouped_gemm(E, N, K, int(max_m), ab.shape[0], dtype, activation,
+                                       _ptr(ab), _ptr(bb), _ptr(mv), _ptr(out)),
+           "oracle_grouped_gemm")
+    return out
+
+
+def post_permute(rows, weights, inv, top_k, dtype):
+    """fp64 weighted combine out[t] = sum_j w[t,j] rows[inv[t*k+j]] (oracle_post_permute)."""
+    rb = _bits(rows)
+    H = rb.shape[1]
+    wv = _c(weights, np.float64).reshape(-1)
+    iv = _c(inv, np.int32).reshape(-1)
+    T = iv.size // top_k
+    out = np.empty((T, H), np.float64)
+    _check(_load().oracle_post_permute(T, H, top_k, dtype, _ptr(rb), _ptr(wv), _ptr(iv),
+                                       _ptr(out)), "oracle_post_permute")
+    return out

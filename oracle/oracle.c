@@ -17,6 +17,8 @@
  *   - flashinfer PR #4048 (CuTe DSL W4A16 MoE) and its weight-scale placement ablation: NVFP4
  *     experts, E2M1 codes with E4M3 block scales over 16 elements and an FP32 per-expert scale
  *     (oracle_moe_tokens_w4 and the stage references after it).
+ *   - The same page's op MoEGroupedGemmFwd in its contiguous and masked layouts
+ *     (oracle_grouped_gemm) and op MoEPostPermuteFwd with route weights (oracle_post_permute).
  *   - ROCm/aiter PR #5973 "[FlyDSL] Optimize MI308 MoE decoding (3/3)", section "Changes":
  *     routes whose expert id is -1 are padding and are skipped; the prefill sort returns each
  *     route's sorted row (the inverse map produced here).
@@ -729,6 +731,83 @@ int oracle_expert_down_w4(int n_rows, int H, int F, int dtype, const uint16_t* a
     const w4_mat m2 = w4_expert(w2q, w2sf, w2a, e, H, F);
     for (int h = 0; h < H; ++h) o[h] = scale[r] * w4_dot(&m2, h, a);
     free(a);
+  }
+  return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Standalone grouped GEMM and post-permute (TileOPs "MoE" page, ops MoEGroupedGemmFwd and     */
+/* MoEPostPermuteFwd).                                                                         */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * oracle_grouped_gemm: out[r, n] = sum_k a[r, k] * b[e(r), n, k] for the rows r of each group e.
+ *   masked layout (max_m > 0): a [E, max_m, K], out [E, max_m, N]; group e owns rows
+ *     e*max_m .. e*max_m + meta[e] - 1 (meta = valid rows per group, clamped to [0, max_m]);
+ *   contiguous layout (max_m == 0): a [P, K], out [P, N]; meta [E] are the inclusive prefix
+ *     sums of the groups' row counts (group e owns rows meta[e-1] .. meta[e] - 1, meta[-1] = 0).
+ * activation 0: plain product (b [E, N, K]); activation 1: silu_and_mul, b [E, 2N, K] with the
+ * gate rows first, out = SiLU(a.b_gate) * (a.b_up).  Rows outside every group are left at 0.
+ */
+int oracle_grouped_gemm(int E, int N, int K, int max_m, int64_t rows, int dtype, int activation,
+                        const uint16_t* a, const uint16_t* b, const int32_t* meta, double* out) {
+  if (E <= 0 || N <= 0 || K <= 0 || max_m < 0 || rows < 0 || (dtype != 0 && dtype != 1) ||
+      (activation != 0 && activation != 1))
+    return ORACLE_ERR_ARG;
+  const double* tab = decode_table(dtype);
+  const int64_t nb = (int64_t)(activation ? 2 : 1) * N;
+  for (int64_t i = 0; i < rows * N; ++i) out[i] = 0.0;
+  int bad = 0;
+  for (int e = 0; e < E; ++e) {
+    int64_t r0, r1;
+    if (max_m > 0) {
+      int m = meta[e] < 0 ? 0 : (meta[e] > max_m ? max_m : meta[e]);
+      r0 = (int64_t)e * max_m;
+      r1 = r0 + m;
+    } else {
+      r0 = e == 0 ? 0 : meta[e - 1];
+      r1 = meta[e];
+    }
+    if (r0 < 0 || r1 < r0 || r1 > rows) {
+      bad = 1;
+      continue;
+    }
+    const uint16_t* be = b + (int64_t)e * nb * K;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t r = r0; r < r1; ++r) {
+      const uint16_t* ar = a + r * K;
+      for (int n = 0; n < N; ++n) {
+        double g = 0.0;
+        for (int k = 0; k < K; ++k) g += tab[ar[k]] * tab[be[(int64_t)n * K + k]];
+        if (activation) {
+          double u = 0.0;
+          for (int k = 0; k < K; ++k) u += tab[ar[k]] * tab[be[(int64_t)(N + n) * K + k]];
+          g = g / (1.0 + exp(-g)) * u;
+        }
+        out[r * N + n] = g;
+      }
+    }
+  }
+  return bad ? ORACLE_ERR_ARG : ORACLE_OK;
+}
+
+/*
+ * oracle_post_permute (TileOPs "MoE" page, op MoEPostPermuteFwd):
+ *   out[t, :] = sum_j weights[t, j] * rows[inv[t*k + j], :]   (routes with inv = -1 skipped)
+ */
+int oracle_post_permute(int T, int H, int top_k, int dtype, const uint16_t* rows_bits,
+                        const double* weights, const int32_t* inv, double* out) {
+  if (T < 0 || H <= 0 || top_k <= 0 || (dtype != 0 && dtype != 1)) return ORACLE_ERR_ARG;
+  const double* tab = decode_table(dtype);
+  for (int t = 0; t < T; ++t) {
+    double* o = out + (int64_t)t * H;
+    for (int h = 0; h < H; ++h) o[h] = 0.0;
+    for (int j = 0; j < top_k; ++j) {
+      const int p = inv[(int64_t)t * top_k + j];
+      if (p < 0) continue;
+      const double w = weights[(int64_t)t * top_k + j];
+      for (int h = 0; h < H; ++h) o[h] += w * tab[rows_bits[(int64_t)p * H + h]];
+    }
   }
   return ORACLE_OK;
 }

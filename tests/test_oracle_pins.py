@@ -504,6 +504,62 @@ def test_ep_shards_partition_the_full_output():
     np.testing.assert_allclose(total, full, rtol=1e-12, atol=1e-14)
 
 
+# --------------------------------------------------------------- grouped GEMM, post-permute
+def _bf16(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("activation", [0, 1])
+def test_masked_grouped_gemm_is_a_matmul_per_group(activation):
+    rng = np.random.default_rng(7)
+    E, max_m, K, N = 3, 9, 40, 12
+    a = _bf16(rng.standard_normal((E, max_m, K)))
+    b = _bf16(rng.standard_normal((E, (2 if activation else 1) * N, K)) / np.sqrt(K))
+    meta = np.array([9, 0, 4], np.int32)
+    out = oracle.grouped_gemm(a, b, meta, oracle.BF16, activation=activation, max_m=max_m)
+    A, Bm = a.double().numpy(), b.double().numpy()
+    ref = np.zeros((E * max_m, N))
+    for e in range(E):
+        rows = A[e, :meta[e]]
+        g = rows @ Bm[e, :N].T
+        if activation:
+            g = g * scipy.special.expit(g) * (rows @ Bm[e, N:].T)
+        ref[e * max_m:e * max_m + meta[e]] = g
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_contiguous_grouped_gemm_uses_inclusive_prefix_sums():
+    rng = np.random.default_rng(8)
+    E, K, N = 4, 24, 8
+    counts = np.array([3, 0, 5, 2])
+    psum = np.cumsum(counts).astype(np.int32)  # inclusive: group e ends at psum[e]
+    a = _bf16(rng.standard_normal((int(psum[-1]), K)))
+    b = _bf16(rng.standard_normal((E, N, K)))
+    out = oracle.grouped_gemm(a, b, psum, oracle.BF16)
+    A, Bm = a.double().numpy(), b.double().numpy()
+    starts = np.concatenate([[0], psum[:-1]])
+    for e in range(E):
+        np.testing.assert_allclose(out[starts[e]:psum[e]], A[starts[e]:psum[e]] @ Bm[e].T,
+                                   rtol=1e-12, atol=1e-12)
+
+
+def test_post_permute_is_a_weighted_gather_sum():
+    rng = np.random.default_rng(9)
+    T, k, H, rows = 6, 3, 16, 20
+    x = _bf16(rng.standard_normal((rows, H)))
+    w = rng.random((T, k))
+    inv = rng.permutation(rows)[:T * k].astype(np.int32)
+    inv[4] = -1
+    out = oracle.post_permute(x, w, inv, k, oracle.BF16)
+    X = x.double().numpy()
+    ref = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            if inv[t * k + j] >= 0:
+                ref[t] += w[t, j] * X[inv[t * k + j]]
+    np.testing.assert_allclose(out, ref, rtol=1e-13, atol=1e-14)
+
+
 # ------------------------------------------------------------------------- skewed routing
 def test_skew_bias_is_minus_alpha_log1p_of_a_ranking():
     b = inputs.skew_bias(16, 0.1, seed=0).double().numpy()
