@@ -562,6 +562,137 @@ def run_reference(args, w):
     return res
 
 
+# ----------------------------------------------------------- grouped GEMM (masked layout) arm
+PUBLISHED_GROUPED_MS = {"ds-v3-ep8-masked": 0.4851}  # TileOPs MoE page (hardware not stated)
+
+
+def run_grouped_gemm(args, w, ws_n, rank, local):
+    """moe_grouped_gemm on a masked-layout workload: K timed calls (a CUDA-graph replay each),
+    inputs resident in HBM; the same contract as the fused line."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from mixture_experts_forward_moe_gb300 import binding as B
+    from mixture_experts_forward_moe_gb300 import inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    d = inputs.generate_grouped_gemm(w, seed=args.seed, device=dev)
+    a, b, meta = d["a"], d["b"], d["meta"]
+    out = torch.zeros((w.E, w.max_m, w.N), dtype=w.dtype, device=dev)
+    g = B.grouped_gemm_desc(a, b)
+    wsp = B.new_workspace(B.lib().moe_grouped_gemm_workspace_size(B.ctypes.byref(g)), dev)
+    stream = torch.cuda.current_stream()
+    valid = int(meta.sum())
+
+    def step():
+        B.moe_grouped_gemm(a, b, meta, out=out, workspace=wsp)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    graph = None
+    if not args.eager:
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            step()
+        stream.wait_stream(cap)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        torch.cuda.synchronize()
+    run = graph.replay if graph is not None else step
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local) if rank == 0 else None
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        run()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop() if clocks else None
+    step_ms = [x.elapsed_time(y) for x, y in zip(starts, ends)]
+    max_ms = max_over_ranks(float(sum(step_ms)))
+    ms = max_ms / args.steps
+    st = B.get_device_status(wsp)
+    if st != B.MOE_OK:
+        raise RuntimeError(f"device status: {B.status_string(st)}")
+    flops = w.flops(valid)
+    value = job_throughput(flops, ws_n, args.steps, max_ms) / 1e12
+    hbm_gbs, bf16_peak, bf16_sust, peak_src = measured_peaks()
+    eb = 2
+    ab = w.E * w.N * w.K * eb + valid * w.K * eb + valid * w.N * eb  # weights + valid rows in/out
+    achieved = ab / (ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "moe_gemm_kernel (grouped, masked layout)",
+                "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
+                "traffic": None, "algorithmic_bytes": ab, "avg_launch_ms": ms,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                "timing": "event pair around each call (one graph replay: tile list + GEMM)",
+                "tensor": {"achieved_tflops": flops / (ms * 1e-3) / 1e12,
+                           "peak_tflops": bf16_sust,
+                           "frac": flops / (ms * 1e-3) / 1e12 / bf16_sust}}
+    res = {
+        "metric": "moe_grouped_gemm device ms, TFLOP/s & HBM GB/s (masked layout)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": ws_n, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic: N(0,1) a, N(0,1/K) b, valid "
+        f"rows per group uniform in [{w.m_lo}, {w.m_hi}]",
+        "config": {"workload": w.name, "E": w.E, "max_m": w.max_m, "K": w.K, "N": w.N,
+                   "valid_rows": valid, "global_batch": valid * ws_n,
+                   "parallelism": f"replicas x{ws_n}",
+                   "l2": f"no flush: each call streams {w.E * w.N * w.K * eb / 1e9:.2f} GB of "
+                         f"weights, more than twice the L2",
+                   "timing": "one CUDA-graph replay per step; CUDA event pair per step"},
+        "roofline": roofline, "gpu_launches": 2 * args.steps, "clocks": clk,
+        "context_published_ms": {"ms": PUBLISHED_GROUPED_MS.get(w.name),
+                                 "where": "TileOPs MoE page, MoEGroupedGemmFwd (hardware not "
+                                          "stated)"},
+    }
+    if not args.no_e2e:
+        h_a = a.cpu().pin_memory()
+        h_meta = meta.cpu().pin_memory()
+        h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        a_dev, meta_dev = torch.empty_like(a), torch.empty_like(meta)
+        n_e2e = max(1, min(args.steps, 50))
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_e2e)]
+        torch.cuda.synchronize()
+        for i in range(n_e2e):
+            es[2 * i].record(stream)
+            a_dev.copy_(h_a, non_blocking=True)
+            meta_dev.copy_(h_meta, non_blocking=True)
+            B.moe_grouped_gemm(a_dev, b, meta_dev, out=out, workspace=wsp)
+            h_out.copy_(out, non_blocking=True)
+            es[2 * i + 1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = statistics.mean(es[2 * i].elapsed_time(es[2 * i + 1]) for i in range(n_e2e))
+        res["e2e"] = {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                      "h2d_bytes_per_step": h_a.numel() * 2 + h_meta.numel() * 4,
+                      "d2h_bytes_per_step": h_out.numel() * 2, "ms_per_step": e2e_ms}
+    if not args.no_cpu_baseline and rank == 0:
+        # the oracle on one sampled row per group, timed for about cpu_budget seconds
+        rows = np.arange(w.E) * w.max_m
+        a_s = a.reshape(w.E * w.max_m, w.K)[torch.from_numpy(rows).to(dev)].cpu()
+        b_c = b.cpu()
+        t0, passes = time.perf_counter(), 0
+        while time.perf_counter() - t0 < args.cpu_budget and passes < 1000:
+            for e in range(w.E):
+                oracle.grouped_gemm(a_s[e:e + 1].reshape(1, 1, w.K), b_c[e:e + 1],
+                                    np.array([1], np.int32), oracle.BF16, max_m=1)
+            passes += 1
+        el = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": w.flops(w.E) * passes / el / 1e12, "unit": "TFLOP/s",
+                               "cores": oracle.num_threads(), "kind": "oracle",
+                               "sample": f"1 valid row per group ({w.E} rows) per pass, "
+                                         f"{passes} passes in {el:.1f} s"}
+    return res
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -583,6 +714,28 @@ def main(argv=None):
     import torch
 
     from mixture_experts_forward_moe_gb300 import inputs
+    if args.workload in inputs.GROUPED_GEMM_WORKLOADS:
+        gw = inputs.GROUPED_GEMM_WORKLOADS[args.workload]
+        ws_n, rank, local = dist_env()
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable": "the oracle arm covers the "
+                                  "fused workloads; the grouped GEMM line carries its own "
+                                  "cpu_baseline"}), flush=True)
+            return 0
+        if ws_n > 1:
+            import torch.distributed as dist
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        try:
+            res = run_grouped_gemm(args, gw, ws_n, rank, local)
+        finally:
+            if ws_n > 1:
+                import torch.distributed as dist
+                dist.destroy_process_group()
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return 0
     w = inputs.workload(args.workload)
     if args.dtype == "f16":
         w = w.with_(dtype=torch.float16)

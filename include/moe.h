@@ -325,6 +325,71 @@ moe_status_t moe_align_sort_noalloc(const moe_problem_t* p, int32_t block_m,
                                     int32_t* inv_route, int32_t* status_out, void* stream);
 
 /* ---------------------------------------------------------------------------------------- */
+/* Expert-parallel building blocks (TileOPs "MoE" page: ops MoEPrePermuteFwd, MoEGroupedGemmFwd */
+/* in its masked and contiguous layouts, MoEPostPermuteFwd), for callers that move tokens      */
+/* between GPUs themselves and run the experts on local expert ids.                            */
+/* ---------------------------------------------------------------------------------------- */
+
+/*
+ * moe_pre_permute -- op MoEPrePermuteFwd: the rows of hidden_states in local-expert order
+ * (contiguous layout, tight packing, alignment 1).  p->E is the number of local experts;
+ * local_ids [T, top_k] int32 holds local expert ids in [0, E), or -1 for a route to another GPU.
+ *   permuted   [T*top_k, H] dtype out: rows [offsets[e], offsets[e+1]) are the tokens routed to
+ *              local expert e, in ascending route order; rows from offsets[E] on are untouched
+ *   offsets    [E+1] out (prefix sums; offsets[E] = local routes), sorted_ids [T*top_k] out
+ *              (route index r = t*top_k + j of each row, then -1), inv_route [T*top_k] out
+ *              (row of each route, -1 for other GPUs' routes)
+ *   workspace  moe_workspace_size(p) bytes (scratch and status word).
+ * An id outside [-1, E) is treated as -1 and sets MOE_ERR_BAD_EXPERT_ID in the status word.
+ */
+moe_status_t moe_pre_permute(const moe_problem_t* p, const void* hidden_states,
+                             const int32_t* local_ids, void* permuted, int32_t* offsets,
+                             int32_t* sorted_ids, int32_t* inv_route, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* Grouped GEMM description (op MoEGroupedGemmFwd). */
+typedef struct {
+  int32_t E;          /* groups (experts), 1 <= E <= 1024 */
+  int32_t N;          /* output columns; a multiple of 8 */
+  int32_t K;          /* reduction length; a multiple of 8 */
+  int32_t max_m;      /* > 0: masked layout; 0: contiguous layout */
+  int64_t rows;       /* contiguous layout: rows P of a and out (ignored when masked) */
+  int32_t dtype;      /* moe_dtype_t of a, b and a 16-bit out */
+  int32_t activation; /* 0: plain product; 1: silu_and_mul (b holds gate rows then up rows) */
+  int32_t out_f32;    /* plain product only: out is f32 (the "bf16/f32" form) */
+} moe_grouped_gemm_t;
+
+/*
+ * moe_grouped_gemm -- op MoEGroupedGemmFwd: out[r, :] = a[r, :] . b[e(r)]^T for the rows r of
+ * each group e, on the tcgen05 tensor cores (f32 accumulation, one rounding to dtype unless
+ * out_f32), with silu_and_mul when activation = 1:
+ *   masked layout (max_m > 0): a [E, max_m, K], out [E, max_m, N]; layout_metadata [E] int32 is
+ *     the number of valid rows of each group (clamped to [0, max_m]); group e owns rows
+ *     e*max_m .. e*max_m + layout_metadata[e] - 1, and the other rows of out are untouched;
+ *   contiguous layout (max_m == 0): a [rows, K], out [rows, N]; layout_metadata [E] int32 holds
+ *     the inclusive prefix sums of the groups' row counts (group e owns rows
+ *     layout_metadata[e-1] .. layout_metadata[e] - 1, with layout_metadata[-1] = 0).
+ *   b [E, N, K] (activation 0) or [E, 2N, K] (activation 1) dtype, K contiguous.
+ *   workspace  moe_grouped_gemm_workspace_size(g) bytes; a prefix sum that decreases or passes
+ *              `rows` sets MOE_ERR_INVALID_ARG in its status word (moe_get_device_status).
+ */
+size_t moe_grouped_gemm_workspace_size(const moe_grouped_gemm_t* g);
+moe_status_t moe_grouped_gemm(const moe_grouped_gemm_t* g, const void* a, const void* b,
+                              const int32_t* layout_metadata, void* out, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/*
+ * moe_post_permute -- op MoEPostPermuteFwd: the weighted top-k combine
+ *   out[t, :] = round( sum_{j=0..k-1} topk_weights[t*k+j] * rows[inv_route[t*k+j], :] )
+ * summed in f32 in fixed j order (deterministic), rounded once to dtype; routes with
+ * inv_route -1 are skipped (a token with none gets a zero row).
+ *   rows [*, H] dtype; topk_weights [T*k] f32; inv_route [T*k] int32; out [T, H] dtype.
+ */
+moe_status_t moe_post_permute(const moe_problem_t* p, const void* rows,
+                              const float* topk_weights, const int32_t* inv_route, void* out,
+                              void* stream);
+
+/* ---------------------------------------------------------------------------------------- */
 /* Status.                                                                                    */
 /* ---------------------------------------------------------------------------------------- */
 

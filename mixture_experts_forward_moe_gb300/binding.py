@@ -38,7 +38,8 @@ EXPORTED = (
     "moe_gemm2", "moe_combine", "moe_shared_expert_fwd", "moe_get_device_status",
     "moe_status_string", "moe_set_wait_limit_ns", "moe_stage_name", "moe_profile_enable",
     "moe_profile_collect", "moe_align_sort_noalloc", "fused_moe_fwd_w4a16", "moe_gemm1_w4a16",
-    "moe_gemm2_w4a16", "moe_nvfp4_pack", "moe_nvfp4_packed_bytes",
+    "moe_gemm2_w4a16", "moe_nvfp4_pack", "moe_nvfp4_packed_bytes", "moe_pre_permute",
+    "moe_grouped_gemm_workspace_size", "moe_grouped_gemm", "moe_post_permute",
 )
 
 
@@ -51,6 +52,14 @@ class MoeProblem(ctypes.Structure):
         ("routed_scaling_factor", ctypes.c_float), ("S", ctypes.c_int32),
         ("activation", ctypes.c_int32), ("ep_num_local", ctypes.c_int32),
         ("ep_local_offset", ctypes.c_int32),
+    ]
+
+
+class GroupedGemm(ctypes.Structure):
+    _fields_ = [
+        ("E", ctypes.c_int32), ("N", ctypes.c_int32), ("K", ctypes.c_int32),
+        ("max_m", ctypes.c_int32), ("rows", ctypes.c_int64), ("dtype", ctypes.c_int32),
+        ("activation", ctypes.c_int32), ("out_f32", ctypes.c_int32),
     ]
 
 
@@ -110,6 +119,14 @@ def lib():
             L.moe_gemm2_w4a16.argtypes = [PP, i32, P, P, P, P, P, P, P, P, sz, P]
             L.moe_nvfp4_pack.restype = ctypes.c_int
             L.moe_nvfp4_pack.argtypes = [i64, i32, i32, P, P, P, P]
+            L.moe_pre_permute.argtypes = [PP, P, P, P, P, P, P, P, sz, P]
+            GG = ctypes.POINTER(GroupedGemm)
+            L.moe_grouped_gemm_workspace_size.restype = sz
+            L.moe_grouped_gemm_workspace_size.argtypes = [GG]
+            L.moe_grouped_gemm.argtypes = [GG, P, P, P, P, P, sz, P]
+            L.moe_post_permute.argtypes = [PP, P, P, P, P, P]
+            for fn in ("moe_pre_permute", "moe_grouped_gemm", "moe_post_permute"):
+                getattr(L, fn).restype = ctypes.c_int
             L.moe_nvfp4_packed_bytes.restype = i64
             L.moe_nvfp4_packed_bytes.argtypes = [i64, i32, i32]
             for fn in ("fused_moe_fwd", "moe_route", "moe_align_sort", "moe_gemm1_swiglu",
@@ -590,3 +607,84 @@ def moe_gemm2_w4a16(act, sorted_ids, offsets, topk_weights, w_down, T, top_k, bl
                                  _p(w_down.alpha), _p(y), _p(workspace), workspace.numel(),
                                  _stream(stream)), "moe_gemm2_w4a16")
     return y[:cap]
+
+
+# ---------------------------------------------------------- expert-parallel building blocks
+def moe_pre_permute(hidden_states, local_ids, num_local_experts, workspace=None, stream=None):
+    """Rows of hidden_states in local-expert order (include/moe.h: moe_pre_permute).  Returns
+    dict(permuted [T*k, H], offsets [E+1], sorted_ids [T*k], inv_route [T*k])."""
+    T, H = hidden_states.shape
+    k = local_ids.shape[1]
+    E = int(num_local_experts)
+    dt = hidden_states.dtype
+    _need(hidden_states, "hidden_states", dt)
+    _need(local_ids, "local_ids", torch.int32, (T, k))
+    prob = make_problem(T, H, E, 8, k, dt)
+    dev = hidden_states.device
+    permuted = torch.empty((max(T * k, 1), H), dtype=dt, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    sorted_ids = torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)
+    inv = torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)
+    nbytes = workspace_size(prob)
+    if workspace is None:
+        workspace = _workspace(nbytes, dev)
+    _check(lib().moe_pre_permute(ctypes.byref(prob), _p(hidden_states), _p(local_ids),
+                                 _p(permuted), _p(offsets), _p(sorted_ids), _p(inv),
+                                 _p(workspace), workspace.numel(), _stream(stream)),
+           "moe_pre_permute")
+    return dict(permuted=permuted[:T * k], offsets=offsets, sorted_ids=sorted_ids[:T * k],
+                inv_route=inv[:T * k])
+
+
+def grouped_gemm_desc(a, b, activation="none", out_f32=False) -> GroupedGemm:
+    """The moe_grouped_gemm_t of a (masked [E, max_m, K] or contiguous [P, K]) and b."""
+    E = b.shape[0]
+    N = b.shape[1] // (2 if activation == "silu" else 1)
+    K = b.shape[2]
+    if activation not in ("none", "silu"):
+        raise ValueError(f"unsupported grouped-GEMM activation {activation}")
+    max_m = a.shape[1] if a.dim() == 3 else 0
+    rows = 0 if a.dim() == 3 else a.shape[0]
+    return GroupedGemm(E, N, K, max_m, rows, _DTYPES[a.dtype], 1 if activation == "silu" else 0,
+                       int(bool(out_f32)))
+
+
+def moe_grouped_gemm(a, b, layout_metadata, activation="none", out_f32=False, out=None,
+                     workspace=None, stream=None):
+    """Grouped GEMM (include/moe.h: moe_grouped_gemm).  a [E, max_m, K] with valid-row counts
+    (masked layout) or a [P, K] with inclusive prefix sums (contiguous layout); b [E, N, K], or
+    [E, 2N, K] with activation="silu" (silu_and_mul).  Returns out shaped like a with N cols."""
+    g = grouped_gemm_desc(a, b, activation, out_f32)
+    dt = a.dtype
+    _need(a, "a", dt)
+    _need(b, "b", dt)
+    _need(layout_metadata, "layout_metadata", torch.int32, (g.E,))
+    shape = tuple(a.shape[:-1]) + (g.N,)
+    odt = torch.float32 if out_f32 else dt
+    if out is None:
+        out = torch.zeros(shape, dtype=odt, device=a.device)
+    _need(out, "out", odt, shape)
+    nbytes = lib().moe_grouped_gemm_workspace_size(ctypes.byref(g))
+    if nbytes == 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, "moe_grouped_gemm_workspace_size")
+    if workspace is None:
+        workspace = _workspace(int(nbytes), a.device)
+    _check(lib().moe_grouped_gemm(ctypes.byref(g), _p(a), _p(b), _p(layout_metadata), _p(out),
+                                  _p(workspace), workspace.numel(), _stream(stream)),
+           "moe_grouped_gemm")
+    return out
+
+
+def moe_post_permute(rows, topk_weights, inv_route, stream=None):
+    """Weighted top-k combine (include/moe.h: moe_post_permute); returns out [T, H]."""
+    T, k = topk_weights.shape
+    H = rows.shape[1]
+    dt = rows.dtype
+    _need(rows, "rows", dt)
+    _need(topk_weights, "topk_weights", torch.float32, (T, k))
+    _need(inv_route, "inv_route", torch.int32)
+    prob = make_problem(T, H, k, 8, k, dt)
+    out = torch.empty((T, H), dtype=dt, device=rows.device)
+    _check(lib().moe_post_permute(ctypes.byref(prob), _p(rows), _p(topk_weights), _p(inv_route),
+                                  _p(out), _stream(stream)), "moe_post_permute")
+    return out

@@ -639,6 +639,105 @@ moe_status_t moe_shared_expert_fwd(const moe_problem_t* p, const void* hidden_st
                               status_word(workspace), (cudaStream_t)stream, false));
 }
 
+// ---- expert-parallel building blocks ------------------------------------------------------
+
+moe_status_t moe_pre_permute(const moe_problem_t* p, const void* hidden_states,
+                             const int32_t* local_ids, void* permuted, int32_t* offsets,
+                             int32_t* sorted_ids, int32_t* inv_route, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  moe_status_t st = check_problem(p);
+  if (st != MOE_OK) return st;
+  if (!workspace || !offsets || !sorted_ids || !inv_route) return MOE_ERR_INVALID_ARG;
+  if (p->T > 0 && (!hidden_states || !local_ids || !permuted)) return MOE_ERR_INVALID_ARG;
+  const moe_problem_t P = local_view(*p);
+  const Layout L = make_layout(*p, 1);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = (cudaStream_t)stream;
+  void* ws = workspace;
+  MOE_TRY(launch_align_sort(P, 1, local_ids, at<int32_t>(ws, L.counts), offsets, sorted_ids,
+                            L.cap, nullptr, inv_route, at<int32_t>(ws, L.chunk), status_word(ws),
+                            s, false));
+  if (p->T == 0) return MOE_OK;
+  return from_cuda(launch_permute(P.dtype, P.top_k, P.H, hidden_states, sorted_ids, offsets, P.E,
+                                  L.cap, permuted, s, true));
+}
+
+namespace {
+
+bool grouped_gemm_valid(const moe_grouped_gemm_t* g) {
+  if (!g || g->E < 1 || g->E > 1024 || g->N <= 0 || g->K <= 0 || g->max_m < 0) return false;
+  if (g->N % 8 != 0 || g->K % 8 != 0) return false;
+  if (g->dtype != MOE_BF16 && g->dtype != MOE_F16) return false;
+  if (g->activation != 0 && g->activation != 1) return false;
+  if (g->out_f32 && g->activation != 0) return false;
+  if (g->max_m == 0 && g->rows < 0) return false;
+  const int64_t rows = g->max_m > 0 ? (int64_t)g->E * g->max_m : g->rows;
+  return rows < ((int64_t)1 << 31);
+}
+
+int64_t grouped_gemm_rows(const moe_grouped_gemm_t* g) {
+  return g->max_m > 0 ? (int64_t)g->E * g->max_m : g->rows;
+}
+
+int64_t grouped_gemm_max_tiles(const moe_grouped_gemm_t* g) {
+  return grouped_gemm_rows(g) / kTileRows + g->E + 1;
+}
+
+}  // namespace
+
+size_t moe_grouped_gemm_workspace_size(const moe_grouped_gemm_t* g) {
+  if (!grouped_gemm_valid(g)) return 0;
+  return kHeaderBytes + align_up(sizeof(Tile) * (size_t)grouped_gemm_max_tiles(g), 256);
+}
+
+moe_status_t moe_grouped_gemm(const moe_grouped_gemm_t* g, const void* a, const void* b,
+                              const int32_t* layout_metadata, void* out, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (!grouped_gemm_valid(g)) return MOE_ERR_INVALID_ARG;
+  if (!workspace || !layout_metadata) return MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < moe_grouped_gemm_workspace_size(g)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const int64_t rows = grouped_gemm_rows(g);
+  if (rows == 0) return MOE_OK;
+  if (!a || !b || !out) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  void* ws = workspace;
+  Tile* tiles = at<Tile>(ws, kHeaderBytes);
+  MOE_TRY(launch_build_tiles_meta(g->E, g->max_m, rows, layout_metadata, tiles, tile_counter(ws),
+                                  kTileRows, status_word(ws), s, false));
+  GemmCall c{};
+  c.dtype = g->dtype;
+  c.status = status_word(ws);
+  c.E = g->E;
+  c.mode = kSorted;
+  c.K = g->K;
+  c.n_out = g->N;
+  c.w = b;
+  c.b = a;
+  c.b_rows = rows;
+  c.out = out;
+  c.tiles = tiles;
+  c.n_tiles = tile_counter(ws);
+  c.max_tiles = (int)grouped_gemm_max_tiles(g);
+  c.tile_rows = kTileRows;
+  if (g->out_f32) {
+    c.gemm1 = 0;  // f32 rows, scale 1 (no sorted_ids)
+  } else {
+    c.gemm1 = 1;
+    c.act = g->activation ? MOE_ACT_SILU : kActIdentity;
+  }
+  return from_cuda(launch_gemm(c, s, true));
+}
+
+moe_status_t moe_post_permute(const moe_problem_t* p, const void* rows,
+                              const float* topk_weights, const int32_t* inv_route, void* out,
+                              void* stream) {
+  moe_status_t st = check_problem(p);
+  if (st != MOE_OK) return st;
+  if (p->T > 0 && (!rows || !topk_weights || !inv_route || !out)) return MOE_ERR_INVALID_ARG;
+  return from_cuda(launch_post_permute(p->dtype, p->T, p->top_k, p->H, rows, topk_weights,
+                                       inv_route, out, (cudaStream_t)stream, false));
+}
+
 int64_t moe_nvfp4_packed_bytes(int64_t n_mats, int32_t rows, int32_t K) {
   if (n_mats < 0 || rows <= 0 || K <= 0 || rows % 128 != 0 || K % 128 != 0) return -1;
   return n_mats * (int64_t)rows * K / 2 + n_mats * (int64_t)rows * K / 16;

@@ -118,6 +118,18 @@ cudaError_t launch_permute(int dtype, int top_k, int H, const void* hidden,
                            const int32_t* sorted_ids, const int32_t* offsets, int E, int64_t cap,
                            void* a_sorted, cudaStream_t s, bool pdl);
 
+// Tile list over a grouped-GEMM layout (masked or prefix sums) and the weighted post-permute.
+cudaError_t launch_build_tiles_meta(int E, int max_m, int64_t rows, const int32_t* meta,
+                                    Tile* tiles, int* n_tiles, int tile_rows, int* status,
+                                    cudaStream_t s, bool pdl);
+cudaError_t launch_post_permute(int dtype, int T, int K, int H, const void* rows,
+                                const float* w, const int32_t* inv, void* out, cudaStream_t s,
+                                bool pdl);
+
+// Activation code of the single-projection GEMM that writes the product itself (the plain
+// grouped GEMM); not a moe_activation_t a caller can pass.
+constexpr int kActIdentity = 3;
+
 // NVFP4 weights -> the packed tile layout the W4A16 GEMMs read (nvfp4_pack.cu).
 cudaError_t launch_nvfp4_pack(int64_t n_mats, int rows, int K, const uint8_t* codes,
                               const uint8_t* scales, uint8_t* tiles, cudaStream_t s);

@@ -654,10 +654,15 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
                 }
               } else {
                 tmem_ld_x16(tb + (uint32_t)(half * kN) + c, h);
+                if (p.act == kActIdentity) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  const float r = fmaxf(h[j] * al, 0.0f);
-                  h[j] = r * r;
+                  for (int j = 0; j < 16; ++j) h[j] *= al;
+                } else {
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) {
+                    const float r = fmaxf(h[j] * al, 0.0f);
+                    h[j] = r * r;
+                  }
                 }
               }
 #pragma unroll
@@ -693,8 +698,12 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
           if (p.mode == kSorted) {
             if (i < U.nrows) {
               dst = U.row0 + i;
-              const int sid = p.sorted_ids[dst];
-              sc = sid >= 0 ? p.topk_w[sid] : 0.0f;
+              if (p.sorted_ids) {  // a route's row, scaled by its weight; padding rows give 0
+                const int sid = p.sorted_ids[dst];
+                sc = sid >= 0 ? p.topk_w[sid] : 0.0f;
+              } else {  // the plain grouped GEMM
+                sc = 1.0f;
+              }
             }
           } else if (p.mode == kDirect) {
             if (i < p.P && p.topk_ids[i] == U.e) {
@@ -823,9 +832,9 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   kp.token_rows = c.gemm1 && c.mode == kSorted && c.token_rows;
   if (c.token_rows && (!kp.token_rows || c.T > kTileRows || c.tile_rows != kTileRows))
     return cudaErrorInvalidValue;
-  if (c.gemm1 && (c.act < MOE_ACT_SILU || c.act > MOE_ACT_RELU2)) return cudaErrorInvalidValue;
+  if (c.gemm1 && (c.act < MOE_ACT_SILU || c.act > kActIdentity)) return cudaErrorInvalidValue;
   kp.act = c.act;
-  kp.gated = c.gemm1 && c.act != MOE_ACT_RELU2;
+  kp.gated = c.gemm1 && c.act != MOE_ACT_RELU2 && c.act != kActIdentity;
   kp.slab_rows = (c.gemm1 && !kp.gated) ? 2 * kSlab : kSlab;
   kp.second_off = kp.gated ? c.n_out : kSlab;
   kp.K = c.K;

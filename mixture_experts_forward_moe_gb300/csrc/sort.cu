@@ -217,6 +217,48 @@ __global__ void __launch_bounds__(1024)
   if (e == E - 1) *n_tiles = incl;
 }
 
+// Tiles of at most tile_rows rows over the groups of a grouped-GEMM layout (TileOPs "MoE" page,
+// op MoEGroupedGemmFwd): masked (max_m > 0) group e owns rows e*max_m .. + clamp(meta[e], 0,
+// max_m); contiguous (max_m == 0) meta holds the inclusive prefix sums of the groups' rows.  A
+// decreasing prefix sum or one past `rows` sets MOE_ERR_INVALID_ARG and drops the group.
+__global__ void __launch_bounds__(1024)
+    build_tiles_meta_kernel(int E, int max_m, int64_t rows, const int32_t* __restrict__ meta,
+                            Tile* __restrict__ tiles, int* __restrict__ n_tiles, int tile_rows,
+                            int* __restrict__ status) {
+  __shared__ int warp_tot[32];
+  pdl_wait();
+  pdl_trigger();
+  const int e = threadIdx.x;
+  int r0 = 0, seg = 0;
+  if (e < E) {
+    if (max_m > 0) {
+      r0 = e * max_m;
+      seg = min(max(meta[e], 0), max_m);
+    } else {
+      r0 = e == 0 ? 0 : meta[e - 1];
+      seg = meta[e] - r0;
+      if (r0 < 0 || seg < 0 || (int64_t)meta[e] > rows) {
+        set_status(status, MOE_ERR_INVALID_ARG);
+        seg = 0;
+      }
+    }
+  }
+  const int nt = (seg + tile_rows - 1) / tile_rows;
+  const int incl = block_inclusive_scan(nt, warp_tot);
+  const int base = incl - nt;
+  for (int i = 0; i < nt; ++i) {
+    Tile t;
+    t.e = e;
+    t.row0 = r0 + i * tile_rows;
+    t.nrows = min(tile_rows, seg - i * tile_rows);
+    t.first = base;
+    t.count = nt;
+    t.pad0 = t.pad1 = t.pad2 = 0;
+    tiles[base + i] = t;
+  }
+  if (e == E - 1) *n_tiles = incl;
+}
+
 // The whole sort in one CTA of 1024 threads (32 warps), for up to kFusedSortMaxRoutes routes
 // (beyond that the chunked kernels, which spread the ranking over many CTAs, are faster):
 // warp w owns the contiguous routes [w*per, (w+1)*per).  Pass A counts each warp's routes per
@@ -406,7 +448,55 @@ __global__ void __launch_bounds__(128)
   *reinterpret_cast<uint2*>(out + (int64_t)t * H + 4 * v) = *reinterpret_cast<const uint2*>(o);
 }
 
+// out[t, :] = round( sum_j w[t, j] * rows[inv[t*K + j], :] ), f32 in fixed j order (TileOPs
+// "MoE" page, op MoEPostPermuteFwd), 8 columns per thread; routes with inv = -1 are skipped.
+template <typename T>
+__global__ void __launch_bounds__(128)
+    post_permute_kernel(int K, int H, const T* __restrict__ rows, const float* __restrict__ w,
+                        const int32_t* __restrict__ inv, T* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.y;
+  const int v = blockIdx.x * blockDim.x + threadIdx.x;  // 8 columns per thread
+  if (v >= H / 8) return;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < K; ++j) {
+    const int r = t * K + j;
+    const int p = inv[r];
+    if (p < 0) continue;
+    const float wj = w[r];
+    const uint4 raw = reinterpret_cast<const uint4*>(rows + (int64_t)p * H)[v];
+    const T* x = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[c] = fmaf(wj, DT<T>::to_f(x[c]), acc[c]);
+  }
+  T o[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) o[c] = DT<T>::from_f(acc[c]);
+  reinterpret_cast<uint4*>(out + (int64_t)t * H)[v] = *reinterpret_cast<const uint4*>(o);
+}
+
 }  // namespace
+
+cudaError_t launch_build_tiles_meta(int E, int max_m, int64_t rows, const int32_t* meta,
+                                    Tile* tiles, int* n_tiles, int tile_rows, int* status,
+                                    cudaStream_t s, bool pdl) {
+  return launch_k(build_tiles_meta_kernel, dim3(1), dim3(1024), 0, s, pdl, E, max_m, rows, meta,
+                  tiles, n_tiles, tile_rows, status);
+}
+
+cudaError_t launch_post_permute(int dtype, int T, int K, int H, const void* rows,
+                                const float* w, const int32_t* inv, void* out, cudaStream_t s,
+                                bool pdl) {
+  if (T == 0) return cudaSuccess;
+  const dim3 grid((H / 8 + 127) / 128, T);
+  if (dtype == MOE_BF16)
+    return launch_k(post_permute_kernel<__nv_bfloat16>, grid, dim3(128), 0, s, pdl, K, H,
+                    static_cast<const __nv_bfloat16*>(rows), w, inv,
+                    static_cast<__nv_bfloat16*>(out));
+  return launch_k(post_permute_kernel<__half>, grid, dim3(128), 0, s, pdl, K, H,
+                  static_cast<const __half*>(rows), w, inv, static_cast<__half*>(out));
+}
 
 bool fused_sort_fits(const moe_problem_t& p) {
   return (int64_t)p.T * p.top_k <= kFusedSortMaxRoutes && p.E <= 1024;

@@ -275,3 +275,43 @@ def random_weights(n: int, seed: int, device="cpu") -> torch.Tensor:
     gen = torch.Generator(device="cpu")
     gen.manual_seed(seed)
     return torch.rand((n,), generator=gen, dtype=torch.float32).to(device)
+
+
+# --------------------------------------------------------------------------- grouped GEMM
+@dataclasses.dataclass(frozen=True)
+class GroupedGemmWorkload:
+    """A masked-layout grouped GEMM (TileOPs MoE page, op MoEGroupedGemmFwd): a [E, max_m, K],
+    b [E, N, K], and the valid rows of each group drawn uniformly in [m_lo, m_hi]."""
+    name: str
+    E: int
+    max_m: int
+    K: int
+    N: int
+    m_lo: int
+    m_hi: int
+    dtype: torch.dtype = torch.bfloat16
+
+    def flops(self, valid_rows: int) -> float:
+        return 2.0 * valid_rows * self.N * self.K
+
+
+# The page's "ds-v3-ep8-masked" workload: 32 local experts, up to 128 rows each, the DeepSeek-V3
+# gate/up weights [4096, 7168].  Its printed 372 TFLOP/s at 0.4851 ms implies 96 valid rows per
+# group on average, the mean of the uniform draw in [64, 128] used here.
+GROUPED_GEMM_WORKLOADS = {
+    "ds-v3-ep8-masked": GroupedGemmWorkload("ds-v3-ep8-masked", E=32, max_m=128, K=7168,
+                                            N=4096, m_lo=64, m_hi=128),
+}
+
+
+def generate_grouped_gemm(w: GroupedGemmWorkload, seed: int = 0, device="cuda") -> dict:
+    """a ~ N(0, 1), b ~ N(0, 1/K) (one generator seeded with `seed`, in that order) and the
+    valid-row counts (a CPU generator seeded with seed + 1)."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    a = _randn((w.E, w.max_m, w.K), gen, device, 1.0, w.dtype)
+    b = _randn((w.E, w.N, w.K), gen, device, 1.0 / math.sqrt(w.K), w.dtype)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed + 1)
+    meta = torch.randint(w.m_lo, w.m_hi + 1, (w.E,), generator=g, dtype=torch.int32)
+    return {"a": a, "b": b, "meta": meta.to(device)}
