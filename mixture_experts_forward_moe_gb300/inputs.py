@@ -315,3 +315,84 @@ def generate_grouped_gemm(w: GroupedGemmWorkload, seed: int = 0, device="cuda") 
     g.manual_seed(seed + 1)
     meta = torch.randint(w.m_lo, w.m_hi + 1, (w.E,), generator=g, dtype=torch.int32)
     return {"a": a, "b": b, "meta": meta.to(device)}
+
+
+# -------------------------------------------------------------- FP8 block-scaled grouped GEMM
+@dataclasses.dataclass(frozen=True)
+class Fp8GemmWorkload:
+    """A masked-layout FP8 grouped GEMM (TileOPs MoE page, op MoEGroupedGemmFP8Fwd): a
+    [E, max_m, K] and b [E, N, K] in E4M3 with f32 scales per 128-k block of a row of a and per
+    128 x 128 block of b; `total` valid rows spread over the groups (the page's "T")."""
+    name: str
+    E: int
+    max_m: int
+    K: int
+    N: int
+    total: int
+
+    def flops(self, valid_rows: int) -> float:
+        return 2.0 * valid_rows * self.N * self.K
+
+
+def _fp8_table():
+    out = {}
+    shapes = {"ds-v3": (7168, 4096, 2048), "qwen3-235b": (4096, 3072, 1536),
+              "kimi-k2": (7168, 4096, 2048)}
+    experts = {"ds-v3": 32, "qwen3-235b": 16, "kimi-k2": 48}
+    rows = [("ds-v3-e8", 8, 128, 768)]
+    for model in ("ds-v3", "qwen3-235b", "kimi-k2"):
+        for b_, t in ((64, 64), (256, 256)):
+            rows.append((f"{model}-dec-b{b_}", experts[model], b_, t))
+    for prefix, E, max_m, T in rows:
+        model = prefix.split("-dec")[0].replace("-e8", "")
+        H, up_n, F = shapes[model]
+        suffix = "-masked" if prefix == "ds-v3-e8" else ""
+        out[f"{prefix}-up{suffix}"] = Fp8GemmWorkload(f"{prefix}-up{suffix}", E, max_m, H,
+                                                      up_n, T)
+        out[f"{prefix}-down{suffix}"] = Fp8GemmWorkload(f"{prefix}-down{suffix}", E, max_m, F,
+                                                        H, T)
+    return out
+
+
+# The page's 14 MoEGroupedGemmFP8Fwd workloads (a [E, max_m, K], b [E, N, K], T valid rows).
+FP8_GEMM_WORKLOADS = _fp8_table()
+
+
+def quantize_fp8_blocks(x: torch.Tensor, block_rows: int):
+    """x [rows, K] f32 -> (E4M3 bytes [rows, K], f32 scales [ceil(rows/block_rows), K/128]):
+    one scale per block of block_rows x 128, amax / 448 (1 for an all-zero block), values
+    rounded to nearest even by torch's float8_e4m3fn conversion."""
+    rows, K = x.shape
+    nb = (rows + block_rows - 1) // block_rows
+    pad = nb * block_rows - rows
+    xp = torch.nn.functional.pad(x, (0, 0, 0, pad)) if pad else x
+    blocks = xp.view(nb, block_rows, K // 128, 128)
+    amax = blocks.abs().amax(dim=(1, 3))  # [nb, K/128]
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    q = (blocks / scale[:, None, :, None]).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn)
+    q = q.view(nb * block_rows, K)[:rows]
+    return q.view(torch.uint8).contiguous(), scale.contiguous()
+
+
+def generate_fp8_gemm(w: Fp8GemmWorkload, seed: int = 0, device="cuda") -> dict:
+    """a ~ N(0, 1) and b ~ N(0, 1/K) (one generator seeded with `seed`, a first), quantised
+    to E4M3 with per-(row, 128-k) scales for a and per-(128 x 128) scales for b; the valid rows
+    of each group are `total` draws of a uniformly random group (a CPU generator seeded with
+    seed + 1), each count capped at max_m."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    a32 = _randn((w.E * w.max_m, w.K), gen, device, 1.0, torch.float32)
+    a, a_scale = quantize_fp8_blocks(a32, 1)
+    del a32
+    b = torch.empty((w.E, w.N, w.K), dtype=torch.uint8, device=device)
+    b_scale = torch.empty((w.E, w.N // 128, w.K // 128), dtype=torch.float32, device=device)
+    for e in range(w.E):
+        x = _randn((w.N, w.K), gen, device, 1.0 / math.sqrt(w.K), torch.float32)
+        b[e], b_scale[e] = quantize_fp8_blocks(x, 128)
+        del x
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed + 1)
+    pick = torch.randint(0, w.E, (w.total,), generator=g)
+    meta = torch.bincount(pick, minlength=w.E).clamp_(max=w.max_m).to(torch.int32)
+    return {"a": a.view(w.E, w.max_m, w.K), "a_scale": a_scale.view(w.E, w.max_m, w.K // 128),
+            "b": b, "b_scale": b_scale, "meta": meta.to(device)}

@@ -79,6 +79,7 @@ def _load():
             _lib.oracle_combine.argtypes = [i32, i32, i32, i32, P, P, P, P]
             _lib.oracle_num_threads.restype = i32
             _lib.oracle_grouped_gemm.argtypes = [i32, i32, i32, i32, i64, i32, i32, P, P, P, P]
+            _lib.oracle_grouped_gemm_fp8.argtypes = [i32, i32, i32, i32, i64, P, P, P, P, P, P]
             _lib.oracle_post_permute.argtypes = [i32, i32, i32, i32, P, P, P, P]
             _lib.oracle_e2m1_to_double.restype = f64
             _lib.oracle_e2m1_to_double.argtypes = [i32]
@@ -362,4 +363,23 @@ def post_permute(rows, weights, inv, top_k, dtype):
     out = np.empty((T, H), np.float64)
     _check(_load().oracle_post_permute(T, H, top_k, dtype, _ptr(rb), _ptr(wv), _ptr(iv),
                                        _ptr(out)), "oracle_post_permute")
+    return out
+
+
+def grouped_gemm_fp8(a, a_scale, b, b_scale, meta, max_m=0):
+    """fp64 FP8 block-scaled grouped GEMM (oracle_grouped_gemm_fp8).  a [E, max_m, K] (masked,
+    max_m > 0) or [P, K] E4M3 bytes, a_scale [.., K/128] f32, b [E, N, K] E4M3 bytes, b_scale
+    [E, N/128, K/128] f32.  Returns out [rows, N]."""
+    ab = _u8(a)
+    K = ab.shape[-1]
+    ab = ab.reshape(-1, K)
+    asv = _f32(a_scale).reshape(ab.shape[0], -1)
+    bb = _u8(b)
+    E, N, _ = bb.shape
+    bsv = _f32(b_scale)
+    mv = _c(meta, np.int32)
+    out = np.empty((ab.shape[0], N), np.float64)
+    _check(_load().oracle_grouped_gemm_fp8(E, N, K, int(max_m), ab.shape[0], _ptr(ab),
+                                           _ptr(asv), _ptr(bb), _ptr(bsv), _ptr(mv), _ptr(out)),
+           "oracle_grouped_gemm_fp8")
     return out

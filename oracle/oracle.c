@@ -17,6 +17,8 @@
  *   - flashinfer PR #4048 (CuTe DSL W4A16 MoE) and its weight-scale placement ablation: NVFP4
  *     experts, E2M1 codes with E4M3 block scales over 16 elements and an FP32 per-expert scale
  *     (oracle_moe_tokens_w4 and the stage references after it).
+ *   - The same page's op MoEGroupedGemmFP8Fwd: E4M3 operands with f32 scales per 128-k block of
+ *     a row and per 128 x 128 block of weights (oracle_grouped_gemm_fp8).
  *   - The same page's op MoEGroupedGemmFwd in its contiguous and masked layouts
  *     (oracle_grouped_gemm) and op MoEPostPermuteFwd with route weights (oracle_post_permute).
  *   - ROCm/aiter PR #5973 "[FlyDSL] Optimize MI308 MoE decoding (3/3)", section "Changes":
@@ -810,6 +812,56 @@ int oracle_post_permute(int T, int H, int top_k, int dtype, const uint16_t* rows
     }
   }
   return ORACLE_OK;
+}
+
+/*
+ * oracle_grouped_gemm_fp8 (TileOPs "MoE" page, op MoEGroupedGemmFP8Fwd): the grouped GEMM of
+ * E4M3 operands with f32 block scales, masked (max_m > 0) or contiguous (max_m == 0) layout as
+ * in oracle_grouped_gemm:
+ *   out[r, n] = sum_kb a_scale[r, kb] * b_scale[e, n/128, kb]
+ *                      * sum_{k in block kb} e4m3(a[r, k]) * e4m3(b[e, n, k])
+ * with k blocks of 128; a [rows, K] and b [E, N, K] are E4M3 bytes, a_scale [rows, ceil(K/128)]
+ * and b_scale [E, ceil(N/128), ceil(K/128)] f32.
+ */
+int oracle_grouped_gemm_fp8(int E, int N, int K, int max_m, int64_t rows, const uint8_t* a,
+                            const float* a_scale, const uint8_t* b, const float* b_scale,
+                            const int32_t* meta, double* out) {
+  if (E <= 0 || N <= 0 || K <= 0 || max_m < 0 || rows < 0) return ORACLE_ERR_ARG;
+  fp_tables();
+  const int kbs = (K + 127) / 128, nbs = (N + 127) / 128;
+  for (int64_t i = 0; i < rows * N; ++i) out[i] = 0.0;
+  int bad = 0;
+  for (int e = 0; e < E; ++e) {
+    int64_t r0, r1;
+    if (max_m > 0) {
+      int m = meta[e] < 0 ? 0 : (meta[e] > max_m ? max_m : meta[e]);
+      r0 = (int64_t)e * max_m;
+      r1 = r0 + m;
+    } else {
+      r0 = e == 0 ? 0 : meta[e - 1];
+      r1 = meta[e];
+    }
+    if (r0 < 0 || r1 < r0 || r1 > rows) {
+      bad = 1;
+      continue;
+    }
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t r = r0; r < r1; ++r) {
+      for (int n = 0; n < N; ++n) {
+        const uint8_t* br = b + ((int64_t)e * N + n) * K;
+        double acc = 0.0;
+        for (int kb = 0; kb < kbs; ++kb) {
+          double part = 0.0;
+          for (int k = kb * 128; k < K && k < kb * 128 + 128; ++k)
+            part += g_e4m3[a[r * K + k]] * g_e4m3[br[k]];
+          acc += (double)a_scale[r * kbs + kb] *
+                 (double)b_scale[((int64_t)e * nbs + n / 128) * kbs + kb] * part;
+        }
+        out[r * N + n] = acc;
+      }
+    }
+  }
+  return bad ? ORACLE_ERR_ARG : ORACLE_OK;
 }
 
 int oracle_num_threads(void) {

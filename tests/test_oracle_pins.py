@@ -560,6 +560,46 @@ def test_post_permute_is_a_weighted_gather_sum():
     np.testing.assert_allclose(out, ref, rtol=1e-13, atol=1e-14)
 
 
+def _e4m3(u8):
+    return torch.from_numpy(np.ascontiguousarray(u8)).view(torch.float8_e4m3fn).double().numpy()
+
+
+@pytest.mark.parametrize("masked", [True, False])
+def test_fp8_grouped_gemm_is_a_matmul_of_the_dequantised_blocks(masked):
+    # Dequantise with torch's E4M3 decoder and the block scales, then numpy matmuls per group.
+    w = inputs.Fp8GemmWorkload("t", E=3, max_m=20, K=256, N=256, total=30)
+    d = inputs.generate_fp8_gemm(w, seed=2, device="cpu")
+    a = d["a"].reshape(-1, w.K).numpy()
+    sa = d["a_scale"].reshape(-1, w.K // 128).numpy().astype(np.float64)
+    A = _e4m3(a) * np.repeat(sa, 128, axis=1)
+    meta = d["meta"].numpy()
+    if masked:
+        out = oracle.grouped_gemm_fp8(d["a"], d["a_scale"], d["b"], d["b_scale"], meta,
+                                      max_m=w.max_m)
+        starts = np.arange(w.E) * w.max_m
+        ends = starts + meta
+    else:
+        ends = np.cumsum(meta).astype(np.int32)
+        starts = np.concatenate([[0], ends[:-1]])
+        rows = int(ends[-1])
+        out = oracle.grouped_gemm_fp8(d["a"].reshape(-1, w.K)[:rows], d["a_scale"].reshape(
+            -1, w.K // 128)[:rows], d["b"], d["b_scale"], ends)
+    for e in range(w.E):
+        Bm = _e4m3(d["b"][e].numpy()) * np.repeat(np.repeat(
+            d["b_scale"][e].numpy().astype(np.float64), 128, axis=0), 128, axis=1)
+        src = A[starts[e]:ends[e]] if masked else A[starts[e]:ends[e]]
+        np.testing.assert_allclose(out[starts[e]:ends[e]], src @ Bm.T, rtol=1e-10, atol=1e-12)
+    assert np.sum(meta) == 30 and np.all(meta <= w.max_m)
+
+
+def test_fp8_block_quantisation_round_trips_within_e4m3_precision():
+    x = torch.randn(64, 256, generator=torch.Generator().manual_seed(0))
+    q, sc = inputs.quantize_fp8_blocks(x, 1)
+    back = _e4m3(q.numpy()) * np.repeat(sc.numpy().astype(np.float64), 128, axis=1)
+    err = np.abs(back - x.double().numpy())
+    assert np.all(err <= 2.0 ** -4 * np.repeat(sc.numpy() * 448.0, 128, axis=1) + 1e-12)
+
+
 # ------------------------------------------------------------------------- skewed routing
 def test_skew_bias_is_minus_alpha_log1p_of_a_ranking():
     b = inputs.skew_bias(16, 0.1, seed=0).double().numpy()
