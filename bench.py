@@ -563,7 +563,15 @@ def run_reference(args, w):
 
 
 # ----------------------------------------------------------- grouped GEMM (masked layout) arm
-PUBLISHED_GROUPED_MS = {"ds-v3-ep8-masked": 0.4851}  # TileOPs MoE page (hardware not stated)
+PUBLISHED_GROUPED_MS = {  # TileOPs MoE page, MoEGroupedGemmFwd / MoEGroupedGemmFP8Fwd (hardware
+    "ds-v3-ep8-masked": 0.4851,  # not stated)
+    "ds-v3-e8-up-masked": 0.0743, "ds-v3-e8-down-masked": 0.0424, "ds-v3-dec-b64-up": 0.2266,
+    "ds-v3-dec-b64-down": 0.1157, "ds-v3-dec-b256-up": 0.2420, "ds-v3-dec-b256-down": 0.1309,
+    "qwen3-235b-dec-b64-up": 0.0598, "qwen3-235b-dec-b64-down": 0.0351,
+    "qwen3-235b-dec-b256-up": 0.0605, "qwen3-235b-dec-b256-down": 0.0358,
+    "kimi-k2-dec-b64-up": 0.2638, "kimi-k2-dec-b64-down": 0.1430, "kimi-k2-dec-b256-up": 0.3545,
+    "kimi-k2-dec-b256-down": 0.1892,
+}
 
 
 def run_grouped_gemm(args, w, ws_n, rank, local):
@@ -578,16 +586,22 @@ def run_grouped_gemm(args, w, ws_n, rank, local):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    d = inputs.generate_grouped_gemm(w, seed=args.seed, device=dev)
+    fp8 = isinstance(w, inputs.Fp8GemmWorkload)
+    d = (inputs.generate_fp8_gemm if fp8 else inputs.generate_grouped_gemm)(w, seed=args.seed,
+                                                                           device=dev)
     a, b, meta = d["a"], d["b"], d["meta"]
-    out = torch.zeros((w.E, w.max_m, w.N), dtype=w.dtype, device=dev)
-    g = B.grouped_gemm_desc(a, b)
+    out = torch.zeros((w.E, w.max_m, w.N), dtype=torch.bfloat16, device=dev)
+    g = B.GroupedGemm(w.E, w.N, w.K, w.max_m, 0, B.MOE_BF16, 0, 0)
     wsp = B.new_workspace(B.lib().moe_grouped_gemm_workspace_size(B.ctypes.byref(g)), dev)
     stream = torch.cuda.current_stream()
     valid = int(meta.sum())
 
     def step():
-        B.moe_grouped_gemm(a, b, meta, out=out, workspace=wsp)
+        if fp8:
+            B.moe_grouped_gemm_fp8(a, d["a_scale"], b, d["b_scale"], meta, out=out,
+                                   workspace=wsp)
+        else:
+            B.moe_grouped_gemm(a, b, meta, out=out, workspace=wsp)
 
     for _ in range(args.warmup):
         step()
@@ -626,24 +640,42 @@ def run_grouped_gemm(args, w, ws_n, rank, local):
     flops = w.flops(valid)
     value = job_throughput(flops, ws_n, args.steps, max_ms) / 1e12
     hbm_gbs, bf16_peak, bf16_sust, peak_src = measured_peaks()
-    eb = 2
-    ab = w.E * w.N * w.K * eb + valid * w.K * eb + valid * w.N * eb  # weights + valid rows in/out
+    eb = 1 if fp8 else 2  # bytes per element of a and b
+    # weights (+ their block scales) + the valid rows in (+ scales) and out (bf16)
+    ab = (w.E * w.N * w.K * eb + valid * w.K * eb + valid * w.N * 2 +
+          ((w.E * (w.N // 128) * (w.K // 128) + valid * (w.K // 128)) * 4 if fp8 else 0))
     achieved = ab / (ms * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": "moe_gemm_kernel (grouped, masked layout)",
+    # FP8 tensor peak: the measured bf16 peak times the nominal fp8/bf16 ratio (4.5 / 2.25)
+    tpeak = bf16_sust * (2.0 if fp8 else 1.0)
+    roofline = {"bound": "hbm", "kernel": ("moe_gemm_fp8_kernel" if fp8 else "moe_gemm_kernel")
+                + " (grouped, masked layout)",
                 "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s", "frac": achieved / hbm_gbs,
                 "traffic": None, "algorithmic_bytes": ab, "avg_launch_ms": ms,
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
                 "timing": "event pair around each call (one graph replay: tile list + GEMM)",
                 "tensor": {"achieved_tflops": flops / (ms * 1e-3) / 1e12,
-                           "peak_tflops": bf16_sust,
-                           "frac": flops / (ms * 1e-3) / 1e12 / bf16_sust}}
+                           "peak_tflops": tpeak,
+                           "peak_source": "bf16_tflops_sustained" + (" x 2 (fp8 nominal ratio)"
+                                                                    if fp8 else ""),
+                           "frac": flops / (ms * 1e-3) / 1e12 / tpeak}}
+    if flops / (tpeak * 1e12) > ab / (hbm_gbs * 1e9):  # tensor-bound by the algorithmic work
+        hbm_part = dict(roofline)
+        roofline = {"bound": "tensor", "kernel": hbm_part["kernel"],
+                    "achieved": flops / (ms * 1e-3) / 1e12, "peak": tpeak, "unit": "TFLOP/s",
+                    "frac": flops / (ms * 1e-3) / 1e12 / tpeak, "traffic": None,
+                    "algorithmic_flops": flops, "avg_launch_ms": ms, "hbm": hbm_part}
     res = {
-        "metric": "moe_grouped_gemm device ms, TFLOP/s & HBM GB/s (masked layout)",
+        "metric": ("moe_grouped_gemm_fp8" if fp8 else "moe_grouped_gemm")
+                  + " device ms, TFLOP/s & HBM GB/s (masked layout)",
         "value": value, "unit": "TFLOP/s", "n_gpus": ws_n, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic: N(0,1) a, N(0,1/K) b, valid "
-        f"rows per group uniform in [{w.m_lo}, {w.m_hi}]",
+        "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
+        "data": ("synthetic: N(0,1) a and N(0,1/K) b quantised to E4M3 with block scales, "
+                 f"{w.total} valid rows spread uniformly over the groups" if fp8 else
+                 "synthetic: N(0,1) a, N(0,1/K) b, valid rows per group uniform in "
+                 f"[{w.m_lo}, {w.m_hi}]"),
         "config": {"workload": w.name, "E": w.E, "max_m": w.max_m, "K": w.K, "N": w.N,
+                   "weights": "e4m3 with 128x128 f32 block scales" if fp8 else "bf16",
                    "valid_rows": valid, "global_batch": valid * ws_n,
                    "parallelism": f"replicas x{ws_n}",
                    "l2": f"no flush: each call streams {w.E * w.N * w.K * eb / 1e9:.2f} GB of "
@@ -654,7 +686,7 @@ def run_grouped_gemm(args, w, ws_n, rank, local):
                                  "where": "TileOPs MoE page, MoEGroupedGemmFwd (hardware not "
                                           "stated)"},
     }
-    if not args.no_e2e:
+    if not args.no_e2e and not fp8:
         h_a = a.cpu().pin_memory()
         h_meta = meta.cpu().pin_memory()
         h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
@@ -674,7 +706,48 @@ def run_grouped_gemm(args, w, ws_n, rank, local):
         res["e2e"] = {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                       "h2d_bytes_per_step": h_a.numel() * 2 + h_meta.numel() * 4,
                       "d2h_bytes_per_step": h_out.numel() * 2, "ms_per_step": e2e_ms}
-    if not args.no_cpu_baseline and rank == 0:
+    if not args.no_e2e and fp8:
+        h_a = a.cpu().pin_memory()
+        h_sa = d["a_scale"].cpu().pin_memory()
+        h_meta = meta.cpu().pin_memory()
+        h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        a_dev, sa_dev, meta_dev = torch.empty_like(a), torch.empty_like(d["a_scale"]), \
+            torch.empty_like(meta)
+        n_e2e = max(1, min(args.steps, 50))
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_e2e)]
+        torch.cuda.synchronize()
+        for i in range(n_e2e):
+            es[2 * i].record(stream)
+            a_dev.copy_(h_a, non_blocking=True)
+            sa_dev.copy_(h_sa, non_blocking=True)
+            meta_dev.copy_(h_meta, non_blocking=True)
+            B.moe_grouped_gemm_fp8(a_dev, sa_dev, b, d["b_scale"], meta_dev, out=out,
+                                   workspace=wsp)
+            h_out.copy_(out, non_blocking=True)
+            es[2 * i + 1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = statistics.mean(es[2 * i].elapsed_time(es[2 * i + 1]) for i in range(n_e2e))
+        res["e2e"] = {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                      "h2d_bytes_per_step": h_a.numel() + h_sa.numel() * 4 + h_meta.numel() * 4,
+                      "d2h_bytes_per_step": h_out.numel() * 2, "ms_per_step": e2e_ms}
+    if not args.no_cpu_baseline and rank == 0 and fp8:
+        rows = np.arange(w.E) * w.max_m
+        idx = torch.from_numpy(rows).to(dev)
+        a_s = a.reshape(w.E * w.max_m, w.K)[idx].cpu()
+        sa_s = d["a_scale"].reshape(w.E * w.max_m, w.K // 128)[idx].cpu()
+        b_c, bs_c = b.cpu(), d["b_scale"].cpu()
+        t0, passes = time.perf_counter(), 0
+        while time.perf_counter() - t0 < args.cpu_budget and passes < 1000:
+            for e in range(w.E):
+                oracle.grouped_gemm_fp8(a_s[e:e + 1], sa_s[e:e + 1], b_c[e:e + 1],
+                                        bs_c[e:e + 1], np.array([1], np.int32))
+            passes += 1
+        el = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": w.flops(w.E) * passes / el / 1e12, "unit": "TFLOP/s",
+                               "cores": oracle.num_threads(), "kind": "oracle",
+                               "sample": f"1 row per group ({w.E} rows) per pass, {passes} "
+                                         f"passes in {el:.1f} s"}
+    if not args.no_cpu_baseline and rank == 0 and not fp8:
         # the oracle on one sampled row per group, timed for about cpu_budget seconds
         rows = np.arange(w.E) * w.max_m
         a_s = a.reshape(w.E * w.max_m, w.K)[torch.from_numpy(rows).to(dev)].cpu()
@@ -714,8 +787,10 @@ def main(argv=None):
     import torch
 
     from mixture_experts_forward_moe_gb300 import inputs
-    if args.workload in inputs.GROUPED_GEMM_WORKLOADS:
-        gw = inputs.GROUPED_GEMM_WORKLOADS[args.workload]
+    if args.workload in inputs.GROUPED_GEMM_WORKLOADS or \
+            args.workload in inputs.FP8_GEMM_WORKLOADS:
+        gw = inputs.GROUPED_GEMM_WORKLOADS.get(args.workload) or \
+            inputs.FP8_GEMM_WORKLOADS[args.workload]
         ws_n, rank, local = dist_env()
         if args.impl == "reference":
             if rank == 0:

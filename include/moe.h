@@ -379,6 +379,23 @@ moe_status_t moe_grouped_gemm(const moe_grouped_gemm_t* g, const void* a, const 
                               size_t workspace_bytes, void* stream);
 
 /*
+ * moe_grouped_gemm_fp8 -- op MoEGroupedGemmFP8Fwd: the grouped GEMM of E4M3 operands with f32
+ * block scales, on the tcgen05 tensor cores (kind::f8f6f4):
+ *   out[r, n] = sum_kb a_scale[r, kb] * b_scale[e, n/128, kb]
+ *                      * sum_{k in block kb} e4m3(a[r, k]) * e4m3(b[e, n, k])
+ * with 128-k blocks, f32 accumulation and one rounding to bf16.  Layouts and layout_metadata as
+ * for moe_grouped_gemm (masked or contiguous); a is [E, max_m, K] or [rows, K] E4M3 bytes,
+ * a_scale [.., K/128] f32 (one per row and 128-k block), b [E, N, K] E4M3 bytes, b_scale
+ * [E, N/128, K/128] f32 (one per 128 x 128 block), out bf16 [.., N].  g->dtype must be MOE_BF16
+ * (the output type), activation 0, out_f32 0; N and K multiples of 128 (MOE_ERR_UNSUPPORTED).
+ * workspace: moe_grouped_gemm_workspace_size(g) bytes.
+ */
+moe_status_t moe_grouped_gemm_fp8(const moe_grouped_gemm_t* g, const uint8_t* a,
+                                  const float* a_scale, const uint8_t* b, const float* b_scale,
+                                  const int32_t* layout_metadata, void* out, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/*
  * moe_post_permute -- op MoEPostPermuteFwd: the weighted top-k combine
  *   out[t, :] = round( sum_{j=0..k-1} topk_weights[t*k+j] * rows[inv_route[t*k+j], :] )
  * summed in f32 in fixed j order (deterministic), rounded once to dtype; routes with

@@ -40,6 +40,7 @@ EXPORTED = (
     "moe_profile_collect", "moe_align_sort_noalloc", "fused_moe_fwd_w4a16", "moe_gemm1_w4a16",
     "moe_gemm2_w4a16", "moe_nvfp4_pack", "moe_nvfp4_packed_bytes", "moe_pre_permute",
     "moe_grouped_gemm_workspace_size", "moe_grouped_gemm", "moe_post_permute",
+    "moe_grouped_gemm_fp8",
 )
 
 
@@ -125,6 +126,8 @@ def lib():
             L.moe_grouped_gemm_workspace_size.argtypes = [GG]
             L.moe_grouped_gemm.argtypes = [GG, P, P, P, P, P, sz, P]
             L.moe_post_permute.argtypes = [PP, P, P, P, P, P]
+            L.moe_grouped_gemm_fp8.argtypes = [GG, P, P, P, P, P, P, P, sz, P]
+            L.moe_grouped_gemm_fp8.restype = ctypes.c_int
             for fn in ("moe_pre_permute", "moe_grouped_gemm", "moe_post_permute"):
                 getattr(L, fn).restype = ctypes.c_int
             L.moe_nvfp4_packed_bytes.restype = i64
@@ -687,4 +690,34 @@ def moe_post_permute(rows, topk_weights, inv_route, stream=None):
     out = torch.empty((T, H), dtype=dt, device=rows.device)
     _check(lib().moe_post_permute(ctypes.byref(prob), _p(rows), _p(topk_weights), _p(inv_route),
                                   _p(out), _stream(stream)), "moe_post_permute")
+    return out
+
+
+def moe_grouped_gemm_fp8(a, a_scale, b, b_scale, layout_metadata, out=None, workspace=None,
+                         stream=None):
+    """FP8 block-scaled grouped GEMM (include/moe.h: moe_grouped_gemm_fp8).  a: E4M3 bytes
+    [E, max_m, K] (masked) or [rows, K] (contiguous), a_scale [.., K/128] f32, b [E, N, K] E4M3
+    bytes, b_scale [E, N/128, K/128] f32.  Returns bf16 out shaped like a with N columns."""
+    E, N, K = b.shape
+    max_m = a.shape[1] if a.dim() == 3 else 0
+    rows = 0 if a.dim() == 3 else a.shape[0]
+    g = GroupedGemm(E, N, K, max_m, rows, MOE_BF16, 0, 0)
+    _need(a, "a", torch.uint8)
+    _need(a_scale, "a_scale", torch.float32, tuple(a.shape[:-1]) + (K // 128,))
+    _need(b, "b", torch.uint8)
+    _need(b_scale, "b_scale", torch.float32, (E, N // 128, K // 128))
+    _need(layout_metadata, "layout_metadata", torch.int32, (E,))
+    shape = tuple(a.shape[:-1]) + (N,)
+    if out is None:
+        out = torch.zeros(shape, dtype=torch.bfloat16, device=a.device)
+    _need(out, "out", torch.bfloat16, shape)
+    nbytes = lib().moe_grouped_gemm_workspace_size(ctypes.byref(g))
+    if nbytes == 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, "moe_grouped_gemm_workspace_size")
+    if workspace is None:
+        workspace = _workspace(int(nbytes), a.device)
+    _check(lib().moe_grouped_gemm_fp8(ctypes.byref(g), _p(a), _p(a_scale), _p(b), _p(b_scale),
+                                      _p(layout_metadata), _p(out), _p(workspace),
+                                      workspace.numel(), _stream(stream)),
+           "moe_grouped_gemm_fp8")
     return out

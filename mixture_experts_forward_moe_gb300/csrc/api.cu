@@ -728,6 +728,28 @@ moe_status_t moe_grouped_gemm(const moe_grouped_gemm_t* g, const void* a, const 
   return from_cuda(launch_gemm(c, s, true));
 }
 
+moe_status_t moe_grouped_gemm_fp8(const moe_grouped_gemm_t* g, const uint8_t* a,
+                                  const float* a_scale, const uint8_t* b, const float* b_scale,
+                                  const int32_t* layout_metadata, void* out, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  if (!grouped_gemm_valid(g)) return MOE_ERR_INVALID_ARG;
+  if (g->dtype != MOE_BF16 || g->activation != 0 || g->out_f32) return MOE_ERR_UNSUPPORTED;
+  if (g->N % 128 != 0 || g->K % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!workspace || !layout_metadata) return MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < moe_grouped_gemm_workspace_size(g)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const int64_t rows = grouped_gemm_rows(g);
+  if (rows == 0) return MOE_OK;
+  if (!a || !a_scale || !b || !b_scale || !out) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  void* ws = workspace;
+  Tile* tiles = at<Tile>(ws, kHeaderBytes);
+  MOE_TRY(launch_build_tiles_meta(g->E, g->max_m, rows, layout_metadata, tiles, tile_counter(ws),
+                                  kTileRows, status_word(ws), s, false));
+  return from_cuda(launch_gemm_fp8(g->E, g->N, g->K, rows, a, a_scale, b, b_scale, tiles,
+                                   tile_counter(ws), (int)grouped_gemm_max_tiles(g),
+                                   static_cast<__nv_bfloat16*>(out), status_word(ws), s, true));
+}
+
 moe_status_t moe_post_permute(const moe_problem_t* p, const void* rows,
                               const float* topk_weights, const int32_t* inv_route, void* out,
                               void* stream) {

@@ -1,0 +1,77 @@
+"""FP8 (E4M3) block-scaled grouped GEMM on the GPU vs the fp64 oracle (TileOPs MoE page, op
+MoEGroupedGemmFP8Fwd): small masked and contiguous cases with every valid row compared, and the
+page's full-size workloads on sampled rows of every group."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import assert_rounded_close
+from mixture_experts_forward_moe_gb300 import binding as B
+from mixture_experts_forward_moe_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("E,max_m,K,N,total", [(3, 144, 384, 256, 200),  # a 2-tile group
+                                               (5, 16, 128, 128, 9),       # 1-row groups
+                                               (2, 64, 1024, 384, 128)])
+def test_fp8_masked_grouped_gemm_matches_oracle(E, max_m, K, N, total, cuda_device):
+    w = inputs.Fp8GemmWorkload("t", E=E, max_m=max_m, K=K, N=N, total=total)
+    d = inputs.generate_fp8_gemm(w, seed=E + K, device=cuda_device)
+    out = B.moe_grouped_gemm_fp8(d["a"], d["a_scale"], d["b"], d["b_scale"], d["meta"])
+    torch.cuda.synchronize()
+    meta = d["meta"].cpu().numpy()
+    ref = oracle.grouped_gemm_fp8(d["a"].cpu(), d["a_scale"].cpu(), d["b"].cpu(),
+                                  d["b_scale"].cpu(), meta, max_m=max_m)
+    live = np.concatenate([np.arange(e * max_m, e * max_m + int(meta[e])) for e in range(E)])
+    got = out.reshape(E * max_m, N)[torch.from_numpy(live).to(cuda_device)]
+    assert_rounded_close(got, ref[live], torch.bfloat16, what=f"fp8 masked E={E} K={K} N={N}")
+    dead = np.setdiff1d(np.arange(E * max_m), live)
+    assert torch.all(out.reshape(E * max_m, N)[torch.from_numpy(dead).to(cuda_device)] == 0)
+
+
+def test_fp8_contiguous_grouped_gemm_matches_oracle(cuda_device):
+    w = inputs.Fp8GemmWorkload("t", E=4, max_m=96, K=256, N=256, total=150)
+    d = inputs.generate_fp8_gemm(w, seed=3, device=cuda_device)
+    meta = d["meta"].cpu().numpy()
+    psum = np.cumsum(meta).astype(np.int32)
+    rows = int(psum[-1])
+    a = d["a"].reshape(-1, w.K)[:rows].contiguous()
+    sa = d["a_scale"].reshape(-1, w.K // 128)[:rows].contiguous()
+    out = B.moe_grouped_gemm_fp8(a, sa, d["b"], d["b_scale"],
+                                 torch.from_numpy(psum).to(cuda_device))
+    torch.cuda.synchronize()
+    ref = oracle.grouped_gemm_fp8(a.cpu(), sa.cpu(), d["b"].cpu(), d["b_scale"].cpu(), psum)
+    assert_rounded_close(out, ref, torch.bfloat16, what="fp8 contiguous")
+
+
+FULL = ["ds-v3-e8-up-masked", "ds-v3-dec-b64-down", "qwen3-235b-dec-b256-up",
+        "kimi-k2-dec-b64-up"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_fp8_full_size_workloads(name, cuda_device):
+    w = inputs.FP8_GEMM_WORKLOADS[name]
+    d = inputs.generate_fp8_gemm(w, seed=0, device=cuda_device)
+    out = B.moe_grouped_gemm_fp8(d["a"], d["a_scale"], d["b"], d["b_scale"], d["meta"])
+    torch.cuda.synchronize()
+    meta = d["meta"].cpu().numpy()
+    rows = []
+    for e in range(w.E):  # first and last valid row of each group
+        m = int(meta[e])
+        if m:
+            rows += sorted({e * w.max_m, e * w.max_m + m - 1})
+    rows = np.array(rows[:96])
+    grp = rows // w.max_m
+    a = d["a"].reshape(-1, w.K)[torch.from_numpy(rows).to(cuda_device)].cpu()
+    sa = d["a_scale"].reshape(-1, w.K // 128)[torch.from_numpy(rows).to(cuda_device)].cpu()
+    ref = np.empty((rows.size, w.N))
+    for e in np.unique(grp):  # each group's sampled rows as a one-group contiguous problem
+        sel = np.nonzero(grp == e)[0]
+        ref[sel] = oracle.grouped_gemm_fp8(a[sel], sa[sel], d["b"][e:e + 1].cpu(),
+                                           d["b_scale"][e:e + 1].cpu(),
+                                           np.array([sel.size], np.int32))
+    got = out.reshape(-1, w.N)[torch.from_numpy(rows).to(cuda_device)]
+    assert_rounded_close(got, ref, torch.bfloat16, what=name)
+    assert int(meta.sum()) == min(w.total, int(meta.sum()))
