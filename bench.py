@@ -4,8 +4,8 @@
 A step is one fused_moe_fwd call (router, sort, gather, gemm1 + SwiGLU, gemm2 x route weight,
 combine, shared expert when present) over one batch of seeded synthetic inputs that are already
 resident in HBM.  When a step streams more than twice the L2 in expert weights (every measured
-workload but the tiny one) nothing is flushed between steps; otherwise the L2 is flushed by a
-256 MiB write outside the timed events.
+workload but the tiny one) nothing is flushed between steps; otherwise the L2 is flushed outside
+the timed events by a 256 MiB write followed by a 256 MiB read (clean lines, no write-back).
 A step is one replay of a CUDA graph that holds one captured fused_moe_fwd call (its kernels
 and their programmatic dependencies), so the host issues one launch per step; `--eager` times
 the eager calls instead, and the eager time is reported beside it in any case.  Each step is
@@ -44,6 +44,23 @@ DEFAULT_WORKLOAD = "qwen3-30b-a3b-decode-t32"
 METRIC = "fused_moe_fwd device ms, TFLOP/s & HBM GB/s; % of GB300 roofline per config"
 L2_FLUSH_BYTES = 256 << 20
 L2_BYTES = 126 << 20  # GB300 L2 (about 129 MB)
+
+
+class L2Flush:
+    """Evicts the L2 between timed steps, outside their events: a 256 MiB write (the flush), then
+    a 256 MiB read of another buffer, so the lines left behind are clean and unrelated to the
+    step and the next step pays no write-back of the flush's dirty lines."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
+
+    note = "flushed between steps outside the timed events (256 MiB write, then 256 MiB read)"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -335,20 +352,19 @@ def run_ours(args, w, ws_n, rank, local):
     n_unique = int(torch.unique(lids[lids >= 0]).numel())
     P_local = int((lids >= 0).sum())  # routes this GPU computes
     # Between steps: when the expert weights one step streams exceed twice the L2, nothing of a
-    # step's weights survives into the next and no flush is needed (a flush by writing would
-    # leave dirty lines that the next step pays to write back); otherwise flush by a write.
+    # step's weights survives into the next and no flush is needed; otherwise the L2 is flushed.
     weight_bytes = algorithmic_bytes(w, n_unique, P_local)["total"]
     if weight_bytes > 2 * L2_BYTES:
         flush = None
         l2_note = (f"no flush: each step streams {weight_bytes / 1e9:.2f} GB of expert weights, "
                    f"more than twice the {L2_BYTES >> 20} MiB L2")
     else:
-        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-        l2_note = "flushed between steps (256 MiB write outside the timed events)"
+        flush = L2Flush(dev)
+        l2_note = L2Flush.note
 
     def do_flush():
         if flush is not None:
-            flush.zero_()
+            flush()
 
     for _ in range(args.warmup):
         do_flush()
@@ -595,6 +611,8 @@ def run_grouped_gemm(args, w, ws_n, rank, local):
     wsp = B.new_workspace(B.lib().moe_grouped_gemm_workspace_size(B.ctypes.byref(g)), dev)
     stream = torch.cuda.current_stream()
     valid = int(meta.sum())
+    # groups with at least one valid row: the only weights the op has to read
+    active = int((meta > 0).sum())
 
     def step():
         if fp8:
@@ -619,12 +637,22 @@ def run_grouped_gemm(args, w, ws_n, rank, local):
             step()
         torch.cuda.synchronize()
     run = graph.replay if graph is not None else step
+    # Between steps: a call that streams more than twice the L2 in weights leaves nothing of
+    # them for the next one; a smaller one gets the L2 flushed by a write outside its events.
+    eb = 1 if fp8 else 2  # bytes per element of a and b
+    weight_bytes = active * w.N * w.K * eb
+    flush = L2Flush(dev) if weight_bytes <= 2 * L2_BYTES else None
+    l2_note = (f"no flush: each call streams {weight_bytes / 1e9:.2f} GB of weights, more than "
+               f"twice the {L2_BYTES >> 20} MiB L2" if flush is None else
+               f"each call streams {weight_bytes / 1e9:.2f} GB of weights; " + L2Flush.note)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     clocks = ClockSampler(local) if rank == 0 else None
     barrier()
     torch.cuda.synchronize()
     for i in range(args.steps):
+        if flush is not None:
+            flush()
         starts[i].record(stream)
         run()
         ends[i].record(stream)
@@ -640,10 +668,10 @@ def run_grouped_gemm(args, w, ws_n, rank, local):
     flops = w.flops(valid)
     value = job_throughput(flops, ws_n, args.steps, max_ms) / 1e12
     hbm_gbs, bf16_peak, bf16_sust, peak_src = measured_peaks()
-    eb = 1 if fp8 else 2  # bytes per element of a and b
-    # weights (+ their block scales) + the valid rows in (+ scales) and out (bf16)
-    ab = (w.E * w.N * w.K * eb + valid * w.K * eb + valid * w.N * 2 +
-          ((w.E * (w.N // 128) * (w.K // 128) + valid * (w.K // 128)) * 4 if fp8 else 0))
+    # the weights (+ their block scales) of the groups that have rows, + the valid rows in (+ their
+    # scales) and out (bf16); an empty group's weights are never read
+    ab = (active * w.N * w.K * eb + valid * w.K * eb + valid * w.N * 2 +
+          ((active * (w.N // 128) * (w.K // 128) + valid * (w.K // 128)) * 4 if fp8 else 0))
     achieved = ab / (ms * 1e-3) / 1e9
     # FP8 tensor peak: the measured bf16 peak times the nominal fp8/bf16 ratio (4.5 / 2.25)
     tpeak = bf16_sust * (2.0 if fp8 else 1.0)
@@ -676,10 +704,9 @@ def run_grouped_gemm(args, w, ws_n, rank, local):
                  f"[{w.m_lo}, {w.m_hi}]"),
         "config": {"workload": w.name, "E": w.E, "max_m": w.max_m, "K": w.K, "N": w.N,
                    "weights": "e4m3 with 128x128 f32 block scales" if fp8 else "bf16",
-                   "valid_rows": valid, "global_batch": valid * ws_n,
+                   "valid_rows": valid, "active_groups": active, "global_batch": valid * ws_n,
                    "parallelism": f"replicas x{ws_n}",
-                   "l2": f"no flush: each call streams {w.E * w.N * w.K * eb / 1e9:.2f} GB of "
-                         f"weights, more than twice the L2",
+                   "l2": l2_note,
                    "timing": "one CUDA-graph replay per step; CUDA event pair per step"},
         "roofline": roofline, "gpu_launches": 2 * args.steps, "clocks": clk,
         "context_published_ms": {"ms": PUBLISHED_GROUPED_MS.get(w.name),

@@ -10,12 +10,29 @@
 // k-block partial D_kb = W_slab(kb) . A_tile(kb)^T (four tcgen05.mma kind::f8f6f4 of k = 32, A =
 // weights, B = tokens, both from 128-byte-swizzled shared memory) only needs one scalar b_scale
 // times a per-column (token) a_scale before it is added to the running sum.  Each k block is
-// therefore accumulated in a fresh TMEM buffer (4 in flight), and eight epilogue warps fold
-// scale * D_kb into f32 registers (warp w reads TMEM lanes 32*(w%4)..; warpgroups split the 128
-// token columns in halves), then store the bf16 rows.
+// therefore accumulated in a fresh TMEM buffer, and eight epilogue warps fold scale * D_kb into
+// f32 registers (warp w reads TMEM lanes 32*(w%4)..; warpgroups split the token columns in
+// halves), then store the bf16 rows.
 //
-// Warp roles (320 threads, one CTA per SM, persistent): warp 0 TMA producer, warp 1 MMA issuer,
-// warps 2-9 scale-and-accumulate epilogue.  Every wait is bounded as in gemm.cu.
+// At decode sizes the MMA issuer, not HBM, sets the pace: every barrier wait, tcgen05.mma and
+// commit costs the single issuing thread tens to a hundred cycles, while the MMAs themselves
+// (N = 16..64 tokens) are short.  So for token tiles of up to 64 rows a pipeline stage carries
+// two k blocks (256 k: two weight boxes and two token boxes) and the MMA thread pays one
+// full-barrier wait, one TMEM-buffer wait and one commit per two k blocks; taller tiles keep one
+// k block per stage, where the longer MMAs hide the issue cost and four TMEM buffers keep the
+// epilogue's scale-and-accumulate work off the critical path.  In both, the epilogue learns that
+// a stage's MMAs are done from the stage's empty barrier (the commit that frees its shared
+// memory) instead of a second commit.  The stage count follows the stage size: six stages of
+// 36 KB for 16-row tiles, six of 32 KB for 128.
+//
+// Units are taken round-robin (CTA c: units c, c + G, ...).  Splitting the last partial wave's
+// units along k over all SMs (stream-K, with f32 partials handed between CTAs) was measured on
+// the page's workloads and lost: the pieces are short, and their fixups cost more than the
+// imbalance they remove.
+//
+// Warp roles (384 threads, one CTA per SM, persistent): warp 0 TMA producer, warp 1 MMA issuer
+// (warps 2-3 idle; their warpgroup hands registers to the epilogue), warps 4-11
+// scale-and-accumulate epilogue.  Every wait is bounded as in gemm.cu.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -25,18 +42,29 @@ namespace gb300moe {
 
 namespace {
 
-constexpr int kF8Stages = 6;
-constexpr int kF8BlockK = 128;                                // k per stage = one scale block
-constexpr int kF8WBytes = kSlab * kF8BlockK;                  // 16 KB of weights
-constexpr int kF8TBytes = kTileRows * kF8BlockK;              // up to 16 KB of tokens
-constexpr int kF8StageBytes = kF8WBytes + kF8TBytes;
-constexpr int kF8PBufs = 4;                                   // TMEM partial buffers
-constexpr int kF8Threads = 320;
-constexpr int kF8SmemBytes = kF8Stages * kF8StageBytes + 1024;
+constexpr int kF8BlockK = 128;                  // k per scale block
+constexpr int kF8WBytes = kSlab * kF8BlockK;    // 16 KB of weights per k block
+constexpr int kF8MaxStages = 6;
+// 12 warps in three warpgroups: warpgroup 0 holds the TMA producer (warp 0) and the MMA issuer
+// (warp 1; warps 2-3 idle) and gives up registers (setmaxnreg) to warpgroups 1-2, the epilogue,
+// whose 64 f32 accumulators and 64-column TMEM loads per thread need them:
+// 128 * 56 + 256 * 224 = 64512 = 384 threads * 168 registers at launch.
+constexpr int kF8Threads = 384;
+constexpr int kF8ProducerRegs = 56;
+constexpr int kF8EpilogueRegs = 224;
+static_assert(128 * kF8ProducerRegs + 256 * kF8EpilogueRegs <= kF8Threads * 168,
+              "register split exceeds the launch allocation");
+constexpr int kF8TmemCols = 512;
+// Dynamic shared memory the kernel may use: the per-block maximum less its static part.
+constexpr int kF8SmemLimit = 232448 - 4096;
 constexpr uint64_t kF8DrainNs = 1000000000ull;
 
 struct F8Params {
   int N, num_kb, n_slabs;
+  int tcap;          // token rows a stage holds per k block (16..128, a multiple of 16)
+  int stage_bytes;   // KPS * (16 KB + tcap * 128), KPS = k blocks per stage
+  int stages;        // pipeline stages (<= kF8MaxStages)
+  int nbuf;          // TMEM buffers (KPS * tcap columns each), <= stages
   const Tile* tiles;
   const int* n_tiles;
   const float* a_scale;  // [rows, num_kb]
@@ -51,7 +79,7 @@ struct F8Unit {
 };
 
 // Units of group e occupy [n_slabs*first, n_slabs*(first+count)), slab-major (as in gemm.cu).
-__device__ __forceinline__ bool f8_unit(const F8Params& p, int u, F8Unit& U) {
+__device__ __forceinline__ void f8_unit(const F8Params& p, int u, F8Unit& U) {
   const Tile owner = p.tiles[u / p.n_slabs];
   const int local = u - p.n_slabs * owner.first;
   U.slab = local / owner.count;
@@ -60,7 +88,6 @@ __device__ __forceinline__ bool f8_unit(const F8Params& p, int u, F8Unit& U) {
   U.row0 = t.row0;
   U.nrows = t.nrows;
   U.n_mma = (t.nrows + 15) & ~15;
-  return U.nrows > 0;
 }
 
 __device__ __forceinline__ void f8_wait_drain(uint64_t* bar, uint32_t parity) {
@@ -69,21 +96,21 @@ __device__ __forceinline__ void f8_wait_drain(uint64_t* bar, uint32_t parity) {
     if (global_timer_ns() - t0 > kF8DrainNs) return;
 }
 
+template <int KPS>
 __global__ void __launch_bounds__(kF8Threads, 1)
     moe_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmB16,
                         const __grid_constant__ CUtensorMap tmB64,
                         const __grid_constant__ CUtensorMap tmB128, const F8Params p) {
   extern __shared__ uint8_t dsmem[];
-  __shared__ __align__(8) uint64_t full_bar[kF8Stages];
-  __shared__ __align__(8) uint64_t empty_bar[kF8Stages];
-  __shared__ __align__(8) uint64_t pfull_bar[kF8PBufs];
-  __shared__ __align__(8) uint64_t pempty_bar[kF8PBufs];
+  __shared__ __align__(8) uint64_t full_bar[kF8MaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kF8MaxStages];  // MMAs of the stage done
+  __shared__ __align__(8) uint64_t pempty_bar[kF8MaxStages];  // TMEM buffer read by the epilogue
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
   __shared__ int s_n_units;
-  __shared__ __align__(16) float s_sa[2][kTileRows];  // column scales of one k block
+  __shared__ __align__(16) float s_sa[2][2][kTileRows];  // column scales of a stage's k blocks
 
   const uint32_t raw = smem_u32(dsmem);
   uint8_t* smem = dsmem + ((1024u - (raw & 1023u)) & 1023u);
@@ -92,13 +119,10 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   volatile int* abort_flag = &s_abort;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kF8Stages; ++s) {
+    for (int s = 0; s < kF8MaxStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
-    }
-    for (int b = 0; b < kF8PBufs; ++b) {
-      mbar_init(&pfull_bar[b], 1);
-      mbar_init(&pempty_bar[b], 8);  // one arrival per epilogue warp
+      mbar_init(&pempty_bar[s], 8);  // one arrival per epilogue warp
     }
     mbar_init(&drain_bar, 1);
     s_abort = 0;
@@ -111,7 +135,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     prefetch_tensormap(&tmB128);
   }
   if (warp == 1) {
-    tmem_alloc(&s_tmem_base, kF8PBufs * kTileRows);
+    tmem_alloc(&s_tmem_base, kF8TmemCols);
     tmem_relinquish();
   }
   pdl_wait();
@@ -122,108 +146,127 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
   const int n_units = s_n_units;
+  const int tblk = p.tcap * kF8BlockK;  // bytes of one k block of token rows
 
-  if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int stage = 0, issued = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        F8Unit U;
-        if (!f8_unit(p, u, U)) continue;
-        const uint32_t bytes = kF8WBytes + U.n_mma * kF8BlockK;
-        const int wrow = U.e * p.N + U.slab * kSlab;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.limit_ns, p.status)) {
-            ok = false;
-            break;
-          }
-          uint8_t* sa = smem + stage * kF8StageBytes;
-          uint8_t* sb = sa + kF8WBytes;
-          mbar_arrive_expect_tx(&full_bar[stage], bytes);
-          const int kx = kb * kF8BlockK;
-          tma_load_2d(sa, &tmW, &full_bar[stage], kx, wrow);
-          int r = 0;
-          for (; r + 128 <= U.n_mma; r += 128)
-            tma_load_2d(sb + r * kF8BlockK, &tmB128, &full_bar[stage], kx, U.row0 + r);
-          for (; r + 64 <= U.n_mma; r += 64)
-            tma_load_2d(sb + r * kF8BlockK, &tmB64, &full_bar[stage], kx, U.row0 + r);
-          for (; r < U.n_mma; r += 16)
-            tma_load_2d(sb + r * kF8BlockK, &tmB16, &full_bar[stage], kx, U.row0 + r);
-          ++issued;
-          if (++stage == kF8Stages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      if (*abort_flag) {
-        const int n = issued < kF8Stages ? issued : kF8Stages;
-        for (int i = issued - n; i < issued; ++i)
-          f8_wait_drain(&full_bar[i % kF8Stages], (uint32_t)((i / kF8Stages) & 1));
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      int stage = 0, pb = 0;
-      uint32_t phase = 0, pphase = 0;
-      bool ok = true, issued_any = false;
-      const uint32_t smem_base = smem_u32(smem);
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        F8Unit U;
-        if (!f8_unit(p, u, U)) continue;
-        const uint32_t idesc = idesc_e4m3_m128(U.n_mma);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.limit_ns, p.status) ||
-              !mbar_wait(&pempty_bar[pb], pphase ^ 1u, abort_flag, p.limit_ns, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = smem_base + (uint32_t)(stage * kF8StageBytes);
-          const uint32_t sb = sa + kF8WBytes;
-          const uint32_t d = tmem_base + (uint32_t)(pb * kTileRows);
-#pragma unroll
-          for (int k = 0; k < kF8BlockK / 32; ++k)
-            umma_f8(d, sw128_kmajor_desc(sa + k * 32), sw128_kmajor_desc(sb + k * 32), idesc,
-                    k != 0 ? 1u : 0u);
-          umma_commit(&empty_bar[stage]);
-          umma_commit(&pfull_bar[pb]);
-          issued_any = true;
-          if (++stage == kF8Stages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-          if (++pb == kF8PBufs) {
-            pb = 0;
-            pphase ^= 1u;
+  if (warp < 4) {  // warpgroup 0: producer and MMA issuer
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kF8ProducerRegs));
+    if (warp == 0) {
+      // ------------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        int stage = 0, issued = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+          F8Unit U;
+          f8_unit(p, u, U);
+          const int wrow = U.e * p.N + U.slab * kSlab;
+          for (int kb = 0; kb < p.num_kb; kb += KPS) {
+            const int nk = p.num_kb - kb >= KPS ? KPS : 1;
+            if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.limit_ns, p.status)) {
+              ok = false;
+              break;
+            }
+            uint8_t* sw = smem + stage * p.stage_bytes;
+            uint8_t* st = sw + KPS * kF8WBytes;
+            mbar_arrive_expect_tx(&full_bar[stage],
+                                  (uint32_t)(nk * (kF8WBytes + U.n_mma * kF8BlockK)));
+  #pragma unroll
+            for (int j = 0; j < KPS; ++j) {
+              if (j >= nk) break;
+              const int kx = (kb + j) * kF8BlockK;
+              tma_load_2d(sw + j * kF8WBytes, &tmW, &full_bar[stage], kx, wrow);
+              uint8_t* tb = st + j * tblk;
+              int r = 0;
+              for (; r + 128 <= U.n_mma; r += 128)
+                tma_load_2d(tb + r * kF8BlockK, &tmB128, &full_bar[stage], kx, U.row0 + r);
+              for (; r + 64 <= U.n_mma; r += 64)
+                tma_load_2d(tb + r * kF8BlockK, &tmB64, &full_bar[stage], kx, U.row0 + r);
+              for (; r < U.n_mma; r += 16)
+                tma_load_2d(tb + r * kF8BlockK, &tmB16, &full_bar[stage], kx, U.row0 + r);
+            }
+            ++issued;
+            if (++stage == p.stages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
+        if (*abort_flag) {
+          const int n = issued < p.stages ? issued : p.stages;
+          for (int i = issued - n; i < issued; ++i)
+            f8_wait_drain(&full_bar[i % p.stages], (uint32_t)((i / p.stages) & 1));
+        }
       }
-      if (issued_any) {
-        umma_commit(&drain_bar);
-        f8_wait_drain(&drain_bar, 0);
+    } else if (warp == 1) {
+      // ------------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        int stage = 0, pb = 0;
+        uint32_t phase = 0, pphase = 0;
+        bool ok = true, issued_any = false;
+        const uint32_t smem_base = smem_u32(smem);
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+          F8Unit U;
+          f8_unit(p, u, U);
+          const uint32_t idesc = idesc_e4m3_m128(U.n_mma);
+          for (int kb = 0; kb < p.num_kb; kb += KPS) {
+            const int nk = p.num_kb - kb >= KPS ? KPS : 1;
+            if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.limit_ns, p.status) ||
+                !mbar_wait(&pempty_bar[pb], pphase ^ 1u, abort_flag, p.limit_ns, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sw = smem_base + (uint32_t)(stage * p.stage_bytes);
+            // descriptors of k = 0; a step of 32 bytes along k adds 2 to the address field
+            const uint64_t da = sw128_kmajor_desc(sw);
+            const uint64_t db = sw128_kmajor_desc(sw + (uint32_t)(KPS * kF8WBytes));
+            const uint32_t d = tmem_base + (uint32_t)(pb * KPS * p.tcap);
+  #pragma unroll
+            for (int j = 0; j < KPS; ++j) {
+              if (j >= nk) break;
+              const uint64_t daj = da + (uint64_t)((j * kF8WBytes) >> 4);
+              const uint64_t dbj = db + (uint64_t)((j * tblk) >> 4);
+              const uint32_t dj = d + (uint32_t)(j * p.tcap);
+  #pragma unroll
+              for (int k = 0; k < kF8BlockK / 32; ++k)
+                umma_f8(dj, daj + 2 * k, dbj + 2 * k, idesc, k != 0 ? 1u : 0u);
+            }
+            umma_commit(&empty_bar[stage]);  // frees the smem stage; tells the epilogue
+            issued_any = true;
+            if (++stage == p.stages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            if (++pb == p.nbuf) {
+              pb = 0;
+              pphase ^= 1u;
+            }
+          }
+        }
+        if (issued_any) {
+          umma_commit(&drain_bar);
+          f8_wait_drain(&drain_bar, 0);
+        }
       }
     }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kF8EpilogueRegs));
     // ------------------------------------------------- scale-and-accumulate epilogue (8 warps)
     const int q = warp & 3;          // TMEM lane quarter this warp may read
-    const int g = (warp - 2) >> 2;   // token-column half: [64g, 64g + 64)
+    const int g = (warp - 4) >> 2;   // token-column half: [64g, 64g + 64)
     const int row = q * 32 + lane;   // weight row within the slab
-    const int et = threadIdx.x - 64;  // 0..255
-    int pb = 0, kbc = 0;
-    uint32_t pphase = 0;
+    const int et = threadIdx.x - 128;  // 0..255
+    int stage = 0, pb = 0, sc = 0;
+    uint32_t phase = 0, pphase = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       F8Unit U;
-      if (!f8_unit(p, u, U)) continue;
+      f8_unit(p, u, U);
       float acc[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
       // The scales of k blocks kb .. kb+3 are loaded ahead into registers, so their global
-      // latency overlaps the MMAs instead of every k block waiting for it.
+      // latency overlaps the MMAs instead of every stage waiting for it.
       const float* bs = p.b_scale + ((int64_t)U.e * p.n_slabs + U.slab) * p.num_kb;
       const bool has_row = et < U.nrows;
       const float* as = p.a_scale + (int64_t)(U.row0 + (has_row ? et : 0)) * p.num_kb;
@@ -233,51 +276,63 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         nsa[i] = (has_row && i < p.num_kb) ? as[i] : 0.0f;
         nsw[i] = i < p.num_kb ? bs[i] : 0.0f;
       }
-      for (int kb = 0; kb < p.num_kb; ++kb, ++kbc) {
-        const int buf = kbc & 1;
-        // column scale of this k block: b_scale (one per slab) times the token's a_scale
-        if (et < kTileRows) s_sa[buf][et] = nsw[0] * nsa[0];
+      const int ncols = U.n_mma - g * 64;  // warp-uniform; may be <= 0
+      for (int kb = 0; kb < p.num_kb; kb += KPS) {
+        const int nk = p.num_kb - kb >= KPS ? KPS : 1;
+        const int buf = sc & 1;
+        // column scales of the stage's k blocks: b_scale (one per slab) times the token's
+        // a_scale; the k blocks 4 ahead are fetched in their place
 #pragma unroll
-        for (int i = 0; i < 3; ++i) {
-          nsa[i] = nsa[i + 1];
-          nsw[i] = nsw[i + 1];
+        for (int j = 0; j < KPS; ++j) {
+          if (j < nk) {
+            if (et < kTileRows) s_sa[buf][j][et] = nsw[0] * nsa[0];
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {
+              nsa[i] = nsa[i + 1];
+              nsw[i] = nsw[i + 1];
+            }
+            nsa[3] = (has_row && kb + j + 4 < p.num_kb) ? as[kb + j + 4] : 0.0f;
+            nsw[3] = kb + j + 4 < p.num_kb ? bs[kb + j + 4] : 0.0f;
+          }
         }
-        nsa[3] = (has_row && kb + 4 < p.num_kb) ? as[kb + 4] : 0.0f;
-        nsw[3] = kb + 4 < p.num_kb ? bs[kb + 4] : 0.0f;
-        const bool got = mbar_wait(&pfull_bar[pb], pphase, abort_flag, p.limit_ns, p.status);
+        const bool got = mbar_wait(&empty_bar[stage], phase, abort_flag, p.limit_ns, p.status);
         if (!named_bar_and(1, 256, got)) {  // also publishes s_sa[buf]
           ok = false;
           break;
         }
         tc_fence_after();
-        const int ncols = U.n_mma - g * 64;  // warp-uniform
-        const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) +
-                            (uint32_t)(pb * kTileRows + g * 64);
-        const float4* sc4 = reinterpret_cast<const float4*>(&s_sa[buf][g * 64]);
-        if (ncols >= 64) {  // the whole half in one TMEM load
-          float v[64];
-          tmem_ld_x64(tb, v);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float4 sc = sc4[j];
-            acc[4 * j] = fmaf(sc.x, v[4 * j], acc[4 * j]);
-            acc[4 * j + 1] = fmaf(sc.y, v[4 * j + 1], acc[4 * j + 1]);
-            acc[4 * j + 2] = fmaf(sc.z, v[4 * j + 2], acc[4 * j + 2]);
-            acc[4 * j + 3] = fmaf(sc.w, v[4 * j + 3], acc[4 * j + 3]);
-          }
-        } else {  // decode-sized tiles: only the 16-column chunks that hold tokens
+        for (int j = 0; j < KPS; ++j) {
+          if (j < nk) {
+            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) +
+                                (uint32_t)((KPS * pb + j) * p.tcap + g * 64);
+            const float4* sc4 = reinterpret_cast<const float4*>(&s_sa[buf][j][g * 64]);
+            if (ncols >= 64) {  // the whole half in one TMEM load
+              float v[64];
+              tmem_ld_x64(tb, v);
 #pragma unroll
-          for (int ch = 0; ch < 3; ++ch) {
-            if (ch * 16 < ncols) {
-              float v[16];
-              tmem_ld_x16(tb + (uint32_t)(ch * 16), v);
+              for (int i = 0; i < 16; ++i) {
+                const float4 s4 = sc4[i];
+                acc[4 * i] = fmaf(s4.x, v[4 * i], acc[4 * i]);
+                acc[4 * i + 1] = fmaf(s4.y, v[4 * i + 1], acc[4 * i + 1]);
+                acc[4 * i + 2] = fmaf(s4.z, v[4 * i + 2], acc[4 * i + 2]);
+                acc[4 * i + 3] = fmaf(s4.w, v[4 * i + 3], acc[4 * i + 3]);
+              }
+            } else {  // decode-sized tiles: only the 16-column chunks that hold tokens
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const float4 sc = sc4[ch * 4 + j];
-                acc[ch * 16 + 4 * j] = fmaf(sc.x, v[4 * j], acc[ch * 16 + 4 * j]);
-                acc[ch * 16 + 4 * j + 1] = fmaf(sc.y, v[4 * j + 1], acc[ch * 16 + 4 * j + 1]);
-                acc[ch * 16 + 4 * j + 2] = fmaf(sc.z, v[4 * j + 2], acc[ch * 16 + 4 * j + 2]);
-                acc[ch * 16 + 4 * j + 3] = fmaf(sc.w, v[4 * j + 3], acc[ch * 16 + 4 * j + 3]);
+              for (int ch = 0; ch < 3; ++ch) {
+                if (ch * 16 < ncols) {
+                  float v[16];
+                  tmem_ld_x16(tb + (uint32_t)(ch * 16), v);
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    const float4 s4 = sc4[ch * 4 + i];
+                    acc[ch * 16 + 4 * i] = fmaf(s4.x, v[4 * i], acc[ch * 16 + 4 * i]);
+                    acc[ch * 16 + 4 * i + 1] = fmaf(s4.y, v[4 * i + 1], acc[ch * 16 + 4 * i + 1]);
+                    acc[ch * 16 + 4 * i + 2] = fmaf(s4.z, v[4 * i + 2], acc[ch * 16 + 4 * i + 2]);
+                    acc[ch * 16 + 4 * i + 3] = fmaf(s4.w, v[4 * i + 3], acc[ch * 16 + 4 * i + 3]);
+                  }
+                }
               }
             }
           }
@@ -285,7 +340,12 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&pempty_bar[pb]);
-        if (++pb == kF8PBufs) {
+        ++sc;
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++pb == p.nbuf) {
           pb = 0;
           pphase ^= 1u;
         }
@@ -306,16 +366,17 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, kF8PBufs * kTileRows);
+    tmem_dealloc(tmem_base, kF8TmemCols);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_fp8(int E, int N, int K, int64_t rows, const uint8_t* a,
-                            const float* a_scale, const uint8_t* b, const float* b_scale,
-                            const Tile* tiles, const int* n_tiles, int max_tiles,
-                            __nv_bfloat16* out, int* status, cudaStream_t s, bool pdl) {
+cudaError_t launch_gemm_fp8(int E, int N, int K, int64_t rows, int max_tile_rows,
+                            const uint8_t* a, const float* a_scale, const uint8_t* b,
+                            const float* b_scale, const Tile* tiles, const int* n_tiles,
+                            int max_tiles, __nv_bfloat16* out, int* status, cudaStream_t s,
+                            bool pdl) {
   if (N % kSlab != 0 || K % kF8BlockK != 0 || rows <= 0) return cudaErrorInvalidValue;
   CUtensorMap tmW, tmB16, tmB64, tmB128;
   if (!make_map_bytes(&tmW, b, (uint64_t)K, (uint64_t)E * N, kF8BlockK, kSlab) ||
@@ -327,6 +388,16 @@ cudaError_t launch_gemm_fp8(int E, int N, int K, int64_t rows, const uint8_t* a,
   p.N = N;
   p.num_kb = K / kF8BlockK;
   p.n_slabs = N / kSlab;
+  // Token rows per stage and k block: the tallest tile this layout can produce.
+  int tcap = max_tile_rows < 1 ? 1 : (max_tile_rows > kTileRows ? kTileRows : max_tile_rows);
+  tcap = (tcap + 15) & ~15;
+  p.tcap = tcap;
+  const int kps = tcap <= 64 ? 2 : 1;
+  p.stage_bytes = kps * (kF8WBytes + tcap * kF8BlockK);
+  p.stages = (kF8SmemLimit - 1024) / p.stage_bytes;
+  if (p.stages > kF8MaxStages) p.stages = kF8MaxStages;
+  p.nbuf = kF8TmemCols / (kps * tcap);
+  if (p.nbuf > p.stages) p.nbuf = p.stages;  // the epilogue never falls a full ring behind
   p.tiles = tiles;
   p.n_tiles = n_tiles;
   p.a_scale = a_scale;
@@ -336,18 +407,20 @@ cudaError_t launch_gemm_fp8(int E, int N, int K, int64_t rows, const uint8_t* a,
   p.limit_ns = wait_limit_ns();
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(moe_gemm_fp8_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kF8SmemBytes);
-    if (e != cudaSuccess) return e;
+    for (auto k : {moe_gemm_fp8_kernel<1>, moe_gemm_fp8_kernel<2>}) {
+      cudaError_t e =
+          cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kF8SmemLimit);
+      if (e != cudaSuccess) return e;
+    }
     attr_set = true;
   }
   const long long upper = (long long)max_tiles * p.n_slabs;
   const int sms = num_sms();
   const int grid = (int)(upper < sms ? upper : sms);
   if (grid <= 0) return cudaSuccess;
-  return launch_k(moe_gemm_fp8_kernel, dim3(grid), dim3(kF8Threads), kF8SmemBytes, s, pdl, tmW,
-                  tmB16, tmB64, tmB128, p);
+  const size_t smem = (size_t)p.stages * p.stage_bytes + 1024;
+  return launch_k(kps == 2 ? moe_gemm_fp8_kernel<2> : moe_gemm_fp8_kernel<1>, dim3(grid),
+                  dim3(kF8Threads), smem, s, pdl, tmW, tmB16, tmB64, tmB128, p);
 }
 
 }  // namespace gb300moe

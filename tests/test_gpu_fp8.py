@@ -13,9 +13,15 @@ from mixture_experts_forward_moe_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 
+# Pipeline stages carry two k blocks for token tiles of up to 64 rows and one for taller tiles:
+# (3, 144, ...) and (1, 128, 5120, ...) take one-block stages (the latter one 128-row unit of 40
+# k blocks); (5, 16, 128, ...) a single one-block stage; (2, 64, 1024, ...) two-block stages
+# throughout; (8, 48, 384, ...) 48-row stages and an odd k-block count (a one-block last stage).
 @pytest.mark.parametrize("E,max_m,K,N,total", [(3, 144, 384, 256, 200),  # a 2-tile group
                                                (5, 16, 128, 128, 9),       # 1-row groups
-                                               (2, 64, 1024, 384, 128)])
+                                               (2, 64, 1024, 384, 128),
+                                               (1, 128, 5120, 128, 128),
+                                               (8, 48, 384, 128, 60)])
 def test_fp8_masked_grouped_gemm_matches_oracle(E, max_m, K, N, total, cuda_device):
     w = inputs.Fp8GemmWorkload("t", E=E, max_m=max_m, K=K, N=N, total=total)
     d = inputs.generate_fp8_gemm(w, seed=E + K, device=cuda_device)
@@ -44,6 +50,16 @@ def test_fp8_contiguous_grouped_gemm_matches_oracle(cuda_device):
     torch.cuda.synchronize()
     ref = oracle.grouped_gemm_fp8(a.cpu(), sa.cpu(), d["b"].cpu(), d["b_scale"].cpu(), psum)
     assert_rounded_close(out, ref, torch.bfloat16, what="fp8 contiguous")
+
+
+def test_fp8_grouped_gemm_is_deterministic(cuda_device):
+    """Every output element is summed in one fixed order: two calls give the same bits."""
+    w = inputs.Fp8GemmWorkload("t", E=6, max_m=128, K=2048, N=512, total=500)
+    d = inputs.generate_fp8_gemm(w, seed=21, device=cuda_device)
+    outs = [B.moe_grouped_gemm_fp8(d["a"], d["a_scale"], d["b"], d["b_scale"], d["meta"])
+            for _ in range(2)]
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
 
 
 FULL = ["ds-v3-e8-up-masked", "ds-v3-dec-b64-down", "qwen3-235b-dec-b256-up",
