@@ -411,6 +411,7 @@ moe_status_t run_fused(const moe_problem_t* p, const Experts& X, const void* hid
     g1.n_tiles = tile_counter(ws);
     g1.max_tiles = (int)L.max_tiles;
     g1.tile_rows = kTileRows;
+    g1.early_tiles = token_rows ? 0 : 1;  // sort, then permute, then gemm1
     {
       StageTimer t(kGemm1, s);
       MOE_TRY(launch_gemm(g1, s, true));
@@ -430,6 +431,7 @@ moe_status_t run_fused(const moe_problem_t* p, const Experts& X, const void* hid
     g2.tiles = tiles2;
     g2.n_tiles = tile_counter2(ws);
     g2.tile_rows = tile_rows2;
+    g2.early_tiles = 1;  // sort, [permute,] gemm1, then gemm2
     {
       StageTimer t(kGemm2, s);
       MOE_TRY(launch_gemm(g2, s, true));

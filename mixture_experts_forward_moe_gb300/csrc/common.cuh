@@ -180,6 +180,9 @@ struct GemmCall {
   int dense_rows;
   // gemm2 route weights
   const float* topk_w;
+  // sorted mode: the tile list was written at least two launches before this GEMM, so the
+  // kernel may read it (and prefetch its first units' weights) before its dependency wait
+  int early_tiles;
   int* status;
 };
 

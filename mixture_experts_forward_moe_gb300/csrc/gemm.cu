@@ -121,6 +121,11 @@ struct KParams {
   const int32_t* topk_ids;
   const float* topk_w;
   int P, top_k, T, dense_rows;
+  // Sorted mode, bf16/f16 weights: before waiting for the previous kernel, the CTA pulls the
+  // first `prefetch_steps` K steps of weights of its first units into L2.  Only set when the
+  // tile list was written at least two launches earlier (it is then complete when this kernel
+  // starts).
+  int prefetch_steps;
   void* out;
   int* status;
   uint64_t limit_ns;
@@ -262,6 +267,24 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
   if (warp == 1) {
     tmem_alloc(&s_tmem_base, C::kTmemCols);
     tmem_relinquish();
+  }
+  if constexpr (!kW4) {
+    // The previous kernel may still be running on other SMs (this grid starts as its CTAs
+    // finish): stream the first units' weights into L2 meanwhile.  They depend on nothing that
+    // kernel writes.
+    if (p.prefetch_steps > 0 && p.mode == kSorted && threadIdx.x == 0) {
+      const int n = (*p.n_tiles) * p.n_slabs;
+      int left = p.prefetch_steps;
+      for (int u = blockIdx.x; u < n && left > 0; u += gridDim.x) {
+        Unit U;
+        if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
+        const int wrow = U.e * p.w_rows_per_expert + U.slab * p.slab_rows;
+        for (int kb = 0; kb < p.num_kb && left > 0; ++kb, --left) {
+          tma_prefetch_l2_2d(&tmW, kb * kBlockK, wrow);
+          if (kGemm1 && U.two) tma_prefetch_l2_2d(&tmW, kb * kBlockK, wrow + p.second_off);
+        }
+      }
+    }
   }
   pdl_wait();
   pdl_trigger();
@@ -867,6 +890,7 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   kp.out = c.out;
   kp.status = c.status;
   kp.limit_ns = wait_limit_ns();
+  kp.prefetch_steps = 0;
 
   if (c.tile_rows != 128 && c.tile_rows != 256) return cudaErrorInvalidValue;
   long long upper = 0;
@@ -879,6 +903,12 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   if (upper <= 0 || c.b_rows <= 0) return cudaSuccess;
   const int sms = num_sms();
   const int grid = (int)(upper < sms ? upper : sms);
+  if (c.early_tiles && c.mode == kSorted && !c.w4) {
+    // Up to ~48 MB (well under the L2) of first-unit weights over the whole grid.
+    const int64_t step_bytes = (int64_t)kSlab * kBlockK * 2 * (c.gemm1 && kp.gated ? 2 : 1);
+    const int64_t budget = (48ll << 20) / grid / step_bytes;
+    kp.prefetch_steps = (int)(budget < kp.num_kb * 4 ? budget : kp.num_kb * 4);
+  }
 
   if (c.gemm1) {
     return c.dtype == MOE_BF16 ? launch_rows<true, __nv_bfloat16>(c, kp, grid, s, pdl)

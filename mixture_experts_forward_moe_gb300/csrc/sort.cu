@@ -402,50 +402,95 @@ __global__ void __launch_bounds__(128)
 }
 
 // out[t, :] = round(sum_j y[inv[t*K+j], :] + shared[t, :]): f32 rows in, one rounding out.
-// A thread owns 4 columns; the route rows are loaded 8 at a time before they are summed, in j
-// order, so the sum is the same on every run.
+// A CTA owns one token and `cpc` chunks of 512 columns (4 per thread); the token's route rows
+// are looked up once into shared memory, and each thread then streams its columns of those rows
+// with up to 16 loads of 16 bytes in flight (two chunks of 8 routes).  The routes are summed in
+// j order, so the sum is the same on every run and for every cpc.
+constexpr int kCombineThreads = 128;
+
+// 16-byte read-only load when `pred`, else zeros: a predicated load, so that a group of them
+// can all be in flight before the first add.
+__device__ __forceinline__ float4 ld_f4_if(const float* ptr, bool pred) {
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  asm("{\n\t.reg .pred q;\n\t"
+      "setp.ne.b32 q, %5, 0;\n\t"
+      "@q ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];\n\t}\n"
+      : "+f"(v.x), "+f"(v.y), "+f"(v.z), "+f"(v.w)
+      : "l"(ptr), "r"((int)pred));
+  return v;
+}
+
 template <typename T>
-__global__ void __launch_bounds__(128)
-    combine_kernel(int K, int H, const float* __restrict__ y, const int32_t* __restrict__ inv,
-                   const int32_t* __restrict__ ids, const float* __restrict__ shared,
-                   T* __restrict__ out) {
+__device__ __forceinline__ void combine_store(T* out, float4 a) {
+  T o[4] = {DT<T>::from_f(a.x), DT<T>::from_f(a.y), DT<T>::from_f(a.z), DT<T>::from_f(a.w)};
+  *reinterpret_cast<uint2*>(out) = *reinterpret_cast<const uint2*>(o);
+}
+
+__device__ __forceinline__ void add4(float4& a, const float4 b) {
+  a.x += b.x;
+  a.y += b.y;
+  a.z += b.z;
+  a.w += b.w;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_kernel(int K, int H, int cpc, const float* __restrict__ y,
+                   const int32_t* __restrict__ inv, const int32_t* __restrict__ ids,
+                   const float* __restrict__ shared, T* __restrict__ out) {
+  __shared__ int s_row[32];  // y row of each route of the token, -1 to skip
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.y;
-  const int v = blockIdx.x * blockDim.x + threadIdx.x;  // 4 columns per thread
-  if (v >= H / 4) return;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j0 = 0; j0 < K; j0 += 8) {
-    float4 row[8];
+  if (threadIdx.x < K) {
+    const int r = t * K + threadIdx.x;
+    s_row[threadIdx.x] = (ids && ids[r] < 0) ? -1 : (inv ? inv[r] : r);
+  }
+  __syncthreads();
+  const int nv = H / 4;  // float4 columns of a row
+  const int v_end = min(nv, (blockIdx.x + 1) * cpc * kCombineThreads);
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  int v = blockIdx.x * cpc * kCombineThreads + threadIdx.x;
+  // two chunks at a time: 16 independent loads before the first add
+  for (; v + kCombineThreads < v_end; v += 2 * kCombineThreads) {
+    float4 acc0 = zero, acc1 = zero;
+    for (int j0 = 0; j0 < K; j0 += 8) {
+      float4 r0[8], r1[8];
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      const int j = j0 + jj;
-      int p = -1;
-      if (j < K) {
-        const int r = t * K + j;
-        p = (ids && ids[r] < 0) ? -1 : (inv ? inv[r] : r);
+      for (int jj = 0; jj < 8; ++jj) {
+        const int p = j0 + jj < K ? s_row[j0 + jj] : -1;
+        const float* src = y + (int64_t)(p < 0 ? 0 : p) * H + 4 * v;
+        r0[jj] = ld_f4_if(src, p >= 0);
+        r1[jj] = ld_f4_if(src + 4 * kCombineThreads, p >= 0);
       }
-      row[jj] = p >= 0 ? reinterpret_cast<const float4*>(y + (int64_t)p * H)[v]
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      acc.x += row[jj].x;
-      acc.y += row[jj].y;
-      acc.z += row[jj].z;
-      acc.w += row[jj].w;
+      for (int jj = 0; jj < 8; ++jj) {
+        add4(acc0, r0[jj]);
+        add4(acc1, r1[jj]);
+      }
     }
+    if (shared) {
+      add4(acc0, reinterpret_cast<const float4*>(shared + (int64_t)t * H)[v]);
+      add4(acc1, reinterpret_cast<const float4*>(shared + (int64_t)t * H)[v + kCombineThreads]);
+    }
+    combine_store(out + (int64_t)t * H + 4 * v, acc0);
+    combine_store(out + (int64_t)t * H + 4 * (v + kCombineThreads), acc1);
   }
-  if (shared) {
-    const float4 sh = reinterpret_cast<const float4*>(shared + (int64_t)t * H)[v];
-    acc.x += sh.x;
-    acc.y += sh.y;
-    acc.z += sh.z;
-    acc.w += sh.w;
+  if (v < v_end) {  // the last, odd chunk (or its ragged end)
+    float4 acc = zero;
+    for (int j0 = 0; j0 < K; j0 += 8) {
+      float4 r0[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const int p = j0 + jj < K ? s_row[j0 + jj] : -1;
+        r0[jj] = ld_f4_if(y + (int64_t)(p < 0 ? 0 : p) * H + 4 * v, p >= 0);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) add4(acc, r0[jj]);
+    }
+    if (shared) add4(acc, reinterpret_cast<const float4*>(shared + (int64_t)t * H)[v]);
+    combine_store(out + (int64_t)t * H + 4 * v, acc);
   }
-  T o[4] = {DT<T>::from_f(acc.x), DT<T>::from_f(acc.y), DT<T>::from_f(acc.z),
-            DT<T>::from_f(acc.w)};
-  *reinterpret_cast<uint2*>(out + (int64_t)t * H + 4 * v) = *reinterpret_cast<const uint2*>(o);
 }
 
 // out[t, :] = round( sum_j w[t, j] * rows[inv[t*K + j], :] ), f32 in fixed j order (TileOPs
@@ -582,14 +627,20 @@ cudaError_t launch_combine(const moe_problem_t& p, const void* y_route,
                            const int32_t* inv_route, const int32_t* ids, const void* shared_out,
                            void* out, cudaStream_t s, bool pdl) {
   if (p.T == 0) return cudaSuccess;
-  dim3 grid((p.H / 4 + 127) / 128, p.T);
+  // Chunks of 512 columns per CTA: as many as keep about 16 CTAs of 128 threads per SM busy in
+  // one round (a whole row per CTA at prefill sizes, one chunk per CTA at decode sizes).
+  const int nch = (p.H / 4 + kCombineThreads - 1) / kCombineThreads;
+  const int64_t want = 16ll * num_sms();
+  int cpc = (int)((int64_t)nch * p.T / want);
+  cpc = cpc < 1 ? 1 : (cpc > nch ? nch : cpc);
+  dim3 grid((nch + cpc - 1) / cpc, p.T);
   const float* y = static_cast<const float*>(y_route);
   const float* sh = static_cast<const float*>(shared_out);
   if (p.dtype == MOE_BF16)
-    return launch_k(combine_kernel<__nv_bfloat16>, grid, dim3(128), 0, s, pdl, p.top_k, p.H, y,
-                    inv_route, ids, sh, static_cast<__nv_bfloat16*>(out));
-  return launch_k(combine_kernel<__half>, grid, dim3(128), 0, s, pdl, p.top_k, p.H, y,
-                  inv_route, ids, sh, static_cast<__half*>(out));
+    return launch_k(combine_kernel<__nv_bfloat16>, grid, dim3(kCombineThreads), 0, s, pdl,
+                    p.top_k, p.H, cpc, y, inv_route, ids, sh, static_cast<__nv_bfloat16*>(out));
+  return launch_k(combine_kernel<__half>, grid, dim3(kCombineThreads), 0, s, pdl, p.top_k, p.H,
+                  cpc, y, inv_route, ids, sh, static_cast<__half*>(out));
 }
 
 }  // namespace gb300moe
