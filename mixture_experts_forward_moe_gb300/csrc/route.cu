@@ -83,12 +83,17 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   // keys; keep the keepG best groups (ties -> lower group id); exclude the rest.
   if (G > 1 && keepG < G) {
     const int gsz = E / G;
+    int gi[VPL];  // group of each of this lane's experts (-1 past E)
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      gi[i] = e < E ? e / gsz : -1;
+    }
     for (int g = 0; g < G; ++g) {
       float m1 = -INFINITY, m2 = -INFINITY;
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && e / gsz == g) {
+        if (gi[i] == g) {
           const float v = key[i];
           if (v > m1) {
             m2 = m1;
@@ -125,10 +130,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
       kept |= 1u << bg;
     }
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((kept >> (e / gsz)) & 1u)) live[i] = false;
-    }
+    for (int i = 0; i < VPL; ++i)
+      if (gi[i] >= 0 && !((kept >> gi[i]) & 1u)) live[i] = false;
   }
 
   // top_k rounds of warp argmax; lane j keeps the j-th selection.

@@ -87,9 +87,9 @@ __device__ void write_tile_list(int E, int excl, int padded, int rows, Tile* til
   if (e == E - 1) *n_tiles = incl;
 }
 
-// Per expert, the exclusive prefix of the chunk histograms over chunks (a warp per expert,
-// lanes over chunks, shuffle scans), then the block scan of the padded totals into the segment
-// offsets, the padding slots, tile_expert and (optionally) the two GEMM tile lists.
+// Per expert, the exclusive prefix of the chunk histograms over chunks (a thread per expert),
+// then the block scan of the padded totals into the segment offsets, the padding slots,
+// tile_expert and (optionally) the two GEMM tile lists.
 __global__ void __launch_bounds__(1024)
     sort_scan_kernel(int n_chunks, int E, int block_m, int64_t cap,
                      int32_t* __restrict__ chunk_counts, int32_t* __restrict__ counts,
@@ -102,32 +102,27 @@ __global__ void __launch_bounds__(1024)
   __shared__ int s_expert_total[1024];
   pdl_wait();
   pdl_trigger();
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  constexpr int kGroups = 4;  // 4 x 32 chunks loaded at once (independent loads)
-  for (int ex = w; ex < E; ex += 32) {
+  {
+    // Thread e walks expert e's column of the chunk histograms: at each step the warp reads
+    // one contiguous row segment, 16 chunks ahead (independent loads), and leaves the
+    // exclusive prefix (the chunk's base within the expert) in their place.
+    constexpr int kAhead = 16;
+    const int ex = threadIdx.x;
     int carry = 0;
-    for (int c0 = 0; c0 < n_chunks; c0 += 32 * kGroups) {
-      int v[kGroups];
+    if (ex < E) {
+      for (int c0 = 0; c0 < n_chunks; c0 += kAhead) {
+        int v[kAhead];
 #pragma unroll
-      for (int g = 0; g < kGroups; ++g) {
-        const int c = c0 + 32 * g + lane;
-        v[g] = c < n_chunks ? chunk_counts[(size_t)c * E + ex] : 0;
-      }
+        for (int i = 0; i < kAhead; ++i)
+          v[i] = c0 + i < n_chunks ? chunk_counts[(size_t)(c0 + i) * E + ex] : 0;
 #pragma unroll
-      for (int g = 0; g < kGroups; ++g) {
-        const int c = c0 + 32 * g + lane;
-        int incl = v[g];
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const int o = __shfl_up_sync(0xffffffffu, incl, off);
-          if (lane >= off) incl += o;
+        for (int i = 0; i < kAhead; ++i) {
+          if (c0 + i < n_chunks) chunk_counts[(size_t)(c0 + i) * E + ex] = carry;
+          carry += v[i];
         }
-        if (c < n_chunks)  // the chunk's base within expert ex
-          chunk_counts[(size_t)c * E + ex] = carry + incl - v[g];
-        carry += __shfl_sync(0xffffffffu, incl, 31);
       }
+      s_expert_total[ex] = carry;
     }
-    if (lane == 0) s_expert_total[ex] = carry;
   }
   __syncthreads();
   const int e = threadIdx.x;
@@ -259,15 +254,28 @@ __global__ void __launch_bounds__(1024)
   if (e == E - 1) *n_tiles = incl;
 }
 
+// Mask of the lanes whose v equals this lane's (0 <= v < 2^nbits), from one ballot per bit: the
+// mask __match_any_sync returns, at a fraction of its cost when most values differ.
+__device__ __forceinline__ unsigned match_by_ballots(int v, int nbits) {
+  unsigned m = 0xffffffffu;
+  for (int b = 0; b < nbits; ++b) {
+    const int bit = (v >> b) & 1;
+    const unsigned bb = __ballot_sync(0xffffffffu, bit);
+    m &= bit ? bb : ~bb;
+  }
+  return m;
+}
+
 // The whole sort in one CTA of 1024 threads (32 warps), for up to kFusedSortMaxRoutes routes
 // (beyond that the chunked kernels, which spread the ranking over many CTAs, are faster):
-// warp w owns the contiguous routes [w*per, (w+1)*per).  Pass A counts each warp's routes per
-// expert (lanes with the same id found with __match_any_sync); a per-expert prefix over the
-// warps, after the block scan of the padded totals, turns the counts into each warp's first
-// position in every expert segment; pass B walks the same routes in the same order and places
-// each one at that base plus its rank among the equal ids before it.  The result is the same
-// stable order as the chunked kernels, from a single launch.  With `tiles` it also writes the
-// GEMM tile list over the segments.
+// warp w owns the contiguous routes [w*per, (w+1)*per), per <= 256, which it reads once into
+// registers.  Pass A counts each warp's routes per expert (shared-memory atomics into the
+// warp's own counters); a per-expert prefix over the warps, after the block scan of the padded
+// totals, turns the counts into each warp's first position in every expert segment; pass B
+// walks the same routes in the same order and places each one at that base plus its rank among
+// the equal ids before it (lanes with the same id found by ballots on the id's bits).  The
+// result is the same stable order as the chunked kernels, from a single launch.  With `tiles`
+// it also writes the GEMM tile list over the segments.
 constexpr int kFusedSortMaxRoutes = 8192;
 
 __global__ void __launch_bounds__(1024)
@@ -289,28 +297,24 @@ __global__ void __launch_bounds__(1024)
   const int per = (P + 31) / 32;
   const int r0 = w * per, r1 = min(P, r0 + per);
   const unsigned lt_mask = (1u << lane) - 1u;
-  // Routes are read 8 groups of 32 at a time (independent loads, one latency per batch) and
-  // processed in route order.
+  // A warp's routes are read once, 8 groups of 32 (independent loads, one latency), and kept in
+  // registers for both passes: per <= 32 * kBatch because P <= kFusedSortMaxRoutes.
   constexpr int kBatch = 8;
-  for (int b0 = r0; b0 < r1; b0 += 32 * kBatch) {  // pass A: per-warp histogram
-    int eb[kBatch];
+  static_assert(32 * 32 * kBatch >= kFusedSortMaxRoutes, "one batch per warp");
+  int eb[kBatch];
 #pragma unroll
-    for (int g = 0; g < kBatch; ++g) {
-      const int r = b0 + 32 * g + lane;
-      eb[g] = r < r1 ? ids[r] : -1;
+  for (int g = 0; g < kBatch; ++g) {
+    const int r = r0 + 32 * g + lane;
+    int e = r < r1 ? ids[r] : -1;
+    if (e < -1 || e >= E) {
+      set_status(status, MOE_ERR_BAD_EXPERT_ID);
+      e = -1;
     }
-#pragma unroll
-    for (int g = 0; g < kBatch; ++g) {
-      int e = eb[g];
-      if (e < -1 || e >= E) {
-        set_status(status, MOE_ERR_BAD_EXPERT_ID);
-        e = -1;
-      }
-      const unsigned m = __match_any_sync(0xffffffffu, e);
-      if (e >= 0 && lane == __ffs(m) - 1) wc[e] += __popc(m);
-      __syncwarp();
-    }
+    eb[g] = e;
   }
+#pragma unroll
+  for (int g = 0; g < kBatch; ++g)  // pass A: per-warp histogram
+    if (eb[g] >= 0) atomicAdd(&wc[eb[g]], 1);
   __syncthreads();
   int total = 0;
   if (tid < E)
@@ -333,19 +337,14 @@ __global__ void __launch_bounds__(1024)
     s_total = incl;
   }
   __syncthreads();
-  for (int b0 = r0; b0 < r1; b0 += 32 * kBatch) {  // pass B: stable scatter
-    int eb[kBatch];
+  {  // pass B: stable scatter
+    const int nbits = 32 - __clz(E);  // e + 1 lies in [0, E]
 #pragma unroll
     for (int g = 0; g < kBatch; ++g) {
-      const int r = b0 + 32 * g + lane;
-      eb[g] = r < r1 ? ids[r] : -1;
-    }
-#pragma unroll
-    for (int g = 0; g < kBatch; ++g) {
-      const int r = b0 + 32 * g + lane;
-      int e = eb[g];
-      if (e < -1 || e >= E) e = -1;
-      const unsigned m = __match_any_sync(0xffffffffu, e);
+      if (r0 + 32 * g >= r1) break;  // warp-uniform
+      const int r = r0 + 32 * g + lane;
+      const int e = eb[g];
+      const unsigned m = match_by_ballots(e + 1, nbits);
       const int base = e >= 0 ? wc[e] : 0;
       __syncwarp();
       if (r < r1) {
