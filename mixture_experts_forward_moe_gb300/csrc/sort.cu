@@ -380,7 +380,12 @@ __global__ void __launch_bounds__(1024)
 }
 
 // a_sorted[p, :] = hidden[sorted_ids[p] / top_k, :] for p < offsets[E]; padding rows are zero.
-__global__ void __launch_bounds__(128)
+// A CTA copies whole rows (grid-stride): each thread loads up to 8 of its 16-byte pieces of the
+// row before it stores any, and the next row's source index is fetched during the copy.
+constexpr int kPermuteThreads = 128;
+constexpr int kPermuteAhead = 8;
+
+__global__ void __launch_bounds__(kPermuteThreads)
     permute_kernel(int top_k, int H, const uint16_t* __restrict__ hidden,
                    const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ offsets,
                    int E, uint16_t* __restrict__ a_sorted) {
@@ -388,15 +393,29 @@ __global__ void __launch_bounds__(128)
   pdl_trigger();
   const int64_t rows = offsets[E];
   const int nvec = H / 8;
-  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
-    const int sid = sorted_ids[row];
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  int64_t row = blockIdx.x;
+  int sid = row < rows ? sorted_ids[row] : -1;
+  for (; row < rows; row += gridDim.x) {
+    const int64_t next = row + gridDim.x;
+    const int next_sid = next < rows ? sorted_ids[next] : -1;
     uint4* dst = reinterpret_cast<uint4*>(a_sorted + row * H);
-    if (sid < 0) {
-      for (int v = threadIdx.x; v < nvec; v += blockDim.x) dst[v] = make_uint4(0, 0, 0, 0);
-    } else {
-      const uint4* src = reinterpret_cast<const uint4*>(hidden + (int64_t)(sid / top_k) * H);
-      for (int v = threadIdx.x; v < nvec; v += blockDim.x) dst[v] = src[v];
+    const uint4* src =
+        reinterpret_cast<const uint4*>(hidden + (int64_t)(sid < 0 ? 0 : sid / top_k) * H);
+    for (int v0 = 0; v0 < nvec; v0 += kPermuteThreads * kPermuteAhead) {
+      uint4 buf[kPermuteAhead];
+#pragma unroll
+      for (int i = 0; i < kPermuteAhead; ++i) {
+        const int v = v0 + i * kPermuteThreads + threadIdx.x;
+        buf[i] = (sid >= 0 && v < nvec) ? __ldg(src + v) : zero;
+      }
+#pragma unroll
+      for (int i = 0; i < kPermuteAhead; ++i) {
+        const int v = v0 + i * kPermuteThreads + threadIdx.x;
+        if (v < nvec) dst[v] = buf[i];
+      }
     }
+    sid = next_sid;
   }
 }
 
@@ -617,7 +636,7 @@ cudaError_t launch_permute(int dtype, int top_k, int H, const void* hidden,
   (void)dtype;  // a row copy: the element type does not matter
   if (cap <= 0) return cudaSuccess;
   const int64_t grid = cap < 4096 ? cap : 4096;
-  return launch_k(permute_kernel, dim3((int)grid), dim3(128), 0, s, pdl, top_k, H,
+  return launch_k(permute_kernel, dim3((int)grid), dim3(kPermuteThreads), 0, s, pdl, top_k, H,
                   static_cast<const uint16_t*>(hidden), sorted_ids, offsets, E,
                   static_cast<uint16_t*>(a_sorted));
 }
