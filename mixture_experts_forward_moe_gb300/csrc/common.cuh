@@ -28,6 +28,18 @@ constexpr size_t kHeaderBytes = 256;
 
 // Experts whose weights this GPU holds (an expert-parallel shard, or all E), and the problem
 // as the post-routing stages see it: ids are local indices in [0, local_experts) or -1.
+// CTAs a persistent GEMM uses for `units` equal units when it has `ctas` of them: the fewest
+// that keep each CTA's share at ceil(units / ctas), so every working CTA gets that share or one
+// less and none sits out the last wave's tail.  CTAs from this count on take no unit.  (The
+// 16-bit-weight GEMMs use it: their units stream weights at HBM speed, so a last wave on fewer
+// SMs leaves HBM idle.  The FP8 and NVFP4 GEMMs do not: their units run at the SM's own pace,
+// and the FP8 one measured slower on fewer CTAs.)
+__host__ __device__ __forceinline__ int balanced_ctas(int units, int ctas) {
+  if (units <= 0 || ctas <= 0) return ctas;
+  const int waves = (units + ctas - 1) / ctas;
+  return (units + waves - 1) / waves;
+}
+
 inline int local_experts(const moe_problem_t& p) {
   return p.ep_num_local > 0 ? p.ep_num_local : p.E;
 }

@@ -274,8 +274,9 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
     // kernel writes.
     if (p.prefetch_steps > 0 && p.mode == kSorted && threadIdx.x == 0) {
       const int n = (*p.n_tiles) * p.n_slabs;
+      const int G = balanced_ctas(n, gridDim.x);  // as for the unit loops below
       int left = p.prefetch_steps;
-      for (int u = blockIdx.x; u < n && left > 0; u += gridDim.x) {
+      for (int u = blockIdx.x < G ? blockIdx.x : n; u < n && left > 0; u += G) {
         Unit U;
         if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
         const int wrow = U.e * p.w_rows_per_expert + U.slab * p.slab_rows;
@@ -303,6 +304,11 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
   const int n_units = s_n_units;
+  // CTAs that take units (the stride) and this CTA's first unit.  16-bit weights stream at HBM
+  // speed, so their units are spread evenly over as few CTAs as keep the per-CTA share; the
+  // NVFP4 units run at the SM's own (MMA issue) pace and keep every CTA.
+  const int G = kW4 ? (int)gridDim.x : balanced_ctas(n_units, gridDim.x);
+  const int u0 = blockIdx.x < G ? (int)blockIdx.x : n_units;
 
   if (kW4 && warp == 0) {
     // ---------------------------------------------- NVFP4 weight producer (one lane)
@@ -313,7 +319,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       int issued = 0;
       bool ok = true;
       const int64_t slabs_per_expert = p.w_rows_per_expert / kSlab;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      for (int u = u0; u < n_units && ok; u += G) {
         Unit U;
         if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
         const int n_w = U.two ? 2 : 1;
@@ -351,7 +357,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       uint32_t tph = 0;
       int issued = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      for (int u = u0; u < n_units && ok; u += G) {
         Unit U;
         if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
         for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -407,7 +413,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&afull_bar[slot]);
     };
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    for (int u = u0; u < n_units && ok; u += G) {
       Unit U;
       if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
       const bool active = !kGemm1 || dg == 0 || U.two;
@@ -481,7 +487,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      for (int u = u0; u < n_units && ok; u += G) {
         Unit U;
         if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
         const uint32_t wbytes = U.two ? 2 * kSlab * kBlockK * 2 : kSlab * kBlockK * 2;
@@ -533,7 +539,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       bool ok = true;
       bool issued_any = false;
       const uint32_t smem_base = smem_u32(smem);
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      for (int u = u0; u < n_units && ok; u += G) {
         Unit U;
         if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.limit_ns, p.status)) break;
@@ -616,7 +622,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
     const int et = threadIdx.x - 64;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    for (int u = u0; u < n_units; u += G) {
       Unit U;
       if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
       // NVFP4: the expert's FP32 scale multiplies the FP32 accumulator (before the activation)
