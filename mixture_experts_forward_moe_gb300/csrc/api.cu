@@ -111,13 +111,17 @@ bool use_direct(const moe_problem_t& p) {
 
 // Token rows per tile of the sorted down-projection GEMM: 256 when the experts average at
 // least 96 routed rows (prefill), so an expert's weights reach the SMs at most once per 256
-// rows; 128 otherwise (decode), which keeps deeper pipelines.  The gate/up GEMM always uses
-// 128-row tiles: at 256 rows its two accumulators fill TMEM and the epilogue could no longer
-// overlap the next unit's K loop, which measured slower on the prefill shapes.
+// rows; 64 when they average at most 32 (decode), whose tiles stage two 64-k blocks at a time
+// and so pay the MMA issuer's per-stage costs once per 32 KB of weights; 128 in between.  The
+// gate/up GEMM always uses 128-row tiles: at 256 rows its two accumulators fill TMEM and the
+// epilogue could no longer overlap the next unit's K loop, which measured slower on the
+// prefill shapes.
 int sorted_tile_rows(const moe_problem_t& p) {
   const int64_t P = (int64_t)p.T * p.top_k;
   const int64_t active = P < p.E ? P : p.E;
-  return active > 0 && P / active >= 96 ? kTileRowsWide : kTileRows;
+  if (active <= 0) return kTileRows;
+  if (P / active >= 96) return kTileRowsWide;
+  return P / active <= 32 ? kTileRowsNarrow : kTileRows;
 }
 
 // Token rows per tile of the dense shared-expert GEMMs.
@@ -137,7 +141,7 @@ Layout make_layout(const moe_problem_t& p, int block_m) {
   L.P = (int64_t)p.T * p.top_k;
   L.cap = L.P + (int64_t)p.E * (block_m - 1);
   L.n_chunks = (L.P + kSortChunk - 1) / kSortChunk;
-  L.max_tiles = L.cap / kTileRows + p.E + 1;
+  L.max_tiles = L.cap / kTileRowsNarrow + p.E + 1;  // the most tiles any tile height gives
   size_t off = kHeaderBytes;
   auto take = [&](size_t bytes) {
     const size_t o = off;

@@ -66,14 +66,23 @@ namespace {
 // Every tcgen05.mma of M = 128 and k = 16 takes about the same time whatever N and wherever A
 // comes from, so at decode sizes the MMA issue rate bounds these GEMMs; the rings are sized so
 // that the decoders and the loads keep it fed.
+//
+// 64-row token tiles (the down projection at decode sizes): a stage carries two 64-k blocks
+// (kKps = 2), so the MMA issuer pays one barrier wait and one commit per 32 KB of weights
+// instead of per 16 KB; at a few tokens per expert those per-stage costs, not HBM, would
+// otherwise set the pace.
 template <bool kGemm1, int kN, bool kW4 = false>
 struct Cfg {
-  static_assert(kN == 128 || kN == 256, "tile rows");
+  static_assert(kN == 64 || kN == 128 || kN == 256, "tile rows");
+  static_assert(kN != 64 || (!kGemm1 && !kW4), "64-row tiles: 16-bit down projection only");
   static_assert(!kW4 || kN == 128, "NVFP4 tiles are 128 token rows");
   static constexpr int kSlabs = kGemm1 ? 2 : 1;
-  static constexpr int kStageK = kW4 ? 128 : kBlockK;  // k per pipeline stage
-  static constexpr int kStages = kGemm1 ? (kN == 128 ? 4 : 3) : (kN == 128 ? 7 : 4);
-  static constexpr int kABytes = kSlabs * kSlab * kBlockK * 2;
+  static constexpr int kKps = kN == 64 ? 2 : 1;  // 64-k blocks per stage (16-bit weights)
+  static constexpr int kStageK = kW4 ? 128 : kBlockK * kKps;  // k per pipeline stage
+  static constexpr int kStages = kGemm1 ? (kN == 128 ? 4 : 3) : (kN == 64 ? 4 : (kN == 128 ? 7 : 4));
+  static constexpr int kASubBytes = kSlabs * kSlab * kBlockK * 2;  // weights of one 64-k block
+  static constexpr int kBSubBytes = kN * kBlockK * 2;              // tokens of one 64-k block
+  static constexpr int kABytes = kASubBytes * (kW4 ? 1 : kKps);
   static constexpr int kBBytes = kN * kStageK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   // NVFP4 rings
@@ -491,29 +500,35 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
         Unit U;
         if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
         const uint32_t wbytes = U.two ? 2 * kSlab * kBlockK * 2 : kSlab * kBlockK * 2;
-        const uint32_t bytes = wbytes + U.n_mma * kBlockK * 2;
+        const uint32_t bytes = wbytes + U.n_mma * kBlockK * 2;  // per 64-k block
         const int wrow = U.e * p.w_rows_per_expert + U.slab * p.slab_rows;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = 0; kb < p.num_kb; kb += C::kKps) {
+          const int nsub = p.num_kb - kb < C::kKps ? p.num_kb - kb : C::kKps;
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.limit_ns, p.status)) {
             ok = false;
             break;
           }
-          uint8_t* sa = smem + stage * C::kStageBytes;
-          uint8_t* sb = sa + C::kABytes;
-          mbar_arrive_expect_tx(&full_bar[stage], bytes);
-          const int kx = kb * kBlockK;
-          tma_load_2d(sa, &tmW, &full_bar[stage], kx, wrow);
-          if (kGemm1 && U.two)
-            tma_load_2d(sa + kSlab * kBlockK * 2, &tmW, &full_bar[stage], kx,
-                        wrow + p.second_off);
-          // Token rows in as few copies as possible: 128-, then 64-, then 16-row boxes.
-          int r = 0;
-          for (; r + 128 <= U.n_mma; r += 128)
-            tma_load_2d(sb + r * kBlockK * 2, &tmB128, &full_bar[stage], kx, U.b_row0 + r);
-          for (; r + 64 <= U.n_mma; r += 64)
-            tma_load_2d(sb + r * kBlockK * 2, &tmB64, &full_bar[stage], kx, U.b_row0 + r);
-          for (; r < U.n_mma; r += 16)
-            tma_load_2d(sb + r * kBlockK * 2, &tmB, &full_bar[stage], kx, U.b_row0 + r);
+          uint8_t* sa0 = smem + stage * C::kStageBytes;
+          mbar_arrive_expect_tx(&full_bar[stage], bytes * nsub);
+#pragma unroll
+          for (int j = 0; j < C::kKps; ++j) {
+            if (j >= nsub) break;
+            uint8_t* sa = sa0 + j * C::kASubBytes;
+            uint8_t* sb = sa0 + C::kABytes + j * C::kBSubBytes;
+            const int kx = (kb + j) * kBlockK;
+            tma_load_2d(sa, &tmW, &full_bar[stage], kx, wrow);
+            if (kGemm1 && U.two)
+              tma_load_2d(sa + kSlab * kBlockK * 2, &tmW, &full_bar[stage], kx,
+                          wrow + p.second_off);
+            // Token rows in as few copies as possible: 128-, then 64-, then 16-row boxes.
+            int r = 0;
+            for (; r + 128 <= U.n_mma; r += 128)
+              tma_load_2d(sb + r * kBlockK * 2, &tmB128, &full_bar[stage], kx, U.b_row0 + r);
+            for (; r + 64 <= U.n_mma; r += 64)
+              tma_load_2d(sb + r * kBlockK * 2, &tmB64, &full_bar[stage], kx, U.b_row0 + r);
+            for (; r < U.n_mma; r += 16)
+              tma_load_2d(sb + r * kBlockK * 2, &tmB, &full_bar[stage], kx, U.b_row0 + r);
+          }
           ++issued;
           if (++stage == C::kStages) {
             stage = 0;
@@ -546,7 +561,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * C::kAccCols);
         const uint32_t idesc = idesc_f16_m128(U.n_mma, DT<T>::kIsBF16);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = 0; kb < p.num_kb; kb += C::kKps) {  // NVFP4: kKps = 1, 128-k stages
           if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.limit_ns, p.status)) {
             ok = false;
             break;
@@ -585,14 +600,21 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
               phase ^= 1u;
             }
           } else {
+            const int nsub = p.num_kb - kb < C::kKps ? p.num_kb - kb : C::kKps;
 #pragma unroll
-            for (int k = 0; k < kBlockK / 16; ++k) {
-              const uint64_t bdesc = sw128_kmajor_desc(sb + k * 32);
-              const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
-              umma_f16(d, sw128_kmajor_desc(sa + k * 32), bdesc, idesc, accum);
-              if (kGemm1 && U.two)
-                umma_f16(d + kN, sw128_kmajor_desc(sa + kSlab * kBlockK * 2 + k * 32), bdesc,
-                         idesc, accum);
+            for (int j = 0; j < C::kKps; ++j) {
+              if (j >= nsub) break;
+              const uint32_t aj = sa + (uint32_t)(j * C::kASubBytes);
+              const uint32_t bj = sb + (uint32_t)(j * C::kBSubBytes);
+#pragma unroll
+              for (int k = 0; k < kBlockK / 16; ++k) {
+                const uint64_t bdesc = sw128_kmajor_desc(bj + k * 32);
+                const uint32_t accum = (kb | j | k) != 0 ? 1u : 0u;
+                umma_f16(d, sw128_kmajor_desc(aj + k * 32), bdesc, idesc, accum);
+                if (kGemm1 && U.two)
+                  umma_f16(d + kN, sw128_kmajor_desc(aj + kSlab * kBlockK * 2 + k * 32), bdesc,
+                           idesc, accum);
+              }
             }
             umma_commit(&empty_bar[stage]);
             issued_any = true;
@@ -849,6 +871,9 @@ template <bool kGemm1, typename T>
 cudaError_t launch_rows(const GemmCall& c, const KParams& kp, int grid, cudaStream_t s,
                         bool pdl) {
   if (c.w4) return launch_typed<kGemm1, 128, __nv_bfloat16, true>(c, kp, grid, s, pdl);
+  if constexpr (!kGemm1) {
+    if (c.tile_rows == 64) return launch_typed<false, 64, T, false>(c, kp, grid, s, pdl);
+  }
   return c.tile_rows == 256 ? launch_typed<kGemm1, 256, T, false>(c, kp, grid, s, pdl)
                             : launch_typed<kGemm1, 128, T, false>(c, kp, grid, s, pdl);
 }
@@ -898,7 +923,9 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   kp.limit_ns = wait_limit_ns();
   kp.prefetch_steps = 0;
 
-  if (c.tile_rows != 128 && c.tile_rows != 256) return cudaErrorInvalidValue;
+  if (c.tile_rows != 128 && c.tile_rows != 256 &&
+      !(c.tile_rows == 64 && !c.gemm1 && !c.w4 && c.mode == kSorted))
+    return cudaErrorInvalidValue;
   long long upper = 0;
   if (c.mode == kSorted)
     upper = (long long)c.max_tiles * kp.n_slabs;
