@@ -314,10 +314,13 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
   const uint32_t tmem_base = s_tmem_base;
   const int n_units = s_n_units;
   // CTAs that take units (the stride) and this CTA's first unit.  16-bit weights stream at HBM
-  // speed, so their units are spread evenly over as few CTAs as keep the per-CTA share; the
-  // NVFP4 units run at the SM's own (MMA issue) pace and keep every CTA.
-  const int G = kW4 ? (int)gridDim.x : balanced_ctas(n_units, gridDim.x);
+  // speed, so their units are spread evenly over as few CTAs as keep the per-CTA share.  The
+  // NVFP4 units run at the SM's own (MMA issue) pace and keep every CTA, and their loops keep
+  // reading the stride from gridDim (a register copy of it measured 14 % slower there).
+  const int G = balanced_ctas(n_units, gridDim.x);
   const int u0 = blockIdx.x < G ? (int)blockIdx.x : n_units;
+#define UNIT_FIRST (kW4 ? (int)blockIdx.x : u0)
+#define UNIT_STRIDE (kW4 ? (int)gridDim.x : G)
 
   if (kW4 && warp == 0) {
     // ---------------------------------------------- NVFP4 weight producer (one lane)
@@ -328,7 +331,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       int issued = 0;
       bool ok = true;
       const int64_t slabs_per_expert = p.w_rows_per_expert / kSlab;
-      for (int u = u0; u < n_units && ok; u += G) {
+      for (int u = UNIT_FIRST; u < n_units && ok; u += UNIT_STRIDE) {
         Unit U;
         if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
         const int n_w = U.two ? 2 : 1;
@@ -366,7 +369,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       uint32_t tph = 0;
       int issued = 0;
       bool ok = true;
-      for (int u = u0; u < n_units && ok; u += G) {
+      for (int u = UNIT_FIRST; u < n_units && ok; u += UNIT_STRIDE) {
         Unit U;
         if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
         for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -422,7 +425,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&afull_bar[slot]);
     };
-    for (int u = u0; u < n_units && ok; u += G) {
+    for (int u = UNIT_FIRST; u < n_units && ok; u += UNIT_STRIDE) {
       Unit U;
       if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
       const bool active = !kGemm1 || dg == 0 || U.two;
@@ -496,7 +499,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      for (int u = u0; u < n_units && ok; u += G) {
+      for (int u = UNIT_FIRST; u < n_units && ok; u += UNIT_STRIDE) {
         Unit U;
         if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
         const uint32_t wbytes = U.two ? 2 * kSlab * kBlockK * 2 : kSlab * kBlockK * 2;
@@ -554,7 +557,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       bool ok = true;
       bool issued_any = false;
       const uint32_t smem_base = smem_u32(smem);
-      for (int u = u0; u < n_units && ok; u += G) {
+      for (int u = UNIT_FIRST; u < n_units && ok; u += UNIT_STRIDE) {
         Unit U;
         if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.limit_ns, p.status)) break;
@@ -644,7 +647,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
     const int et = threadIdx.x - 64;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = u0; u < n_units; u += G) {
+    for (int u = UNIT_FIRST; u < n_units; u += UNIT_STRIDE) {
       Unit U;
       if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
       // NVFP4: the expert's FP32 scale multiplies the FP32 accumulator (before the activation)
@@ -805,6 +808,8 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
     tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
+#undef UNIT_FIRST
+#undef UNIT_STRIDE
 
 // ---- host side -----------------------------------------------------------------------------
 
