@@ -210,7 +210,9 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) 
   }
 }
 
-template <bool kGemm1, int kN, typename T, bool kW4>
+// kBal: the units are spread evenly over balanced_ctas(units, gridDim.x) CTAs (decode-sized
+// launches); otherwise every CTA takes units c, c + gridDim.x, ...
+template <bool kGemm1, int kN, typename T, bool kW4, bool kBal>
 __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmB,
@@ -283,7 +285,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
     // kernel writes.
     if (p.prefetch_steps > 0 && p.mode == kSorted && threadIdx.x == 0) {
       const int n = (*p.n_tiles) * p.n_slabs;
-      const int G = balanced_ctas(n, gridDim.x);  // as for the unit loops below
+      const int G = kBal ? balanced_ctas(n, gridDim.x) : (int)gridDim.x;  // as below
       int left = p.prefetch_steps;
       for (int u = blockIdx.x < G ? blockIdx.x : n; u < n && left > 0; u += G) {
         Unit U;
@@ -313,14 +315,15 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
   const int n_units = s_n_units;
-  // CTAs that take units (the stride) and this CTA's first unit.  16-bit weights stream at HBM
-  // speed, so their units are spread evenly over as few CTAs as keep the per-CTA share.  The
-  // NVFP4 units run at the SM's own (MMA issue) pace and keep every CTA, and their loops keep
-  // reading the stride from gridDim (a register copy of it measured 14 % slower there).
+  // CTAs that take units (the stride) and this CTA's first unit.  At decode sizes (kBal) the
+  // 16-bit weights stream at HBM speed, so the units are spread evenly over as few CTAs as keep
+  // the per-CTA share.  Otherwise the loops read the stride from gridDim directly: held in a
+  // register instead, it measured 3 % slower at prefill sizes and 14 % slower in the NVFP4
+  // kernels (same register counts).
   const int G = balanced_ctas(n_units, gridDim.x);
   const int u0 = blockIdx.x < G ? (int)blockIdx.x : n_units;
-#define UNIT_FIRST (kW4 ? (int)blockIdx.x : u0)
-#define UNIT_STRIDE (kW4 ? (int)gridDim.x : G)
+#define UNIT_FIRST (kBal ? u0 : (int)blockIdx.x)
+#define UNIT_STRIDE (kBal ? G : (int)gridDim.x)
 
   if (kW4 && warp == 0) {
     // ---------------------------------------------- NVFP4 weight producer (one lane)
@@ -846,7 +849,7 @@ bool make_map(CUtensorMap* m, int dtype, const void* base, uint64_t inner, uint6
   return r == CUDA_SUCCESS;
 }
 
-template <bool kGemm1, int kN, typename T, bool kW4>
+template <bool kGemm1, int kN, typename T, bool kW4, bool kBal = false>
 cudaError_t launch_typed(const GemmCall& c, const KParams& kp, int grid, cudaStream_t s,
                          bool pdl) {
   using C = Cfg<kGemm1, kN, kW4>;
@@ -860,7 +863,7 @@ cudaError_t launch_typed(const GemmCall& c, const KParams& kp, int grid, cudaStr
       !make_map(&tmB128, c.dtype, c.b, (uint64_t)c.K, (uint64_t)c.b_rows, 128))
     return cudaErrorInvalidValue;
   if (kW4) tmW = tmB;
-  auto kern = moe_gemm_kernel<kGemm1, kN, T, kW4>;
+  auto kern = moe_gemm_kernel<kGemm1, kN, T, kW4, kBal>;
   static bool attr_set = false;  // one per instantiation: set once per process
   if (!attr_set) {
     cudaError_t e =
@@ -872,15 +875,23 @@ cudaError_t launch_typed(const GemmCall& c, const KParams& kp, int grid, cudaStr
                   tmB128, kp);
 }
 
+// Decode-sized launch: sorted or direct units of experts that average at most 64 routed rows.
+bool decode_sized(const GemmCall& c) {
+  if (c.P <= 0 || (c.mode != kSorted && c.mode != kDirect)) return false;
+  const int64_t active = c.P < c.E ? c.P : c.E;
+  return (int64_t)c.P / active <= 64;
+}
+
 template <bool kGemm1, typename T>
 cudaError_t launch_rows(const GemmCall& c, const KParams& kp, int grid, cudaStream_t s,
                         bool pdl) {
   if (c.w4) return launch_typed<kGemm1, 128, __nv_bfloat16, true>(c, kp, grid, s, pdl);
-  if constexpr (!kGemm1) {
-    if (c.tile_rows == 64) return launch_typed<false, 64, T, false>(c, kp, grid, s, pdl);
+  if constexpr (!kGemm1) {  // 64-row tiles are decode tiles: balanced
+    if (c.tile_rows == 64) return launch_typed<false, 64, T, false, true>(c, kp, grid, s, pdl);
   }
-  return c.tile_rows == 256 ? launch_typed<kGemm1, 256, T, false>(c, kp, grid, s, pdl)
-                            : launch_typed<kGemm1, 128, T, false>(c, kp, grid, s, pdl);
+  if (c.tile_rows == 256) return launch_typed<kGemm1, 256, T, false>(c, kp, grid, s, pdl);
+  return decode_sized(c) ? launch_typed<kGemm1, 128, T, false, true>(c, kp, grid, s, pdl)
+                         : launch_typed<kGemm1, 128, T, false>(c, kp, grid, s, pdl);
 }
 
 }  // namespace
