@@ -749,14 +749,19 @@ moe_status_t moe_grouped_gemm_fp8(const moe_grouped_gemm_t* g, const uint8_t* a,
   cudaStream_t s = (cudaStream_t)stream;
   void* ws = workspace;
   Tile* tiles = at<Tile>(ws, kHeaderBytes);
-  MOE_TRY(launch_build_tiles_meta(g->E, g->max_m, rows, layout_metadata, tiles, tile_counter(ws),
-                                  kTileRows, status_word(ws), s, false));
+  // Up to 128 groups the GEMM derives its tile list from the metadata itself (one launch);
+  // beyond, the tile-list kernel writes it first.
+  const bool own_tiles = g->E <= 128;
+  if (!own_tiles)
+    MOE_TRY(launch_build_tiles_meta(g->E, g->max_m, rows, layout_metadata, tiles,
+                                    tile_counter(ws), kTileRows, status_word(ws), s, false));
   // the tallest tile: a group's rows, at most max_m (masked) or all rows (contiguous), and 128
   const int64_t tall = g->max_m > 0 ? g->max_m : rows;
   return from_cuda(launch_gemm_fp8(g->E, g->N, g->K, rows,
                                    (int)(tall < kTileRows ? tall : kTileRows), a, a_scale, b,
                                    b_scale, tiles, tile_counter(ws),
                                    (int)grouped_gemm_max_tiles(g),
+                                   own_tiles ? layout_metadata : nullptr, g->max_m,
                                    static_cast<__nv_bfloat16*>(out), status_word(ws), s, true));
 }
 

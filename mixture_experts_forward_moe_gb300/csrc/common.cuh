@@ -141,11 +141,13 @@ cudaError_t launch_post_permute(int dtype, int T, int K, int H, const void* rows
 
 // FP8 (E4M3) block-scaled grouped GEMM (gemm_fp8.cu); out is bf16 [rows, N].
 // max_tile_rows bounds the rows of any tile of the layout (it sizes the token stages).
+// With `meta` (E <= 128 groups) the kernel derives the tile list itself from the layout
+// metadata (max_m > 0: masked counts; 0: inclusive prefix sums) and `tiles` is not read.
 cudaError_t launch_gemm_fp8(int E, int N, int K, int64_t rows, int max_tile_rows,
                             const uint8_t* a, const float* a_scale, const uint8_t* b,
                             const float* b_scale, const Tile* tiles, const int* n_tiles,
-                            int max_tiles, __nv_bfloat16* out, int* status, cudaStream_t s,
-                            bool pdl);
+                            int max_tiles, const int32_t* meta, int max_m,
+                            __nv_bfloat16* out, int* status, cudaStream_t s, bool pdl);
 
 // Activation code of the single-projection GEMM that writes the product itself (the plain
 // grouped GEMM); not a moe_activation_t a caller can pass.

@@ -67,6 +67,12 @@ struct F8Params {
   int nbuf;          // TMEM buffers (KPS * tcap columns each), <= stages
   const Tile* tiles;
   const int* n_tiles;
+  // With `meta`, the tile list is not read from `tiles` but derived in the prologue from the
+  // layout metadata (at most kF8FusedGroups groups): masked (max_m > 0) counts, or contiguous
+  // (max_m == 0) inclusive prefix sums over `rows` rows.
+  const int32_t* meta;
+  int E, max_m;
+  long long rows;
   const float* a_scale;  // [rows, num_kb]
   const float* b_scale;  // [E, n_slabs, num_kb]
   __nv_bfloat16* out;    // [rows, N]
@@ -78,16 +84,44 @@ struct F8Unit {
   int e, slab, row0, nrows, n_mma;
 };
 
+// Groups a launch can take its tile list from directly (shared-memory tables below).
+constexpr int kF8FusedGroups = 128;
+
+// The groups as the prologue tabulates them: tile g of the list belongs to the group e with
+// tfirst[e] <= g < tfirst[e + 1]; its rows start at row0[e] + 128 * (g - tfirst[e]).
+struct F8Groups {
+  const int* tfirst;  // [E + 1]
+  const int* row0;    // [E]
+  const int* cnt;     // [E]
+  int E;
+};
+
 // Units of group e occupy [n_slabs*first, n_slabs*(first+count)), slab-major (as in gemm.cu).
-__device__ __forceinline__ void f8_unit(const F8Params& p, int u, F8Unit& U) {
-  const Tile owner = p.tiles[u / p.n_slabs];
-  const int local = u - p.n_slabs * owner.first;
-  U.slab = local / owner.count;
-  const Tile t = p.tiles[owner.first + local % owner.count];
-  U.e = t.e;
-  U.row0 = t.row0;
-  U.nrows = t.nrows;
-  U.n_mma = (t.nrows + 15) & ~15;
+// `cur` is the caller's group cursor: a CTA visits its units in increasing order, so the owning
+// group (the last whose first tile is <= the unit's tile) is found by stepping it forward.
+__device__ __forceinline__ void f8_unit(const F8Params& p, const F8Groups& gr, int u, int& cur,
+                                        F8Unit& U) {
+  if (p.meta != nullptr) {
+    const int ti = u / p.n_slabs;
+    while (cur + 1 < gr.E && gr.tfirst[cur + 1] <= ti) ++cur;
+    const int lo = cur;
+    const int first = gr.tfirst[lo], count = gr.tfirst[lo + 1] - first;
+    const int local = u - p.n_slabs * first;
+    const int j = local % count;
+    U.slab = local / count;
+    U.e = lo;
+    U.row0 = gr.row0[lo] + j * kTileRows;
+    U.nrows = min(kTileRows, gr.cnt[lo] - j * kTileRows);
+  } else {
+    const Tile owner = p.tiles[u / p.n_slabs];
+    const int local = u - p.n_slabs * owner.first;
+    U.slab = local / owner.count;
+    const Tile t = p.tiles[owner.first + local % owner.count];
+    U.e = t.e;
+    U.row0 = t.row0;
+    U.nrows = t.nrows;
+  }
+  U.n_mma = (U.nrows + 15) & ~15;
 }
 
 __device__ __forceinline__ void f8_wait_drain(uint64_t* bar, uint32_t parity) {
@@ -110,6 +144,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
   __shared__ int s_n_units;
+  __shared__ int s_tfirst[kF8FusedGroups + 1], s_row0[kF8FusedGroups], s_cnt[kF8FusedGroups];
   __shared__ __align__(16) float s_sa[2][2][kTileRows];  // column scales of a stage's k blocks
 
   const uint32_t raw = smem_u32(dsmem);
@@ -140,12 +175,60 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   }
   pdl_wait();
   pdl_trigger();
-  if (threadIdx.x == 0) s_n_units = (*p.n_tiles) * p.n_slabs;
+  if (p.meta == nullptr) {
+    if (threadIdx.x == 0) s_n_units = (*p.n_tiles) * p.n_slabs;
+  } else if (warp == 0) {
+    // The tile list from the layout metadata: lane l tabulates groups 4l .. 4l+3 (rows and
+    // 128-row tiles), a warp scan gives each group's first tile.  As in the tile-list kernel,
+    // a contiguous prefix sum that decreases or passes `rows` sets MOE_ERR_INVALID_ARG and
+    // drops its group.
+    int nt[4], tot = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = lane * 4 + i;
+      int r0 = 0, c = 0;
+      if (e < p.E) {
+        if (p.max_m > 0) {
+          r0 = e * p.max_m;
+          c = min(max(p.meta[e], 0), p.max_m);
+        } else {
+          r0 = e == 0 ? 0 : p.meta[e - 1];
+          c = p.meta[e] - r0;
+          if (r0 < 0 || c < 0 || (long long)p.meta[e] > p.rows) {
+            if (p.status) atomicCAS(p.status, 0, (int)MOE_ERR_INVALID_ARG);
+            c = 0;
+          }
+        }
+        s_row0[e] = r0;
+        s_cnt[e] = c;
+      }
+      nt[i] = (c + kTileRows - 1) / kTileRows;
+      tot += nt[i];
+    }
+    int incl = tot;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    int run = incl - tot;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = lane * 4 + i;
+      if (e < p.E) s_tfirst[e] = run;
+      run += nt[i];
+    }
+    if (lane == 31) {
+      s_tfirst[p.E] = incl;
+      s_n_units = incl * p.n_slabs;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
   const int n_units = s_n_units;
+  const F8Groups gr{s_tfirst, s_row0, s_cnt, p.E};
   const int tblk = p.tcap * kF8BlockK;  // bytes of one k block of token rows
 
   if (warp < 4) {  // warpgroup 0: producer and MMA issuer
@@ -156,9 +239,10 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         int stage = 0, issued = 0;
         uint32_t phase = 0;
         bool ok = true;
+        int gcur = 0;  // group cursor (tile list from the metadata)
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
           F8Unit U;
-          f8_unit(p, u, U);
+          f8_unit(p, gr, u, gcur, U);
           const int wrow = U.e * p.N + U.slab * kSlab;
           for (int kb = 0; kb < p.num_kb; kb += KPS) {
             const int nk = p.num_kb - kb >= KPS ? KPS : 1;
@@ -204,9 +288,10 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         uint32_t phase = 0, pphase = 0;
         bool ok = true, issued_any = false;
         const uint32_t smem_base = smem_u32(smem);
+        int gcur = 0;  // group cursor (tile list from the metadata)
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
           F8Unit U;
-          f8_unit(p, u, U);
+          f8_unit(p, gr, u, gcur, U);
           const uint32_t idesc = idesc_e4m3_m128(U.n_mma);
           for (int kb = 0; kb < p.num_kb; kb += KPS) {
             const int nk = p.num_kb - kb >= KPS ? KPS : 1;
@@ -259,9 +344,10 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     int stage = 0, pb = 0, sc = 0;
     uint32_t phase = 0, pphase = 0;
     bool ok = true;
+    int gcur = 0;  // group cursor (tile list from the metadata)
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       F8Unit U;
-      f8_unit(p, u, U);
+      f8_unit(p, gr, u, gcur, U);
       float acc[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
@@ -375,8 +461,9 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 cudaError_t launch_gemm_fp8(int E, int N, int K, int64_t rows, int max_tile_rows,
                             const uint8_t* a, const float* a_scale, const uint8_t* b,
                             const float* b_scale, const Tile* tiles, const int* n_tiles,
-                            int max_tiles, __nv_bfloat16* out, int* status, cudaStream_t s,
-                            bool pdl) {
+                            int max_tiles, const int32_t* meta, int max_m,
+                            __nv_bfloat16* out, int* status, cudaStream_t s, bool pdl) {
+  if (meta != nullptr && E > kF8FusedGroups) return cudaErrorInvalidValue;
   if (N % kSlab != 0 || K % kF8BlockK != 0 || rows <= 0) return cudaErrorInvalidValue;
   CUtensorMap tmW, tmB16, tmB64, tmB128;
   if (!make_map_bytes(&tmW, b, (uint64_t)K, (uint64_t)E * N, kF8BlockK, kSlab) ||
@@ -400,6 +487,10 @@ cudaError_t launch_gemm_fp8(int E, int N, int K, int64_t rows, int max_tile_rows
   if (p.nbuf > p.stages) p.nbuf = p.stages;  // the epilogue never falls a full ring behind
   p.tiles = tiles;
   p.n_tiles = n_tiles;
+  p.meta = meta;
+  p.E = E;
+  p.max_m = max_m;
+  p.rows = rows;
   p.a_scale = a_scale;
   p.b_scale = b_scale;
   p.out = out;

@@ -62,6 +62,36 @@ def test_fp8_grouped_gemm_is_deterministic(cuda_device):
     assert torch.equal(outs[0], outs[1])
 
 
+def test_fp8_many_groups_take_the_tile_list_kernel(cuda_device):
+    """Past 128 groups the tile list comes from the tile-list kernel instead of the GEMM's own
+    prologue: 130 groups of up to 3 rows, every valid row compared."""
+    w = inputs.Fp8GemmWorkload("t", E=130, max_m=16, K=256, N=128, total=200)
+    d = inputs.generate_fp8_gemm(w, seed=4, device=cuda_device)
+    out = B.moe_grouped_gemm_fp8(d["a"], d["a_scale"], d["b"], d["b_scale"], d["meta"])
+    torch.cuda.synchronize()
+    meta = d["meta"].cpu().numpy()
+    ref = oracle.grouped_gemm_fp8(d["a"].cpu(), d["a_scale"].cpu(), d["b"].cpu(),
+                                  d["b_scale"].cpu(), meta, max_m=w.max_m)
+    live = np.concatenate([np.arange(e * w.max_m, e * w.max_m + int(meta[e]))
+                           for e in range(w.E)])
+    got = out.reshape(w.E * w.max_m, w.N)[torch.from_numpy(live).to(cuda_device)]
+    assert_rounded_close(got, ref[live], torch.bfloat16, what="fp8 masked E=130")
+
+
+def test_fp8_reports_a_bad_prefix_sum(cuda_device):
+    """A contiguous layout whose prefix sums decrease: the group is dropped and the status word
+    says MOE_ERR_INVALID_ARG."""
+    w = inputs.Fp8GemmWorkload("t", E=3, max_m=32, K=128, N=128, total=48)
+    d = inputs.generate_fp8_gemm(w, seed=6, device=cuda_device)
+    a = d["a"].reshape(-1, w.K)[:32].contiguous()
+    sa = d["a_scale"].reshape(-1, w.K // 128)[:32].contiguous()
+    meta = torch.tensor([10, 5, 32], dtype=torch.int32, device=cuda_device)  # decreasing
+    g = B.GroupedGemm(w.E, w.N, w.K, 0, 32, B.MOE_BF16, 0, 0)
+    ws = B.new_workspace(B.lib().moe_grouped_gemm_workspace_size(B.ctypes.byref(g)), cuda_device)
+    B.moe_grouped_gemm_fp8(a, sa, d["b"], d["b_scale"], meta, workspace=ws)
+    assert B.get_device_status(ws) == B.MOE_ERR_INVALID_ARG
+
+
 FULL = ["ds-v3-e8-up-masked", "ds-v3-dec-b64-down", "qwen3-235b-dec-b256-up",
         "kimi-k2-dec-b64-up"]
 
