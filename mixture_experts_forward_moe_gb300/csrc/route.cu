@@ -81,7 +81,39 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 
   // Grouped selection: group g = experts [g*E/G, (g+1)*E/G); score = sum of its two largest
   // keys; keep the keepG best groups (ties -> lower group id); exclude the rest.
-  if (G > 1 && keepG < G) {
+  if (G > 1 && keepG < G && E == 32 * VPL && G == VPL) {
+    // Groups of exactly 32 experts (DeepSeek-V3: 256 in 8): lane value i belongs to group i.
+    // All G top-2 reductions run interleaved, every lane ends with every group's score, and
+    // each lane ranks the groups itself (no shared memory, no serial selection).
+    float m1[VPL], m2[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      m1[i] = key[i];
+      m2[i] = -INFINITY;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const float o1 = __shfl_xor_sync(kFull, m1[i], off);
+        const float o2 = __shfl_xor_sync(kFull, m2[i], off);
+        const float hi = fmaxf(m1[i], o1);
+        const float lo = fmaxf(fminf(m1[i], o1), fmaxf(m2[i], o2));
+        m1[i] = hi;
+        m2[i] = lo;
+      }
+    }
+    float gs[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) gs[i] = __fadd_rn(m1[i], m2[i]);
+#pragma unroll
+    for (int g = 0; g < VPL; ++g) {
+      int rank = 0;  // groups that rank before g (larger score, ties -> lower group id)
+#pragma unroll
+      for (int h = 0; h < VPL; ++h) rank += (h != g && before(gs[h], h, gs[g], g)) ? 1 : 0;
+      if (rank >= keepG) live[g] = false;
+    }
+  } else if (G > 1 && keepG < G) {
     const int gsz = E / G;
     int gi[VPL];  // group of each of this lane's experts (-1 past E)
 #pragma unroll
@@ -137,38 +169,98 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   // top_k rounds of warp argmax; lane j keeps the j-th selection.
   int my_e = -1;
   float my_v = 0.0f;
-  for (int j = 0; j < K; ++j) {
-    float bk = -INFINITY;
-    int be = INT_MAX;
+  if constexpr (VPL <= 4) {
+    // Each lane first sorts its candidates (best first; dead ones last), so a round compares
+    // only the lanes' heads and the winning lane shifts its list down by one.  (Measured: at 8
+    // values a lane its registers left the 4096-token grid a second wave, and at 12 the
+    // unrolled insertion sort cost more than rescanning.)
+    float hk[VPL], hs[VPL];
+    int he[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
-      const int e = lane + 32 * i;
-      if (live[i] && (be == INT_MAX || before(key[i], e, bk, be))) {
-        bk = key[i];
-        be = e;
-      }
+      hk[i] = live[i] ? key[i] : -INFINITY;
+      he[i] = live[i] ? lane + 32 * i : INT_MAX;
+      hs[i] = sc[i];
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ok = __shfl_xor_sync(kFull, bk, off);
-      const int oe = __shfl_xor_sync(kFull, be, off);
-      if (before(ok, oe, bk, be)) {
-        bk = ok;
-        be = oe;
-      }
-    }
-    float cand = 0.0f;
+    for (int i = 1; i < VPL; ++i) {  // insertion sort, fully unrolled (registers only)
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      if (lane + 32 * i == be) {
-        live[i] = false;
-        cand = sc[i];
+      for (int j = i; j > 0; --j) {
+        if (before(hk[j], he[j], hk[j - 1], he[j - 1])) {
+          const float tk = hk[j], ts = hs[j];
+          const int te = he[j];
+          hk[j] = hk[j - 1];
+          he[j] = he[j - 1];
+          hs[j] = hs[j - 1];
+          hk[j - 1] = tk;
+          he[j - 1] = te;
+          hs[j - 1] = ts;
+        }
       }
     }
-    const float v = __shfl_sync(kFull, cand, be & 31);
-    if (lane == j) {
-      my_e = be;
-      my_v = v;
+    for (int j = 0; j < K; ++j) {
+      float bk = hk[0];
+      int be = he[0];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ok = __shfl_xor_sync(kFull, bk, off);
+        const int oe = __shfl_xor_sync(kFull, be, off);
+        if (before(ok, oe, bk, be)) {
+          bk = ok;
+          be = oe;
+        }
+      }
+      const int wl = be & 31;  // the winning lane holds expert be at its head
+      const float v = __shfl_sync(kFull, hs[0], wl);
+      if (lane == wl) {
+#pragma unroll
+        for (int i = 0; i + 1 < VPL; ++i) {
+          hk[i] = hk[i + 1];
+          he[i] = he[i + 1];
+          hs[i] = hs[i + 1];
+        }
+        hk[VPL - 1] = -INFINITY;
+        he[VPL - 1] = INT_MAX;
+      }
+      if (lane == j) {
+        my_e = be;
+        my_v = v;
+      }
+    }
+  } else {
+    for (int j = 0; j < K; ++j) {
+      float bk = -INFINITY;
+      int be = INT_MAX;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        if (live[i] && (be == INT_MAX || before(key[i], e, bk, be))) {
+          bk = key[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ok = __shfl_xor_sync(kFull, bk, off);
+        const int oe = __shfl_xor_sync(kFull, be, off);
+        if (before(ok, oe, bk, be)) {
+          bk = ok;
+          be = oe;
+        }
+      }
+      float cand = 0.0f;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        if (lane + 32 * i == be) {
+          live[i] = false;
+          cand = sc[i];
+        }
+      }
+      const float v = __shfl_sync(kFull, cand, be & 31);
+      if (lane == j) {
+        my_e = be;
+        my_v = v;
+      }
     }
   }
 
