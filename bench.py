@@ -336,8 +336,10 @@ def run_ours(args, w, ws_n, rank, local):
         kw.update(shared_w_gate_up=d["shared_w_gate_up"], shared_w_down=d["shared_w_down"])
     fwd = B.fused_moe_fwd_w4a16 if w4 else B.fused_moe_fwd
     prob = B.make_problem(w.T, w.H, w.E, w.F, w.top_k, w.dtype, w.scoring_func, w.renormalize,
-                          w.num_expert_group, w.topk_group, w.routed_scaling_factor, w.S)
-    wsp = B.new_workspace(B.workspace_size(prob), dev)
+                          w.num_expert_group, w.topk_group, w.routed_scaling_factor, w.S,
+                          w.activation, w.ep_local, w.ep_offset)
+    # the W4A16 path also takes the gate/up GEMM's split-K scratch
+    wsp = B.new_workspace(B.workspace_size_w4a16(prob) if w4 else B.workspace_size(prob), dev)
     out = torch.empty((w.T, w.H), dtype=w.dtype, device=dev)
     stream = torch.cuda.current_stream()
 

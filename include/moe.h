@@ -101,6 +101,15 @@ typedef struct {
  * with block_m = 1 (see moe_stage_workspace_size for other alignments). */
 size_t moe_workspace_size(const moe_problem_t* p);
 
+/* Bytes of workspace fused_moe_fwd_w4a16 can use for problem p (0 if p is invalid): those of
+ * moe_workspace_size(p), plus, for T <= 64, scratch that lets the NVFP4 gate/up GEMM split
+ * each unit's K range over two CTAs when that shortens its last wave (a per-unit counter and
+ * two halves of f32 partial accumulators: 2048 * round16(T) bytes per unit, at most 1024
+ * units of 128 gate/up rows).  Given only moe_workspace_size(p) bytes, fused_moe_fwd_w4a16
+ * runs unsplit; the results agree to f32 rounding either way, and each setting is
+ * deterministic. */
+size_t moe_workspace_size_w4a16(const moe_problem_t* p);
+
 /* Slots of sorted_ids (and rows of the sorted intermediate buffers) moe_align_sort may use for
  * alignment block_m: T*top_k + E*(block_m-1).  -1 if the arguments are invalid. */
 int64_t moe_sorted_capacity(const moe_problem_t* p, int32_t block_m);

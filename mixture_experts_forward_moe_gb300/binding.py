@@ -33,7 +33,8 @@ def gate_up_rows(activation: str, F: int) -> int:
 
 # Every symbol include/moe.h declares.
 EXPORTED = (
-    "moe_workspace_size", "moe_sorted_capacity", "moe_stage_workspace_size",
+    "moe_workspace_size", "moe_workspace_size_w4a16", "moe_sorted_capacity",
+    "moe_stage_workspace_size",
     "moe_workspace_init", "fused_moe_fwd", "moe_route", "moe_align_sort", "moe_gemm1_swiglu",
     "moe_gemm2", "moe_combine", "moe_shared_expert_fwd", "moe_get_device_status",
     "moe_status_string", "moe_set_wait_limit_ns", "moe_stage_name", "moe_profile_enable",
@@ -90,6 +91,8 @@ def lib():
             PP = ctypes.POINTER(MoeProblem)
             L.moe_workspace_size.restype = sz
             L.moe_workspace_size.argtypes = [PP]
+            L.moe_workspace_size_w4a16.restype = sz
+            L.moe_workspace_size_w4a16.argtypes = [PP]
             L.moe_sorted_capacity.restype = i64
             L.moe_sorted_capacity.argtypes = [PP, i32]
             L.moe_stage_workspace_size.restype = sz
@@ -193,6 +196,13 @@ def workspace_size(prob: MoeProblem) -> int:
     if n == 0:
         raise MoeError(MOE_ERR_INVALID_ARG, "moe_workspace_size")
     return int(n)
+
+
+def workspace_size_w4a16(prob: MoeProblem) -> int:
+    n = lib().moe_workspace_size_w4a16(ctypes.byref(prob))
+    if n == 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, "moe_workspace_size_w4a16")
+    return n
 
 
 def stage_workspace_size(prob: MoeProblem, block_m: int) -> int:
@@ -549,7 +559,7 @@ def fused_moe_fwd_w4a16(hidden_states, gating_output, w_gate_up, w_down, top_k, 
     prob = make_problem(T, H, E, F, top_k, dt, scoring_func, renormalize, num_expert_group,
                         topk_group, routed_scaling_factor, 0, activation,
                         E_l if E_l != E else 0, ep_local_offset)
-    nbytes = workspace_size(prob)
+    nbytes = workspace_size_w4a16(prob)
     if workspace is None:
         workspace = _workspace(nbytes, hidden_states.device)
     if out is None:

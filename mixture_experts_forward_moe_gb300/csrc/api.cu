@@ -168,6 +168,33 @@ Layout make_layout(const moe_problem_t& p, int block_m) {
   return L;
 }
 
+// Split-K scratch of the NVFP4 gate/up GEMM in fused_moe_fwd_w4a16 (token rows, T <= 64),
+// placed after the common layout: a counter per unit, then per unit two halves of f32 partial
+// accumulators (gate and up, round16(T) columns of 128 rows each), for up to kSplitMaxUnits
+// units.  Its bytes are what moe_workspace_size_w4a16 adds; with a smaller workspace the GEMM
+// runs unsplit.
+constexpr int64_t kSplitMaxUnits = 1024;
+constexpr int kSplitMaxT = 64;
+
+struct SplitLayout {
+  int64_t units, cols;
+  size_t cnt, part, total;  // offsets from the start of the scratch, and its bytes
+};
+
+SplitLayout split_layout(const moe_problem_t& lp) {  // lp: the local view of the problem
+  SplitLayout S{0, 0, 0, 0, 0};
+  if (lp.T <= 0 || lp.T > kSplitMaxT || !fused_sort_fits(lp) || lp.F % kSlab != 0) return S;
+  const int64_t P = (int64_t)lp.T * lp.top_k;
+  const int64_t active = P < lp.E ? P : lp.E;  // one tile per active expert over token rows
+  const int64_t units = active * (lp.F / kSlab);
+  S.units = units < kSplitMaxUnits ? units : kSplitMaxUnits;
+  S.cols = (lp.T + 15) & ~15;
+  S.cnt = 0;
+  S.part = align_up(sizeof(int) * (size_t)S.units, 256);
+  S.total = S.part + (size_t)S.units * 2 * 2 * (size_t)S.cols * kSlab * sizeof(float);
+  return S;
+}
+
 template <typename P>
 P* at(void* ws, size_t off) {
   return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
@@ -265,6 +292,11 @@ extern "C" {
 size_t moe_workspace_size(const moe_problem_t* p) {
   if (check_problem(p) != MOE_OK) return 0;
   return make_layout(*p, 1).total;
+}
+
+size_t moe_workspace_size_w4a16(const moe_problem_t* p) {
+  if (check_problem(p) != MOE_OK) return 0;
+  return make_layout(*p, 1).total + split_layout(local_view(*p)).total;
 }
 
 size_t moe_stage_workspace_size(const moe_problem_t* p, int32_t block_m) {
@@ -377,11 +409,20 @@ moe_status_t run_fused(const moe_problem_t* p, const Experts& X, const void* hid
     Tile* tiles = at<Tile>(ws, L.tiles);    // gemm1: 128-row tiles
     Tile* tiles2 = at<Tile>(ws, L.tiles2);  // gemm2: tile_rows2-row tiles
     const int tile_rows2 = X.w4 ? kTileRows : sorted_tile_rows(P);
-    if (fused_sort_fits(P)) {  // sort and both tile lists in one launch
+    // With T <= 128 every expert's rows fit one tile of all T tokens: gemm1 reads hidden_states
+    // directly and no gathered copy is made.
+    const bool token_rows = P.T <= kTileRows;
+    SplitLayout S{0, 0, 0, 0, 0};
+    if (X.w4 && token_rows) {
+      S = split_layout(P);
+      if (S.total == 0 || workspace_bytes < L.total + S.total) S.units = 0;
+    }
+    int* split_cnt = S.units ? at<int>(ws, L.total + S.cnt) : nullptr;
+    if (fused_sort_fits(P)) {  // sort and both tile lists in one launch (and split counters)
       StageTimer t(kSort, s);
       MOE_TRY(launch_sort_fused(P, 1, ids, counts, offsets, sorted, L.cap, nullptr, inv_route,
                                 tiles, tile_counter(ws), kTileRows, tiles2, tile_counter2(ws),
-                                tile_rows2, status, s, true));
+                                tile_rows2, status, s, true, split_cnt, (int)S.units));
       t.done(1);
     } else {
       StageTimer t(kSort, s);
@@ -391,9 +432,6 @@ moe_status_t run_fused(const moe_problem_t* p, const Experts& X, const void* hid
                                         tile_counter2(ws), tile_rows2));
       t.done(3);
     }
-    // With T <= 128 every expert's rows fit one tile of all T tokens: gemm1 reads hidden_states
-    // directly and no gathered copy is made.
-    const bool token_rows = P.T <= kTileRows;
     if (!token_rows) {
       StageTimer t(kPermute, s);
       MOE_TRY(launch_permute(P.dtype, P.top_k, P.H, hidden_states, sorted, offsets, P.E, L.cap,
@@ -416,12 +454,21 @@ moe_status_t run_fused(const moe_problem_t* p, const Experts& X, const void* hid
     g1.max_tiles = (int)L.max_tiles;
     g1.tile_rows = kTileRows;
     g1.early_tiles = token_rows ? 0 : 1;  // sort, then permute, then gemm1
+    if (split_cnt) {
+      g1.split_cap = (int)S.units;
+      g1.split_cols = (int)S.cols;
+      g1.split_part = at<float>(ws, L.total + S.part);
+      g1.split_cnt = split_cnt;
+    }
     {
       StageTimer t(kGemm1, s);
       MOE_TRY(launch_gemm(g1, s, true));
       t.done(1);
     }
     GemmCall g2 = g1;
+    g2.split_cap = 0;
+    g2.split_part = nullptr;
+    g2.split_cnt = nullptr;
     g2.gemm1 = 0;
     g2.token_rows = 0;
     g2.b_rows = L.cap;

@@ -107,13 +107,15 @@ cudaError_t launch_align_sort(const moe_problem_t& p, int block_m, const int32_t
                               int32_t* chunk_scratch, int* status, cudaStream_t s, bool pdl);
 
 // The sort in one launch (one CTA) when it fits (T*top_k <= 8192); with `tiles` (`tiles2`)
-// it also writes the GEMM tile list of tile_rows (tile_rows2) rows per tile.
+// it also writes the GEMM tile list of tile_rows (tile_rows2) rows per tile, and it zeroes
+// zero[0, n_zero) (the split-K counters of the GEMM that follows).
 bool fused_sort_fits(const moe_problem_t& p);
 cudaError_t launch_sort_fused(const moe_problem_t& p, int block_m, const int32_t* ids,
                               int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
                               int64_t cap, int32_t* tile_expert, int32_t* inv_route, Tile* tiles,
                               int* n_tiles, int tile_rows, Tile* tiles2, int* n_tiles2,
-                              int tile_rows2, int* status, cudaStream_t s, bool pdl);
+                              int tile_rows2, int* status, cudaStream_t s, bool pdl,
+                              int* zero = nullptr, int n_zero = 0);
 // The sort as three launches over 256-route chunks (any size), using chunk_scratch
 // (ceil(T*top_k/256) * E int32); with `tiles` (`tiles2`) the scan also writes the GEMM tile
 // lists.
@@ -198,6 +200,15 @@ struct GemmCall {
   // sorted mode: the tile list was written at least two launches before this GEMM, so the
   // kernel may read it (and prefetch its first units' weights) before its dependency wait
   int early_tiles;
+  // NVFP4 gate/up GEMM over token rows: when it shortens the last wave, each unit's K range is
+  // split in two halves run by different CTAs.  Both store their f32 accumulators in
+  // split_part (split_cols columns per accumulator); the half that finishes second, told by
+  // split_cnt[unit] (zeroed before the launch), adds the other's and writes the output.  Only
+  // when the units number at most split_cap (0: never).
+  int split_cap;
+  int split_cols;
+  float* split_part;
+  int* split_cnt;
   int* status;
 };
 

@@ -70,14 +70,17 @@ namespace {
 // 64-row token tiles (the down projection at decode sizes): a stage carries two 64-k blocks
 // (kKps = 2), so the MMA issuer pays one barrier wait and one commit per 32 KB of weights
 // instead of per 16 KB; at a few tokens per expert those per-stage costs, not HBM, would
-// otherwise set the pace.
+// otherwise set the pace.  The NVFP4 gate/up GEMM over at most 64 token rows uses 64-row tiles
+// for another reason: its gate and up accumulators then take 128 TMEM columns, so two
+// accumulator buffers fit beside the decoded-weight ring and a unit's epilogue overlaps the
+// next unit's MMAs (at 128 rows there is room for one).
 template <bool kGemm1, int kN, bool kW4 = false>
 struct Cfg {
   static_assert(kN == 64 || kN == 128 || kN == 256, "tile rows");
-  static_assert(kN != 64 || (!kGemm1 && !kW4), "64-row tiles: 16-bit down projection only");
-  static_assert(!kW4 || kN == 128, "NVFP4 tiles are 128 token rows");
+  static_assert(kN != 64 || kGemm1 == kW4, "64-row tiles: 16-bit down proj. or NVFP4 gate/up");
+  static_assert(!kW4 || kN == 128 || (kN == 64 && kGemm1), "NVFP4 tiles are 128 (64) rows");
   static constexpr int kSlabs = kGemm1 ? 2 : 1;
-  static constexpr int kKps = kN == 64 ? 2 : 1;  // 64-k blocks per stage (16-bit weights)
+  static constexpr int kKps = (kN == 64 && !kW4) ? 2 : 1;  // 64-k blocks per stage (16-bit)
   static constexpr int kStageK = kW4 ? 128 : kBlockK * kKps;  // k per pipeline stage
   static constexpr int kStages = kGemm1 ? (kN == 128 ? 4 : 3) : (kN == 64 ? 4 : (kN == 128 ? 7 : 4));
   static constexpr int kASubBytes = kSlabs * kSlab * kBlockK * 2;  // weights of one 64-k block
@@ -99,7 +102,8 @@ struct Cfg {
   static constexpr int kPassCols = 64;
   static constexpr int kStagingBytes = kGemm1 ? kPassCols * kSlab * 2 : 0;
   static constexpr int kAccCols = kGemm1 ? 2 * kN : kN;  // per accumulator buffer
-  static constexpr int kAccBufs = kW4 ? (kGemm1 ? 1 : 2) : ((kGemm1 && kN == 256) ? 1 : 2);
+  static constexpr int kAccBufs =
+      kW4 ? ((kGemm1 && kN == 128) ? 1 : 2) : ((kGemm1 && kN == 256) ? 1 : 2);
   static constexpr int kABase = kAccBufs * kAccCols;  // first TMEM ring column
   static constexpr int kASlotCols = kSlabs * 32;      // 64 k of every slab
   static constexpr int kAStages = kW4 ? (512 - kABase) / kASlotCols : 1;
@@ -135,6 +139,10 @@ struct KParams {
   // tile list was written at least two launches earlier (it is then complete when this kernel
   // starts).
   int prefetch_steps;
+  // NVFP4 gate/up GEMM: split-K in two halves when it shortens the last wave (GemmCall).
+  int split_cap, split_cols;
+  float* split_part;
+  int* split_cnt;
   void* out;
   int* status;
   uint64_t limit_ns;
@@ -142,8 +150,10 @@ struct KParams {
 
 struct Unit {
   int e, row0, nrows, n_mma, slab;
-  int b_row0;  // first token-side row the unit loads
-  bool two;    // gemm1: the second weight tile is used (always when gated)
+  int b_row0;    // first token-side row the unit loads
+  bool two;      // gemm1: the second weight tile is used (always when gated)
+  int kb0, kb1;  // K steps [kb0, kb1) of this piece of work
+  int part;      // split-K: index of this half's partial accumulators (-1: no split)
 };
 
 __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
@@ -193,6 +203,41 @@ __device__ __forceinline__ bool decode_unit(const KParams& p, int u, Unit& U) {
   return U.nrows > 0;
 }
 
+// Work item u of ks per unit (ks = 2: split-K; item 2v runs K steps [0, num_kb/2) of unit v and
+// item 2v+1 the rest).
+template <bool kGemm1, int kN>
+__device__ __forceinline__ bool decode_item(const KParams& p, int u, int ks, Unit& U) {
+  const bool split = ks == 2;
+  if (!decode_unit<kGemm1, kN>(p, split ? (u >> 1) : u, U)) return false;
+  U.kb0 = 0;
+  U.kb1 = p.num_kb;
+  U.part = -1;
+  if (split) {
+    const int mid = p.num_kb >> 1;
+    if (u & 1)
+      U.kb0 = mid;
+    else
+      U.kb1 = mid;
+    U.part = u;
+  }
+  return true;
+}
+
+// Split-K cost model of the NVFP4 gate/up GEMM over at most 64 token rows, in K steps per CTA:
+// a whole unit costs its num_kb steps plus kSplitWholeOver, a half its num_kb/2 plus
+// kSplitHalfOver (the extra epilogue and the exchange of partials), fitted to timings of both
+// forms on GB300 (DeepSeek-V3 EP8 shard, T = 32: 56 K steps a unit, 224 units on 152 SMs,
+// 135 us whole, 108 us split; Qwen3-30B-A3B, T = 32: 16 K steps, 660 units, where the model
+// keeps whole units).
+constexpr int kSplitWholeOver = 3;
+constexpr int kSplitHalfOver = 4;
+
+__host__ __device__ inline bool split_pays(int n, int ctas, int num_kb) {
+  if (n <= 0 || ctas <= 0 || num_kb < 2) return false;
+  const int whole = (n + ctas - 1) / ctas, halves = (2 * n + ctas - 1) / ctas;
+  return halves * (num_kb + 2 * kSplitHalfOver) < whole * (2 * num_kb + 2 * kSplitWholeOver);
+}
+
 // GELU, tanh form: g/2 * (1 + tanh(sqrt(2/pi) * (g + 0.044715 g^3))), in f32.
 __device__ __forceinline__ float gelu_tanh_f32(float g) {
   const float u = 0.7978845608028654f * (g + 0.044715f * g * g * g);
@@ -219,6 +264,9 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
                     const __grid_constant__ CUtensorMap tmB64,
                     const __grid_constant__ CUtensorMap tmB128, const KParams p) {
   using C = Cfg<kGemm1, kN, kW4>;
+  // Split-K is built into the NVFP4 gate/up kernel for at most 64 token rows only: the other
+  // kernels keep K loops with compile-time bounds.
+  constexpr bool kSplit = kW4 && kGemm1 && kN == 64;
   extern __shared__ uint8_t dsmem[];
   __shared__ __align__(8) uint64_t full_bar[C::kFullBars];   // NVFP4: the token ring
   __shared__ __align__(8) uint64_t empty_bar[C::kFullBars];
@@ -232,6 +280,8 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
   __shared__ int s_n_units;
+  __shared__ int s_ks;          // work items per unit (2: split-K)
+  __shared__ int s_split_last;  // epilogue: this half finished the unit second
   __shared__ int ent_col[kGemm1 ? kN : 1];
   __shared__ int ent_dst[kN];
   __shared__ float col_scale[kGemm1 ? 1 : kN];
@@ -308,13 +358,21 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       n = p.P * p.n_slabs;
     else
       n = ((p.dense_rows + kN - 1) / kN) * p.n_slabs;
-    s_n_units = n;
+    // NVFP4 gate/up: split every unit's K range in two when, by the cost model, the halves end
+    // the last wave sooner than whole units would (the MMA issue rate, not HBM, paces these
+    // kernels, so an SM left idle is time lost).
+    int ks = 1;
+    if (kSplit && p.split_cap > 0 && n <= p.split_cap && split_pays(n, gridDim.x, p.num_kb))
+      ks = 2;
+    s_ks = ks;
+    s_n_units = n * ks;
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
-  const int n_units = s_n_units;
+  const int n_units = s_n_units;       // work items
+  const int ks = kSplit ? s_ks : 1;
   // CTAs that take units (the stride) and this CTA's first unit.  At decode sizes (kBal) the
   // 16-bit weights stream at HBM speed, so the units are spread evenly over as few CTAs as keep
   // the per-CTA share.  Otherwise the loops read the stride from gridDim directly: held in a
@@ -336,12 +394,12 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       const int64_t slabs_per_expert = p.w_rows_per_expert / kSlab;
       for (int u = UNIT_FIRST; u < n_units && ok; u += UNIT_STRIDE) {
         Unit U;
-        if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
+        if (!decode_item<kGemm1, kN>(p, u, ks, U)) continue;
         const int n_w = U.two ? 2 : 1;
         const int64_t t0 = ((int64_t)U.e * slabs_per_expert + U.slab * p.slab_rows / kSlab) *
                            p.num_kb;
         const int64_t t1 = t0 + (int64_t)(p.second_off / kSlab) * p.num_kb;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = U.kb0; kb < U.kb1; ++kb) {
           if (!mbar_wait(&wempty_bar[ws], wph ^ 1u, abort_flag, p.limit_ns, p.status)) {
             ok = false;
             break;
@@ -374,8 +432,8 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       bool ok = true;
       for (int u = UNIT_FIRST; u < n_units && ok; u += UNIT_STRIDE) {
         Unit U;
-        if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        if (!decode_item<kGemm1, kN>(p, u, ks, U)) continue;
+        for (int kb = U.kb0; kb < U.kb1; ++kb) {
           if (!mbar_wait(&empty_bar[ts], tph ^ 1u, abort_flag, p.limit_ns, p.status)) {
             ok = false;
             break;
@@ -430,10 +488,10 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
     };
     for (int u = UNIT_FIRST; u < n_units && ok; u += UNIT_STRIDE) {
       Unit U;
-      if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
+      if (!decode_item<kGemm1, kN>(p, u, ks, U)) continue;
       const bool active = !kGemm1 || dg == 0 || U.two;
       const int slab = kGemm1 ? dg : 0;
-      for (int kb = 0; kb < p.num_kb; ++kb) {
+      for (int kb = U.kb0; kb < U.kb1; ++kb) {
         if (!mbar_wait(&wfull_bar[ws], wph, abort_flag, p.limit_ns, p.status)) {
           ok = false;
           break;
@@ -504,7 +562,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       bool ok = true;
       for (int u = UNIT_FIRST; u < n_units && ok; u += UNIT_STRIDE) {
         Unit U;
-        if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
+        if (!decode_item<kGemm1, kN>(p, u, ks, U)) continue;
         const uint32_t wbytes = U.two ? 2 * kSlab * kBlockK * 2 : kSlab * kBlockK * 2;
         const uint32_t bytes = wbytes + U.n_mma * kBlockK * 2;  // per 64-k block
         const int wrow = U.e * p.w_rows_per_expert + U.slab * p.slab_rows;
@@ -562,12 +620,12 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       const uint32_t smem_base = smem_u32(smem);
       for (int u = UNIT_FIRST; u < n_units && ok; u += UNIT_STRIDE) {
         Unit U;
-        if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
+        if (!decode_item<kGemm1, kN>(p, u, ks, U)) continue;
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.limit_ns, p.status)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * C::kAccCols);
         const uint32_t idesc = idesc_f16_m128(U.n_mma, DT<T>::kIsBF16);
-        for (int kb = 0; kb < p.num_kb; kb += C::kKps) {  // NVFP4: kKps = 1, 128-k stages
+        for (int kb = U.kb0; kb < U.kb1; kb += C::kKps) {  // NVFP4: kKps = 1, 128-k stages
           if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.limit_ns, p.status)) {
             ok = false;
             break;
@@ -591,7 +649,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
 #pragma unroll
               for (int k = 0; k < kBlockK / 16; ++k) {
                 const uint64_t bdesc = sw128_kmajor_desc(tb + hh * (kN * kBlockK * 2) + k * 32);
-                const uint32_t accum = (kb | hh | k) != 0 ? 1u : 0u;
+                const uint32_t accum = ((kb - U.kb0) | hh | k) != 0 ? 1u : 0u;
                 umma_f16_tmem_a(d, a + k * 8, bdesc, idesc, accum);
                 if (kGemm1 && U.two) umma_f16_tmem_a(d + kN, a + 32 + k * 8, bdesc, idesc, accum);
               }
@@ -606,7 +664,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
               phase ^= 1u;
             }
           } else {
-            const int nsub = p.num_kb - kb < C::kKps ? p.num_kb - kb : C::kKps;
+            const int nsub = U.kb1 - kb < C::kKps ? U.kb1 - kb : C::kKps;
 #pragma unroll
             for (int j = 0; j < C::kKps; ++j) {
               if (j >= nsub) break;
@@ -652,7 +710,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
     uint32_t acc_phase = 0;
     for (int u = UNIT_FIRST; u < n_units; u += UNIT_STRIDE) {
       Unit U;
-      if (!decode_unit<kGemm1, kN>(p, u, U)) continue;
+      if (!decode_item<kGemm1, kN>(p, u, ks, U)) continue;
       // NVFP4: the expert's FP32 scale multiplies the FP32 accumulator (before the activation)
       const float al = kW4 ? p.alpha[U.e] : 1.0f;
       if constexpr (kGemm1) {
@@ -680,6 +738,41 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
         tc_fence_after();
         const uint32_t tb =
             tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
+        const float* other = nullptr;  // split-K: the other half's accumulators
+        if constexpr (kW4) {
+          if (U.part >= 0) {
+            // Store both accumulators (f32, column-major: a warp writes 128 bytes per column),
+            // then count this half in.  The half that comes second adds the first one's
+            // partials to its own: a + b is the same either way round, so the result does not
+            // depend on which half finished first.
+            const int64_t stride = (int64_t)2 * p.split_cols * kSlab;  // floats per half
+            float* mine = p.split_part + (int64_t)U.part * stride;
+            for (int c = 0; c < U.n_mma; c += 16) {
+              float g[16], v[16];
+              tmem_ld2_x16(tb + c, tb + kN + c, g, v);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                __stcg(mine + (int64_t)(c + j) * kSlab + row, g[j]);
+                __stcg(mine + (int64_t)(p.split_cols + c + j) * kSlab + row, v[j]);
+              }
+            }
+            __threadfence();
+            named_bar_sync(1, 128);
+            if (et == 0) s_split_last = atomicAdd(&p.split_cnt[U.part >> 1], 1);
+            named_bar_sync(1, 128);
+            if (s_split_last == 0) {  // the other half writes the unit's output
+              tc_fence_before();
+              mbar_arrive(&tempty_bar[acc]);
+              if (++acc == C::kAccBufs) {
+                acc = 0;
+                acc_phase ^= 1u;
+              }
+              continue;
+            }
+            __threadfence();
+            other = p.split_part + (int64_t)(U.part ^ 1) * stride;
+          }
+        }
         T* stg = reinterpret_cast<T*>(staging);
         T* out = static_cast<T*>(p.out);
         const int n_halves = p.gated ? 1 : (U.two ? 2 : 1);
@@ -695,6 +788,13 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
                 float g[16], v[16];
                 tmem_ld2_x16(tb + c, tb + kN + c, g, v);
                 if constexpr (kW4) {
+                  if (other) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                      g[j] += __ldcg(other + (int64_t)(c + j) * kSlab + row);
+                      v[j] += __ldcg(other + (int64_t)(p.split_cols + c + j) * kSlab + row);
+                    }
+                  }
 #pragma unroll
                   for (int j = 0; j < 16; ++j) {
                     g[j] *= al;
@@ -711,6 +811,13 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
                 }
               } else {
                 tmem_ld_x16(tb + (uint32_t)(half * kN) + c, h);
+                if constexpr (kW4) {
+                  if (other) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                      h[j] += __ldcg(other + (int64_t)(half * p.split_cols + c + j) * kSlab + row);
+                  }
+                }
                 if (p.act == kActIdentity) {
 #pragma unroll
                   for (int j = 0; j < 16; ++j) h[j] *= al;
@@ -885,7 +992,12 @@ bool decode_sized(const GemmCall& c) {
 template <bool kGemm1, typename T>
 cudaError_t launch_rows(const GemmCall& c, const KParams& kp, int grid, cudaStream_t s,
                         bool pdl) {
-  if (c.w4) return launch_typed<kGemm1, 128, __nv_bfloat16, true>(c, kp, grid, s, pdl);
+  if (c.w4) {
+    if constexpr (kGemm1) {  // split-K over at most 64 token rows, two accumulator buffers
+      if (kp.split_cap > 0) return launch_typed<true, 64, __nv_bfloat16, true>(c, kp, grid, s, pdl);
+    }
+    return launch_typed<kGemm1, 128, __nv_bfloat16, true>(c, kp, grid, s, pdl);
+  }
   if constexpr (!kGemm1) {  // 64-row tiles are decode tiles: balanced
     if (c.tile_rows == 64) return launch_typed<false, 64, T, false, true>(c, kp, grid, s, pdl);
   }
@@ -938,6 +1050,25 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   kp.status = c.status;
   kp.limit_ns = wait_limit_ns();
   kp.prefetch_steps = 0;
+  kp.split_cap = 0;
+  kp.split_cols = 0;
+  kp.split_part = nullptr;
+  kp.split_cnt = nullptr;
+  if (c.w4 && c.gemm1 && kp.token_rows && c.T <= 64 && c.split_cap > 0 && c.split_part &&
+      c.split_cnt) {
+    if (c.split_cols < ((c.T + 15) & ~15)) return cudaErrorInvalidValue;
+    // The split-capable kernel (64-row tiles) only when splitting pays for the most units the
+    // call can have (one tile per routed expert); it then decides on the actual count.
+    const int64_t active = (int64_t)c.P < c.E ? (int64_t)c.P : (int64_t)c.E;
+    const int64_t n_max = active * kp.n_slabs;
+    const int64_t ctas = 2 * n_max < num_sms() ? 2 * n_max : num_sms();
+    if (n_max <= c.split_cap && split_pays((int)n_max, (int)ctas, kp.num_kb)) {
+      kp.split_cap = c.split_cap;
+      kp.split_cols = c.split_cols;
+      kp.split_part = c.split_part;
+      kp.split_cnt = c.split_cnt;
+    }
+  }
 
   if (c.tile_rows != 128 && c.tile_rows != 256 &&
       !(c.tile_rows == 64 && !c.gemm1 && !c.w4 && c.mode == kSorted))
@@ -951,6 +1082,7 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
     upper = (long long)((c.dense_rows + c.tile_rows - 1) / c.tile_rows) * kp.n_slabs;
   if (upper <= 0 || c.b_rows <= 0) return cudaSuccess;
   const int sms = num_sms();
+  if (kp.split_cap > 0) upper *= 2;  // room for the split halves
   const int grid = (int)(upper < sms ? upper : sms);
   if (c.early_tiles && c.mode == kSorted && !c.w4) {
     // Up to ~48 MB (well under the L2) of first-unit weights over the whole grid.

@@ -284,13 +284,15 @@ __global__ void __launch_bounds__(1024)
                       int32_t* __restrict__ sorted_ids, int32_t* __restrict__ tile_expert,
                       int64_t tile_len, int32_t* __restrict__ inv_route, Tile* __restrict__ tiles,
                       int* __restrict__ n_tiles, int tile_rows, Tile* __restrict__ tiles2,
-                      int* __restrict__ n_tiles2, int tile_rows2, int* status) {
+                      int* __restrict__ n_tiles2, int tile_rows2, int* status,
+                      int* __restrict__ zero, int n_zero) {
   extern __shared__ int warp_cnt[];  // [32][E]
   __shared__ int warp_tot[32];
   __shared__ int s_total;
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  for (int i = tid; i < n_zero; i += blockDim.x) zero[i] = 0;
   for (int i = tid; i < 32 * E; i += blockDim.x) warp_cnt[i] = 0;
   __syncthreads();
   int* wc = warp_cnt + w * E;
@@ -569,7 +571,8 @@ cudaError_t launch_sort_fused(const moe_problem_t& p, int block_m, const int32_t
                               int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
                               int64_t cap, int32_t* tile_expert, int32_t* inv_route, Tile* tiles,
                               int* n_tiles, int tile_rows, Tile* tiles2, int* n_tiles2,
-                              int tile_rows2, int* status, cudaStream_t s, bool pdl) {
+                              int tile_rows2, int* status, cudaStream_t s, bool pdl, int* zero,
+                              int n_zero) {
   const int P = p.T * p.top_k;
   const size_t smem = sizeof(int) * 32 * (size_t)p.E;
   static bool attr_set = false;
@@ -583,7 +586,8 @@ cudaError_t launch_sort_fused(const moe_problem_t& p, int block_m, const int32_t
   const int64_t tile_len = (cap + block_m - 1) / block_m;
   return launch_k(sort_fused_kernel, dim3(1), dim3(1024), smem, s, pdl, ids, P, p.E, block_m,
                   cap, counts, offsets, sorted_ids, tile_expert, tile_len, inv_route, tiles,
-                  n_tiles, tile_rows, tiles2, n_tiles2, tile_rows2, status);
+                  n_tiles, tile_rows, tiles2, n_tiles2, tile_rows2, status, zero,
+                  zero ? n_zero : 0);
 }
 
 cudaError_t launch_align_sort_chunked(const moe_problem_t& p, int block_m, const int32_t* ids,

@@ -196,6 +196,55 @@ def test_w4a16_is_deterministic_and_graph_replayable(cuda_device):
     assert torch.equal(out, a)
 
 
+SPLIT = [
+    # units = active experts x F/128, few against the SMs, and 8 K steps each: every unit's K
+    # range is split in two
+    W("w4-split-t16", T=16, H=1024, E=8, F=640, top_k=2, weights="nvfp4"),
+    # odd number of 128-k steps (9: halves of 4 and 5), GeGLU-tanh, sigmoid routing
+    W("w4-split-t24-odd-k-gelu", T=24, H=1152, E=6, F=256, top_k=3, scoring_func="sigmoid",
+      bias_std=0.1, routed_scaling_factor=2.5, activation="gelu_tanh", weights="nvfp4"),
+    # ReLU2: 256-row units whose second half can be empty
+    W("w4-split-t40-relu2", T=40, H=1024, E=8, F=384, top_k=2, activation="relu2",
+      weights="nvfp4"),
+]
+
+
+@pytest.mark.parametrize("w", SPLIT, ids=lambda w: w.name)
+def test_w4a16_split_k_matches_oracle_and_unsplit_run(w, cuda_device):
+    """The gate/up GEMM's split-K path (workspace of moe_workspace_size_w4a16 bytes) and the
+    unsplit one (moe_workspace_size bytes) each match the oracle and are deterministic, and they
+    agree with each other to a few f32 roundings.  The split path's per-unit counters, which
+    sit right after the common workspace, end each call at 2 (both halves counted in)."""
+    d = inputs.generate(w, seed=7, device=cuda_device)
+    prob = B.make_problem(w.T, w.H, w.E, w.F, w.top_k, w.dtype, w.scoring_func, w.renormalize,
+                          w.num_expert_group, w.topk_group, w.routed_scaling_factor, 0,
+                          w.activation)
+    n_small, n_big = B.workspace_size(prob), B.workspace_size_w4a16(prob)
+    assert n_big > n_small
+    ws_small = B.new_workspace(n_small, cuda_device)
+    ws_big = B.new_workspace(n_big, cuda_device)
+    ref, _, _, _ = oracle_fused(w, d)
+    outs = {}
+    for name, ws in (("unsplit", ws_small), ("split", ws_big)):
+        a = run_fused(w, d, workspace=ws).clone()
+        b = run_fused(w, d, workspace=ws).clone()
+        torch.cuda.synchronize()
+        assert B.get_device_status(ws) == B.MOE_OK
+        assert torch.equal(a, b), f"{w.name} {name}: repeat call not bit-identical"
+        assert_output_close(a, ref, w.dtype, what=f"{w.name} {name}")
+        outs[name] = a
+    cnt = ws_big[n_small:n_small + 4 * 64].view(torch.int32).cpu().numpy()
+    assert set(np.unique(cnt)) <= {0, 2} and cnt.max() == 2, f"split counters {cnt[:16]}"
+    # Each output is rounded once to bf16 from f32 sums that differ only in their grouping
+    # (and through gemm1's bf16-rounded activations): within one ulp plus a sliver of the RMS.
+    sp, un = to_np(outs["split"]), to_np(outs["unsplit"])
+    rms = float(np.sqrt(np.mean(un * un)))
+    err = np.abs(sp - un)
+    bound = 2 * half_ulp(np.abs(un) * (1 + 2.0 ** -7), w.dtype) + 2e-3 * rms
+    log_parity(f"{w.name} split vs unsplit", max_err_over_rms=float(err.max()) / rms)
+    assert np.all(err <= bound), f"{w.name}: split and unsplit differ by {err.max():.3e}"
+
+
 def test_w4a16_rejects_unsupported_shapes(cuda_device):
     w = W("bad", T=4, H=192, E=4, F=128, top_k=2, weights="nvfp4")  # H not a multiple of 128
     d = inputs.generate(w, seed=0, device=cuda_device)
