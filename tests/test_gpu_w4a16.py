@@ -235,6 +235,15 @@ def test_w4a16_split_k_matches_oracle_and_unsplit_run(w, cuda_device):
         outs[name] = a
     cnt = ws_big[n_small:n_small + 4 * 64].view(torch.int32).cpu().numpy()
     assert set(np.unique(cnt)) <= {0, 2} and cnt.max() == 2, f"split counters {cnt[:16]}"
+    # A workspace whose every byte past the status header starts as 0xFF (counters at -1,
+    # partials NaN): the sort zeroes the counters and each half writes its partials before the
+    # other reads them, so the result is the clean run's, bit for bit.
+    poison = B.new_workspace(n_big, cuda_device)
+    poison[256:] = 0xFF
+    c = run_fused(w, d, workspace=poison).clone()
+    torch.cuda.synchronize()
+    assert B.get_device_status(poison) == B.MOE_OK
+    assert torch.equal(c, outs["split"]), f"{w.name}: poisoned split workspace changed the output"
     # Each output is rounded once to bf16 from f32 sums that differ only in their grouping
     # (and through gemm1's bf16-rounded activations): within one ulp plus a sliver of the RMS.
     sp, un = to_np(outs["split"]), to_np(outs["unsplit"])
