@@ -251,68 +251,82 @@ def local_ids(w, ids):
 
 
 # ------------------------------------------------------------------------------- CPU oracle arm
-def oracle_rate(w, d, budget_s: float, max_tokens=None):
-    """Time the CPU oracle (routing + per-token expert MLP) on a bounded token sample.
+class OracleSample:
+    """The CPU oracle (routing + per-token expert MLP) on the first n tokens of a workload, n
+    sized so that one pass takes about a quarter of `budget_s`.  The setup (the full routing,
+    the used experts' weights copied to the host) runs once; `run` then times passes."""
 
-    Returns (TFLOP/s, seconds, tokens per pass, passes, cores)."""
-    import numpy as np
-    import torch
+    def __init__(self, w, d, budget_s: float, max_tokens=None):
+        import numpy as np
+        import torch
 
-    import oracle
-    gating = d["gating_output"].cpu().numpy()
-    bias = None if d["correction_bias"] is None else d["correction_bias"].cpu().numpy()
-    sc = oracle.SOFTMAX if w.scoring_func == "softmax" else oracle.SIGMOID
-    ids, wts, _ = oracle.route(gating, w.top_k, sc, w.renormalize, w.num_expert_group,
-                               w.topk_group, w.routed_scaling_factor, bias)
-    ids = local_ids(w, ids)
-    flops_tok = w.flops(int((ids >= 0).sum())) / w.T
-    # Sample: the first n tokens, n sized for about 1/4 of the budget per pass.
-    cores = oracle.num_threads()
-    n = max(1, min(w.T, int(0.25 * budget_s * 2e9 * cores / flops_tok)))
-    if max_tokens:
-        n = min(n, max_tokens)
-    toks = np.arange(n, dtype=np.int32)
-    act_code = {"silu": oracle.ACT_SILU, "gelu_tanh": oracle.ACT_GELU_TANH,
-                "relu2": oracle.ACT_RELU2}[w.activation]
-    if w.weights == "nvfp4":
-        w1 = tuple(t.cpu() for t in d.get("w_gate_up_canonical", d["w_gate_up"]))
-        w2 = tuple(t.cpu() for t in d.get("w_down_canonical", d["w_down"]))
-        g_n = np.ascontiguousarray(gating[:n])
-        hid = d["hidden_states"].cpu()
+        import oracle
+        self.w, self.oracle = w, oracle
+        gating = d["gating_output"].cpu().numpy()
+        self.bias = None if d["correction_bias"] is None else d["correction_bias"].cpu().numpy()
+        self.sc = oracle.SOFTMAX if w.scoring_func == "softmax" else oracle.SIGMOID
+        ids, wts, _ = oracle.route(gating, w.top_k, self.sc, w.renormalize, w.num_expert_group,
+                                   w.topk_group, w.routed_scaling_factor, self.bias)
+        self.ids, self.wts = local_ids(w, ids), wts
+        self.flops_tok = w.flops(int((self.ids >= 0).sum())) / w.T
+        self.cores = oracle.num_threads()
+        n = max(1, min(w.T, int(0.25 * budget_s * 2e9 * self.cores / self.flops_tok)))
+        if max_tokens:
+            n = min(n, max_tokens)
+        self.n = n
+        self.toks = np.arange(n, dtype=np.int32)
+        self.act = {"silu": oracle.ACT_SILU, "gelu_tanh": oracle.ACT_GELU_TANH,
+                    "relu2": oracle.ACT_RELU2}[w.activation]
+        self.g_n = np.ascontiguousarray(gating[:n])
+        self.hid = d["hidden_states"].cpu()
+        self.w4 = w.weights == "nvfp4"
+        if self.w4:
+            self.w1 = tuple(t.cpu() for t in d.get("w_gate_up_canonical", d["w_gate_up"]))
+            self.w2 = tuple(t.cpu() for t in d.get("w_down_canonical", d["w_down"]))
+            return
+        used = sorted(set(int(e) for e in self.ids[:n].reshape(-1) if e >= 0))
+        self.slot = np.full(w.E_local, -1, np.int32)
+        self.slot[used] = np.arange(len(used), dtype=np.int32)
+        idx = torch.tensor(used, dtype=torch.long, device=d["w_gate_up"].device)
+        self.wgu = d["w_gate_up"].index_select(0, idx).cpu()
+        self.wdn = d["w_down"].index_select(0, idx).cpu()
+        self.sgu = None if d["shared_w_gate_up"] is None else d["shared_w_gate_up"].cpu()
+        self.sdn = None if d["shared_w_down"] is None else d["shared_w_down"].cpu()
+        self.dt = oracle.BF16 if w.dtype == torch.bfloat16 else oracle.F16
+
+    def one_pass(self):
+        w, o = self.w, self.oracle
+        o.route(self.g_n, w.top_k, self.sc, w.renormalize, w.num_expert_group, w.topk_group,
+                w.routed_scaling_factor, self.bias)
+        if self.w4:
+            o.moe_tokens_w4(self.hid, self.ids, self.wts, self.w1, self.w2, o.BF16,
+                            tokens=self.toks, activation=self.act)
+        else:
+            o.moe_tokens(self.hid, self.ids, self.wts, self.wgu, self.wdn, self.dt,
+                         tokens=self.toks, expert_slot=self.slot, num_experts=w.E_local,
+                         shared_w_gate_up=self.sgu, shared_w_down=self.sdn, activation=self.act)
+
+    def run(self, budget_s: float):
+        """Passes (at least one) until budget_s has elapsed: (seconds, passes)."""
         passes, t0 = 0, time.perf_counter()
         while True:
-            oracle.route(g_n, w.top_k, sc, w.renormalize, w.num_expert_group, w.topk_group,
-                         w.routed_scaling_factor, bias)
-            oracle.moe_tokens_w4(hid, ids, wts, w1, w2, oracle.BF16, tokens=toks,
-                                 activation=act_code)
+            self.one_pass()
             passes += 1
             el = time.perf_counter() - t0
-            if el >= budget_s or (passes >= 1 and el * (passes + 1) / passes > 3 * budget_s):
-                break
-        return flops_tok * n * passes / el / 1e12, el, n, passes, cores
-    used = sorted(set(int(e) for e in ids[:n].reshape(-1) if e >= 0))
-    slot = np.full(w.E_local, -1, np.int32)
-    slot[used] = np.arange(len(used), dtype=np.int32)
-    idx = torch.tensor(used, dtype=torch.long, device=d["w_gate_up"].device)
-    wgu = d["w_gate_up"].index_select(0, idx).cpu()
-    wdn = d["w_down"].index_select(0, idx).cpu()
-    sgu = None if d["shared_w_gate_up"] is None else d["shared_w_gate_up"].cpu()
-    sdn = None if d["shared_w_down"] is None else d["shared_w_down"].cpu()
-    hid = d["hidden_states"].cpu()
-    dt = oracle.BF16 if w.dtype == torch.bfloat16 else oracle.F16
-    g_n = np.ascontiguousarray(gating[:n])
-    passes, t0 = 0, time.perf_counter()
-    while True:
-        i2, w2, _ = oracle.route(g_n, w.top_k, sc, w.renormalize, w.num_expert_group,
-                                 w.topk_group, w.routed_scaling_factor, bias)
-        oracle.moe_tokens(hid, ids, wts, wgu, wdn, dt, tokens=toks, expert_slot=slot,
-                          num_experts=w.E_local, shared_w_gate_up=sgu, shared_w_down=sdn,
-                          activation=act_code)
-        passes += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s or (passes >= 1 and el * (passes + 1) / passes > 3 * budget_s):
-            break
-    return flops_tok * n * passes / el / 1e12, el, n, passes, cores
+            if el >= budget_s or el * (passes + 1) / passes > 3 * budget_s:
+                return el, passes
+
+    def flops(self, passes: int) -> float:
+        return self.flops_tok * self.n * passes
+
+
+def oracle_rate(w, d, budget_s: float, max_tokens=None):
+    """Time the CPU oracle on a bounded token sample.
+
+    Returns (TFLOP/s, seconds, tokens per pass, passes, cores)."""
+    s = OracleSample(w, d, budget_s, max_tokens)
+    el, passes = s.run(budget_s)
+    return s.flops(passes) / el / 1e12, el, s.n, passes, s.cores
 
 
 # ------------------------------------------------------------------------------------ main arm
@@ -554,15 +568,17 @@ def run_reference(args, w):
     from mixture_experts_forward_moe_gb300 import inputs
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
     d = inputs.generate(w, seed=args.seed, device=dev)
-    per_step = max(0.5, min(10.0, 60.0 / max(1, args.steps + args.warmup)))
+    # About two minutes of oracle work over all warm-up and timed steps, whatever K and W are.
+    per_step = max(0.01, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
+    sample = OracleSample(w, d, per_step)
     for _ in range(args.warmup):
-        oracle_rate(w, d, budget_s=0.0, max_tokens=None)
-    times, flops, n_last, cores = [], 0.0, 0, 1
+        sample.run(per_step)
+    times, flops = [], 0.0
     for _ in range(args.steps):
-        rate, el, n, passes, cores = oracle_rate(w, d, budget_s=per_step)
+        el, passes = sample.run(per_step)
         times.append(el)
-        flops += rate * el * 1e12
-        n_last = n
+        flops += sample.flops(passes)
+    n_last, cores = sample.n, sample.cores
     total = sum(times)
     value = flops / total / 1e12
     res = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
