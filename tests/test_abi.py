@@ -52,6 +52,37 @@ def test_workspace_size_and_capacity():
     assert L.moe_stage_workspace_size(ctypes.byref(p), 1) == n
 
 
+def _align256(n):
+    return (n + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("kw", [
+    dict(T=32, H=2048, E=128, F=768, top_k=8),                   # Qwen3-30B decode: 768 units
+    dict(T=32, H=7168, E=256, F=2048, top_k=8, ep_num_local=32),  # EP8 shard: 32 local experts
+    dict(T=7, H=256, E=16, F=384, top_k=2),                     # few routes: units from P
+    dict(T=64, H=512, E=512, F=4096, top_k=8),                  # more than 1024 units: capped
+])
+def test_w4a16_workspace_adds_the_split_scratch(kw):
+    """moe_workspace_size_w4a16 = moe_workspace_size + the split-K scratch its header defines:
+    a counter per unit (256-byte aligned), then 2048 * round16(T) bytes per unit, for
+    min(min(T*top_k, E_local) * F/128, 1024) units."""
+    L = B.lib()
+    p = _prob(**kw)
+    base = L.moe_workspace_size(ctypes.byref(p))
+    e_local = kw.get("ep_num_local", 0) or kw["E"]
+    units = min(min(kw["T"] * kw["top_k"], e_local) * (kw["F"] // 128), 1024)
+    scratch = _align256(4 * units) + units * 2048 * ((kw["T"] + 15) // 16 * 16)
+    assert L.moe_workspace_size_w4a16(ctypes.byref(p)) == base + scratch
+
+
+@pytest.mark.parametrize("kw", [dict(T=65), dict(T=512, H=256, E=16, F=128, top_k=4),
+                                dict(T=0)])
+def test_w4a16_workspace_has_no_scratch_past_64_tokens(kw):
+    L = B.lib()
+    p = _prob(**kw)
+    assert L.moe_workspace_size_w4a16(ctypes.byref(p)) == L.moe_workspace_size(ctypes.byref(p))
+
+
 @pytest.mark.parametrize("kw,code", [
     (dict(T=-1), B.MOE_ERR_INVALID_ARG),
     (dict(top_k=17), B.MOE_ERR_INVALID_ARG),          # top_k > E
