@@ -454,6 +454,7 @@ moe_status_t run_fused(const moe_problem_t* p, const Experts& X, const void* hid
     g1.max_tiles = (int)L.max_tiles;
     g1.tile_rows = kTileRows;
     g1.early_tiles = token_rows ? 0 : 1;  // sort, then permute, then gemm1
+    g1.route_ids = token_rows ? ids : nullptr;  // route, sort, then gemm1
     if (split_cnt) {
       g1.split_cap = (int)S.units;
       g1.split_cols = (int)S.cols;
@@ -466,6 +467,7 @@ moe_status_t run_fused(const moe_problem_t* p, const Experts& X, const void* hid
       t.done(1);
     }
     GemmCall g2 = g1;
+    g2.route_ids = nullptr;
     g2.split_cap = 0;
     g2.split_part = nullptr;
     g2.split_cnt = nullptr;

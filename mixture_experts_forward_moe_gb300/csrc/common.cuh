@@ -209,6 +209,10 @@ struct GemmCall {
   int split_cols;
   float* split_part;
   int* split_cnt;
+  // 16-bit gate/up GEMM over token rows: the router's ids [P].  The unit list (one tile per
+  // routed expert, in expert order) follows from them, so the weight producer and the MMA
+  // issuer start before the sort has finished; only the epilogue waits for it.
+  const int32_t* route_ids;
   int* status;
 };
 

@@ -139,6 +139,8 @@ struct KParams {
   // tile list was written at least two launches earlier (it is then complete when this kernel
   // starts).
   int prefetch_steps;
+  // 16-bit gate/up GEMM over token rows: the router's ids (GemmCall::route_ids).
+  const int32_t* route_ids;
   // NVFP4 gate/up GEMM: split-K in two halves when it shortens the last wave (GemmCall).
   int split_cap, split_cols;
   float* split_part;
@@ -223,6 +225,43 @@ __device__ __forceinline__ bool decode_item(const KParams& p, int u, int ks, Uni
   return true;
 }
 
+// decode_item for the roles that run before the sort has finished (gate/up over token rows):
+// unit v is slab v % n_slabs of the (v / n_slabs)-th routed expert in `emask`, the bitmask of
+// the experts the router chose, because the sort's tile list holds one tile per routed expert
+// in expert order.  These roles need neither the unit's rows nor its position in the sorted
+// order; the epilogue reads those from the tile list after its dependency wait.
+template <bool kGemm1, int kN>
+__device__ __forceinline__ bool decode_item_routed(const KParams& p, const uint32_t* emask, int u,
+                                                   int ks, Unit& U) {
+  const bool split = ks == 2;
+  const int v = split ? (u >> 1) : u;
+  const int rank = v / p.n_slabs;
+  int word = 0, seen = 0;
+  while (word < 32 && seen + __popc(emask[word]) <= rank) seen += __popc(emask[word++]);
+  if (word == 32) return false;
+  uint32_t m = emask[word];
+  for (int i = seen; i < rank; ++i) m &= m - 1;  // drop the lower routed experts of the word
+  U.e = word * 32 + __ffs(m) - 1;
+  U.slab = v % p.n_slabs;
+  U.row0 = 0;
+  U.nrows = p.T;
+  U.b_row0 = 0;
+  U.n_mma = round16(p.T);
+  U.two = kGemm1 && (p.gated || U.slab * p.slab_rows + kSlab < p.n_out);
+  U.kb0 = 0;
+  U.kb1 = p.num_kb;
+  U.part = -1;
+  if (split) {
+    const int mid = p.num_kb >> 1;
+    if (u & 1)
+      U.kb0 = mid;
+    else
+      U.kb1 = mid;
+    U.part = u;
+  }
+  return true;
+}
+
 // Split-K cost model of the NVFP4 gate/up GEMM over at most 64 token rows, in K steps per CTA:
 // a whole unit costs its num_kb steps plus kSplitWholeOver, a half its num_kb/2 plus
 // kSplitHalfOver (the extra epilogue and the exchange of partials), fitted to timings of both
@@ -282,6 +321,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
   __shared__ int s_n_units;
   __shared__ int s_ks;          // work items per unit (2: split-K)
   __shared__ int s_split_last;  // epilogue: this half finished the unit second
+  __shared__ uint32_t s_emask[kW4 ? 1 : 32];  // routed experts (gate/up over token rows)
   __shared__ int ent_col[kGemm1 ? kN : 1];
   __shared__ int ent_dst[kN];
   __shared__ float col_scale[kGemm1 ? 1 : kN];
@@ -348,11 +388,32 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       }
     }
   }
-  pdl_wait();
+  // 16-bit gate/up over token rows: the units follow from the router's ids, so only the
+  // epilogue waits for the sort (below); the router finished before the sort released this
+  // grid, and the ids are read from L2.
+  const bool routed = !kW4 && kGemm1 && p.route_ids != nullptr && p.mode == kSorted;
+  const uint32_t* emask = routed ? s_emask : nullptr;
+  if (routed) {
+    if (warp == 0) {
+      s_emask[lane] = 0u;
+      __syncwarp();
+      for (int r = lane; r < p.P; r += 32) {
+        const int e = __ldcg(p.route_ids + r);
+        if (e >= 0 && e < p.E) atomicOr(&s_emask[e >> 5], 1u << (e & 31));
+      }
+      __syncwarp();
+    }
+  } else {
+    pdl_wait();
+  }
   pdl_trigger();
   if (threadIdx.x == 0) {
     int n = 0;
-    if (p.mode == kSorted)
+    if (routed) {
+      int active = 0;
+      for (int i = 0; i < 32; ++i) active += __popc(s_emask[i]);
+      n = active * p.n_slabs;
+    } else if (p.mode == kSorted)
       n = (*p.n_tiles) * p.n_slabs;
     else if (p.mode == kDirect)
       n = p.P * p.n_slabs;
@@ -562,7 +623,9 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       bool ok = true;
       for (int u = UNIT_FIRST; u < n_units && ok; u += UNIT_STRIDE) {
         Unit U;
-        if (!decode_item<kGemm1, kN>(p, u, ks, U)) continue;
+        if (!(routed ? decode_item_routed<kGemm1, kN>(p, emask, u, ks, U)
+                     : decode_item<kGemm1, kN>(p, u, ks, U)))
+          continue;
         const uint32_t wbytes = U.two ? 2 * kSlab * kBlockK * 2 : kSlab * kBlockK * 2;
         const uint32_t bytes = wbytes + U.n_mma * kBlockK * 2;  // per 64-k block
         const int wrow = U.e * p.w_rows_per_expert + U.slab * p.slab_rows;
@@ -620,7 +683,9 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       const uint32_t smem_base = smem_u32(smem);
       for (int u = UNIT_FIRST; u < n_units && ok; u += UNIT_STRIDE) {
         Unit U;
-        if (!decode_item<kGemm1, kN>(p, u, ks, U)) continue;
+        if (!(routed ? decode_item_routed<kGemm1, kN>(p, emask, u, ks, U)
+                     : decode_item<kGemm1, kN>(p, u, ks, U)))
+          continue;
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.limit_ns, p.status)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * C::kAccCols);
@@ -708,6 +773,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
     const int et = threadIdx.x - 64;
     int acc = 0;
     uint32_t acc_phase = 0;
+    if (routed) pdl_wait();  // the tile list and the sorted ids come from the sort
     for (int u = UNIT_FIRST; u < n_units; u += UNIT_STRIDE) {
       Unit U;
       if (!decode_item<kGemm1, kN>(p, u, ks, U)) continue;
@@ -1050,6 +1116,7 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   kp.status = c.status;
   kp.limit_ns = wait_limit_ns();
   kp.prefetch_steps = 0;
+  kp.route_ids = (c.gemm1 && kp.token_rows && !c.w4 && c.E <= 1024) ? c.route_ids : nullptr;
   kp.split_cap = 0;
   kp.split_cols = 0;
   kp.split_part = nullptr;
