@@ -295,8 +295,10 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) 
 }
 
 // kBal: the units are spread evenly over balanced_ctas(units, gridDim.x) CTAs (decode-sized
-// launches); otherwise every CTA takes units c, c + gridDim.x, ...
-template <bool kGemm1, int kN, typename T, bool kW4, bool kBal>
+// launches); otherwise every CTA takes units c, c + gridDim.x, ...  kRouted: the NVFP4 gate/up
+// kernel for token rows, whose roles may take their units from the router's ids (the 16-bit
+// kernels decide at run time; the NVFP4 loops measured 1 % slower with that branch in them).
+template <bool kGemm1, int kN, typename T, bool kW4, bool kBal, bool kRouted = false>
 __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmB,
@@ -321,7 +323,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
   __shared__ int s_n_units;
   __shared__ int s_ks;          // work items per unit (2: split-K)
   __shared__ int s_split_last;  // epilogue: this half finished the unit second
-  __shared__ uint32_t s_emask[kW4 ? 1 : 32];  // routed experts (gate/up over token rows)
+  __shared__ uint32_t s_emask[(kGemm1 && (!kW4 || kRouted)) ? 32 : 1];  // routed experts
   __shared__ int ent_col[kGemm1 ? kN : 1];
   __shared__ int ent_dst[kN];
   __shared__ float col_scale[kGemm1 ? 1 : kN];
@@ -391,7 +393,8 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
   // 16-bit gate/up over token rows: the units follow from the router's ids, so only the
   // epilogue waits for the sort (below); the router finished before the sort released this
   // grid, and the ids are read from L2.
-  const bool routed = !kW4 && kGemm1 && p.route_ids != nullptr && p.mode == kSorted;
+  const bool routed =
+      (!kW4 || kRouted) && kGemm1 && p.route_ids != nullptr && p.mode == kSorted;
   const uint32_t* emask = routed ? s_emask : nullptr;
   if (routed) {
     if (warp == 0) {
@@ -455,7 +458,9 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       const int64_t slabs_per_expert = p.w_rows_per_expert / kSlab;
       for (int u = UNIT_FIRST; u < n_units && ok; u += UNIT_STRIDE) {
         Unit U;
-        if (!decode_item<kGemm1, kN>(p, u, ks, U)) continue;
+        if (!(routed ? decode_item_routed<kGemm1, kN>(p, emask, u, ks, U)
+                     : decode_item<kGemm1, kN>(p, u, ks, U)))
+          continue;
         const int n_w = U.two ? 2 : 1;
         const int64_t t0 = ((int64_t)U.e * slabs_per_expert + U.slab * p.slab_rows / kSlab) *
                            p.num_kb;
@@ -493,7 +498,9 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       bool ok = true;
       for (int u = UNIT_FIRST; u < n_units && ok; u += UNIT_STRIDE) {
         Unit U;
-        if (!decode_item<kGemm1, kN>(p, u, ks, U)) continue;
+        if (!(routed ? decode_item_routed<kGemm1, kN>(p, emask, u, ks, U)
+                     : decode_item<kGemm1, kN>(p, u, ks, U)))
+          continue;
         for (int kb = U.kb0; kb < U.kb1; ++kb) {
           if (!mbar_wait(&empty_bar[ts], tph ^ 1u, abort_flag, p.limit_ns, p.status)) {
             ok = false;
@@ -549,7 +556,9 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
     };
     for (int u = UNIT_FIRST; u < n_units && ok; u += UNIT_STRIDE) {
       Unit U;
-      if (!decode_item<kGemm1, kN>(p, u, ks, U)) continue;
+      if (!(routed ? decode_item_routed<kGemm1, kN>(p, emask, u, ks, U)
+                   : decode_item<kGemm1, kN>(p, u, ks, U)))
+        continue;
       const bool active = !kGemm1 || dg == 0 || U.two;
       const int slab = kGemm1 ? dg : 0;
       for (int kb = U.kb0; kb < U.kb1; ++kb) {
@@ -1022,7 +1031,7 @@ bool make_map(CUtensorMap* m, int dtype, const void* base, uint64_t inner, uint6
   return r == CUDA_SUCCESS;
 }
 
-template <bool kGemm1, int kN, typename T, bool kW4, bool kBal = false>
+template <bool kGemm1, int kN, typename T, bool kW4, bool kBal = false, bool kRouted = false>
 cudaError_t launch_typed(const GemmCall& c, const KParams& kp, int grid, cudaStream_t s,
                          bool pdl) {
   using C = Cfg<kGemm1, kN, kW4>;
@@ -1036,7 +1045,7 @@ cudaError_t launch_typed(const GemmCall& c, const KParams& kp, int grid, cudaStr
       !make_map(&tmB128, c.dtype, c.b, (uint64_t)c.K, (uint64_t)c.b_rows, 128))
     return cudaErrorInvalidValue;
   if (kW4) tmW = tmB;
-  auto kern = moe_gemm_kernel<kGemm1, kN, T, kW4, kBal>;
+  auto kern = moe_gemm_kernel<kGemm1, kN, T, kW4, kBal, kRouted>;
   static bool attr_set = false;  // one per instantiation: set once per process
   if (!attr_set) {
     cudaError_t e =
@@ -1059,8 +1068,11 @@ template <bool kGemm1, typename T>
 cudaError_t launch_rows(const GemmCall& c, const KParams& kp, int grid, cudaStream_t s,
                         bool pdl) {
   if (c.w4) {
-    if constexpr (kGemm1) {  // split-K over at most 64 token rows, two accumulator buffers
-      if (kp.split_cap > 0) return launch_typed<true, 64, __nv_bfloat16, true>(c, kp, grid, s, pdl);
+    if constexpr (kGemm1) {
+      if (kp.split_cap > 0)  // split-K over at most 64 token rows, two accumulator buffers
+        return launch_typed<true, 64, __nv_bfloat16, true, false, true>(c, kp, grid, s, pdl);
+      if (kp.route_ids)  // token rows: units from the router's ids
+        return launch_typed<true, 128, __nv_bfloat16, true, false, true>(c, kp, grid, s, pdl);
     }
     return launch_typed<kGemm1, 128, __nv_bfloat16, true>(c, kp, grid, s, pdl);
   }
@@ -1116,7 +1128,7 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   kp.status = c.status;
   kp.limit_ns = wait_limit_ns();
   kp.prefetch_steps = 0;
-  kp.route_ids = (c.gemm1 && kp.token_rows && !c.w4 && c.E <= 1024) ? c.route_ids : nullptr;
+  kp.route_ids = (c.gemm1 && kp.token_rows && c.E <= 1024) ? c.route_ids : nullptr;
   kp.split_cap = 0;
   kp.split_cols = 0;
   kp.split_part = nullptr;
