@@ -322,8 +322,10 @@ moe_status_t moe_shared_expert_fwd(const moe_problem_t* p, const void* hidden_st
  * expert histograms and a status word) lives in a static device array of 256 KiB + 256 bytes
  * inside the library, which every GPU that loads the library holds until the process exits.
  *   status_out  device int32 or NULL: receives MOE_OK or MOE_ERR_BAD_EXPERT_ID for this call
- * Limits: ceil(T*top_k/256) * E <= 65536, else MOE_ERR_WORKSPACE_TOO_SMALL (nothing enqueued);
- * E <= 1024.  The first call on a device looks up the array's address (cudaGetSymbolAddress,
+ * The problem is checked as in moe_align_sort (argument errors MOE_ERR_INVALID_ARG, E > 1024 or
+ * top_k > 32 MOE_ERR_UNSUPPORTED); with an expert-parallel shard the ids index its ep_num_local
+ * experts.  Limit of the static array: ceil(T*top_k/256) * (local experts) <= 65536, else
+ * MOE_ERR_WORKSPACE_TOO_SMALL (nothing enqueued).  The first call on a device looks up the array's address (cudaGetSymbolAddress,
  * with that device current); make it before any stream capture.  No call allocates.  Every call
  * shares the array and the array keeps the last call's contents: each call clears the status
  * word itself, and calls that overlap on the GPU (concurrent streams or threads) race.

@@ -76,7 +76,9 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 int elt_bytes(const moe_problem_t&) { return 2; }
 
-// Checks the problem; returns MOE_OK, MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED.
+}  // namespace
+
+// Declared in common.cuh.
 moe_status_t check_problem(const moe_problem_t* p) {
   if (!p) return MOE_ERR_INVALID_ARG;
   if (p->T < 0 || p->H <= 0 || p->E <= 0 || p->F <= 0 || p->top_k <= 0 || p->S < 0)
@@ -104,6 +106,8 @@ moe_status_t check_problem(const moe_problem_t* p) {
   if ((int64_t)p->T * p->top_k > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
+
+namespace {
 
 bool use_direct(const moe_problem_t& p) {
   return p.T <= kDirectMaxT && (int64_t)p.T * p.top_k <= kDirectMaxRoutes;

@@ -221,4 +221,9 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl);
 uint64_t wait_limit_ns();
 int num_sms();
 
+// Checks a problem description (sizes, routing options, the expert-parallel shard, the limits
+// of the kernels: E <= 1024, top_k <= 32, T*top_k <= 2^30); returns MOE_OK,
+// MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED.
+moe_status_t check_problem(const moe_problem_t* p);
+
 }  // namespace gb300moe

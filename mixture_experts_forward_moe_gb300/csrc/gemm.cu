@@ -408,8 +408,8 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
     }
   } else {
     pdl_wait();
+    pdl_trigger();
   }
-  pdl_trigger();
   if (threadIdx.x == 0) {
     int n = 0;
     if (routed) {
@@ -782,7 +782,12 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
     const int et = threadIdx.x - 64;
     int acc = 0;
     uint32_t acc_phase = 0;
-    if (routed) pdl_wait();  // the tile list and the sorted ids come from the sort
+    if (routed) {
+      // The tile list and the sorted ids come from the sort.  Dependents are released only
+      // after this wait: the next kernel may read what the sort wrote before its own wait.
+      pdl_wait();
+      pdl_trigger();
+    }
     for (int u = UNIT_FIRST; u < n_units; u += UNIT_STRIDE) {
       Unit U;
       if (!decode_item<kGemm1, kN>(p, u, ks, U)) continue;

@@ -62,8 +62,10 @@ extern "C" moe_status_t moe_align_sort_noalloc(const moe_problem_t* p, int32_t b
                                                int32_t* offsets, int32_t* sorted_ids,
                                                int32_t* tile_expert, int32_t* inv_route,
                                                int32_t* status_out, void* stream) {
-  if (!p || p->T < 0 || p->E <= 0 || p->E > 1024 || p->top_k <= 0 || p->top_k > p->E)
-    return MOE_ERR_INVALID_ARG;
+  // The same checks as moe_align_sort: sizes, top_k <= 32, E <= 1024 and a shard
+  // (ep_local_offset, ep_num_local) inside [0, E), so the local expert count is at most 1024.
+  const moe_status_t st = check_problem(p);
+  if (st != MOE_OK) return st;
   if (block_m <= 0 || block_m > 1024) return MOE_ERR_INVALID_ARG;
   if (!counts || !offsets || !sorted_ids || !inv_route) return MOE_ERR_INVALID_ARG;
   if (p->T > 0 && !topk_ids) return MOE_ERR_INVALID_ARG;

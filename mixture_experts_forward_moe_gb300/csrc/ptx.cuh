@@ -22,9 +22,11 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 
 // ---- programmatic dependent launch ------------------------------------------------------------
 // Every kernel of the path calls pdl_wait() before it touches global memory that an earlier
-// kernel of the stream writes or reads, and pdl_trigger() only after that wait, so when kernel
-// X+1 starts early, every kernel before X has completed.  Both are no-ops for a kernel launched
-// without the programmatic-serialization attribute.
+// kernel of the stream writes or reads, and pdl_trigger() only after that wait (in every thread
+// that triggers), so when kernel X+1 starts early, every kernel before X has completed.  The
+// gate/up GEMM over token rows has its producer and MMA roles start before the wait; there only
+// the epilogue, which waits, triggers.  Both are no-ops for a kernel launched without the
+// programmatic-serialization attribute.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
