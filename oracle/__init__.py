@@ -71,6 +71,7 @@ def _load():
             _lib.oracle_sigmoid_key_f32.restype = ctypes.c_float
             _lib.oracle_sigmoid_key_f32.argtypes = [ctypes.c_float]
             _lib.oracle_route.argtypes = [i32, i32, i32, i32, i32, i32, i32, f64, P, P, P, P, P]
+            _lib.oracle_route_select_f64.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P]
             _lib.oracle_align_sort.argtypes = [i32, i32, i32, i32, P, P, P, P, i64, P, i64, P]
             _lib.oracle_moe_tokens.argtypes = [i32, P, i32, i32, i32, i32, i32, i32, i32, P, P, P,
                                                P, P, P, i32, P, P, P]
@@ -152,6 +153,22 @@ def route(gating, top_k, scoring=SOFTMAX, renormalize=True, num_expert_group=0, 
                               _ptr(ids), _ptr(w), _ptr(nt))
     _check(rc, "oracle_route")
     return ids, w, nt
+
+
+def route_select_f64(gating, top_k, num_expert_group=0, topk_group=0, bias=None):
+    """The sigmoid (+ correction bias, + groups) selection on the plain fp64 definition
+    (oracle.c: oracle_route_select_f64).  Returns (ids int32 [T,k] in descending key order,
+    boundary_gap float64 [T], order_gap float64 [T])."""
+    g = _c(gating, np.float32)
+    T, E = g.shape
+    b = None if bias is None else _c(bias, np.float32)
+    ids = np.empty((T, top_k), np.int32)
+    bgap = np.empty((T,), np.float64)
+    ogap = np.empty((T,), np.float64)
+    rc = _load().oracle_route_select_f64(T, E, top_k, num_expert_group, topk_group, _ptr(g),
+                                         _ptr(b), _ptr(ids), _ptr(bgap), _ptr(ogap))
+    _check(rc, "oracle_route_select_f64")
+    return ids, bgap, ogap
 
 
 def align_sort(ids, E, block_m):

@@ -274,6 +274,110 @@ int oracle_route(int T, int E, int top_k, int scoring, int renormalize, int num_
   return ORACLE_OK;
 }
 
+/* a ranks before b in fp64: larger key first, equal keys -> lower index first. */
+static int ranks_before_d(double ka, int ia, double kb, int ib) {
+  return ka > kb || (ka == kb && ia < ib);
+}
+
+static int pick_best_d(const double* keys, const unsigned char* allowed, int n) {
+  int best = -1;
+  for (int i = 0; i < n; ++i) {
+    if (!allowed[i]) continue;
+    if (best < 0 || ranks_before_d(keys[i], i, keys[best], best)) best = i;
+  }
+  return best;
+}
+
+/*
+ * oracle_route_select_f64: the sigmoid selection of oracle_route taken on the plain definition,
+ * every step in fp64 (TileOPs "MoE" page, FusedTopKFwd / FusedMoEFwd parameters scoring_func,
+ * correction_bias, num_expert_group, topk_group): s_e = 1 / (1 + exp(-x_e)),
+ * b_e = s_e + correction_bias_e; a group's score is the sum of its two largest b; the topk_group
+ * best groups are kept (ties -> lower group); the top_k largest b among the kept experts are
+ * selected (ties -> lower id), in descending order.  It exists to check the f32 selection key
+ * of oracle_route against the definition it approximates.
+ * Per token it also returns
+ *   boundary_gap  the smallest fp64 gap at a selection boundary: between the last kept and the
+ *                 first dropped group score, and between the top_k-th and the next candidate
+ *                 key (+inf where there is no such pair).  Below ~1e-6 the f32 keys may
+ *                 legitimately choose differently.
+ *   order_gap     the smallest gap between consecutive selected keys (+inf for top_k = 1):
+ *                 below ~1e-6 the f32 keys may order the same experts differently.
+ */
+int oracle_route_select_f64(int T, int E, int top_k, int num_expert_group, int topk_group,
+                            const float* gating, const float* bias, int32_t* ids,
+                            double* boundary_gap, double* order_gap) {
+  if (T < 0 || E <= 0 || top_k <= 0 || top_k > E) return ORACLE_ERR_ARG;
+  int G = num_expert_group > 1 ? num_expert_group : 1;
+  int keepG = G > 1 ? topk_group : 1;
+  if (G > 1 && (E % G != 0 || E / G < 2 || keepG < 1 || keepG > G || keepG * (E / G) < top_k))
+    return ORACLE_ERR_ARG;
+  double* key = (double*)malloc(sizeof(double) * E);
+  unsigned char* allowed = (unsigned char*)malloc(E);
+  double* gscore = (double*)malloc(sizeof(double) * G);
+  unsigned char* gallowed = (unsigned char*)malloc(G);
+  unsigned char* gkeep = (unsigned char*)malloc(G);
+  for (int t = 0; t < T; ++t) {
+    const float* x = gating + (int64_t)t * E;
+    int32_t* id_t = ids + (int64_t)t * top_k;
+    double bgap = INFINITY, ogap = INFINITY;
+    for (int e = 0; e < E; ++e) {
+      double sv = 1.0 / (1.0 + exp(-(double)x[e]));
+      key[e] = bias ? sv + (double)bias[e] : sv;
+      if (key[e] != key[e]) key[e] = -INFINITY; /* a NaN key ranks lowest */
+      allowed[e] = 1;
+    }
+    if (G > 1 && keepG < G) {
+      int gs = E / G;
+      for (int g = 0; g < G; ++g) {
+        double m1 = -INFINITY, m2 = -INFINITY;
+        for (int i = 0; i < gs; ++i) {
+          double v = key[g * gs + i];
+          if (v > m1) { m2 = m1; m1 = v; }
+          else if (v > m2) { m2 = v; }
+        }
+        gscore[g] = m1 + m2;
+        gallowed[g] = 1;
+        gkeep[g] = 0;
+      }
+      int last = -1;
+      for (int j = 0; j < keepG; ++j) {
+        int g = pick_best_d(gscore, gallowed, G);
+        gkeep[g] = 1;
+        gallowed[g] = 0;
+        last = g;
+      }
+      int next = pick_best_d(gscore, gallowed, G);
+      if (next >= 0) bgap = fabs(gscore[last] - gscore[next]);
+      for (int e = 0; e < E; ++e) allowed[e] = gkeep[e / gs];
+    }
+    for (int j = 0; j < top_k; ++j) {
+      int e = pick_best_d(key, allowed, E);
+      id_t[j] = e;
+      allowed[e] = 0;
+      if (j > 0) {
+        double d = fabs(key[id_t[j - 1]] - key[e]);
+        if (d < ogap) ogap = d;
+      }
+    }
+    {
+      int next = pick_best_d(key, allowed, E);
+      if (next >= 0) {
+        double d = fabs(key[id_t[top_k - 1]] - key[next]);
+        if (d < bgap) bgap = d;
+      }
+    }
+    if (boundary_gap) boundary_gap[t] = bgap;
+    if (order_gap) order_gap[t] = ogap;
+  }
+  free(key);
+  free(allowed);
+  free(gscore);
+  free(gallowed);
+  free(gkeep);
+  return ORACLE_OK;
+}
+
 /* ------------------------------------------------------------------------------------------ */
 /* Expert sort (TileOPs "MoE" page, op MoEPermuteAlignFwd; aiter PR #5973 "Changes": the sort */
 /* returns each route's sorted row).  A plain counting sort of flat route indices r = t*k + j. */

@@ -19,3 +19,17 @@ def cuda_device():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     return torch.device("cuda:0")
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Print the parity figures of the output comparisons (rows compared, max|gpu - oracle| /
+    RMS, and what is left after half an ulp of the output's final rounding), also under -q."""
+    helpers = sys.modules.get("helpers")
+    recs = [r for r in getattr(helpers, "PARITY_RECORDS", []) if r.get("summary")]
+    if not recs:
+        return
+    terminalreporter.section("output parity (max|gpu-oracle|/RMS; bound 1e-2 + half ulp)")
+    for r in recs:
+        terminalreporter.write_line(
+            f"{r['what']}: {r['rows']} rows, raw {r['max_err_over_rms']:.4f}, "
+            f"minus half ulp {r['max_err_minus_half_ulp_over_rms']:.4f}")

@@ -35,7 +35,11 @@ def half_ulp(x, dtype):
     return np.maximum(np.where(a > 0, np.exp2(e - bits), 0.0), tiny)
 
 
+PARITY_RECORDS = []  # every log_parity record of this session (conftest prints the summaries)
+
+
 def log_parity(what, **kw):
+    PARITY_RECORDS.append(dict(what=what, **kw))
     path = os.environ.get("MOE_PARITY_LOG")
     if path:
         with open(path, "a") as f:
@@ -86,12 +90,41 @@ def assert_output_close(gpu, ref, dtype, tol=RMS_TOL, what=""):
     hu = half_ulp(r, dtype)
     excess = float(np.max(err - hu)) / rms
     log_parity(what, max_err_over_rms=float(err.max()) / rms, max_err_minus_half_ulp_over_rms=excess,
-               tol=tol)
+               tol=tol, rows=int(r.shape[0]) if r.ndim > 1 else 1, summary=True)
     worst = int(np.argmax(err - hu))
     assert np.all(err <= tol * rms + hu), (f"{what}: |gpu-ref|={err.flat[worst]:.3e} at "
                                            f"ref={r.flat[worst]:.4e}: exceeds {tol}*RMS "
                                            f"({tol * rms:.3e}) + half ulp ({hu.flat[worst]:.3e})")
     return float(err.max()) / rms
+
+
+NEAR_TIE = 1e-6  # fp64 gap at a selection boundary below which the f32 keys may choose otherwise
+
+
+def check_ids_against_plain_selection(w, d, ids, what=""):
+    """Sigmoid routing: the GPU's ids (chosen on f32 keys) against the selection of the plain
+    fp64 definition (oracle.route_select_f64: fp64 sigmoid + bias, groups by the sum of the two
+    largest keys, ties to the lower index).  On every token whose fp64 boundary gap is at
+    least NEAR_TIE the experts must be the same, and in the same order where consecutive
+    selected keys are also that far apart.  Returns (tokens, near-tie tokens at a boundary,
+    tokens with near-equal selected keys), also written to the parity log."""
+    if w.scoring_func != "sigmoid":
+        return None
+    got = ids.cpu().numpy() if isinstance(ids, torch.Tensor) else np.asarray(ids)
+    bias = None if d["correction_bias"] is None else d["correction_bias"].cpu().numpy()
+    ref, bgap, ogap = oracle.route_select_f64(d["gating_output"].cpu().numpy(), w.top_k,
+                                              w.num_expert_group, w.topk_group, bias)
+    clear = bgap >= NEAR_TIE
+    same_set = np.all(np.sort(got, axis=1) == np.sort(ref, axis=1), axis=1)
+    bad = np.nonzero(clear & ~same_set)[0]
+    assert bad.size == 0, f"{what}: ids differ from the fp64 selection on tokens {bad[:10]}"
+    ordered = clear & (ogap >= NEAR_TIE)
+    assert np.array_equal(got[ordered], ref[ordered]), f"{what}: id order differs from fp64"
+    counts = (int(got.shape[0]), int((~clear).sum()), int((clear & ~ordered).sum()))
+    log_parity(what, tokens=counts[0], near_tie_tokens=counts[1], order_near_tie_tokens=counts[2])
+    print(f"{what}: ids equal the fp64 selection on {counts[0] - counts[1]} of {counts[0]} "
+          f"tokens ({counts[1]} near-tie at a boundary, {counts[2]} with near-equal keys)")
+    return counts
 
 
 def scoring_code(w):
@@ -134,9 +167,12 @@ def oracle_fused(w, d, tokens=None, routed=None):
     used = sorted(set(int(e) for e in ids[tl].reshape(-1) if e >= 0))
     slot = np.full(w.E_local, -1, np.int32)
     slot[used] = np.arange(len(used), dtype=np.int32)
-    idx = torch.tensor(used, dtype=torch.long, device=d["w_gate_up"].device)
-    wgu = d["w_gate_up"].index_select(0, idx).cpu() if used else d["w_gate_up"][:1].cpu()
-    wd = d["w_down"].index_select(0, idx).cpu() if used else d["w_down"][:1].cpu()
+    if len(used) == w.E_local:  # every expert: copy the weights as they are
+        wgu, wd = d["w_gate_up"].cpu(), d["w_down"].cpu()
+    else:
+        idx = torch.tensor(used, dtype=torch.long, device=d["w_gate_up"].device)
+        wgu = d["w_gate_up"].index_select(0, idx).cpu() if used else d["w_gate_up"][:1].cpu()
+        wd = d["w_down"].index_select(0, idx).cpu() if used else d["w_down"][:1].cpu()
     sgu = None if d["shared_w_gate_up"] is None else d["shared_w_gate_up"].cpu()
     sd = None if d["shared_w_down"] is None else d["shared_w_down"].cpu()
     out = oracle.moe_tokens(d["hidden_states"].cpu(), ids, wts, wgu, wd, dt_code(w.dtype),

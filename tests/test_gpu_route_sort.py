@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import oracle_route, run_route
+from helpers import check_ids_against_plain_selection, oracle_route, run_route
 from mixture_experts_forward_moe_gb300 import binding as B
 from mixture_experts_forward_moe_gb300 import inputs
 
@@ -37,6 +37,7 @@ def test_route_matches_oracle(w, cuda_device):
     r_ids, r_w, _ = oracle_route(w, d)
     assert np.array_equal(ids.cpu().numpy(), r_ids)
     np.testing.assert_allclose(wts.cpu().numpy(), r_w, rtol=2e-6, atol=1e-7)
+    check_ids_against_plain_selection(w, d, ids, what=f"route {w.name}")
 
 
 def test_route_ties_go_to_lower_id(cuda_device):

@@ -264,7 +264,7 @@ def test_w4a16_rejects_unsupported_shapes(cuda_device):
 
 FULL = [
     ("qwen3-30b-a3b-decode-t32-w4a16", None),
-    ("deepseek-v3-ep8-shard-t512-w4a16", 24),
+    ("deepseek-v3-ep8-shard-t512-w4a16", None),
 ]
 
 
@@ -293,7 +293,7 @@ def test_w4a16_full_size_workloads(name, n_sample, cuda_device):
 
 @pytest.mark.parametrize("name,n_sample", [("deepseek-v3-ep8-shard-t32-w4a16", None),
                                            ("deepseek-v3-ep8-shard-t32", None),
-                                           ("deepseek-v3-ep8-shard-t4096", 16)],
+                                           ("deepseek-v3-ep8-shard-t4096", 512)],
                          ids=["t32-w4a16", "t32-bf16", "t4096-bf16"])
 def test_ep8_shards_of_deepseek_v3_sum_to_full_output(name, n_sample, cuda_device):
     """The eight EP8 shards of DeepSeek-V3 (32 experts each), run one after another."""

@@ -146,6 +146,100 @@ def test_route_grouped_brute_force(E, G, keep, k):
         np.testing.assert_allclose(w[t], s / s.sum() * 2.5, rtol=1e-12)
 
 
+@pytest.mark.parametrize("E,G,keep,k", [(16, 0, 0, 4), (16, 4, 2, 4), (24, 6, 3, 5),
+                                         (32, 8, 4, 8), (12, 4, 1, 2), (8, 0, 0, 1)])
+def test_route_select_f64_brute_force(E, G, keep, k):
+    """The plain-definition selection (fp64 sigmoid + bias) against a brute force over every
+    subset of groups and a full sort, with its boundary and order gaps recomputed here."""
+    rng = np.random.default_rng(100 + E + G + keep + k)
+    T = 60
+    g = rng.standard_normal((T, E)).astype(np.float32)
+    bias = (0.1 * rng.standard_normal(E)).astype(np.float32)
+    g[0, :] = 0.0  # equal logits
+    g[1, : E // 2] = g[1, E // 2:]  # pairwise equal logits
+    ids, bgap, ogap = oracle.route_select_f64(g, k, G, keep, bias)
+    grouped = G > 1 and keep < G
+    for t in range(T):
+        keys = scipy.special.expit(g[t].astype(np.float64)) + bias.astype(np.float64)
+        allowed = [True] * E
+        want_b = math.inf
+        if grouped:
+            gs = E // G
+            scores = [sum(sorted(keys[x * gs:(x + 1) * gs].tolist())[-2:]) for x in range(G)]
+            order = sorted(range(G), key=lambda x: (-scores[x], x))
+            best = set(order[:keep])
+            best_sub = min(itertools.combinations(range(G), keep),
+                           key=lambda sub: sorted((-scores[x], x) for x in sub))
+            assert best == set(best_sub)
+            allowed = [(e // gs) in best for e in range(E)]
+            want_b = abs(scores[order[keep - 1]] - scores[order[keep]])
+        cand = sorted((e for e in range(E) if allowed[e]), key=lambda e: (-keys[e], e))
+        assert list(ids[t]) == cand[:k], t
+        if len(cand) > k:
+            want_b = min(want_b, abs(keys[cand[k - 1]] - keys[cand[k]]))
+        want_o = min((abs(keys[cand[j]] - keys[cand[j + 1]]) for j in range(k - 1)),
+                     default=math.inf)
+        assert bgap[t] == pytest.approx(want_b, rel=1e-12, abs=1e-15)
+        assert ogap[t] == pytest.approx(want_o, rel=1e-12, abs=1e-15)
+    # without a bias every key of row 0 is sigmoid(0): all ties, lower groups and ids win
+    ids0, bgap0, ogap0 = oracle.route_select_f64(g[:1], k, G, keep, None)
+    assert list(ids0[0]) == list(range(k))
+    assert bgap0[0] == (0.0 if (grouped or k < E) else math.inf)
+    assert ogap0[0] == (0.0 if k > 1 else math.inf)
+
+
+# Routing inputs of the sigmoid workloads, drawn on the CPU with their distributions
+# (gating ~ N(0,1) f32, correction_bias ~ N(0, 0.1^2)): name, T, E, top_k, groups, kept.
+SIGMOID_ROUTING = [
+    ("deepseek-v3-grouped-prefill-t4096", 4096, 256, 8, 8, 4),
+    ("kimi-k2-shared-t512", 512, 384, 8, 0, 0),
+    ("sorted-grouped", 160, 64, 6, 8, 3),
+    ("sorted-sigmoid-shared", 96, 24, 4, 0, 0),
+    ("smoke-sorted", 24, 16, 4, 4, 2),
+]
+NEAR_TIE = 1e-6
+
+
+@pytest.mark.parametrize("name,T,E,k,G,keep", SIGMOID_ROUTING, ids=[r[0] for r in SIGMOID_ROUTING])
+def test_f32_routing_key_selects_as_the_plain_definition(name, T, E, k, G, keep):
+    """oracle_route selects on an f32 sigmoid key (the precision of gating_output).  On every
+    token whose fp64 selection boundary gap is at least 1e-6 it must choose the same experts as
+    the plain fp64 definition, and in the same order where consecutive selected keys are also
+    that far apart; closer tokens are counted (expected: none or a handful).  The f32 key is
+    within 3 ulp of the true sigmoid, so a gap of 1e-6 leaves a margin of about 5x."""
+    near_total = 0
+    for seed in range(3):
+        gen = torch.Generator().manual_seed(seed)
+        g = torch.randn((T, E), generator=gen, dtype=torch.float32).numpy()
+        bias = (0.1 * torch.randn((E,), generator=gen, dtype=torch.float32)).numpy()
+        ids32, _, _ = oracle.route(g, k, oracle.SIGMOID, True, G, keep, 2.5, bias)
+        ids64, bgap, ogap = oracle.route_select_f64(g, k, G, keep, bias)
+        clear = bgap >= NEAR_TIE
+        same_set = np.all(np.sort(ids32, axis=1) == np.sort(ids64, axis=1), axis=1)
+        assert np.all(same_set[clear]), np.nonzero(clear & ~same_set)[0][:10]
+        ordered = clear & (ogap >= NEAR_TIE)
+        assert np.array_equal(ids32[ordered], ids64[ordered])
+        near = int((~clear).sum())
+        near_total += near
+        print(f"{name} seed {seed}: {T} tokens, {near} near-tie at the selection boundary, "
+              f"{int((clear & ~ordered).sum())} with near-equal selected keys")
+    assert near_total <= max(3, 3 * T // 1000)
+
+
+def test_f32_routing_key_differs_from_plain_only_at_near_ties():
+    """A constructed near-tie: two experts whose fp64 keys differ by less than the f32 key's
+    resolution.  The plain definition ranks them by fp64; the gap reported is below 1e-6, so
+    the cross-check above accepts either choice for that token only."""
+    E, k = 8, 1
+    g = np.full((1, E), -4.0, np.float32)
+    g[0, 2] = np.float32(1.0)
+    g[0, 5] = np.nextafter(np.float32(1.0), np.float32(2.0))  # one f32 ulp above
+    _, bgap, _ = oracle.route_select_f64(g, k, 0, 0, None)
+    ids64, _, _ = oracle.route_select_f64(g, k, 0, 0, None)
+    assert ids64[0, 0] == 5
+    assert 0 < bgap[0] < NEAR_TIE
+
+
 def test_grouping_with_all_groups_kept_equals_ungrouped():
     rng = np.random.default_rng(3)
     g = rng.standard_normal((50, 32)).astype(np.float32)
