@@ -151,6 +151,31 @@ moe_status_t fused_moe_fwd(const moe_problem_t* p, const void* hidden_states,
                            size_t workspace_bytes, void* stream);
 
 /*
+ * fused_moe_fwd_host -- fused_moe_fwd (TileOPs "MoE" page, ops FusedMoEFwd and
+ * FusedMoESharedExpertFwd) for a caller whose batch lives in HOST memory:
+ *   hidden_states_host  [T,H] dtype, host memory
+ *   gating_output_host  [T,E] f32, host memory
+ *   out_host            [T,H] dtype, host memory (written in full)
+ * The weights, correction_bias and workspace are device memory, as in fused_moe_fwd.  On
+ * `stream` the call enqueues one cudaMemcpyAsync host->device per input into staging buffers
+ * at the end of the workspace, the fused forward, and one cudaMemcpyAsync device->host of the
+ * output; it returns without synchronising, and out_host holds the result once the stream has
+ * passed that point.  Page-locked host buffers keep the copies asynchronous (with pageable
+ * memory CUDA stages them and the call may block the host).  The host buffers must stay valid
+ * and unmodified until then.
+ *   workspace_bytes >= moe_workspace_size(p) + moe_host_staging_bytes(p); the staging takes the
+ * last moe_host_staging_bytes(p) bytes below the 256-byte-aligned end of the workspace.
+ * Argument errors (the checks of fused_moe_fwd included) return before anything is enqueued.
+ */
+size_t moe_host_staging_bytes(const moe_problem_t* p);
+moe_status_t fused_moe_fwd_host(const moe_problem_t* p, const void* hidden_states_host,
+                                const float* gating_output_host, const void* w_gate_up,
+                                const void* w_down, const float* correction_bias,
+                                const void* shared_w_gate_up, const void* shared_w_down,
+                                void* out_host, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/*
  * fused_moe_fwd_w4a16 -- fused_moe_fwd with NVFP4 routed experts and bf16 activations
  * (flashinfer PR #4048, quant_mode "w4a16": NVFP4 weights decoded for a BF16 MMA, the FP32
  * per-expert scale applied to the FP32 accumulator, as its weight-scale placement ablation
@@ -173,6 +198,17 @@ moe_status_t fused_moe_fwd_w4a16(const moe_problem_t* p, const void* hidden_stat
                                  const float* w_down_alpha, const float* correction_bias,
                                  void* out, void* workspace, size_t workspace_bytes,
                                  void* stream);
+
+/* fused_moe_fwd_w4a16 from host buffers, as fused_moe_fwd_host: workspace_bytes >=
+ * moe_workspace_size(p) (or moe_workspace_size_w4a16(p), for the split-K scratch) +
+ * moe_host_staging_bytes(p). */
+moe_status_t fused_moe_fwd_w4a16_host(const moe_problem_t* p, const void* hidden_states_host,
+                                      const float* gating_output_host,
+                                      const uint8_t* w_gate_up_tiles,
+                                      const float* w_gate_up_alpha, const uint8_t* w_down_tiles,
+                                      const float* w_down_alpha, const float* correction_bias,
+                                      void* out_host, void* workspace, size_t workspace_bytes,
+                                      void* stream);
 
 /*
  * moe_nvfp4_pack -- rearrange NVFP4 weights into the tile layout the W4A16 GEMMs stream (a

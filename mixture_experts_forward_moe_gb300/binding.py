@@ -41,7 +41,8 @@ EXPORTED = (
     "moe_profile_collect", "moe_align_sort_noalloc", "fused_moe_fwd_w4a16", "moe_gemm1_w4a16",
     "moe_gemm2_w4a16", "moe_nvfp4_pack", "moe_nvfp4_packed_bytes", "moe_pre_permute",
     "moe_grouped_gemm_workspace_size", "moe_grouped_gemm", "moe_post_permute",
-    "moe_grouped_gemm_fp8",
+    "moe_grouped_gemm_fp8", "moe_host_staging_bytes", "fused_moe_fwd_host",
+    "fused_moe_fwd_w4a16_host",
 )
 
 
@@ -119,6 +120,10 @@ def lib():
             L.moe_align_sort_noalloc.restype = ctypes.c_int
             L.moe_align_sort_noalloc.argtypes = [PP, i32, P, P, P, P, P, P, P, P]
             L.fused_moe_fwd_w4a16.argtypes = [PP, P, P, P, P, P, P, P, P, P, sz, P]
+            L.moe_host_staging_bytes.restype = sz
+            L.moe_host_staging_bytes.argtypes = [PP]
+            L.fused_moe_fwd_host.argtypes = [PP, P, P, P, P, P, P, P, P, P, sz, P]
+            L.fused_moe_fwd_w4a16_host.argtypes = [PP, P, P, P, P, P, P, P, P, P, sz, P]
             L.moe_gemm1_w4a16.argtypes = [PP, i32, P, P, P, P, P, P, P, sz, P]
             L.moe_gemm2_w4a16.argtypes = [PP, i32, P, P, P, P, P, P, P, P, sz, P]
             L.moe_nvfp4_pack.restype = ctypes.c_int
@@ -475,23 +480,69 @@ def moe_shared_expert_fwd(hidden_states, shared_w_gate_up, shared_w_down, worksp
     return out
 
 
-def fused_moe_fwd_host(hidden_host, gating_host, w_gate_up, w_down, top_k, out_host=None,
-                       dev_bufs=None, **kw):
-    """End-to-end call from pinned HOST buffers: host->device copies of the step's inputs, the
-    fused forward, and the device->host copy of the output, all on the current stream."""
+def _need_host(t, name, dtype, shape):
+    if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous host tensor")
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be {dtype} {tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
+
+
+def host_workspace_size(prob: MoeProblem, w4a16=False) -> int:
+    """Workspace bytes of the host entry points: the fused call's plus the device staging of
+    the inputs and the output (include/moe.h: moe_host_staging_bytes)."""
+    base = workspace_size_w4a16(prob) if w4a16 else workspace_size(prob)
+    return base + int(lib().moe_host_staging_bytes(ctypes.byref(prob)))
+
+
+def fused_moe_fwd_host(hidden_host, gating_host, w_gate_up, w_down, top_k, renormalize=True,
+                       scoring_func="softmax", correction_bias=None, num_expert_group=0,
+                       topk_group=0, routed_scaling_factor=1.0, shared_w_gate_up=None,
+                       shared_w_down=None, out_host=None, workspace=None, stream=None,
+                       activation="silu", ep_local_offset=0):
+    """The fused forward from HOST buffers in one library call (include/moe.h:
+    fused_moe_fwd_host, or fused_moe_fwd_w4a16_host for Nvfp4Weights): the host->device copies
+    of hidden_host and gating_host, the fused path and the device->host copy into out_host
+    (page-locked when it is created here) are all enqueued on the stream by the library.
+    Returns out_host, valid once the stream has reached the end of the call."""
+    w4 = isinstance(w_gate_up, Nvfp4Weights)
+    T, H = hidden_host.shape
+    E = gating_host.shape[1]
+    dt = hidden_host.dtype
     dev = w_gate_up.device
-    if dev_bufs is None:
-        dev_bufs = dict(hidden=torch.empty(hidden_host.shape, dtype=hidden_host.dtype, device=dev),
-                        gating=torch.empty(gating_host.shape, dtype=gating_host.dtype, device=dev))
-    dev_bufs["hidden"].copy_(hidden_host, non_blocking=True)
-    dev_bufs["gating"].copy_(gating_host, non_blocking=True)
-    fwd = fused_moe_fwd_w4a16 if isinstance(w_gate_up, Nvfp4Weights) else fused_moe_fwd
-    out = fwd(dev_bufs["hidden"], dev_bufs["gating"], w_gate_up, w_down, top_k,
-              out=dev_bufs.get("out"), **kw)
-    dev_bufs["out"] = out
+    if w4:
+        E_l, F = w_gate_up.n_mats, w_down.K
+        _need_w4(w_gate_up, "w_gate_up", E_l, gate_up_rows(activation, F), H)
+        _need_w4(w_down, "w_down", E_l, H, F)
+        S = 0
+    else:
+        E_l, F = w_gate_up.shape[0], w_down.shape[2]
+        _need(w_gate_up, "w_gate_up", dt, (E_l, gate_up_rows(activation, F), H))
+        _need(w_down, "w_down", dt, (E_l, H, F))
+        S = 0 if shared_w_down is None else shared_w_down.shape[1]
+    _need_host(hidden_host, "hidden_host", dt, (T, H))
+    _need_host(gating_host, "gating_host", torch.float32, (T, E))
+    if correction_bias is not None:
+        _need(correction_bias, "correction_bias", torch.float32, (E,))
+    prob = make_problem(T, H, E, F, top_k, dt, scoring_func, renormalize, num_expert_group,
+                        topk_group, routed_scaling_factor, S, activation,
+                        E_l if E_l != E else 0, ep_local_offset)
+    if workspace is None:
+        workspace = _workspace(host_workspace_size(prob, w4), dev)
     if out_host is None:
-        out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    out_host.copy_(out, non_blocking=True)
+        out_host = torch.empty((T, H), dtype=dt, pin_memory=True)
+    _need_host(out_host, "out_host", dt, (T, H))
+    if w4:
+        rc = lib().fused_moe_fwd_w4a16_host(
+            ctypes.byref(prob), _p(hidden_host), _p(gating_host), _p(w_gate_up.tiles),
+            _p(w_gate_up.alpha), _p(w_down.tiles), _p(w_down.alpha), _p(correction_bias),
+            _p(out_host), _p(workspace), workspace.numel(), _stream(stream))
+        _check(rc, "fused_moe_fwd_w4a16_host")
+    else:
+        rc = lib().fused_moe_fwd_host(
+            ctypes.byref(prob), _p(hidden_host), _p(gating_host), _p(w_gate_up), _p(w_down),
+            _p(correction_bias), _p(shared_w_gate_up), _p(shared_w_down), _p(out_host),
+            _p(workspace), workspace.numel(), _stream(stream))
+        _check(rc, "fused_moe_fwd_host")
     return out_host
 
 

@@ -128,6 +128,14 @@ int sorted_tile_rows(const moe_problem_t& p) {
   return P / active <= 32 ? kTileRowsNarrow : kTileRows;
 }
 
+// The down projection of fused_moe_fwd runs on pairs of SMs (gemm_pair.cu) when its tiles have
+// 256 rows (experts average at least 96 routed rows) and H splits into whole 256-row pair units.
+bool use_pair_gemm2(const moe_problem_t& p) {
+  if (p.T <= kTileRows || sorted_tile_rows(p) != kTileRowsWide) return false;
+  if (p.H % (2 * kSlab) != 0) return false;
+  return pair_gemm_available(p.dtype);
+}
+
 // Token rows per tile of the dense shared-expert GEMMs.
 int dense_tile_rows(const moe_problem_t& p) { return p.T > kTileRows ? kTileRowsWide : kTileRows; }
 
@@ -416,6 +424,7 @@ moe_status_t run_fused(const moe_problem_t* p, const Experts& X, const void* hid
     // With T <= 128 every expert's rows fit one tile of all T tokens: gemm1 reads hidden_states
     // directly and no gathered copy is made.
     const bool token_rows = P.T <= kTileRows;
+    const bool pair2 = !X.w4 && use_pair_gemm2(P);
     SplitLayout S{0, 0, 0, 0, 0};
     if (X.w4 && token_rows) {
       S = split_layout(P);
@@ -491,7 +500,7 @@ moe_status_t run_fused(const moe_problem_t* p, const Experts& X, const void* hid
     g2.early_tiles = 1;  // sort, [permute,] gemm1, then gemm2
     {
       StageTimer t(kGemm2, s);
-      MOE_TRY(launch_gemm(g2, s, true));
+      MOE_TRY(pair2 ? launch_gemm_pair(g2, s, true) : launch_gemm(g2, s, true));
       t.done(1);
     }
     inv = inv_route;
@@ -529,6 +538,100 @@ moe_status_t fused_moe_fwd_w4a16(const moe_problem_t* p, const void* hidden_stat
   const Experts X{w_gate_up_tiles, w_down_tiles, w_gate_up_alpha, w_down_alpha, 1};
   return run_fused(p, X, hidden_states, gating_output, correction_bias, nullptr, nullptr, out,
                    workspace, workspace_bytes, stream);
+}
+
+// ---- from host buffers -------------------------------------------------------------------
+namespace {
+
+// Staging for the host entry points, carved from the END of the caller's workspace: hidden
+// states [T,H] dtype, router logits [T,E] f32 and the output [T,H] dtype, each 256-byte aligned.
+struct HostStaging {
+  size_t hidden, gating, out, total;
+};
+
+HostStaging host_staging(const moe_problem_t& p) {
+  HostStaging h;
+  h.hidden = align_up((size_t)p.T * p.H * elt_bytes(p), 256);
+  h.gating = align_up((size_t)p.T * p.E * sizeof(float), 256);
+  h.out = h.hidden;
+  h.total = h.hidden + h.gating + h.out;
+  return h;
+}
+
+}  // namespace
+
+size_t moe_host_staging_bytes(const moe_problem_t* p) {
+  if (check_problem(p) != MOE_OK) return 0;
+  return host_staging(*p).total;
+}
+
+namespace {
+
+moe_status_t run_fused_host(const moe_problem_t* p, const Experts& X, const void* hidden_host,
+                            const float* gating_host, const float* correction_bias,
+                            const void* shared_w_gate_up, const void* shared_w_down,
+                            void* out_host, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  moe_status_t st = check_problem(p);
+  if (st != MOE_OK) return st;
+  if (!workspace) return MOE_ERR_INVALID_ARG;
+  if (p->T > 0 && (!hidden_host || !gating_host || !out_host)) return MOE_ERR_INVALID_ARG;
+  const HostStaging h = host_staging(*p);
+  if (workspace_bytes < h.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  // The staging sits at the 256-byte-aligned end; the fused path gets the bytes before it.
+  const uintptr_t end = (reinterpret_cast<uintptr_t>(workspace) + workspace_bytes) & ~(uintptr_t)255;
+  if (end < reinterpret_cast<uintptr_t>(workspace) + h.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  char* stage = reinterpret_cast<char*>(end - h.total);
+  const size_t fused_bytes = (size_t)(stage - static_cast<char*>(workspace));
+  void* d_hidden = stage;
+  float* d_gating = reinterpret_cast<float*>(stage + h.hidden);
+  void* d_out = stage + h.hidden + h.gating;
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t hid_bytes = (size_t)p->T * p->H * elt_bytes(*p);
+  if (p->T > 0) {
+    // Argument errors of the fused call come back before anything is enqueued: check them on
+    // the device staging addresses first (T = 0 would skip the checks of the weights).
+    if (!X.w1 || !X.w2 || (X.w4 && (!X.a1 || !X.a2))) return MOE_ERR_INVALID_ARG;
+    if (X.w4 && (st = check_w4(*p)) != MOE_OK) return st;
+    if ((p->S > 0) != (shared_w_gate_up != nullptr) || (p->S > 0) != (shared_w_down != nullptr))
+      return MOE_ERR_INVALID_ARG;
+    if (correction_bias && p->scoring != MOE_SIGMOID) return MOE_ERR_UNSUPPORTED;
+    if (fused_bytes < make_layout(*p, 1).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    MOE_TRY(cudaMemcpyAsync(d_hidden, hidden_host, hid_bytes, cudaMemcpyHostToDevice, s));
+    MOE_TRY(cudaMemcpyAsync(d_gating, gating_host, (size_t)p->T * p->E * sizeof(float),
+                            cudaMemcpyHostToDevice, s));
+  }
+  st = run_fused(p, X, d_hidden, d_gating, correction_bias, shared_w_gate_up, shared_w_down,
+                 d_out, workspace, fused_bytes, stream);
+  if (st != MOE_OK || p->T == 0) return st;
+  MOE_TRY(cudaMemcpyAsync(out_host, d_out, hid_bytes, cudaMemcpyDeviceToHost, s));
+  return MOE_OK;
+}
+
+}  // namespace
+
+moe_status_t fused_moe_fwd_host(const moe_problem_t* p, const void* hidden_states_host,
+                                const float* gating_output_host, const void* w_gate_up,
+                                const void* w_down, const float* correction_bias,
+                                const void* shared_w_gate_up, const void* shared_w_down,
+                                void* out_host, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  const Experts X{w_gate_up, w_down, nullptr, nullptr, 0};
+  return run_fused_host(p, X, hidden_states_host, gating_output_host, correction_bias,
+                        shared_w_gate_up, shared_w_down, out_host, workspace, workspace_bytes,
+                        stream);
+}
+
+moe_status_t fused_moe_fwd_w4a16_host(const moe_problem_t* p, const void* hidden_states_host,
+                                      const float* gating_output_host,
+                                      const uint8_t* w_gate_up_tiles,
+                                      const float* w_gate_up_alpha, const uint8_t* w_down_tiles,
+                                      const float* w_down_alpha, const float* correction_bias,
+                                      void* out_host, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+  const Experts X{w_gate_up_tiles, w_down_tiles, w_gate_up_alpha, w_down_alpha, 1};
+  return run_fused_host(p, X, hidden_states_host, gating_output_host, correction_bias, nullptr,
+                        nullptr, out_host, workspace, workspace_bytes, stream);
 }
 
 moe_status_t moe_route(const moe_problem_t* p, const float* gating_output,

@@ -218,6 +218,12 @@ struct GemmCall {
 
 cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl);
 
+// The grouped down projection on pairs of SMs (gemm_pair.cu): sorted mode with 256-row tiles,
+// 16-bit weights, n_out a multiple of 256.  pair_gemm_available: whether clusters of two fit on
+// this device.
+cudaError_t launch_gemm_pair(const GemmCall& c, cudaStream_t s, bool pdl);
+bool pair_gemm_available(int dtype);
+
 uint64_t wait_limit_ns();
 int num_sms();
 

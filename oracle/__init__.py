@@ -74,7 +74,7 @@ def _load():
             _lib.oracle_route_select_f64.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P]
             _lib.oracle_align_sort.argtypes = [i32, i32, i32, i32, P, P, P, P, i64, P, i64, P]
             _lib.oracle_moe_tokens.argtypes = [i32, P, i32, i32, i32, i32, i32, i32, i32, P, P, P,
-                                               P, P, P, i32, P, P, P]
+                                               P, P, P, i32, P, P, P, P]
             _lib.oracle_expert_act.argtypes = [i32, i32, i32, i32, i32, P, P, P, P]
             _lib.oracle_expert_down.argtypes = [i32, i32, i32, i32, P, P, P, P, P]
             _lib.oracle_combine.argtypes = [i32, i32, i32, i32, P, P, P, P]
@@ -88,7 +88,7 @@ def _load():
             _lib.oracle_e4m3_to_double.argtypes = [i32]
             _lib.oracle_nvfp4_dequant.argtypes = [i64, i32, P, P, P, i64, P]
             _lib.oracle_moe_tokens_w4.argtypes = [i32, P, i32, i32, i32, i32, i32, i32, i32, P,
-                                                  P, P, P, P, P, P, P, P, P]
+                                                  P, P, P, P, P, P, P, P, P, P]
             _lib.oracle_expert_act_w4.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P]
             _lib.oracle_expert_down_w4.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P]
     return _lib
@@ -196,13 +196,15 @@ def align_sort(ids, E, block_m):
 
 def moe_tokens(hidden, ids, weights, w_gate_up, w_down, dtype, tokens=None, expert_slot=None,
                shared_w_gate_up=None, shared_w_down=None, num_experts=None,
-               activation=ACT_SILU):
+               activation=ACT_SILU, act_noise=False):
     """fp64 fused MoE output for the listed tokens (all tokens when ``tokens`` is None).
 
     hidden/w_* are 16-bit bit arrays (or torch tensors).  When ``expert_slot`` is given,
     w_gate_up/w_down hold only the slots it maps experts to and ``num_experts`` is E.
     ``activation`` is ACT_SILU, ACT_GELU_TANH (both gated: w_gate_up has 2F rows per expert) or
-    ACT_RELU2 (F rows per expert)."""
+    ACT_RELU2 (F rows per expert).  With ``act_noise`` returns (out, noise): noise is the
+    per-element scale of the error that rounding each act value to ``dtype`` before the down
+    projection adds (oracle.c: oracle_moe_tokens)."""
     hb = _bits(hidden)
     T, H = hb.shape
     idv = _c(ids, np.int32)
@@ -218,15 +220,16 @@ def moe_tokens(hidden, ids, weights, w_gate_up, w_down, dtype, tokens=None, expe
     S = 0 if sd is None else sd.shape[-1]
     tl = np.arange(T, dtype=np.int32) if tokens is None else _c(tokens, np.int32)
     out = np.empty((tl.size, H), np.float64)
+    noise = np.empty((tl.size, H), np.float64) if act_noise else None
     if wgu.shape[-2] != gate_up_rows(activation, F) or (
             sgu is not None and sgu.shape[0] != gate_up_rows(activation, S)):
         raise ValueError("w_gate_up rows do not match the activation")
     rc = _load().oracle_moe_tokens(tl.size, _ptr(tl), T, H, E, F, k, dtype, activation,
                                    _ptr(hb), _ptr(idv),
                                    _ptr(wv), _ptr(wgu), _ptr(wd), _ptr(slot), S, _ptr(sgu),
-                                   _ptr(sd), _ptr(out))
+                                   _ptr(sd), _ptr(out), _ptr(noise))
     _check(rc, "oracle_moe_tokens")
-    return out
+    return (out, noise) if act_noise else out
 
 
 def expert_act(x_rows, expert_of_row, w_gate_up, dtype, activation=ACT_SILU):
@@ -302,10 +305,11 @@ def nvfp4_dequant(q, sf, alpha, rows_per_alpha=None):
     return out
 
 
-def moe_tokens_w4(hidden, ids, weights, w1, w2, dtype, tokens=None, activation=ACT_SILU):
+def moe_tokens_w4(hidden, ids, weights, w1, w2, dtype, tokens=None, activation=ACT_SILU,
+                  act_noise=False):
     """fp64 fused MoE output with NVFP4 experts.  w1 = (q [E,R1,H/2], sf [E,R1,H/16], alpha [E])
     for the gate/up projection (R1 = 2F, or F for ReLU2), w2 = (q [E,H,F/2], sf [E,H,F/16],
-    alpha [E]) for the down projection."""
+    alpha [E]) for the down projection.  ``act_noise``: as in moe_tokens."""
     hb = _bits(hidden)
     T, H = hb.shape
     idv = _c(ids, np.int32)
@@ -319,11 +323,12 @@ def moe_tokens_w4(hidden, ids, weights, w1, w2, dtype, tokens=None, activation=A
         raise ValueError("w1 does not match the activation and shapes")
     tl = np.arange(T, dtype=np.int32) if tokens is None else _c(tokens, np.int32)
     out = np.empty((tl.size, H), np.float64)
+    noise = np.empty((tl.size, H), np.float64) if act_noise else None
     rc = _load().oracle_moe_tokens_w4(tl.size, _ptr(tl), T, H, E, F, k, dtype, activation,
                                       _ptr(hb), _ptr(idv), _ptr(wv), _ptr(q1), _ptr(s1), _ptr(a1),
-                                      _ptr(q2), _ptr(s2), _ptr(a2), _ptr(out))
+                                      _ptr(q2), _ptr(s2), _ptr(a2), _ptr(out), _ptr(noise))
     _check(rc, "oracle_moe_tokens_w4")
-    return out
+    return (out, noise) if act_noise else out
 
 
 def expert_act_w4(x_rows, expert_of_row, w1, dtype, activation=ACT_SILU):

@@ -487,6 +487,36 @@ static void down_rows(const double* tab, const uint16_t* wd, const double* act, 
   }
 }
 
+/* Half the spacing of a 16-bit float type at |a| (dtype 0 bf16: 8 significant bits, 1 f16:
+ * 11; below the smallest normal the subnormal spacing): the largest error of rounding a to it. */
+static double half_ulp16(int dtype, double a) {
+  a = fabs(a);
+  if (a == 0.0) return 0.0;
+  int ex;
+  frexp(a, &ex); /* a = m * 2^ex with m in [0.5, 1): a lies in the binade [2^(ex-1), 2^ex) */
+  const int bits = dtype == 0 ? 8 : 11;
+  const int emin = dtype == 0 ? -126 : -14;
+  const int e = ex - 1 < emin ? emin : ex - 1;
+  return ldexp(1.0, e - bits);
+}
+
+/* noise[h] += wsq * sum_f (Wd[h,f] * half_ulp16(act[f]))^2: the variance scale of the error that
+ * rounding act to the 16-bit type adds to y[h] = Wd . act (each rounding error lies within
+ * +-half an ulp of its act value). */
+static void down_noise(const double* tab, const uint16_t* wd, const double* act, int H, int F,
+                       int dtype, double wsq, double* u, double* noise) {
+  for (int f = 0; f < F; ++f) u[f] = half_ulp16(dtype, act[f]);
+  for (int h = 0; h < H; ++h) {
+    const uint16_t* w = wd + (int64_t)h * F;
+    double s = 0.0;
+    for (int f = 0; f < F; ++f) {
+      const double c = tab[w[f]] * u[f];
+      s += c * c;
+    }
+    noise[h] += wsq * s;
+  }
+}
+
 /* Expert weights are addressed through slot[e] (identity when slot is NULL) so that a caller
  * can pass only the experts a sampled set of tokens touches. */
 static const uint16_t* expert_ptr(const uint16_t* base, const int32_t* slot, int e, int64_t stride) {
@@ -502,12 +532,17 @@ static const uint16_t* expert_ptr(const uint16_t* base, const int32_t* slot, int
  * with act() the activation selected by `activation` (ORACLE_ACT_*, see act_rows); the shared
  * expert uses the same activation.
  * Routes with id -1 are skipped.  out is [n_tok, H] in the order of tok_list.
+ * act_noise (nullable, [n_tok, H]): per output element
+ *   sqrt( sum_j weights[t,j]^2 sum_f (W_down[e_j][h,f] u(act_j[f]))^2 + shared term )
+ * with u(a) half an ulp of the 16-bit dtype at a -- the scale of the error a computation that
+ * rounds each act value to that dtype before the down projection makes (a diagnostic of the
+ * arithmetic; out itself never rounds).
  */
 int oracle_moe_tokens(int n_tok, const int32_t* tok_list, int T, int H, int E, int F, int top_k,
                       int dtype, int activation, const uint16_t* hidden, const int32_t* ids,
                       const double* weights, const uint16_t* w_gate_up, const uint16_t* w_down,
                       const int32_t* expert_slot, int S, const uint16_t* shared_w_gate_up,
-                      const uint16_t* shared_w_down, double* out) {
+                      const uint16_t* shared_w_down, double* out, double* act_noise) {
   if (n_tok < 0 || H <= 0 || E <= 0 || F <= 0 || top_k <= 0 || (dtype != 0 && dtype != 1) ||
       activation < ORACLE_ACT_SILU || activation > ORACLE_ACT_RELU2)
     return ORACLE_ERR_ARG;
@@ -525,8 +560,12 @@ int oracle_moe_tokens(int n_tok, const int32_t* tok_list, int T, int H, int E, i
     double* x = (double*)malloc(sizeof(double) * H);
     double* act = (double*)malloc(sizeof(double) * Fmax);
     double* y = (double*)malloc(sizeof(double) * H);
+    double* u = act_noise ? (double*)malloc(sizeof(double) * Fmax) : NULL;
+    double* nz = act_noise ? act_noise + (int64_t)i * H : NULL;
     for (int h = 0; h < H; ++h) x[h] = tab[hidden[(int64_t)t * H + h]];
     for (int h = 0; h < H; ++h) o[h] = 0.0;
+    if (nz)
+      for (int h = 0; h < H; ++h) nz[h] = 0.0;
     for (int j = 0; j < top_k; ++j) {
       int e = ids[(int64_t)t * top_k + j];
       if (e == -1) continue;
@@ -545,15 +584,20 @@ int oracle_moe_tokens(int n_tok, const int32_t* tok_list, int T, int H, int E, i
       act_rows(tab, wgu, x, H, F, activation, act);
       down_rows(tab, wd, act, H, F, y);
       for (int h = 0; h < H; ++h) o[h] += w * y[h];
+      if (nz) down_noise(tab, wd, act, H, F, dtype, w * w, u, nz);
     }
     if (S > 0) {
       act_rows(tab, shared_w_gate_up, x, H, S, activation, act);
       down_rows(tab, shared_w_down, act, H, S, y);
       for (int h = 0; h < H; ++h) o[h] += y[h];
+      if (nz) down_noise(tab, shared_w_down, act, H, S, dtype, 1.0, u, nz);
     }
+    if (nz)
+      for (int h = 0; h < H; ++h) nz[h] = sqrt(nz[h]);
     free(x);
     free(act);
     free(y);
+    free(u);
   }
   if (bad & 2) return ORACLE_ERR_ID;
   if (bad) return ORACLE_ERR_ARG;
@@ -727,6 +771,18 @@ static double w4_dot(const w4_mat* m, int64_t row, const double* x) {
   return m->alpha * s;
 }
 
+/* sum_k (W[row, k] u[k])^2 for an NVFP4 matrix, W including alpha. */
+static double w4_dot_sq(const w4_mat* m, int64_t row, const double* u) {
+  const uint8_t* q = m->q + row * (m->K / 2);
+  const uint8_t* sf = m->sf + row * (m->K / 16);
+  double s = 0.0;
+  for (int k = 0; k < m->K; ++k) {
+    const double c = m->alpha * nvfp4_elem(q, sf, k) * u[k];
+    s += c * c;
+  }
+  return s;
+}
+
 static void act_rows_w4(const w4_mat* wgu, const double* x, int F, int activation, double* act) {
   for (int f = 0; f < F; ++f) {
     const double g = w4_dot(wgu, f, x);
@@ -745,12 +801,14 @@ static void act_rows_w4(const w4_mat* wgu, const double* x, int F, int activatio
  *   w1q [E, R1, H/2], w1sf [E, R1, H/16], w1a [E]   (R1 = 2F gated, F for ReLU2)
  *   w2q [E, H, F/2],  w2sf [E, H, F/16],  w2a [E]
  * The activations (hidden) are 16-bit; the weight of each term is the NVFP4 value above.
+ * act_noise (nullable): as in oracle_moe_tokens, for act rounded to `dtype`.
  */
 int oracle_moe_tokens_w4(int n_tok, const int32_t* tok_list, int T, int H, int E, int F,
                          int top_k, int dtype, int activation, const uint16_t* hidden,
                          const int32_t* ids, const double* weights, const uint8_t* w1q,
                          const uint8_t* w1sf, const float* w1a, const uint8_t* w2q,
-                         const uint8_t* w2sf, const float* w2a, double* out) {
+                         const uint8_t* w2sf, const float* w2a, double* out,
+                         double* act_noise) {
   if (n_tok < 0 || H <= 0 || E <= 0 || F <= 0 || top_k <= 0 || (dtype != 0 && dtype != 1) ||
       activation < ORACLE_ACT_SILU || activation > ORACLE_ACT_RELU2 || H % 16 || F % 16)
     return ORACLE_ERR_ARG;
@@ -768,8 +826,12 @@ int oracle_moe_tokens_w4(int n_tok, const int32_t* tok_list, int T, int H, int E
     }
     double* x = (double*)malloc(sizeof(double) * H);
     double* act = (double*)malloc(sizeof(double) * F);
+    double* u = act_noise ? (double*)malloc(sizeof(double) * F) : NULL;
+    double* nz = act_noise ? act_noise + (int64_t)i * H : NULL;
     for (int h = 0; h < H; ++h) x[h] = tab[hidden[(int64_t)t * H + h]];
     for (int h = 0; h < H; ++h) o[h] = 0.0;
+    if (nz)
+      for (int h = 0; h < H; ++h) nz[h] = 0.0;
     for (int j = 0; j < top_k; ++j) {
       int e = ids[(int64_t)t * top_k + j];
       if (e == -1) continue;
@@ -782,9 +844,16 @@ int oracle_moe_tokens_w4(int n_tok, const int32_t* tok_list, int T, int H, int E
       act_rows_w4(&m1, x, F, activation, act);
       const double w = weights[(int64_t)t * top_k + j];
       for (int h = 0; h < H; ++h) o[h] += w * w4_dot(&m2, h, act);
+      if (nz) {
+        for (int f = 0; f < F; ++f) u[f] = half_ulp16(dtype, act[f]);
+        for (int h = 0; h < H; ++h) nz[h] += w * w * w4_dot_sq(&m2, h, u);
+      }
     }
+    if (nz)
+      for (int h = 0; h < H; ++h) nz[h] = sqrt(nz[h]);
     free(x);
     free(act);
+    free(u);
   }
   if (bad & 2) return ORACLE_ERR_ID;
   if (bad) return ORACLE_ERR_ARG;

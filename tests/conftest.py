@@ -28,8 +28,12 @@ def pytest_terminal_summary(terminalreporter):
     recs = [r for r in getattr(helpers, "PARITY_RECORDS", []) if r.get("summary")]
     if not recs:
         return
-    terminalreporter.section("output parity (max|gpu-oracle|/RMS; bound 1e-2 + half ulp)")
+    terminalreporter.section("output parity: max|gpu-oracle|/RMS raw and after half an ulp of "
+                             "the final rounding; worst element in act-rounding sigmas")
     for r in recs:
+        z = r.get("max_z")
         terminalreporter.write_line(
             f"{r['what']}: {r['rows']} rows, raw {r['max_err_over_rms']:.4f}, "
-            f"minus half ulp {r['max_err_minus_half_ulp_over_rms']:.4f}")
+            f"minus half ulp {r['max_err_minus_half_ulp_over_rms']:.4f}"
+            + ("" if z is None else f", worst {z:.2f} sigma, "
+                                    f"{r['over_stated']} elements over 1e-2*RMS + half ulp"))

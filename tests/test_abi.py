@@ -139,3 +139,30 @@ def test_status_strings():
 def test_wait_limit_knob_round_trips():
     old = B.set_wait_limit_ns(12345)
     assert B.set_wait_limit_ns(old) == 12345
+
+
+def test_host_entry_staging_and_argument_checks():
+    """fused_moe_fwd_host: staging size, and argument errors returned before any copy or launch
+    (the pointers here are never dereferenced)."""
+    L = B.lib()
+    p = _prob(T=32, H=256, E=16, F=128)
+    stage = L.moe_host_staging_bytes(ctypes.byref(p))
+    assert stage == 2 * _align256(32 * 256 * 2) + _align256(32 * 16 * 4)
+    need = L.moe_workspace_size(ctypes.byref(p)) + stage
+    h = ctypes.c_void_p(0x10000)
+    d = ctypes.c_void_p(0x1000000)  # 256-byte aligned
+    f = L.fused_moe_fwd_host
+    assert f(ctypes.byref(p), None, h, d, d, None, None, None, h, d, need, None) == \
+        B.MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(p), h, h, d, d, None, None, None, None, d, need, None) == \
+        B.MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(p), h, h, None, d, None, None, None, h, d, need, None) == \
+        B.MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(p), h, h, d, d, None, None, None, h, d, need - 1, None) == \
+        B.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert f(ctypes.byref(p), h, h, d, d, d, None, None, h, d, need, None) == \
+        B.MOE_ERR_UNSUPPORTED  # correction bias with softmax scoring
+    assert L.fused_moe_fwd_w4a16_host(ctypes.byref(p), h, h, d, None, d, d, None, h, d, need,
+                                      None) == B.MOE_ERR_INVALID_ARG  # no alpha
+    bad = _prob(T=32, H=256, E=16, F=128, top_k=0)
+    assert L.moe_host_staging_bytes(ctypes.byref(bad)) == 0

@@ -88,9 +88,9 @@ def test_fused_w4a16_matches_oracle(w, cuda_device):
     out = run_fused(w, d)
     ids, _ = run_route(w, d)
     torch.cuda.synchronize()
-    ref, r_ids, _, _ = oracle_fused(w, d)
+    ref, r_ids, _, _, noise = oracle_fused(w, d)
     assert np.array_equal(ids.cpu().numpy(), r_ids)
-    assert_output_close(out, ref, w.dtype, what=w.name)
+    assert_output_close(out, ref, w.dtype, noise, what=w.name)
     assert B.get_device_status(B._workspace(0, cuda_device)) == B.MOE_OK
 
 
@@ -128,15 +128,12 @@ def check_shards_sum_to_full(w, dev, seed, n_sample=None):
         hu = half_ulp(o, w.dtype) if hu is None else hu + half_ulp(o, w.dtype)
     tokens = (np.arange(w.T) if n_sample is None
               else np.unique(np.linspace(0, w.T - 1, n_sample).astype(np.int32)))
-    ref, _, _, _ = oracle_fused(wf, d, tokens=tokens, routed=routed)
+    ref, _, _, _, noise = oracle_fused(wf, d, tokens=tokens, routed=routed)
     got, hu = total[tokens], hu[tokens]
-    rms = float(np.sqrt(np.mean(ref * ref)))
-    err = np.abs(got - ref)
-    log_parity(w.name + " shard sum", max_err_over_rms=float(err.max()) / rms,
-               max_err_minus_half_ulps_over_rms=float(np.max(err - hu)) / rms, tol=RMS_TOL)
-    worst = int(np.argmax(err - hu))
-    assert np.all(err <= RMS_TOL * rms + hu), (
-        f"{w.name}: shard sum off by {err.flat[worst]:.3e} at ref={ref.flat[worst]:.4e}")
+    # each shard's output was rounded once: the half ulps of the shards replace the one of a
+    # single output (with the binade-crossing margin of the shards' own values)
+    assert_output_close(got, ref, w.dtype, noise, what=w.name + " shard sum",
+                        extra_ulps=hu * (1 + 2.0 ** -7))
     del d
     torch.cuda.empty_cache()
 
@@ -223,7 +220,7 @@ def test_w4a16_split_k_matches_oracle_and_unsplit_run(w, cuda_device):
     assert n_big > n_small
     ws_small = B.new_workspace(n_small, cuda_device)
     ws_big = B.new_workspace(n_big, cuda_device)
-    ref, _, _, _ = oracle_fused(w, d)
+    ref, _, _, _, noise = oracle_fused(w, d)
     outs = {}
     for name, ws in (("unsplit", ws_small), ("split", ws_big)):
         a = run_fused(w, d, workspace=ws).clone()
@@ -231,7 +228,7 @@ def test_w4a16_split_k_matches_oracle_and_unsplit_run(w, cuda_device):
         torch.cuda.synchronize()
         assert B.get_device_status(ws) == B.MOE_OK
         assert torch.equal(a, b), f"{w.name} {name}: repeat call not bit-identical"
-        assert_output_close(a, ref, w.dtype, what=f"{w.name} {name}")
+        assert_output_close(a, ref, w.dtype, noise, what=f"{w.name} {name}")
         outs[name] = a
     cnt = ws_big[n_small:n_small + 4 * 64].view(torch.int32).cpu().numpy()
     assert set(np.unique(cnt)) <= {0, 2} and cnt.max() == 2, f"split counters {cnt[:16]}"
@@ -281,8 +278,8 @@ def test_w4a16_full_size_workloads(name, n_sample, cuda_device):
     assert np.array_equal(ids.cpu().numpy(), routed[0]), "routing ids differ"
     tokens = (np.arange(w.T) if n_sample is None
               else np.unique(np.linspace(0, w.T - 1, n_sample).astype(np.int32)))
-    ref, _, _, _ = oracle_fused(w, d, tokens=tokens, routed=routed)
-    assert_output_close(out[torch.from_numpy(tokens).to(cuda_device).long()], ref, w.dtype,
+    ref, _, _, _, noise = oracle_fused(w, d, tokens=tokens, routed=routed)
+    assert_output_close(out[torch.from_numpy(tokens).to(cuda_device).long()], ref, w.dtype, noise,
                         what=name)
     out2 = run_fused(w, d)
     assert torch.equal(out, out2), "repeat call not bit-identical"

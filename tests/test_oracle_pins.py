@@ -327,6 +327,70 @@ def test_single_expert_top1_is_dense_swiglu(dtype):
         np.testing.assert_allclose(out[t], _dense_swiglu(x[t], wgu, wd), rtol=1e-10, atol=1e-12)
 
 
+def _half_ulp_np(a, dtype):
+    """Half the bf16/f16 spacing at |a| from numpy's own float32/float16 spacing (bf16 keeps
+    the top 16 bits of a float32: its spacing is 2^16 float32 spacings)."""
+    a = np.abs(np.asarray(a, np.float64))
+    if dtype == torch.bfloat16:
+        sp = np.spacing(a.astype(np.float32)).astype(np.float64) * 2.0 ** 16
+        sp = np.maximum(sp, 2.0 ** -133)  # bf16 subnormal spacing
+    else:
+        sp = np.spacing(a.astype(np.float16)).astype(np.float64)
+    return np.where(a > 0, sp / 2, 0.0)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_act_noise_is_the_rounding_error_scale_of_a_dense_expert(dtype):
+    """E = 1, top_k = 1, plus a shared expert: the noise output equals
+    sqrt(sum_f (Wd[h,f] u(act_f))^2 + the shared expert's term) with u half the dtype's spacing
+    at the exact act value, computed here with numpy's spacing."""
+    w = inputs.Workload("t", T=5, H=64, E=1, F=40, top_k=1, dtype=dtype, S=24)
+    d = inputs.generate(w, seed=3, device="cpu")
+    ids, wts, _ = oracle.route(d["gating_output"].numpy(), 1)
+    dt = oracle.BF16 if dtype == torch.bfloat16 else oracle.F16
+    out, noise = oracle.moe_tokens(d["hidden_states"], ids, wts, d["w_gate_up"], d["w_down"], dt,
+                                   shared_w_gate_up=d["shared_w_gate_up"],
+                                   shared_w_down=d["shared_w_down"], act_noise=True)
+    x = d["hidden_states"].double().numpy()
+    out_plain = oracle.moe_tokens(d["hidden_states"], ids, wts, d["w_gate_up"], d["w_down"], dt,
+                                  shared_w_gate_up=d["shared_w_gate_up"],
+                                  shared_w_down=d["shared_w_down"])
+    assert np.array_equal(out, out_plain)  # the noise pass leaves the output alone
+    for t in range(w.T):
+        var = np.zeros(w.H)
+        for wgu, wd in ((d["w_gate_up"][0], d["w_down"][0]),
+                        (d["shared_w_gate_up"], d["shared_w_down"])):
+            wgu, wd = wgu.double().numpy(), wd.double().numpy()
+            n = wgu.shape[0] // 2
+            g, u = wgu[:n] @ x[t], wgu[n:] @ x[t]
+            act = g / (1.0 + np.exp(-g)) * u
+            var += (wd ** 2) @ (_half_ulp_np(act, dtype) ** 2)
+        np.testing.assert_allclose(noise[t], np.sqrt(var), rtol=1e-12)
+
+
+def test_act_noise_predicts_the_error_of_rounding_act():
+    """The bf16 pipeline's act rounding, done here with torch: over 24 tokens x 8 routes of
+    H = 512 outputs, (y_rounded - y) / noise has the spread of a sum of uniform rounding errors
+    (standard deviation about 1/sqrt(3) of the noise scale) and stays within 7/sqrt(3) of it."""
+    w = inputs.Workload("t", T=24, H=512, E=16, F=256, top_k=8)
+    d = inputs.generate(w, seed=4, device="cpu")
+    ids, wts, _ = oracle.route(d["gating_output"].numpy(), w.top_k)
+    ref, noise = oracle.moe_tokens(d["hidden_states"], ids, wts, d["w_gate_up"], d["w_down"],
+                                   oracle.BF16, act_noise=True)
+    x = d["hidden_states"].double().numpy()
+    rounded = np.zeros_like(ref)
+    for t in range(w.T):
+        for j in range(w.top_k):
+            e = ids[t, j]
+            wgu, wd = d["w_gate_up"][e].double().numpy(), d["w_down"][e].double().numpy()
+            g, u = wgu[:w.F] @ x[t], wgu[w.F:] @ x[t]
+            act = torch.from_numpy(g / (1.0 + np.exp(-g)) * u).to(torch.bfloat16).double().numpy()
+            rounded[t] += wts[t, j] * (wd @ act)
+    z = (rounded - ref) / noise
+    assert 0.8 / math.sqrt(3) < float(np.std(z)) < 1.1 / math.sqrt(3), float(np.std(z))
+    assert float(np.max(np.abs(z))) < 7 / math.sqrt(3)
+
+
 def _routed_case(seed=2, T=9, E=6, k=3, H=32, F=16, S=0, rsf=1.0):
     w = inputs.Workload("t", T=T, H=H, E=E, F=F, top_k=k, S=S, routed_scaling_factor=rsf)
     d = inputs.generate(w, seed=seed, device="cpu")
