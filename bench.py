@@ -139,9 +139,9 @@ def algorithmic_bytes(w, n_unique: int, P=None) -> dict:
     return dict(
         total=weights + acts,
         gemm1=n_unique * g * w.F * w.H * wb + b1 + P * w.F * eb,
-        gemm2=n_unique * w.H * w.F * wb + P * w.F * eb + P * w.H * eb,
+        gemm2=n_unique * w.H * w.F * wb + P * w.F * eb + P * w.H * 4,  # f32 route rows
         shared_gemm1=g * w.S * w.H * eb + w.T * w.H * eb + w.T * w.S * eb,
-        shared_gemm2=w.S * w.H * eb + w.T * w.S * eb + w.T * w.H * eb,
+        shared_gemm2=w.S * w.H * eb + w.T * w.S * eb + w.T * w.H * 4,  # f32 shared output
     )
 
 

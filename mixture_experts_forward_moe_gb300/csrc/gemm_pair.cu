@@ -391,22 +391,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
 
 // ---- host side -----------------------------------------------------------------------------
 
-// 2-D map over a row-major [rows, inner] 16-bit tensor, box {64, box_rows}, 128-byte swizzle.
-bool make_map16(CUtensorMap* m, int dtype, const void* base, uint64_t inner, uint64_t rows,
-                uint32_t box_rows) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kBlockK, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(m,
-             dtype == MOE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-             2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Clusters of two that can be resident at once for moe_gemm_pair_kernel<T> on the current
 // device (0 when none can); also sets the kernel's shared-memory limit.
 template <typename T>

@@ -418,4 +418,20 @@ inline bool make_map_bytes(CUtensorMap* m, const void* base, uint64_t inner, uin
          CUDA_SUCCESS;
 }
 
+// Map over a row-major [rows, inner] 16-bit tensor (dtype: moe_dtype_t), box {64, box_rows},
+// 128-byte swizzle, zero fill outside the tensor.
+inline bool make_map16(CUtensorMap* m, int dtype, const void* base, uint64_t inner, uint64_t rows,
+                       uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace gb300moe
