@@ -708,9 +708,13 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
           const uint32_t sa = smem_base + (uint32_t)(stage * C::kStageBytes);
           const uint32_t sb = sa + C::kABytes;
           if constexpr (kW4) {
-            // A (decoded weights) from two TMEM ring slots of 64 k each; B: the token slot.
-            const uint32_t tb = smem_base + (uint32_t)(C::kNW * C::kWBytes + stage * C::kBBytes);
-            for (int hh = 0; hh < 2 && ok; ++hh) {
+            // A (decoded weights) from two TMEM ring slots of 64 k each; B: the token slot.  The
+            // descriptor of a 64-k half of the token slot is the slot's plus (half offset) / 16.
+            const uint64_t tdesc = sw128_kmajor_desc(
+                smem_base + (uint32_t)(C::kNW * C::kWBytes + stage * C::kBBytes));
+            const bool two = kGemm1 && U.two;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
               const int idx = a_cnt + hh;
               const int slot = idx % C::kAStages;
               if (!mbar_wait(&afull_bar[slot], (uint32_t)((idx / C::kAStages) & 1), abort_flag,
@@ -720,13 +724,12 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
               }
               tc_fence_after();
               const uint32_t a = tmem_base + (uint32_t)(C::kABase + slot * C::kASlotCols);
-#pragma unroll
-              for (int k = 0; k < kBlockK / 16; ++k) {
-                const uint64_t bdesc = sw128_kmajor_desc(tb + hh * (kN * kBlockK * 2) + k * 32);
-                const uint32_t accum = ((kb - U.kb0) | hh | k) != 0 ? 1u : 0u;
-                umma_f16_tmem_a(d, a + k * 8, bdesc, idesc, accum);
-                if (kGemm1 && U.two) umma_f16_tmem_a(d + kN, a + 32 + k * 8, bdesc, idesc, accum);
-              }
+              const uint64_t bdesc = tdesc + (uint64_t)(hh * (kN * kBlockK * 2 / 16));
+              const uint32_t accum = (kb != U.kb0 || hh != 0) ? 1u : 0u;
+              if (two)
+                umma_tmem_a_kblock2(d, a, d + kN, a + 32, bdesc, idesc, accum);
+              else
+                umma_tmem_a_kblock(d, a, bdesc, idesc, accum);
               umma_commit(&aempty_bar[slot]);
               issued_any = true;
             }

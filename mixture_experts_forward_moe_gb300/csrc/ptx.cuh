@@ -220,15 +220,47 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t ta, float (&a)[16]) {
   for (int i = 0; i < 16; ++i) a[i] = __uint_as_float(r[i]);
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T: the A operand (M = 128 rows, one per TMEM lane, 16-bit
-// elements packed two per 32-bit column in K order) is read from tensor memory.
-__device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                uint32_t idesc, uint32_t accumulate) {
+// One 64-k block of D[tmem] (+)= A[tmem] * B[smem]^T as four k = 16 MMAs issued back to back
+// from one statement.  A (M = 128 rows, one per TMEM lane, 16-bit elements packed two per
+// 32-bit column in K order) from columns a, a+8, a+16, a+24; B descriptors b, b+2, b+4, b+6
+// (32 bytes further along a 128-byte-swizzled K-major row per step).  The first MMA
+// accumulates when `acc` is nonzero, the other three always.  The issuing thread is latency
+// bound (about 44 cycles per tcgen05.mma at small N); any scalar work between two MMAs adds to
+// that, so every operand is formed before the first one.
+__device__ __forceinline__ void umma_tmem_a_kblock(uint32_t d, uint32_t a, uint64_t b,
+                                                   uint32_t idesc, uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p, q;\n\t.reg .b32 a1, a2, a3;\n\t.reg .b64 b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+      "add.u64 b1, %2, 2;\n\tadd.u64 b2, %2, 4;\n\tadd.u64 b3, %2, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, q;\n\t}\n" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// The same for two accumulators that share B (gate into d0 from A columns a0.., up into d1
+// from a1..), interleaved: eight MMAs.
+__device__ __forceinline__ void umma_tmem_a_kblock2(uint32_t d0, uint32_t a0, uint32_t d1,
+                                                    uint32_t a1, uint64_t b, uint32_t idesc,
+                                                    uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b32 x1, x2, x3, y1, y2, y3;\n\t.reg .b64 b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"
+      "add.u32 x1, %1, 8;\n\tadd.u32 x2, %1, 16;\n\tadd.u32 x3, %1, 24;\n\t"
+      "add.u32 y1, %3, 8;\n\tadd.u32 y2, %3, 16;\n\tadd.u32 y3, %3, 24;\n\t"
+      "add.u64 b1, %4, 2;\n\tadd.u64 b2, %4, 4;\n\tadd.u64 b3, %4, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %4, %5, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%2], [%3], %4, %5, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [x1], b1, %5, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%2], [y1], b1, %5, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [x2], b2, %5, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%2], [y2], b2, %5, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [x3], b3, %5, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%2], [y3], b3, %5, q;\n\t}\n" ::"r"(d0),
+      "r"(a0), "r"(d1), "r"(a1), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
 
