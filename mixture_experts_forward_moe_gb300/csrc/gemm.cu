@@ -70,15 +70,22 @@ namespace {
 // 64-row token tiles (the down projection at decode sizes): a stage carries two 64-k blocks
 // (kKps = 2), so the MMA issuer pays one barrier wait and one commit per 32 KB of weights
 // instead of per 16 KB; at a few tokens per expert those per-stage costs, not HBM, would
-// otherwise set the pace.  The NVFP4 gate/up GEMM over at most 64 token rows uses 64-row tiles
-// for another reason: its gate and up accumulators then take 128 TMEM columns, so two
-// accumulator buffers fit beside the decoded-weight ring and a unit's epilogue overlaps the
-// next unit's MMAs (at 128 rows there is room for one).
-template <bool kGemm1, int kN, bool kW4 = false>
+// otherwise set the pace.
+//
+// Two CTAs per SM (k2Cta): the NVFP4 down projection and the NVFP4 gate/up GEMM over at most
+// 64 tokens (64-row tiles) run two CTAs on each SM, each with half the TMEM (256 columns: one
+// accumulator buffer and the decoded-weight ring), about half the shared memory and four
+// decoder warps.  One MMA-issuing thread is latency bound (about 44 cycles per tcgen05.mma at
+// these N when nothing else runs on its SMSP, and twice that next to busy decoder warps), so a
+// second issuer per SM measured 19-21 % faster on the down projection and 12 % on the gate/up
+// GEMM.  The 128-row gate/up GEMM keeps one CTA: its accumulators alone fill 256 columns.
+template <bool kGemm1, int kN, bool kW4 = false, bool k2Cta = false>
 struct Cfg {
   static_assert(kN == 64 || kN == 128 || kN == 256, "tile rows");
   static_assert(kN != 64 || kGemm1 == kW4, "64-row tiles: 16-bit down proj. or NVFP4 gate/up");
   static_assert(!kW4 || kN == 128 || (kN == 64 && kGemm1), "NVFP4 tiles are 128 (64) rows");
+  static_assert(!k2Cta || (kW4 && kN == (kGemm1 ? 64 : 128)),
+                "two CTAs per SM: the NVFP4 down proj. and 64-row gate/up");
   static constexpr int kSlabs = kGemm1 ? 2 : 1;
   static constexpr int kKps = (kN == 64 && !kW4) ? 2 : 1;  // 64-k blocks per stage (16-bit)
   static constexpr int kStageK = kW4 ? 128 : kBlockK * kKps;  // k per pipeline stage
@@ -93,8 +100,8 @@ struct Cfg {
   static constexpr int kSfBytes = kSlab * 8;  // block scales of one slab (128 k)
   static constexpr int kTileBytes = kQBytes + kSfBytes;  // one tile of the packed layout
   static constexpr int kWBytes = kSlabs * kTileBytes;
-  static constexpr int kNW = kGemm1 ? 6 : 8;
-  static constexpr int kNT = kGemm1 ? 3 : 4;
+  static constexpr int kNW = k2Cta ? (kGemm1 ? 3 : 4) : (kGemm1 ? 6 : 8);
+  static constexpr int kNT = k2Cta ? 2 : (kGemm1 ? 3 : 4);
   static constexpr int kRingBytes = kW4 ? kNW * kWBytes + kNT * kBBytes : kStages * kStageBytes;
   static constexpr int kFullBars = kW4 ? kNT : kStages;  // token (or combined) ring barriers
   // gemm1 transposes 64 token columns at a time through shared memory; gemm2 writes f32 rows
@@ -103,14 +110,23 @@ struct Cfg {
   static constexpr int kStagingBytes = kGemm1 ? kPassCols * kSlab * 2 : 0;
   static constexpr int kAccCols = kGemm1 ? 2 * kN : kN;  // per accumulator buffer
   static constexpr int kAccBufs =
-      kW4 ? ((kGemm1 && kN == 128) ? 1 : 2) : ((kGemm1 && kN == 256) ? 1 : 2);
+      kW4 ? ((k2Cta || (kGemm1 && kN == 128)) ? 1 : 2) : ((kGemm1 && kN == 256) ? 1 : 2);
   static constexpr int kABase = kAccBufs * kAccCols;  // first TMEM ring column
   static constexpr int kASlotCols = kSlabs * 32;      // 64 k of every slab
-  static constexpr int kAStages = kW4 ? (512 - kABase) / kASlotCols : 1;
-  static constexpr int kTmemCols = kW4 ? 512 : kAccBufs * kAccCols;
-  static constexpr int kThreads = kW4 ? 480 : 192;
+  static constexpr int kTmemTotal = k2Cta ? 256 : 512;  // two CTAs per SM share the 512 columns
+  static constexpr int kAStages = kW4 ? (kTmemTotal - kABase) / kASlotCols : 1;
+  static constexpr int kTmemCols = kW4 ? kTmemTotal : kAccBufs * kAccCols;
+  // NVFP4 warps: 0 weight producer, 1 MMA, 2-5 epilogue, then the decoders (eight; four, each
+  // doing both groups' rows, with two CTAs per SM), then the token producer.
+  static constexpr int kDecWarps = k2Cta ? 4 : 8;
+  static constexpr int kTokWarp = 6 + kDecWarps;
+  static constexpr int kThreads = kW4 ? 32 * (kTokWarp + 1) : 192;
+  static constexpr int kMinBlocks = k2Cta ? 2 : 1;
+  // Warps that write each decoded-weight slot: gemm1 slots hold both slabs (two groups).
+  static constexpr int kSlotWriters = (kGemm1 && !k2Cta) ? 8 : 4;
   static constexpr int kSmemBytes = kRingBytes + kStagingBytes + 1024;
-  static_assert(!kW4 || kABase + kAStages * kASlotCols <= 512, "TMEM columns");
+  static_assert(!kW4 || kABase + kAStages * kASlotCols <= kTmemTotal, "TMEM columns");
+  static_assert(!k2Cta || kSmemBytes <= 110 * 1024, "shared memory of two CTAs per SM");
   static_assert(kStageBytes % 1024 == 0 && kABytes % 1024 == 0 && kWBytes % 1024 == 0 &&
                     kBBytes % 1024 == 0,
                 "swizzle-atom alignment");
@@ -142,7 +158,9 @@ struct KParams {
   // 16-bit gate/up GEMM over token rows: the router's ids (GemmCall::route_ids).
   const int32_t* route_ids;
   // NVFP4 gate/up GEMM: split-K in two halves when it shortens the last wave (GemmCall).
-  int split_cap, split_cols;
+  // sm_slots: SMs the launch occupies (its CTAs, or the SM count when two share an SM), the
+  // unit of the split cost model.
+  int split_cap, split_cols, sm_slots;
   float* split_part;
   int* split_cnt;
   void* out;
@@ -298,13 +316,15 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) 
 // launches); otherwise every CTA takes units c, c + gridDim.x, ...  kRouted: the NVFP4 gate/up
 // kernel for token rows, whose roles may take their units from the router's ids (the 16-bit
 // kernels decide at run time; the NVFP4 loops measured 1 % slower with that branch in them).
-template <bool kGemm1, int kN, typename T, bool kW4, bool kBal, bool kRouted = false>
-__global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
+template <bool kGemm1, int kN, typename T, bool kW4, bool kBal, bool kRouted = false,
+          bool k2Cta = false>
+__global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4, k2Cta>::kThreads,
+                                  Cfg<kGemm1, kN, kW4, k2Cta>::kMinBlocks)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmB64,
                     const __grid_constant__ CUtensorMap tmB128, const KParams p) {
-  using C = Cfg<kGemm1, kN, kW4>;
+  using C = Cfg<kGemm1, kN, kW4, k2Cta>;
   // Split-K is built into the NVFP4 gate/up kernel for at most 64 token rows only: the other
   // kernels keep K loops with compile-time bounds.
   constexpr bool kSplit = kW4 && kGemm1 && kN == 64;
@@ -346,10 +366,10 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
     if (kW4) {
       for (int s = 0; s < C::kNW; ++s) {
         mbar_init(&wfull_bar[s], 1);
-        mbar_init(&wempty_bar[s], 8);      // one arrival per decoder warp
+        mbar_init(&wempty_bar[s], C::kDecWarps);  // one arrival per decoder warp
       }
       for (int a = 0; a < C::kAStages; ++a) {
-        mbar_init(&afull_bar[a], kGemm1 ? 8 : 4);  // the warps that write the slot
+        mbar_init(&afull_bar[a], C::kSlotWriters);  // the warps that write the slot
         mbar_init(&aempty_bar[a], 1);
       }
     }
@@ -426,7 +446,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
     // the last wave sooner than whole units would (the MMA issue rate, not HBM, paces these
     // kernels, so an SM left idle is time lost).
     int ks = 1;
-    if (kSplit && p.split_cap > 0 && n <= p.split_cap && split_pays(n, gridDim.x, p.num_kb))
+    if (kSplit && p.split_cap > 0 && n <= p.split_cap && split_pays(n, p.sm_slots, p.num_kb))
       ks = 2;
     s_ks = ks;
     s_n_units = n * ks;
@@ -489,7 +509,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
           mbar_wait_drain(&wfull_bar[i % C::kNW], (uint32_t)((i / C::kNW) & 1));
       }
     }
-  } else if (kW4 && warp == 14) {
+  } else if (kW4 && warp == C::kTokWarp) {
     // ---------------------------------------------- NVFP4 token producer (one lane)
     if (lane == 0) {
       int ts = 0;
@@ -533,15 +553,17 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
           mbar_wait_drain(&full_bar[i % C::kNT], (uint32_t)((i / C::kNT) & 1));
       }
     }
-  } else if (kW4 && warp >= 6) {
-    // ------------------------------------------------------- NVFP4 decoders (8 warps)
-    // Warp w owns TMEM lanes 32*(w%4)..+31, i.e. weight rows of the slab.  gemm1: group 0
-    // (warps 6-9) decodes the gate slab and group 1 the up slab, both into the same 64-k ring
-    // slot (columns 0-31 and 32-63).  gemm2: group g decodes k 64g..64g+63 of the stage into
-    // its own slot.  A thread decodes one weight row: 16-byte chunks of 32 codes, two scales
+  } else if (kW4 && warp >= 6 && warp < 6 + C::kDecWarps) {
+    // ------------------------------------------------------- NVFP4 decoders (8 or 4 warps)
+    // Warp w owns TMEM lanes 32*(w%4)..+31, i.e. weight rows of the slab.  Two groups of work:
+    // gemm1: group g decodes slab g (gate, up) into columns 32g..32g+31 of each 64-k ring slot;
+    // gemm2: group g decodes k 64g..64g+63 of the stage into its own slot.  With eight decoder
+    // warps, warps 6-9 are group 0 and 10-13 group 1; with four (two CTAs per SM) every warp
+    // does both.  A thread decodes one weight row: 16-byte chunks of 32 codes, two scales
     // each.  Stores are pipelined: a slot's tcgen05.st is waited for and the slot handed to the
-    // MMA only after the next half has been decoded, so the store latency hides behind ALU work.
-    const int dg = (warp - 6) >> 2;
+    // MMA only after the next slot's first decode, so the store latency hides behind ALU work.
+    constexpr int kG = C::kDecWarps == 4 ? 2 : 1;  // groups per warp
+    const int g0 = kG == 2 ? 0 : (warp - 6) >> 2;
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
     int ws = 0;
@@ -559,23 +581,26 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
       if (!(routed ? decode_item_routed<kGemm1, kN>(p, emask, u, ks, U)
                    : decode_item<kGemm1, kN>(p, u, ks, U)))
         continue;
-      const bool active = !kGemm1 || dg == 0 || U.two;
-      const int slab = kGemm1 ? dg : 0;
       for (int kb = U.kb0; kb < U.kb1; ++kb) {
         if (!mbar_wait(&wfull_bar[ws], wph, abort_flag, p.limit_ns, p.status)) {
           ok = false;
           break;
         }
-        const uint8_t* tile = smem + ws * C::kWBytes + slab * C::kTileBytes;
-        const uint8_t* qrow = tile + row * 64;
-        const uint2 sfw = *reinterpret_cast<const uint2*>(tile + C::kQBytes + row * 8);
-        uint32_t s2[8];
-        nvfp4_scales(sfw.x, *reinterpret_cast<uint32_t(*)[4]>(&s2[0]));
-        nvfp4_scales(sfw.y, *reinterpret_cast<uint32_t(*)[4]>(&s2[4]));
+        const uint8_t* wslot = smem + ws * C::kWBytes;
+        // the row's block scales in each slab this warp decodes (gemm2: one slab)
+        constexpr int kSc = kGemm1 ? kG : 1;
+        uint32_t s2[kSc][8];
+#pragma unroll
+        for (int i = 0; i < kSc; ++i) {
+          const uint8_t* tile = wslot + (kGemm1 ? g0 + i : 0) * C::kTileBytes;
+          const uint2 sfw = *reinterpret_cast<const uint2*>(tile + C::kQBytes + row * 8);
+          nvfp4_scales(sfw.x, *reinterpret_cast<uint32_t(*)[4]>(&s2[i][0]));
+          nvfp4_scales(sfw.y, *reinterpret_cast<uint32_t(*)[4]>(&s2[i][4]));
+        }
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          // gemm1: both groups write half hh of the stage; gemm2: group dg writes half dg.
-          if (!kGemm1 && hh != dg) continue;
+          // gemm1: every group writes half hh of the stage; gemm2: only group hh does.
+          if (!kGemm1 && kG == 1 && hh != g0) continue;
           const int idx = a_cnt + hh;
           const int slot = idx % C::kAStages;
           if (!mbar_wait(&aempty_bar[slot], (uint32_t)(((idx / C::kAStages) & 1) ^ 1),
@@ -584,30 +609,43 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4>::kThreads, 1)
             break;
           }
           tc_fence_after();
-          if (!active) {
-            hand_over(slot);
-            continue;
-          }
-          uint32_t v[32];
+          bool stored = false;
 #pragma unroll
-          for (int jj = 0; jj < 2; ++jj) {
-            const int j = 2 * hh + jj;  // 32-k chunk of the stage
-            // packed layout: chunk j of row r sits at chunk j ^ ((r >> 1) & 3)
-            const uint4 qw = *reinterpret_cast<const uint4*>(qrow + ((j ^ ((row >> 1) & 3)) << 4));
-            nvfp4_decode8(qw.x, s2[2 * j], *reinterpret_cast<uint32_t(*)[4]>(&v[16 * jj]));
-            nvfp4_decode8(qw.y, s2[2 * j], *reinterpret_cast<uint32_t(*)[4]>(&v[16 * jj + 4]));
-            nvfp4_decode8(qw.z, s2[2 * j + 1], *reinterpret_cast<uint32_t(*)[4]>(&v[16 * jj + 8]));
-            nvfp4_decode8(qw.w, s2[2 * j + 1],
-                          *reinterpret_cast<uint32_t(*)[4]>(&v[16 * jj + 12]));
+          for (int gi = 0; gi < kG; ++gi) {
+            const int g = g0 + gi;
+            if (!kGemm1 && g != hh) continue;
+            if (kGemm1 && g == 1 && !U.two) continue;  // no second slab: nothing to decode
+            const int slab = kGemm1 ? g : 0;
+            const uint32_t* sc = s2[kGemm1 ? gi : 0];
+            const uint8_t* qrow = wslot + slab * C::kTileBytes + row * 64;
+            uint32_t v[32];
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              const int j = 2 * hh + jj;  // 32-k chunk of the stage
+              // packed layout: chunk j of row r sits at chunk j ^ ((r >> 1) & 3)
+              const uint4 qw =
+                  *reinterpret_cast<const uint4*>(qrow + ((j ^ ((row >> 1) & 3)) << 4));
+              nvfp4_decode8(qw.x, sc[2 * j], *reinterpret_cast<uint32_t(*)[4]>(&v[16 * jj]));
+              nvfp4_decode8(qw.y, sc[2 * j], *reinterpret_cast<uint32_t(*)[4]>(&v[16 * jj + 4]));
+              nvfp4_decode8(qw.z, sc[2 * j + 1],
+                            *reinterpret_cast<uint32_t(*)[4]>(&v[16 * jj + 8]));
+              nvfp4_decode8(qw.w, sc[2 * j + 1],
+                            *reinterpret_cast<uint32_t(*)[4]>(&v[16 * jj + 12]));
+            }
+            if (pending >= 0) {  // the previous store has had a whole decode to land
+              tmem_wait_st();
+              hand_over(pending);
+              pending = -1;
+            }
+            const uint32_t col =
+                (uint32_t)(C::kABase + slot * C::kASlotCols + (kGemm1 ? slab * 32 : 0));
+            tmem_st_x32(tmem_base + lane_addr + col, v);
+            stored = true;
           }
-          if (pending >= 0) {  // the previous store has had a whole decode to land
-            tmem_wait_st();
-            hand_over(pending);
-          }
-          const uint32_t col =
-              (uint32_t)(C::kABase + slot * C::kASlotCols + (kGemm1 ? slab * 32 : 0));
-          tmem_st_x32(tmem_base + lane_addr + col, v);
-          pending = slot;
+          if (stored)
+            pending = slot;
+          else
+            hand_over(slot);
         }
         if (!ok) break;
         __syncwarp();
@@ -1039,10 +1077,11 @@ bool make_map(CUtensorMap* m, int dtype, const void* base, uint64_t inner, uint6
   return r == CUDA_SUCCESS;
 }
 
-template <bool kGemm1, int kN, typename T, bool kW4, bool kBal = false, bool kRouted = false>
+template <bool kGemm1, int kN, typename T, bool kW4, bool kBal = false, bool kRouted = false,
+          bool k2Cta = false>
 cudaError_t launch_typed(const GemmCall& c, const KParams& kp, int grid, cudaStream_t s,
                          bool pdl) {
-  using C = Cfg<kGemm1, kN, kW4>;
+  using C = Cfg<kGemm1, kN, kW4, k2Cta>;
   CUtensorMap tmW, tmB, tmB64, tmB128;
   const uint64_t w_rows = (uint64_t)c.E * (uint64_t)kp.w_rows_per_expert;
   // NVFP4 weights are read with plain bulk copies: tmW is then a copy of the token map, unused.
@@ -1053,7 +1092,7 @@ cudaError_t launch_typed(const GemmCall& c, const KParams& kp, int grid, cudaStr
       !make_map(&tmB128, c.dtype, c.b, (uint64_t)c.K, (uint64_t)c.b_rows, 128))
     return cudaErrorInvalidValue;
   if (kW4) tmW = tmB;
-  auto kern = moe_gemm_kernel<kGemm1, kN, T, kW4, kBal, kRouted>;
+  auto kern = moe_gemm_kernel<kGemm1, kN, T, kW4, kBal, kRouted, k2Cta>;
   static bool attr_set = false;  // one per instantiation: set once per process
   if (!attr_set) {
     cudaError_t e =
@@ -1073,16 +1112,31 @@ bool decode_sized(const GemmCall& c) {
 }
 
 template <bool kGemm1, typename T>
-cudaError_t launch_rows(const GemmCall& c, const KParams& kp, int grid, cudaStream_t s,
+cudaError_t launch_rows(const GemmCall& c, const KParams& kp, long long units, cudaStream_t s,
                         bool pdl) {
+  const int sms = num_sms();
+  const int grid = (int)(units < sms ? units : sms);
   if (c.w4) {
     if constexpr (kGemm1) {
-      if (kp.split_cap > 0)  // split-K over at most 64 token rows, two accumulator buffers
-        return launch_typed<true, 64, __nv_bfloat16, true, false, true>(c, kp, grid, s, pdl);
+      // At most 64 tokens (token rows or the direct path): 64-row tiles, two CTAs per SM,
+      // split-K when the cost model says it pays.
+      if ((kp.token_rows || c.mode == kDirect) && c.T <= 64) {
+        const int grid2 = (int)(units < 2 * sms ? units : 2 * sms);
+        KParams kq = kp;
+        kq.sm_slots = grid2 < sms ? grid2 : sms;
+        return launch_typed<true, 64, __nv_bfloat16, true, false, true, true>(c, kq, grid2, s,
+                                                                             pdl);
+      }
       if (kp.route_ids)  // token rows: units from the router's ids
         return launch_typed<true, 128, __nv_bfloat16, true, false, true>(c, kp, grid, s, pdl);
+      return launch_typed<true, 128, __nv_bfloat16, true>(c, kp, grid, s, pdl);
+    } else {
+      // Two CTAs per SM, each with its own MMA issuer: one issuing thread is latency bound
+      // and, next to the decoders, reaches well under half the tensor pipe's MMA rate.
+      const int grid2 = (int)(units < 2 * sms ? units : 2 * sms);
+      return launch_typed<false, 128, __nv_bfloat16, true, false, false, true>(c, kp, grid2, s,
+                                                                              pdl);
     }
-    return launch_typed<kGemm1, 128, __nv_bfloat16, true>(c, kp, grid, s, pdl);
   }
   if constexpr (!kGemm1) {  // 64-row tiles are decode tiles: balanced
     if (c.tile_rows == 64) return launch_typed<false, 64, T, false, true>(c, kp, grid, s, pdl);
@@ -1139,6 +1193,7 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   kp.route_ids = (c.gemm1 && kp.token_rows && c.E <= 1024) ? c.route_ids : nullptr;
   kp.split_cap = 0;
   kp.split_cols = 0;
+  kp.sm_slots = 0;
   kp.split_part = nullptr;
   kp.split_cnt = nullptr;
   if (c.w4 && c.gemm1 && kp.token_rows && c.T <= 64 && c.split_cap > 0 && c.split_part &&
@@ -1170,7 +1225,7 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   if (upper <= 0 || c.b_rows <= 0) return cudaSuccess;
   const int sms = num_sms();
   if (kp.split_cap > 0) upper *= 2;  // room for the split halves
-  const int grid = (int)(upper < sms ? upper : sms);
+  const int grid = (int)(upper < sms ? upper : sms);  // the prefetch budget's CTA count
   if (c.early_tiles && c.mode == kSorted && !c.w4) {
     // Up to ~48 MB (well under the L2) of first-unit weights over the whole grid.
     const int64_t step_bytes = (int64_t)kSlab * kBlockK * 2 * (c.gemm1 && kp.gated ? 2 : 1);
@@ -1179,11 +1234,11 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   }
 
   if (c.gemm1) {
-    return c.dtype == MOE_BF16 ? launch_rows<true, __nv_bfloat16>(c, kp, grid, s, pdl)
-                               : launch_rows<true, __half>(c, kp, grid, s, pdl);
+    return c.dtype == MOE_BF16 ? launch_rows<true, __nv_bfloat16>(c, kp, upper, s, pdl)
+                               : launch_rows<true, __half>(c, kp, upper, s, pdl);
   }
-  return c.dtype == MOE_BF16 ? launch_rows<false, __nv_bfloat16>(c, kp, grid, s, pdl)
-                             : launch_rows<false, __half>(c, kp, grid, s, pdl);
+  return c.dtype == MOE_BF16 ? launch_rows<false, __nv_bfloat16>(c, kp, upper, s, pdl)
+                             : launch_rows<false, __half>(c, kp, upper, s, pdl);
 }
 
 }  // namespace gb300moe
