@@ -119,13 +119,27 @@ bool use_direct(const moe_problem_t& p) {
 // and so pay the MMA issuer's per-stage costs once per 32 KB of weights; 128 in between.  The
 // gate/up GEMM always uses 128-row tiles: at 256 rows its two accumulators fill TMEM and the
 // epilogue could no longer overlap the next unit's K loop, which measured slower on the
-// prefill shapes.
-int sorted_tile_rows(const moe_problem_t& p) {
+// prefill shapes.  The averages are over all E experts of the problem, not the shard's: an
+// expert-parallel shard's experts receive their share of the T * top_k routes, and the routes
+// to other shards are padding.
+int64_t rows_per_expert(const moe_problem_t& p) {
   const int64_t P = (int64_t)p.T * p.top_k;
   const int64_t active = P < p.E ? P : p.E;
-  if (active <= 0) return kTileRows;
-  if (P / active >= 96) return kTileRowsWide;
-  return P / active <= 32 ? kTileRowsNarrow : kTileRows;
+  return active > 0 ? P / active : 0;
+}
+
+int sorted_tile_rows(const moe_problem_t& p) {
+  const int64_t r = rows_per_expert(p);
+  if (r <= 0) return kTileRows;
+  if (r >= 96) return kTileRowsWide;
+  return r <= 32 ? kTileRowsNarrow : kTileRows;
+}
+
+// Token rows per tile of the NVFP4 gate/up GEMM over gathered rows: 64 (two CTAs per SM, each
+// with its own MMA issuer) while the experts average at most 64 routed rows; 128 above, where
+// the 64-row tiles' doubled MMA count costs more than the second issuer gains.
+int w4_gate_up_tile_rows(const moe_problem_t& p) {
+  return rows_per_expert(p) <= 64 ? kTileRowsNarrow : kTileRows;
 }
 
 // The down projection of fused_moe_fwd runs on pairs of SMs (gemm_pair.cu) when its tiles have
@@ -418,13 +432,14 @@ moe_status_t run_fused(const moe_problem_t* p, const Experts& X, const void* hid
     int32_t* offsets = at<int32_t>(ws, L.offsets);
     int32_t* sorted = at<int32_t>(ws, L.sorted);
     int32_t* inv_route = at<int32_t>(ws, L.inv);
-    Tile* tiles = at<Tile>(ws, L.tiles);    // gemm1: 128-row tiles
+    Tile* tiles = at<Tile>(ws, L.tiles);    // gemm1: tile_rows1-row tiles
     Tile* tiles2 = at<Tile>(ws, L.tiles2);  // gemm2: tile_rows2-row tiles
-    const int tile_rows2 = X.w4 ? kTileRows : sorted_tile_rows(P);
+    const int tile_rows2 = X.w4 ? kTileRows : sorted_tile_rows(*p);
     // With T <= 128 every expert's rows fit one tile of all T tokens: gemm1 reads hidden_states
     // directly and no gathered copy is made.
     const bool token_rows = P.T <= kTileRows;
-    const bool pair2 = !X.w4 && use_pair_gemm2(P);
+    const int tile_rows1 = (X.w4 && !token_rows) ? w4_gate_up_tile_rows(*p) : kTileRows;
+    const bool pair2 = !X.w4 && use_pair_gemm2(*p);
     SplitLayout S{0, 0, 0, 0, 0};
     if (X.w4 && token_rows) {
       S = split_layout(P);
@@ -434,14 +449,14 @@ moe_status_t run_fused(const moe_problem_t* p, const Experts& X, const void* hid
     if (fused_sort_fits(P)) {  // sort and both tile lists in one launch (and split counters)
       StageTimer t(kSort, s);
       MOE_TRY(launch_sort_fused(P, 1, ids, counts, offsets, sorted, L.cap, nullptr, inv_route,
-                                tiles, tile_counter(ws), kTileRows, tiles2, tile_counter2(ws),
+                                tiles, tile_counter(ws), tile_rows1, tiles2, tile_counter2(ws),
                                 tile_rows2, status, s, true, split_cnt, (int)S.units));
       t.done(1);
     } else {
       StageTimer t(kSort, s);
       MOE_TRY(launch_align_sort_chunked(P, 1, ids, counts, offsets, sorted, L.cap, nullptr,
                                         inv_route, at<int32_t>(ws, L.chunk), status, s, true,
-                                        tiles, tile_counter(ws), kTileRows, tiles2,
+                                        tiles, tile_counter(ws), tile_rows1, tiles2,
                                         tile_counter2(ws), tile_rows2));
       t.done(3);
     }
@@ -465,7 +480,7 @@ moe_status_t run_fused(const moe_problem_t* p, const Experts& X, const void* hid
     g1.tiles = tiles;
     g1.n_tiles = tile_counter(ws);
     g1.max_tiles = (int)L.max_tiles;
-    g1.tile_rows = kTileRows;
+    g1.tile_rows = tile_rows1;
     g1.early_tiles = token_rows ? 0 : 1;  // sort, then permute, then gemm1
     g1.route_ids = token_rows ? ids : nullptr;  // route, sort, then gemm1
     if (split_cnt) {
@@ -679,7 +694,7 @@ moe_status_t gemm1_staged(const moe_problem_t* p, int32_t block_m, const void* h
   cudaStream_t s = (cudaStream_t)stream;
   void* ws = workspace;
   Tile* tiles = at<Tile>(ws, L.tiles);
-  const int tile_rows = kTileRows;
+  const int tile_rows = X.w4 ? w4_gate_up_tile_rows(*p) : kTileRows;
   MOE_TRY(launch_build_tiles(P.E, offsets, tiles, tile_counter(ws), tile_rows, s, false));
   MOE_TRY(launch_permute(P.dtype, P.top_k, P.H, hidden_states, sorted_ids, offsets, P.E, L.cap,
                          at<void>(ws, L.a_sorted), s, true));
@@ -716,7 +731,7 @@ moe_status_t gemm2_staged(const moe_problem_t* p, int32_t block_m, const void* a
   cudaStream_t s = (cudaStream_t)stream;
   void* ws = workspace;
   Tile* tiles = at<Tile>(ws, L.tiles);
-  const int tile_rows = X.w4 ? kTileRows : sorted_tile_rows(P);
+  const int tile_rows = X.w4 ? kTileRows : sorted_tile_rows(*p);
   MOE_TRY(launch_build_tiles(P.E, offsets, tiles, tile_counter(ws), tile_rows, s, false));
   GemmCall g2 = base_call(P, status_word(ws));
   g2.gemm1 = 0;

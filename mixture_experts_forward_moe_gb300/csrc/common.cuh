@@ -20,7 +20,7 @@ constexpr int kMaxSMs = 256;
 // with the 128-byte swizzle.
 constexpr int kTileRows = 128;
 constexpr int kTileRowsWide = 256;
-constexpr int kTileRowsNarrow = 64;  // down-projection tiles at decode sizes
+constexpr int kTileRowsNarrow = 64;  // 16-bit down projection at decode sizes; NVFP4 gate/up
 constexpr int kSlab = 128;
 constexpr int kBlockK = 64;
 

@@ -1118,9 +1118,10 @@ cudaError_t launch_rows(const GemmCall& c, const KParams& kp, long long units, c
   const int grid = (int)(units < sms ? units : sms);
   if (c.w4) {
     if constexpr (kGemm1) {
-      // At most 64 tokens (token rows or the direct path): 64-row tiles, two CTAs per SM,
-      // split-K when the cost model says it pays.
-      if ((kp.token_rows || c.mode == kDirect) && c.T <= 64) {
+      // At most 64 tokens (token rows or the direct path), or 64-row tiles of gathered rows:
+      // two CTAs per SM, split-K (token rows only) when the cost model says it pays.
+      if (((kp.token_rows || c.mode == kDirect) && c.T <= 64) ||
+          (c.mode == kSorted && !kp.token_rows && c.tile_rows == kTileRowsNarrow)) {
         const int grid2 = (int)(units < 2 * sms ? units : 2 * sms);
         KParams kq = kp;
         kq.sm_slots = grid2 < sms ? grid2 : sms;
@@ -1168,10 +1169,14 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   kp.w4 = nullptr;
   kp.alpha = nullptr;
   if (c.w4) {
-    // NVFP4 weights: bf16 activations, 128-row token tiles, K and the output width whole
-    // multiples of 128 (one stage is 128 k; a weight slab never crosses an expert).
-    if (c.dtype != MOE_BF16 || c.tile_rows != kTileRows || c.K % 128 != 0 || c.n_out % 128 != 0 ||
-        !c.alpha || (reinterpret_cast<uintptr_t>(c.w) & 15) != 0)
+    // NVFP4 weights: bf16 activations, 128-row token tiles (64 for the gate/up GEMM over
+    // gathered rows), K and the output width whole multiples of 128 (one stage is 128 k; a
+    // weight slab never crosses an expert).
+    const bool tiles_ok = c.tile_rows == kTileRows ||
+                          (c.tile_rows == kTileRowsNarrow && c.gemm1 && c.mode == kSorted &&
+                           !c.token_rows);
+    if (c.dtype != MOE_BF16 || !tiles_ok || c.K % 128 != 0 || c.n_out % 128 != 0 || !c.alpha ||
+        (reinterpret_cast<uintptr_t>(c.w) & 15) != 0)
       return cudaErrorInvalidValue;
     kp.num_kb = c.K / 128;
     kp.w4 = static_cast<const uint8_t*>(c.w);
@@ -1213,7 +1218,7 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   }
 
   if (c.tile_rows != 128 && c.tile_rows != 256 &&
-      !(c.tile_rows == 64 && !c.gemm1 && !c.w4 && c.mode == kSorted))
+      !(c.tile_rows == 64 && c.mode == kSorted && (c.w4 ? c.gemm1 : !c.gemm1)))
     return cudaErrorInvalidValue;
   long long upper = 0;
   if (c.mode == kSorted)
