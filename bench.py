@@ -328,7 +328,8 @@ class OracleSample:
         w, o = self.w, self.oracle
         if self.w4:
             ref, noise = o.moe_tokens_w4(self.hid, self.ids, self.wts, self.w1, self.w2, o.BF16,
-                                         tokens=self.toks, activation=self.act, act_noise=True)
+                                         tokens=self.toks, activation=self.act, act_noise=True,
+                                         act_dtype=o.F16)  # the NVFP4 path's act is f16
         else:
             ref, noise = o.moe_tokens(self.hid, self.ids, self.wts, self.wgu, self.wdn, self.dt,
                                       tokens=self.toks, expert_slot=self.slot,
@@ -345,12 +346,19 @@ class OracleSample:
         hux = np.where(au > 0, np.exp2(np.floor(np.log2(np.where(au > 0, au, 1.0))) - bits), 0.0)
         sigma = noise / math.sqrt(3.0)
         z = (err - hux - 1e-3 * rms) / np.where(sigma > 0, sigma, np.inf)
+        res = float(np.max(err - hu)) / rms
+        if self.w4:
+            note = (f"act in f16 (the NVFP4 path); the stated 1e-2 RMS + half an ulp is "
+                    f"{'met' if res <= 1e-2 else 'not met'}")
+        else:
+            note = (f"act in {'bf16' if bits == 8 else 'f16'}; the stated 1e-2 RMS + half an ulp "
+                    f"is {'met' if res <= 1e-2 else 'not met'} on this sample (a bf16 act "
+                    f"intermediate cannot meet it on whole outputs)")
         return {"tokens": int(self.n), "max_err_over_rms": float(err.max()) / rms,
-                "max_err_minus_half_ulp_over_rms": float(np.max(err - hu)) / rms,
+                "max_err_minus_half_ulp_over_rms": res,
                 "max_err_in_act_rounding_sigmas": float(z.max()),
                 "bound": "|gpu - oracle| <= half ulp of the output + 7 sigma of the act rounding "
-                         "to the 16-bit dtype + 1e-3 RMS (the stated 1e-2 RMS is not reachable "
-                         "by a bf16 act intermediate on whole outputs)"}
+                         "+ 1e-3 RMS; " + note}
 
 
 # ------------------------------------------------------------------------------------ main arm
@@ -510,7 +518,9 @@ def run_ours(args, w, ws_n, rank, local):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws_n,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f16",
+        # the NVFP4 path's GEMMs take f16 tokens and decoded f16 weights (bf16 in and out)
+        "vs_baseline": None,
+        "dtype": "f16" if w.weights == "nvfp4" or w.dtype != torch.bfloat16 else "bf16",
         "data": "synthetic: seeded N(0,1) hidden states and router logits, N(0,1/fan_in) "
                 "weights" + (", N(0, 0.1^2) correction bias" if w.bias_std else ""),
         "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "F": w.F,

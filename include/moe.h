@@ -22,8 +22,8 @@
  *    captured into a CUDA graph and replayed with the same buffers.
  *  - Errors: argument errors return synchronously, before any launch, and enqueue nothing.
  *    A failed launch returns MOE_ERR_CUDA.  Errors found on the device (an expert id outside
- *    [-1, E), a bounded wait that gave up) are written to a status word inside the workspace
- *    and read with moe_get_device_status.
+ *    [-1, E), a bounded wait that gave up, an NVFP4-path value past the f16 range) are written
+ *    to a status word inside the workspace and read with moe_get_device_status.
  *  - Expert id -1 in a caller-supplied topk_ids marks a padding route: it is skipped and
  *    contributes nothing (ROCm/aiter PR #5973 "[FlyDSL] Optimize MI308 MoE decoding (3/3)",
  *    "Changes": routes with expert ID -1 are skipped).
@@ -48,7 +48,9 @@ typedef enum {
   MOE_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < the size the call needs */
   MOE_ERR_CUDA = 4,                /* a CUDA launch or API call failed */
   MOE_ERR_TIMEOUT = 5,             /* device: a bounded wait inside a kernel gave up */
-  MOE_ERR_BAD_EXPERT_ID = 6        /* device: an expert id outside [-1, E) was seen */
+  MOE_ERR_BAD_EXPERT_ID = 6,       /* device: an expert id outside [-1, E) was seen */
+  MOE_ERR_F16_RANGE = 7            /* device: an NVFP4-path token or act value at or past
+                                      65520 in magnitude (the f16 range it computes in) */
 } moe_status_t;
 
 typedef enum { MOE_BF16 = 0, MOE_F16 = 1 } moe_dtype_t;
@@ -177,7 +179,7 @@ moe_status_t fused_moe_fwd_host(const moe_problem_t* p, const void* hidden_state
 
 /*
  * fused_moe_fwd_w4a16 -- fused_moe_fwd with NVFP4 routed experts and bf16 activations
- * (flashinfer PR #4048, quant_mode "w4a16": NVFP4 weights decoded for a BF16 MMA, the FP32
+ * (flashinfer PR #4048, quant_mode "w4a16": NVFP4 weights decoded for a 16-bit MMA, the FP32
  * per-expert scale applied to the FP32 accumulator, as its weight-scale placement ablation
  * keeps).  Each routed weight is
  *   W[e,n,k] = e2m1(code[e,n,k]) * e4m3(sf[e,n,k/16]) * alpha[e]
@@ -191,6 +193,11 @@ moe_status_t fused_moe_fwd_host(const moe_problem_t* p, const void* hidden_state
  *   w_down_alpha    [E_l] f32
  * (E_l = p->ep_num_local, or E).  Other arguments as fused_moe_fwd.  Requires p->dtype
  * MOE_BF16, H and F multiples of 128 and p->S == 0 (MOE_ERR_UNSUPPORTED otherwise).
+ * The GEMMs compute in f16: e2m1 * e4m3 is an exact f16, the bf16 hidden states are converted
+ * to f16 (exact from 2^-14 to 65504 in magnitude; smaller ones round to the f16 grid, an error
+ * of at most 2^-25) and the act intermediate is kept in f16 (three more bits than bf16).  A
+ * hidden or act value of 65520 or more in magnitude would overflow: the call then sets
+ * MOE_ERR_F16_RANGE in the device status word and its output is not valid.
  */
 moe_status_t fused_moe_fwd_w4a16(const moe_problem_t* p, const void* hidden_states,
                                  const float* gating_output, const uint8_t* w_gate_up_tiles,
@@ -294,7 +301,9 @@ moe_status_t moe_gemm1_swiglu(const moe_problem_t* p, int32_t block_m, const voi
                               size_t workspace_bytes, void* stream);
 
 /* moe_gemm1_w4a16 -- moe_gemm1_swiglu with NVFP4 gate/up weights (packed tiles and scale as
- * in fused_moe_fwd_w4a16).  Requires MOE_BF16, H and F multiples of 128. */
+ * in fused_moe_fwd_w4a16): hidden_states bf16 as there, act written as f16 [cap, F] (the type
+ * these GEMMs compute in; MOE_ERR_F16_RANGE as in fused_moe_fwd_w4a16).  Requires MOE_BF16, H
+ * and F multiples of 128. */
 moe_status_t moe_gemm1_w4a16(const moe_problem_t* p, int32_t block_m, const void* hidden_states,
                              const int32_t* sorted_ids, const int32_t* offsets,
                              const uint8_t* w_gate_up_tiles, const float* w_gate_up_alpha,
@@ -314,7 +323,8 @@ moe_status_t moe_gemm2(const moe_problem_t* p, int32_t block_m, const void* act,
                        void* y_route, void* workspace, size_t workspace_bytes, void* stream);
 
 /* moe_gemm2_w4a16 -- moe_gemm2 with NVFP4 down weights (packed tiles and scale as in
- * fused_moe_fwd_w4a16).  Requires MOE_BF16, H and F multiples of 128. */
+ * fused_moe_fwd_w4a16), act read as f16 [cap, F] (what moe_gemm1_w4a16 writes).  Requires
+ * MOE_BF16 (the problem's type), H and F multiples of 128. */
 moe_status_t moe_gemm2_w4a16(const moe_problem_t* p, int32_t block_m, const void* act,
                              const int32_t* sorted_ids, const int32_t* offsets,
                              const float* topk_weights, const uint8_t* w_down_tiles,

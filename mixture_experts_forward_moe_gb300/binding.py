@@ -16,6 +16,7 @@ from . import build as _build
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED = 0, 1, 2
 MOE_ERR_WORKSPACE_TOO_SMALL, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_BAD_EXPERT_ID = 3, 4, 5, 6
+MOE_ERR_F16_RANGE = 7
 MOE_BF16, MOE_F16 = 0, 1
 MOE_SOFTMAX, MOE_SIGMOID = 0, 1
 
@@ -627,7 +628,7 @@ def fused_moe_fwd_w4a16(hidden_states, gating_output, w_gate_up, w_down, top_k, 
 def moe_gemm1_w4a16(hidden_states, sorted_ids, offsets, w_gate_up, top_k, block_m=1,
                     workspace=None, stream=None, activation="silu"):
     """Grouped gate/up GEMM with NVFP4 weights + activation (include/moe.h: moe_gemm1_w4a16);
-    returns act [cap, F] bf16."""
+    returns act [cap, F] f16 (the type the NVFP4 GEMMs compute in)."""
     T, H = hidden_states.shape
     E_l, rows = w_gate_up.n_mats, w_gate_up.rows
     F = rows if activation == "relu2" else rows // 2
@@ -637,7 +638,7 @@ def moe_gemm1_w4a16(hidden_states, sorted_ids, offsets, w_gate_up, top_k, block_
     _need(offsets, "offsets", torch.int32, (E_l + 1,))
     prob = make_problem(T, H, E_l, F, top_k, torch.bfloat16, activation=activation)
     cap = sorted_capacity(prob, block_m)
-    act = torch.empty((max(cap, 1), F), dtype=torch.bfloat16, device=hidden_states.device)
+    act = torch.empty((max(cap, 1), F), dtype=torch.float16, device=hidden_states.device)
     nbytes = stage_workspace_size(prob, block_m)
     if workspace is None:
         workspace = _workspace(nbytes, hidden_states.device)
@@ -651,10 +652,10 @@ def moe_gemm1_w4a16(hidden_states, sorted_ids, offsets, w_gate_up, top_k, block_
 def moe_gemm2_w4a16(act, sorted_ids, offsets, topk_weights, w_down, T, top_k, block_m=1,
                     workspace=None, stream=None):
     """Grouped down GEMM with NVFP4 weights x route weight (include/moe.h: moe_gemm2_w4a16);
-    returns f32 y_route [cap, H]."""
+    act is f16, as moe_gemm1_w4a16 returns it; returns f32 y_route [cap, H]."""
     E_l, H, F = w_down.n_mats, w_down.rows, w_down.K
     _need_w4(w_down, "w_down", E_l, H, F)
-    _need(act, "act", torch.bfloat16)
+    _need(act, "act", torch.float16)
     _need(sorted_ids, "sorted_ids", torch.int32)
     _need(offsets, "offsets", torch.int32, (E_l + 1,))
     _need(topk_weights, "topk_weights", torch.float32)

@@ -385,11 +385,16 @@ moe_status_t run_fused(const moe_problem_t* p, const Experts& X, const void* hid
   int* status = status_word(ws);
   int32_t* ids = at<int32_t>(ws, L.ids);
   float* w = at<float>(ws, L.w);
+  // The NVFP4 GEMMs take f16 token rows.  Up to 128 tokens the router's launch writes them (in
+  // the gathered-rows buffer, unused then); beyond, the permute converts while it gathers.
+  void* rows16 = (X.w4 && p->T <= kTileRows) ? at<void>(ws, L.a_sorted) : nullptr;
   {
     StageTimer t(kRoute, s);
-    MOE_TRY(launch_route(*p, gating_output, correction_bias, ids, w, s, false));
+    MOE_TRY(launch_route(*p, gating_output, correction_bias, ids, w, s, false, hidden_states,
+                         rows16, status));
     t.done(1);
   }
+  const void* tokens = rows16 ? rows16 : hidden_states;  // the gate/up GEMM's token rows
   // Past the router every id is a local expert index (or -1): the stages see E_local experts.
   const moe_problem_t P = local_view(*p);
 
@@ -402,7 +407,7 @@ moe_status_t run_fused(const moe_problem_t* p, const Experts& X, const void* hid
     g1.K = P.H;
     g1.n_out = P.F;
     set_weights(g1, X, true);
-    g1.b = hidden_states;
+    g1.b = tokens;
     g1.b_rows = P.T;
     g1.out = at<void>(ws, L.act);
     g1.topk_ids = ids;
@@ -463,7 +468,7 @@ moe_status_t run_fused(const moe_problem_t* p, const Experts& X, const void* hid
     if (!token_rows) {
       StageTimer t(kPermute, s);
       MOE_TRY(launch_permute(P.dtype, P.top_k, P.H, hidden_states, sorted, offsets, P.E, L.cap,
-                             at<void>(ws, L.a_sorted), s, true));
+                             at<void>(ws, L.a_sorted), s, true, X.w4 != 0, status));
       t.done(1);
     }
     GemmCall g1 = base_call(P, status);
@@ -472,7 +477,7 @@ moe_status_t run_fused(const moe_problem_t* p, const Experts& X, const void* hid
     g1.K = P.H;
     g1.n_out = P.F;
     set_weights(g1, X, true);
-    g1.b = token_rows ? hidden_states : at<void>(ws, L.a_sorted);
+    g1.b = token_rows ? tokens : at<void>(ws, L.a_sorted);
     g1.b_rows = token_rows ? P.T : L.cap;
     g1.token_rows = token_rows ? 1 : 0;
     g1.sorted_ids = sorted;
@@ -697,7 +702,7 @@ moe_status_t gemm1_staged(const moe_problem_t* p, int32_t block_m, const void* h
   const int tile_rows = X.w4 ? w4_gate_up_tile_rows(*p) : kTileRows;
   MOE_TRY(launch_build_tiles(P.E, offsets, tiles, tile_counter(ws), tile_rows, s, false));
   MOE_TRY(launch_permute(P.dtype, P.top_k, P.H, hidden_states, sorted_ids, offsets, P.E, L.cap,
-                         at<void>(ws, L.a_sorted), s, true));
+                         at<void>(ws, L.a_sorted), s, true, X.w4 != 0, status_word(ws)));
   GemmCall g1 = base_call(P, status_word(ws));
   g1.gemm1 = 1;
   g1.mode = kSorted;
@@ -981,6 +986,7 @@ const char* moe_status_string(moe_status_t s) {
     case MOE_ERR_CUDA: return "CUDA launch or API error";
     case MOE_ERR_TIMEOUT: return "a bounded wait inside a kernel timed out";
     case MOE_ERR_BAD_EXPERT_ID: return "expert id outside [-1, E)";
+    case MOE_ERR_F16_RANGE: return "an NVFP4-path value past the f16 range";
   }
   return "unknown status";
 }

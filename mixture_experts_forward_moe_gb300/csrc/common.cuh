@@ -97,8 +97,13 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
 
 // ---- launchers (defined in the .cu files, called by api.cu) ------------------------------
 // `pdl`: true when the launch follows another kernel of the same entry point.
+// With `rows_f16`, extra CTAs of the same launch also write hidden_states ([T, H] bf16) to
+// rows_f16 as f16 (the NVFP4 path's token rows), setting MOE_ERR_F16_RANGE in `status` for a
+// value past the f16 range.
 cudaError_t launch_route(const moe_problem_t& p, const float* gating, const float* bias,
-                         int32_t* ids, float* w, cudaStream_t s, bool pdl);
+                         int32_t* ids, float* w, cudaStream_t s, bool pdl,
+                         const void* hidden = nullptr, void* rows_f16 = nullptr,
+                         int* status = nullptr);
 
 // The sort: one launch when it fits, else the chunked form.
 cudaError_t launch_align_sort(const moe_problem_t& p, int block_m, const int32_t* ids,
@@ -129,9 +134,12 @@ cudaError_t launch_align_sort_chunked(const moe_problem_t& p, int block_m, const
 cudaError_t launch_build_tiles(int E, const int32_t* offsets, Tile* tiles, int* n_tiles,
                                int tile_rows, cudaStream_t s, bool pdl);
 
+// to_f16: bf16 rows in, f16 rows out (the NVFP4 path), MOE_ERR_F16_RANGE in `status` for a
+// value past the f16 range.
 cudaError_t launch_permute(int dtype, int top_k, int H, const void* hidden,
                            const int32_t* sorted_ids, const int32_t* offsets, int E, int64_t cap,
-                           void* a_sorted, cudaStream_t s, bool pdl);
+                           void* a_sorted, cudaStream_t s, bool pdl, bool to_f16 = false,
+                           int* status = nullptr);
 
 // Tile list over a grouped-GEMM layout (masked or prefix sums) and the weighted post-permute.
 cudaError_t launch_build_tiles_meta(int E, int max_m, int64_t rows, const int32_t* meta,
@@ -154,6 +162,23 @@ cudaError_t launch_gemm_fp8(int E, int N, int K, int64_t rows, int max_tile_rows
 // Activation code of the single-projection GEMM that writes the product itself (the plain
 // grouped GEMM); not a moe_activation_t a caller can pass.
 constexpr int kActIdentity = 3;
+// Magnitude from which a value rounds to an infinite f16 (the NVFP4 path's token rows and act
+// are f16).
+constexpr float kF16Overflow = 65520.0f;
+
+// Eight bf16 values (one 16-byte vector) to f16: exact from 2^-14 to 65504 in magnitude,
+// rounded to the nearest f16 below 2^-14 (an error of at most 2^-25); returns true when one
+// of them is at or past kF16Overflow (it becomes infinite).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v, bool& over) {
+  const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+  over |= fabsf(f.x) >= kF16Overflow || fabsf(f.y) >= kF16Overflow;
+  const __half2 h = __floats2half2_rn(f.x, f.y);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 v, bool& over) {
+  return make_uint4(bf16x2_to_f16x2(v.x, over), bf16x2_to_f16x2(v.y, over),
+                    bf16x2_to_f16x2(v.z, over), bf16x2_to_f16x2(v.w, over));
+}
 
 // NVFP4 weights -> the packed tile layout the W4A16 GEMMs read (nvfp4_pack.cu).
 cudaError_t launch_nvfp4_pack(int64_t n_mats, int rows, int K, const uint8_t* codes,

@@ -950,6 +950,12 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4, k2Cta>::kThreads,
                   }
                 }
               }
+              if constexpr (kW4) {  // the f16 act: a value past the f16 range is an error
+                bool over = false;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) over |= fabsf(h[j]) >= kF16Overflow;
+                if (over) set_status(p.status, MOE_ERR_F16_RANGE);
+              }
 #pragma unroll
               for (int j = 0; j < 16; ++j) stg[(c - c0 + j) * kSlab + row] = DT<T>::from_f(h[j]);
             }
@@ -1084,12 +1090,15 @@ cudaError_t launch_typed(const GemmCall& c, const KParams& kp, int grid, cudaStr
   using C = Cfg<kGemm1, kN, kW4, k2Cta>;
   CUtensorMap tmW, tmB, tmB64, tmB128;
   const uint64_t w_rows = (uint64_t)c.E * (uint64_t)kp.w_rows_per_expert;
-  // NVFP4 weights are read with plain bulk copies: tmW is then a copy of the token map, unused.
-  if (!kW4 && !make_map(&tmW, c.dtype, c.w, (uint64_t)c.K, w_rows, kSlab))
+  // The token rows are of the kernel's 16-bit type (f16 for the NVFP4 kernels, whatever the
+  // problem's type); so are 16-bit weights.  NVFP4 weights are read with plain bulk copies: tmW
+  // is then a copy of the token map, unused.
+  const int tdt = DT<T>::kIsBF16 ? MOE_BF16 : MOE_F16;
+  if (!kW4 && !make_map(&tmW, tdt, c.w, (uint64_t)c.K, w_rows, kSlab))
     return cudaErrorInvalidValue;
-  if (!make_map(&tmB, c.dtype, c.b, (uint64_t)c.K, (uint64_t)c.b_rows, 16) ||
-      !make_map(&tmB64, c.dtype, c.b, (uint64_t)c.K, (uint64_t)c.b_rows, 64) ||
-      !make_map(&tmB128, c.dtype, c.b, (uint64_t)c.K, (uint64_t)c.b_rows, 128))
+  if (!make_map(&tmB, tdt, c.b, (uint64_t)c.K, (uint64_t)c.b_rows, 16) ||
+      !make_map(&tmB64, tdt, c.b, (uint64_t)c.K, (uint64_t)c.b_rows, 64) ||
+      !make_map(&tmB128, tdt, c.b, (uint64_t)c.K, (uint64_t)c.b_rows, 128))
     return cudaErrorInvalidValue;
   if (kW4) tmW = tmB;
   auto kern = moe_gemm_kernel<kGemm1, kN, T, kW4, kBal, kRouted, k2Cta>;
@@ -1125,18 +1134,16 @@ cudaError_t launch_rows(const GemmCall& c, const KParams& kp, long long units, c
         const int grid2 = (int)(units < 2 * sms ? units : 2 * sms);
         KParams kq = kp;
         kq.sm_slots = grid2 < sms ? grid2 : sms;
-        return launch_typed<true, 64, __nv_bfloat16, true, false, true, true>(c, kq, grid2, s,
-                                                                             pdl);
+        return launch_typed<true, 64, __half, true, false, true, true>(c, kq, grid2, s, pdl);
       }
       if (kp.route_ids)  // token rows: units from the router's ids
-        return launch_typed<true, 128, __nv_bfloat16, true, false, true>(c, kp, grid, s, pdl);
-      return launch_typed<true, 128, __nv_bfloat16, true>(c, kp, grid, s, pdl);
+        return launch_typed<true, 128, __half, true, false, true>(c, kp, grid, s, pdl);
+      return launch_typed<true, 128, __half, true>(c, kp, grid, s, pdl);
     } else {
       // Two CTAs per SM, each with its own MMA issuer: one issuing thread is latency bound
       // and, next to the decoders, reaches well under half the tensor pipe's MMA rate.
       const int grid2 = (int)(units < 2 * sms ? units : 2 * sms);
-      return launch_typed<false, 128, __nv_bfloat16, true, false, false, true>(c, kp, grid2, s,
-                                                                              pdl);
+      return launch_typed<false, 128, __half, true, false, false, true>(c, kp, grid2, s, pdl);
     }
   }
   if constexpr (!kGemm1) {  // 64-row tiles are decode tiles: balanced
@@ -1169,9 +1176,9 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   kp.w4 = nullptr;
   kp.alpha = nullptr;
   if (c.w4) {
-    // NVFP4 weights: bf16 activations, 128-row token tiles (64 for the gate/up GEMM over
-    // gathered rows), K and the output width whole multiples of 128 (one stage is 128 k; a
-    // weight slab never crosses an expert).
+    // NVFP4 weights: a bf16 problem (its token rows and act reach the GEMMs as f16), 128-row
+    // token tiles (64 for the gate/up GEMM over gathered rows), K and the output width whole
+    // multiples of 128 (one stage is 128 k; a weight slab never crosses an expert).
     const bool tiles_ok = c.tile_rows == kTileRows ||
                           (c.tile_rows == kTileRowsNarrow && c.gemm1 && c.mode == kSorted &&
                            !c.token_rows);

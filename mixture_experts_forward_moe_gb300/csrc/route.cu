@@ -51,10 +51,22 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     route_kernel(int T, int E, int K, int scoring, int renorm, int G, int keepG, float rsf,
                  int loc0, int nloc, const float* __restrict__ gating,
                  const float* __restrict__ bias, int32_t* __restrict__ ids,
-                 float* __restrict__ wout) {
+                 float* __restrict__ wout, int conv_ctas, int64_t conv_vec,
+                 const uint4* __restrict__ conv_src, uint4* __restrict__ conv_dst,
+                 int* __restrict__ status) {
   __shared__ float s_gscore[kWarpsPerBlock][32];
   pdl_wait();
   pdl_trigger();
+  const int route_ctas = (int)gridDim.x - conv_ctas;
+  if ((int)blockIdx.x >= route_ctas) {
+    // The NVFP4 path's token rows: hidden_states to f16, 16 bytes at a time.
+    bool over = false;
+    for (int64_t v = (int64_t)(blockIdx.x - route_ctas) * blockDim.x + threadIdx.x; v < conv_vec;
+         v += (int64_t)conv_ctas * blockDim.x)
+      conv_dst[v] = bf16x8_to_f16x8(__ldg(conv_src + v), over);
+    if (over) set_status(status, MOE_ERR_F16_RANGE);
+    return;
+  }
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
   const int t = blockIdx.x * kWarpsPerBlock + wib;
@@ -295,30 +307,41 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 
 template <int VPL>
 cudaError_t launch_vpl(const moe_problem_t& p, const float* gating, const float* bias,
-                       int32_t* ids, float* w, cudaStream_t s, bool pdl) {
+                       int32_t* ids, float* w, cudaStream_t s, bool pdl, const void* hidden,
+                       void* rows_f16, int* status) {
   const int G = p.num_expert_group > 1 ? p.num_expert_group : 1;
   const int keepG = G > 1 ? p.topk_group : 1;
   const int blocks = (p.T + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const int loc0 = p.ep_num_local > 0 ? p.ep_local_offset : 0;
   const int nloc = local_experts(p);
-  return launch_k(route_kernel<VPL>, dim3(blocks), dim3(kWarpsPerBlock * 32), 0, s, pdl, p.T,
-                  p.E, p.top_k, p.scoring, p.renormalize, G, keepG, p.routed_scaling_factor,
-                  loc0, nloc, gating, bias, ids, w);
+  // Conversion CTAs: about two 16-byte vectors per thread, at most one wave of the SMs.
+  const int64_t conv_vec = rows_f16 ? (int64_t)p.T * p.H / 8 : 0;
+  const int64_t per_cta = 2ll * kWarpsPerBlock * 32;
+  int64_t conv = (conv_vec + per_cta - 1) / per_cta;
+  if (conv > num_sms()) conv = num_sms();
+  return launch_k(route_kernel<VPL>, dim3(blocks + (int)conv), dim3(kWarpsPerBlock * 32), 0, s,
+                  pdl, p.T, p.E, p.top_k, p.scoring, p.renormalize, G, keepG,
+                  p.routed_scaling_factor, loc0, nloc, gating, bias, ids, w, (int)conv, conv_vec,
+                  static_cast<const uint4*>(hidden), static_cast<uint4*>(rows_f16), status);
 }
 
 }  // namespace
 
 cudaError_t launch_route(const moe_problem_t& p, const float* gating, const float* bias,
-                         int32_t* ids, float* w, cudaStream_t s, bool pdl) {
+                         int32_t* ids, float* w, cudaStream_t s, bool pdl, const void* hidden,
+                         void* rows_f16, int* status) {
   if (p.T == 0) return cudaSuccess;
+  if (rows_f16 && (!hidden || p.H % 8 != 0)) return cudaErrorInvalidValue;
   const int need = (p.E + 31) / 32;
-  if (need <= 1) return launch_vpl<1>(p, gating, bias, ids, w, s, pdl);
-  if (need <= 2) return launch_vpl<2>(p, gating, bias, ids, w, s, pdl);
-  if (need <= 4) return launch_vpl<4>(p, gating, bias, ids, w, s, pdl);
-  if (need <= 8) return launch_vpl<8>(p, gating, bias, ids, w, s, pdl);
-  if (need <= 12) return launch_vpl<12>(p, gating, bias, ids, w, s, pdl);
-  if (need <= 16) return launch_vpl<16>(p, gating, bias, ids, w, s, pdl);
-  return launch_vpl<32>(p, gating, bias, ids, w, s, pdl);
+#define ROUTE_VPL(V) launch_vpl<V>(p, gating, bias, ids, w, s, pdl, hidden, rows_f16, status)
+  if (need <= 1) return ROUTE_VPL(1);
+  if (need <= 2) return ROUTE_VPL(2);
+  if (need <= 4) return ROUTE_VPL(4);
+  if (need <= 8) return ROUTE_VPL(8);
+  if (need <= 12) return ROUTE_VPL(12);
+  if (need <= 16) return ROUTE_VPL(16);
+  return ROUTE_VPL(32);
+#undef ROUTE_VPL
 }
 
 }  // namespace gb300moe

@@ -384,15 +384,18 @@ __global__ void __launch_bounds__(1024)
 // a_sorted[p, :] = hidden[sorted_ids[p] / top_k, :] for p < offsets[E]; padding rows are zero.
 // A CTA copies whole rows (grid-stride): each thread loads up to 8 of its 16-byte pieces of the
 // row before it stores any, and the next row's source index is fetched during the copy.
+// kToF16: bf16 rows in, f16 rows out (the NVFP4 path), a value past the f16 range flagged.
 constexpr int kPermuteThreads = 128;
 constexpr int kPermuteAhead = 8;
 
+template <bool kToF16>
 __global__ void __launch_bounds__(kPermuteThreads)
     permute_kernel(int top_k, int H, const uint16_t* __restrict__ hidden,
                    const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ offsets,
-                   int E, uint16_t* __restrict__ a_sorted) {
+                   int E, uint16_t* __restrict__ a_sorted, int* __restrict__ status) {
   pdl_wait();
   pdl_trigger();
+  bool over = false;
   const int64_t rows = offsets[E];
   const int nvec = H / 8;
   const uint4 zero = make_uint4(0, 0, 0, 0);
@@ -414,11 +417,12 @@ __global__ void __launch_bounds__(kPermuteThreads)
 #pragma unroll
       for (int i = 0; i < kPermuteAhead; ++i) {
         const int v = v0 + i * kPermuteThreads + threadIdx.x;
-        if (v < nvec) dst[v] = buf[i];
+        if (v < nvec) dst[v] = kToF16 ? bf16x8_to_f16x8(buf[i], over) : buf[i];
       }
     }
     sid = next_sid;
   }
+  if (kToF16 && over) set_status(status, MOE_ERR_F16_RANGE);
 }
 
 // out[t, :] = round(sum_j y[inv[t*K+j], :] + shared[t, :]): f32 rows in, one rounding out.
@@ -636,13 +640,15 @@ cudaError_t launch_build_tiles(int E, const int32_t* offsets, Tile* tiles, int* 
 
 cudaError_t launch_permute(int dtype, int top_k, int H, const void* hidden,
                            const int32_t* sorted_ids, const int32_t* offsets, int E, int64_t cap,
-                           void* a_sorted, cudaStream_t s, bool pdl) {
-  (void)dtype;  // a row copy: the element type does not matter
+                           void* a_sorted, cudaStream_t s, bool pdl, bool to_f16, int* status) {
   if (cap <= 0) return cudaSuccess;
+  if (to_f16 && dtype != MOE_BF16) return cudaErrorInvalidValue;
+  // without to_f16 a row copy: the element type does not matter
   const int64_t grid = cap < 4096 ? cap : 4096;
-  return launch_k(permute_kernel, dim3((int)grid), dim3(kPermuteThreads), 0, s, pdl, top_k, H,
+  auto kern = to_f16 ? permute_kernel<true> : permute_kernel<false>;
+  return launch_k(kern, dim3((int)grid), dim3(kPermuteThreads), 0, s, pdl, top_k, H,
                   static_cast<const uint16_t*>(hidden), sorted_ids, offsets, E,
-                  static_cast<uint16_t*>(a_sorted));
+                  static_cast<uint16_t*>(a_sorted), status);
 }
 
 cudaError_t launch_combine(const moe_problem_t& p, const void* y_route,

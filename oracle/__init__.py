@@ -87,8 +87,8 @@ def _load():
             _lib.oracle_e4m3_to_double.restype = f64
             _lib.oracle_e4m3_to_double.argtypes = [i32]
             _lib.oracle_nvfp4_dequant.argtypes = [i64, i32, P, P, P, i64, P]
-            _lib.oracle_moe_tokens_w4.argtypes = [i32, P, i32, i32, i32, i32, i32, i32, i32, P,
-                                                  P, P, P, P, P, P, P, P, P, P]
+            _lib.oracle_moe_tokens_w4.argtypes = [i32, P, i32, i32, i32, i32, i32, i32, i32,
+                                                  i32, P, P, P, P, P, P, P, P, P, P, P]
             _lib.oracle_expert_act_w4.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P]
             _lib.oracle_expert_down_w4.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P]
     return _lib
@@ -306,10 +306,11 @@ def nvfp4_dequant(q, sf, alpha, rows_per_alpha=None):
 
 
 def moe_tokens_w4(hidden, ids, weights, w1, w2, dtype, tokens=None, activation=ACT_SILU,
-                  act_noise=False):
+                  act_noise=False, act_dtype=None):
     """fp64 fused MoE output with NVFP4 experts.  w1 = (q [E,R1,H/2], sf [E,R1,H/16], alpha [E])
     for the gate/up projection (R1 = 2F, or F for ReLU2), w2 = (q [E,H,F/2], sf [E,H,F/16],
-    alpha [E]) for the down projection.  ``act_noise``: as in moe_tokens."""
+    alpha [E]) for the down projection.  ``act_noise``: as in moe_tokens, for act rounded to
+    ``act_dtype`` (default: ``dtype``)."""
     hb = _bits(hidden)
     T, H = hb.shape
     idv = _c(ids, np.int32)
@@ -324,7 +325,8 @@ def moe_tokens_w4(hidden, ids, weights, w1, w2, dtype, tokens=None, activation=A
     tl = np.arange(T, dtype=np.int32) if tokens is None else _c(tokens, np.int32)
     out = np.empty((tl.size, H), np.float64)
     noise = np.empty((tl.size, H), np.float64) if act_noise else None
-    rc = _load().oracle_moe_tokens_w4(tl.size, _ptr(tl), T, H, E, F, k, dtype, activation,
+    adt = dtype if act_dtype is None else act_dtype
+    rc = _load().oracle_moe_tokens_w4(tl.size, _ptr(tl), T, H, E, F, k, dtype, adt, activation,
                                       _ptr(hb), _ptr(idv), _ptr(wv), _ptr(q1), _ptr(s1), _ptr(a1),
                                       _ptr(q2), _ptr(s2), _ptr(a2), _ptr(out), _ptr(noise))
     _check(rc, "oracle_moe_tokens_w4")

@@ -800,17 +800,20 @@ static void act_rows_w4(const w4_mat* wgu, const double* x, int F, int activatio
  * oracle_moe_tokens_w4: oracle_moe_tokens with NVFP4 routed experts (no shared expert):
  *   w1q [E, R1, H/2], w1sf [E, R1, H/16], w1a [E]   (R1 = 2F gated, F for ReLU2)
  *   w2q [E, H, F/2],  w2sf [E, H, F/16],  w2a [E]
- * The activations (hidden) are 16-bit; the weight of each term is the NVFP4 value above.
- * act_noise (nullable): as in oracle_moe_tokens, for act rounded to `dtype`.
+ * The activations (hidden) are 16-bit of `dtype`; the weight of each term is the NVFP4 value
+ * above.  act_noise (nullable): as in oracle_moe_tokens, for act rounded to the 16-bit type
+ * act_dtype (0 bf16, 1 f16).
  */
 int oracle_moe_tokens_w4(int n_tok, const int32_t* tok_list, int T, int H, int E, int F,
-                         int top_k, int dtype, int activation, const uint16_t* hidden,
+                         int top_k, int dtype, int act_dtype, int activation,
+                         const uint16_t* hidden,
                          const int32_t* ids, const double* weights, const uint8_t* w1q,
                          const uint8_t* w1sf, const float* w1a, const uint8_t* w2q,
                          const uint8_t* w2sf, const float* w2a, double* out,
                          double* act_noise) {
   if (n_tok < 0 || H <= 0 || E <= 0 || F <= 0 || top_k <= 0 || (dtype != 0 && dtype != 1) ||
-      activation < ORACLE_ACT_SILU || activation > ORACLE_ACT_RELU2 || H % 16 || F % 16)
+      (act_dtype != 0 && act_dtype != 1) || activation < ORACLE_ACT_SILU ||
+      activation > ORACLE_ACT_RELU2 || H % 16 || F % 16)
     return ORACLE_ERR_ARG;
   const double* tab = decode_table(dtype);
   fp_tables();
@@ -845,7 +848,7 @@ int oracle_moe_tokens_w4(int n_tok, const int32_t* tok_list, int T, int H, int E
       const double w = weights[(int64_t)t * top_k + j];
       for (int h = 0; h < H; ++h) o[h] += w * w4_dot(&m2, h, act);
       if (nz) {
-        for (int f = 0; f < F; ++f) u[f] = half_ulp16(dtype, act[f]);
+        for (int f = 0; f < F; ++f) u[f] = half_ulp16(act_dtype, act[f]);
         for (int h = 0; h < H; ++h) nz[h] += w * w * w4_dot_sq(&m2, h, u);
       }
     }

@@ -189,9 +189,11 @@ def oracle_fused(w, d, tokens=None, routed=None):
     if w.weights == "nvfp4":
         w1 = tuple(t.cpu() for t in d["w_gate_up"])
         w2 = tuple(t.cpu() for t in d["w_down"])
+        # the NVFP4 path keeps its act in f16
         out, noise = oracle.moe_tokens_w4(d["hidden_states"].cpu(), lids, wts, w1, w2,
                                           dt_code(w.dtype), tokens=tl,
-                                          activation=ACT_CODES[w.activation], act_noise=True)
+                                          activation=ACT_CODES[w.activation], act_noise=True,
+                                          act_dtype=oracle.F16)
         return out, ids, wts, near, noise
     ids_g, ids = ids, lids
     used = sorted(set(int(e) for e in ids[tl].reshape(-1) if e >= 0))

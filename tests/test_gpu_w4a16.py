@@ -54,16 +54,17 @@ def test_w4a16_gemms_match_oracle(T, k, E, H, F, activation, cuda_device):
     x_rows = d["hidden_states"].cpu()[torch.from_numpy(sid // k).long()]
     w1 = tuple(t.cpu() for t in d["w_gate_up"])
     ref_act = oracle.expert_act_w4(x_rows, eo, w1, oracle.BF16, activation=ACT_CODES[activation])
-    assert_rounded_close(act[:rows], ref_act, torch.bfloat16, what=f"w4 act {activation} T={T}")
+    assert act.dtype == torch.float16  # the NVFP4 GEMMs compute in f16
+    assert_rounded_close(act[:rows], ref_act, torch.float16, what=f"w4 act {activation} T={T}")
 
-    a_in = inputs.random_rows(act.shape[0], F, seed=5, dtype=torch.bfloat16, std=0.5)
+    a_in = inputs.random_rows(act.shape[0], F, seed=5, dtype=torch.float16, std=0.5)
     a_in = a_in.to(cuda_device)
     tw = inputs.random_weights(T * k, seed=6).to(cuda_device)
     y = B.moe_gemm2_w4a16(a_in, sorted_ids, offsets, tw, w2_packed, T, k)
     torch.cuda.synchronize()
     scale = tw.cpu().numpy().astype(np.float64)[sid]
     w2 = tuple(t.cpu() for t in d["w_down"])
-    ref_y = oracle.expert_down_w4(a_in[:rows].cpu(), eo, scale, w2, oracle.BF16)
+    ref_y = oracle.expert_down_w4(a_in[:rows].cpu(), eo, scale, w2, oracle.F16)
     assert_rms_close(y[:rows], ref_y, tol=1e-4, what=f"w4 y_route T={T} H={H} F={F}")
     assert B.get_device_status(B._workspace(0, cuda_device)) == B.MOE_OK
 
@@ -249,6 +250,47 @@ def test_w4a16_split_k_matches_oracle_and_unsplit_run(w, cuda_device):
     bound = 2 * half_ulp(np.abs(un) * (1 + 2.0 ** -7), w.dtype) + 2e-3 * rms
     log_parity(f"{w.name} split vs unsplit", max_err_over_rms=float(err.max()) / rms)
     assert np.all(err <= bound), f"{w.name}: split and unsplit differ by {err.max():.3e}"
+
+
+RANGE_CASES = [
+    ("token rows, a hidden value past f16", W("r1", T=16, H=256, E=8, F=128, top_k=2,
+                                              weights="nvfp4"), "hidden"),
+    ("gathered rows, a hidden value past f16", W("r2", T=200, H=256, E=8, F=128, top_k=2,
+                                                 weights="nvfp4"), "hidden"),
+    ("act past f16 from in-range tokens", W("r3", T=16, H=256, E=8, F=128, top_k=2,
+                                            weights="nvfp4"), "act"),
+]
+
+
+@pytest.mark.parametrize("what,w,kind", RANGE_CASES, ids=[c[0] for c in RANGE_CASES])
+def test_w4a16_flags_values_past_the_f16_range(what, w, kind, cuda_device):
+    """The NVFP4 path computes in f16: a bf16 hidden value of 65536 (the first past f16's
+    range), or an act that grows past it, sets MOE_ERR_F16_RANGE in the status word; the same
+    inputs brought into range leave it clear."""
+    d = inputs.generate(w, seed=4, device=cuda_device)
+    x = d["hidden_states"]
+    if kind == "hidden":
+        # hidden column 5 meets only zero gate/up weights (E2M1 code 0: element 5 is the high
+        # nibble of byte 2), so only the token-row conversion can see the value there
+        d["w_gate_up"][0][:, :, 2] &= 0x0F
+        x[3, 5] = 65536.0
+    else:  # every token 2000: gate and up values near 2000, act near 2000 * 2000
+        x.fill_(2000.0)
+    prob = B.make_problem(w.T, w.H, w.E, w.F, w.top_k, w.dtype, w.scoring_func, w.renormalize,
+                          w.num_expert_group, w.topk_group, w.routed_scaling_factor, 0,
+                          w.activation)
+    ws = B.new_workspace(B.workspace_size(prob), cuda_device)
+    run_fused(w, d, workspace=ws)
+    torch.cuda.synchronize()
+    assert B.get_device_status(ws) == B.MOE_ERR_F16_RANGE, what
+    if kind == "hidden":
+        x[3, 5] = 60000.0  # in range: exact in f16
+    else:
+        x.fill_(2.0)
+    ws2 = B.new_workspace(B.workspace_size(prob), cuda_device)
+    run_fused(w, d, workspace=ws2)
+    torch.cuda.synchronize()
+    assert B.get_device_status(ws2) == B.MOE_OK, what
 
 
 def test_w4a16_rejects_unsupported_shapes(cuda_device):
