@@ -163,7 +163,7 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
-GEMM_SOURCES = ("gemm.cu", "gemm_pair.cu", "ptx.cuh", "common.cuh")
+GEMM_SOURCES = ("gemm.cu", "gemm_pair.cu", "ptx.cuh", "common.cuh", "nvfp4.cuh")
 
 
 def kernel_source_hash() -> str:
