@@ -81,11 +81,12 @@ namespace {
 // GEMM.  The 128-row gate/up GEMM keeps one CTA: its accumulators alone fill 256 columns.
 template <bool kGemm1, int kN, bool kW4 = false, bool k2Cta = false>
 struct Cfg {
-  static_assert(kN == 64 || kN == 128 || kN == 256, "tile rows");
+  static_assert(kN == 32 || kN == 64 || kN == 128 || kN == 256, "tile rows");
   static_assert(kN != 64 || kGemm1 == kW4, "64-row tiles: 16-bit down proj. or NVFP4 gate/up");
-  static_assert(!kW4 || kN == 128 || (kN == 64 && kGemm1), "NVFP4 tiles are 128 (64) rows");
-  static_assert(!k2Cta || (kW4 && kN == (kGemm1 ? 64 : 128)),
-                "two CTAs per SM: the NVFP4 down proj. and 64-row gate/up");
+  static_assert(kN != 32 || (kGemm1 && kW4 && k2Cta), "32-row tiles: NVFP4 gate/up, two CTAs");
+  static_assert(!kW4 || kN == 128 || (kN <= 64 && kGemm1), "NVFP4 tiles are 128 (64, 32) rows");
+  static_assert(!k2Cta || (kW4 && (kGemm1 ? kN <= 64 : kN == 128)),
+                "two CTAs per SM: the NVFP4 down proj. and 32/64-row gate/up");
   static constexpr int kSlabs = kGemm1 ? 2 : 1;
   static constexpr int kKps = (kN == 64 && !kW4) ? 2 : 1;  // 64-k blocks per stage (16-bit)
   static constexpr int kStageK = kW4 ? 128 : kBlockK * kKps;  // k per pipeline stage
@@ -101,7 +102,7 @@ struct Cfg {
   static constexpr int kTileBytes = kQBytes + kSfBytes;  // one tile of the packed layout
   static constexpr int kWBytes = kSlabs * kTileBytes;
   static constexpr int kNW = k2Cta ? (kGemm1 ? 3 : 4) : (kGemm1 ? 6 : 8);
-  static constexpr int kNT = k2Cta ? 2 : (kGemm1 ? 3 : 4);
+  static constexpr int kNT = k2Cta ? (kN == 32 ? 4 : 2) : (kGemm1 ? 3 : 4);
   static constexpr int kRingBytes = kW4 ? kNW * kWBytes + kNT * kBBytes : kStages * kStageBytes;
   static constexpr int kFullBars = kW4 ? kNT : kStages;  // token (or combined) ring barriers
   // gemm1 transposes 64 token columns at a time through shared memory; gemm2 writes f32 rows
@@ -327,7 +328,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4, k2Cta>::kThreads,
   using C = Cfg<kGemm1, kN, kW4, k2Cta>;
   // Split-K is built into the NVFP4 gate/up kernel for at most 64 token rows only: the other
   // kernels keep K loops with compile-time bounds.
-  constexpr bool kSplit = kW4 && kGemm1 && kN == 64;
+  constexpr bool kSplit = kW4 && kGemm1 && kN <= 64;
   extern __shared__ uint8_t dsmem[];
   __shared__ __align__(8) uint64_t full_bar[C::kFullBars];   // NVFP4: the token ring
   __shared__ __align__(8) uint64_t empty_bar[C::kFullBars];
@@ -1127,13 +1128,19 @@ cudaError_t launch_rows(const GemmCall& c, const KParams& kp, long long units, c
   const int grid = (int)(units < sms ? units : sms);
   if (c.w4) {
     if constexpr (kGemm1) {
-      // At most 64 tokens (token rows or the direct path), or 64-row tiles of gathered rows:
-      // two CTAs per SM, split-K (token rows only) when the cost model says it pays.
-      if (((kp.token_rows || c.mode == kDirect) && c.T <= 64) ||
+      // At most 64 tokens over token rows, the direct path with at most 64 routes (its epilogue
+      // keeps one entry per route, in arrays of the tile's rows), or 64-row tiles of gathered
+      // rows: two CTAs per SM, split-K (token rows only) when the cost model says it pays.  Up
+      // to 32 tokens (routes) the tiles have 32 rows: their accumulators take 64 TMEM columns,
+      // which leaves three 64-k slots for the decoded weights instead of two.
+      const bool narrow = (kp.token_rows && c.T <= 32) || (c.mode == kDirect && c.P <= 32);
+      if ((kp.token_rows && c.T <= 64) || (c.mode == kDirect && c.P <= 64) ||
           (c.mode == kSorted && !kp.token_rows && c.tile_rows == kTileRowsNarrow)) {
         const int grid2 = (int)(units < 2 * sms ? units : 2 * sms);
         KParams kq = kp;
         kq.sm_slots = grid2 < sms ? grid2 : sms;
+        if (narrow)
+          return launch_typed<true, 32, __half, true, false, true, true>(c, kq, grid2, s, pdl);
         return launch_typed<true, 64, __half, true, false, true, true>(c, kq, grid2, s, pdl);
       }
       if (kp.route_ids)  // token rows: units from the router's ids

@@ -72,6 +72,9 @@ def test_w4a16_gemms_match_oracle(T, k, E, H, F, activation, cuda_device):
 SMALL = [
     W("w4-direct-t4", T=4, H=256, E=16, F=128, top_k=4, weights="nvfp4"),
     W("w4-direct-t8-k8", T=8, H=384, E=64, F=256, top_k=8, weights="nvfp4"),
+    # 128 routes on the direct path: past the 64-row two-CTA kernel (its epilogue keeps one
+    # entry per route), so the 128-row kernel runs it
+    W("w4-direct-t8-k16", T=8, H=256, E=64, F=128, top_k=16, weights="nvfp4"),
     W("w4-sorted-t37-sigmoid", T=37, H=256, E=12, F=256, top_k=3, scoring_func="sigmoid",
       bias_std=0.1, routed_scaling_factor=2.5, weights="nvfp4"),
     W("w4-sorted-t300-gathered", T=300, H=256, E=8, F=128, top_k=2, weights="nvfp4"),
