@@ -135,11 +135,13 @@ int sorted_tile_rows(const moe_problem_t& p) {
   return r <= 32 ? kTileRowsNarrow : kTileRows;
 }
 
-// Token rows per tile of the NVFP4 gate/up GEMM over gathered rows: 64 (two CTAs per SM, each
-// with its own MMA issuer) while the experts average at most 64 routed rows; 128 above, where
-// the 64-row tiles' doubled MMA count costs more than the second issuer gains.
+// Token rows per tile of the NVFP4 gate/up GEMM over gathered rows: 32 while the experts average
+// at most 16 routed rows and 64 while they average at most 64 (two CTAs per SM, each with its
+// own MMA issuer; 32-row accumulators leave three decoded-weight slots in TMEM instead of two);
+// 128 above, where the narrow tiles' extra MMAs cost more than the second issuer gains.
 int w4_gate_up_tile_rows(const moe_problem_t& p) {
-  return rows_per_expert(p) <= 64 ? kTileRowsNarrow : kTileRows;
+  const int64_t r = rows_per_expert(p);
+  return r <= 16 ? kTileRowsNvfp4Min : (r <= 64 ? kTileRowsNarrow : kTileRows);
 }
 
 // The down projection of fused_moe_fwd runs on pairs of SMs (gemm_pair.cu) when its tiles have
@@ -167,7 +169,7 @@ Layout make_layout(const moe_problem_t& p, int block_m) {
   L.P = (int64_t)p.T * p.top_k;
   L.cap = L.P + (int64_t)p.E * (block_m - 1);
   L.n_chunks = (L.P + kSortChunk - 1) / kSortChunk;
-  L.max_tiles = L.cap / kTileRowsNarrow + p.E + 1;  // the most tiles any tile height gives
+  L.max_tiles = L.cap / kTileRowsNvfp4Min + p.E + 1;  // the most tiles any tile height gives
   size_t off = kHeaderBytes;
   auto take = [&](size_t bytes) {
     const size_t o = off;

@@ -21,6 +21,7 @@ constexpr int kMaxSMs = 256;
 constexpr int kTileRows = 128;
 constexpr int kTileRowsWide = 256;
 constexpr int kTileRowsNarrow = 64;  // 16-bit down projection at decode sizes; NVFP4 gate/up
+constexpr int kTileRowsNvfp4Min = 32;  // NVFP4 gate/up tiles at the smallest decode sizes
 constexpr int kSlab = 128;
 constexpr int kBlockK = 64;
 

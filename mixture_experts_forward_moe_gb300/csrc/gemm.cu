@@ -1129,13 +1129,15 @@ cudaError_t launch_rows(const GemmCall& c, const KParams& kp, long long units, c
   if (c.w4) {
     if constexpr (kGemm1) {
       // At most 64 tokens over token rows, the direct path with at most 64 routes (its epilogue
-      // keeps one entry per route, in arrays of the tile's rows), or 64-row tiles of gathered
+      // keeps one entry per route, in arrays of the tile's rows), or 32/64-row tiles of gathered
       // rows: two CTAs per SM, split-K (token rows only) when the cost model says it pays.  Up
-      // to 32 tokens (routes) the tiles have 32 rows: their accumulators take 64 TMEM columns,
-      // which leaves three 64-k slots for the decoded weights instead of two.
-      const bool narrow = (kp.token_rows && c.T <= 32) || (c.mode == kDirect && c.P <= 32);
+      // to 32 tokens (routes, tile rows) the tiles have 32 rows: their accumulators take 64 TMEM
+      // columns, which leaves three 64-k slots for the decoded weights instead of two.
+      const bool gathered = c.mode == kSorted && !kp.token_rows;
+      const bool narrow = (kp.token_rows && c.T <= 32) || (c.mode == kDirect && c.P <= 32) ||
+                          (gathered && c.tile_rows == kTileRowsNvfp4Min);
       if ((kp.token_rows && c.T <= 64) || (c.mode == kDirect && c.P <= 64) ||
-          (c.mode == kSorted && !kp.token_rows && c.tile_rows == kTileRowsNarrow)) {
+          (gathered && c.tile_rows <= kTileRowsNarrow)) {
         const int grid2 = (int)(units < 2 * sms ? units : 2 * sms);
         KParams kq = kp;
         kq.sm_slots = grid2 < sms ? grid2 : sms;
@@ -1186,9 +1188,10 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
     // NVFP4 weights: a bf16 problem (its token rows and act reach the GEMMs as f16), 128-row
     // token tiles (64 for the gate/up GEMM over gathered rows), K and the output width whole
     // multiples of 128 (one stage is 128 k; a weight slab never crosses an expert).
-    const bool tiles_ok = c.tile_rows == kTileRows ||
-                          (c.tile_rows == kTileRowsNarrow && c.gemm1 && c.mode == kSorted &&
-                           !c.token_rows);
+    const bool tiles_ok =
+        c.tile_rows == kTileRows ||
+        ((c.tile_rows == kTileRowsNarrow || c.tile_rows == kTileRowsNvfp4Min) && c.gemm1 &&
+         c.mode == kSorted && !c.token_rows);
     if (c.dtype != MOE_BF16 || !tiles_ok || c.K % 128 != 0 || c.n_out % 128 != 0 || !c.alpha ||
         (reinterpret_cast<uintptr_t>(c.w) & 15) != 0)
       return cudaErrorInvalidValue;
@@ -1232,7 +1235,8 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   }
 
   if (c.tile_rows != 128 && c.tile_rows != 256 &&
-      !(c.tile_rows == 64 && c.mode == kSorted && (c.w4 ? c.gemm1 : !c.gemm1)))
+      !(c.tile_rows == 64 && c.mode == kSorted && (c.w4 ? c.gemm1 : !c.gemm1)) &&
+      !(c.tile_rows == 32 && c.mode == kSorted && c.w4 && c.gemm1))
     return cudaErrorInvalidValue;
   long long upper = 0;
   if (c.mode == kSorted)

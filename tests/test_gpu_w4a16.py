@@ -83,6 +83,10 @@ SMALL = [
       activation="gelu_tanh", weights="nvfp4"),
     W("w4-sorted-t64-relu2", T=64, H=256, E=8, F=384, top_k=2, activation="relu2",
       weights="nvfp4"),
+    # gathered rows, 10 routes per expert on average: 32-row gate/up tiles; the skew gives some
+    # experts several tiles
+    W("w4-sorted-t160-32row-tiles-skewed", T=160, H=256, E=64, F=128, top_k=4, skew_alpha=0.5,
+      weights="nvfp4"),
 ]
 
 
