@@ -186,7 +186,8 @@ Layout make_layout(const moe_problem_t& p, int block_m) {
   L.tiles = take(sizeof(Tile) * L.max_tiles);
   L.tiles2 = take(sizeof(Tile) * L.max_tiles);
   // The gathered rows: the staged gate/up GEMM always gathers; fused_moe_fwd needs them only
-  // for T > 128 (it reads hidden_states directly on the direct path and when T <= 128).
+  // for T > 128 (it reads hidden_states directly on the direct path and when T <= 128, except
+  // that the NVFP4 path then keeps its f16 copy of hidden_states here).
   L.a_sorted = take((size_t)L.cap * p.H * eb);
   L.act = take((size_t)L.cap * p.F * eb);
   L.y = take((size_t)L.cap * p.H * sizeof(float));  // weighted down-projection rows, f32
