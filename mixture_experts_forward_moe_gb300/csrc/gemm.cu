@@ -72,13 +72,15 @@ namespace {
 // instead of per 16 KB; at a few tokens per expert those per-stage costs, not HBM, would
 // otherwise set the pace.
 //
-// Two CTAs per SM (k2Cta): the NVFP4 down projection and the NVFP4 gate/up GEMM over at most
-// 64 tokens (64-row tiles) run two CTAs on each SM, each with half the TMEM (256 columns: one
-// accumulator buffer and the decoded-weight ring), about half the shared memory and four
-// decoder warps.  One MMA-issuing thread is latency bound (about 44 cycles per tcgen05.mma at
-// these N when nothing else runs on its SMSP, and twice that next to busy decoder warps), so a
-// second issuer per SM measured 19-21 % faster on the down projection and 12 % on the gate/up
-// GEMM.  The 128-row gate/up GEMM keeps one CTA: its accumulators alone fill 256 columns.
+// Two CTAs per SM (k2Cta): the NVFP4 down projection and the NVFP4 gate/up GEMM with 64- or
+// 32-row tiles (at most 64 tokens, or gathered rows at decode sizes) run two CTAs on each SM,
+// each with half the TMEM (256 columns: one accumulator buffer and the decoded-weight ring),
+// about half the shared memory and four decoder warps.  One MMA-issuing thread is latency
+// bound (about 44 cycles per tcgen05.mma at these N when nothing else runs on its SMSP, and
+// twice that next to busy decoder warps), so a second issuer per SM measured 19-21 % faster on
+// the down projection and 12 % on the gate/up GEMM.  32-row gate/up accumulators (64 columns)
+// leave three 64-k slots for the decoded weights instead of two (another 9 %).  The 128-row
+// gate/up GEMM keeps one CTA: its accumulators alone fill 256 columns.
 template <bool kGemm1, int kN, bool kW4 = false, bool k2Cta = false>
 struct Cfg {
   static_assert(kN == 32 || kN == 64 || kN == 128 || kN == 256, "tile rows");
@@ -1186,8 +1188,8 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   kp.alpha = nullptr;
   if (c.w4) {
     // NVFP4 weights: a bf16 problem (its token rows and act reach the GEMMs as f16), 128-row
-    // token tiles (64 for the gate/up GEMM over gathered rows), K and the output width whole
-    // multiples of 128 (one stage is 128 k; a weight slab never crosses an expert).
+    // token tiles (64 or 32 for the gate/up GEMM over gathered rows), K and the output width
+    // whole multiples of 128 (one stage is 128 k; a weight slab never crosses an expert).
     const bool tiles_ok =
         c.tile_rows == kTileRows ||
         ((c.tile_rows == kTileRowsNarrow || c.tile_rows == kTileRowsNvfp4Min) && c.gemm1 &&
