@@ -40,6 +40,27 @@ def test_wait_timeout_is_reported_and_context_survives(T, cuda_device):
     assert_output_close(out, ref, w.dtype, noise, what=f"after timeout T={T}")
 
 
+# NVFP4: T=4 runs the direct path (32-row gate/up and down projection at two CTAs per SM), T=96
+# the 128-row gate/up over token rows (one CTA per SM), T=200 gathered rows in 64-row tiles.
+@pytest.mark.parametrize("T", [4, 96, 200])
+def test_wait_timeout_in_nvfp4_kernels_is_reported_and_context_survives(T, cuda_device):
+    w = inputs.Workload("timeout-w4", T=T, H=1024, E=16, F=256, top_k=4, weights="nvfp4")
+    d = inputs.generate(w, seed=6, device=cuda_device)
+    ws = _workspace(w, cuda_device)
+    old = B.set_wait_limit_ns(0)
+    try:
+        run_fused(w, d, workspace=ws)
+        status = B.get_device_status(ws)  # synchronises
+    finally:
+        B.set_wait_limit_ns(old)
+    assert status == B.MOE_ERR_TIMEOUT
+    out = run_fused(w, d, workspace=ws)
+    torch.cuda.synchronize()
+    assert B.get_device_status(ws) == B.MOE_OK
+    ref, _, _, _, noise = oracle_fused(w, d)
+    assert_output_close(out, ref, w.dtype, noise, what=f"NVFP4 after timeout T={T}")
+
+
 def test_bad_expert_id_in_staged_gemm_is_reported(cuda_device):
     # moe_align_sort treats the bad id as padding and reports it.
     ids = inputs.random_ids(12, 2, 8, seed=3)
