@@ -161,9 +161,7 @@ struct KParams {
   // 16-bit gate/up GEMM over token rows: the router's ids (GemmCall::route_ids).
   const int32_t* route_ids;
   // NVFP4 gate/up GEMM: split-K in two halves when it shortens the last wave (GemmCall).
-  // sm_slots: SMs the launch occupies (its CTAs, or the SM count when two share an SM), the
-  // unit of the split cost model.
-  int split_cap, split_cols, sm_slots;
+  int split_cap, split_cols;
   float* split_part;
   int* split_cnt;
   void* out;
@@ -286,9 +284,10 @@ __device__ __forceinline__ bool decode_item_routed(const KParams& p, const uint3
 // Split-K cost model of the NVFP4 gate/up GEMM over at most 64 token rows, in K steps per CTA:
 // a whole unit costs its num_kb steps plus kSplitWholeOver, a half its num_kb/2 plus
 // kSplitHalfOver (the extra epilogue and the exchange of partials), fitted to timings of both
-// forms on GB300 (DeepSeek-V3 EP8 shard, T = 32: 56 K steps a unit, 224 units on 152 SMs,
-// 135 us whole, 108 us split; Qwen3-30B-A3B, T = 32: 16 K steps, 660 units, where the model
-// keeps whole units).
+// forms on GB300 at one CTA per SM (DeepSeek-V3 EP8 shard, T = 32: 56 K steps a unit, 224 units
+// on 152 SMs, 135 us whole, 108 us split; Qwen3-30B-A3B, T = 32: 16 K steps, 660 units, where
+// the model keeps whole units).  With two CTAs per SM it counts CTAs: the EP8 shard's 224 units
+// then fit one round of 304 CTAs and stay whole (72 us, against 77 us split).
 constexpr int kSplitWholeOver = 3;
 constexpr int kSplitHalfOver = 4;
 
@@ -449,7 +448,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4, k2Cta>::kThreads,
     // the last wave sooner than whole units would (the MMA issue rate, not HBM, paces these
     // kernels, so an SM left idle is time lost).
     int ks = 1;
-    if (kSplit && p.split_cap > 0 && n <= p.split_cap && split_pays(n, p.sm_slots, p.num_kb))
+    if (kSplit && p.split_cap > 0 && n <= p.split_cap && split_pays(n, gridDim.x, p.num_kb))
       ks = 2;
     s_ks = ks;
     s_n_units = n * ks;
@@ -1141,11 +1140,9 @@ cudaError_t launch_rows(const GemmCall& c, const KParams& kp, long long units, c
       if ((kp.token_rows && c.T <= 64) || (c.mode == kDirect && c.P <= 64) ||
           (gathered && c.tile_rows <= kTileRowsNarrow)) {
         const int grid2 = (int)(units < 2 * sms ? units : 2 * sms);
-        KParams kq = kp;
-        kq.sm_slots = grid2 < sms ? grid2 : sms;
         if (narrow)
-          return launch_typed<true, 32, __half, true, false, true, true>(c, kq, grid2, s, pdl);
-        return launch_typed<true, 64, __half, true, false, true, true>(c, kq, grid2, s, pdl);
+          return launch_typed<true, 32, __half, true, false, true, true>(c, kp, grid2, s, pdl);
+        return launch_typed<true, 64, __half, true, false, true, true>(c, kp, grid2, s, pdl);
       }
       if (kp.route_ids)  // token rows: units from the router's ids
         return launch_typed<true, 128, __half, true, false, true>(c, kp, grid, s, pdl);
@@ -1217,17 +1214,17 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   kp.route_ids = (c.gemm1 && kp.token_rows && c.E <= 1024) ? c.route_ids : nullptr;
   kp.split_cap = 0;
   kp.split_cols = 0;
-  kp.sm_slots = 0;
   kp.split_part = nullptr;
   kp.split_cnt = nullptr;
   if (c.w4 && c.gemm1 && kp.token_rows && c.T <= 64 && c.split_cap > 0 && c.split_part &&
       c.split_cnt) {
     if (c.split_cols < ((c.T + 15) & ~15)) return cudaErrorInvalidValue;
-    // The split-capable kernel (64-row tiles) only when splitting pays for the most units the
-    // call can have (one tile per routed expert); it then decides on the actual count.
+    // Split scratch only when splitting pays for the most units the call can have (one tile
+    // per routed expert); the kernel (two CTAs per SM, the model counts CTAs) then decides on
+    // the actual count.
     const int64_t active = (int64_t)c.P < c.E ? (int64_t)c.P : (int64_t)c.E;
     const int64_t n_max = active * kp.n_slabs;
-    const int64_t ctas = 2 * n_max < num_sms() ? 2 * n_max : num_sms();
+    const int64_t ctas = 2 * n_max < 2 * num_sms() ? 2 * n_max : 2 * num_sms();
     if (n_max <= c.split_cap && split_pays((int)n_max, (int)ctas, kp.num_kb)) {
       kp.split_cap = c.split_cap;
       kp.split_cols = c.split_cols;
