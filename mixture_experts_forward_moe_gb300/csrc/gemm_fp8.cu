@@ -45,18 +45,31 @@ namespace {
 constexpr int kF8BlockK = 128;                  // k per scale block
 constexpr int kF8WBytes = kSlab * kF8BlockK;    // 16 KB of weights per k block
 constexpr int kF8MaxStages = 6;
-// 12 warps in three warpgroups: warpgroup 0 holds the TMA producer (warp 0) and the MMA issuer
-// (warp 1; warps 2-3 idle) and gives up registers (setmaxnreg) to warpgroups 1-2, the epilogue,
-// whose 64 f32 accumulators and 64-column TMEM loads per thread need them:
-// 128 * 56 + 256 * 224 = 64512 = 384 threads * 168 registers at launch.
-constexpr int kF8Threads = 384;
-constexpr int kF8ProducerRegs = 56;
-constexpr int kF8EpilogueRegs = 224;
-static_assert(128 * kF8ProducerRegs + 256 * kF8EpilogueRegs <= kF8Threads * 168,
-              "register split exceeds the launch allocation");
-constexpr int kF8TmemCols = 512;
-// Dynamic shared memory the kernel may use: the per-block maximum less its static part.
-constexpr int kF8SmemLimit = 232448 - 4096;
+// One CTA per SM: 12 warps in three warpgroups.  Warpgroup 0 holds the TMA producer (warp 0)
+// and the MMA issuer (warp 1; warps 2-3 idle) and gives up registers (setmaxnreg) to
+// warpgroups 1-2, the epilogue (token columns 0-63 and 64-127), whose 64 f32 accumulators and
+// 64-column TMEM loads per thread need them: 128 * 56 + 256 * 224 = 64512 = 384 threads * 168
+// registers at launch.
+// Two CTAs per SM (k2Cta; token tiles of at most 64 rows, which leave warpgroup 2 idle): 8
+// warps, warpgroup 1 alone is the epilogue; 256 TMEM columns and half the shared memory each.
+// Each SM then runs two MMA issuers: one issuing thread is latency bound and slows further
+// next to the epilogue warps on its SMSP.  128 * 56 + 128 * 200 = 32768 = 256 threads * 128.
+template <bool k2Cta>
+struct F8Cfg {
+  static constexpr int kThreads = k2Cta ? 256 : 384;
+  static constexpr int kEpiThreads = kThreads - 128;
+  static constexpr int kProducerRegs = 56;
+  static constexpr int kEpilogueRegs = k2Cta ? 200 : 224;
+  static constexpr int kLaunchRegs = k2Cta ? 128 : 168;
+  static constexpr int kMinBlocks = k2Cta ? 2 : 1;
+  static constexpr int kTmemCols = k2Cta ? 256 : 512;
+  // Dynamic shared memory the kernel may use: the block's share of the SM's 228 KB, less the
+  // per-block reserve and the static part.
+  static constexpr int kSmemLimit = k2Cta ? 233472 / 2 - 1024 - 4096 : 232448 - 4096;
+  static_assert(128 * kProducerRegs + kEpiThreads * kEpilogueRegs <= kThreads * kLaunchRegs,
+                "register split exceeds the launch allocation");
+  static_assert(kThreads * kLaunchRegs * kMinBlocks <= 65536, "registers of the SM");
+};
 constexpr uint64_t kF8DrainNs = 1000000000ull;
 
 struct F8Params {
@@ -130,8 +143,8 @@ __device__ __forceinline__ void f8_wait_drain(uint64_t* bar, uint32_t parity) {
     if (global_timer_ns() - t0 > kF8DrainNs) return;
 }
 
-template <int KPS>
-__global__ void __launch_bounds__(kF8Threads, 1)
+template <int KPS, bool k2Cta>
+__global__ void __launch_bounds__(F8Cfg<k2Cta>::kThreads, F8Cfg<k2Cta>::kMinBlocks)
     moe_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmB16,
                         const __grid_constant__ CUtensorMap tmB64,
@@ -157,7 +170,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     for (int s = 0; s < kF8MaxStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
-      mbar_init(&pempty_bar[s], 8);  // one arrival per epilogue warp
+      mbar_init(&pempty_bar[s], F8Cfg<k2Cta>::kEpiThreads / 32);  // one per epilogue warp
     }
     mbar_init(&drain_bar, 1);
     s_abort = 0;
@@ -170,7 +183,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     prefetch_tensormap(&tmB128);
   }
   if (warp == 1) {
-    tmem_alloc(&s_tmem_base, kF8TmemCols);
+    tmem_alloc(&s_tmem_base, F8Cfg<k2Cta>::kTmemCols);
     tmem_relinquish();
   }
   pdl_wait();
@@ -232,7 +245,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   const int tblk = p.tcap * kF8BlockK;  // bytes of one k block of token rows
 
   if (warp < 4) {  // warpgroup 0: producer and MMA issuer
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kF8ProducerRegs));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(F8Cfg<k2Cta>::kProducerRegs));
     if (warp == 0) {
       // ------------------------------------------------------------------ TMA producer
       if (lane == 0) {
@@ -335,12 +348,12 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       }
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kF8EpilogueRegs));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(F8Cfg<k2Cta>::kEpilogueRegs));
     // ------------------------------------------------- scale-and-accumulate epilogue (8 warps)
     const int q = warp & 3;          // TMEM lane quarter this warp may read
     const int g = (warp - 4) >> 2;   // token-column half: [64g, 64g + 64)
     const int row = q * 32 + lane;   // weight row within the slab
-    const int et = threadIdx.x - 128;  // 0..255
+    const int et = threadIdx.x - 128;  // 0 .. kEpiThreads - 1
     int stage = 0, pb = 0, sc = 0;
     uint32_t phase = 0, pphase = 0;
     bool ok = true;
@@ -382,7 +395,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
           }
         }
         const bool got = mbar_wait(&empty_bar[stage], phase, abort_flag, p.limit_ns, p.status);
-        if (!named_bar_and(1, 256, got)) {  // also publishes s_sa[buf]
+        if (!named_bar_and(1, F8Cfg<k2Cta>::kEpiThreads, got)) {  // also publishes s_sa[buf]
           ok = false;
           break;
         }
@@ -452,7 +465,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, kF8TmemCols);
+    tmem_dealloc(tmem_base, F8Cfg<k2Cta>::kTmemCols);
   }
 }
 
@@ -480,10 +493,15 @@ cudaError_t launch_gemm_fp8(int E, int N, int K, int64_t rows, int max_tile_rows
   tcap = (tcap + 15) & ~15;
   p.tcap = tcap;
   const int kps = tcap <= 64 ? 2 : 1;
+  // Two CTAs per SM (one epilogue warpgroup covers the tile) for short K: measured on the page's
+  // b64 shapes, the down projections (12-16 k blocks) gained 6-8 %, while the up projections
+  // (32-56 k blocks) lost up to 4 % to the halved pipeline depth of each CTA.
+  const bool two = tcap <= 64 && p.num_kb <= 16;
+  const int smem_limit = two ? F8Cfg<true>::kSmemLimit : F8Cfg<false>::kSmemLimit;
   p.stage_bytes = kps * (kF8WBytes + tcap * kF8BlockK);
-  p.stages = (kF8SmemLimit - 1024) / p.stage_bytes;
+  p.stages = (smem_limit - 1024) / p.stage_bytes;
   if (p.stages > kF8MaxStages) p.stages = kF8MaxStages;
-  p.nbuf = kF8TmemCols / (kps * tcap);
+  p.nbuf = (two ? F8Cfg<true>::kTmemCols : F8Cfg<false>::kTmemCols) / (kps * tcap);
   if (p.nbuf > p.stages) p.nbuf = p.stages;  // the epilogue never falls a full ring behind
   p.tiles = tiles;
   p.n_tiles = n_tiles;
@@ -498,20 +516,29 @@ cudaError_t launch_gemm_fp8(int E, int N, int K, int64_t rows, int max_tile_rows
   p.limit_ns = wait_limit_ns();
   static bool attr_set = false;
   if (!attr_set) {
-    for (auto k : {moe_gemm_fp8_kernel<1>, moe_gemm_fp8_kernel<2>}) {
-      cudaError_t e =
-          cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kF8SmemLimit);
+    for (auto k : {moe_gemm_fp8_kernel<1, false>, moe_gemm_fp8_kernel<2, false>}) {
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           F8Cfg<false>::kSmemLimit);
       if (e != cudaSuccess) return e;
     }
+    cudaError_t e = cudaFuncSetAttribute(moe_gemm_fp8_kernel<2, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         F8Cfg<true>::kSmemLimit);
+    if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const long long upper = (long long)max_tiles * p.n_slabs;
   const int sms = num_sms();
-  const int grid = (int)(upper < sms ? upper : sms);
+  const long long slots = two ? 2ll * sms : sms;
+  const int grid = (int)(upper < slots ? upper : slots);
   if (grid <= 0) return cudaSuccess;
   const size_t smem = (size_t)p.stages * p.stage_bytes + 1024;
-  return launch_k(kps == 2 ? moe_gemm_fp8_kernel<2> : moe_gemm_fp8_kernel<1>, dim3(grid),
-                  dim3(kF8Threads), smem, s, pdl, tmW, tmB16, tmB64, tmB128, p);
+  if (two)
+    return launch_k(moe_gemm_fp8_kernel<2, true>, dim3(grid), dim3(F8Cfg<true>::kThreads), smem,
+                    s, pdl, tmW, tmB16, tmB64, tmB128, p);
+  return launch_k(kps == 2 ? moe_gemm_fp8_kernel<2, false> : moe_gemm_fp8_kernel<1, false>,
+                  dim3(grid), dim3(F8Cfg<false>::kThreads), smem, s, pdl, tmW, tmB16, tmB64,
+                  tmB128, p);
 }
 
 }  // namespace gb300moe
