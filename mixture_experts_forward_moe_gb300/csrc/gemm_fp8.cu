@@ -75,6 +75,7 @@ constexpr uint64_t kF8DrainNs = 1000000000ull;
 struct F8Params {
   int N, num_kb, n_slabs;
   int tcap;          // token rows a stage holds per k block (16..128, a multiple of 16)
+  int tile_h;        // rows per tile of a group (128, or 64 at two CTAs per SM)
   int stage_bytes;   // KPS * (16 KB + tcap * 128), KPS = k blocks per stage
   int stages;        // pipeline stages (<= kF8MaxStages)
   int nbuf;          // TMEM buffers (KPS * tcap columns each), <= stages
@@ -123,8 +124,8 @@ __device__ __forceinline__ void f8_unit(const F8Params& p, const F8Groups& gr, i
     const int j = local % count;
     U.slab = local / count;
     U.e = lo;
-    U.row0 = gr.row0[lo] + j * kTileRows;
-    U.nrows = min(kTileRows, gr.cnt[lo] - j * kTileRows);
+    U.row0 = gr.row0[lo] + j * p.tile_h;
+    U.nrows = min(p.tile_h, gr.cnt[lo] - j * p.tile_h);
   } else {
     const Tile owner = p.tiles[u / p.n_slabs];
     const int local = u - p.n_slabs * owner.first;
@@ -215,7 +216,7 @@ __global__ void __launch_bounds__(F8Cfg<k2Cta>::kThreads, F8Cfg<k2Cta>::kMinBloc
         s_row0[e] = r0;
         s_cnt[e] = c;
       }
-      nt[i] = (c + kTileRows - 1) / kTileRows;
+      nt[i] = (c + p.tile_h - 1) / p.tile_h;
       tot += nt[i];
     }
     int incl = tot;
@@ -491,12 +492,16 @@ cudaError_t launch_gemm_fp8(int E, int N, int K, int64_t rows, int max_tile_rows
   // Token rows per stage and k block: the tallest tile this layout can produce.
   int tcap = max_tile_rows < 1 ? 1 : (max_tile_rows > kTileRows ? kTileRows : max_tile_rows);
   tcap = (tcap + 15) & ~15;
+  // Two CTAs per SM (one epilogue warpgroup covers a 64-row tile) for short K: measured on the
+  // page's b64 shapes, the down projections (12-16 k blocks) gained 6-8 %, while the up
+  // projections (32-56 k blocks) lost up to 4 % to the halved pipeline depth of each CTA.
+  // Layouts taller than 64 rows then run 64-row tiles (a group's slab of weights is read once
+  // from HBM by its adjacent units, the rest from L2), when the kernel makes its own tile list.
+  const bool two = p.num_kb <= 16 && (tcap <= 64 || meta != nullptr);
+  if (two && tcap > 64) tcap = 64;
   p.tcap = tcap;
+  p.tile_h = two ? 64 : kTileRows;
   const int kps = tcap <= 64 ? 2 : 1;
-  // Two CTAs per SM (one epilogue warpgroup covers the tile) for short K: measured on the page's
-  // b64 shapes, the down projections (12-16 k blocks) gained 6-8 %, while the up projections
-  // (32-56 k blocks) lost up to 4 % to the halved pipeline depth of each CTA.
-  const bool two = tcap <= 64 && p.num_kb <= 16;
   const int smem_limit = two ? F8Cfg<true>::kSmemLimit : F8Cfg<false>::kSmemLimit;
   p.stage_bytes = kps * (kF8WBytes + tcap * kF8BlockK);
   p.stages = (smem_limit - 1024) / p.stage_bytes;

@@ -14,9 +14,10 @@ pytestmark = pytest.mark.gpu
 
 
 # Pipeline stages carry two k blocks for token tiles of up to 64 rows and one for taller tiles:
-# (3, 144, ...) and (1, 128, 5120, ...) take one-block stages (the latter one 128-row unit of 40
-# k blocks); (5, 16, 128, ...) a single one-block stage; (2, 64, 1024, ...) two-block stages
-# throughout; (8, 48, 384, ...) 48-row stages and an odd k-block count (a one-block last stage).
+# (1, 128, 5120, ...) takes one-block stages (one 128-row unit of 40 k blocks, one CTA per SM);
+# the short-K cases run two CTAs per SM: (3, 144, ...) in 64-row tiles (a group of three
+# tiles), (5, 16, 128, ...) a single two-block stage, (2, 64, 1024, ...) two-block stages
+# throughout, (8, 48, 384, ...) 48-row stages and an odd k-block count (a one-block last stage).
 @pytest.mark.parametrize("E,max_m,K,N,total", [(3, 144, 384, 256, 200),  # a 2-tile group
                                                (5, 16, 128, 128, 9),       # 1-row groups
                                                (2, 64, 1024, 384, 128),
