@@ -492,15 +492,20 @@ cudaError_t launch_gemm_fp8(int E, int N, int K, int64_t rows, int max_tile_rows
   // Token rows per stage and k block: the tallest tile this layout can produce.
   int tcap = max_tile_rows < 1 ? 1 : (max_tile_rows > kTileRows ? kTileRows : max_tile_rows);
   tcap = (tcap + 15) & ~15;
-  // Two CTAs per SM (one epilogue warpgroup covers a 64-row tile) for short K: measured on the
-  // page's b64 shapes, the down projections (12-16 k blocks) gained 6-8 %, while the up
-  // projections (32-56 k blocks) lost up to 4 % to the halved pipeline depth of each CTA.
-  // Layouts taller than 64 rows then run 64-row tiles (a group's slab of weights is read once
-  // from HBM by its adjacent units, the rest from L2), when the kernel makes its own tile list.
-  const bool two = p.num_kb <= 16 && (tcap <= 64 || meta != nullptr);
-  if (two && tcap > 64) tcap = 64;
+  // 64-row tiles with two k blocks per stage ("narrow"): always when no group can exceed 64
+  // rows; for a masked layout of at least 256 rows per group too.  The layout's capacity does
+  // not say how many rows its groups hold (the counts live on the device), so this is a rule:
+  // the page's 256-row layouts hold 5-16 rows a group and gained 8-21 % with narrow tiles
+  // (a group's weight slab is read from HBM once by adjacent units, the rest from L2), while
+  // its 128-row layout holds about 96 a group, and its up projection lost 33 % to twice the
+  // units.  Narrow tiles of at most 16 k blocks run two CTAs per SM (one epilogue warpgroup
+  // covers a 64-row tile): the b64 down projections gained 6-8 %, the up projections (32-56 k
+  // blocks) lost up to 4 % to the halved pipeline depth of each CTA.
+  const bool narrow = tcap <= 64 || (meta != nullptr && max_m >= 256);
+  const bool two = narrow && p.num_kb <= 16;
+  if (narrow && tcap > 64) tcap = 64;
   p.tcap = tcap;
-  p.tile_h = two ? 64 : kTileRows;
+  p.tile_h = narrow ? 64 : kTileRows;
   const int kps = tcap <= 64 ? 2 : 1;
   const int smem_limit = two ? F8Cfg<true>::kSmemLimit : F8Cfg<false>::kSmemLimit;
   p.stage_bytes = kps * (kF8WBytes + tcap * kF8BlockK);

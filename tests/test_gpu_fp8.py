@@ -14,15 +14,17 @@ pytestmark = pytest.mark.gpu
 
 
 # Pipeline stages carry two k blocks for token tiles of up to 64 rows and one for taller tiles:
-# (1, 128, 5120, ...) takes one-block stages (one 128-row unit of 40 k blocks, one CTA per SM);
-# the short-K cases run two CTAs per SM: (3, 144, ...) in 64-row tiles (a group of three
-# tiles), (5, 16, 128, ...) a single two-block stage, (2, 64, 1024, ...) two-block stages
-# throughout, (8, 48, 384, ...) 48-row stages and an odd k-block count (a one-block last stage).
+# (3, 144, ...) and (1, 128, 5120, ...) take one-block stages of 128-row tiles at one CTA per
+# SM (the latter one unit of 40 k blocks); (4, 256, 512, ...) 64-row tiles of a 256-row layout
+# at two CTAs per SM, with a group of three tiles; (5, 16, 128, ...) a single two-block stage,
+# (2, 64, 1024, ...) two-block stages throughout, (8, 48, 384, ...) 48-row stages and an odd
+# k-block count (a one-block last stage), all at two CTAs per SM.
 @pytest.mark.parametrize("E,max_m,K,N,total", [(3, 144, 384, 256, 200),  # a 2-tile group
                                                (5, 16, 128, 128, 9),       # 1-row groups
                                                (2, 64, 1024, 384, 128),
                                                (1, 128, 5120, 128, 128),
-                                               (8, 48, 384, 128, 60)])
+                                               (8, 48, 384, 128, 60),
+                                               (4, 256, 512, 256, 600)])
 def test_fp8_masked_grouped_gemm_matches_oracle(E, max_m, K, N, total, cuda_device):
     w = inputs.Fp8GemmWorkload("t", E=E, max_m=max_m, K=K, N=N, total=total)
     d = inputs.generate_fp8_gemm(w, seed=E + K, device=cuda_device)
