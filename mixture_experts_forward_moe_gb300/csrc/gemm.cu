@@ -123,7 +123,13 @@ struct Cfg {
   // doing both groups' rows, with two CTAs per SM), then the token producer.
   static constexpr int kDecWarps = k2Cta ? 4 : 8;
   static constexpr int kTokWarp = 6 + kDecWarps;
-  static constexpr int kThreads = kW4 ? 32 * (kTokWarp + 1) : 192;
+  // The NVFP4 gate/up GEMMs issue the up projection's MMAs from a second thread, in a warp of
+  // its own after the others (on another SMSP than warp 1): the barriers the MMAs free then
+  // count two commits.  (The 16-bit GEMMs, paced by HBM, measured slower with two issuers.)
+  static constexpr bool kDual = kW4 && kGemm1;
+  static constexpr int kIssuers = kDual ? 2 : 1;
+  static constexpr int kMma2Warp = kTokWarp + 1;
+  static constexpr int kThreads = kW4 ? 32 * (kTokWarp + 1 + (kDual ? 1 : 0)) : 192;
   static constexpr int kMinBlocks = k2Cta ? 2 : 1;
   // Warps that write each decoded-weight slot: gemm1 slots hold both slabs (two groups).
   static constexpr int kSlotWriters = (kGemm1 && !k2Cta) ? 8 : 4;
@@ -335,7 +341,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4, k2Cta>::kThreads,
   __shared__ __align__(8) uint64_t empty_bar[C::kFullBars];
   __shared__ __align__(8) uint64_t tfull_bar[C::kAccBufs];
   __shared__ __align__(8) uint64_t tempty_bar[C::kAccBufs];
-  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t drain_bar[2];  // one per MMA issuer
   __shared__ __align__(8) uint64_t afull_bar[C::kAStages];   // NVFP4: decoded slot ready
   __shared__ __align__(8) uint64_t aempty_bar[C::kAStages];  // NVFP4: slot consumed by the MMA
   __shared__ __align__(8) uint64_t wfull_bar[kW4 ? C::kNW : 1];   // NVFP4: weights landed
@@ -363,7 +369,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4, k2Cta>::kThreads,
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kFullBars; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&empty_bar[s], C::kIssuers);  // freed by every MMA issuer's commit
     }
     if (kW4) {
       for (int s = 0; s < C::kNW; ++s) {
@@ -372,14 +378,15 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4, k2Cta>::kThreads,
       }
       for (int a = 0; a < C::kAStages; ++a) {
         mbar_init(&afull_bar[a], C::kSlotWriters);  // the warps that write the slot
-        mbar_init(&aempty_bar[a], 1);
+        mbar_init(&aempty_bar[a], C::kIssuers);
       }
     }
     for (int a = 0; a < C::kAccBufs; ++a) {
-      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tfull_bar[a], C::kIssuers);
       mbar_init(&tempty_bar[a], 128);
     }
-    mbar_init(&drain_bar, 1);
+    mbar_init(&drain_bar[0], 1);
+    mbar_init(&drain_bar[1], 1);
     s_abort = 0;
     fence_mbar_init();
   }
@@ -719,8 +726,11 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4, k2Cta>::kThreads,
           mbar_wait_drain(&full_bar[i % C::kStages], (uint32_t)((i / C::kStages) & 1));
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || (C::kDual && warp == C::kMma2Warp)) {
+    // ------------------------------------------------------------------ MMA issuer(s)
+    // kDual: warp 1 issues the gate (first slab) MMAs and warp kMma2Warp the up (second slab)
+    // ones; both wait for the same stages and commit to every barrier the MMAs free.
+    const bool upper = C::kDual && warp != 1;
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -766,12 +776,20 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4, k2Cta>::kThreads,
               const uint32_t a = tmem_base + (uint32_t)(C::kABase + slot * C::kASlotCols);
               const uint64_t bdesc = tdesc + (uint64_t)(hh * (kN * kBlockK * 2 / 16));
               const uint32_t accum = (kb != U.kb0 || hh != 0) ? 1u : 0u;
-              if (two)
-                umma_tmem_a_kblock2(d, a, d + kN, a + 32, bdesc, idesc, accum);
-              else
+              if (!C::kDual) {
+                if (two)
+                  umma_tmem_a_kblock2(d, a, d + kN, a + 32, bdesc, idesc, accum);
+                else
+                  umma_tmem_a_kblock(d, a, bdesc, idesc, accum);
+                issued_any = true;
+              } else if (!upper) {
                 umma_tmem_a_kblock(d, a, bdesc, idesc, accum);
+                issued_any = true;
+              } else if (two) {
+                umma_tmem_a_kblock(d + kN, a + 32, bdesc, idesc, accum);
+                issued_any = true;
+              }
               umma_commit(&aempty_bar[slot]);
-              issued_any = true;
             }
             if (!ok) break;
             a_cnt += 2;
@@ -791,14 +809,14 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4, k2Cta>::kThreads,
               for (int k = 0; k < kBlockK / 16; ++k) {
                 const uint64_t bdesc = sw128_kmajor_desc(bj + k * 32);
                 const uint32_t accum = (kb | j | k) != 0 ? 1u : 0u;
-                umma_f16(d, sw128_kmajor_desc(aj + k * 32), bdesc, idesc, accum);
-                if (kGemm1 && U.two)
+                if (!upper) umma_f16(d, sw128_kmajor_desc(aj + k * 32), bdesc, idesc, accum);
+                if (kGemm1 && U.two && (upper || !C::kDual))
                   umma_f16(d + kN, sw128_kmajor_desc(aj + kSlab * kBlockK * 2 + k * 32), bdesc,
                            idesc, accum);
               }
             }
             umma_commit(&empty_bar[stage]);
-            issued_any = true;
+            issued_any |= !upper || (kGemm1 && U.two);
             if (++stage == C::kStages) {
               stage = 0;
               phase ^= 1u;
@@ -812,10 +830,10 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4, k2Cta>::kThreads,
           acc_phase ^= 1u;
         }
       }
-      // Every MMA issued by this thread has completed once drain_bar flips.
+      // Every MMA issued by this thread has completed once its drain barrier flips.
       if (issued_any) {
-        umma_commit(&drain_bar);
-        mbar_wait_drain(&drain_bar, 0);
+        umma_commit(&drain_bar[upper ? 1 : 0]);
+        mbar_wait_drain(&drain_bar[upper ? 1 : 0], 0);
       }
     }
   } else {
