@@ -144,6 +144,13 @@ int w4_gate_up_tile_rows(const moe_problem_t& p) {
   return r <= 16 ? kTileRowsNvfp4Min : (r <= 64 ? kTileRowsNarrow : kTileRows);
 }
 
+// Token rows per tile of the NVFP4 down projection: 64 while the experts average at most 64
+// routed rows (the accumulators of a stage's two 64-k halves then fit TMEM, one per MMA issuer),
+// 128 above.
+int w4_down_tile_rows(const moe_problem_t& p) {
+  return rows_per_expert(p) <= 64 ? kTileRowsNarrow : kTileRows;
+}
+
 // The down projection of fused_moe_fwd runs on pairs of SMs (gemm_pair.cu) when its tiles have
 // 256 rows (experts average at least 96 routed rows) and H splits into whole 256-row pair units.
 bool use_pair_gemm2(const moe_problem_t& p) {
@@ -442,7 +449,7 @@ moe_status_t run_fused(const moe_problem_t* p, const Experts& X, const void* hid
     int32_t* inv_route = at<int32_t>(ws, L.inv);
     Tile* tiles = at<Tile>(ws, L.tiles);    // gemm1: tile_rows1-row tiles
     Tile* tiles2 = at<Tile>(ws, L.tiles2);  // gemm2: tile_rows2-row tiles
-    const int tile_rows2 = X.w4 ? kTileRows : sorted_tile_rows(*p);
+    const int tile_rows2 = X.w4 ? w4_down_tile_rows(*p) : sorted_tile_rows(*p);
     // With T <= 128 every expert's rows fit one tile of all T tokens: gemm1 reads hidden_states
     // directly and no gathered copy is made.
     const bool token_rows = P.T <= kTileRows;
@@ -739,7 +746,7 @@ moe_status_t gemm2_staged(const moe_problem_t* p, int32_t block_m, const void* a
   cudaStream_t s = (cudaStream_t)stream;
   void* ws = workspace;
   Tile* tiles = at<Tile>(ws, L.tiles);
-  const int tile_rows = X.w4 ? kTileRows : sorted_tile_rows(*p);
+  const int tile_rows = X.w4 ? w4_down_tile_rows(*p) : sorted_tile_rows(*p);
   MOE_TRY(launch_build_tiles(P.E, offsets, tiles, tile_counter(ws), tile_rows, s, false));
   GemmCall g2 = base_call(P, status_word(ws));
   g2.gemm1 = 0;

@@ -84,10 +84,11 @@ namespace {
 template <bool kGemm1, int kN, bool kW4 = false, bool k2Cta = false>
 struct Cfg {
   static_assert(kN == 32 || kN == 64 || kN == 128 || kN == 256, "tile rows");
-  static_assert(kN != 64 || kGemm1 == kW4, "64-row tiles: 16-bit down proj. or NVFP4 gate/up");
+  static_assert(kN != 64 || kW4 || !kGemm1, "64-row tiles: 16-bit down proj. or NVFP4");
   static_assert(kN != 32 || (kGemm1 && kW4 && k2Cta), "32-row tiles: NVFP4 gate/up, two CTAs");
-  static_assert(!kW4 || kN == 128 || (kN <= 64 && kGemm1), "NVFP4 tiles are 128 (64, 32) rows");
-  static_assert(!k2Cta || (kW4 && (kGemm1 ? kN <= 64 : kN == 128)),
+  static_assert(!kW4 || kN == 128 || kN == 64 || (kN == 32 && kGemm1),
+                "NVFP4 tiles are 128 or 64 rows (32 for gate/up)");
+  static_assert(!k2Cta || (kW4 && (kGemm1 ? kN <= 64 : kN >= 64)),
                 "two CTAs per SM: the NVFP4 down proj. and 32/64-row gate/up");
   static constexpr int kSlabs = kGemm1 ? 2 : 1;
   static constexpr int kKps = (kN == 64 && !kW4) ? 2 : 1;  // 64-k blocks per stage (16-bit)
@@ -104,14 +105,17 @@ struct Cfg {
   static constexpr int kTileBytes = kQBytes + kSfBytes;  // one tile of the packed layout
   static constexpr int kWBytes = kSlabs * kTileBytes;
   static constexpr int kNW = k2Cta ? (kGemm1 ? 3 : 4) : (kGemm1 ? 6 : 8);
-  static constexpr int kNT = k2Cta ? (kN == 32 ? 4 : 2) : (kGemm1 ? 3 : 4);
+  static constexpr int kNT = k2Cta ? ((kN == 32 || (!kGemm1 && kN == 64)) ? 4 : 2) : (kGemm1 ? 3 : 4);
   static constexpr int kRingBytes = kW4 ? kNW * kWBytes + kNT * kBBytes : kStages * kStageBytes;
   static constexpr int kFullBars = kW4 ? kNT : kStages;  // token (or combined) ring barriers
   // gemm1 transposes 64 token columns at a time through shared memory; gemm2 writes f32 rows
   // straight from registers.
   static constexpr int kPassCols = 64;
   static constexpr int kStagingBytes = kGemm1 ? kPassCols * kSlab * 2 : 0;
-  static constexpr int kAccCols = kGemm1 ? 2 * kN : kN;  // per accumulator buffer
+  // The NVFP4 down projection over 64-row tiles accumulates each stage's two 64-k halves in two
+  // accumulators (one per MMA issuer, below), which the epilogue adds.
+  static constexpr bool kKHalves = kW4 && !kGemm1 && kN == 64;
+  static constexpr int kAccCols = (kGemm1 || kKHalves) ? 2 * kN : kN;  // per accumulator buffer
   static constexpr int kAccBufs =
       kW4 ? ((k2Cta || (kGemm1 && kN == 128)) ? 1 : 2) : ((kGemm1 && kN == 256) ? 1 : 2);
   static constexpr int kABase = kAccBufs * kAccCols;  // first TMEM ring column
@@ -124,10 +128,13 @@ struct Cfg {
   static constexpr int kDecWarps = k2Cta ? 4 : 8;
   static constexpr int kTokWarp = 6 + kDecWarps;
   // The NVFP4 gate/up GEMMs issue the up projection's MMAs from a second thread, in a warp of
-  // its own after the others (on another SMSP than warp 1): the barriers the MMAs free then
-  // count two commits.  (The 16-bit GEMMs, paced by HBM, measured slower with two issuers.)
-  static constexpr bool kDual = kW4 && kGemm1;
+  // its own after the others (on another SMSP than warp 1), and the 64-row down projection the
+  // second 64-k half of every stage: the token stage and the accumulator then count two
+  // commits, and a decoded-weight slot the commits of the issuers that read it.  (The 16-bit
+  // GEMMs, paced by HBM, measured slower with two issuers.)
+  static constexpr bool kDual = kW4 && (kGemm1 || kKHalves);
   static constexpr int kIssuers = kDual ? 2 : 1;
+  static constexpr int kSlotReaders = kKHalves ? 1 : kIssuers;
   static constexpr int kMma2Warp = kTokWarp + 1;
   static constexpr int kThreads = kW4 ? 32 * (kTokWarp + 1 + (kDual ? 1 : 0)) : 192;
   static constexpr int kMinBlocks = k2Cta ? 2 : 1;
@@ -378,7 +385,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4, k2Cta>::kThreads,
       }
       for (int a = 0; a < C::kAStages; ++a) {
         mbar_init(&afull_bar[a], C::kSlotWriters);  // the warps that write the slot
-        mbar_init(&aempty_bar[a], C::kIssuers);
+        mbar_init(&aempty_bar[a], C::kSlotReaders);
       }
     }
     for (int a = 0; a < C::kAccBufs; ++a) {
@@ -729,7 +736,8 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4, k2Cta>::kThreads,
   } else if (warp == 1 || (C::kDual && warp == C::kMma2Warp)) {
     // ------------------------------------------------------------------ MMA issuer(s)
     // kDual: warp 1 issues the gate (first slab) MMAs and warp kMma2Warp the up (second slab)
-    // ones; both wait for the same stages and commit to every barrier the MMAs free.
+    // ones, or (kKHalves) the first and the second 64-k half of every stage, each into its own
+    // accumulator; both wait for the same token stages and commit to the barriers they free.
     const bool upper = C::kDual && warp != 1;
     if (lane == 0) {
       int stage = 0;
@@ -765,6 +773,7 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4, k2Cta>::kThreads,
             const bool two = kGemm1 && U.two;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
+              if (C::kKHalves && (hh != 0) != upper) continue;  // the other issuer's half
               const int idx = a_cnt + hh;
               const int slot = idx % C::kAStages;
               if (!mbar_wait(&afull_bar[slot], (uint32_t)((idx / C::kAStages) & 1), abort_flag,
@@ -775,8 +784,11 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4, k2Cta>::kThreads,
               tc_fence_after();
               const uint32_t a = tmem_base + (uint32_t)(C::kABase + slot * C::kASlotCols);
               const uint64_t bdesc = tdesc + (uint64_t)(hh * (kN * kBlockK * 2 / 16));
-              const uint32_t accum = (kb != U.kb0 || hh != 0) ? 1u : 0u;
-              if (!C::kDual) {
+              const uint32_t accum = (kb != U.kb0 || (hh != 0 && !C::kKHalves)) ? 1u : 0u;
+              if (C::kKHalves) {
+                umma_tmem_a_kblock(d + (uint32_t)(hh * kN), a, bdesc, idesc, accum);
+                issued_any = true;
+              } else if (!C::kDual) {
                 if (two)
                   umma_tmem_a_kblock2(d, a, d + kN, a + 32, bdesc, idesc, accum);
                 else
@@ -1038,7 +1050,14 @@ __global__ void __launch_bounds__(Cfg<kGemm1, kN, kW4, k2Cta>::kThreads,
         const bool in_range = h < p.n_out;
         for (int c0 = 0; c0 < U.n_mma; c0 += 16) {
           float g[16];
-          tmem_ld_x16(tb + c0, g);
+          if constexpr (C::kKHalves) {  // the two 64-k halves' accumulators
+            float v[16];
+            tmem_ld2_x16(tb + c0, tb + kN + c0, g, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) g[j] += v[j];
+          } else {
+            tmem_ld_x16(tb + c0, g);
+          }
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int dst = ent_dst[c0 + j];
@@ -1167,8 +1186,13 @@ cudaError_t launch_rows(const GemmCall& c, const KParams& kp, long long units, c
       return launch_typed<true, 128, __half, true>(c, kp, grid, s, pdl);
     } else {
       // Two CTAs per SM, each with its own MMA issuer: one issuing thread is latency bound
-      // and, next to the decoders, reaches well under half the tensor pipe's MMA rate.
+      // and, next to the decoders, reaches well under half the tensor pipe's MMA rate.  With
+      // 64-row tiles (and on the direct path with at most 64 routes) the two accumulators of
+      // the k halves fit TMEM, and each CTA has two issuers.
       const int grid2 = (int)(units < 2 * sms ? units : 2 * sms);
+      if ((c.mode == kSorted && c.tile_rows == kTileRowsNarrow) ||
+          (c.mode == kDirect && c.P <= 64))
+        return launch_typed<false, 64, __half, true, false, false, true>(c, kp, grid2, s, pdl);
       return launch_typed<false, 128, __half, true, false, false, true>(c, kp, grid2, s, pdl);
     }
   }
@@ -1203,10 +1227,12 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   kp.alpha = nullptr;
   if (c.w4) {
     // NVFP4 weights: a bf16 problem (its token rows and act reach the GEMMs as f16), 128-row
-    // token tiles (64 or 32 for the gate/up GEMM over gathered rows), K and the output width
-    // whole multiples of 128 (one stage is 128 k; a weight slab never crosses an expert).
+    // token tiles (64 for the down projection, 64 or 32 for the gate/up GEMM over gathered
+    // rows), K and the output width whole multiples of 128 (one stage is 128 k; a weight slab
+    // never crosses an expert).
     const bool tiles_ok =
         c.tile_rows == kTileRows ||
+        (c.tile_rows == kTileRowsNarrow && !c.gemm1 && c.mode == kSorted) ||
         ((c.tile_rows == kTileRowsNarrow || c.tile_rows == kTileRowsNvfp4Min) && c.gemm1 &&
          c.mode == kSorted && !c.token_rows);
     if (c.dtype != MOE_BF16 || !tiles_ok || c.K % 128 != 0 || c.n_out % 128 != 0 || !c.alpha ||
@@ -1252,7 +1278,7 @@ cudaError_t launch_gemm(const GemmCall& c, cudaStream_t s, bool pdl) {
   }
 
   if (c.tile_rows != 128 && c.tile_rows != 256 &&
-      !(c.tile_rows == 64 && c.mode == kSorted && (c.w4 ? c.gemm1 : !c.gemm1)) &&
+      !(c.tile_rows == 64 && c.mode == kSorted && (c.w4 || !c.gemm1)) &&
       !(c.tile_rows == 32 && c.mode == kSorted && c.w4 && c.gemm1))
     return cudaErrorInvalidValue;
   long long upper = 0;
