@@ -441,9 +441,10 @@ def moe_gemm2(act, sorted_ids, offsets, topk_weights, w_down, T, top_k, block_m=
 
 
 def moe_combine(y_route, inv_route, T, top_k, topk_ids=None, shared_out=None, out=None,
-                dtype=torch.bfloat16, stream=None):
+                dtype=torch.bfloat16, stream=None, E=None, ep_num_local=0, ep_local_offset=0):
     """Deterministic top-k combine (include/moe.h: moe_combine) of f32 rows; returns out
-    [T, H] in `dtype`."""
+    [T, H] in `dtype`.  E, ep_num_local and ep_local_offset describe an expert-parallel shard
+    (topk_ids then hold local ids, -1 for routes to other shards)."""
     _need(y_route, "y_route", torch.float32)
     H = y_route.shape[1]
     if inv_route is not None:
@@ -452,7 +453,8 @@ def moe_combine(y_route, inv_route, T, top_k, topk_ids=None, shared_out=None, ou
         _need(topk_ids, "topk_ids", torch.int32)
     if shared_out is not None:
         _need(shared_out, "shared_out", torch.float32, (T, H))
-    prob = make_problem(T, H, max(top_k, 1), 8, top_k, dtype)
+    prob = make_problem(T, H, E if E is not None else max(top_k, 1), 8, top_k, dtype,
+                        ep_num_local=ep_num_local, ep_local_offset=ep_local_offset)
     if out is None:
         out = torch.empty((T, H), dtype=dtype, device=y_route.device)
     _check(lib().moe_combine(ctypes.byref(prob), _p(y_route), _p(inv_route), _p(topk_ids),

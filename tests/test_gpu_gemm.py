@@ -124,6 +124,32 @@ def test_combine_matches_oracle(dtype, cuda_device):
     assert_rounded_close(out2, ref2, dtype, rel_rms=1e-6, what="combine identity")
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_combine_on_an_expert_parallel_shard(dtype, cuda_device):
+    """A shard holding 32 of 256 experts: a token averages one route with a row here, and at
+    2048 tokens of H = 7168 a CTA covers at least 8 column chunks, so the combine takes its
+    shard form (each token's local routes listed first).  Tokens 0-3 have all 8 routes local,
+    token 4 five, and about a third have none (their output is the shared row alone)."""
+    T, k, E, n_loc, H = 2048, 8, 256, 32, 7168
+    ids = inputs.random_ids(T, k, E, seed=21).numpy()
+    ids[0:4] = np.arange(8, dtype=np.int32)             # all eight routes local
+    ids[4] = np.array([0, 40, 1, 2, 90, 3, 4, 200], np.int32)  # five of eight
+    local = np.where(ids < n_loc, ids, -1).astype(np.int32)
+    is_local = local.reshape(-1) >= 0
+    n_rows = int(is_local.sum())
+    rng = np.random.default_rng(21)
+    inv = np.full(T * k, -1, np.int32)
+    inv[is_local] = rng.permutation(n_rows).astype(np.int32)  # rows in a shuffled order
+    y16 = inputs.random_rows(n_rows, H, seed=22, dtype=torch.bfloat16)
+    sh16 = inputs.random_rows(T, H, seed=23, dtype=torch.bfloat16)
+    out = B.moe_combine(y16.float().to(cuda_device), torch.from_numpy(inv).to(cuda_device), T, k,
+                        topk_ids=torch.from_numpy(local).to(cuda_device),
+                        shared_out=sh16.float().to(cuda_device), dtype=dtype, E=E,
+                        ep_num_local=n_loc, ep_local_offset=0)
+    ref = oracle.combine(y16, inv, k, oracle.BF16, shared=sh16)
+    assert_rounded_close(out, ref, dtype, rel_rms=1e-6, what="combine on a shard")
+
+
 @pytest.mark.parametrize("T,H,S", [(1, 256, 128), (37, 192, 320), (300, 128, 136)])
 def test_shared_expert_matches_oracle(T, H, S, cuda_device):
     w = inputs.Workload("s", T=T, H=H, E=2, F=16, top_k=1, S=S)
