@@ -31,6 +31,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -166,13 +167,22 @@ def measured_peaks():
 GEMM_SOURCES = ("gemm.cu", "gemm_pair.cu", "ptx.cuh", "common.cuh", "nvfp4.cuh")
 
 
+def _code_only(text: str) -> str:
+    """C++ source without its comments, trailing blanks and empty lines: edits to comments
+    leave a kernel as it was."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_hash() -> str:
-    """Hash of the sources that define the grouped GEMM kernel (the dominant kernel)."""
+    """Hash of the code (comments left out) of the sources that define the grouped GEMM kernel
+    (the dominant kernel)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mixture_experts_forward_moe_gb300", "csrc")
     for fn in GEMM_SOURCES:
-        with open(os.path.join(csrc, fn), "rb") as f:
-            h.update(fn.encode() + f.read())
+        with open(os.path.join(csrc, fn), encoding="utf-8") as f:
+            h.update(fn.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

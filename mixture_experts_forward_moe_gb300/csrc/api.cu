@@ -543,8 +543,8 @@ moe_status_t run_fused(const moe_problem_t* p, const Experts& X, const void* hid
   }
   {
     StageTimer t(kCombine, s);
-    MOE_TRY(launch_combine(P, y_rows, inv, ids, sh_out, out, s, true,
-                           combine_shard_is_sparse(*p)));
+    // the whole problem: its expert-parallel fields choose the combine kernel
+    MOE_TRY(launch_combine(*p, y_rows, inv, ids, sh_out, out, s, true));
     t.done(1);
   }
   return MOE_OK;
@@ -811,7 +811,7 @@ moe_status_t moe_combine(const moe_problem_t* p, const void* y_route, const int3
   if (st != MOE_OK) return st;
   if (p->T > 0 && (!y_route || !out)) return MOE_ERR_INVALID_ARG;
   return from_cuda(launch_combine(*p, y_route, inv_route, topk_ids, shared_out, out,
-                                  (cudaStream_t)stream, false, combine_shard_is_sparse(*p)));
+                                  (cudaStream_t)stream, false));
 }
 
 moe_status_t moe_shared_expert_fwd(const moe_problem_t* p, const void* hidden_states,

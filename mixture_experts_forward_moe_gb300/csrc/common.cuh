@@ -185,15 +185,11 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 v, bool& over) {
 cudaError_t launch_nvfp4_pack(int64_t n_mats, int rows, int K, const uint8_t* codes,
                               const uint8_t* scales, uint8_t* tiles, cudaStream_t s);
 
-// sparse: an expert-parallel shard whose tokens average at most two routes to its experts
-// (combine_shard_is_sparse); the kernel then lists each token's routes with a row first.
+// p is the caller's whole problem (its expert-parallel fields decide the kernel: a shard whose
+// tokens average at most two routes to its experts lists each token's routes first).
 cudaError_t launch_combine(const moe_problem_t& p, const void* y_route,
                            const int32_t* inv_route, const int32_t* ids, const void* shared_out,
-                           void* out, cudaStream_t s, bool pdl, bool sparse = false);
-
-inline bool combine_shard_is_sparse(const moe_problem_t& p) {
-  return p.ep_num_local > 0 && (int64_t)p.top_k * p.ep_num_local <= 2ll * p.E;
-}
+                           void* out, cudaStream_t s, bool pdl);
 
 // Grouped GEMM on tcgen05.  mode: 0 = sorted segments (tile list), 1 = direct from topk_ids
 // (T <= 8), 2 = dense rows (one expert, all rows: the shared expert).

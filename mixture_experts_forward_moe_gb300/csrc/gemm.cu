@@ -60,21 +60,26 @@ namespace {
 //    (moe_nvfp4_pack: the 128 rows' E2M1 codes for 128 k, then their E4M3 block scales), one
 //    contiguous bulk copy; freed by the decoders;
 //  * token ring (kNT slots): two 128-byte-swizzled 64-k boxes of token rows; freed by the MMA;
-//  * TMEM ring (kAStages slots of 64 k): eight decoder warps turn the codes into bf16 and store
-//    them there (one column holds two consecutive k of one weight row); the MMA reads its A
-//    operand from it.  The accumulators take the first 256 columns and the ring the rest.
+//  * TMEM ring (kAStages slots of 64 k): the decoder warps (eight, or four per CTA with two
+//    CTAs per SM) turn the codes into exact f16 values and store them there (one column holds
+//    two consecutive k of one weight row); the MMA reads its A operand from it.  The
+//    accumulators take the first columns and the ring the rest.
+//  * MMA issue: one thread per chain.  The gate/up GEMMs issue the gate and the up chain from
+//    two warps, and the 64-row down projection the first and the second 64-k half of every
+//    stage into two accumulators that the epilogue adds.
 // Every tcgen05.mma of M = 128 and k = 16 takes about the same time whatever N and wherever A
 // comes from, so at decode sizes the MMA issue rate bounds these GEMMs; the rings are sized so
 // that the decoders and the loads keep it fed.
 //
-// 64-row token tiles (the down projection at decode sizes): a stage carries two 64-k blocks
-// (kKps = 2), so the MMA issuer pays one barrier wait and one commit per 32 KB of weights
-// instead of per 16 KB; at a few tokens per expert those per-stage costs, not HBM, would
-// otherwise set the pace.
+// 64-row token tiles of the 16-bit GEMMs (the down projection at decode sizes): a stage carries
+// two 64-k blocks (kKps = 2), so the MMA issuer pays one barrier wait and one commit per 32 KB of
+// weights instead of per 16 KB; at a few tokens per expert those per-stage costs, not HBM,
+// would otherwise set the pace.
 //
-// Two CTAs per SM (k2Cta): the NVFP4 down projection and the NVFP4 gate/up GEMM with 64- or
-// 32-row tiles (at most 64 tokens, or gathered rows at decode sizes) run two CTAs on each SM,
-// each with half the TMEM (256 columns: one accumulator buffer and the decoded-weight ring),
+// Two CTAs per SM (k2Cta): the NVFP4 down projection (128- or 64-row tiles) and the NVFP4
+// gate/up GEMM with 64- or 32-row tiles (at most 64 tokens, or gathered rows at decode sizes)
+// run two CTAs on each SM, each with half the TMEM (256 columns: one accumulator buffer and the
+// decoded-weight ring),
 // about half the shared memory and four decoder warps.  One MMA-issuing thread is latency
 // bound (about 44 cycles per tcgen05.mma at these N when nothing else runs on its SMSP, and
 // twice that next to busy decoder warps), so a second issuer per SM measured 19-21 % faster on

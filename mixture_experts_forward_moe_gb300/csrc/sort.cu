@@ -728,7 +728,9 @@ cudaError_t launch_permute(int dtype, int top_k, int H, const void* hidden,
 
 cudaError_t launch_combine(const moe_problem_t& p, const void* y_route,
                            const int32_t* inv_route, const int32_t* ids, const void* shared_out,
-                           void* out, cudaStream_t s, bool pdl, bool sparse) {
+                           void* out, cudaStream_t s, bool pdl) {
+  // An expert-parallel shard whose tokens average at most two routes to its experts.
+  const bool sparse = p.ep_num_local > 0 && (int64_t)p.top_k * p.ep_num_local <= 2ll * p.E;
   if (p.T == 0) return cudaSuccess;
   // Chunks of 512 columns per CTA: as many as keep about 16 CTAs of 128 threads per SM busy in
   // one round (a whole row per CTA at prefill sizes, one chunk per CTA at decode sizes).
