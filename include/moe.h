@@ -337,7 +337,10 @@ moe_status_t moe_gemm2_w4a16(const moe_problem_t* p, int32_t block_m, const void
  *   out[t,:] = round( sum_{j=0..k-1} y_route[inv_route[t*k+j], :] (+ shared_out[t,:]) )
  * summed in f32 in fixed j order, shared term last (deterministic: no atomics), rounded once
  * to dtype.  Routes with inv_route -1, or with topk_ids -1 when topk_ids is given, are
- * skipped.  inv_route NULL means the identity (route r at row r).
+ * skipped.  inv_route NULL means the identity (route r at row r).  On an expert-parallel shard
+ * (p->ep_num_local > 0; topk_ids are then the shard's local ids, -1 for a route to another
+ * shard) the result is the same; when its tokens average at most two local routes, large calls
+ * use a kernel that lists each token's local routes before it loads their rows.
  *   y_route [rows,H] f32; inv_route [T*k] or NULL; topk_ids [T*k] or NULL;
  *   shared_out [T,H] f32 or NULL; out [T,H] dtype
  */
