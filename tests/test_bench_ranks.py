@@ -57,3 +57,22 @@ def test_single_process_helpers():
     w = inputs.WORKLOADS["qwen3-30b-a3b-decode-t32"]
     ab = bench.algorithmic_bytes(w, 112)
     assert ab["total"] == 112 * 3 * 768 * 2048 * 2 + 32 * 2048 * 2 * 2 + 32 * 128 * 4
+
+
+def test_kernel_hash_ignores_comments_but_not_code():
+    src = "int a = 1;  // one\n/* a block\n   comment */\n\nint b = 2;\n"
+    assert bench._code_only(src) == "int a = 1;\nint b = 2;"
+    assert bench._code_only(src.replace("// one", "// uno")) == bench._code_only(src)
+    assert bench._code_only(src.replace("b = 2", "b = 3")) != bench._code_only(src)
+
+
+def test_recorded_traffic_only_for_the_captured_kernels(monkeypatch):
+    import json
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)
+    wl, per = next(iter(rec["per_launch_bytes"].items()))
+    stage, nbytes = next(iter(per.items()))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: rec["kernel_source_hash"])
+    assert bench.recorded_traffic(wl, stage) == nbytes
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
+    assert bench.recorded_traffic(wl, stage) is None
