@@ -166,3 +166,16 @@ def test_host_entry_staging_and_argument_checks():
                                       None) == B.MOE_ERR_INVALID_ARG  # no alpha
     bad = _prob(T=32, H=256, E=16, F=128, top_k=0)
     assert L.moe_host_staging_bytes(ctypes.byref(bad)) == 0
+
+
+@pytest.mark.parametrize("n_loc,off,code", [
+    (32, 240, B.MOE_ERR_INVALID_ARG),   # the shard runs past the last expert
+    (-1, 0, B.MOE_ERR_INVALID_ARG),
+    (0, 8, B.MOE_ERR_INVALID_ARG),      # an offset without a shard
+])
+def test_combine_rejects_a_bad_shard_before_launch(n_loc, off, code):
+    """moe_combine checks the problem (its expert-parallel fields choose the kernel) before it
+    touches a pointer or the device."""
+    p = B.make_problem(64, 256, 256, 8, 8, ep_num_local=n_loc, ep_local_offset=off)
+    d = ctypes.c_void_p(16)
+    assert B.lib().moe_combine(ctypes.byref(p), d, d, d, None, d, None) == code
